@@ -1,0 +1,532 @@
+#!/usr/bin/env python3
+"""Benchmark of the TT-linear forward + backward on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+tt_forward then tt_backward of the 768x768 TT layer (modes (12,8,8)x(8,8,12),
+ranks 30, 16384 tokens, bf16 activations) by default.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the host cores
+
+Under torchrun every rank runs its own replica (tokens are independent rows;
+no data-path collective); the timing is the max over ranks and the value is
+the tokens of all ranks over that time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TT-linear fwd+bwd tokens/s on 1 GB300 and % of roofline; CPU-oracle speedup"
+DEFAULT_WORKLOAD = "tt768_bf16"
+ELEM = {"bf16": 2, "f32": 4}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--tokens", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--target-seconds", type=float, default=3.0,
+                   help="timed-region length used when --steps is not given")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# shared helpers
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic(w, T):
+    """FLOP and bytes of one fwd+bwd step, and bytes per token pass of each kernel.
+
+    FLOP = 6 T r' (N + M) per layer (the merged contraction order: x A, z' B,
+    dy B^T, z'^T dy, dz A^T, x^T dz); bytes = e T (3N + 2M) per layer (x read
+    by both passes, y written, dy read, dx written).
+    """
+    import numpy as np
+    e = ELEM[w.act]
+    flop = 0
+    byt = 0
+    fwd_b = 0
+    bwd_b = 0
+    for L in w.layers:
+        r = L.ranks[L.d]
+        if w.diag == "pruned_half":
+            r = r - r // 2
+        flop += 6 * T * r * (L.N + L.M)
+    if w.ffn:
+        up, dn = w.layers
+        byt = e * T * (3 * up.N + 2 * dn.M)
+        fwd_b = e * T * (up.N + dn.M)
+        bwd_b = e * T * (2 * up.N + dn.M)
+    else:
+        L = w.layers[0]
+        byt = e * T * (3 * L.N + 2 * L.M)
+        fwd_b = e * T * (L.N + L.M)
+        bwd_b = e * T * (2 * L.N + L.M)
+    return {"flop": int(flop), "bytes": int(byt), "fwd_bytes": int(fwd_b),
+            "bwd_bytes": int(bwd_b)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_step(w, inp):
+    """One fwd+bwd of the oracle over the given inputs."""
+    from oracle import tt_oracle as O
+    import numpy as np
+    if w.ffn:
+        up = ([c.astype(np.float64) for c in inp.layers[0].cores],
+              [e.astype(np.float64) for e in inp.layers[0].diags])
+        dn = ([c.astype(np.float64) for c in inp.layers[1].cores],
+              [e.astype(np.float64) for e in inp.layers[1].diags])
+        O.ffn_forward(up, dn, w.layers[0].d, w.layers[1].d, inp.x)
+        O.ffn_backward(up, dn, w.layers[0].d, w.layers[1].d, inp.x, inp.dy)
+    else:
+        L = w.layers[0]
+        cores = [c.astype(np.float64) for c in inp.layers[0].cores]
+        diags = [e.astype(np.float64) for e in inp.layers[0].diags]
+        O.chained_forward(cores, diags, L.d, inp.x)
+        O.chained_backward(cores, diags, L.d, inp.x, inp.dy)
+
+
+def time_oracle(w, sample_tokens, budget_s):
+    """Run the oracle on samples of sample_tokens until budget_s has passed."""
+    from tensor_train_compressed_tt_gb300 import synth
+    inp = synth.draw(w, seed=0, tokens=sample_tokens)
+    oracle_step(w, inp)  # warm (BLAS thread pool, page-in)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_step(w, inp)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return n * sample_tokens / el, n, el
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm_sorted = sorted(sm)
+        return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    T_full = args.tokens or w.tokens
+    K = args.steps if args.steps is not None else 20
+    W = args.warmup
+    # calibrate: tokens/s of the oracle on a small sample
+    rate, _, _ = time_oracle(w, min(T_full, 256), 1.0)
+    budget = 120.0
+    per_step = budget / max(1, K + W)
+    sample = int(max(16, min(T_full, rate * per_step)))
+    from tensor_train_compressed_tt_gb300 import synth
+    inp = synth.draw(w, seed=0, tokens=sample)
+    for _ in range(W):
+        oracle_step(w, inp)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_step(w, inp)
+    el = time.perf_counter() - t0
+    value = K * sample / el
+    cores = oracle_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": 1e3 * el / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "tokens": T_full,
+                   "sample_tokens_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} of {T_full} tokens per step, fp64 numpy oracle "
+                                   f"(merged contraction order), {K} steps"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def traffic_for(phase_name, workload):
+    """DRAM bytes per launch from the committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            entries = json.load(f)
+    except Exception:
+        return None
+    for e in entries:
+        if e.get("phase") != phase_name or e.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, e["source"])
+        if not os.path.exists(src):
+            return None
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != e.get("source_sha"):
+            return None
+        return e.get("dram_bytes_per_launch")
+    return None
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    from tensor_train_compressed_tt_gb300 import _build, synth, ttc
+    from tensor_train_compressed_tt_gb300.layer import TTFFN, TTLinear
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(ttc.LIB_PATH):
+        _build.build()
+    T = args.tokens or w.tokens
+    dt = torch.bfloat16 if w.act == "bf16" else torch.float32
+    e = ELEM[w.act]
+
+    # ---- setup: parameters and rotating activation sets larger than 2x L2
+    inp0 = synth.draw(w, seed=rank, tokens=T)
+    if w.ffn:
+        up, dn = w.layers
+        mod = TTFFN((up.in_modes, up.out_modes, up.ranks), (dn.in_modes, dn.out_modes, dn.ranks),
+                    dt)
+        params = [torch.from_numpy(synth.pack(l.cores, l.diags)).to(dev) for l in inp0.layers]
+        N, M = up.N, dn.M
+        n_par = [p.numel() for p in params]
+    else:
+        L = w.layers[0]
+        mod = TTLinear(L.in_modes, L.out_modes, L.ranks, dt)
+        params = [torch.from_numpy(synth.pack(inp0.layers[0].cores, inp0.layers[0].diags)).to(dev)]
+        N, M = L.N, L.M
+        n_par = [params[0].numel()]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    set_bytes = e * T * (2 * N + 2 * M)
+    nsets = max(2, -(-2 * l2 // set_bytes) + 1)
+    sets = []
+    for i in range(nsets):
+        g = torch.Generator(device=dev)
+        g.manual_seed(1000 * rank + i)
+        x = torch.randn((T, N), generator=g, device=dev, dtype=torch.float32).to(dt)
+        dy = torch.randn((T, M), generator=g, device=dev, dtype=torch.float32).to(dt)
+        y = torch.empty((T, M), device=dev, dtype=dt)
+        dx = torch.empty((T, N), device=dev, dtype=dt)
+        sets.append((x, dy, y, dx))
+    # the first set holds the seeded synthetic inputs of the workload
+    sets[0][0].copy_(torch.from_numpy(inp0.x).to(dev).to(dt))
+    sets[0][1].copy_(torch.from_numpy(inp0.dy).to(dev).to(dt))
+    dparams = [torch.empty(n, device=dev, dtype=torch.float32) for n in n_par]
+    ws = mod.workspace(T, dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    wsp, wsn = ws.data_ptr(), ws.numel()
+
+    def step(i):
+        x, dy, y, dx = sets[i % nsets]
+        if w.ffn:
+            ttc.check(ttc.tt_ffn_forward(mod.plan, T, x.data_ptr(), params[0].data_ptr(),
+                                         params[1].data_ptr(), y.data_ptr(), wsp, wsn, sh))
+            ttc.check(ttc.tt_ffn_backward(mod.plan, T, x.data_ptr(), dy.data_ptr(),
+                                          params[0].data_ptr(), params[1].data_ptr(),
+                                          dx.data_ptr(), dparams[0].data_ptr(),
+                                          dparams[1].data_ptr(), wsp, wsn, sh))
+        else:
+            ttc.check(ttc.tt_forward(mod.plan, T, x.data_ptr(), params[0].data_ptr(),
+                                     y.data_ptr(), wsp, wsn, sh))
+            ttc.check(ttc.tt_backward(mod.plan, T, x.data_ptr(), dy.data_ptr(),
+                                      params[0].data_ptr(), dx.data_ptr(),
+                                      dparams[0].data_ptr(), wsp, wsn, sh))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    W = max(3, args.warmup)
+    for i in range(W):
+        step(i)
+    ttc.check(ttc.tt_get_device_status(wsp, sh), "device status after warm-up")
+    barrier()
+    # choose K for a timed region of about target-seconds when not given
+    if args.steps is None:
+        t0 = time.perf_counter()
+        for i in range(5):
+            step(i)
+        torch.cuda.synchronize(dev)
+        per = (time.perf_counter() - t0) / 5
+        K = int(min(100000, max(20, args.target_seconds / max(per, 1e-6))))
+        if world > 1:
+            import torch.distributed as dist
+            kt = torch.tensor([K], device=dev)
+            dist.all_reduce(kt, op=dist.ReduceOp.MIN)
+            K = int(kt.item())
+    else:
+        K = args.steps
+    barrier()
+
+    # ---- timed region
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    l0 = ttc.lib().tt_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for i in range(K):
+        step(i)
+    ev1.record(stream)
+    barrier()
+    launches = int(ttc.lib().tt_launch_count() - l0)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / K
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ttc.check(ttc.tt_get_device_status(wsp, sh), "device status after timed region")
+
+    # ---- per-phase CUDA-event timing of the library's kernels (same steps)
+    ttc.lib().tt_profile_enable(1)
+    barrier()
+    for i in range(K):
+        step(i)
+    barrier()
+    phases = {}
+    import ctypes
+    for ph in range(5):
+        tot = ctypes.c_double()
+        n = ctypes.c_int64()
+        ttc.check(ttc.lib().tt_profile_phase(ph, ctypes.byref(tot), ctypes.byref(n)))
+        name = ttc.lib().tt_profile_phase_name(ph)
+        name = name.decode() if isinstance(name, bytes) else str(name)
+        if n.value:
+            phases[name] = {"ms_total": tot.value, "intervals": n.value,
+                            "us_per_interval": 1e3 * tot.value / n.value}
+    ttc.lib().tt_profile_enable(0)
+
+    alg = algorithmic(w, T)
+    peak, peak_kind = measured_peaks()
+    bytes_of = {"forward_tokens": alg["fwd_bytes"], "backward_tokens": alg["bwd_bytes"]}
+    dom = None
+    for nm in ("backward_tokens", "forward_tokens"):
+        if nm in phases and (dom is None or phases[nm]["ms_total"] > phases[dom]["ms_total"]):
+            dom = nm
+    roof = None
+    if dom is not None:
+        per_launch_s = phases[dom]["us_per_interval"] * 1e-6
+        if w.ffn:
+            per_launch_s *= 2  # two layers bracketed per pass; bytes cover the pair
+        ach = bytes_of[dom] / per_launch_s / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / peak,
+                "traffic": traffic_for(dom, w.name),
+                "algorithmic_bytes_per_launch": bytes_of[dom]}
+    t_roof = alg["bytes"] / (peak * 1e9)
+    value = world * T / (ms * 1e-3)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        x, dy, y, dx = sets[0]
+        hx = torch.empty(x.shape, dtype=dt, pin_memory=True)
+        hdy = torch.empty(dy.shape, dtype=dt, pin_memory=True)
+        hy = torch.empty(y.shape, dtype=dt, pin_memory=True)
+        hdx = torch.empty(dx.shape, dtype=dt, pin_memory=True)
+        hdp = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in n_par]
+        hx.copy_(x)
+        hdy.copy_(dy)
+        Ke = max(3, min(K, 200))
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            dy.copy_(hdy, non_blocking=True)
+            step(0)
+            hy.copy_(y, non_blocking=True)
+            hdx.copy_(dx, non_blocking=True)
+            for hp, dp in zip(hdp, dparams):
+                hp.copy_(dp, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        a1.record(stream)
+        barrier()
+        ems = a0.elapsed_time(a1) / Ke
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ems], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * T / (ems * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(hx.numel() * e + hdy.numel() * e),
+               "d2h_bytes_per_step": int(hy.numel() * e + hdx.numel() * e + 4 * sum(n_par)),
+               "ms_per_step": ems, "steps": Ke}
+
+    # ---- oracle on the host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = min(T, 2048)
+        rate, n, el = time_oracle(w, sample, 10.0)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{n} fwd+bwd passes of the fp64 numpy oracle on {sample} of the "
+                         f"{T} tokens ({el:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.act, "data": "synthetic",
+            "config": {"workload": w.name, "description": w.description, "tokens": T,
+                       "modes": [list(L.modes) for L in w.layers],
+                       "ranks": [list(L.ranks) for L in w.layers],
+                       "l2": f"{nsets} rotating input/output sets of {set_bytes / 1e6:.1f} MB "
+                             f"(> 2x L2 of {l2 / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "roofline_step": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3),
+                              "algorithmic_bytes": alg["bytes"], "algorithmic_flop": alg["flop"],
+                              "peak_gbs": peak, "peak_kind": peak_kind},
+            "phases_us": {k: round(v["us_per_interval"], 3) for k, v in phases.items()},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from tensor_train_compressed_tt_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

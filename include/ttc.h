@@ -1,0 +1,155 @@
+/*
+ * libttc: forward and backward of a rank-gated tensor-train (TT) linear layer
+ * on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The layer (CoMERA project page, "Learn the ranks while training", figure of
+ * a tensor-train layer with rank-control diagonals):
+ *   W (M x N), N = n_1*...*n_d, M = m_1*...*m_d, is a chain of 2d cores
+ *   G_k of shape (r_{k-1}, s_k, r_k), r_0 = r_2d = 1, input modes first:
+ *   s = (n_1..n_d, m_1..m_d).  A diagonal D_k sits on every internal link
+ *   k = 1..2d-1; the rank of a link is the number of nonzeros of D_k, and a
+ *   zero entry drops the matching slice of both neighbouring cores.
+ *   With j = (j_1..j_d), i = (i_1..i_d) row-major (first mode most
+ *   significant):
+ *     W[i,j] = G_1[0,j_1,:] D_1 G_2[:,j_2,:] ... D_d ... G_2d[:,i_d,0]
+ *   forward   y[t,i] = sum_j W[i,j] x[t,j]                (no bias)
+ *   backward  for L = sum dy[t,i] y[t,i]:  dx = dy W,  dG_k = dL/dG_k,
+ *             dD_k = dL/dD_k, except that dD_k[a] is returned as 0 where
+ *             D_k[a] == 0 (the rank-truncated layer has no such parameter).
+ * The contraction order is the one of the project page, "Making small tensor
+ * operations fast on GPUs", bullet "One contraction order for both passes":
+ * the input-side cores are merged into A (N x r_d), the output-side cores
+ * into B (r_d x M), and x is contracted through them
+ * (y = ((x A) diag(D_d)) B).
+ *
+ * Conventions for every call:
+ *  - All device pointers are plain CUDA device addresses owned by the caller.
+ *    The library allocates no device memory; it uses the caller's workspace.
+ *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls only enqueue work; none synchronises, except
+ *    tt_get_device_status.
+ *  - Argument errors are reported before anything is enqueued.  A failed
+ *    launch returns TT_ERR_CUDA.  Errors found on the device (a bounded wait
+ *    that ran out, a failed consistency check) are recorded in a status word
+ *    inside the workspace and read back by tt_get_device_status.
+ *  - Activations: x is (T, N), y is (T, M), dy is (T, M), dx is (T, N), all
+ *    row-major, dense, in the plan's activation type (f32 or bf16), 16-byte
+ *    aligned.  Cores, diagonals and their gradients are f32.
+ *  - Packed parameters: one f32 buffer holding G_1..G_2d, each
+ *    (r_{k-1}, s_k, r_k) row-major, followed by D_1..D_{2d-1}
+ *    (tt_param_layout gives the offsets).  dparams has the same layout.
+ */
+#ifndef TTC_H
+#define TTC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TT_MAX_D 4 /* order 2d <= 8 */
+
+typedef enum tt_status {
+  TT_OK = 0,
+  TT_ERR_INVALID_ARG = 1, /* bad descriptor, NULL or misaligned pointer, T < 0 */
+  TT_ERR_UNSUPPORTED = 2, /* valid layer this build has no kernel for */
+  TT_ERR_WORKSPACE = 3,   /* workspace missing or smaller than tt_workspace_size */
+  TT_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  TT_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (device status) */
+  TT_ERR_DEVICE = 6       /* a device-side consistency check failed (device status) */
+} tt_status;
+
+typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1 } tt_dtype;
+
+/* flags of tt_desc */
+#define TT_ACCUMULATE 1u /* backward adds into dparams instead of overwriting */
+
+typedef struct tt_desc {
+  int d;                        /* 1..TT_MAX_D: number of input (= output) modes */
+  int in_modes[TT_MAX_D];       /* n_1..n_d, each >= 1 */
+  int out_modes[TT_MAX_D];      /* m_1..m_d, each >= 1 */
+  int ranks[2 * TT_MAX_D + 1];  /* r_0..r_2d; r_0 = r_2d = 1, others >= 1 */
+  int act;                      /* tt_dtype of x, y, dx, dy */
+  unsigned flags;               /* TT_ACCUMULATE */
+} tt_desc;
+
+typedef struct tt_plan_s tt_plan_t; /* opaque, immutable host object */
+
+/* Rank caps read off the printed rank table (project page, "Results",
+ * "Internal tensor-train ranks of each layer in one encoder block"):
+ * r_k = min(R, prod s_<=k, prod s_>k), r_0 = r_2d = 1.  ranks receives 2d+1
+ * values.  Host only. */
+tt_status tt_default_ranks(int d, const int* in_modes, const int* out_modes, int R,
+                           int* ranks);
+
+/* Validate desc and build a plan (host only; no device work, no allocation on
+ * the device).  *out is owned by the caller and freed with tt_destroy. */
+tt_status tt_plan(const tt_desc* desc, tt_plan_t** out);
+
+/* FFN pair y = TT_down(GELU(TT_up(x))) with the exact erf GELU; up's output
+ * width must equal down's input width and both must use the same act type. */
+tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out);
+
+void tt_destroy(tt_plan_t* plan);
+
+/* Offsets (in floats) of every core and diagonal inside the packed parameter
+ * buffer: core_off receives 2d values, diag_off 2d-1, *n_floats the total.
+ * For an FFN plan these describe the up layer; use tt_ffn_param_layout. */
+tt_status tt_param_layout(const tt_plan_t* plan, size_t* core_off, size_t* diag_off,
+                          size_t* n_floats);
+tt_status tt_ffn_param_layout(const tt_plan_t* plan, int layer /*0 up, 1 down*/,
+                              size_t* core_off, size_t* diag_off, size_t* n_floats);
+
+/* Bytes of device workspace a forward or backward call with T tokens needs
+ * (the same value serves both).  The workspace must be 256-byte aligned. */
+tt_status tt_workspace_size(const tt_plan_t* plan, int64_t T, size_t* bytes);
+
+/* y = x W^T for T tokens.  T == 0 is a no-op. */
+tt_status tt_forward(const tt_plan_t* plan, int64_t T, const void* x, const float* params,
+                     void* y, void* ws, size_t ws_bytes, void* stream);
+
+/* dx = dy W and dparams = dL/dparams (overwritten, or added to under
+ * TT_ACCUMULATE).  Recomputes what the forward computed; needs no state from
+ * a forward call.  T == 0 writes zero gradients (or leaves them under
+ * TT_ACCUMULATE). */
+tt_status tt_backward(const tt_plan_t* plan, int64_t T, const void* x, const void* dy,
+                      const float* params, void* dx, float* dparams, void* ws,
+                      size_t ws_bytes, void* stream);
+
+/* FFN pair: params_up / params_down are the two packed buffers. */
+tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,
+                         const float* params_up, const float* params_down, void* y, void* ws,
+                         size_t ws_bytes, void* stream);
+tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const void* dy,
+                          const float* params_up, const float* params_down, void* dx,
+                          float* dparams_up, float* dparams_down, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Synchronise stream, read and clear the device status word in ws.
+ * Returns TT_OK, TT_ERR_TIMEOUT or TT_ERR_DEVICE (or TT_ERR_CUDA). */
+tt_status tt_get_device_status(const void* ws, void* stream);
+
+const char* tt_status_string(tt_status s);
+
+/* ---- measurement hooks (host side, not thread-safe) ------------------------
+ * When enabled, every kernel phase the library enqueues is bracketed by CUDA
+ * events on the caller's stream, and every kernel launch is counted.  Phases:
+ * 0 merge (chain merges, forward), 1 forward token pass, 2 backward token pass,
+ * 3 merge backward, 4 elementwise (GELU).  Not part of the CoMERA method:
+ * it lets a benchmark time the library's own kernels with CUDA events. */
+#define TT_NUM_PHASES 5
+void tt_profile_enable(int on); /* on != 0: clear records and start; 0: stop */
+/* Synchronise on the recorded events and return the summed milliseconds and
+ * the number of bracketed intervals of one phase since the last enable. */
+tt_status tt_profile_phase(int phase, double* total_ms, int64_t* intervals);
+const char* tt_profile_phase_name(int phase);
+/* Total kernels this library has launched in this process (monotonic). */
+uint64_t tt_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTC_H */

@@ -1,0 +1,253 @@
+// Plain SIMT (CUDA-core, fp32 FMA) kernels of libttc.
+//
+// These carry the f32-activation path (exact fp32 arithmetic, no tensor
+// cores, so results stay within 1e-4 of the fp64 definition), the merges of
+// the core chain and their backward (all T-independent and tiny), and the
+// elementwise GELU of the FFN pair.
+#include <cuda_bf16.h>
+
+#include "ttc_internal.h"
+
+namespace ttc {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float ld_as_f32(const T* p, int64_t i);
+template <>
+__device__ __forceinline__ float ld_as_f32<float>(const float* p, int64_t i) {
+  return p[i];
+}
+template <>
+__device__ __forceinline__ float ld_as_f32<__nv_bfloat16>(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void st_from_f32(T* p, int64_t i, float v);
+template <>
+__device__ __forceinline__ void st_from_f32<float>(float* p, int64_t i, float v) {
+  p[i] = v;
+}
+template <>
+__device__ __forceinline__ void st_from_f32<__nv_bfloat16>(__nv_bfloat16* p, int64_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_c(const T* p, int64_t i) {
+  return ld_as_f32<T>(p, i);
+}
+
+constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
+
+// 64x64 output tile per block, 4x4 per thread, K staged through shared
+// memory 16 at a time.  gridDim.z splits K (only with kAtomic).
+template <typename TA, typename TB, typename TC>
+__global__ void __launch_bounds__(NT) gemm_kernel(GemmArgs g) {
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Bs[BK][BN + 4];
+  const TA* A = static_cast<const TA*>(g.A);
+  const TB* B = static_cast<const TB*>(g.B);
+  TC* C = static_cast<TC*>(g.C);
+  const int tid = threadIdx.x;
+  const int tx = tid % 16, ty = tid / 16;
+  const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+  int64_t kbeg = 0, kend = g.k;
+  if (gridDim.z > 1) {
+    int64_t chunk = (g.k + gridDim.z - 1) / gridDim.z;
+    chunk = (chunk + BK - 1) / BK * BK;
+    kbeg = (int64_t)blockIdx.z * chunk;
+    kend = kbeg + chunk < g.k ? kbeg + chunk : g.k;
+  }
+  float acc[4][4] = {};
+  for (int64_t k0 = kbeg; k0 < kend; k0 += BK) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int idx = tid + e * NT;  // 0..1023
+      int mm = idx % BM, kk = idx / BM;
+      int64_t gm = m0 + mm, gk = k0 + kk;
+      float v = 0.f;
+      if (gm < g.m && gk < kend) {
+        v = ld_as_f32<TA>(A, gm * g.sam + gk * g.sak);
+        if (g.kscale) v *= g.kscale[gk % g.klen];
+      }
+      As[kk][mm] = v;
+      int nn = idx % BN;
+      int64_t gn = n0 + nn;
+      float w = 0.f;
+      if (gn < g.n && gk < kend) w = ld_as_f32<TB>(B, gk * g.sbk + gn * g.sbn);
+      Bs[kk][nn] = w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int64_t gm = m0 + ty * 4 + i;
+    if (gm >= g.m) continue;
+    float rs = g.rscale ? g.rscale[gm] : 1.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int64_t gn = n0 + tx * 4 + j;
+      if (gn >= g.n) continue;
+      float v = acc[i][j] * rs;
+      if (g.cscale) v *= g.cscale[gn % g.clen];
+      int64_t ci = gm * g.scm + gn * g.scn;
+      if (g.mode == kAtomic) {
+        atomicAdd(reinterpret_cast<float*>(C) + ci, v);
+      } else if (g.mode == kAccumulate) {
+        st_from_f32<TC>(C, ci, ld_c<TC>(C, ci) + v);
+      } else {
+        st_from_f32<TC>(C, ci, v);
+      }
+    }
+  }
+}
+
+template <typename TA, typename TB, typename TC>
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
+  dim3 grid((unsigned)((g.n + BN - 1) / BN), (unsigned)((g.m + BM - 1) / BM), 1);
+  if (g.mode == kAtomic) {
+    // split K so that the grid covers the GPU a few times over
+    int64_t tiles = (int64_t)grid.x * grid.y;
+    int64_t want = (600 + tiles - 1) / tiles;
+    int64_t maxs = (g.k + 4 * BK - 1) / (4 * BK);
+    int64_t z = want < maxs ? want : maxs;
+    if (z < 1) z = 1;
+    if (z > 65535) z = 65535;
+    grid.z = (unsigned)z;
+  }
+  gemm_kernel<TA, TB, TC><<<grid, NT, 0, st>>>(g);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+__global__ void coldot_kernel(int64_t nrows, int ncols, const float* X, int64_t sx,
+                              const float* Y, int64_t sy, const float* mask, float* out,
+                              int accumulate) {
+  const int c = blockIdx.x;
+  float s = 0.f;
+  for (int64_t u = threadIdx.x; u < nrows; u += blockDim.x) s += X[u * sx + c] * Y[u * sy + c];
+  __shared__ float red[32];
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    s = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (threadIdx.x == 0) {
+      bool keep = !mask || mask[c] != 0.f;
+      if (accumulate) {
+        if (keep) out[c] += s;
+      } else {
+        out[c] = keep ? s : 0.f;
+      }
+    }
+  }
+}
+
+__global__ void scale_periodic_kernel(int64_t n, const float* in, const float* scale, int len,
+                                      float* out, int accumulate) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v = in[i];
+    if (scale) v *= scale[i % len];
+    out[i] = accumulate ? out[i] + v : v;
+  }
+}
+
+__device__ __forceinline__ float gelu_f(float h) {
+  return 0.5f * h * (1.f + erff(h * 0.70710678118654752f));
+}
+__device__ __forceinline__ float gelu_grad_f(float h) {
+  float Phi = 0.5f * (1.f + erff(h * 0.70710678118654752f));
+  float phi = 0.39894228040143268f * expf(-0.5f * h * h);
+  return fmaf(h, phi, Phi);
+}
+
+template <typename TO>
+__global__ void gelu_fwd_kernel(int64_t n, const float* h, TO* a) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    st_from_f32<TO>(a, i, gelu_f(h[i]));
+}
+
+__global__ void gelu_bwd_kernel(int64_t n, const float* h, float* da) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    da[i] *= gelu_grad_f(h[i]);
+}
+
+unsigned grid_for(int64_t n, int threads) {
+  int64_t b = (n + threads - 1) / threads;
+  if (b > 65535LL * 8) b = 65535LL * 8;
+  if (b < 1) b = 1;
+  return (unsigned)b;
+}
+
+}  // namespace
+
+cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st) {
+  if (g.m <= 0 || g.n <= 0) return cudaSuccess;
+  using bf = __nv_bfloat16;
+  const int key = g.ta * 4 + g.tb * 2 + g.tc;
+  switch (key) {
+    case 0: return launch_gemm<float, float, float>(g, st);
+    case 1: return launch_gemm<float, float, bf>(g, st);
+    case 2: return launch_gemm<float, bf, float>(g, st);
+    case 3: return launch_gemm<float, bf, bf>(g, st);
+    case 4: return launch_gemm<bf, float, float>(g, st);
+    case 5: return launch_gemm<bf, float, bf>(g, st);
+    case 6: return launch_gemm<bf, bf, float>(g, st);
+    default: return launch_gemm<bf, bf, bf>(g, st);
+  }
+}
+
+cudaError_t coldot(int64_t nrows, int ncols, const float* X, int64_t sx, const float* Y,
+                   int64_t sy, const float* mask, float* out, bool accumulate,
+                   cudaStream_t st) {
+  if (ncols <= 0) return cudaSuccess;
+  coldot_kernel<<<ncols, 256, 0, st>>>(nrows, ncols, X, sx, Y, sy, mask, out, accumulate);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t scale_periodic(int64_t n, const float* in, const float* scale, int len, float* out,
+                           bool accumulate, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  scale_periodic_kernel<<<grid_for(n, 256), 256, 0, st>>>(n, in, scale, len, out, accumulate);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t gelu_fwd(int64_t n, const float* h, void* a, int ta, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (ta == TT_DT_BF16)
+    gelu_fwd_kernel<__nv_bfloat16>
+        <<<grid_for(n, 256), 256, 0, st>>>(n, h, static_cast<__nv_bfloat16*>(a));
+  else
+    gelu_fwd_kernel<float><<<grid_for(n, 256), 256, 0, st>>>(n, h, static_cast<float*>(a));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t gelu_bwd(int64_t n, const float* h, float* da, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  gelu_bwd_kernel<<<grid_for(n, 256), 256, 0, st>>>(n, h, da);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace ttc

@@ -1,0 +1,569 @@
+// libttc C ABI: plans, parameter/workspace layout, argument checks and the
+// orchestration of the kernels for one TT layer and for the GELU FFN pair.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "tc_fused.h"
+#include "ttc_internal.h"
+
+namespace ttc {
+namespace {
+
+constexpr int64_t kMaxDim = 1 << 20;   // N, M
+constexpr int kMaxRank = 4096;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
+  if (!desc || !L) return TT_ERR_INVALID_ARG;
+  const int d = desc->d;
+  if (d < 1 || d > TT_MAX_D) return TT_ERR_INVALID_ARG;
+  if (desc->act != TT_DT_F32 && desc->act != TT_DT_BF16) return TT_ERR_INVALID_ARG;
+  if (desc->flags & ~TT_ACCUMULATE) return TT_ERR_INVALID_ARG;
+  LayerPlan p;
+  p.d = d;
+  p.K = 2 * d;
+  p.act = desc->act;
+  p.flags = desc->flags;
+  p.N = 1;
+  p.M = 1;
+  for (int k = 0; k < d; ++k) {
+    if (desc->in_modes[k] < 1 || desc->out_modes[k] < 1) return TT_ERR_INVALID_ARG;
+    p.s[k] = desc->in_modes[k];
+    p.s[d + k] = desc->out_modes[k];
+    p.N *= desc->in_modes[k];
+    p.M *= desc->out_modes[k];
+    if (p.N > kMaxDim || p.M > kMaxDim) return TT_ERR_UNSUPPORTED;
+  }
+  for (int k = 0; k <= p.K; ++k) {
+    p.r[k] = desc->ranks[k];
+    if (p.r[k] < 1 || p.r[k] > kMaxRank) return TT_ERR_INVALID_ARG;
+  }
+  if (p.r[0] != 1 || p.r[p.K] != 1) return TT_ERR_INVALID_ARG;
+  p.rd = p.r[d];
+  size_t off = 0;
+  for (int k = 0; k < p.K; ++k) {
+    p.core_off[k] = off;
+    off += (size_t)p.r[k] * p.s[k] * p.r[k + 1];
+  }
+  for (int e = 0; e < p.K - 1; ++e) {
+    p.diag_off[e] = off;
+    off += (size_t)p.r[e + 1];
+  }
+  p.n_floats = off;
+  // rows of the merged prefix ending at core k
+  int64_t u = 1;
+  for (int k = 0; k < d; ++k) {
+    u *= p.s[k];
+    p.U[k] = u;
+  }
+  u = p.rd;
+  for (int k = d; k < p.K; ++k) {
+    u *= p.s[k];
+    p.U[k] = u;
+  }
+  *L = p;
+  return TT_OK;
+}
+
+// ---- workspace ------------------------------------------------------------
+struct WsLayout {
+  size_t P[kMaxK] = {};  // merged chain prefixes (floats), 0 where aliased to params
+  size_t dA = 0, dB = 0, q0 = 0, q1 = 0, z = 0, dzp = 0;
+  size_t tc = 0;         // tensor-core path operands
+  size_t end = 0;        // end of this layer's scratch
+};
+
+size_t chain_len(const LayerPlan& L, int k) { return (size_t)L.U[k] * L.r[k + 1]; }
+
+size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w) {
+  size_t off = align_up(base, 256);
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  size_t qmax = 0;
+  for (int k = 0; k < L.K; ++k) {
+    size_t n = chain_len(L, k);
+    if (n > qmax) qmax = n;
+    w->P[k] = (k == 0 || k == L.d) ? 0 : take(n * sizeof(float));
+  }
+  w->dA = take((size_t)L.N * L.rd * sizeof(float));
+  w->dB = take((size_t)L.rd * L.M * sizeof(float));
+  w->q0 = take(qmax * sizeof(float));
+  w->q1 = take(qmax * sizeof(float));
+  w->z = take((size_t)T * L.rd * sizeof(float));
+  w->dzp = take((size_t)T * L.rd * sizeof(float));
+  w->tc = take(tc_operand_bytes(L));
+  w->end = off;
+  return off;
+}
+
+struct FfnLayout {
+  WsLayout up, down;
+  size_t h = 0, a = 0, da = 0, end = 0;
+};
+
+size_t ffn_layout(const tt_plan_s* p, int64_t T, FfnLayout* f) {
+  size_t e0 = layer_layout(p->L[0], T, 256, &f->up);
+  size_t e1 = layer_layout(p->L[1], T, 256, &f->down);
+  size_t off = align_up(e0 > e1 ? e0 : e1, 256);
+  const size_t hb = (size_t)T * p->L[0].M * sizeof(float);
+  f->h = off;
+  off = align_up(off + hb, 256);
+  f->a = off;
+  off = align_up(off + hb, 256);
+  f->da = off;
+  off = align_up(off + hb, 256);
+  f->end = off;
+  return off;
+}
+
+#define TT_CUDA(call)                                      \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return TT_ERR_CUDA;             \
+  } while (0)
+
+float* fptr(void* ws, size_t off) { return reinterpret_cast<float*>(static_cast<char*>(ws) + off); }
+
+// ---- merges ---------------------------------------------------------------
+// P_k = reshape((P_{k-1} * D_{k-1}) . G_k) for k on one side of the chain.
+tt_status merge_chain(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
+                      const float** P, cudaStream_t st) {
+  for (int k = 0; k < L.K; ++k) {
+    if (k == 0 || k == L.d) {
+      P[k] = params + L.core_off[k];
+      continue;
+    }
+    GemmArgs g;
+    g.m = L.U[k - 1];
+    g.n = (int64_t)L.s[k] * L.r[k + 1];
+    g.k = L.r[k];
+    g.A = P[k - 1]; g.sam = L.r[k]; g.sak = 1;
+    g.kscale = params + L.diag_off[k - 1]; g.klen = L.r[k];
+    g.B = params + L.core_off[k]; g.sbk = g.n; g.sbn = 1;
+    float* out = fptr(ws, w.P[k]);
+    g.C = out; g.scm = g.n; g.scn = 1;
+    TT_CUDA(gemm_simt(g, st));
+    P[k] = out;
+  }
+  return TT_OK;
+}
+
+// Reverse of merge_chain on the cores [k_first, k_last]: dP_{k_last} is in
+// dlast (unscaled); writes dG_k for every core of the side and dD_e for the
+// links inside it.
+tt_status merge_chain_backward(const LayerPlan& L, const float* params, const float** P,
+                               int k_first, int k_last, const float* dlast, float* dparams,
+                               bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
+  const int mode = acc ? kAccumulate : kStore;
+  const float* Y = dlast;      // stored dP_k (unscaled by D_k)
+  const float* yscale = nullptr;  // D_k to apply to the last index of Y, if any
+  float* bufs[2] = {fptr(ws, w.q0), fptr(ws, w.q1)};
+  int flip = 0;
+  for (int k = k_last; k > k_first; --k) {
+    const int rk = L.r[k], rk1 = L.r[k + 1];
+    const int64_t U = L.U[k - 1];
+    const int64_t ncol = (int64_t)L.s[k] * rk1;
+    const float* Dprev = params + L.diag_off[k - 1];
+    // dG_k = diag(D_{k-1}) P_{k-1}^T Y
+    GemmArgs g;
+    g.m = rk; g.n = ncol; g.k = U;
+    g.A = P[k - 1]; g.sam = 1; g.sak = rk;
+    g.B = Y; g.sbk = ncol; g.sbn = 1;
+    g.rscale = Dprev;
+    g.cscale = yscale; g.clen = rk1;
+    g.C = dparams + L.core_off[k]; g.scm = ncol; g.scn = 1;
+    g.mode = mode;
+    TT_CUDA(gemm_simt(g, st));
+    // dQ = Y G_k^T   (U x r_k)
+    float* dQ = bufs[flip];
+    GemmArgs h;
+    h.m = U; h.n = rk; h.k = ncol;
+    h.A = Y; h.sam = ncol; h.sak = 1;
+    h.kscale = yscale; h.klen = rk1;
+    h.B = params + L.core_off[k]; h.sbk = 1; h.sbn = ncol;
+    h.C = dQ; h.scm = rk; h.scn = 1;
+    TT_CUDA(gemm_simt(h, st));
+    // dD_{k-1}[b] = sum_u P_{k-1}[u,b] dQ[u,b]  (0 where D_{k-1}[b] == 0)
+    TT_CUDA(coldot(U, rk, P[k - 1], rk, dQ, rk, Dprev, dparams + L.diag_off[k - 1], acc, st));
+    Y = dQ;
+    yscale = Dprev;
+    flip ^= 1;
+  }
+  // first core of the side: dG = Y * yscale
+  const size_t n = (size_t)L.r[k_first] * L.s[k_first] * L.r[k_first + 1];
+  TT_CUDA(scale_periodic((int64_t)n, Y, yscale, L.r[k_first + 1],
+                         dparams + L.core_off[k_first], acc, st));
+  return TT_OK;
+}
+
+// ---- one layer ---------------------------------------------------------------
+tt_status layer_forward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
+                               const float* params, const float** P, void* y, int ty, void* ws,
+                               const WsLayout& w, cudaStream_t st);
+tt_status layer_backward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
+                                const void* dy, int tdy, const float* params, const float** P,
+                                void* dx, int tdx, float* dparams, bool acc, void* ws,
+                                const WsLayout& w, cudaStream_t st);
+
+tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, const float* params,
+                        void* y, int ty, void* ws, const WsLayout& w, cudaStream_t st) {
+  const float* P[kMaxK];
+  prof_begin(kPhMerge, st);
+  tt_status s = merge_chain(L, params, ws, w, P, st);
+  prof_end(kPhMerge, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhFwd, st);
+  s = layer_forward_tokens(L, T, x, tx, params, P, y, ty, ws, w, st);
+  prof_end(kPhFwd, st);
+  return s;
+}
+
+tt_status layer_forward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
+                               const float* params, const float** P, void* y, int ty, void* ws,
+                               const WsLayout& w, cudaStream_t st) {
+  const float* A = P[L.d - 1];   // N x rd
+  const float* B = P[L.K - 1];   // rd x M
+  const float* Dm = params + L.diag_off[L.d - 1];
+  if (tx == TT_DT_BF16 && ty == TT_DT_BF16 && tc_supported(L)) {
+    return tc_forward(L, T, x, params, A, B, y, ws, w.tc, st);
+  }
+  float* z = fptr(ws, w.z);
+  GemmArgs g;
+  g.m = T; g.n = L.rd; g.k = L.N;
+  g.A = x; g.sam = L.N; g.sak = 1; g.ta = tx;
+  g.B = A; g.sbk = L.rd; g.sbn = 1;
+  g.C = z; g.scm = L.rd; g.scn = 1;
+  TT_CUDA(gemm_simt(g, st));
+  GemmArgs h;
+  h.m = T; h.n = L.M; h.k = L.rd;
+  h.A = z; h.sam = L.rd; h.sak = 1;
+  h.kscale = Dm; h.klen = L.rd;
+  h.B = B; h.sbk = L.M; h.sbn = 1;
+  h.C = y; h.scm = L.M; h.scn = 1; h.tc = ty;
+  TT_CUDA(gemm_simt(h, st));
+  return TT_OK;
+}
+
+tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, const void* dy,
+                         int tdy, const float* params, void* dx, int tdx, float* dparams,
+                         bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
+  const float* P[kMaxK];
+  prof_begin(kPhMerge, st);
+  tt_status s = merge_chain(L, params, ws, w, P, st);
+  prof_end(kPhMerge, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhBwd, st);
+  s = layer_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
+  prof_end(kPhBwd, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhMergeBwd, st);
+  s = merge_chain_backward(L, params, P, 0, L.d - 1, fptr(ws, w.dA), dparams, acc, ws, w, st);
+  if (s == TT_OK)
+    s = merge_chain_backward(L, params, P, L.d, L.K - 1, fptr(ws, w.dB), dparams, acc, ws, w,
+                             st);
+  prof_end(kPhMergeBwd, st);
+  return s;
+}
+
+tt_status layer_backward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
+                                const void* dy, int tdy, const float* params, const float** P,
+                                void* dx, int tdx, float* dparams, bool acc, void* ws,
+                                const WsLayout& w, cudaStream_t st) {
+  tt_status s = TT_OK;
+  const float* A = P[L.d - 1];
+  const float* B = P[L.K - 1];
+  const float* Dm = params + L.diag_off[L.d - 1];
+  float* dA = fptr(ws, w.dA);
+  float* dB = fptr(ws, w.dB);
+  TT_CUDA(cudaMemsetAsync(dA, 0, (size_t)L.N * L.rd * sizeof(float), st));
+  TT_CUDA(cudaMemsetAsync(dB, 0, (size_t)L.rd * L.M * sizeof(float), st));
+  if (tx == TT_DT_BF16 && tdy == TT_DT_BF16 && tdx == TT_DT_BF16 && tc_supported(L)) {
+    s = tc_backward(L, T, x, dy, params, A, B, dx, dparams + L.diag_off[L.d - 1], acc, dA, dB,
+                    ws, w.tc, st);
+    if (s != TT_OK) return s;
+  } else if (T > 0) {
+    float* z = fptr(ws, w.z);
+    float* dzp = fptr(ws, w.dzp);
+    GemmArgs g;  // z = x A
+    g.m = T; g.n = L.rd; g.k = L.N;
+    g.A = x; g.sam = L.N; g.sak = 1; g.ta = tx;
+    g.B = A; g.sbk = L.rd; g.sbn = 1;
+    g.C = z; g.scm = L.rd; g.scn = 1;
+    TT_CUDA(gemm_simt(g, st));
+    GemmArgs h;  // dz' = dy B^T
+    h.m = T; h.n = L.rd; h.k = L.M;
+    h.A = dy; h.sam = L.M; h.sak = 1; h.ta = tdy;
+    h.B = B; h.sbk = 1; h.sbn = L.M;
+    h.C = dzp; h.scm = L.rd; h.scn = 1;
+    TT_CUDA(gemm_simt(h, st));
+    // dD_d = sum_t z * dz'
+    TT_CUDA(coldot(T, L.rd, z, L.rd, dzp, L.rd, Dm, dparams + L.diag_off[L.d - 1], acc, st));
+    GemmArgs a;  // dx = (dz' D) A^T
+    a.m = T; a.n = L.N; a.k = L.rd;
+    a.A = dzp; a.sam = L.rd; a.sak = 1;
+    a.kscale = Dm; a.klen = L.rd;
+    a.B = A; a.sbk = 1; a.sbn = L.rd;
+    a.C = dx; a.scm = L.N; a.scn = 1; a.tc = tdx;
+    TT_CUDA(gemm_simt(a, st));
+    GemmArgs b;  // dA = x^T (dz' D)
+    b.m = L.N; b.n = L.rd; b.k = T;
+    b.A = x; b.sam = 1; b.sak = L.N; b.ta = tx;
+    b.B = dzp; b.sbk = L.rd; b.sbn = 1;
+    b.cscale = Dm; b.clen = L.rd;
+    b.C = dA; b.scm = L.rd; b.scn = 1; b.mode = kAtomic;
+    TT_CUDA(gemm_simt(b, st));
+    GemmArgs c;  // dB = diag(D) z^T dy
+    c.m = L.rd; c.n = L.M; c.k = T;
+    c.A = z; c.sam = 1; c.sak = L.rd;
+    c.rscale = Dm;
+    c.B = dy; c.sbk = L.M; c.sbn = 1; c.tb = tdy;
+    c.C = dB; c.scm = L.M; c.scn = 1; c.mode = kAtomic;
+    TT_CUDA(gemm_simt(c, st));
+  } else if (!acc) {
+    TT_CUDA(cudaMemsetAsync(dparams + L.diag_off[L.d - 1], 0, L.rd * sizeof(float), st));
+  }
+  return TT_OK;
+}
+
+tt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws || !aligned(ws, 256)) return TT_ERR_WORKSPACE;
+  if (ws_bytes < need) return TT_ERR_WORKSPACE;
+  return TT_OK;
+}
+
+bool act_aligned(const void* p) { return p && aligned(p, 16); }
+
+}  // namespace
+}  // namespace ttc
+
+using namespace ttc;
+
+extern "C" {
+
+tt_status tt_default_ranks(int d, const int* in_modes, const int* out_modes, int R, int* ranks) {
+  if (d < 1 || d > TT_MAX_D || !in_modes || !out_modes || !ranks || R < 1)
+    return TT_ERR_INVALID_ARG;
+  int s[kMaxK];
+  for (int k = 0; k < d; ++k) {
+    if (in_modes[k] < 1 || out_modes[k] < 1) return TT_ERR_INVALID_ARG;
+    s[k] = in_modes[k];
+    s[d + k] = out_modes[k];
+  }
+  const int K = 2 * d;
+  ranks[0] = 1;
+  ranks[K] = 1;
+  for (int k = 1; k < K; ++k) {
+    int64_t left = 1, right = 1;
+    for (int i = 0; i < k; ++i) left = left * s[i] > R ? (int64_t)R + 1 : left * s[i];
+    for (int i = k; i < K; ++i) right = right * s[i] > R ? (int64_t)R + 1 : right * s[i];
+    int64_t v = R;
+    if (left < v) v = left;
+    if (right < v) v = right;
+    ranks[k] = (int)v;
+  }
+  return TT_OK;
+}
+
+tt_status tt_plan(const tt_desc* desc, tt_plan_t** out) {
+  if (!out) return TT_ERR_INVALID_ARG;
+  *out = nullptr;
+  LayerPlan L;
+  tt_status s = build_layer(desc, &L);
+  if (s != TT_OK) return s;
+  tt_plan_s* p = new (std::nothrow) tt_plan_s();
+  if (!p) return TT_ERR_INVALID_ARG;
+  p->kind = 0;
+  p->L[0] = L;
+  *out = p;
+  return TT_OK;
+}
+
+tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out) {
+  if (!out) return TT_ERR_INVALID_ARG;
+  *out = nullptr;
+  LayerPlan a, b;
+  tt_status s = build_layer(up, &a);
+  if (s != TT_OK) return s;
+  s = build_layer(down, &b);
+  if (s != TT_OK) return s;
+  if (a.M != b.N || a.act != b.act || a.flags != b.flags) return TT_ERR_INVALID_ARG;
+  tt_plan_s* p = new (std::nothrow) tt_plan_s();
+  if (!p) return TT_ERR_INVALID_ARG;
+  p->kind = 1;
+  p->L[0] = a;
+  p->L[1] = b;
+  *out = p;
+  return TT_OK;
+}
+
+void tt_destroy(tt_plan_t* plan) { delete plan; }
+
+static tt_status layout_out(const LayerPlan& L, size_t* core_off, size_t* diag_off,
+                            size_t* n_floats) {
+  if (!core_off || !diag_off || !n_floats) return TT_ERR_INVALID_ARG;
+  for (int k = 0; k < L.K; ++k) core_off[k] = L.core_off[k];
+  for (int e = 0; e < L.K - 1; ++e) diag_off[e] = L.diag_off[e];
+  *n_floats = L.n_floats;
+  return TT_OK;
+}
+
+tt_status tt_param_layout(const tt_plan_t* plan, size_t* core_off, size_t* diag_off,
+                          size_t* n_floats) {
+  if (!plan) return TT_ERR_INVALID_ARG;
+  return layout_out(plan->L[0], core_off, diag_off, n_floats);
+}
+
+tt_status tt_ffn_param_layout(const tt_plan_t* plan, int layer, size_t* core_off,
+                              size_t* diag_off, size_t* n_floats) {
+  if (!plan || plan->kind != 1 || layer < 0 || layer > 1) return TT_ERR_INVALID_ARG;
+  return layout_out(plan->L[layer], core_off, diag_off, n_floats);
+}
+
+tt_status tt_workspace_size(const tt_plan_t* plan, int64_t T, size_t* bytes) {
+  if (!plan || !bytes || T < 0) return TT_ERR_INVALID_ARG;
+  if (plan->kind == 0) {
+    WsLayout w;
+    *bytes = layer_layout(plan->L[0], T, 256, &w);
+  } else {
+    FfnLayout f;
+    *bytes = ffn_layout(plan, T, &f);
+  }
+  return TT_OK;
+}
+
+tt_status tt_forward(const tt_plan_t* plan, int64_t T, const void* x, const float* params,
+                     void* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!plan || plan->kind != 0 || T < 0) return TT_ERR_INVALID_ARG;
+  const LayerPlan& L = plan->L[0];
+  if (T == 0) return TT_OK;
+  if (!act_aligned(x) || !act_aligned(y) || !params || !aligned(params, 4))
+    return TT_ERR_INVALID_ARG;
+  WsLayout w;
+  size_t need = layer_layout(L, T, 256, &w);
+  tt_status s = check_ws(ws, ws_bytes, need);
+  if (s != TT_OK) return s;
+  return layer_forward(L, T, x, L.act, params, y, L.act, ws, w, static_cast<cudaStream_t>(stream));
+}
+
+tt_status tt_backward(const tt_plan_t* plan, int64_t T, const void* x, const void* dy,
+                      const float* params, void* dx, float* dparams, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (!plan || plan->kind != 0 || T < 0) return TT_ERR_INVALID_ARG;
+  const LayerPlan& L = plan->L[0];
+  if (!params || !dparams || !aligned(params, 4) || !aligned(dparams, 4))
+    return TT_ERR_INVALID_ARG;
+  if (T > 0 && (!act_aligned(x) || !act_aligned(dy) || !act_aligned(dx)))
+    return TT_ERR_INVALID_ARG;
+  WsLayout w;
+  size_t need = layer_layout(L, T, 256, &w);
+  tt_status s = check_ws(ws, ws_bytes, need);
+  if (s != TT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool acc = (L.flags & TT_ACCUMULATE) != 0;
+  return layer_backward(L, T, x, L.act, dy, L.act, params, dx, L.act, dparams, acc, ws, w, st);
+}
+
+tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,
+                         const float* params_up, const float* params_down, void* y, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (!plan || plan->kind != 1 || T < 0) return TT_ERR_INVALID_ARG;
+  if (T == 0) return TT_OK;
+  if (!act_aligned(x) || !act_aligned(y) || !params_up || !params_down ||
+      !aligned(params_up, 4) || !aligned(params_down, 4))
+    return TT_ERR_INVALID_ARG;
+  FfnLayout f;
+  size_t need = ffn_layout(plan, T, &f);
+  tt_status s = check_ws(ws, ws_bytes, need);
+  if (s != TT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const LayerPlan& U = plan->L[0];
+  const LayerPlan& D = plan->L[1];
+  float* h = fptr(ws, f.h);
+  float* a = fptr(ws, f.a);
+  s = layer_forward(U, T, x, U.act, params_up, h, TT_DT_F32, ws, f.up, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhElem, st);
+  TT_CUDA(gelu_fwd(T * U.M, h, a, TT_DT_F32, st));
+  prof_end(kPhElem, st);
+  return layer_forward(D, T, a, TT_DT_F32, params_down, y, D.act, ws, f.down, st);
+}
+
+tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const void* dy,
+                          const float* params_up, const float* params_down, void* dx,
+                          float* dparams_up, float* dparams_down, void* ws, size_t ws_bytes,
+                          void* stream) {
+  if (!plan || plan->kind != 1 || T < 0) return TT_ERR_INVALID_ARG;
+  if (!params_up || !params_down || !dparams_up || !dparams_down || !aligned(params_up, 4) ||
+      !aligned(params_down, 4) || !aligned(dparams_up, 4) || !aligned(dparams_down, 4))
+    return TT_ERR_INVALID_ARG;
+  if (T > 0 && (!act_aligned(x) || !act_aligned(dy) || !act_aligned(dx)))
+    return TT_ERR_INVALID_ARG;
+  FfnLayout f;
+  size_t need = ffn_layout(plan, T, &f);
+  tt_status s = check_ws(ws, ws_bytes, need);
+  if (s != TT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const LayerPlan& U = plan->L[0];
+  const LayerPlan& D = plan->L[1];
+  const bool acc = (U.flags & TT_ACCUMULATE) != 0;
+  float* h = fptr(ws, f.h);
+  float* a = fptr(ws, f.a);
+  float* da = fptr(ws, f.da);
+  if (T > 0) {
+    s = layer_forward(U, T, x, U.act, params_up, h, TT_DT_F32, ws, f.up, st);
+    if (s != TT_OK) return s;
+    prof_begin(kPhElem, st);
+    TT_CUDA(gelu_fwd(T * U.M, h, a, TT_DT_F32, st));
+    prof_end(kPhElem, st);
+  }
+  s = layer_backward(D, T, a, TT_DT_F32, dy, D.act, params_down, da, TT_DT_F32, dparams_down,
+                     acc, ws, f.down, st);
+  if (s != TT_OK) return s;
+  if (T > 0) {
+    prof_begin(kPhElem, st);
+    TT_CUDA(gelu_bwd(T * U.M, h, da, st));
+    prof_end(kPhElem, st);
+  }
+  return layer_backward(U, T, x, U.act, da, TT_DT_F32, params_up, dx, U.act, dparams_up, acc,
+                        ws, f.up, st);
+}
+
+tt_status tt_get_device_status(const void* ws, void* stream) {
+  if (!ws) return TT_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceStatus h{0, 0};
+  if (cudaStreamSynchronize(st) != cudaSuccess) return TT_ERR_CUDA;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return TT_ERR_CUDA;
+  if (h.code != 0) {
+    DeviceStatus z{0, 0};
+    if (cudaMemcpy(const_cast<void*>(ws), &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess)
+      return TT_ERR_CUDA;
+  }
+  if (h.code == TT_ERR_TIMEOUT) return TT_ERR_TIMEOUT;
+  if (h.code != 0) return TT_ERR_DEVICE;
+  return TT_OK;
+}
+
+const char* tt_status_string(tt_status s) {
+  switch (s) {
+    case TT_OK: return "TT_OK";
+    case TT_ERR_INVALID_ARG: return "TT_ERR_INVALID_ARG: invalid argument";
+    case TT_ERR_UNSUPPORTED: return "TT_ERR_UNSUPPORTED: no kernel for this layer";
+    case TT_ERR_WORKSPACE: return "TT_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case TT_ERR_CUDA: return "TT_ERR_CUDA: CUDA call or launch failed";
+    case TT_ERR_TIMEOUT: return "TT_ERR_TIMEOUT: a bounded device wait ran out";
+    case TT_ERR_DEVICE: return "TT_ERR_DEVICE: device-side check failed";
+  }
+  return "unknown tt_status";
+}
+
+}  // extern "C"

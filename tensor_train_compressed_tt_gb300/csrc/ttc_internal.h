@@ -1,0 +1,86 @@
+// Internal declarations shared by the libttc translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "ttc.h"
+
+namespace ttc {
+
+constexpr int kMaxK = 2 * TT_MAX_D;  // cores per layer
+
+// One TT layer after validation.  Core k (0-based) has shape
+// (r[k], s[k], r[k+1]); diagonal e (0-based) sits on the link between core e
+// and core e+1 and has r[e+1] entries; the middle diagonal is e = d-1.
+struct LayerPlan {
+  int d = 0, K = 0;
+  int s[kMaxK] = {};
+  int r[kMaxK + 1] = {};
+  int64_t N = 0, M = 0;
+  int rd = 0;         // middle rank r_d
+  int act = TT_DT_F32;
+  unsigned flags = 0;
+  size_t core_off[kMaxK] = {};
+  size_t diag_off[kMaxK - 1] = {};
+  size_t n_floats = 0;
+  // chain: U[k] = number of rows of the merged prefix ending at core k
+  // (input side: s_0..s_k; output side: r_d * s_d..s_k)
+  int64_t U[kMaxK] = {};
+};
+
+}  // namespace ttc
+
+struct tt_plan_s {
+  int kind = 0;  // 0 = single layer, 1 = FFN pair
+  ttc::LayerPlan L[2];
+};
+
+namespace ttc {
+
+// ---- device status word (first 256 bytes of every workspace) -------------
+struct DeviceStatus {
+  unsigned code;    // 0 = ok, else a tt_status value
+  unsigned detail;  // where it happened (kernel-specific)
+};
+
+// ---- measurement hooks (profile.cu) ---------------------------------------
+enum Phase { kPhMerge = 0, kPhFwd = 1, kPhBwd = 2, kPhMergeBwd = 3, kPhElem = 4 };
+void prof_begin(int phase, cudaStream_t st);
+void prof_end(int phase, cudaStream_t st);
+void count_launches(int n);
+
+// ---- SIMT kernels (simt_kernels.cu) ----------------------------------------
+enum GemmMode { kStore = 0, kAccumulate = 1, kAtomic = 2 };
+
+// C[m,n] (op)= rscale[m] * cscale[n % clen] * sum_k A[m,k] kscale[k % klen] B[k,n]
+// Element (i,j) of X lives at X[i*si + j*sj].  Types: 0 = f32, 1 = bf16.
+struct GemmArgs {
+  int64_t m = 0, n = 0, k = 0;
+  const void* A = nullptr; int64_t sam = 0, sak = 0; int ta = 0;
+  const void* B = nullptr; int64_t sbk = 0, sbn = 0; int tb = 0;
+  void* C = nullptr; int64_t scm = 0, scn = 0; int tc = 0;
+  const float* kscale = nullptr; int klen = 1;
+  const float* rscale = nullptr;
+  const float* cscale = nullptr; int clen = 1;
+  int mode = kStore;
+};
+cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t st);
+
+// out[c] (=|+=) sum_u X[u*sx + c] * Y[u*sy + c], c < ncols; out[c] = 0 (or
+// left unchanged when accumulating) where mask[c] == 0.
+cudaError_t coldot(int64_t nrows, int ncols, const float* X, int64_t sx, const float* Y,
+                   int64_t sy, const float* mask, float* out, bool accumulate,
+                   cudaStream_t st);
+
+// out[i] (=|+=) in[i] * scale[i % len]  (scale may be null: plain copy)
+cudaError_t scale_periodic(int64_t n, const float* in, const float* scale, int len, float* out,
+                           bool accumulate, cudaStream_t st);
+
+// a = GELU(h) (exact erf form), written as f32 or bf16
+cudaError_t gelu_fwd(int64_t n, const float* h, void* a, int ta, cudaStream_t st);
+// dh = da * GELU'(h), in place over da (f32)
+cudaError_t gelu_bwd(int64_t n, const float* h, float* da, cudaStream_t st);
+
+}  // namespace ttc

@@ -1,0 +1,128 @@
+"""PyTorch-facing wrappers over the libttc C ABI.
+
+PyTorch supplies device memory and the stream; each method marshals tensor
+pointers into one libttc call.  No arithmetic happens here.
+"""
+
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import ttc
+
+_DT = {torch.float32: ttc.TT_DT_F32, torch.bfloat16: ttc.TT_DT_BF16}
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+class TTLinear:
+    """One TT linear layer: y (T x M) = x (T x N) W^T, W given by packed cores."""
+
+    def __init__(self, in_modes: Sequence[int], out_modes: Sequence[int],
+                 ranks: Sequence[int], dtype: torch.dtype = torch.bfloat16,
+                 accumulate: bool = False):
+        self.in_modes = tuple(in_modes)
+        self.out_modes = tuple(out_modes)
+        self.ranks = tuple(ranks)
+        self.dtype = dtype
+        flags = ttc.TT_ACCUMULATE if accumulate else 0
+        self.desc = ttc.make_desc(in_modes, out_modes, ranks, _DT[dtype], flags)
+        self.plan = ttc.tt_plan(self.desc)
+        self.core_off, self.diag_off, self.n_params = ttc.tt_param_layout(self.plan)
+        self.N = 1
+        self.M = 1
+        for n in in_modes:
+            self.N *= n
+        for m in out_modes:
+            self.M *= m
+
+    def workspace_bytes(self, T: int) -> int:
+        return ttc.tt_workspace_size(self.plan, T)
+
+    def workspace(self, T: int, device="cuda") -> torch.Tensor:
+        return torch.empty(self.workspace_bytes(T), dtype=torch.uint8, device=device)
+
+    def forward(self, x: torch.Tensor, params: torch.Tensor, y: Optional[torch.Tensor] = None,
+                ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.M), dtype=self.dtype, device=x.device)
+        if ws is None:
+            ws = self.workspace(T, x.device)
+        ttc.check(ttc.tt_forward(self.plan, T, _ptr(x), _ptr(params), _ptr(y), _ptr(ws),
+                                 ws.numel(), _stream(stream)), "tt_forward")
+        return y
+
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, params: torch.Tensor,
+                 dx: Optional[torch.Tensor] = None, dparams: Optional[torch.Tensor] = None,
+                 ws: Optional[torch.Tensor] = None, stream=None):
+        T = x.shape[0]
+        if dx is None:
+            dx = torch.empty((T, self.N), dtype=self.dtype, device=x.device)
+        if dparams is None:
+            dparams = torch.empty(self.n_params, dtype=torch.float32, device=x.device)
+        if ws is None:
+            ws = self.workspace(T, x.device)
+        ttc.check(ttc.tt_backward(self.plan, T, _ptr(x), _ptr(dy), _ptr(params), _ptr(dx),
+                                  _ptr(dparams), _ptr(ws), ws.numel(), _stream(stream)),
+                  "tt_backward")
+        return dx, dparams
+
+
+class TTFFN:
+    """y = TT_down(GELU(TT_up(x))), exact erf GELU, both layers through one plan."""
+
+    def __init__(self, up: Sequence[Sequence[int]], down: Sequence[Sequence[int]],
+                 dtype: torch.dtype = torch.bfloat16, accumulate: bool = False):
+        flags = ttc.TT_ACCUMULATE if accumulate else 0
+        self.dtype = dtype
+        self.up_desc = ttc.make_desc(up[0], up[1], up[2], _DT[dtype], flags)
+        self.down_desc = ttc.make_desc(down[0], down[1], down[2], _DT[dtype], flags)
+        self.plan = ttc.tt_ffn_plan(self.up_desc, self.down_desc)
+        self.layout = [ttc.tt_ffn_param_layout(self.plan, i) for i in (0, 1)]
+        self.N = 1
+        self.M = 1
+        for n in up[0]:
+            self.N *= n
+        for m in down[1]:
+            self.M *= m
+
+    def workspace(self, T: int, device="cuda") -> torch.Tensor:
+        return torch.empty(ttc.tt_workspace_size(self.plan, T), dtype=torch.uint8,
+                           device=device)
+
+    def forward(self, x, p_up, p_down, y=None, ws=None, stream=None):
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.M), dtype=self.dtype, device=x.device)
+        if ws is None:
+            ws = self.workspace(T, x.device)
+        ttc.check(ttc.tt_ffn_forward(self.plan, T, _ptr(x), _ptr(p_up), _ptr(p_down), _ptr(y),
+                                     _ptr(ws), ws.numel(), _stream(stream)), "tt_ffn_forward")
+        return y
+
+    def backward(self, x, dy, p_up, p_down, dx=None, dp_up=None, dp_down=None, ws=None,
+                 stream=None):
+        T = x.shape[0]
+        if dx is None:
+            dx = torch.empty((T, self.N), dtype=self.dtype, device=x.device)
+        if dp_up is None:
+            dp_up = torch.empty(self.layout[0][2], dtype=torch.float32, device=x.device)
+        if dp_down is None:
+            dp_down = torch.empty(self.layout[1][2], dtype=torch.float32, device=x.device)
+        if ws is None:
+            ws = self.workspace(T, x.device)
+        ttc.check(ttc.tt_ffn_backward(self.plan, T, _ptr(x), _ptr(dy), _ptr(p_up),
+                                      _ptr(p_down), _ptr(dx), _ptr(dp_up), _ptr(dp_down),
+                                      _ptr(ws), ws.numel(), _stream(stream)),
+                  "tt_ffn_backward")
+        return dx, dp_up, dp_down

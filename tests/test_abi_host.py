@@ -1,0 +1,131 @@
+"""Host-side checks of the libttc C ABI (no GPU work is launched here)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import tt_oracle as O
+from tensor_train_compressed_tt_gb300 import synth, ttc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tensor_train_compressed_tt_gb300 import _build
+    _build.build()
+    return ttc.lib()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        txt = open(os.path.join(ROOT, "include", fn)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        names |= set(re.findall(r"\b(tt_[a-z_0-9]+)\s*\(", txt))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_symbols()
+    assert {"tt_plan", "tt_forward", "tt_backward", "tt_workspace_size"} <= names
+    for n in sorted(names):
+        assert hasattr(lib, n), n
+
+
+def _desc(shape, act=ttc.TT_DT_BF16, flags=0):
+    return ttc.make_desc(shape.in_modes, shape.out_modes, shape.ranks, act, flags)
+
+
+def test_default_ranks_match_oracle(lib):
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        d = int(rng.integers(1, 5))
+        im = [int(v) for v in rng.integers(1, 20, size=d)]
+        om = [int(v) for v in rng.integers(1, 20, size=d)]
+        R = int(rng.integers(1, 80))
+        assert ttc.tt_default_ranks(im, om, R) == O.rank_caps(im, om, R)
+
+
+@pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
+def test_param_layout_matches_pack(lib, name):
+    w = synth.WORKLOADS[name]
+    for shape in w.layers:
+        plan = ttc.tt_plan(_desc(shape))
+        core_off, diag_off, n = ttc.tt_param_layout(plan)
+        off = 0
+        for k, cs in enumerate(shape.core_shapes()):
+            assert core_off[k] == off
+            off += int(np.prod(cs))
+        for e, ds in enumerate(shape.diag_sizes()):
+            assert diag_off[e] == off
+            off += ds
+        assert n == off
+
+
+def test_ffn_layout_and_validation(lib):
+    w = synth.WORKLOADS["ffn768_3072_bf16"]
+    up, dn = w.layers
+    plan = ttc.tt_ffn_plan(_desc(up), _desc(dn))
+    for i, shape in enumerate((up, dn)):
+        _, _, n = ttc.tt_ffn_param_layout(plan, i)
+        assert n == sum(int(np.prod(c)) for c in shape.core_shapes()) + sum(shape.diag_sizes())
+    with pytest.raises(ttc.TTError):
+        ttc.tt_ffn_plan(_desc(up), _desc(up))   # widths do not chain
+    with pytest.raises(ttc.TTError):
+        ttc.tt_ffn_plan(_desc(up), _desc(dn, act=ttc.TT_DT_F32))
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda d: setattr(d, "d", 0),
+    lambda d: setattr(d, "d", 5),
+    lambda d: d.ranks.__setitem__(0, 2),
+    lambda d: d.ranks.__setitem__(6, 3),
+    lambda d: d.ranks.__setitem__(3, 0),
+    lambda d: d.in_modes.__setitem__(1, 0),
+    lambda d: setattr(d, "act", 7),
+    lambda d: setattr(d, "flags", 0x80),
+])
+def test_invalid_descriptors_rejected(lib, mutate):
+    shape = synth.WORKLOADS["tt768_bf16"].layers[0]
+    desc = _desc(shape)
+    mutate(desc)
+    with pytest.raises(ttc.TTError) as e:
+        ttc.tt_plan(desc)
+    assert e.value.code == 1
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    plan = ttc.tt_plan(_desc(synth.WORKLOADS["tt768_bf16"].layers[0]))
+    a = ttc.tt_workspace_size(plan, 0)
+    b = ttc.tt_workspace_size(plan, 128)
+    c = ttc.tt_workspace_size(plan, 16384)
+    assert 0 < a <= b <= c and a % 256 == 0 and c % 256 == 0
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    plan = ttc.tt_plan(_desc(synth.WORKLOADS["tt768_bf16"].layers[0]))
+    ws_need = ttc.tt_workspace_size(plan, 64)
+    fake = 1 << 40   # never dereferenced: every call below fails its host checks
+    # T == 0 is a no-op for the forward
+    assert ttc.tt_forward(plan, 0, 0, 0, 0, 0, 0) == 0
+    assert ttc.tt_forward(plan, -1, fake, fake, fake, fake, ws_need) == 1
+    assert ttc.tt_forward(plan, 64, 0, fake, fake, fake, ws_need) == 1          # NULL x
+    assert ttc.tt_forward(plan, 64, fake + 2, fake, fake, fake, ws_need) == 1   # misaligned x
+    assert ttc.tt_forward(plan, 64, fake, fake, fake, 0, ws_need) == 3          # no workspace
+    assert ttc.tt_forward(plan, 64, fake, fake, fake, fake + 16, ws_need) == 3  # misaligned ws
+    assert ttc.tt_forward(plan, 64, fake, fake, fake, fake, ws_need - 1) == 3   # too small
+    assert ttc.tt_backward(plan, 64, fake, fake, fake, fake, 0, fake, ws_need) == 1
+    assert ttc.tt_backward(plan, 64, fake, fake + 8, fake, fake, fake, fake, ws_need) == 1
+    # a single-layer plan is not an FFN plan
+    assert ttc.tt_ffn_forward(plan, 64, fake, fake, fake, fake, fake, ws_need) == 1
+
+
+def test_status_strings(lib):
+    for code, name in ttc.STATUS.items():
+        assert ttc.tt_status_string(code).startswith(name)

@@ -1,0 +1,158 @@
+"""GPU parity: libttc (through the C ABI) against the fp64 oracle.
+
+Tolerances (norm-wise relative error per output tensor): 1e-4 for f32
+activations, 2e-2 for bf16 activations with f32 accumulation; tensors whose
+reference is exactly zero (pruned slices, removed layers) must be exactly 0.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import tt_oracle as O
+from tensor_train_compressed_tt_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from tensor_train_compressed_tt_gb300 import _build
+    _build.build()
+
+
+from parity_util import TOL, compare, gpu_ffn, gpu_layer, oracle_ffn, oracle_layer  # noqa: E402
+
+
+def _run(name, tokens=None, seed=0):
+    w = synth.WORKLOADS[name]
+    inp = synth.draw(w, seed=seed, tokens=tokens)
+    shape = w.layers[0]
+    out = gpu_layer(shape, w.act, inp.layers[0], inp.x, inp.dy)
+    ref = oracle_layer(shape, inp.layers[0], inp.x, inp.dy)
+    return compare(out, ref, TOL[w.act], f"{name} T={inp.x.shape[0]}")
+
+
+def test_tiny64_f32():
+    _run("tiny64_f32")
+
+
+@pytest.mark.parametrize("T", [1, 7, 128, 300, 16384])
+def test_tt768_bf16(T):
+    _run("tt768_bf16", tokens=T)
+
+
+@pytest.mark.parametrize("name", ["pruned768_3072_bf16", "pruned768_768_bf16"])
+def test_pruned_equals_truncated(name):
+    _run(name)
+    # and the truncated TT (slices removed) gives the same forward
+    w = synth.WORKLOADS[name]
+    inp = synth.draw(w, seed=0, tokens=257)
+    shape = w.layers[0]
+    tc, td, _ = O.truncate(inp.layers[0].cores, inp.layers[0].diags)
+    tshape = synth.LayerShape(shape.in_modes, shape.out_modes,
+                              tuple([1] + [len(e) for e in td] + [1]))
+    out_t = gpu_layer(tshape, w.act, synth.LayerInputs(tc, td), inp.x, inp.dy)
+    out_z = gpu_layer(shape, w.act, inp.layers[0], inp.x, inp.dy)
+    assert O.rel_err(out_z["y"], out_t["y"]) <= TOL[w.act]
+    assert O.rel_err(out_z["dx"], out_t["dx"]) <= TOL[w.act]
+
+
+@pytest.mark.parametrize("T", [4096])
+def test_tt1024_4096(T):
+    _run("tt1024_4096_bf16", tokens=T)
+
+
+def test_ffn_pair():
+    w = synth.WORKLOADS["ffn768_3072_bf16"]
+    inp = synth.draw(w, seed=0, tokens=1000)
+    out, gu, gd = gpu_ffn(w, inp)
+    ref, ru, rd = oracle_ffn(w, inp)
+    tol = TOL[w.act]
+    assert O.rel_err(out["y"], ref["y"]) <= tol
+    assert O.rel_err(out["dx"], ref["dx"]) <= tol
+    for (a, b) in list(zip(gu[0], ru[0])) + list(zip(gd[0], rd[0])):
+        assert O.rel_err(a, b) <= tol
+    for (a, b) in list(zip(gu[1], ru[1])) + list(zip(gd[1], rd[1])):
+        assert O.rel_err(a, b) <= tol
+
+
+@pytest.mark.parametrize("d", [1, 2, 3, 4])
+@pytest.mark.parametrize("act", ["f32", "bf16"])
+def test_random_small_shapes(d, act):
+    rng = np.random.Generator(np.random.PCG64(100 + d))
+    for trial in range(4):
+        shape = synth.random_shape(rng, d, max_mode=5, max_rank=6)
+        li = synth.draw_layer(rng, shape, 0.5, "uniform" if trial % 2 else "pruned_half")
+        T = int(rng.integers(1, 200))
+        x = rng.standard_normal((T, shape.N)).astype(np.float32)
+        dy = rng.standard_normal((T, shape.M)).astype(np.float32)
+        if act == "bf16":
+            x, dy = synth.round_bf16(x), synth.round_bf16(dy)
+        out = gpu_layer(shape, act, li, x, dy)
+        ref = oracle_layer(shape, li, x, dy)
+        compare(out, ref, TOL[act], f"d={d} {shape} T={T}")
+
+
+def test_zero_tokens_backward_gives_zero_gradients():
+    w = synth.WORKLOADS["tt768_bf16"]
+    inp = synth.draw(w, seed=0, tokens=1)
+    out = gpu_layer(w.layers[0], w.act, inp.layers[0], inp.x[:0], inp.dy[:0])
+    assert out["y"].shape == (0, w.layers[0].M)
+    assert all(np.all(g == 0) for g in out["dcores"])
+    assert all(np.all(g == 0) for g in out["ddiags"])
+
+
+def test_accumulate_flag_adds_into_dparams():
+    import torch as th
+    from tensor_train_compressed_tt_gb300.layer import TTLinear
+    w = synth.WORKLOADS["tt768_bf16"]
+    inp = synth.draw(w, seed=1, tokens=333)
+    s = w.layers[0]
+    params = th.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
+    x = th.from_numpy(inp.x).cuda().bfloat16()
+    dy = th.from_numpy(inp.dy).cuda().bfloat16()
+    plain = TTLinear(s.in_modes, s.out_modes, s.ranks, th.bfloat16)
+    _, g1 = plain.backward(x, dy, params)
+    acc = TTLinear(s.in_modes, s.out_modes, s.ranks, th.bfloat16, accumulate=True)
+    base = th.full_like(g1, 0.25)
+    g2 = base.clone()
+    acc.backward(x, dy, params, dparams=g2)
+    th.cuda.synchronize()
+    np.testing.assert_allclose((g2 - base).cpu().numpy(), g1.cpu().numpy(), rtol=1e-5,
+                               atol=1e-6)
+
+
+def test_all_zero_middle_link_removes_layer():
+    w = synth.WORKLOADS["tt768_bf16"]
+    inp = synth.draw(w, seed=2, tokens=200)
+    li = inp.layers[0]
+    li.diags[w.layers[0].d - 1][:] = 0.0
+    out = gpu_layer(w.layers[0], w.act, li, inp.x, inp.dy)
+    assert np.all(out["y"] == 0) and np.all(out["dx"] == 0)
+    assert all(np.all(g == 0) for g in out["dcores"])
+    assert all(np.all(g == 0) for g in out["ddiags"])
+
+
+def test_full_size_identities_tt1024_4096():
+    """At 32768 tokens: <x,dx> = <G_k,dG_k> = <D_k,dD_k> = <dy,y> for every k."""
+    w = synth.WORKLOADS["tt1024_4096_bf16"]
+    inp = synth.draw(w, seed=0)
+    shape = w.layers[0]
+    out = gpu_layer(shape, w.act, inp.layers[0], inp.x, inp.dy)
+    ref = float(np.sum(out["y"].astype(np.float64) * inp.dy))
+    scale = float(np.linalg.norm(out["y"])) * float(np.linalg.norm(inp.dy))
+    # bf16 rounding of y and dx bounds how well the products can agree
+    assert abs(float(np.sum(inp.x.astype(np.float64) * out["dx"])) - ref) <= 2e-2 * scale
+    for c, g in zip(inp.layers[0].cores, out["dcores"]):
+        assert abs(float(np.sum(c.astype(np.float64) * g)) - ref) <= 2e-2 * scale
+    for e, g in zip(inp.layers[0].diags, out["ddiags"]):
+        assert abs(float(np.sum(e.astype(np.float64) * g)) - ref) <= 2e-2 * scale
+    # sampled rows of y and dx against the oracle, one token at a time
+    rows = np.random.default_rng(0).choice(inp.x.shape[0], 64, replace=False)
+    sub = oracle_layer(shape, inp.layers[0], inp.x[rows], inp.dy[rows])
+    assert O.rel_err(out["y"][rows], sub["y"]) <= TOL[w.act]
+    assert O.rel_err(out["dx"][rows], sub["dx"]) <= TOL[w.act]
