@@ -357,7 +357,7 @@ def run_ours(args, w):
     W = max(3, args.warmup)
     for i in range(W):
         step(i)
-    ttc.check(ttc.tt_get_device_status(wsp, sh), "device status after warm-up")
+    ttc.check(ttc.tt_get_device_status(sh), "device status after warm-up")
     barrier()
     # choose K for a timed region of about target-seconds when not given
     if args.steps is None:
@@ -398,7 +398,7 @@ def run_ours(args, w):
         t = torch.tensor([ms], device=dev, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    ttc.check(ttc.tt_get_device_status(wsp, sh), "device status after timed region")
+    ttc.check(ttc.tt_get_device_status(sh), "device status after timed region")
 
     # ---- per-phase CUDA-event timing of the library's kernels (same steps)
     ttc.lib().tt_profile_enable(1)

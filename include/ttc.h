@@ -31,7 +31,8 @@
  *  - Argument errors are reported before anything is enqueued.  A failed
  *    launch returns TT_ERR_CUDA.  Errors found on the device (a bounded wait
  *    that ran out, a failed consistency check) are recorded in a status word
- *    inside the workspace and read back by tt_get_device_status.
+ *    that the library keeps in device memory, one per GPU (a module-scope
+ *    variable, zero at load), and read back by tt_get_device_status.
  *  - Activations: x is (T, N), y is (T, M), dy is (T, M), dx is (T, N), all
  *    row-major, dense, in the plan's activation type (f32 or bf16), 16-byte
  *    aligned.  Cores, diagonals and their gradients are f32.
@@ -127,9 +128,11 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
                           float* dparams_up, float* dparams_down, void* ws, size_t ws_bytes,
                           void* stream);
 
-/* Synchronise stream, read and clear the device status word in ws.
- * Returns TT_OK, TT_ERR_TIMEOUT or TT_ERR_DEVICE (or TT_ERR_CUDA). */
-tt_status tt_get_device_status(const void* ws, void* stream);
+/* Synchronise stream, then read and clear the status word of the current
+ * device.  The word is sticky: it holds the first error any libttc kernel
+ * on this device recorded since the last read.  Returns TT_OK,
+ * TT_ERR_TIMEOUT or TT_ERR_DEVICE (or TT_ERR_CUDA). */
+tt_status tt_get_device_status(void* stream);
 
 const char* tt_status_string(tt_status s);
 

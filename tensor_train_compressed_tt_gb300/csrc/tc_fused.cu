@@ -1,17 +1,1033 @@
+// Fused token-tile kernels for bf16 activations on sm_103a: tcgen05 MMAs with
+// TMEM accumulators, TMA (128-byte swizzle) staging, mbarrier pipelines.
+//
+// The contraction order is the one of the CoMERA project page ("Making small
+// tensor operations fast on GPUs", bullet "One contraction order for both
+// passes"): the merged input side A (N x r) and output side B (r x M) are
+// applied to a tile of 128 tokens at a time, and the rank-r intermediates
+// z = x A, z' = z diag(D_d), dz' = dy B^T, dz = dz' diag(D_d) never leave the
+// SM (TMEM and shared memory).
+//
+// Layout of the packed operands (bf16, rank padded to RP = 64 with zero rows
+// or columns; the middle rank is compacted to the nonzero entries of D_d, so
+// pruned ranks cost nothing but padding):
+//   At  (RP x N)  B operand of z  = x  . At^T   (K = features, K-major)
+//   Anr (N x RP)  B operand of dx = dz . Anr^T  (K = rank, K-major)
+//   Bm  (RP x M)  B operand of dz'= dy . Bm^T   (K = outputs, K-major)
+//   Bt  (M x RP)  B operand of y  = z' . Bt^T   (K = rank, K-major)
+// The weight-side products dA = x^T dz and dB^T = dy^T z' read the very same
+// x / dy / z' / dz tiles through MN-major descriptors (the 128-byte swizzled
+// [token][64 elements] tile is K-major for the token-side products and
+// MN-major for the weight-side ones).
+//
+// Every mbarrier wait is bounded (global timer); on expiry the CTA records
+// TT_ERR_TIMEOUT in the per-device status word, raises a shared abort flag so
+// the other roles stop, waits (bounded) for its own copies and MMAs, frees its
+// TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
 #include "tc_fused.h"
 
 namespace ttc {
 
-bool tc_supported(const LayerPlan&) { return false; }
-size_t tc_operand_bytes(const LayerPlan&) { return 256; }
-tt_status tc_forward(const LayerPlan&, int64_t, const void*, const float*, const float*,
-                     const float*, void*, void*, size_t, cudaStream_t) {
-  return TT_ERR_UNSUPPORTED;
+__device__ DeviceStatus g_status;
+
+cudaError_t read_and_clear_device_status(DeviceStatus* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(DeviceStatus));
+  if (e != cudaSuccess) return e;
+  DeviceStatus z{0, 0};
+  return cudaMemcpyToSymbol(g_status, &z, sizeof(z));
 }
-tt_status tc_backward(const LayerPlan&, int64_t, const void*, const void*, const float*,
-                      const float*, const float*, void*, float*, bool, float*, float*, void*,
-                      size_t, cudaStream_t) {
-  return TT_ERR_UNSUPPORTED;
+
+namespace {
+
+constexpr int TILE = 128;            // tokens per tile (MMA M)
+constexpr int RP = 64;               // padded rank (one 128-byte swizzle atom)
+constexpr int CH = 128;              // features / outputs per pipeline chunk
+constexpr int BOX = 16 * 1024;       // [128 rows][64 bf16] swizzled box
+constexpr int STAGE = 48 * 1024;     // 2 activation boxes + 16 KB operand
+constexpr int OPND = 32 * 1024;      // operand offset inside a stage
+constexpr int NSTAGE_F = 4;
+constexpr int NSTAGE_B = 3;
+constexpr int NEPI = 8;              // epilogue warps
+constexpr int NTHREADS = (2 + NEPI) * 32;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+// TMEM columns
+constexpr uint32_t F_Z = 0, F_Y = 128;                       // forward
+constexpr uint32_t B_Z = 0, B_DZP = 64, B_W = 128, B_X = 256;  // backward
+constexpr uint32_t TMEM_COLS = 512;
+
+// --------------------------------------------------------------------------
+// PTX helpers
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ void record_error(unsigned code, unsigned where) {
+  if (atomicCAS(&g_status.code, 0u, code) == 0u) atomicExch(&g_status.detail, where);
+}
+
+// Wait for the phase of the given parity; false if aborted or timed out.
+__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                         unsigned where) {
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = gtimer();
+  while (!mbar_try_wait(b, parity)) {
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      record_error(TT_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-uniform wait: lane 0 polls, the result is broadcast, so that the
+// warp stays converged for the .sync.aligned TMEM loads that follow.
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                          unsigned where) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(b, parity, abort_flag, where) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Drain wait used on the way out: bounded, ignores the abort flag.
+__device__ __forceinline__ void drain_bar(uint64_t* b, uint32_t parity) {
+  const uint64_t t0 = gtimer();
+  while (!mbar_try_wait(b, parity)) {
+    if (gtimer() - t0 > kTimeoutNs / 4) return;
+  }
+}
+
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                         int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// smem matrix descriptor, 128-byte swizzle, sm_100 family (version 1)
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc(saddr, 16, 1024); }
+__device__ __forceinline__ uint64_t mndesc(uint32_t saddr, uint32_t lbo) {
+  return sdesc(saddr, lbo, 1024);
+}
+
+// instruction descriptor: bf16 x bf16 -> f32, dense
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t id,
+                                    uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dtmem),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          su32(bar))
+      : "memory");
+}
+
+#define TT_LD32_REGS                                                                         \
+  "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, " \
+  "%19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}"
+
+// 32 consecutive f32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " TT_LD32_REGS ", [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                 "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+                 "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+                 "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+                 "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Write 32 values (columns [32h, 32h+32) of row `row`) as bf16 into a
+// [128][64] tile in the 128-byte swizzled layout used by TMA and the MMAs.
+__device__ __forceinline__ void st_tile_half(uint8_t* tile, int row, int h, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    const int chunk = (4 * h + q) ^ (row & 7);
+    *reinterpret_cast<uint4*>(tile + row * 128 + chunk * 16) = u;
+  }
+}
+
+// 32 bf16 values to global (row-major), 16-byte pieces inside [0, ncols)
+__device__ __forceinline__ void st_row32(__nv_bfloat16* dst_row, int col0, int ncols,
+                                         const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (col0 + 8 * q + 8 > ncols) continue;
+    uint4 u;
+    u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    *reinterpret_cast<uint4*>(dst_row + col0 + 8 * q) = u;
+  }
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+// After the butterfly, lane l holds sum over the warp's 32 lanes of v[l].
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+struct FwdArgs {
+  int64_t T;
+  int N, M, nN, nM, ntiles;
+  const float* Dc;
+  __nv_bfloat16* y;
+};
+
+struct BwdArgs {
+  int64_t T;
+  int N, M, nN, nM, ntiles;
+  const float* Dc;
+  const int* rinfo;  // [0] = r', [1..64] = kept index of each compacted column
+  __nv_bfloat16* dx;
+  float* dAc;  // N x RP
+  float* dBc;  // RP x M
+  float* dDc;  // RP
+};
+
+struct SmemCommon {
+  uint64_t full[4], empty[4];
+  uint64_t z_full, z_empty, zp_full, zp_empty, dzp_full, dzp_empty, dz_full, dz_empty;
+  uint64_t w_full[2], w_empty[2], x_full[2], x_empty[2];
+  uint64_t fin;
+  uint32_t tmem_base;
+  int abort_flag;
+  float Dc[RP];
+};
+
+__device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ void tmem_alloc(uint32_t* slot) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   su32(slot)),
+               "r"(TMEM_COLS)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ void tmem_free(uint32_t base) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base),
+               "r"(TMEM_COLS)
+               : "memory");
+}
+
+// ==========================================================================
+// forward: y = ((x At^T) diag(Dc)) Bt^T per 128-token tile
+// ==========================================================================
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tt_fwd_kernel(const __grid_constant__ CUtensorMap tm_x,
+                  const __grid_constant__ CUtensorMap tm_at,
+                  const __grid_constant__ CUtensorMap tm_bt, FwdArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1k(smem_raw);
+  uint8_t* stages = base;
+  uint8_t* zp_tile = base + NSTAGE_F * STAGE;
+  SmemCommon& S = *reinterpret_cast<SmemCommon*>(zp_tile + BOX);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE_F; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    mbar_init(&S.z_full, 1);
+    mbar_init(&S.z_empty, NEPI);
+    mbar_init(&S.zp_full, NEPI);
+    mbar_init(&S.zp_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.x_full[b], 1);
+      mbar_init(&S.x_empty[b], NEPI);
+    }
+    mbar_init(&S.fin, 1);
+    S.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
+  if (warp == 1) tmem_alloc(&S.tmem_base);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort_flag = &S.abort_flag;
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int it = 0;
+      int last_parity[NSTAGE_F];
+      for (int s = 0; s < NSTAGE_F; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
+        const int tok0 = tile * TILE;
+        for (int c = 0; ok && c < p.nN + p.nM; ++c, ++it) {
+          const int s = it % NSTAGE_F;
+          const uint32_t ph = (it / NSTAGE_F) & 1;
+          if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 1)) { ok = false; break; }
+          uint8_t* st = stages + s * STAGE;
+          if (c < p.nN) {
+            mbar_expect_tx(&S.full[s], STAGE);
+            tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
+            tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
+            tma_load(st + OPND, &tm_at, &S.full[s], c * CH, 0);
+            tma_load(st + OPND + BOX / 2, &tm_at, &S.full[s], c * CH + 64, 0);
+          } else {
+            mbar_expect_tx(&S.full[s], BOX);
+            tma_load(st + OPND, &tm_bt, &S.full[s], 0, (c - p.nN) * CH);
+          }
+          last_parity[s] = (int)ph;
+        }
+      }
+      for (int s = 0; s < NSTAGE_F; ++s)
+        if (last_parity[s] >= 0) drain_bar(&S.full[s], (uint32_t)last_parity[s]);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_z = idesc(128, 64, 0, 0);
+      const uint32_t id_y = idesc(128, 128, 0, 0);
+      const uint32_t zp_addr = su32(zp_tile);
+      int it = 0, yc = 0, tl = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
+        if (!wait_bar(&S.z_empty, (tl & 1) ^ 1, abort_flag, 2)) break;
+        tc_fence_after();
+        for (int c = 0; c < p.nN; ++c, ++it) {
+          const int s = it % NSTAGE_F;
+          if (!wait_bar(&S.full[s], (it / NSTAGE_F) & 1, abort_flag, 3)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = su32(stages + s * STAGE);
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma(tmem + F_Z, kdesc(st + b * BOX) + 2 * k, kdesc(st + OPND + b * (BOX / 2)) + 2 * k,
+                  id_z, (c | b | k) != 0);
+          mma_commit(&S.empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&S.z_full);
+        if (!wait_bar(&S.zp_full, tl & 1, abort_flag, 4)) break;
+        tc_fence_after();
+        for (int c = 0; c < p.nM; ++c, ++it, ++yc) {
+          const int s = it % NSTAGE_F;
+          const int yb = yc & 1;
+          if (!wait_bar(&S.x_empty[yb], ((yc >> 1) & 1) ^ 1, abort_flag, 5)) { ok = false; break; }
+          if (!wait_bar(&S.full[s], (it / NSTAGE_F) & 1, abort_flag, 6)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = su32(stages + s * STAGE);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma(tmem + F_Y + yb * 128, kdesc(zp_addr) + 2 * k, kdesc(st + OPND) + 2 * k, id_y,
+                k != 0);
+          mma_commit(&S.empty[s]);
+          mma_commit(&S.x_full[yb]);
+        }
+        if (!ok) break;
+        mma_commit(&S.zp_empty);
+      }
+      mma_commit(&S.fin);
+      drain_bar(&S.fin, 0);
+    }
+  } else {
+    // ---------------- epilogue: 8 warps, thread = (token row, column half)
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int row = 32 * q + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    int yc = 0, tl = 0;
+    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tl) {
+      const int64_t tok = (int64_t)tile * TILE + row;
+      float v[32];
+      if (!warp_wait(&S.z_full, tl & 1, abort_flag, 7)) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + F_Z + 32 * h, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.z_empty);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= S.Dc[32 * h + j];
+      if (!warp_wait(&S.zp_empty, (tl & 1) ^ 1, abort_flag, 8)) break;
+      st_tile_half(zp_tile, row, h, v);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.zp_full);
+      bool ok = true;
+      for (int c = 0; c < p.nM; ++c, ++yc) {
+        const int yb = yc & 1;
+        if (!warp_wait(&S.x_full[yb], (yc >> 1) & 1, abort_flag, 9)) { ok = false; break; }
+        tc_fence_after();
+        __nv_bfloat16* yrow = p.y + tok * p.M;
+#pragma unroll
+        for (int piece = 0; piece < 2; ++piece) {
+          tmem_ld32(tmem + lane_off + F_Y + yb * 128 + 64 * h + 32 * piece, v);
+          if (tok < p.T) st_row32(yrow, c * CH + 64 * h + 32 * piece, p.M, v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.x_empty[yb]);
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_free(tmem);
+}
+
+// ==========================================================================
+// backward: per 128-token tile
+//   A  z   = x At^T                       (x streamed, 128 features a chunk)
+//   B  dz' = dy Bm^T ; dB^T += dy^T z'    (dy streamed, 128 outputs a chunk)
+//   C  dx  = dz Anr^T ; dA += x^T dz      (x streamed again)
+// with z' = z diag(Dc), dz = dz' diag(Dc), dDc += sum_t z * dz'.
+// ==========================================================================
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tt_bwd_kernel(const __grid_constant__ CUtensorMap tm_x,
+                  const __grid_constant__ CUtensorMap tm_dy,
+                  const __grid_constant__ CUtensorMap tm_at,
+                  const __grid_constant__ CUtensorMap tm_bm,
+                  const __grid_constant__ CUtensorMap tm_anr, BwdArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1k(smem_raw);
+  uint8_t* stages = base;
+  uint8_t* zp_tile = base + NSTAGE_B * STAGE;
+  uint8_t* dz_tile = zp_tile + BOX;
+  SmemCommon& S = *reinterpret_cast<SmemCommon*>(dz_tile + BOX);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE_B; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    mbar_init(&S.z_full, 1);
+    mbar_init(&S.z_empty, NEPI);
+    mbar_init(&S.zp_full, NEPI);
+    mbar_init(&S.zp_empty, 1);
+    mbar_init(&S.dzp_full, 1);
+    mbar_init(&S.dzp_empty, NEPI);
+    mbar_init(&S.dz_full, NEPI);
+    mbar_init(&S.dz_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.w_full[b], 1);
+      mbar_init(&S.w_empty[b], NEPI);
+      mbar_init(&S.x_full[b], 1);
+      mbar_init(&S.x_empty[b], NEPI);
+    }
+    mbar_init(&S.fin, 1);
+    S.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
+  if (warp == 1) tmem_alloc(&S.tmem_base);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort_flag = &S.abort_flag;
+  const int nchunks = 2 * p.nN + p.nM;
+
+  if (warp == 0) {
+    // ---------------- TMA producer: A chunks, B chunks, C chunks per tile
+    if (lane == 0) {
+      int it = 0;
+      int last_parity[NSTAGE_B];
+      for (int s = 0; s < NSTAGE_B; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
+        const int tok0 = tile * TILE;
+        for (int c = 0; c < nchunks; ++c, ++it) {
+          const int s = it % NSTAGE_B;
+          const uint32_t ph = (it / NSTAGE_B) & 1;
+          if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 11)) { ok = false; break; }
+          uint8_t* st = stages + s * STAGE;
+          mbar_expect_tx(&S.full[s], STAGE);
+          if (c < p.nN) {  // A
+            tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
+            tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
+            tma_load(st + OPND, &tm_at, &S.full[s], c * CH, 0);
+            tma_load(st + OPND + BOX / 2, &tm_at, &S.full[s], c * CH + 64, 0);
+          } else if (c < p.nN + p.nM) {  // B
+            const int o = (c - p.nN) * CH;
+            tma_load(st, &tm_dy, &S.full[s], o, tok0);
+            tma_load(st + BOX, &tm_dy, &S.full[s], o + 64, tok0);
+            tma_load(st + OPND, &tm_bm, &S.full[s], o, 0);
+            tma_load(st + OPND + BOX / 2, &tm_bm, &S.full[s], o + 64, 0);
+          } else {  // C
+            const int f = (c - p.nN - p.nM) * CH;
+            tma_load(st, &tm_x, &S.full[s], f, tok0);
+            tma_load(st + BOX, &tm_x, &S.full[s], f + 64, tok0);
+            tma_load(st + OPND, &tm_anr, &S.full[s], 0, f);
+          }
+          last_parity[s] = (int)ph;
+        }
+      }
+      for (int s = 0; s < NSTAGE_B; ++s)
+        if (last_parity[s] >= 0) drain_bar(&S.full[s], (uint32_t)last_parity[s]);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_r = idesc(128, 64, 0, 0);     // token x rank, K-major
+      const uint32_t id_w = idesc(128, 64, 1, 1);     // weight x rank, MN-major
+      const uint32_t id_x = idesc(128, 128, 0, 0);    // token x feature, K-major
+      const uint32_t zp_addr = su32(zp_tile);
+      const uint32_t dz_addr = su32(dz_tile);
+      int it = 0, wc = 0, xc = 0, tl = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
+        // A: z = x At^T
+        if (!wait_bar(&S.z_empty, (tl & 1) ^ 1, abort_flag, 12)) break;
+        tc_fence_after();
+        for (int c = 0; c < p.nN; ++c, ++it) {
+          const int s = it % NSTAGE_B;
+          if (!wait_bar(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 13)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = su32(stages + s * STAGE);
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma(tmem + B_Z, kdesc(st + b * BOX) + 2 * k, kdesc(st + OPND + b * (BOX / 2)) + 2 * k,
+                  id_r, (c | b | k) != 0);
+          mma_commit(&S.empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&S.z_full);
+        // B: dz' = dy Bm^T, dB^T chunk = dy^T z'
+        if (!wait_bar(&S.dzp_empty, (tl & 1) ^ 1, abort_flag, 14)) break;
+        tc_fence_after();
+        for (int c = 0; c < p.nM; ++c, ++it, ++wc) {
+          const int s = it % NSTAGE_B;
+          if (!wait_bar(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 15)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = su32(stages + s * STAGE);
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma(tmem + B_DZP, kdesc(st + b * BOX) + 2 * k,
+                  kdesc(st + OPND + b * (BOX / 2)) + 2 * k, id_r, (c | b | k) != 0);
+          if (c == 0) {
+            if (!wait_bar(&S.zp_full, tl & 1, abort_flag, 16)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const int wb = wc & 1;
+          if (!wait_bar(&S.w_empty[wb], ((wc >> 1) & 1) ^ 1, abort_flag, 17)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma(tmem + B_W + wb * 64, mndesc(st, BOX) + 128 * k, mndesc(zp_addr, 1024) + 128 * k,
+                id_w, k != 0);
+          mma_commit(&S.w_full[wb]);
+          mma_commit(&S.empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&S.dzp_full);
+        mma_commit(&S.zp_empty);
+        // C: dx = dz Anr^T, dA chunk = x^T dz
+        if (!wait_bar(&S.dz_full, tl & 1, abort_flag, 18)) break;
+        tc_fence_after();
+        for (int c = 0; c < p.nN; ++c, ++it, ++xc, ++wc) {
+          const int s = it % NSTAGE_B;
+          if (!wait_bar(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 19)) { ok = false; break; }
+          const int xb = xc & 1;
+          if (!wait_bar(&S.x_empty[xb], ((xc >> 1) & 1) ^ 1, abort_flag, 20)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = su32(stages + s * STAGE);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma(tmem + B_X + xb * 128, kdesc(dz_addr) + 2 * k, kdesc(st + OPND) + 2 * k, id_x,
+                k != 0);
+          mma_commit(&S.x_full[xb]);
+          const int wb = wc & 1;
+          if (!wait_bar(&S.w_empty[wb], ((wc >> 1) & 1) ^ 1, abort_flag, 21)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma(tmem + B_W + wb * 64, mndesc(st, BOX) + 128 * k, mndesc(dz_addr, 1024) + 128 * k,
+                id_w, k != 0);
+          mma_commit(&S.w_full[wb]);
+          mma_commit(&S.empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&S.dz_empty);
+      }
+      mma_commit(&S.fin);
+      drain_bar(&S.fin, 0);
+    }
+  } else {
+    // ---------------- epilogue
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int row = 32 * q + lane;
+    const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    const int rprime = p.rinfo[0];
+    int wc = 0, xc = 0, tl = 0;
+    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tl) {
+      const int64_t tok = (int64_t)tile * TILE + row;
+      float z[32], v[32];
+      bool ok = true;
+      // E1: z -> z' tile
+      if (!warp_wait(&S.z_full, tl & 1, abort_flag, 22)) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + B_Z + 32 * h, z);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.z_empty);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = z[j] * S.Dc[32 * h + j];
+      if (!warp_wait(&S.zp_empty, (tl & 1) ^ 1, abort_flag, 23)) break;
+      st_tile_half(zp_tile, row, h, v);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.zp_full);
+      // E2: dB^T chunks (row = output index within the chunk)
+      for (int c = 0; c < p.nM; ++c, ++wc) {
+        const int wb = wc & 1;
+        if (!warp_wait(&S.w_full[wb], (wc >> 1) & 1, abort_flag, 24)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + B_W + wb * 64 + 32 * h, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.w_empty[wb]);
+        const int io = c * CH + row;
+        if (io < p.M) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int cc = 32 * h + j;
+            if (cc < rprime) atomicAdd(p.dBc + (int64_t)cc * p.M + io, v[j]);
+          }
+        }
+      }
+      if (!ok) break;
+      // E3: dz' -> dDc, dz tile
+      if (!warp_wait(&S.dzp_full, tl & 1, abort_flag, 25)) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_off + B_DZP + 32 * h, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.dzp_empty);
+      {
+        float pr[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pr[j] = z[j] * v[j];
+        const float colsum = warp_transpose_sum(pr, lane);
+        if (32 * h + lane < rprime) atomicAdd(p.dDc + 32 * h + lane, colsum);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= S.Dc[32 * h + j];
+      if (!warp_wait(&S.dz_empty, (tl & 1) ^ 1, abort_flag, 26)) break;
+      st_tile_half(dz_tile, row, h, v);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.dz_full);
+      // E4: dx chunks (row = token), dA chunks (row = feature within the chunk)
+      for (int c = 0; c < p.nN; ++c, ++xc, ++wc) {
+        const int xb = xc & 1;
+        if (!warp_wait(&S.x_full[xb], (xc >> 1) & 1, abort_flag, 27)) { ok = false; break; }
+        tc_fence_after();
+        __nv_bfloat16* dxrow = p.dx + tok * p.N;
+#pragma unroll
+        for (int piece = 0; piece < 2; ++piece) {
+          tmem_ld32(tmem + lane_off + B_X + xb * 128 + 64 * h + 32 * piece, v);
+          if (tok < p.T) st_row32(dxrow, c * CH + 64 * h + 32 * piece, p.N, v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.x_empty[xb]);
+        const int wb = wc & 1;
+        if (!warp_wait(&S.w_full[wb], (wc >> 1) & 1, abort_flag, 28)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + B_W + wb * 64 + 32 * h, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.w_empty[wb]);
+        const int jf = c * CH + row;
+        if (jf < p.N) {
+          float* dst = p.dAc + (int64_t)jf * RP + 32 * h;
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            if (32 * h + 4 * g < rprime)
+              red_add_v4(dst + 4 * g, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_free(tmem);
+}
+
+// ==========================================================================
+// operand packing (compaction of the middle rank) and gradient unpacking
+// ==========================================================================
+__global__ void tc_pack_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                               const float* __restrict__ Dmid, int rd, int N, int M,
+                               __nv_bfloat16* At, __nv_bfloat16* Anr, __nv_bfloat16* Bm,
+                               __nv_bfloat16* Bt, float* Dc, int* rinfo, float* dAc, float* dBc,
+                               float* dDc, int zero_grads) {
+  __shared__ int kept[RP];
+  __shared__ int rcount;
+  if (threadIdx.x == 0) {
+    int c = 0;
+    for (int a = 0; a < rd; ++a)
+      if (Dmid[a] != 0.f) kept[c++] = a;
+    rcount = c;
+    for (; c < RP; ++c) kept[c] = -1;
+  }
+  __syncthreads();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t i = t0; i < (int64_t)N * RP; i += stride) {
+    const int j = (int)(i / RP), c = (int)(i % RP);
+    const float v = kept[c] >= 0 ? A[(int64_t)j * rd + kept[c]] : 0.f;
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    Anr[i] = b;
+    At[(int64_t)c * N + j] = b;
+    if (zero_grads) dAc[i] = 0.f;
+  }
+  for (int64_t i = t0; i < (int64_t)M * RP; i += stride) {
+    const int o = (int)(i / RP), c = (int)(i % RP);
+    const float v = kept[c] >= 0 ? B[(int64_t)kept[c] * M + o] : 0.f;
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    Bt[i] = b;
+    Bm[(int64_t)c * M + o] = b;
+    if (zero_grads) dBc[i] = 0.f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < RP) {
+    const int c = threadIdx.x;
+    Dc[c] = kept[c] >= 0 ? Dmid[kept[c]] : 0.f;
+    rinfo[1 + c] = kept[c];
+    if (c == 0) rinfo[0] = rcount;
+    if (zero_grads) dDc[c] = 0.f;
+  }
+}
+
+__global__ void tc_unpack_kernel(const float* __restrict__ dAc, const float* __restrict__ dBc,
+                                 const float* __restrict__ dDc, const int* __restrict__ rinfo,
+                                 int rd, int N, int M, float* dA, float* dB, float* dDout,
+                                 int acc) {
+  __shared__ int pos[RP];
+  if (threadIdx.x < RP) pos[threadIdx.x] = -1;
+  __syncthreads();
+  if (threadIdx.x < RP) {
+    const int c = threadIdx.x;
+    if (c < rinfo[0]) pos[rinfo[1 + c]] = c;
+  }
+  __syncthreads();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t i = t0; i < (int64_t)N * rd; i += stride) {
+    const int j = (int)(i / rd), a = (int)(i % rd);
+    dA[i] = pos[a] >= 0 ? dAc[(int64_t)j * RP + pos[a]] : 0.f;
+  }
+  for (int64_t i = t0; i < (int64_t)rd * M; i += stride) {
+    const int a = (int)(i / M), o = (int)(i % M);
+    dB[i] = pos[a] >= 0 ? dBc[(int64_t)pos[a] * M + o] : 0.f;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < rd) {
+    const int a = threadIdx.x;
+    const float v = pos[a] >= 0 ? dDc[pos[a]] : 0.f;
+    if (acc)
+      dDout[a] += v;
+    else
+      dDout[a] = v;
+  }
+}
+
+// ==========================================================================
+// host side
+// ==========================================================================
+struct TcLayout {
+  size_t At, Anr, Bm, Bt, Dc, rinfo, dAc, dBc, dDc, total;
+};
+
+size_t al256(size_t v) { return (v + 255) / 256 * 256; }
+
+TcLayout tc_layout(const LayerPlan& L) {
+  TcLayout t;
+  size_t o = 0;
+  auto take = [&](size_t b) {
+    size_t r = o;
+    o = al256(o + b);
+    return r;
+  };
+  t.At = take((size_t)RP * L.N * 2);
+  t.Anr = take((size_t)L.N * RP * 2);
+  t.Bm = take((size_t)RP * L.M * 2);
+  t.Bt = take((size_t)L.M * RP * 2);
+  t.Dc = take(RP * 4);
+  t.rinfo = take((RP + 1) * 4);
+  t.dAc = take((size_t)L.N * RP * 4);
+  t.dBc = take((size_t)RP * L.M * 4);
+  t.dDc = take(RP * 4);
+  t.total = o;
+  return t;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor (outer x inner, row-major), box (box_outer x box_inner),
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemFwd = NSTAGE_F * STAGE + BOX + sizeof(SmemCommon) + 1024;
+constexpr size_t kSmemBwd = NSTAGE_B * STAGE + 2 * BOX + sizeof(SmemCommon) + 1024;
+static_assert(kSmemFwd <= 227 * 1024, "forward smem");
+static_assert(kSmemBwd <= 227 * 1024, "backward smem");
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+cudaError_t set_smem_attrs() {
+  static cudaError_t err = cudaErrorUnknown;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    err = cudaFuncSetAttribute(tt_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kSmemFwd);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(tt_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBwd);
+  });
+  return err;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+tt_status launch_pack(const LayerPlan& L, const float* A, const float* B, const float* params,
+                      void* ws, size_t off, const TcLayout& t, bool zero_grads, cudaStream_t st) {
+  int blocks = (int)((L.N > L.M ? L.N : L.M) * RP / 256 + 1);
+  if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
+  tc_pack_kernel<<<blocks, 256, 0, st>>>(
+      A, B, params + L.diag_off[L.d - 1], L.rd, (int)L.N, (int)L.M,
+      at<__nv_bfloat16>(ws, off + t.At), at<__nv_bfloat16>(ws, off + t.Anr),
+      at<__nv_bfloat16>(ws, off + t.Bm), at<__nv_bfloat16>(ws, off + t.Bt),
+      at<float>(ws, off + t.Dc), at<int>(ws, off + t.rinfo), at<float>(ws, off + t.dAc),
+      at<float>(ws, off + t.dBc), at<float>(ws, off + t.dDc), zero_grads ? 1 : 0);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+}  // namespace
+
+bool tc_supported(const LayerPlan& L) {
+  return L.rd <= RP && L.N % 8 == 0 && L.M % 8 == 0 && L.N >= CH && L.M >= CH &&
+         L.N <= (1 << 20) && L.M <= (1 << 20);
+}
+
+size_t tc_operand_bytes(const LayerPlan& L) {
+  return tc_supported(L) ? tc_layout(L).total : 256;
+}
+
+tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, const float* params,
+                     const float* A, const float* B, void* y, void* ws, size_t off,
+                     cudaStream_t st) {
+  if (T <= 0) return TT_OK;
+  if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
+  const TcLayout t = tc_layout(L);
+  tt_status s = launch_pack(L, A, B, params, ws, off, t, false, st);
+  if (s != TT_OK) return s;
+  if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
+  CUtensorMap mx, mat, mbt;
+  if (!make_map(&mx, x, L.N, T, 64, TILE) ||
+      !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
+      !make_map(&mbt, at<void>(ws, off + t.Bt), RP, L.M, 64, CH))
+    return TT_ERR_CUDA;
+  FwdArgs a;
+  a.T = T;
+  a.N = (int)L.N;
+  a.M = (int)L.M;
+  a.nN = (int)((L.N + CH - 1) / CH);
+  a.nM = (int)((L.M + CH - 1) / CH);
+  a.ntiles = (int)((T + TILE - 1) / TILE);
+  a.Dc = at<float>(ws, off + t.Dc);
+  a.y = static_cast<__nv_bfloat16*>(y);
+  int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+  tt_fwd_kernel<<<grid, NTHREADS, kSmemFwd, st>>>(mx, mat, mbt, a);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
+
+tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy,
+                      const float* params, const float* A, const float* B, void* dx,
+                      float* dDmid, bool acc, float* dA, float* dB, void* ws, size_t off,
+                      cudaStream_t st) {
+  if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
+  const TcLayout t = tc_layout(L);
+  tt_status s = launch_pack(L, A, B, params, ws, off, t, true, st);
+  if (s != TT_OK) return s;
+  if (T > 0) {
+    if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
+    CUtensorMap mx, mdy, mat, mbm, manr;
+    if (!make_map(&mx, x, L.N, T, 64, TILE) || !make_map(&mdy, dy, L.M, T, 64, TILE) ||
+        !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
+        !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
+        !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH))
+      return TT_ERR_CUDA;
+    BwdArgs a;
+    a.T = T;
+    a.N = (int)L.N;
+    a.M = (int)L.M;
+    a.nN = (int)((L.N + CH - 1) / CH);
+    a.nM = (int)((L.M + CH - 1) / CH);
+    a.ntiles = (int)((T + TILE - 1) / TILE);
+    a.Dc = at<float>(ws, off + t.Dc);
+    a.rinfo = at<int>(ws, off + t.rinfo);
+    a.dx = static_cast<__nv_bfloat16*>(dx);
+    a.dAc = at<float>(ws, off + t.dAc);
+    a.dBc = at<float>(ws, off + t.dBc);
+    a.dDc = at<float>(ws, off + t.dDc);
+    int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+    tt_bwd_kernel<<<grid, NTHREADS, kSmemBwd, st>>>(mx, mdy, mat, mbm, manr, a);
+    count_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
+  }
+  int blocks = (int)((L.N > L.M ? L.N : L.M) * L.rd / 256 + 1);
+  if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
+  tc_unpack_kernel<<<blocks, 256, 0, st>>>(at<float>(ws, off + t.dAc), at<float>(ws, off + t.dBc),
+                                           at<float>(ws, off + t.dDc), at<int>(ws, off + t.rinfo),
+                                           L.rd, (int)L.N, (int)L.M, dA, dB, dDmid, acc ? 1 : 0);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 }  // namespace ttc

@@ -537,17 +537,11 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
                         ws, f.up, st);
 }
 
-tt_status tt_get_device_status(const void* ws, void* stream) {
-  if (!ws) return TT_ERR_INVALID_ARG;
+tt_status tt_get_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  DeviceStatus h{0, 0};
   if (cudaStreamSynchronize(st) != cudaSuccess) return TT_ERR_CUDA;
-  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return TT_ERR_CUDA;
-  if (h.code != 0) {
-    DeviceStatus z{0, 0};
-    if (cudaMemcpy(const_cast<void*>(ws), &z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess)
-      return TT_ERR_CUDA;
-  }
+  DeviceStatus h{0, 0};
+  if (read_and_clear_device_status(&h) != cudaSuccess) return TT_ERR_CUDA;
   if (h.code == TT_ERR_TIMEOUT) return TT_ERR_TIMEOUT;
   if (h.code != 0) return TT_ERR_DEVICE;
   return TT_OK;

@@ -39,11 +39,13 @@ struct tt_plan_s {
 
 namespace ttc {
 
-// ---- device status word (first 256 bytes of every workspace) -------------
+// ---- device status word (one per GPU, module-scope device variable) -------
 struct DeviceStatus {
   unsigned code;    // 0 = ok, else a tt_status value
   unsigned detail;  // where it happened (kernel-specific)
 };
+// Copies the current device's status word to *out and zeroes it.
+cudaError_t read_and_clear_device_status(DeviceStatus* out);
 
 // ---- measurement hooks (profile.cu) ---------------------------------------
 enum Phase { kPhMerge = 0, kPhFwd = 1, kPhBwd = 2, kPhMergeBwd = 3, kPhElem = 4 };

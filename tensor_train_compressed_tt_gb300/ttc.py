@@ -76,8 +76,8 @@ def lib() -> ctypes.CDLL:
             "tt_forward": [_P, _I64, _P, _P, _P, _P, _SZ, _P],
             "tt_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_forward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
-            "tt_ffn_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
-            "tt_get_device_status": [_P, _P],
+            "tt_ffn_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+            "tt_get_device_status": [_P],
             "tt_status_string": [ctypes.c_int],
         }
         for name, args in sigs.items():
@@ -205,8 +205,8 @@ def tt_ffn_backward(plan: Plan, T: int, x: int, dy: int, params_up: int, params_
                                  int(ws_bytes), stream)
 
 
-def tt_get_device_status(ws: int, stream: int = 0) -> int:
-    return lib().tt_get_device_status(ws, stream)
+def tt_get_device_status(stream: int = 0) -> int:
+    return lib().tt_get_device_status(stream)
 
 
 def tt_status_string(code: int) -> str:
