@@ -1,0 +1,310 @@
+// Merge engine: device side and launcher.  Included once, by tc_fused.cu, so
+// that the engine shares the device status word and the operand packing code
+// with the tensor-core kernels (one device translation unit).
+#pragma once
+
+#include <atomic>
+
+#include "merge_engine.h"
+
+namespace ttc {
+namespace {
+
+constexpr int kEngThreads = 256;
+constexpr int kET = 32;   // GEMM tile (kET x kET outputs per unit)
+constexpr int kEK = 32;   // K slice staged per iteration
+constexpr int kBarSlots = 64;
+static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
+
+__device__ unsigned g_eng_bar[kBarSlots][32];  // [0] count, [1] generation (own 128-byte line)
+
+// Grid-wide barrier, bounded: false if it timed out (error recorded).  Data
+// produced in one phase and read in a later one is read with L2-only loads
+// (__ldcg), so no stale L1 line can be observed across a barrier.
+__device__ bool eng_grid_barrier(unsigned slot, unsigned nblocks, int* failed) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned* count = &g_eng_bar[slot][0];
+    volatile unsigned* gen = &g_eng_bar[slot][1];
+    const unsigned g0 = *gen;
+    __threadfence();
+    if (atomicAdd(count, 1u) == nblocks - 1) {
+      atomicExch(count, 0u);
+      __threadfence();
+      atomicAdd(const_cast<unsigned*>(gen), 1u);
+    } else {
+      const uint64_t t0 = gtimer();
+      while (*gen == g0) {
+        if (gtimer() - t0 > kTimeoutNs) {
+          record_error(TT_ERR_TIMEOUT, 100);
+          *failed = 1;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return *failed == 0;
+}
+
+// One kET x kET output tile of C over one K slice.
+__device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
+                              float (*Bs)[kET + 1]) {
+  const GemmArgs& g = t.g;
+  const int S = t.splits;
+  const int tiles_n = (int)((g.n + kET - 1) / kET);
+  const int ks = u % S;
+  const int tile = u / S;
+  const int64_t m0 = (int64_t)(tile / tiles_n) * kET, n0 = (int64_t)(tile % tiles_n) * kET;
+  int64_t chunk = (g.k + S - 1) / S;
+  chunk = (chunk + kEK - 1) / kEK * kEK;
+  const int64_t kb = (int64_t)ks * chunk;
+  const int64_t ke = kb + chunk < g.k ? kb + chunk : g.k;
+  const float* A = static_cast<const float*>(g.A);
+  const float* B = static_cast<const float*>(g.B);
+  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+  float acc[2][2] = {};
+  for (int64_t k0 = kb; k0 < ke; k0 += kEK) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = tid + e * kEngThreads;  // 0..1023
+      const int a_m = idx % kET, a_k = idx / kET;
+      const int64_t gm = m0 + a_m, gk = k0 + a_k;
+      float v = 0.f;
+      if (gm < g.m && gk < ke) {
+        v = __ldcg(A + gm * g.sam + gk * g.sak);
+        if (g.kscale) v *= g.kscale[gk % g.klen];
+      }
+      As[a_k][a_m] = v;
+      const int b_n = idx % kET, b_k = idx / kET;
+      const int64_t gn = n0 + b_n, gk2 = k0 + b_k;
+      Bs[b_k][b_n] = (gn < g.n && gk2 < ke) ? __ldcg(B + gk2 * g.sbk + gn * g.sbn) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < kEK; ++kk) {
+      const float a0 = As[kk][ty * 2], a1 = As[kk][ty * 2 + 1];
+      const float b0 = Bs[kk][tx * 2], b1 = Bs[kk][tx * 2 + 1];
+      acc[0][0] = fmaf(a0, b0, acc[0][0]);
+      acc[0][1] = fmaf(a0, b1, acc[0][1]);
+      acc[1][0] = fmaf(a1, b0, acc[1][0]);
+      acc[1][1] = fmaf(a1, b1, acc[1][1]);
+    }
+    __syncthreads();
+  }
+  float* C = static_cast<float*>(g.C);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int64_t gm = m0 + ty * 2 + i;
+    if (gm >= g.m) continue;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int64_t gn = n0 + tx * 2 + j;
+      if (gn >= g.n) continue;
+      if (S > 1) {
+        t.partial[((int64_t)ks * g.m + gm) * g.n + gn] = acc[i][j];
+        continue;
+      }
+      float v = acc[i][j];
+      if (g.rscale) v *= g.rscale[gm];
+      if (g.cscale) v *= g.cscale[gn % g.clen];
+      const int64_t ci = gm * g.scm + gn * g.scn;
+      C[ci] = g.mode == kAccumulate ? __ldcg(C + ci) + v : v;
+    }
+  }
+}
+
+__device__ void eng_gemm_final_unit(const EngTask& t, int u) {
+  const GemmArgs& g = t.g;
+  const int64_t i = (int64_t)u * kEngThreads + threadIdx.x;
+  if (i >= g.m * g.n) return;
+  const int64_t gm = i / g.n, gn = i % g.n;
+  float v = 0.f;
+  for (int ks = 0; ks < t.splits; ++ks) v += __ldcg(t.partial + (int64_t)ks * g.m * g.n + i);
+  if (g.rscale) v *= g.rscale[gm];
+  if (g.cscale) v *= g.cscale[gn % g.clen];
+  float* C = static_cast<float*>(g.C);
+  const int64_t ci = gm * g.scm + gn * g.scn;
+  C[ci] = g.mode == kAccumulate ? __ldcg(C + ci) + v : v;
+}
+
+__device__ void eng_coldot_unit(const EngTask& t, int c, float* red) {
+  float s = 0.f;
+  for (int64_t u = threadIdx.x; u < t.n; u += blockDim.x)
+    s += __ldcg(t.x + u * t.sx + c) * __ldcg(t.y + u * t.sy + c);
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    s = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (threadIdx.x == 0) {
+      const bool keep = !t.s || t.s[c] != 0.f;
+      if (t.acc) {
+        if (keep) t.out[c] += s;
+      } else {
+        t.out[c] = keep ? s : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+__device__ void eng_scale_unit(const EngTask& t, int u) {
+  const int64_t base = (int64_t)u * 1024;
+  for (int e = threadIdx.x; e < 1024; e += blockDim.x) {
+    const int64_t i = base + e;
+    if (i >= t.n) break;
+    float v = __ldcg(t.x + i);
+    if (t.s) v *= t.s[i % t.len];
+    t.out[i] = t.acc ? __ldcg(t.out + i) + v : v;
+  }
+}
+
+__global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant__ EngProgram p) {
+  __shared__ float As[kEK][kET + 1];
+  __shared__ float Bs[kEK][kET + 1];
+  __shared__ float red[32];
+  __shared__ int failed;
+  if (threadIdx.x == 0) {
+    failed = 0;
+    TL_STAMP(2, 0);
+  }
+  __syncthreads();
+  for (int ph = 0; ph < p.nphases; ++ph) {
+    const int t0 = p.phase_begin[ph], t1 = p.phase_begin[ph + 1];
+    int total = 0;
+    for (int t = t0; t < t1; ++t) total += p.t[t].units;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+      int t = t0, uu = u;
+      while (uu >= p.t[t].units) uu -= p.t[t++].units;
+      const EngTask& k = p.t[t];
+      switch (k.kind) {
+        case kEGemm: eng_gemm_unit(k, uu, As, Bs); break;
+        case kEGemmFinal: eng_gemm_final_unit(k, uu); break;
+        case kEColdot: eng_coldot_unit(k, uu, red); break;
+        case kEScale: eng_scale_unit(k, uu); break;
+        case kEPack:
+          tc_pack_unit(k.A, k.B, k.s, k.rd, k.N, k.M, k.tc, k.zero, uu);
+          break;
+        case kEUnpack:
+          tc_unpack_unit(k.tc, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
+          break;
+        default: break;
+      }
+    }
+    if (threadIdx.x == 0) TL_STAMP(2, 1 + 2 * ph);
+    if (ph + 1 < p.nphases && !eng_grid_barrier(p.slot, gridDim.x, &failed)) return;
+    if (threadIdx.x == 0) TL_STAMP(2, 2 + 2 * ph);
+  }
+}
+
+}  // namespace
+
+// ---- host side -------------------------------------------------------------
+
+void EngBuilder::begin_phase() {
+  if (p.nphases >= kEngMaxPhases) {
+    overflow = true;
+    return;
+  }
+  p.phase_begin[p.nphases++] = p.ntasks;
+}
+
+EngTask* EngBuilder::add() {
+  static EngTask dummy;
+  if (p.ntasks >= kEngMaxTasks || p.nphases == 0) {
+    overflow = true;
+    return &dummy;
+  }
+  p.t[p.ntasks] = EngTask();
+  return &p.t[p.ntasks++];
+}
+
+void EngBuilder::end() { p.phase_begin[p.nphases] = p.ntasks; }
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t eng_partial_floats(int64_t m, int64_t n, int64_t k) {
+  (void)k;
+  return (size_t)(m * n) * 16;  // at most 16 K-splits
+}
+
+void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap) {
+  t->kind = kEGemm;
+  t->g = g;
+  const int64_t tiles = ceil_div(g.m, kET) * ceil_div(g.n, kET);
+  int64_t splits = 1;
+  // split long reductions so that a phase has a few units per SM and each
+  // unit still walks at least a few K slices
+  if (partial_ws && tiles < 256) {
+    const int64_t want = ceil_div(256, tiles);
+    const int64_t maxs = ceil_div(g.k, 4 * kEK);
+    splits = want < maxs ? want : maxs;
+    if (splits > 16) splits = 16;
+    if ((size_t)(splits * g.m * g.n) > partial_cap) splits = 1;
+    if (splits < 1) splits = 1;
+  }
+  t->splits = (int)splits;
+  t->partial = splits > 1 ? partial_ws : nullptr;
+  t->units = (int)(tiles * splits);
+}
+
+void eng_pack_task(EngTask* t, const LayerPlan& L, const float* A, const float* B,
+                   const float* Dmid, const TcPtrs& tc, bool zero_grads) {
+  t->kind = kEPack;
+  t->A = A;
+  t->B = B;
+  t->s = Dmid;
+  t->rd = L.rd;
+  t->N = (int)L.N;
+  t->M = (int)L.M;
+  t->tc = tc;
+  t->zero = zero_grads ? 1 : 0;
+  t->units = (int)ceil_div((L.N + L.M) * RP + RP, kPackPer);
+}
+
+void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, float* dA, float* dB,
+                     float* dDout, bool acc) {
+  t->kind = kEUnpack;
+  t->tc = tc;
+  t->rd = L.rd;
+  t->N = (int)L.N;
+  t->M = (int)L.M;
+  t->dA = dA;
+  t->dB = dB;
+  t->out = dDout;
+  t->acc = acc ? 1 : 0;
+  t->units = (int)ceil_div((L.N + L.M) * L.rd + L.rd, kPackPer);
+}
+
+void eng_gemm_final_task(EngTask* t, const EngTask& gemm) {
+  t->kind = kEGemmFinal;
+  t->g = gemm.g;
+  t->splits = gemm.splits;
+  t->partial = gemm.partial;
+  t->units = (int)ceil_div(gemm.g.m * gemm.g.n, kEngThreads);
+}
+
+cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
+  static std::atomic<unsigned> next_slot{0};
+  static int grid = 0;
+  if (!grid) {
+    int dev = 0, sms = 0, per = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, eng_kernel, kEngThreads, 0);
+    grid = sms * (per > 0 ? 1 : 0);
+    if (grid <= 0) return cudaErrorLaunchFailure;
+  }
+  EngProgram p = prog;
+  p.slot = next_slot.fetch_add(1) % kBarSlots;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(eng_kernel),
+                                              dim3(grid), dim3(kEngThreads), args, 0, st);
+  count_launches(1);
+  return e;
+}
+
+}  // namespace ttc

@@ -1,0 +1,77 @@
+// One-launch execution of the T-independent merge work (chain merges, their
+// reverse, operand packing, gradient unpacking): a persistent cooperative
+// kernel walks a short list of phases; the tasks of one phase are spread
+// over all CTAs and a bounded grid barrier separates phases.
+#pragma once
+
+#include "tc_fused.h"
+#include "ttc_internal.h"
+
+namespace ttc {
+
+enum EngKind {
+  kEGemm = 0,      // C (op)= ... (GemmArgs); split-K partials when splits > 1
+  kEGemmFinal = 1, // sum split-K partials, apply scales, store/accumulate into C
+  kEColdot = 2,    // out[c] (=|+=) sum_u X[u,c] Y[u,c] (masked by D == 0)
+  kEScale = 3,     // out[i] (=|+=) in[i] * scale[i % len]
+  kEPack = 4,      // tensor-core operands from A, B, D_d (+ zero gradient sums)
+  kEUnpack = 5     // compacted gradient sums -> dA, dB, dD_d
+};
+
+struct EngTask {
+  int kind = 0;
+  int units = 0;
+  int splits = 1;       // kEGemm / kEGemmFinal
+  int pad = 0;
+  GemmArgs g;           // kEGemm / kEGemmFinal
+  float* partial = nullptr;  // split-K partials [splits][m][n]
+  // kEColdot / kEScale / pack / unpack operands
+  const float* x = nullptr;
+  const float* y = nullptr;
+  const float* s = nullptr;
+  float* out = nullptr;
+  int64_t n = 0, sx = 0, sy = 0;
+  int len = 1, acc = 0;
+  // pack / unpack (s = middle diagonal D_d, out = dD_d for unpack)
+  const float* A = nullptr;
+  const float* B = nullptr;
+  TcPtrs tc;
+  float* dA = nullptr;
+  float* dB = nullptr;
+  int rd = 0, N = 0, M = 0, zero = 0;
+};
+
+constexpr int kEngMaxTasks = 24;
+constexpr int kEngMaxPhases = 8;
+
+struct EngProgram {
+  int ntasks = 0, nphases = 0;
+  unsigned slot = 0;  // grid-barrier slot (set by eng_launch)
+  int phase_begin[kEngMaxPhases + 1] = {};
+  EngTask t[kEngMaxTasks];
+};
+
+// Builders used by the host code (ttc_api.cu).
+struct EngBuilder {
+  EngProgram p;
+  bool overflow = false;
+  void begin_phase();
+  EngTask* add();
+  void end();  // closes the last phase
+};
+
+// Units for a GEMM task of the engine's tile size and a split-K count.
+void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap);
+void eng_gemm_final_task(EngTask* t, const EngTask& gemm);
+void eng_pack_task(EngTask* t, const LayerPlan& L, const float* A, const float* B,
+                   const float* Dmid, const TcPtrs& tc, bool zero_grads);
+void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, float* dA, float* dB,
+                     float* dDout, bool acc);
+
+// Launch (cooperative, one CTA per SM).  Returns cudaSuccess or the error.
+cudaError_t eng_launch(const EngProgram& p, cudaStream_t st);
+
+// Bytes of split-K partial scratch a GEMM of this shape may use.
+size_t eng_partial_floats(int64_t m, int64_t n, int64_t k);
+
+}  // namespace ttc

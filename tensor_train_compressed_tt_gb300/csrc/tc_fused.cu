@@ -100,6 +100,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 
+// Optional per-CTA timeline (global-timer stamps), compiled in only with
+// -DTTC_TIMELINE for performance investigation; the default build has none.
+#ifdef TTC_TIMELINE
+__device__ unsigned long long g_tl[3][256][16];
+#define TL_STAMP(k, slot) (g_tl[(k)][blockIdx.x & 255][(slot)] = gtimer())
+#else
+#define TL_STAMP(k, slot) ((void)0)
+#endif
+
 __device__ void record_error(unsigned code, unsigned where) {
   if (atomicCAS(&g_status.code, 0u, code) == 0u) atomicExch(&g_status.detail, where);
 }
@@ -322,6 +331,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* zp_tile = base + NSTAGE_F * STAGE;
   SmemCommon& S = *reinterpret_cast<SmemCommon*>(zp_tile + BOX);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) TL_STAMP(0, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE_F; ++s) {
@@ -346,6 +356,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  if (threadIdx.x == 0) TL_STAMP(0, 1);
   volatile int* abort_flag = &S.abort_flag;
 
   if (warp == 0) {
@@ -404,6 +415,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!ok) break;
         mma_commit(&S.z_full);
+        TL_STAMP(0, 2);
         if (!wait_bar(&S.zp_full, tl & 1, abort_flag, 4)) break;
         tc_fence_after();
         for (int c = 0; c < p.nM; ++c, ++it, ++yc) {
@@ -422,6 +434,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!ok) break;
         mma_commit(&S.zp_empty);
+        TL_STAMP(0, 4);
       }
       mma_commit(&S.fin);
       drain_bar(&S.fin, 0);
@@ -449,6 +462,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.zp_full);
+      if (warp == 2 && lane == 0) TL_STAMP(0, 3);
       bool ok = true;
       for (int c = 0; c < p.nM; ++c, ++yc) {
         const int yb = yc & 1;
@@ -465,12 +479,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(&S.x_empty[yb]);
       }
       if (!ok) break;
+      if (warp == 2 && lane == 0) TL_STAMP(0, 5);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) TL_STAMP(0, 6);
   if (warp == 1) tmem_free(tmem);
 }
 
@@ -494,6 +510,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* dz_tile = zp_tile + BOX;
   SmemCommon& S = *reinterpret_cast<SmemCommon*>(dz_tile + BOX);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) TL_STAMP(1, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE_B; ++s) {
@@ -524,6 +541,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  if (threadIdx.x == 0) TL_STAMP(1, 1);
   volatile int* abort_flag = &S.abort_flag;
   const int nchunks = 2 * p.nN + p.nM;
 
@@ -594,6 +612,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!ok) break;
         mma_commit(&S.z_full);
+        TL_STAMP(1, 2);
         // B: dz' = dy Bm^T, dB^T chunk = dy^T z'
         if (!wait_bar(&S.dzp_empty, (tl & 1) ^ 1, abort_flag, 14)) break;
         tc_fence_after();
@@ -624,6 +643,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!ok) break;
         mma_commit(&S.dzp_full);
+        TL_STAMP(1, 4);
         mma_commit(&S.zp_empty);
         // C: dx = dz Anr^T, dA chunk = x^T dz
         if (!wait_bar(&S.dz_full, tl & 1, abort_flag, 18)) break;
@@ -682,6 +702,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.zp_full);
+      if (warp == 2 && lane == 0) TL_STAMP(1, 3);
       // E2: dB^T chunks (row = output index within the chunk)
       for (int c = 0; c < p.nM; ++c, ++wc) {
         const int wb = wc & 1;
@@ -722,6 +743,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dz_full);
+      if (warp == 2 && lane == 0) TL_STAMP(1, 5);
       // E4: dx chunks (row = token), dA chunks (row = feature within the chunk)
       for (int c = 0; c < p.nN; ++c, ++xc, ++wc) {
         const int xb = xc & 1;
@@ -753,25 +775,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (!ok) break;
+      if (warp == 2 && lane == 0) TL_STAMP(1, 6);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) TL_STAMP(1, 7);
   if (warp == 1) tmem_free(tmem);
 }
 
 // ==========================================================================
-// operand packing (compaction of the middle rank) and gradient unpacking
+// operand packing (compaction of the middle rank) and gradient unpacking,
+// run as units of the merge engine
 // ==========================================================================
-__global__ void tc_pack_kernel(const float* __restrict__ A, const float* __restrict__ B,
-                               const float* __restrict__ Dmid, int rd, int N, int M,
-                               __nv_bfloat16* At, __nv_bfloat16* Anr, __nv_bfloat16* Bm,
-                               __nv_bfloat16* Bt, float* Dc, int* rinfo, float* dAc, float* dBc,
-                               float* dDc, int zero_grads) {
+constexpr int kPackPer = 1024;  // elements per engine unit
+
+__device__ void tc_pack_unit(const float* __restrict__ A, const float* __restrict__ B,
+                             const float* __restrict__ Dmid, int rd, int N, int M,
+                             const TcPtrs& p, int zero_grads, int unit) {
   __shared__ int kept[RP];
   __shared__ int rcount;
+  __syncthreads();
   if (threadIdx.x == 0) {
     int c = 0;
     for (int a = 0; a < rd; ++a)
@@ -780,62 +806,61 @@ __global__ void tc_pack_kernel(const float* __restrict__ A, const float* __restr
     for (; c < RP; ++c) kept[c] = -1;
   }
   __syncthreads();
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int64_t i = t0; i < (int64_t)N * RP; i += stride) {
-    const int j = (int)(i / RP), c = (int)(i % RP);
-    const float v = kept[c] >= 0 ? A[(int64_t)j * rd + kept[c]] : 0.f;
-    const __nv_bfloat16 b = __float2bfloat16_rn(v);
-    Anr[i] = b;
-    At[(int64_t)c * N + j] = b;
-    if (zero_grads) dAc[i] = 0.f;
-  }
-  for (int64_t i = t0; i < (int64_t)M * RP; i += stride) {
-    const int o = (int)(i / RP), c = (int)(i % RP);
-    const float v = kept[c] >= 0 ? B[(int64_t)kept[c] * M + o] : 0.f;
-    const __nv_bfloat16 b = __float2bfloat16_rn(v);
-    Bt[i] = b;
-    Bm[(int64_t)c * M + o] = b;
-    if (zero_grads) dBc[i] = 0.f;
-  }
-  if (blockIdx.x == 0 && threadIdx.x < RP) {
-    const int c = threadIdx.x;
-    Dc[c] = kept[c] >= 0 ? Dmid[kept[c]] : 0.f;
-    rinfo[1 + c] = kept[c];
-    if (c == 0) rinfo[0] = rcount;
-    if (zero_grads) dDc[c] = 0.f;
+  const int64_t nA = (int64_t)N * RP, nB = (int64_t)M * RP;
+  __nv_bfloat16* At = static_cast<__nv_bfloat16*>(p.At);
+  __nv_bfloat16* Anr = static_cast<__nv_bfloat16*>(p.Anr);
+  __nv_bfloat16* Bm = static_cast<__nv_bfloat16*>(p.Bm);
+  __nv_bfloat16* Bt = static_cast<__nv_bfloat16*>(p.Bt);
+  for (int e = threadIdx.x; e < kPackPer; e += blockDim.x) {
+    const int64_t i = (int64_t)unit * kPackPer + e;
+    if (i < nA) {
+      const int j = (int)(i / RP), c = (int)(i % RP);
+      const float v = kept[c] >= 0 ? __ldcg(A + (int64_t)j * rd + kept[c]) : 0.f;
+      const __nv_bfloat16 b = __float2bfloat16_rn(v);
+      Anr[i] = b;
+      At[(int64_t)c * N + j] = b;
+      if (zero_grads) p.dAc[i] = 0.f;
+    } else if (i < nA + nB) {
+      const int64_t k = i - nA;
+      const int o = (int)(k / RP), c = (int)(k % RP);
+      const float v = kept[c] >= 0 ? __ldcg(B + (int64_t)kept[c] * M + o) : 0.f;
+      const __nv_bfloat16 b = __float2bfloat16_rn(v);
+      Bt[k] = b;
+      Bm[(int64_t)c * M + o] = b;
+      if (zero_grads) p.dBc[k] = 0.f;
+    } else if (i < nA + nB + RP) {
+      const int c = (int)(i - nA - nB);
+      p.Dc[c] = kept[c] >= 0 ? Dmid[kept[c]] : 0.f;
+      p.rinfo[1 + c] = kept[c];
+      if (c == 0) p.rinfo[0] = rcount;
+      if (zero_grads) p.dDc[c] = 0.f;
+    }
   }
 }
 
-__global__ void tc_unpack_kernel(const float* __restrict__ dAc, const float* __restrict__ dBc,
-                                 const float* __restrict__ dDc, const int* __restrict__ rinfo,
-                                 int rd, int N, int M, float* dA, float* dB, float* dDout,
-                                 int acc) {
+__device__ void tc_unpack_unit(const TcPtrs& p, int rd, int N, int M, float* dA, float* dB,
+                               float* dDout, int acc, int unit) {
   __shared__ int pos[RP];
+  __syncthreads();
   if (threadIdx.x < RP) pos[threadIdx.x] = -1;
   __syncthreads();
-  if (threadIdx.x < RP) {
-    const int c = threadIdx.x;
-    if (c < rinfo[0]) pos[rinfo[1 + c]] = c;
-  }
+  if (threadIdx.x < RP && threadIdx.x < p.rinfo[0]) pos[p.rinfo[1 + threadIdx.x]] = threadIdx.x;
   __syncthreads();
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int64_t i = t0; i < (int64_t)N * rd; i += stride) {
-    const int j = (int)(i / rd), a = (int)(i % rd);
-    dA[i] = pos[a] >= 0 ? dAc[(int64_t)j * RP + pos[a]] : 0.f;
-  }
-  for (int64_t i = t0; i < (int64_t)rd * M; i += stride) {
-    const int a = (int)(i / M), o = (int)(i % M);
-    dB[i] = pos[a] >= 0 ? dBc[(int64_t)pos[a] * M + o] : 0.f;
-  }
-  if (blockIdx.x == 0 && threadIdx.x < rd) {
-    const int a = threadIdx.x;
-    const float v = pos[a] >= 0 ? dDc[pos[a]] : 0.f;
-    if (acc)
-      dDout[a] += v;
-    else
-      dDout[a] = v;
+  const int64_t nA = (int64_t)N * rd, nB = (int64_t)rd * M;
+  for (int e = threadIdx.x; e < kPackPer; e += blockDim.x) {
+    const int64_t i = (int64_t)unit * kPackPer + e;
+    if (i < nA) {
+      const int j = (int)(i / rd), a = (int)(i % rd);
+      dA[i] = pos[a] >= 0 ? p.dAc[(int64_t)j * RP + pos[a]] : 0.f;
+    } else if (i < nA + nB) {
+      const int64_t k = i - nA;
+      const int a = (int)(k / M), o = (int)(k % M);
+      dB[k] = pos[a] >= 0 ? p.dBc[(int64_t)pos[a] * M + o] : 0.f;
+    } else if (i < nA + nB + rd) {
+      const int a = (int)(i - nA - nB);
+      const float v = pos[a] >= 0 ? p.dDc[pos[a]] : 0.f;
+      dDout[a] = acc ? dDout[a] + v : v;
+    }
   }
 }
 
@@ -933,20 +958,6 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
-tt_status launch_pack(const LayerPlan& L, const float* A, const float* B, const float* params,
-                      void* ws, size_t off, const TcLayout& t, bool zero_grads, cudaStream_t st) {
-  int blocks = (int)((L.N > L.M ? L.N : L.M) * RP / 256 + 1);
-  if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
-  tc_pack_kernel<<<blocks, 256, 0, st>>>(
-      A, B, params + L.diag_off[L.d - 1], L.rd, (int)L.N, (int)L.M,
-      at<__nv_bfloat16>(ws, off + t.At), at<__nv_bfloat16>(ws, off + t.Anr),
-      at<__nv_bfloat16>(ws, off + t.Bm), at<__nv_bfloat16>(ws, off + t.Bt),
-      at<float>(ws, off + t.Dc), at<int>(ws, off + t.rinfo), at<float>(ws, off + t.dAc),
-      at<float>(ws, off + t.dBc), at<float>(ws, off + t.dDc), zero_grads ? 1 : 0);
-  count_launches(1);
-  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
-}
-
 }  // namespace
 
 bool tc_supported(const LayerPlan& L) {
@@ -958,14 +969,26 @@ size_t tc_operand_bytes(const LayerPlan& L) {
   return tc_supported(L) ? tc_layout(L).total : 256;
 }
 
-tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, const float* params,
-                     const float* A, const float* B, void* y, void* ws, size_t off,
+TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t off) {
+  const TcLayout t = tc_layout(L);
+  TcPtrs p;
+  p.At = at<void>(ws, off + t.At);
+  p.Anr = at<void>(ws, off + t.Anr);
+  p.Bm = at<void>(ws, off + t.Bm);
+  p.Bt = at<void>(ws, off + t.Bt);
+  p.Dc = at<float>(ws, off + t.Dc);
+  p.rinfo = at<int>(ws, off + t.rinfo);
+  p.dAc = at<float>(ws, off + t.dAc);
+  p.dBc = at<float>(ws, off + t.dBc);
+  p.dDc = at<float>(ws, off + t.dDc);
+  return p;
+}
+
+tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws, size_t off,
                      cudaStream_t st) {
   if (T <= 0) return TT_OK;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
-  tt_status s = launch_pack(L, A, B, params, ws, off, t, false, st);
-  if (s != TT_OK) return s;
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
   CUtensorMap mx, mat, mbt;
   if (!make_map(&mx, x, L.N, T, 64, TILE) ||
@@ -987,47 +1010,43 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, const float* 
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
-tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy,
-                      const float* params, const float* A, const float* B, void* dx,
-                      float* dDmid, bool acc, float* dA, float* dB, void* ws, size_t off,
-                      cudaStream_t st) {
+tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
+                      void* ws, size_t off, cudaStream_t st) {
+  if (T <= 0) return TT_OK;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
-  tt_status s = launch_pack(L, A, B, params, ws, off, t, true, st);
-  if (s != TT_OK) return s;
-  if (T > 0) {
-    if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-    CUtensorMap mx, mdy, mat, mbm, manr;
-    if (!make_map(&mx, x, L.N, T, 64, TILE) || !make_map(&mdy, dy, L.M, T, 64, TILE) ||
-        !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
-        !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
-        !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH))
-      return TT_ERR_CUDA;
-    BwdArgs a;
-    a.T = T;
-    a.N = (int)L.N;
-    a.M = (int)L.M;
-    a.nN = (int)((L.N + CH - 1) / CH);
-    a.nM = (int)((L.M + CH - 1) / CH);
-    a.ntiles = (int)((T + TILE - 1) / TILE);
-    a.Dc = at<float>(ws, off + t.Dc);
-    a.rinfo = at<int>(ws, off + t.rinfo);
-    a.dx = static_cast<__nv_bfloat16*>(dx);
-    a.dAc = at<float>(ws, off + t.dAc);
-    a.dBc = at<float>(ws, off + t.dBc);
-    a.dDc = at<float>(ws, off + t.dDc);
-    int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
-    tt_bwd_kernel<<<grid, NTHREADS, kSmemBwd, st>>>(mx, mdy, mat, mbm, manr, a);
-    count_launches(1);
-    if (cudaGetLastError() != cudaSuccess) return TT_ERR_CUDA;
-  }
-  int blocks = (int)((L.N > L.M ? L.N : L.M) * L.rd / 256 + 1);
-  if (blocks > 2 * num_sms()) blocks = 2 * num_sms();
-  tc_unpack_kernel<<<blocks, 256, 0, st>>>(at<float>(ws, off + t.dAc), at<float>(ws, off + t.dBc),
-                                           at<float>(ws, off + t.dDc), at<int>(ws, off + t.rinfo),
-                                           L.rd, (int)L.N, (int)L.M, dA, dB, dDmid, acc ? 1 : 0);
+  if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
+  CUtensorMap mx, mdy, mat, mbm, manr;
+  if (!make_map(&mx, x, L.N, T, 64, TILE) || !make_map(&mdy, dy, L.M, T, 64, TILE) ||
+      !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
+      !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
+      !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH))
+    return TT_ERR_CUDA;
+  BwdArgs a;
+  a.T = T;
+  a.N = (int)L.N;
+  a.M = (int)L.M;
+  a.nN = (int)((L.N + CH - 1) / CH);
+  a.nM = (int)((L.M + CH - 1) / CH);
+  a.ntiles = (int)((T + TILE - 1) / TILE);
+  a.Dc = at<float>(ws, off + t.Dc);
+  a.rinfo = at<int>(ws, off + t.rinfo);
+  a.dx = static_cast<__nv_bfloat16*>(dx);
+  a.dAc = at<float>(ws, off + t.dAc);
+  a.dBc = at<float>(ws, off + t.dBc);
+  a.dDc = at<float>(ws, off + t.dDc);
+  int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+  tt_bwd_kernel<<<grid, NTHREADS, kSmemBwd, st>>>(mx, mdy, mat, mbm, manr, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 }  // namespace ttc
+
+#include "merge_engine.cuh"
+
+#ifdef TTC_TIMELINE
+extern "C" int ttc_timeline_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, ttc::g_tl, bytes);
+}
+#endif

@@ -5,23 +5,34 @@
 
 namespace ttc {
 
+// Device addresses of the packed tensor-core operands and gradient sums.
+struct TcPtrs {
+  void* At = nullptr;    // bf16 [64][N]
+  void* Anr = nullptr;   // bf16 [N][64]
+  void* Bm = nullptr;    // bf16 [64][M]
+  void* Bt = nullptr;    // bf16 [M][64]
+  float* Dc = nullptr;   // [64] compacted middle diagonal (0 past r')
+  int* rinfo = nullptr;  // [0] = r', [1 + c] = original index of column c
+  float* dAc = nullptr;  // [N][64] sum over tokens of x^T dz
+  float* dBc = nullptr;  // [64][M] sum over tokens of z'^T dy
+  float* dDc = nullptr;  // [64]    sum over tokens of z * dz'
+};
+TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t ws_off);
+
 // True when the bf16 fused kernels handle this layer shape.
 bool tc_supported(const LayerPlan& L);
 
 // Bytes of workspace the fused path needs for its packed operands.
 size_t tc_operand_bytes(const LayerPlan& L);
 
-// y = ((x A) diag(D_d)) B with A (N x rd) and B (rd x M) the merged halves (f32,
-// in the workspace); ws_off is the start of this path's operand region.
-tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, const float* params,
-                     const float* A, const float* B, void* y, void* ws, size_t ws_off,
-                     cudaStream_t st);
+// y = ((x A) diag(D_d)) B for T tokens; the packed operands (written by the
+// merge engine's pack phase) are in the workspace at ws_off.
+tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws,
+                     size_t ws_off, cudaStream_t st);
 
-// dx, dD_d (written to dDmid, honouring the prune convention and acc), and
-// dA (N x rd), dB (rd x M) accumulated into the zeroed f32 buffers.
-tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy,
-                      const float* params, const float* A, const float* B, void* dx,
-                      float* dDmid, bool acc, float* dA, float* dB, void* ws, size_t ws_off,
-                      cudaStream_t st);
+// dx for T tokens and the token sums dAc, dBc, dDc (zeroed by the pack
+// phase); the merge engine's unpack phase turns these into dA, dB, dD_d.
+tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
+                      void* ws, size_t ws_off, cudaStream_t st);
 
 }  // namespace ttc

@@ -6,6 +6,7 @@
 #include <cstring>
 #include <new>
 
+#include "merge_engine.h"
 #include "tc_fused.h"
 #include "ttc_internal.h"
 
@@ -74,32 +75,43 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
 // ---- workspace ------------------------------------------------------------
 struct WsLayout {
   size_t P[kMaxK] = {};  // merged chain prefixes (floats), 0 where aliased to params
-  size_t dA = 0, dB = 0, q0 = 0, q1 = 0, z = 0, dzp = 0;
+  size_t dA = 0, dB = 0;
+  size_t q[4] = {};      // reverse-chain dQ ping-pong buffers (input side 0/1, output 2/3)
+  size_t part[4] = {};   // split-K partials (input side 0/1, output 2/3)
+  size_t part_cap = 0;   // floats per partial buffer
+  size_t z = 0, dzp = 0; // SIMT token path intermediates
   size_t tc = 0;         // tensor-core path operands
   size_t end = 0;        // end of this layer's scratch
 };
 
 size_t chain_len(const LayerPlan& L, int k) { return (size_t)L.U[k] * L.r[k + 1]; }
 
-size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w) {
+size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
+                    bool simt_tokens = false) {
   size_t off = align_up(base, 256);
   auto take = [&](size_t bytes) {
     size_t o = off;
     off = align_up(off + bytes, 256);
     return o;
   };
-  size_t qmax = 0;
+  size_t qmax = 0, pmax = 0;
   for (int k = 0; k < L.K; ++k) {
     size_t n = chain_len(L, k);
     if (n > qmax) qmax = n;
+    size_t core = (size_t)L.r[k] * L.s[k] * L.r[k + 1];
+    size_t pf = eng_partial_floats(L.r[k], (int64_t)L.s[k] * L.r[k + 1], 0);
+    (void)core;
+    if (pf > pmax) pmax = pf;
     w->P[k] = (k == 0 || k == L.d) ? 0 : take(n * sizeof(float));
   }
   w->dA = take((size_t)L.N * L.rd * sizeof(float));
   w->dB = take((size_t)L.rd * L.M * sizeof(float));
-  w->q0 = take(qmax * sizeof(float));
-  w->q1 = take(qmax * sizeof(float));
-  w->z = take((size_t)T * L.rd * sizeof(float));
-  w->dzp = take((size_t)T * L.rd * sizeof(float));
+  for (int i = 0; i < 4; ++i) w->q[i] = take(qmax * sizeof(float));
+  for (int i = 0; i < 4; ++i) w->part[i] = take(pmax * sizeof(float));
+  w->part_cap = pmax;
+  const bool tc = !simt_tokens && tc_supported(L) && L.act == TT_DT_BF16;
+  w->z = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
+  w->dzp = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->tc = take(tc_operand_bytes(L));
   w->end = off;
   return off;
@@ -111,8 +123,9 @@ struct FfnLayout {
 };
 
 size_t ffn_layout(const tt_plan_s* p, int64_t T, FfnLayout* f) {
-  size_t e0 = layer_layout(p->L[0], T, 256, &f->up);
-  size_t e1 = layer_layout(p->L[1], T, 256, &f->down);
+  // the FFN layers run their token passes on f32 intermediates (SIMT path)
+  size_t e0 = layer_layout(p->L[0], T, 256, &f->up, true);
+  size_t e1 = layer_layout(p->L[1], T, 256, &f->down, true);
   size_t off = align_up(e0 > e1 ? e0 : e1, 256);
   const size_t hb = (size_t)T * p->L[0].M * sizeof(float);
   f->h = off;
@@ -133,152 +146,196 @@ size_t ffn_layout(const tt_plan_s* p, int64_t T, FfnLayout* f) {
 
 float* fptr(void* ws, size_t off) { return reinterpret_cast<float*>(static_cast<char*>(ws) + off); }
 
-// ---- merges ---------------------------------------------------------------
-// P_k = reshape((P_{k-1} * D_{k-1}) . G_k) for k on one side of the chain.
-tt_status merge_chain(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
-                      const float** P, cudaStream_t st) {
-  for (int k = 0; k < L.K; ++k) {
-    if (k == 0 || k == L.d) {
-      P[k] = params + L.core_off[k];
-      continue;
+// Chain prefix pointers: P_k = reshape((P_{k-1} * D_{k-1}) . G_k) on each side;
+// P_0 and P_d are the first cores themselves.
+void chain_ptrs(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
+                const float** P) {
+  for (int k = 0; k < L.K; ++k)
+    P[k] = (k == 0 || k == L.d) ? params + L.core_off[k] : fptr(ws, w.P[k]);
+}
+
+// ---- merge programs ---------------------------------------------------------
+// Forward merge: phase j computes P_j (input side) and P_{d+j} (output side);
+// a last phase packs the tensor-core operands when that path runs.
+tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
+                            const float** P, bool pack, bool zero_grads, cudaStream_t st) {
+  chain_ptrs(L, params, ws, w, P);
+  EngBuilder b;
+  for (int j = 1; j < L.d; ++j) {
+    b.begin_phase();
+    for (int k : {j, L.d + j}) {
+      GemmArgs g;
+      g.m = L.U[k - 1];
+      g.n = (int64_t)L.s[k] * L.r[k + 1];
+      g.k = L.r[k];
+      g.A = P[k - 1]; g.sam = L.r[k]; g.sak = 1;
+      g.kscale = params + L.diag_off[k - 1]; g.klen = L.r[k];
+      g.B = params + L.core_off[k]; g.sbk = g.n; g.sbn = 1;
+      g.C = const_cast<float*>(P[k]); g.scm = g.n; g.scn = 1;
+      eng_gemm_task(b.add(), g, nullptr, 0);
     }
-    GemmArgs g;
-    g.m = L.U[k - 1];
-    g.n = (int64_t)L.s[k] * L.r[k + 1];
-    g.k = L.r[k];
-    g.A = P[k - 1]; g.sam = L.r[k]; g.sak = 1;
-    g.kscale = params + L.diag_off[k - 1]; g.klen = L.r[k];
-    g.B = params + L.core_off[k]; g.sbk = g.n; g.sbn = 1;
-    float* out = fptr(ws, w.P[k]);
-    g.C = out; g.scm = g.n; g.scn = 1;
-    TT_CUDA(gemm_simt(g, st));
-    P[k] = out;
   }
+  if (pack) {
+    b.begin_phase();
+    eng_pack_task(b.add(), L, P[L.d - 1], P[L.K - 1], params + L.diag_off[L.d - 1],
+                  tc_ptrs(L, ws, w.tc), zero_grads);
+  }
+  b.end();
+  if (b.overflow) return TT_ERR_UNSUPPORTED;
+  if (b.p.nphases == 0) return TT_OK;
+  TT_CUDA(eng_launch(b.p, st));
   return TT_OK;
 }
 
-// Reverse of merge_chain on the cores [k_first, k_last]: dP_{k_last} is in
-// dlast (unscaled); writes dG_k for every core of the side and dD_e for the
-// links inside it.
-tt_status merge_chain_backward(const LayerPlan& L, const float* params, const float** P,
-                               int k_first, int k_last, const float* dlast, float* dparams,
-                               bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
-  const int mode = acc ? kAccumulate : kStore;
-  const float* Y = dlast;      // stored dP_k (unscaled by D_k)
-  const float* yscale = nullptr;  // D_k to apply to the last index of Y, if any
-  float* bufs[2] = {fptr(ws, w.q0), fptr(ws, w.q1)};
-  int flip = 0;
-  for (int k = k_last; k > k_first; --k) {
-    const int rk = L.r[k], rk1 = L.r[k + 1];
-    const int64_t U = L.U[k - 1];
-    const int64_t ncol = (int64_t)L.s[k] * rk1;
-    const float* Dprev = params + L.diag_off[k - 1];
-    // dG_k = diag(D_{k-1}) P_{k-1}^T Y
-    GemmArgs g;
-    g.m = rk; g.n = ncol; g.k = U;
-    g.A = P[k - 1]; g.sam = 1; g.sak = rk;
-    g.B = Y; g.sbk = ncol; g.sbn = 1;
-    g.rscale = Dprev;
-    g.cscale = yscale; g.clen = rk1;
-    g.C = dparams + L.core_off[k]; g.scm = ncol; g.scn = 1;
-    g.mode = mode;
-    TT_CUDA(gemm_simt(g, st));
-    // dQ = Y G_k^T   (U x r_k)
-    float* dQ = bufs[flip];
-    GemmArgs h;
-    h.m = U; h.n = rk; h.k = ncol;
-    h.A = Y; h.sam = ncol; h.sak = 1;
-    h.kscale = yscale; h.klen = rk1;
-    h.B = params + L.core_off[k]; h.sbk = 1; h.sbn = ncol;
-    h.C = dQ; h.scm = rk; h.scn = 1;
-    TT_CUDA(gemm_simt(h, st));
-    // dD_{k-1}[b] = sum_u P_{k-1}[u,b] dQ[u,b]  (0 where D_{k-1}[b] == 0)
-    TT_CUDA(coldot(U, rk, P[k - 1], rk, dQ, rk, Dprev, dparams + L.diag_off[k - 1], acc, st));
-    Y = dQ;
-    yscale = Dprev;
-    flip ^= 1;
+// Backward through the merges.  For one side with cores k_first..k_last and
+// dP_{k_last} = dlast, reverse step k (k_last down to k_first+1) computes
+//   dG_k = diag(D_{k-1}) P_{k-1}^T Y,  dQ = Y G_k^T,  dD_{k-1} = colsum(P_{k-1} * dQ)
+// with Y = dlast for the first step and Y = dQ_prev * D_k afterwards; the
+// first core gets dG = Y * D_{k_first}.  Both sides advance in lockstep, one
+// phase per step; split-K partials of dG_k are reduced in the next phase.
+tt_status run_merge_backward(const LayerPlan& L, const float* params, const float** P,
+                             const float* dA, const float* dB, float* dparams, bool acc,
+                             bool unpack, void* ws, const WsLayout& w, cudaStream_t st) {
+  EngBuilder b;
+  if (unpack) {
+    b.begin_phase();
+    eng_unpack_task(b.add(), L, tc_ptrs(L, ws, w.tc), fptr(ws, w.dA), fptr(ws, w.dB),
+                    dparams + L.diag_off[L.d - 1], acc);
   }
-  // first core of the side: dG = Y * yscale
-  const size_t n = (size_t)L.r[k_first] * L.s[k_first] * L.r[k_first + 1];
-  TT_CUDA(scale_periodic((int64_t)n, Y, yscale, L.r[k_first + 1],
-                         dparams + L.core_off[k_first], acc, st));
+  struct Side {
+    int k_first, k_last;
+    const float* Y;
+    const float* yscale;
+    int qi, pi;          // base index of q / part buffers
+    int flip;
+    EngTask pending;     // split GEMM whose partials the next phase reduces
+    bool has_pending;
+    const float* dQ;     // last dQ (for coldot in the next phase)
+    int coldot_k;        // link whose dD the next phase computes (-1: none)
+  } sides[2] = {{0, L.d - 1, dA, nullptr, 0, 0, 0, EngTask(), false, nullptr, -1},
+                {L.d, L.K - 1, dB, nullptr, 2, 2, 0, EngTask(), false, nullptr, -1}};
+  const int mode = acc ? kAccumulate : kStore;
+  const int steps = L.d - 1;
+  for (int j = 0; j <= steps; ++j) {
+    b.begin_phase();
+    for (Side& sd : sides) {
+      // work left over from the previous step
+      if (sd.has_pending) {
+        eng_gemm_final_task(b.add(), sd.pending);
+        sd.has_pending = false;
+      }
+      if (sd.coldot_k >= 0) {
+        const int k = sd.coldot_k;  // dD_{k-1} from P_{k-1} and dQ_k
+        EngTask* t = b.add();
+        t->kind = kEColdot;
+        t->units = L.r[k];
+        t->x = P[k - 1]; t->sx = L.r[k];
+        t->y = sd.dQ; t->sy = L.r[k];
+        t->n = L.U[k - 1];
+        t->s = params + L.diag_off[k - 1];
+        t->out = dparams + L.diag_off[k - 1];
+        t->acc = acc ? 1 : 0;
+        sd.coldot_k = -1;
+      }
+      if (j < steps) {
+        const int k = sd.k_last - j;
+        const int rk = L.r[k], rk1 = L.r[k + 1];
+        const int64_t U = L.U[k - 1];
+        const int64_t ncol = (int64_t)L.s[k] * rk1;
+        GemmArgs g;  // dG_k
+        g.m = rk; g.n = ncol; g.k = U;
+        g.A = P[k - 1]; g.sam = 1; g.sak = rk;
+        g.B = sd.Y; g.sbk = ncol; g.sbn = 1;
+        g.rscale = params + L.diag_off[k - 1];
+        g.cscale = sd.yscale; g.clen = rk1;
+        g.C = dparams + L.core_off[k]; g.scm = ncol; g.scn = 1;
+        g.mode = mode;
+        EngTask* t = b.add();
+        eng_gemm_task(t, g, fptr(ws, w.part[sd.pi + (sd.flip & 1)]), w.part_cap);
+        if (t->splits > 1) {
+          sd.pending = *t;
+          sd.has_pending = true;
+        }
+        float* dQ = fptr(ws, w.q[sd.qi + (sd.flip & 1)]);
+        GemmArgs h;  // dQ = Y G_k^T
+        h.m = U; h.n = rk; h.k = ncol;
+        h.A = sd.Y; h.sam = ncol; h.sak = 1;
+        h.kscale = sd.yscale; h.klen = rk1;
+        h.B = params + L.core_off[k]; h.sbk = 1; h.sbn = ncol;
+        h.C = dQ; h.scm = rk; h.scn = 1;
+        eng_gemm_task(b.add(), h, nullptr, 0);
+        sd.dQ = dQ;
+        sd.coldot_k = k;
+        sd.Y = dQ;
+        sd.yscale = params + L.diag_off[k - 1];
+        sd.flip ^= 1;
+      } else {
+        // first core of the side
+        EngTask* t = b.add();
+        t->kind = kEScale;
+        t->n = (int64_t)L.r[sd.k_first] * L.s[sd.k_first] * L.r[sd.k_first + 1];
+        t->units = (int)((t->n + 1023) / 1024);
+        t->x = sd.Y;
+        t->s = sd.yscale;
+        t->len = L.r[sd.k_first + 1];
+        t->out = dparams + L.core_off[sd.k_first];
+        t->acc = acc ? 1 : 0;
+      }
+    }
+  }
+  b.end();
+  if (b.overflow) return TT_ERR_UNSUPPORTED;
+  TT_CUDA(eng_launch(b.p, st));
   return TT_OK;
 }
 
 // ---- one layer ---------------------------------------------------------------
-tt_status layer_forward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
-                               const float* params, const float** P, void* y, int ty, void* ws,
-                               const WsLayout& w, cudaStream_t st);
-tt_status layer_backward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
-                                const void* dy, int tdy, const float* params, const float** P,
-                                void* dx, int tdx, float* dparams, bool acc, void* ws,
-                                const WsLayout& w, cudaStream_t st);
+bool use_tc(const LayerPlan& L, int tx, int ty) {
+  return tx == TT_DT_BF16 && ty == TT_DT_BF16 && L.act == TT_DT_BF16 && tc_supported(L);
+}
 
 tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, const float* params,
                         void* y, int ty, void* ws, const WsLayout& w, cudaStream_t st) {
   const float* P[kMaxK];
+  const bool tc = use_tc(L, tx, ty);
   prof_begin(kPhMerge, st);
-  tt_status s = merge_chain(L, params, ws, w, P, st);
+  tt_status s = run_merge_forward(L, params, ws, w, P, tc, false, st);
   prof_end(kPhMerge, st);
   if (s != TT_OK) return s;
   prof_begin(kPhFwd, st);
-  s = layer_forward_tokens(L, T, x, tx, params, P, y, ty, ws, w, st);
+  if (tc) {
+    s = tc_forward(L, T, x, y, ws, w.tc, st);
+  } else {
+    const float* A = P[L.d - 1];   // N x rd
+    const float* B = P[L.K - 1];   // rd x M
+    const float* Dm = params + L.diag_off[L.d - 1];
+    float* z = fptr(ws, w.z);
+    GemmArgs g;
+    g.m = T; g.n = L.rd; g.k = L.N;
+    g.A = x; g.sam = L.N; g.sak = 1; g.ta = tx;
+    g.B = A; g.sbk = L.rd; g.sbn = 1;
+    g.C = z; g.scm = L.rd; g.scn = 1;
+    cudaError_t e = gemm_simt(g, st);
+    if (e == cudaSuccess) {
+      GemmArgs h;
+      h.m = T; h.n = L.M; h.k = L.rd;
+      h.A = z; h.sam = L.rd; h.sak = 1;
+      h.kscale = Dm; h.klen = L.rd;
+      h.B = B; h.sbk = L.M; h.sbn = 1;
+      h.C = y; h.scm = L.M; h.scn = 1; h.tc = ty;
+      e = gemm_simt(h, st);
+    }
+    s = e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  }
   prof_end(kPhFwd, st);
   return s;
 }
 
-tt_status layer_forward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
-                               const float* params, const float** P, void* y, int ty, void* ws,
+// SIMT token pass of the backward: dx, dD_d, and dA / dB sums over tokens.
+tt_status simt_backward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
+                               const void* dy, int tdy, const float* params, const float** P,
+                               void* dx, int tdx, float* dparams, bool acc, void* ws,
                                const WsLayout& w, cudaStream_t st) {
-  const float* A = P[L.d - 1];   // N x rd
-  const float* B = P[L.K - 1];   // rd x M
-  const float* Dm = params + L.diag_off[L.d - 1];
-  if (tx == TT_DT_BF16 && ty == TT_DT_BF16 && tc_supported(L)) {
-    return tc_forward(L, T, x, params, A, B, y, ws, w.tc, st);
-  }
-  float* z = fptr(ws, w.z);
-  GemmArgs g;
-  g.m = T; g.n = L.rd; g.k = L.N;
-  g.A = x; g.sam = L.N; g.sak = 1; g.ta = tx;
-  g.B = A; g.sbk = L.rd; g.sbn = 1;
-  g.C = z; g.scm = L.rd; g.scn = 1;
-  TT_CUDA(gemm_simt(g, st));
-  GemmArgs h;
-  h.m = T; h.n = L.M; h.k = L.rd;
-  h.A = z; h.sam = L.rd; h.sak = 1;
-  h.kscale = Dm; h.klen = L.rd;
-  h.B = B; h.sbk = L.M; h.sbn = 1;
-  h.C = y; h.scm = L.M; h.scn = 1; h.tc = ty;
-  TT_CUDA(gemm_simt(h, st));
-  return TT_OK;
-}
-
-tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, const void* dy,
-                         int tdy, const float* params, void* dx, int tdx, float* dparams,
-                         bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
-  const float* P[kMaxK];
-  prof_begin(kPhMerge, st);
-  tt_status s = merge_chain(L, params, ws, w, P, st);
-  prof_end(kPhMerge, st);
-  if (s != TT_OK) return s;
-  prof_begin(kPhBwd, st);
-  s = layer_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
-  prof_end(kPhBwd, st);
-  if (s != TT_OK) return s;
-  prof_begin(kPhMergeBwd, st);
-  s = merge_chain_backward(L, params, P, 0, L.d - 1, fptr(ws, w.dA), dparams, acc, ws, w, st);
-  if (s == TT_OK)
-    s = merge_chain_backward(L, params, P, L.d, L.K - 1, fptr(ws, w.dB), dparams, acc, ws, w,
-                             st);
-  prof_end(kPhMergeBwd, st);
-  return s;
-}
-
-tt_status layer_backward_tokens(const LayerPlan& L, int64_t T, const void* x, int tx,
-                                const void* dy, int tdy, const float* params, const float** P,
-                                void* dx, int tdx, float* dparams, bool acc, void* ws,
-                                const WsLayout& w, cudaStream_t st) {
-  tt_status s = TT_OK;
   const float* A = P[L.d - 1];
   const float* B = P[L.K - 1];
   const float* Dm = params + L.diag_off[L.d - 1];
@@ -286,52 +343,71 @@ tt_status layer_backward_tokens(const LayerPlan& L, int64_t T, const void* x, in
   float* dB = fptr(ws, w.dB);
   TT_CUDA(cudaMemsetAsync(dA, 0, (size_t)L.N * L.rd * sizeof(float), st));
   TT_CUDA(cudaMemsetAsync(dB, 0, (size_t)L.rd * L.M * sizeof(float), st));
-  if (tx == TT_DT_BF16 && tdy == TT_DT_BF16 && tdx == TT_DT_BF16 && tc_supported(L)) {
-    s = tc_backward(L, T, x, dy, params, A, B, dx, dparams + L.diag_off[L.d - 1], acc, dA, dB,
-                    ws, w.tc, st);
-    if (s != TT_OK) return s;
-  } else if (T > 0) {
-    float* z = fptr(ws, w.z);
-    float* dzp = fptr(ws, w.dzp);
-    GemmArgs g;  // z = x A
-    g.m = T; g.n = L.rd; g.k = L.N;
-    g.A = x; g.sam = L.N; g.sak = 1; g.ta = tx;
-    g.B = A; g.sbk = L.rd; g.sbn = 1;
-    g.C = z; g.scm = L.rd; g.scn = 1;
-    TT_CUDA(gemm_simt(g, st));
-    GemmArgs h;  // dz' = dy B^T
-    h.m = T; h.n = L.rd; h.k = L.M;
-    h.A = dy; h.sam = L.M; h.sak = 1; h.ta = tdy;
-    h.B = B; h.sbk = 1; h.sbn = L.M;
-    h.C = dzp; h.scm = L.rd; h.scn = 1;
-    TT_CUDA(gemm_simt(h, st));
-    // dD_d = sum_t z * dz'
-    TT_CUDA(coldot(T, L.rd, z, L.rd, dzp, L.rd, Dm, dparams + L.diag_off[L.d - 1], acc, st));
-    GemmArgs a;  // dx = (dz' D) A^T
-    a.m = T; a.n = L.N; a.k = L.rd;
-    a.A = dzp; a.sam = L.rd; a.sak = 1;
-    a.kscale = Dm; a.klen = L.rd;
-    a.B = A; a.sbk = 1; a.sbn = L.rd;
-    a.C = dx; a.scm = L.N; a.scn = 1; a.tc = tdx;
-    TT_CUDA(gemm_simt(a, st));
-    GemmArgs b;  // dA = x^T (dz' D)
-    b.m = L.N; b.n = L.rd; b.k = T;
-    b.A = x; b.sam = 1; b.sak = L.N; b.ta = tx;
-    b.B = dzp; b.sbk = L.rd; b.sbn = 1;
-    b.cscale = Dm; b.clen = L.rd;
-    b.C = dA; b.scm = L.rd; b.scn = 1; b.mode = kAtomic;
-    TT_CUDA(gemm_simt(b, st));
-    GemmArgs c;  // dB = diag(D) z^T dy
-    c.m = L.rd; c.n = L.M; c.k = T;
-    c.A = z; c.sam = 1; c.sak = L.rd;
-    c.rscale = Dm;
-    c.B = dy; c.sbk = L.M; c.sbn = 1; c.tb = tdy;
-    c.C = dB; c.scm = L.M; c.scn = 1; c.mode = kAtomic;
-    TT_CUDA(gemm_simt(c, st));
-  } else if (!acc) {
-    TT_CUDA(cudaMemsetAsync(dparams + L.diag_off[L.d - 1], 0, L.rd * sizeof(float), st));
+  if (T == 0) {
+    if (!acc) TT_CUDA(cudaMemsetAsync(dparams + L.diag_off[L.d - 1], 0, L.rd * sizeof(float), st));
+    return TT_OK;
   }
+  float* z = fptr(ws, w.z);
+  float* dzp = fptr(ws, w.dzp);
+  GemmArgs g;  // z = x A
+  g.m = T; g.n = L.rd; g.k = L.N;
+  g.A = x; g.sam = L.N; g.sak = 1; g.ta = tx;
+  g.B = A; g.sbk = L.rd; g.sbn = 1;
+  g.C = z; g.scm = L.rd; g.scn = 1;
+  TT_CUDA(gemm_simt(g, st));
+  GemmArgs h;  // dz' = dy B^T
+  h.m = T; h.n = L.rd; h.k = L.M;
+  h.A = dy; h.sam = L.M; h.sak = 1; h.ta = tdy;
+  h.B = B; h.sbk = 1; h.sbn = L.M;
+  h.C = dzp; h.scm = L.rd; h.scn = 1;
+  TT_CUDA(gemm_simt(h, st));
+  // dD_d = sum_t z * dz'
+  TT_CUDA(coldot(T, L.rd, z, L.rd, dzp, L.rd, Dm, dparams + L.diag_off[L.d - 1], acc, st));
+  GemmArgs a;  // dx = (dz' D) A^T
+  a.m = T; a.n = L.N; a.k = L.rd;
+  a.A = dzp; a.sam = L.rd; a.sak = 1;
+  a.kscale = Dm; a.klen = L.rd;
+  a.B = A; a.sbk = 1; a.sbn = L.rd;
+  a.C = dx; a.scm = L.N; a.scn = 1; a.tc = tdx;
+  TT_CUDA(gemm_simt(a, st));
+  GemmArgs bb;  // dA = x^T (dz' D)
+  bb.m = L.N; bb.n = L.rd; bb.k = T;
+  bb.A = x; bb.sam = 1; bb.sak = L.N; bb.ta = tx;
+  bb.B = dzp; bb.sbk = L.rd; bb.sbn = 1;
+  bb.cscale = Dm; bb.clen = L.rd;
+  bb.C = dA; bb.scm = L.rd; bb.scn = 1; bb.mode = kAtomic;
+  TT_CUDA(gemm_simt(bb, st));
+  GemmArgs c;  // dB = diag(D) z^T dy
+  c.m = L.rd; c.n = L.M; c.k = T;
+  c.A = z; c.sam = 1; c.sak = L.rd;
+  c.rscale = Dm;
+  c.B = dy; c.sbk = L.M; c.sbn = 1; c.tb = tdy;
+  c.C = dB; c.scm = L.M; c.scn = 1; c.mode = kAtomic;
+  TT_CUDA(gemm_simt(c, st));
   return TT_OK;
+}
+
+tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, const void* dy,
+                         int tdy, const float* params, void* dx, int tdx, float* dparams,
+                         bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
+  const float* P[kMaxK];
+  const bool tc = use_tc(L, tx, tdy) && tdx == TT_DT_BF16;
+  prof_begin(kPhMerge, st);
+  tt_status s = run_merge_forward(L, params, ws, w, P, tc, true, st);
+  prof_end(kPhMerge, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhBwd, st);
+  if (tc)
+    s = tc_backward(L, T, x, dy, dx, ws, w.tc, st);
+  else
+    s = simt_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
+  prof_end(kPhBwd, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhMergeBwd, st);
+  s = run_merge_backward(L, params, P, fptr(ws, w.dA), fptr(ws, w.dB), dparams, acc, tc, ws, w,
+                         st);
+  prof_end(kPhMergeBwd, st);
+  return s;
 }
 
 tt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
