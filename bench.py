@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-reuse", action="store_true",
+                   help="re-merge the cores in the backward instead of reusing the forward's")
     p.add_argument("--target-seconds", type=float, default=3.0,
                    help="timed-region length used when --steps is not given")
     return p.parse_args()
@@ -306,7 +308,7 @@ def run_ours(args, w):
         n_par = [p.numel() for p in params]
     else:
         L = w.layers[0]
-        mod = TTLinear(L.in_modes, L.out_modes, L.ranks, dt)
+        mod = TTLinear(L.in_modes, L.out_modes, L.ranks, dt, reuse_merge=not args.no_reuse)
         params = [torch.from_numpy(synth.pack(inp0.layers[0].cores, inp0.layers[0].diags)).to(dev)]
         N, M = L.N, L.M
         n_par = [params[0].numel()]
@@ -501,7 +503,8 @@ def run_ours(args, w):
                        "ranks": [list(L.ranks) for L in w.layers],
                        "l2": f"{nsets} rotating input/output sets of {set_bytes / 1e6:.1f} MB "
                              f"(> 2x L2 of {l2 / 1e6:.0f} MB)",
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"replicas x{world}",
+                       "reuse_merge": (not args.no_reuse) and not w.ffn},
             "roofline": roof,
             "roofline_step": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3),
                               "algorithmic_bytes": alg["bytes"], "algorithmic_flop": alg["flop"],

@@ -66,6 +66,13 @@ typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1 } tt_dtype;
 
 /* flags of tt_desc */
 #define TT_ACCUMULATE 1u /* backward adds into dparams instead of overwriting */
+/* The backward reuses the merged cores that the forward left in the
+ * workspace, as the CoMERA project page describes for its contraction path
+ * (the forward keeps its intermediate results for the backward pass).  The
+ * caller guarantees that a tt_forward call with the same plan, the same
+ * params and the same workspace came before, with nothing else using the
+ * workspace in between; then tt_backward skips re-merging the cores. */
+#define TT_REUSE_MERGE 2u
 
 typedef struct tt_desc {
   int d;                        /* 1..TT_MAX_D: number of input (= output) modes */
@@ -73,7 +80,7 @@ typedef struct tt_desc {
   int out_modes[TT_MAX_D];      /* m_1..m_d, each >= 1 */
   int ranks[2 * TT_MAX_D + 1];  /* r_0..r_2d; r_0 = r_2d = 1, others >= 1 */
   int act;                      /* tt_dtype of x, y, dx, dy */
-  unsigned flags;               /* TT_ACCUMULATE */
+  unsigned flags;               /* TT_ACCUMULATE | TT_REUSE_MERGE */
 } tt_desc;
 
 typedef struct tt_plan_s tt_plan_t; /* opaque, immutable host object */

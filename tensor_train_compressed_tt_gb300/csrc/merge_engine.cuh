@@ -12,11 +12,20 @@ namespace {
 
 constexpr int kEngThreads = 256;
 constexpr int kET = 32;   // GEMM tile (kET x kET outputs per unit)
-constexpr int kEK = 32;   // K slice staged per iteration
+constexpr int kEK = 128;  // K slice staged per iteration (all loads in flight at once)
 constexpr int kBarSlots = 64;
 static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
 
-__device__ unsigned g_eng_bar[kBarSlots][32];  // [0] count, [1] generation (own 128-byte line)
+// Two-level grid barrier state per slot: 16 group counters and a root
+// counter (each on its own 128-byte line) plus the generation word.
+constexpr int kBarGroup = 16;
+constexpr int kBarMaxGroups = 16;
+struct EngBarSlot {
+  unsigned group[kBarMaxGroups][32];
+  unsigned root[32];
+  unsigned gen[32];
+};
+__device__ EngBarSlot g_eng_bar[kBarSlots];
 
 // Grid-wide barrier, bounded: false if it timed out (error recorded).  Data
 // produced in one phase and read in a later one is read with L2-only loads
@@ -24,15 +33,25 @@ __device__ unsigned g_eng_bar[kBarSlots][32];  // [0] count, [1] generation (own
 __device__ bool eng_grid_barrier(unsigned slot, unsigned nblocks, int* failed) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned* count = &g_eng_bar[slot][0];
-    volatile unsigned* gen = &g_eng_bar[slot][1];
+    EngBarSlot& B = g_eng_bar[slot];
+    volatile unsigned* gen = &B.gen[0];
     const unsigned g0 = *gen;
     __threadfence();
-    if (atomicAdd(count, 1u) == nblocks - 1) {
-      atomicExch(count, 0u);
+    const unsigned gi = blockIdx.x / kBarGroup;
+    const unsigned ngroups = (nblocks + kBarGroup - 1) / kBarGroup;
+    const unsigned gsize = min((unsigned)kBarGroup, nblocks - gi * kBarGroup);
+    bool last = false;
+    if (atomicAdd(&B.group[gi][0], 1u) == gsize - 1) {
+      atomicExch(&B.group[gi][0], 0u);
       __threadfence();
-      atomicAdd(const_cast<unsigned*>(gen), 1u);
-    } else {
+      if (atomicAdd(&B.root[0], 1u) == ngroups - 1) {
+        atomicExch(&B.root[0], 0u);
+        __threadfence();
+        atomicAdd(&B.gen[0], 1u);
+        last = true;
+      }
+    }
+    if (!last) {
       const uint64_t t0 = gtimer();
       while (*gen == g0) {
         if (gtimer() - t0 > kTimeoutNs) {
@@ -48,9 +67,29 @@ __device__ bool eng_grid_barrier(unsigned slot, unsigned nblocks, int* failed) {
   return *failed == 0;
 }
 
+// Compaction position of each middle-rank index (-1 if pruned), from D_d
+// (pack) or from the kept list (gather).
+__device__ void eng_pos_map(const EngTask& t, int* pos) {
+  compaction_map(t.s, t.rd, pos, nullptr, nullptr);
+}
+
+// Element f (flat index into dA (N x rd) or dB (rd x M)) read from the
+// compacted token sums.
+__device__ __forceinline__ float eng_gather(const EngTask& t, const int* pos, int64_t f) {
+  if (t.gather == 1) {
+    const int64_t j = f / t.rd;
+    const int c = pos[f - j * t.rd];
+    return c >= 0 ? __ldcg(t.tc.dAc + j * RP + c) : 0.f;
+  }
+  const int64_t a = f / t.M;
+  const int c = pos[a];
+  return c >= 0 ? __ldcg(t.tc.dBc + (f - a * t.M) * RP + c) : 0.f;
+}
+
 // One kET x kET output tile of C over one K slice.
 __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
-                              float (*Bs)[kET + 1]) {
+                              float (*Bs)[kET + 1], int* pos) {
+  if (t.pack_side || t.gather) eng_pos_map(t, pos);
   const GemmArgs& g = t.g;
   const int S = t.splits;
   const int tiles_n = (int)((g.n + kET - 1) / kET);
@@ -67,23 +106,30 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
   float acc[2][2] = {};
   for (int64_t k0 = kb; k0 < ke; k0 += kEK) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int idx = tid + e * kEngThreads;  // 0..1023
+    for (int e = 0; e < (kET * kEK) / kEngThreads; ++e) {
+      const int idx = tid + e * kEngThreads;
       const int a_m = idx % kET, a_k = idx / kET;
       const int64_t gm = m0 + a_m, gk = k0 + a_k;
       float v = 0.f;
       if (gm < g.m && gk < ke) {
-        v = __ldcg(A + gm * g.sam + gk * g.sak);
+        const int64_t f = gm * g.sam + gk * g.sak;
+        v = (t.gather && t.gather_op == 0) ? eng_gather(t, pos, f) : __ldcg(A + f);
         if (g.kscale) v *= g.kscale[gk % g.klen];
       }
       As[a_k][a_m] = v;
       const int b_n = idx % kET, b_k = idx / kET;
       const int64_t gn = n0 + b_n, gk2 = k0 + b_k;
-      Bs[b_k][b_n] = (gn < g.n && gk2 < ke) ? __ldcg(B + gk2 * g.sbk + gn * g.sbn) : 0.f;
+      float w = 0.f;
+      if (gn < g.n && gk2 < ke) {
+        const int64_t f = gk2 * g.sbk + gn * g.sbn;
+        w = (t.gather && t.gather_op == 1) ? eng_gather(t, pos, f) : __ldcg(B + f);
+      }
+      Bs[b_k][b_n] = w;
     }
     __syncthreads();
+    const int kn = (int)(ke - k0 < kEK ? ke - k0 : kEK);
 #pragma unroll 8
-    for (int kk = 0; kk < kEK; ++kk) {
+    for (int kk = 0; kk < kn; ++kk) {
       const float a0 = As[kk][ty * 2], a1 = As[kk][ty * 2 + 1];
       const float b0 = Bs[kk][tx * 2], b1 = Bs[kk][tx * 2 + 1];
       acc[0][0] = fmaf(a0, b0, acc[0][0]);
@@ -111,6 +157,26 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
       if (g.cscale) v *= g.cscale[gn % g.clen];
       const int64_t ci = gm * g.scm + gn * g.scn;
       C[ci] = g.mode == kAccumulate ? __ldcg(C + ci) + v : v;
+      if (t.pack_side) {
+        // C is A (N x rd) or B (rd x M), row-major with scm = n, scn = 1
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        if (t.pack_side == 1) {
+          const int64_t jj = ci / t.rd;
+          const int c = pos[ci - jj * t.rd];
+          if (c >= 0) {
+            static_cast<__nv_bfloat16*>(t.tc.Anr)[jj * RP + c] = b;
+            static_cast<__nv_bfloat16*>(t.tc.At)[(int64_t)c * t.N + jj] = b;
+          }
+        } else {
+          const int64_t a = ci / t.M;
+          const int c = pos[a];
+          if (c >= 0) {
+            const int64_t o = ci - a * t.M;
+            static_cast<__nv_bfloat16*>(t.tc.Bt)[o * RP + c] = b;
+            static_cast<__nv_bfloat16*>(t.tc.Bm)[(int64_t)c * t.M + o] = b;
+          }
+        }
+      }
     }
   }
 }
@@ -156,7 +222,7 @@ __device__ void eng_scale_unit(const EngTask& t, int u) {
   for (int e = threadIdx.x; e < 1024; e += blockDim.x) {
     const int64_t i = base + e;
     if (i >= t.n) break;
-    float v = __ldcg(t.x + i);
+    float v = t.x ? __ldcg(t.x + i) : 0.f;
     if (t.s) v *= t.s[i % t.len];
     t.out[i] = t.acc ? __ldcg(t.out + i) + v : v;
   }
@@ -166,12 +232,16 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
   __shared__ float As[kEK][kET + 1];
   __shared__ float Bs[kEK][kET + 1];
   __shared__ float red[32];
+  __shared__ int pos[RP];
   __shared__ int failed;
   if (threadIdx.x == 0) {
     failed = 0;
     TL_STAMP(2, 0);
   }
   __syncthreads();
+#ifdef TTC_TIMELINE
+  int nu = 0;
+#endif
   for (int ph = 0; ph < p.nphases; ++ph) {
     const int t0 = p.phase_begin[ph], t1 = p.phase_begin[ph + 1];
     int total = 0;
@@ -180,19 +250,33 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       int t = t0, uu = u;
       while (uu >= p.t[t].units) uu -= p.t[t++].units;
       const EngTask& k = p.t[t];
+#ifdef TTC_TIMELINE
+      if (threadIdx.x == 0 && nu < 8) {
+        g_tlu[blockIdx.x & 255][nu][0] = ph * 100 + t;
+        g_tlu[blockIdx.x & 255][nu][1] = gtimer();
+      }
+#endif
       switch (k.kind) {
-        case kEGemm: eng_gemm_unit(k, uu, As, Bs); break;
+        case kEGemm: eng_gemm_unit(k, uu, As, Bs, pos); break;
         case kEGemmFinal: eng_gemm_final_unit(k, uu); break;
         case kEColdot: eng_coldot_unit(k, uu, red); break;
         case kEScale: eng_scale_unit(k, uu); break;
         case kEPack:
-          tc_pack_unit(k.A, k.B, k.s, k.rd, k.N, k.M, k.tc, k.zero, uu);
+          tc_pack_unit(k.A, k.B, k.s, k.rd, k.N, k.M, k.tc, k.zero, k.pad_only, uu);
+          break;
+        case kEDd:
+          tc_dd_unit(k.tc, k.s, k.rd, k.out, k.acc);
           break;
         case kEUnpack:
-          tc_unpack_unit(k.tc, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
+          tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
           break;
         default: break;
       }
+#ifdef TTC_TIMELINE
+      __syncthreads();
+      if (threadIdx.x == 0 && nu < 8) g_tlu[blockIdx.x & 255][nu][2] = gtimer();
+      ++nu;
+#endif
     }
     if (threadIdx.x == 0) TL_STAMP(2, 1 + 2 * ph);
     if (ph + 1 < p.nphases && !eng_grid_barrier(p.slot, gridDim.x, &failed)) return;
@@ -240,7 +324,7 @@ void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t part
   // unit still walks at least a few K slices
   if (partial_ws && tiles < 256) {
     const int64_t want = ceil_div(256, tiles);
-    const int64_t maxs = ceil_div(g.k, 4 * kEK);
+    const int64_t maxs = ceil_div(g.k, kEK);
     splits = want < maxs ? want : maxs;
     if (splits > 16) splits = 16;
     if ((size_t)(splits * g.m * g.n) > partial_cap) splits = 1;
@@ -251,9 +335,21 @@ void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t part
   t->units = (int)(tiles * splits);
 }
 
+void eng_dd_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
+                 float* dDout, bool acc) {
+  t->kind = kEDd;
+  t->s = Dmid;
+  t->tc = tc;
+  t->rd = L.rd;
+  t->out = dDout;
+  t->acc = acc ? 1 : 0;
+  t->units = 1;
+}
+
 void eng_pack_task(EngTask* t, const LayerPlan& L, const float* A, const float* B,
-                   const float* Dmid, const TcPtrs& tc, bool zero_grads) {
+                   const float* Dmid, const TcPtrs& tc, bool zero_grads, bool pad_only) {
   t->kind = kEPack;
+  t->pad_only = pad_only ? 1 : 0;
   t->A = A;
   t->B = B;
   t->s = Dmid;
@@ -265,9 +361,10 @@ void eng_pack_task(EngTask* t, const LayerPlan& L, const float* A, const float* 
   t->units = (int)ceil_div((L.N + L.M) * RP + RP, kPackPer);
 }
 
-void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, float* dA, float* dB,
-                     float* dDout, bool acc) {
+void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
+                     float* dA, float* dB, float* dDout, bool acc) {
   t->kind = kEUnpack;
+  t->s = Dmid;
   t->tc = tc;
   t->rd = L.rd;
   t->N = (int)L.N;

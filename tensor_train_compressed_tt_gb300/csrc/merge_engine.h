@@ -15,7 +15,8 @@ enum EngKind {
   kEColdot = 2,    // out[c] (=|+=) sum_u X[u,c] Y[u,c] (masked by D == 0)
   kEScale = 3,     // out[i] (=|+=) in[i] * scale[i % len]
   kEPack = 4,      // tensor-core operands from A, B, D_d (+ zero gradient sums)
-  kEUnpack = 5     // compacted gradient sums -> dA, dB, dD_d
+  kEUnpack = 5,    // compacted gradient sums -> dA, dB, dD_d
+  kEDd = 6         // compacted dD_d sum -> dD_d only
 };
 
 struct EngTask {
@@ -39,6 +40,12 @@ struct EngTask {
   float* dA = nullptr;
   float* dB = nullptr;
   int rd = 0, N = 0, M = 0, zero = 0;
+  // kEGemm extras for the tensor-core path:
+  //  pack_side 1/2: the GEMM computes A (N x rd) / B (rd x M); its epilogue
+  //    also writes the compacted bf16 operands (tc, compaction from s = D_d).
+  //  gather 1/2: the operand that reads dA / dB (gather_op 0 = A, 1 = B)
+  //    reads the compacted token sums tc.dAc / tc.dBc instead.
+  int pack_side = 0, gather = 0, gather_op = 0, pad_only = 0;
 };
 
 constexpr int kEngMaxTasks = 24;
@@ -64,9 +71,11 @@ struct EngBuilder {
 void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap);
 void eng_gemm_final_task(EngTask* t, const EngTask& gemm);
 void eng_pack_task(EngTask* t, const LayerPlan& L, const float* A, const float* B,
-                   const float* Dmid, const TcPtrs& tc, bool zero_grads);
-void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, float* dA, float* dB,
-                     float* dDout, bool acc);
+                   const float* Dmid, const TcPtrs& tc, bool zero_grads, bool pad_only = false);
+void eng_dd_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
+                 float* dDout, bool acc);
+void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
+                     float* dA, float* dB, float* dDout, bool acc);
 
 // Launch (cooperative, one CTA per SM).  Returns cudaSuccess or the error.
 cudaError_t eng_launch(const EngProgram& p, cudaStream_t st);

@@ -51,9 +51,10 @@ constexpr int CH = 128;              // features / outputs per pipeline chunk
 constexpr int BOX = 16 * 1024;       // [128 rows][64 bf16] swizzled box
 constexpr int STAGE = 48 * 1024;     // 2 activation boxes + 16 KB operand
 constexpr int OPND = 32 * 1024;      // operand offset inside a stage
-constexpr int NSTAGE_F = 4;
+constexpr int NSTAGE_F = 3;
 constexpr int NSTAGE_B = 3;
 constexpr int NEPI = 8;              // epilogue warps
+constexpr int STG = 4096;            // one epilogue staging box: 32 rows x 128 bytes
 constexpr int NTHREADS = (2 + NEPI) * 32;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
@@ -104,6 +105,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
 // -DTTC_TIMELINE for performance investigation; the default build has none.
 #ifdef TTC_TIMELINE
 __device__ unsigned long long g_tl[3][256][16];
+__device__ unsigned long long g_tlu[256][8][3];  // engine units: (phase*100+task, start, end)
 #define TL_STAMP(k, slot) (g_tl[(k)][blockIdx.x & 255][(slot)] = gtimer())
 #else
 #define TL_STAMP(k, slot) ((void)0)
@@ -236,25 +238,57 @@ __device__ __forceinline__ void st_tile_half(uint8_t* tile, int row, int h, cons
   }
 }
 
-// 32 bf16 values to global (row-major), 16-byte pieces inside [0, ncols)
-__device__ __forceinline__ void st_row32(__nv_bfloat16* dst_row, int col0, int ncols,
-                                         const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (col0 + 8 * q + 8 > ncols) continue;
-    uint4 u;
-    u.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
-    u.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-    u.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
-    u.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
-    *reinterpret_cast<uint4*>(dst_row + col0 + 8 * q) = u;
-  }
+__device__ __forceinline__ void tma_store(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(su32(src)), "r"(c0), "r"(c1)
+      : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
+// Element-wise atomic add of a shared-memory box into global memory.
+__device__ __forceinline__ void tma_reduce_add(const CUtensorMap* map, const void* src, int c0,
+                                               int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(su32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N committed bulk groups of this thread still read smem.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Staging boxes are [32 rows][128 bytes] with the 128-byte swizzle the
+// tensor maps use: 16-byte chunk q of row r lives at r*128 + (q ^ (r & 7))*16.
+__device__ __forceinline__ void stage_bf16_32(uint8_t* box, int r, int piece,
+                                              const float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 u;
+    u.x = pack_bf16(v[8 * i + 0], v[8 * i + 1]);
+    u.y = pack_bf16(v[8 * i + 2], v[8 * i + 3]);
+    u.z = pack_bf16(v[8 * i + 4], v[8 * i + 5]);
+    u.w = pack_bf16(v[8 * i + 6], v[8 * i + 7]);
+    const int q = 4 * piece + i;
+    *reinterpret_cast<uint4*>(box + r * 128 + ((q ^ (r & 7)) << 4)) = u;
+  }
+}
+__device__ __forceinline__ void stage_f32_32(uint8_t* box, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 f = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    *reinterpret_cast<float4*>(box + r * 128 + ((q ^ (r & 7)) << 4)) = f;
+  }
 }
 
 // After the butterfly, lane l holds sum over the warp's 32 lanes of v[l].
@@ -286,7 +320,7 @@ struct BwdArgs {
   const int* rinfo;  // [0] = r', [1..64] = kept index of each compacted column
   __nv_bfloat16* dx;
   float* dAc;  // N x RP
-  float* dBc;  // RP x M
+  float* dBc;  // M x RP
   float* dDc;  // RP
 };
 
@@ -324,12 +358,14 @@ __device__ void tmem_free(uint32_t base) {
 __global__ void __launch_bounds__(NTHREADS, 1)
     tt_fwd_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_at,
-                  const __grid_constant__ CUtensorMap tm_bt, FwdArgs p) {
+                  const __grid_constant__ CUtensorMap tm_bt,
+                  const __grid_constant__ CUtensorMap tm_y, FwdArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1k(smem_raw);
   uint8_t* stages = base;
   uint8_t* zp_tile = base + NSTAGE_F * STAGE;
-  SmemCommon& S = *reinterpret_cast<SmemCommon*>(zp_tile + BOX);
+  uint8_t* staging = zp_tile + BOX;  // 2 boxes per epilogue warp
+  SmemCommon& S = *reinterpret_cast<SmemCommon*>(staging + NEPI * 2 * STG);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) TL_STAMP(0, 0);
 
@@ -445,9 +481,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int h = (warp - 2) >> 2;
     const int row = 32 * q + lane;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+    uint8_t* my_stg = staging + (warp - 2) * 2 * STG;
     int yc = 0, tl = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tl) {
-      const int64_t tok = (int64_t)tile * TILE + row;
       float v[32];
       if (!warp_wait(&S.z_full, tl & 1, abort_flag, 7)) break;
       tc_fence_after();
@@ -468,19 +504,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int yb = yc & 1;
         if (!warp_wait(&S.x_full[yb], (yc >> 1) & 1, abort_flag, 9)) { ok = false; break; }
         tc_fence_after();
-        __nv_bfloat16* yrow = p.y + tok * p.M;
+        uint8_t* box = my_stg + (yc & 1) * STG;
+        if (lane == 0) bulk_wait_read<1>();  // the store that used this box is done reading
+        __syncwarp();
 #pragma unroll
         for (int piece = 0; piece < 2; ++piece) {
           tmem_ld32(tmem + lane_off + F_Y + yb * 128 + 64 * h + 32 * piece, v);
-          if (tok < p.T) st_row32(yrow, c * CH + 64 * h + 32 * piece, p.M, v);
+          stage_bf16_32(box, lane, piece, v);
         }
         tc_fence_before();
+        fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.x_empty[yb]);
+        if (lane == 0) {
+          mbar_arrive(&S.x_empty[yb]);
+          const int col = c * CH + 64 * h;
+          if (col < p.M && (int64_t)tile * TILE + 32 * q < p.T)
+            tma_store(&tm_y, box, col, tile * TILE + 32 * q);
+          bulk_commit();  // one group per chunk, empty if skipped: keeps the box ring in step
+        }
       }
       if (!ok) break;
       if (warp == 2 && lane == 0) TL_STAMP(0, 5);
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -502,13 +548,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tm_dy,
                   const __grid_constant__ CUtensorMap tm_at,
                   const __grid_constant__ CUtensorMap tm_bm,
-                  const __grid_constant__ CUtensorMap tm_anr, BwdArgs p) {
+                  const __grid_constant__ CUtensorMap tm_anr,
+                  const __grid_constant__ CUtensorMap tm_dx,
+                  const __grid_constant__ CUtensorMap tm_dac,
+                  const __grid_constant__ CUtensorMap tm_dbc, BwdArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1k(smem_raw);
   uint8_t* stages = base;
   uint8_t* zp_tile = base + NSTAGE_B * STAGE;
   uint8_t* dz_tile = zp_tile + BOX;
-  SmemCommon& S = *reinterpret_cast<SmemCommon*>(dz_tile + BOX);
+  uint8_t* staging = dz_tile + BOX;  // one box per epilogue warp
+  SmemCommon& S = *reinterpret_cast<SmemCommon*>(staging + NEPI * STG);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) TL_STAMP(1, 0);
 
@@ -683,9 +733,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int row = 32 * q + lane;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int rprime = p.rinfo[0];
+    uint8_t* box = staging + (warp - 2) * STG;
     int wc = 0, xc = 0, tl = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tl) {
-      const int64_t tok = (int64_t)tile * TILE + row;
       float z[32], v[32];
       bool ok = true;
       // E1: z -> z' tile
@@ -712,12 +762,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.w_empty[wb]);
-        const int io = c * CH + row;
-        if (io < p.M) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int cc = 32 * h + j;
-            if (cc < rprime) atomicAdd(p.dBc + (int64_t)cc * p.M + io, v[j]);
+        // rows = outputs c*128 + 32q.., columns = compacted ranks 32h..
+        if (32 * h < rprime && c * CH + 32 * q < p.M) {
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          stage_f32_32(box, lane, v);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add(&tm_dbc, box, 32 * h, c * CH + 32 * q);
+            bulk_commit();
           }
         }
       }
@@ -749,15 +803,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int xb = xc & 1;
         if (!warp_wait(&S.x_full[xb], (xc >> 1) & 1, abort_flag, 27)) { ok = false; break; }
         tc_fence_after();
-        __nv_bfloat16* dxrow = p.dx + tok * p.N;
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
 #pragma unroll
         for (int piece = 0; piece < 2; ++piece) {
           tmem_ld32(tmem + lane_off + B_X + xb * 128 + 64 * h + 32 * piece, v);
-          if (tok < p.T) st_row32(dxrow, c * CH + 64 * h + 32 * piece, p.N, v);
+          stage_bf16_32(box, lane, piece, v);
         }
         tc_fence_before();
+        fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&S.x_empty[xb]);
+        if (lane == 0) {
+          mbar_arrive(&S.x_empty[xb]);
+          const int col = c * CH + 64 * h;
+          if (col < p.N && (int64_t)tile * TILE + 32 * q < p.T) {
+            tma_store(&tm_dx, box, col, tile * TILE + 32 * q);
+            bulk_commit();
+          }
+        }
         const int wb = wc & 1;
         if (!warp_wait(&S.w_full[wb], (wc >> 1) & 1, abort_flag, 28)) { ok = false; break; }
         tc_fence_after();
@@ -765,18 +828,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.w_empty[wb]);
-        const int jf = c * CH + row;
-        if (jf < p.N) {
-          float* dst = p.dAc + (int64_t)jf * RP + 32 * h;
-#pragma unroll
-          for (int g = 0; g < 8; ++g)
-            if (32 * h + 4 * g < rprime)
-              red_add_v4(dst + 4 * g, v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+        // rows = features c*128 + 32q.., columns = compacted ranks 32h..
+        if (32 * h < rprime && c * CH + 32 * q < p.N) {
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+          stage_f32_32(box, lane, v);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add(&tm_dac, box, 32 * h, c * CH + 32 * q);
+            bulk_commit();
+          }
         }
       }
       if (!ok) break;
       if (warp == 2 && lane == 0) TL_STAMP(1, 6);
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -792,20 +860,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // ==========================================================================
 constexpr int kPackPer = 1024;  // elements per engine unit
 
-__device__ void tc_pack_unit(const float* __restrict__ A, const float* __restrict__ B,
-                             const float* __restrict__ Dmid, int rd, int N, int M,
-                             const TcPtrs& p, int zero_grads, int unit) {
-  __shared__ int kept[RP];
-  __shared__ int rcount;
+// Compaction of the middle rank, computed by the whole block in parallel:
+// pos[a] = position of a among the nonzero entries of D (or -1), kept[c] = a
+// for c < r' (-1 beyond), *rcount = r'.  All threads must call it.
+__device__ void compaction_map(const float* __restrict__ D, int rd, int* pos, int* kept,
+                               int* rcount) {
+  __shared__ unsigned masks[2];
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int c = 0;
-    for (int a = 0; a < rd; ++a)
-      if (Dmid[a] != 0.f) kept[c++] = a;
-    rcount = c;
-    for (; c < RP; ++c) kept[c] = -1;
+  const int a = threadIdx.x;
+  bool nz = false;
+  if (a < RP) {
+    nz = a < rd && __ldcg(D + a) != 0.f;
+    const unsigned m = __ballot_sync(0xffffffffu, nz);
+    if ((a & 31) == 0) masks[a >> 5] = m;
   }
   __syncthreads();
+  if (a < RP) {
+    const unsigned m0 = masks[0], m1 = masks[1];
+    const int before = a < 32 ? __popc(m0 & ((1u << a) - 1u))
+                              : __popc(m0) + __popc(m1 & ((1u << (a - 32)) - 1u));
+    const int r = __popc(m0) + __popc(m1);
+    if (pos) pos[a] = nz ? before : -1;
+    if (kept) {
+      if (nz) kept[before] = a;
+      if (a >= r) kept[a] = -1;
+    }
+    if (a == 0 && rcount) *rcount = r;
+  }
+  __syncthreads();
+}
+
+// pad_only: write only the padding columns (c >= r') and the metadata; the
+// merge GEMMs' epilogues write the compacted columns themselves.
+__device__ void tc_pack_unit(const float* __restrict__ A, const float* __restrict__ B,
+                             const float* __restrict__ Dmid, int rd, int N, int M,
+                             const TcPtrs& p, int zero_grads, int pad_only, int unit) {
+  __shared__ int kept[RP];
+  __shared__ int rcount;
+  compaction_map(Dmid, rd, nullptr, kept, &rcount);
   const int64_t nA = (int64_t)N * RP, nB = (int64_t)M * RP;
   __nv_bfloat16* At = static_cast<__nv_bfloat16*>(p.At);
   __nv_bfloat16* Anr = static_cast<__nv_bfloat16*>(p.Anr);
@@ -815,18 +907,22 @@ __device__ void tc_pack_unit(const float* __restrict__ A, const float* __restric
     const int64_t i = (int64_t)unit * kPackPer + e;
     if (i < nA) {
       const int j = (int)(i / RP), c = (int)(i % RP);
-      const float v = kept[c] >= 0 ? __ldcg(A + (int64_t)j * rd + kept[c]) : 0.f;
-      const __nv_bfloat16 b = __float2bfloat16_rn(v);
-      Anr[i] = b;
-      At[(int64_t)c * N + j] = b;
+      if (!pad_only || kept[c] < 0) {
+        const float v = kept[c] >= 0 ? __ldcg(A + (int64_t)j * rd + kept[c]) : 0.f;
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        Anr[i] = b;
+        At[(int64_t)c * N + j] = b;
+      }
       if (zero_grads) p.dAc[i] = 0.f;
     } else if (i < nA + nB) {
       const int64_t k = i - nA;
       const int o = (int)(k / RP), c = (int)(k % RP);
-      const float v = kept[c] >= 0 ? __ldcg(B + (int64_t)kept[c] * M + o) : 0.f;
-      const __nv_bfloat16 b = __float2bfloat16_rn(v);
-      Bt[k] = b;
-      Bm[(int64_t)c * M + o] = b;
+      if (!pad_only || kept[c] < 0) {
+        const float v = kept[c] >= 0 ? __ldcg(B + (int64_t)kept[c] * M + o) : 0.f;
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        Bt[k] = b;
+        Bm[(int64_t)c * M + o] = b;
+      }
       if (zero_grads) p.dBc[k] = 0.f;
     } else if (i < nA + nB + RP) {
       const int c = (int)(i - nA - nB);
@@ -838,27 +934,35 @@ __device__ void tc_pack_unit(const float* __restrict__ A, const float* __restric
   }
 }
 
-__device__ void tc_unpack_unit(const TcPtrs& p, int rd, int N, int M, float* dA, float* dB,
-                               float* dDout, int acc, int unit) {
+// dD_d (uncompacted, prune convention, accumulate) from the token sum dDc.
+__device__ void tc_dd_unit(const TcPtrs& p, const float* Dmid, int rd, float* dDout, int acc) {
   __shared__ int pos[RP];
-  __syncthreads();
-  if (threadIdx.x < RP) pos[threadIdx.x] = -1;
-  __syncthreads();
-  if (threadIdx.x < RP && threadIdx.x < p.rinfo[0]) pos[p.rinfo[1 + threadIdx.x]] = threadIdx.x;
-  __syncthreads();
+  compaction_map(Dmid, rd, pos, nullptr, nullptr);
+  if (threadIdx.x < rd) {
+    const int a = threadIdx.x;
+    const int c = pos[a];
+    const float v = c >= 0 ? __ldcg(p.dDc + c) : 0.f;
+    dDout[a] = acc ? dDout[a] + v : v;
+  }
+}
+
+__device__ void tc_unpack_unit(const TcPtrs& p, const float* Dmid, int rd, int N, int M,
+                               float* dA, float* dB, float* dDout, int acc, int unit) {
+  __shared__ int pos[RP];
+  compaction_map(Dmid, rd, pos, nullptr, nullptr);
   const int64_t nA = (int64_t)N * rd, nB = (int64_t)rd * M;
   for (int e = threadIdx.x; e < kPackPer; e += blockDim.x) {
     const int64_t i = (int64_t)unit * kPackPer + e;
     if (i < nA) {
       const int j = (int)(i / rd), a = (int)(i % rd);
-      dA[i] = pos[a] >= 0 ? p.dAc[(int64_t)j * RP + pos[a]] : 0.f;
+      dA[i] = pos[a] >= 0 ? __ldcg(p.dAc + (int64_t)j * RP + pos[a]) : 0.f;
     } else if (i < nA + nB) {
       const int64_t k = i - nA;
       const int a = (int)(k / M), o = (int)(k % M);
-      dB[k] = pos[a] >= 0 ? p.dBc[(int64_t)pos[a] * M + o] : 0.f;
+      dB[k] = pos[a] >= 0 ? __ldcg(p.dBc + (int64_t)o * RP + pos[a]) : 0.f;
     } else if (i < nA + nB + rd) {
       const int a = (int)(i - nA - nB);
-      const float v = pos[a] >= 0 ? p.dDc[pos[a]] : 0.f;
+      const float v = pos[a] >= 0 ? __ldcg(p.dDc + pos[a]) : 0.f;
       dDout[a] = acc ? dDout[a] + v : v;
     }
   }
@@ -908,24 +1012,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor (outer x inner, row-major), box (box_outer x box_inner),
-// 128-byte swizzle, zero fill outside the tensor.
+// 2-D tensor (outer x inner, row-major) of bf16 or f32, box
+// (box_outer x box_inner), 128-byte swizzle, zero fill outside the tensor.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer) {
+              uint32_t box_outer, bool f32 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const uint64_t esz = f32 ? 4 : 2;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * esz};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemFwd = NSTAGE_F * STAGE + BOX + sizeof(SmemCommon) + 1024;
-constexpr size_t kSmemBwd = NSTAGE_B * STAGE + 2 * BOX + sizeof(SmemCommon) + 1024;
+constexpr size_t kSmemFwd = NSTAGE_F * STAGE + BOX + NEPI * 2 * STG + sizeof(SmemCommon) + 1024;
+constexpr size_t kSmemBwd = NSTAGE_B * STAGE + 2 * BOX + NEPI * STG + sizeof(SmemCommon) + 1024;
 static_assert(kSmemFwd <= 227 * 1024, "forward smem");
 static_assert(kSmemBwd <= 227 * 1024, "backward smem");
 
@@ -990,10 +1096,11 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-  CUtensorMap mx, mat, mbt;
+  CUtensorMap mx, mat, mbt, my;
   if (!make_map(&mx, x, L.N, T, 64, TILE) ||
       !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
-      !make_map(&mbt, at<void>(ws, off + t.Bt), RP, L.M, 64, CH))
+      !make_map(&mbt, at<void>(ws, off + t.Bt), RP, L.M, 64, CH) ||
+      !make_map(&my, y, L.M, T, 64, 32))
     return TT_ERR_CUDA;
   FwdArgs a;
   a.T = T;
@@ -1005,7 +1112,7 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   a.Dc = at<float>(ws, off + t.Dc);
   a.y = static_cast<__nv_bfloat16*>(y);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
-  tt_fwd_kernel<<<grid, NTHREADS, kSmemFwd, st>>>(mx, mat, mbt, a);
+  tt_fwd_kernel<<<grid, NTHREADS, kSmemFwd, st>>>(mx, mat, mbt, my, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
@@ -1016,11 +1123,14 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-  CUtensorMap mx, mdy, mat, mbm, manr;
+  CUtensorMap mx, mdy, mat, mbm, manr, mdx, mdac, mdbc;
   if (!make_map(&mx, x, L.N, T, 64, TILE) || !make_map(&mdy, dy, L.M, T, 64, TILE) ||
       !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
       !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
-      !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH))
+      !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH) ||
+      !make_map(&mdx, dx, L.N, T, 64, 32) ||
+      !make_map(&mdac, at<void>(ws, off + t.dAc), RP, L.N, 32, 32, true) ||
+      !make_map(&mdbc, at<void>(ws, off + t.dBc), RP, L.M, 32, 32, true))
     return TT_ERR_CUDA;
   BwdArgs a;
   a.T = T;
@@ -1036,7 +1146,7 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.dBc = at<float>(ws, off + t.dBc);
   a.dDc = at<float>(ws, off + t.dDc);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
-  tt_bwd_kernel<<<grid, NTHREADS, kSmemBwd, st>>>(mx, mdy, mat, mbm, manr, a);
+  tt_bwd_kernel<<<grid, NTHREADS, kSmemBwd, st>>>(mx, mdy, mat, mbm, manr, mdx, mdac, mdbc, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
@@ -1048,5 +1158,12 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
 #ifdef TTC_TIMELINE
 extern "C" int ttc_timeline_read(void* host, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(host, ttc::g_tl, bytes);
+}
+extern "C" int ttc_timeline_units_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, ttc::g_tlu, bytes);
+}
+extern "C" int ttc_timeline_units_clear(void) {
+  static unsigned long long zero[256 * 8 * 3];
+  return (int)cudaMemcpyToSymbol(ttc::g_tlu, zero, sizeof(zero));
 }
 #endif

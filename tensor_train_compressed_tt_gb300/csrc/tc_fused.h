@@ -14,7 +14,7 @@ struct TcPtrs {
   float* Dc = nullptr;   // [64] compacted middle diagonal (0 past r')
   int* rinfo = nullptr;  // [0] = r', [1 + c] = original index of column c
   float* dAc = nullptr;  // [N][64] sum over tokens of x^T dz
-  float* dBc = nullptr;  // [64][M] sum over tokens of z'^T dy
+  float* dBc = nullptr;  // [M][64] sum over tokens of dy^T z'
   float* dDc = nullptr;  // [64]    sum over tokens of z * dz'
 };
 TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t ws_off);

@@ -25,7 +25,7 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
   const int d = desc->d;
   if (d < 1 || d > TT_MAX_D) return TT_ERR_INVALID_ARG;
   if (desc->act != TT_DT_F32 && desc->act != TT_DT_BF16) return TT_ERR_INVALID_ARG;
-  if (desc->flags & ~TT_ACCUMULATE) return TT_ERR_INVALID_ARG;
+  if (desc->flags & ~(TT_ACCUMULATE | TT_REUSE_MERGE)) return TT_ERR_INVALID_ARG;
   LayerPlan p;
   p.d = d;
   p.K = 2 * d;
@@ -155,14 +155,23 @@ void chain_ptrs(const LayerPlan& L, const float* params, void* ws, const WsLayou
 }
 
 // ---- merge programs ---------------------------------------------------------
-// Forward merge: phase j computes P_j (input side) and P_{d+j} (output side);
-// a last phase packs the tensor-core operands when that path runs.
+// Forward merge: phase j computes P_j (input side) and P_{d+j} (output side).
+// On the tensor-core path the GEMMs that produce A and B also write the
+// compacted bf16 operands, and the first phase writes the padding and the
+// metadata (and zeroes the token sums for a backward call).
 tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
                             const float** P, bool pack, bool zero_grads, cudaStream_t st) {
   chain_ptrs(L, params, ws, w, P);
+  const float* Dmid = params + L.diag_off[L.d - 1];
+  const TcPtrs tc = pack ? tc_ptrs(L, ws, w.tc) : TcPtrs();
   EngBuilder b;
+  if (L.d == 1 && pack) {
+    b.begin_phase();
+    eng_pack_task(b.add(), L, P[0], P[1], Dmid, tc, zero_grads, false);
+  }
   for (int j = 1; j < L.d; ++j) {
     b.begin_phase();
+    if (pack && j == 1) eng_pack_task(b.add(), L, nullptr, nullptr, Dmid, tc, zero_grads, true);
     for (int k : {j, L.d + j}) {
       GemmArgs g;
       g.m = L.U[k - 1];
@@ -172,13 +181,17 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
       g.kscale = params + L.diag_off[k - 1]; g.klen = L.r[k];
       g.B = params + L.core_off[k]; g.sbk = g.n; g.sbn = 1;
       g.C = const_cast<float*>(P[k]); g.scm = g.n; g.scn = 1;
-      eng_gemm_task(b.add(), g, nullptr, 0);
+      EngTask* t = b.add();
+      eng_gemm_task(t, g, nullptr, 0);
+      if (pack && j == L.d - 1) {
+        t->pack_side = (k == j) ? 1 : 2;
+        t->tc = tc;
+        t->s = Dmid;
+        t->rd = L.rd;
+        t->N = (int)L.N;
+        t->M = (int)L.M;
+      }
     }
-  }
-  if (pack) {
-    b.begin_phase();
-    eng_pack_task(b.add(), L, P[L.d - 1], P[L.K - 1], params + L.diag_off[L.d - 1],
-                  tc_ptrs(L, ws, w.tc), zero_grads);
   }
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
@@ -195,12 +208,16 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
 // phase per step; split-K partials of dG_k are reduced in the next phase.
 tt_status run_merge_backward(const LayerPlan& L, const float* params, const float** P,
                              const float* dA, const float* dB, float* dparams, bool acc,
-                             bool unpack, void* ws, const WsLayout& w, cudaStream_t st) {
+                             bool unpack, bool rezero, void* ws, const WsLayout& w,
+                             cudaStream_t st) {
   EngBuilder b;
-  if (unpack) {
+  const int steps = L.d - 1;
+  const TcPtrs tc = unpack ? tc_ptrs(L, ws, w.tc) : TcPtrs();
+  if (unpack && steps == 0) {
+    // order 2: the merges are the cores themselves; unpack in full first
     b.begin_phase();
-    eng_unpack_task(b.add(), L, tc_ptrs(L, ws, w.tc), fptr(ws, w.dA), fptr(ws, w.dB),
-                    dparams + L.diag_off[L.d - 1], acc);
+    eng_unpack_task(b.add(), L, tc, params + L.diag_off[L.d - 1], fptr(ws, w.dA),
+                    fptr(ws, w.dB), dparams + L.diag_off[L.d - 1], acc);
   }
   struct Side {
     int k_first, k_last;
@@ -215,9 +232,11 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
   } sides[2] = {{0, L.d - 1, dA, nullptr, 0, 0, 0, EngTask(), false, nullptr, -1},
                 {L.d, L.K - 1, dB, nullptr, 2, 2, 0, EngTask(), false, nullptr, -1}};
   const int mode = acc ? kAccumulate : kStore;
-  const int steps = L.d - 1;
   for (int j = 0; j <= steps; ++j) {
     b.begin_phase();
+    if (unpack && steps > 0 && j == 0)
+      eng_dd_task(b.add(), L, tc, params + L.diag_off[L.d - 1], dparams + L.diag_off[L.d - 1],
+                  acc);
     for (Side& sd : sides) {
       // work left over from the previous step
       if (sd.has_pending) {
@@ -252,6 +271,15 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
         g.mode = mode;
         EngTask* t = b.add();
         eng_gemm_task(t, g, fptr(ws, w.part[sd.pi + (sd.flip & 1)]), w.part_cap);
+        const int gat = (unpack && j == 0) ? (&sd == &sides[0] ? 1 : 2) : 0;
+        if (gat) {  // read dA / dB straight from the compacted token sums
+          t->gather = gat;
+          t->gather_op = 1;
+          t->s = params + L.diag_off[L.d - 1];
+          t->tc = tc;
+          t->rd = L.rd;
+          t->M = (int)L.M;
+        }
         if (t->splits > 1) {
           sd.pending = *t;
           sd.has_pending = true;
@@ -263,13 +291,37 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
         h.kscale = sd.yscale; h.klen = rk1;
         h.B = params + L.core_off[k]; h.sbk = 1; h.sbn = ncol;
         h.C = dQ; h.scm = rk; h.scn = 1;
-        eng_gemm_task(b.add(), h, nullptr, 0);
+        EngTask* th = b.add();
+        eng_gemm_task(th, h, nullptr, 0);
+        if (gat) {
+          th->gather = gat;
+          th->gather_op = 0;
+          th->s = params + L.diag_off[L.d - 1];
+          th->tc = tc;
+          th->rd = L.rd;
+          th->M = (int)L.M;
+        }
         sd.dQ = dQ;
         sd.coldot_k = k;
         sd.Y = dQ;
         sd.yscale = params + L.diag_off[k - 1];
         sd.flip ^= 1;
       } else {
+        if (rezero && &sd == &sides[0]) {
+          // leave the token sums zeroed for the next backward that reuses
+          // this workspace's merge (they were last read before a barrier)
+          const float* bufs[3] = {tc.dAc, tc.dBc, tc.dDc};
+          const int64_t lens[3] = {L.N * 64, 64 * L.M, 64};
+          for (int q = 0; q < 3; ++q) {
+            EngTask* z = b.add();
+            z->kind = kEScale;
+            z->n = lens[q];
+            z->units = (int)((z->n + 1023) / 1024);
+            z->x = nullptr;
+            z->out = const_cast<float*>(bufs[q]);
+            z->acc = 0;
+          }
+        }
         // first core of the side
         EngTask* t = b.add();
         t->kind = kEScale;
@@ -298,8 +350,9 @@ tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, co
                         void* y, int ty, void* ws, const WsLayout& w, cudaStream_t st) {
   const float* P[kMaxK];
   const bool tc = use_tc(L, tx, ty);
+  const bool reuse = (L.flags & TT_REUSE_MERGE) != 0;
   prof_begin(kPhMerge, st);
-  tt_status s = run_merge_forward(L, params, ws, w, P, tc, false, st);
+  tt_status s = run_merge_forward(L, params, ws, w, P, tc, reuse, st);
   prof_end(kPhMerge, st);
   if (s != TT_OK) return s;
   prof_begin(kPhFwd, st);
@@ -392,10 +445,16 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
                          bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
   const float* P[kMaxK];
   const bool tc = use_tc(L, tx, tdy) && tdx == TT_DT_BF16;
-  prof_begin(kPhMerge, st);
-  tt_status s = run_merge_forward(L, params, ws, w, P, tc, true, st);
-  prof_end(kPhMerge, st);
-  if (s != TT_OK) return s;
+  const bool reuse = (L.flags & TT_REUSE_MERGE) != 0;
+  tt_status s = TT_OK;
+  if (reuse) {
+    chain_ptrs(L, params, ws, w, P);
+  } else {
+    prof_begin(kPhMerge, st);
+    s = run_merge_forward(L, params, ws, w, P, tc, true, st);
+    prof_end(kPhMerge, st);
+    if (s != TT_OK) return s;
+  }
   prof_begin(kPhBwd, st);
   if (tc)
     s = tc_backward(L, T, x, dy, dx, ws, w.tc, st);
@@ -404,8 +463,8 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   prof_end(kPhBwd, st);
   if (s != TT_OK) return s;
   prof_begin(kPhMergeBwd, st);
-  s = run_merge_backward(L, params, P, fptr(ws, w.dA), fptr(ws, w.dB), dparams, acc, tc, ws, w,
-                         st);
+  s = run_merge_backward(L, params, P, fptr(ws, w.dA), fptr(ws, w.dB), dparams, acc, tc,
+                         tc && reuse, ws, w, st);
   prof_end(kPhMergeBwd, st);
   return s;
 }

@@ -21,6 +21,7 @@ TT_MAX_D = 4
 TT_DT_F32 = 0
 TT_DT_BF16 = 1
 TT_ACCUMULATE = 1
+TT_REUSE_MERGE = 2
 
 STATUS = {
     0: "TT_OK",

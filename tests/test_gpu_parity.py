@@ -156,3 +156,31 @@ def test_full_size_identities_tt1024_4096():
     sub = oracle_layer(shape, inp.layers[0], inp.x[rows], inp.dy[rows])
     assert O.rel_err(out["y"][rows], sub["y"]) <= TOL[w.act]
     assert O.rel_err(out["dx"][rows], sub["dx"]) <= TOL[w.act]
+
+
+@pytest.mark.parametrize("name", ["tt768_bf16", "pruned768_3072_bf16", "tiny64_f32"])
+def test_reuse_merge_matches_default(name):
+    """TT_REUSE_MERGE: backward after forward on the same workspace, twice."""
+    import torch as th
+    from tensor_train_compressed_tt_gb300.layer import TTLinear
+    w = synth.WORKLOADS[name]
+    inp = synth.draw(w, seed=3, tokens=min(w.tokens, 700))
+    s = w.layers[0]
+    dt = th.bfloat16 if w.act == "bf16" else th.float32
+    params = th.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
+    x = th.from_numpy(inp.x).cuda().to(dt)
+    dy = th.from_numpy(inp.dy).cuda().to(dt)
+    ref = TTLinear(s.in_modes, s.out_modes, s.ranks, dt)
+    y0 = ref.forward(x, params)
+    dx0, g0 = ref.backward(x, dy, params)
+    reu = TTLinear(s.in_modes, s.out_modes, s.ranks, dt, reuse_merge=True)
+    ws = reu.workspace(x.shape[0])
+    for _ in range(2):
+        y1 = reu.forward(x, params, ws=ws)
+        dx1, g1 = reu.backward(x, dy, params, ws=ws)
+        dx2, g2 = reu.backward(x, dy, params, ws=ws)   # a second backward reuses again
+        th.cuda.synchronize()
+        assert th.equal(y0, y1)
+        assert th.equal(dx0, dx1) and th.equal(dx0, dx2)
+        np.testing.assert_allclose(g1.cpu().numpy(), g0.cpu().numpy(), rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(g2.cpu().numpy(), g0.cpu().numpy(), rtol=1e-5, atol=1e-6)
