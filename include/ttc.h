@@ -126,6 +126,20 @@ tt_status tt_backward(const tt_plan_t* plan, int64_t T, const void* x, const voi
                       const float* params, void* dx, float* dparams, void* ws,
                       size_t ws_bytes, void* stream);
 
+/* The forward above for callers that cannot allocate device memory (a
+ * plain-C host or plugin without a device allocator of its own, or a process
+ * that must not call cudaMalloc once running).  The CoMERA pages have no
+ * counterpart of this call; it only changes where scratch comes from.
+ * Scratch is a fixed 32 MiB device array inside the library, held on every
+ * GPU that loads it until exit; the caller passes only inputs and outputs.
+ * Returns TT_ERR_WORKSPACE when tt_workspace_size(plan, T) exceeds 32 MiB.
+ * The first call on a device looks the array's address up (once per device)
+ * and should come before any stream capture.  All calls share the array:
+ * calls that overlap on the GPU race on it.  Nothing in it needs to start at
+ * zero.  Otherwise behaves like tt_forward. */
+tt_status tt_forward_noalloc(const tt_plan_t* plan, int64_t T, const void* x,
+                             const float* params, void* y, void* stream);
+
 /* FFN pair: params_up / params_down are the two packed buffers. */
 tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,
                          const float* params_up, const float* params_down, void* y, void* ws,

@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             "tt_ffn_param_layout": [_P, ctypes.c_int, _P, _P, _P],
             "tt_workspace_size": [_P, _I64, _P],
             "tt_forward": [_P, _I64, _P, _P, _P, _P, _SZ, _P],
+            "tt_forward_noalloc": [_P, _I64, _P, _P, _P, _P],
             "tt_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_forward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
@@ -184,6 +185,11 @@ def tt_forward(plan: Plan, T: int, x: int, params: int, y: int, ws: int, ws_byte
     """Returns the tt_status code (0 = TT_OK)."""
     return lib().tt_forward(ctypes.c_void_p(plan.handle), int(T), x, params, y, ws,
                             int(ws_bytes), stream)
+
+
+def tt_forward_noalloc(plan: Plan, T: int, x: int, params: int, y: int, stream: int = 0) -> int:
+    """tt_forward with the library's fixed device scratch (no caller workspace)."""
+    return lib().tt_forward_noalloc(ctypes.c_void_p(plan.handle), int(T), x, params, y, stream)
 
 
 def tt_backward(plan: Plan, T: int, x: int, dy: int, params: int, dx: int, dparams: int,
