@@ -71,7 +71,8 @@ typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1 } tt_dtype;
  * (the forward keeps its intermediate results for the backward pass).  The
  * caller guarantees that a tt_forward call with the same plan, the same
  * params and the same workspace came before, with nothing else using the
- * workspace in between; then tt_backward skips re-merging the cores. */
+ * workspace in between; then tt_backward skips re-merging the cores.  FFN
+ * plans ignore it (their two layers share workspace regions). */
 #define TT_REUSE_MERGE 2u
 
 typedef struct tt_desc {

@@ -15,6 +15,7 @@ constexpr int kET = 32;   // GEMM tile (kET x kET outputs per unit)
 constexpr int kEK = 128;  // K slice staged per iteration (all loads in flight at once)
 constexpr int kBarSlots = 64;
 static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
+static_assert(sizeof(EngTask) % 16 == 0, "task descriptors are copied in 16-byte pieces");
 
 // Two-level grid barrier state per slot: 16 group counters and a root
 // counter (each on its own 128-byte line) plus the generation word.
@@ -75,20 +76,22 @@ __device__ void eng_pos_map(const EngTask& t, int* pos) {
 
 // Element f (flat index into dA (N x rd) or dB (rd x M)) read from the
 // compacted token sums.
-__device__ __forceinline__ float eng_gather(const EngTask& t, const int* pos, int64_t f) {
+// (32-bit index arithmetic: N*rd and rd*M stay far below 2^31.)
+__device__ __forceinline__ float eng_gather(const EngTask& t, const int* pos, int64_t f64) {
+  const unsigned f = (unsigned)f64;
   if (t.gather == 1) {
-    const int64_t j = f / t.rd;
-    const int c = pos[f - j * t.rd];
-    return c >= 0 ? __ldcg(t.tc.dAc + j * RP + c) : 0.f;
+    const unsigned j = f / (unsigned)t.rd;
+    const int c = pos[f - j * (unsigned)t.rd];
+    return c >= 0 ? __ldcg(t.tc.dAc + (size_t)j * RP + c) : 0.f;
   }
-  const int64_t a = f / t.M;
+  const unsigned a = f / (unsigned)t.M;
   const int c = pos[a];
-  return c >= 0 ? __ldcg(t.tc.dBc + (f - a * t.M) * RP + c) : 0.f;
+  return c >= 0 ? __ldcg(t.tc.dBc + (size_t)(f - a * (unsigned)t.M) * RP + c) : 0.f;
 }
 
 // One kET x kET output tile of C over one K slice.
 __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
-                              float (*Bs)[kET + 1], int* pos) {
+                              float (*Bs)[kET + 1], int* pos, float* ksc, float* csc) {
   if (t.pack_side || t.gather) eng_pos_map(t, pos);
   const GemmArgs& g = t.g;
   const int S = t.splits;
@@ -104,20 +107,36 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
   const float* B = static_cast<const float*>(g.B);
   const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
   float acc[2][2] = {};
+  // the periodic scales of this tile's columns, once per unit
+  if (tid < kET) {
+    const int64_t gn = n0 + tid;
+    csc[tid] = (g.cscale && gn < g.n) ? g.cscale[(unsigned)gn % (unsigned)g.clen] : 1.f;
+  }
   for (int64_t k0 = kb; k0 < ke; k0 += kEK) {
-#pragma unroll
+    // the periodic scales of this K slice, one index computation per thread
+    if (tid < kEK) {
+      const int64_t gk = k0 + tid;
+      ksc[tid] = (g.kscale && gk < ke) ? g.kscale[(unsigned)gk % (unsigned)g.klen] : 1.f;
+    }
+    __syncthreads();
+    // coalesced loads: walk the operand's unit-stride index fastest (the
+    // [kEK][kET+1] tiles are conflict-free either way)
+    const bool a_kfast = g.sak == 1 && g.sam != 1;
+    const bool b_kfast = g.sbk == 1 && g.sbn != 1;
+#pragma unroll 4
     for (int e = 0; e < (kET * kEK) / kEngThreads; ++e) {
       const int idx = tid + e * kEngThreads;
-      const int a_m = idx % kET, a_k = idx / kET;
+      const int a_m = a_kfast ? idx / kEK : idx % kET;
+      const int a_k = a_kfast ? idx % kEK : idx / kET;
       const int64_t gm = m0 + a_m, gk = k0 + a_k;
       float v = 0.f;
       if (gm < g.m && gk < ke) {
         const int64_t f = gm * g.sam + gk * g.sak;
-        v = (t.gather && t.gather_op == 0) ? eng_gather(t, pos, f) : __ldcg(A + f);
-        if (g.kscale) v *= g.kscale[gk % g.klen];
+        v = ((t.gather && t.gather_op == 0) ? eng_gather(t, pos, f) : __ldcg(A + f)) * ksc[a_k];
       }
       As[a_k][a_m] = v;
-      const int b_n = idx % kET, b_k = idx / kET;
+      const int b_n = b_kfast ? idx / kEK : idx % kET;
+      const int b_k = b_kfast ? idx % kEK : idx / kET;
       const int64_t gn = n0 + b_n, gk2 = k0 + b_k;
       float w = 0.f;
       if (gn < g.n && gk2 < ke) {
@@ -152,28 +171,28 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
         t.partial[((int64_t)ks * g.m + gm) * g.n + gn] = acc[i][j];
         continue;
       }
-      float v = acc[i][j];
+      float v = acc[i][j] * csc[tx * 2 + j];
       if (g.rscale) v *= g.rscale[gm];
-      if (g.cscale) v *= g.cscale[gn % g.clen];
       const int64_t ci = gm * g.scm + gn * g.scn;
       C[ci] = g.mode == kAccumulate ? __ldcg(C + ci) + v : v;
       if (t.pack_side) {
         // C is A (N x rd) or B (rd x M), row-major with scm = n, scn = 1
         const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        const unsigned cu = (unsigned)ci;
         if (t.pack_side == 1) {
-          const int64_t jj = ci / t.rd;
-          const int c = pos[ci - jj * t.rd];
+          const unsigned jj = cu / (unsigned)t.rd;
+          const int c = pos[cu - jj * (unsigned)t.rd];
           if (c >= 0) {
-            static_cast<__nv_bfloat16*>(t.tc.Anr)[jj * RP + c] = b;
-            static_cast<__nv_bfloat16*>(t.tc.At)[(int64_t)c * t.N + jj] = b;
+            static_cast<__nv_bfloat16*>(t.tc.Anr)[(size_t)jj * RP + c] = b;
+            static_cast<__nv_bfloat16*>(t.tc.At)[(size_t)c * t.N + jj] = b;
           }
         } else {
-          const int64_t a = ci / t.M;
+          const unsigned a = cu / (unsigned)t.M;
           const int c = pos[a];
           if (c >= 0) {
-            const int64_t o = ci - a * t.M;
-            static_cast<__nv_bfloat16*>(t.tc.Bt)[o * RP + c] = b;
-            static_cast<__nv_bfloat16*>(t.tc.Bm)[(int64_t)c * t.M + o] = b;
+            const unsigned o = cu - a * (unsigned)t.M;
+            static_cast<__nv_bfloat16*>(t.tc.Bt)[(size_t)o * RP + c] = b;
+            static_cast<__nv_bfloat16*>(t.tc.Bm)[(size_t)c * t.M + o] = b;
           }
         }
       }
@@ -185,11 +204,11 @@ __device__ void eng_gemm_final_unit(const EngTask& t, int u) {
   const GemmArgs& g = t.g;
   const int64_t i = (int64_t)u * kEngThreads + threadIdx.x;
   if (i >= g.m * g.n) return;
-  const int64_t gm = i / g.n, gn = i % g.n;
+  const unsigned gm = (unsigned)i / (unsigned)g.n, gn = (unsigned)i - gm * (unsigned)g.n;
   float v = 0.f;
   for (int ks = 0; ks < t.splits; ++ks) v += __ldcg(t.partial + (int64_t)ks * g.m * g.n + i);
   if (g.rscale) v *= g.rscale[gm];
-  if (g.cscale) v *= g.cscale[gn % g.clen];
+  if (g.cscale) v *= g.cscale[gn % (unsigned)g.clen];
   float* C = static_cast<float*>(g.C);
   const int64_t ci = gm * g.scm + gn * g.scn;
   C[ci] = g.mode == kAccumulate ? __ldcg(C + ci) + v : v;
@@ -223,7 +242,7 @@ __device__ void eng_scale_unit(const EngTask& t, int u) {
     const int64_t i = base + e;
     if (i >= t.n) break;
     float v = t.x ? __ldcg(t.x + i) : 0.f;
-    if (t.s) v *= t.s[i % t.len];
+    if (t.s) v *= t.s[(unsigned)i % (unsigned)t.len];
     t.out[i] = t.acc ? __ldcg(t.out + i) + v : v;
   }
 }
@@ -233,6 +252,9 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
   __shared__ float Bs[kEK][kET + 1];
   __shared__ float red[32];
   __shared__ int pos[RP];
+  __shared__ float ksc[kEK];
+  __shared__ float csc[kET];
+  __shared__ __align__(16) EngTask task;  // the current unit's task, copied once
   __shared__ int failed;
   if (threadIdx.x == 0) {
     failed = 0;
@@ -249,7 +271,16 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       int t = t0, uu = u;
       while (uu >= p.t[t].units) uu -= p.t[t++].units;
-      const EngTask& k = p.t[t];
+      // copy the task descriptor out of the parameter block once per unit:
+      // every later field read is then a shared-memory read
+      __syncthreads();
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(&p.t[t]);
+        uint4* dst = reinterpret_cast<uint4*>(&task);
+        for (int i = threadIdx.x; i < (int)(sizeof(EngTask) / 16); i += blockDim.x) dst[i] = src[i];
+      }
+      __syncthreads();
+      const EngTask& k = task;
 #ifdef TTC_TIMELINE
       if (threadIdx.x == 0 && nu < 8) {
         g_tlu[blockIdx.x & 255][nu][0] = ph * 100 + t;
@@ -257,7 +288,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       }
 #endif
       switch (k.kind) {
-        case kEGemm: eng_gemm_unit(k, uu, As, Bs, pos); break;
+        case kEGemm: eng_gemm_unit(k, uu, As, Bs, pos, ksc, csc); break;
         case kEGemmFinal: eng_gemm_final_unit(k, uu); break;
         case kEColdot: eng_coldot_unit(k, uu, red); break;
         case kEScale: eng_scale_unit(k, uu); break;

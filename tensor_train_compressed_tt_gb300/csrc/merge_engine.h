@@ -19,7 +19,7 @@ enum EngKind {
   kEDd = 6         // compacted dD_d sum -> dD_d only
 };
 
-struct EngTask {
+struct alignas(16) EngTask {
   int kind = 0;
   int units = 0;
   int splits = 1;       // kEGemm / kEGemmFinal

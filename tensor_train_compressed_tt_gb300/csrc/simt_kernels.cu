@@ -190,6 +190,37 @@ __global__ void gelu_bwd_kernel(int64_t n, const float* h, float* da) {
     da[i] *= gelu_grad_f(h[i]);
 }
 
+// bf16 in / bf16 out, 8 elements per thread (n is a multiple of 8)
+__global__ void gelu_fwd_bf16_kernel(int64_t n8, const uint4* __restrict__ h, uint4* a) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint4 u = h[i];
+    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(p[k]);
+      p[k] = __floats2bfloat162_rn(gelu_f(f.x), gelu_f(f.y));
+    }
+    a[i] = u;
+  }
+}
+
+__global__ void gelu_bwd_bf16_kernel(int64_t n8, const uint4* __restrict__ h, uint4* da) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    uint4 uh = h[i], ud = da[i];
+    const __nv_bfloat162* ph = reinterpret_cast<const __nv_bfloat162*>(&uh);
+    __nv_bfloat162* pd = reinterpret_cast<__nv_bfloat162*>(&ud);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 fh = __bfloat1622float2(ph[k]);
+      const float2 fd = __bfloat1622float2(pd[k]);
+      pd[k] = __floats2bfloat162_rn(fd.x * gelu_grad_f(fh.x), fd.y * gelu_grad_f(fh.y));
+    }
+    da[i] = ud;
+  }
+}
+
 unsigned grid_for(int64_t n, int threads) {
   int64_t b = (n + threads - 1) / threads;
   if (b > 65535LL * 8) b = 65535LL * 8;
@@ -239,6 +270,24 @@ cudaError_t gelu_fwd(int64_t n, const float* h, void* a, int ta, cudaStream_t st
         <<<grid_for(n, 256), 256, 0, st>>>(n, h, static_cast<__nv_bfloat16*>(a));
   else
     gelu_fwd_kernel<float><<<grid_for(n, 256), 256, 0, st>>>(n, h, static_cast<float*>(a));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t gelu_fwd_bf16(int64_t n, const void* h, void* a, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (n % 8) return cudaErrorInvalidValue;
+  gelu_fwd_bf16_kernel<<<grid_for(n / 8, 256), 256, 0, st>>>(
+      n / 8, static_cast<const uint4*>(h), static_cast<uint4*>(a));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t gelu_bwd_bf16(int64_t n, const void* h, void* da, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (n % 8) return cudaErrorInvalidValue;
+  gelu_bwd_bf16_kernel<<<grid_for(n / 8, 256), 256, 0, st>>>(
+      n / 8, static_cast<const uint4*>(h), static_cast<uint4*>(da));
   count_launches(1);
   return cudaGetLastError();
 }

@@ -98,9 +98,7 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   for (int k = 0; k < L.K; ++k) {
     size_t n = chain_len(L, k);
     if (n > qmax) qmax = n;
-    size_t core = (size_t)L.r[k] * L.s[k] * L.r[k + 1];
     size_t pf = eng_partial_floats(L.r[k], (int64_t)L.s[k] * L.r[k + 1], 0);
-    (void)core;
     if (pf > pmax) pmax = pf;
     w->P[k] = (k == 0 || k == L.d) ? 0 : take(n * sizeof(float));
   }
@@ -122,12 +120,18 @@ struct FfnLayout {
   size_t h = 0, a = 0, da = 0, end = 0;
 };
 
+// Both layers of a bf16 FFN pair run on the tensor-core path with bf16
+// intermediates h, a = GELU(h), da; otherwise on the SIMT path in f32.
+bool ffn_tc(const tt_plan_s* p) {
+  return p->L[0].act == TT_DT_BF16 && tc_supported(p->L[0]) && tc_supported(p->L[1]);
+}
+
 size_t ffn_layout(const tt_plan_s* p, int64_t T, FfnLayout* f) {
-  // the FFN layers run their token passes on f32 intermediates (SIMT path)
-  size_t e0 = layer_layout(p->L[0], T, 256, &f->up, true);
-  size_t e1 = layer_layout(p->L[1], T, 256, &f->down, true);
+  const bool tc = ffn_tc(p);
+  size_t e0 = layer_layout(p->L[0], T, 256, &f->up, !tc);
+  size_t e1 = layer_layout(p->L[1], T, 256, &f->down, !tc);
   size_t off = align_up(e0 > e1 ? e0 : e1, 256);
-  const size_t hb = (size_t)T * p->L[0].M * sizeof(float);
+  const size_t hb = (size_t)T * p->L[0].M * (tc ? 2 : sizeof(float));
   f->h = off;
   off = align_up(off + hb, 256);
   f->a = off;
@@ -531,6 +535,10 @@ tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out) {
   s = build_layer(down, &b);
   if (s != TT_OK) return s;
   if (a.M != b.N || a.act != b.act || a.flags != b.flags) return TT_ERR_INVALID_ARG;
+  // the two layers share workspace regions, so a merge cannot be kept
+  // from the forward to the backward: TT_REUSE_MERGE has no effect here
+  a.flags &= ~TT_REUSE_MERGE;
+  b.flags &= ~TT_REUSE_MERGE;
   tt_plan_s* p = new (std::nothrow) tt_plan_s();
   if (!p) return TT_ERR_INVALID_ARG;
   p->kind = 1;
@@ -624,6 +632,14 @@ tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,
   const LayerPlan& D = plan->L[1];
   float* h = fptr(ws, f.h);
   float* a = fptr(ws, f.a);
+  if (ffn_tc(plan)) {
+    s = layer_forward(U, T, x, TT_DT_BF16, params_up, h, TT_DT_BF16, ws, f.up, st);
+    if (s != TT_OK) return s;
+    prof_begin(kPhElem, st);
+    TT_CUDA(gelu_fwd_bf16(T * U.M, h, a, st));
+    prof_end(kPhElem, st);
+    return layer_forward(D, T, a, TT_DT_BF16, params_down, y, TT_DT_BF16, ws, f.down, st);
+  }
   s = layer_forward(U, T, x, U.act, params_up, h, TT_DT_F32, ws, f.up, st);
   if (s != TT_OK) return s;
   prof_begin(kPhElem, st);
@@ -653,6 +669,25 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
   float* h = fptr(ws, f.h);
   float* a = fptr(ws, f.a);
   float* da = fptr(ws, f.da);
+  if (ffn_tc(plan)) {
+    if (T > 0) {
+      s = layer_forward(U, T, x, TT_DT_BF16, params_up, h, TT_DT_BF16, ws, f.up, st);
+      if (s != TT_OK) return s;
+      prof_begin(kPhElem, st);
+      TT_CUDA(gelu_fwd_bf16(T * U.M, h, a, st));
+      prof_end(kPhElem, st);
+    }
+    s = layer_backward(D, T, a, TT_DT_BF16, dy, TT_DT_BF16, params_down, da, TT_DT_BF16,
+                       dparams_down, acc, ws, f.down, st);
+    if (s != TT_OK) return s;
+    if (T > 0) {
+      prof_begin(kPhElem, st);
+      TT_CUDA(gelu_bwd_bf16(T * U.M, h, da, st));
+      prof_end(kPhElem, st);
+    }
+    return layer_backward(U, T, x, TT_DT_BF16, da, TT_DT_BF16, params_up, dx, TT_DT_BF16,
+                          dparams_up, acc, ws, f.up, st);
+  }
   if (T > 0) {
     s = layer_forward(U, T, x, U.act, params_up, h, TT_DT_F32, ws, f.up, st);
     if (s != TT_OK) return s;

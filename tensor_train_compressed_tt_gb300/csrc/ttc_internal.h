@@ -84,5 +84,8 @@ cudaError_t scale_periodic(int64_t n, const float* in, const float* scale, int l
 cudaError_t gelu_fwd(int64_t n, const float* h, void* a, int ta, cudaStream_t st);
 // dh = da * GELU'(h), in place over da (f32)
 cudaError_t gelu_bwd(int64_t n, const float* h, float* da, cudaStream_t st);
+// bf16 variants (n a multiple of 8, 16-byte aligned buffers)
+cudaError_t gelu_fwd_bf16(int64_t n, const void* h, void* a, cudaStream_t st);
+cudaError_t gelu_bwd_bf16(int64_t n, const void* h, void* da, cudaStream_t st);
 
 }  // namespace ttc

@@ -122,8 +122,9 @@ def test_accumulate_flag_adds_into_dparams():
     g2 = base.clone()
     acc.backward(x, dy, params, dparams=g2)
     th.cuda.synchronize()
-    np.testing.assert_allclose((g2 - base).cpu().numpy(), g1.cpu().numpy(), rtol=1e-5,
-                               atol=1e-6)
+    # the token sums are reduced with atomics, so the two runs may add in a
+    # different order: compare norm-wise
+    assert O.rel_err((g2 - base).cpu().numpy(), g1.cpu().numpy()) <= 1e-5
 
 
 def test_all_zero_middle_link_removes_layer():
@@ -182,5 +183,6 @@ def test_reuse_merge_matches_default(name):
         th.cuda.synchronize()
         assert th.equal(y0, y1)
         assert th.equal(dx0, dx1) and th.equal(dx0, dx2)
-        np.testing.assert_allclose(g1.cpu().numpy(), g0.cpu().numpy(), rtol=1e-5, atol=1e-6)
-        np.testing.assert_allclose(g2.cpu().numpy(), g0.cpu().numpy(), rtol=1e-5, atol=1e-6)
+        # atomically reduced token sums: equal up to summation order
+        assert O.rel_err(g1.cpu().numpy(), g0.cpu().numpy()) <= 1e-5
+        assert O.rel_err(g2.cpu().numpy(), g0.cpu().numpy()) <= 1e-5
