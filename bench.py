@@ -92,6 +92,26 @@ def algorithmic(w, T):
             "bwd_bytes": int(bwd_b)}
 
 
+def all_reduce_scalar(v, op, device=None):
+    """Reduce one number over all ranks ("max", "min" or "sum"); identity
+    without an initialised process group.  NCCL groups reduce on the GPU,
+    others (gloo) on the CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    ops = {"max": dist.ReduceOp.MAX, "min": dist.ReduceOp.MIN, "sum": dist.ReduceOp.SUM}
+    dist.all_reduce(t, op=ops[op])
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank, world, step_ms_max):
+    """Tokens of all ranks per second, timed by the slowest rank."""
+    return world * tokens_per_rank / (step_ms_max * 1e-3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -369,11 +389,7 @@ def run_ours(args, w):
         torch.cuda.synchronize(dev)
         per = (time.perf_counter() - t0) / 5
         K = int(min(100000, max(20, args.target_seconds / max(per, 1e-6))))
-        if world > 1:
-            import torch.distributed as dist
-            kt = torch.tensor([K], device=dev)
-            dist.all_reduce(kt, op=dist.ReduceOp.MIN)
-            K = int(kt.item())
+        K = int(all_reduce_scalar(K, "min", dev))
     else:
         K = args.steps
     barrier()
@@ -394,12 +410,7 @@ def run_ours(args, w):
     barrier()
     launches = int(ttc.lib().tt_launch_count() - l0)
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1) / K
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = all_reduce_scalar(ev0.elapsed_time(ev1) / K, "max", dev)
     ttc.check(ttc.tt_get_device_status(sh), "device status after timed region")
 
     # ---- per-phase CUDA-event timing of the library's kernels (same steps)
@@ -439,7 +450,7 @@ def run_ours(args, w):
                 "traffic": traffic_for(dom, w.name),
                 "algorithmic_bytes_per_launch": bytes_of[dom]}
     t_roof = alg["bytes"] / (peak * 1e9)
-    value = world * T / (ms * 1e-3)
+    value = whole_job_rate(T, world, ms)
 
     # ---- end to end through the C ABI with host buffers
     e2e = None
@@ -473,13 +484,8 @@ def run_ours(args, w):
             e2e_step()
         a1.record(stream)
         barrier()
-        ems = a0.elapsed_time(a1) / Ke
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ems], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * T / (ems * 1e-3), "unit": "tokens/s",
+        ems = all_reduce_scalar(a0.elapsed_time(a1) / Ke, "max", dev)
+        e2e = {"value": whole_job_rate(T, world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(hx.numel() * e + hdy.numel() * e),
                "d2h_bytes_per_step": int(hy.numel() * e + hdx.numel() * e + 4 * sum(n_par)),
                "ms_per_step": ems, "steps": Ke}

@@ -1,0 +1,57 @@
+"""The benchmark's multi-rank bookkeeping on CPU (gloo, world size 2).
+
+Each rank runs its own replica; the step time is the slowest rank's and the
+value counts the tokens of every rank.
+"""
+
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms = bench.all_reduce_scalar(1.5 + rank, "max")
+    k = bench.all_reduce_scalar(100 - 7 * rank, "min")
+    tot = bench.all_reduce_scalar(rank + 1, "sum")
+    rate = bench.whole_job_rate(16384, world, ms)
+    q.put((rank, ms, k, tot, rate))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_like_the_benchmark():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, k, tot, rate in res:
+        assert ms == 2.5 and k == 93 and tot == 3
+        assert rate == pytest.approx(2 * 16384 / 2.5e-3)
+
+
+def test_single_process_is_identity():
+    import bench
+    assert bench.all_reduce_scalar(3.25, "max") == 3.25
+    assert bench.whole_job_rate(100, 1, 1.0) == pytest.approx(1e5)
