@@ -42,6 +42,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--eager", action="store_true",
+                   help="launch every step from the host instead of replaying a CUDA graph")
     p.add_argument("--no-reuse", action="store_true",
                    help="re-merge the cores in the backward instead of reusing the forward's")
     p.add_argument("--target-seconds", type=float, default=3.0,
@@ -354,7 +356,7 @@ def run_ours(args, w):
     sh = int(stream.cuda_stream)
     wsp, wsn = ws.data_ptr(), ws.numel()
 
-    def step(i):
+    def step(i, sh=sh):
         x, dy, y, dx = sets[i % nsets]
         if w.ffn:
             ttc.check(ttc.tt_ffn_forward(mod.plan, T, x.data_ptr(), params[0].data_ptr(),
@@ -381,11 +383,40 @@ def run_ours(args, w):
         step(i)
     ttc.check(ttc.tt_get_device_status(sh), "device status after warm-up")
     barrier()
+
+    # One CUDA graph per rotating input set holds a whole fwd+bwd step, as
+    # the CoMERA pages capture their training step; --eager launches from
+    # the host every time instead.
+    graphs, graph_note, launches_per_step = None, "eager", None
+    if not args.eager:
+        try:
+            graphs = []
+            for j in range(nsets):
+                g = torch.cuda.CUDAGraph()
+                c0 = ttc.lib().tt_launch_count()
+                with torch.cuda.graph(g):
+                    step(j, int(torch.cuda.current_stream().cuda_stream))
+                launches_per_step = int(ttc.lib().tt_launch_count() - c0)
+                graphs.append(g)
+            for j in range(max(3, nsets)):
+                graphs[j % nsets].replay()
+            torch.cuda.synchronize(dev)
+            ttc.check(ttc.tt_get_device_status(sh), "device status after graph warm-up")
+            graph_note = "cuda_graph"
+        except Exception as e:  # capture unsupported: time the eager loop
+            graphs, graph_note = None, f"eager (graph capture failed: {type(e).__name__}: {e})"
+            torch.cuda.synchronize(dev)
+
+    def run(i):
+        if graphs is not None:
+            graphs[i % nsets].replay()
+        else:
+            step(i)
     # choose K for a timed region of about target-seconds when not given
     if args.steps is None:
         t0 = time.perf_counter()
         for i in range(5):
-            step(i)
+            run(i)
         torch.cuda.synchronize(dev)
         per = (time.perf_counter() - t0) / 5
         K = int(min(100000, max(20, args.target_seconds / max(per, 1e-6))))
@@ -405,13 +436,27 @@ def run_ours(args, w):
     barrier()
     ev0.record(stream)
     for i in range(K):
-        step(i)
+        run(i)
     ev1.record(stream)
     barrier()
     launches = int(ttc.lib().tt_launch_count() - l0)
+    if graphs is not None:
+        launches = K * launches_per_step  # replays launch without the host counter
     clk = clocks.stop()
     ms = all_reduce_scalar(ev0.elapsed_time(ev1) / K, "max", dev)
     ttc.check(ttc.tt_get_device_status(sh), "device status after timed region")
+
+    # the same steps launched eagerly, for reference
+    Ke = min(K, 2000)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(Ke):
+        step(i)
+    e1.record(stream)
+    barrier()
+    ms_eager = all_reduce_scalar(e0.elapsed_time(e1) / Ke, "max", dev)
 
     # ---- per-phase CUDA-event timing of the library's kernels (same steps)
     ttc.lib().tt_profile_enable(1)
@@ -510,7 +555,9 @@ def run_ours(args, w):
                        "l2": f"{nsets} rotating input/output sets of {set_bytes / 1e6:.1f} MB "
                              f"(> 2x L2 of {l2 / 1e6:.0f} MB)",
                        "parallelism": f"replicas x{world}",
-                       "reuse_merge": (not args.no_reuse) and not w.ffn},
+                       "reuse_merge": (not args.no_reuse) and not w.ffn,
+                       "launch": graph_note},
+            "ms_per_step_eager": ms_eager,
             "roofline": roof,
             "roofline_step": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3),
                               "algorithmic_bytes": alg["bytes"], "algorithmic_flop": alg["flop"],

@@ -15,7 +15,7 @@ constexpr int kET = 32;   // GEMM tile (kET x kET outputs per unit)
 constexpr int kEK = 128;  // K slice staged per iteration (all loads in flight at once)
 constexpr int kBarSlots = 64;
 static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
-static_assert(sizeof(EngTask) % 16 == 0, "task descriptors are copied in 16-byte pieces");
+static_assert(sizeof(EngProgram) % 16 == 0, "the program is copied in 16-byte pieces");
 
 // Two-level grid barrier state per slot: 16 group counters and a root
 // counter (each on its own 128-byte line) plus the generation word.
@@ -120,30 +120,41 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
     }
     __syncthreads();
     // coalesced loads: walk the operand's unit-stride index fastest (the
-    // [kEK][kET+1] tiles are conflict-free either way)
+    // [kEK][kET+1] tiles are conflict-free either way).  All 2 x 16 loads of
+    // a thread are issued before any is used, so they overlap in flight.
+    constexpr int kPer = (kET * kEK) / kEngThreads;
     const bool a_kfast = g.sak == 1 && g.sam != 1;
     const bool b_kfast = g.sbk == 1 && g.sbn != 1;
-#pragma unroll 4
-    for (int e = 0; e < (kET * kEK) / kEngThreads; ++e) {
+    float va[kPer], vb[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
       const int idx = tid + e * kEngThreads;
       const int a_m = a_kfast ? idx / kEK : idx % kET;
       const int a_k = a_kfast ? idx % kEK : idx / kET;
       const int64_t gm = m0 + a_m, gk = k0 + a_k;
-      float v = 0.f;
+      va[e] = 0.f;
       if (gm < g.m && gk < ke) {
         const int64_t f = gm * g.sam + gk * g.sak;
-        v = ((t.gather && t.gather_op == 0) ? eng_gather(t, pos, f) : __ldcg(A + f)) * ksc[a_k];
+        va[e] = (t.gather && t.gather_op == 0) ? eng_gather(t, pos, f) : __ldcg(A + f);
       }
-      As[a_k][a_m] = v;
       const int b_n = b_kfast ? idx / kEK : idx % kET;
       const int b_k = b_kfast ? idx % kEK : idx / kET;
       const int64_t gn = n0 + b_n, gk2 = k0 + b_k;
-      float w = 0.f;
+      vb[e] = 0.f;
       if (gn < g.n && gk2 < ke) {
         const int64_t f = gk2 * g.sbk + gn * g.sbn;
-        w = (t.gather && t.gather_op == 1) ? eng_gather(t, pos, f) : __ldcg(B + f);
+        vb[e] = (t.gather && t.gather_op == 1) ? eng_gather(t, pos, f) : __ldcg(B + f);
       }
-      Bs[b_k][b_n] = w;
+    }
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int idx = tid + e * kEngThreads;
+      const int a_m = a_kfast ? idx / kEK : idx % kET;
+      const int a_k = a_kfast ? idx % kEK : idx / kET;
+      As[a_k][a_m] = va[e] * ksc[a_k];
+      const int b_n = b_kfast ? idx / kEK : idx % kET;
+      const int b_k = b_kfast ? idx % kEK : idx / kET;
+      Bs[b_k][b_n] = vb[e];
     }
     __syncthreads();
     const int kn = (int)(ke - k0 < kEK ? ke - k0 : kEK);
@@ -216,6 +227,7 @@ __device__ void eng_gemm_final_unit(const EngTask& t, int u) {
 
 __device__ void eng_coldot_unit(const EngTask& t, int c, float* red) {
   float s = 0.f;
+#pragma unroll 8
   for (int64_t u = threadIdx.x; u < t.n; u += blockDim.x)
     s += __ldcg(t.x + u * t.sx + c) * __ldcg(t.y + u * t.sy + c);
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -247,15 +259,22 @@ __device__ void eng_scale_unit(const EngTask& t, int u) {
   }
 }
 
-__global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant__ EngProgram p) {
+__global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant__ EngProgram prog) {
   __shared__ float As[kEK][kET + 1];
   __shared__ float Bs[kEK][kET + 1];
   __shared__ float red[32];
   __shared__ int pos[RP];
   __shared__ float ksc[kEK];
   __shared__ float csc[kET];
-  __shared__ __align__(16) EngTask task;  // the current unit's task, copied once
+  __shared__ __align__(16) EngProgram p;  // the whole program, copied once per CTA
   __shared__ int failed;
+  pdl_wait();  // params and workspace may be written by the previous grid
+  pdl_trigger();
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(&prog);
+    uint4* dst = reinterpret_cast<uint4*>(&p);
+    for (int i = threadIdx.x; i < (int)(sizeof(EngProgram) / 16); i += blockDim.x) dst[i] = src[i];
+  }
   if (threadIdx.x == 0) {
     failed = 0;
     TL_STAMP(2, 0);
@@ -271,16 +290,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       int t = t0, uu = u;
       while (uu >= p.t[t].units) uu -= p.t[t++].units;
-      // copy the task descriptor out of the parameter block once per unit:
-      // every later field read is then a shared-memory read
-      __syncthreads();
-      {
-        const uint4* src = reinterpret_cast<const uint4*>(&p.t[t]);
-        uint4* dst = reinterpret_cast<uint4*>(&task);
-        for (int i = threadIdx.x; i < (int)(sizeof(EngTask) / 16); i += blockDim.x) dst[i] = src[i];
-      }
-      __syncthreads();
-      const EngTask& k = task;
+      const EngTask& k = p.t[t];
 #ifdef TTC_TIMELINE
       if (threadIdx.x == 0 && nu < 8) {
         g_tlu[blockIdx.x & 255][nu][0] = ph * 100 + t;
@@ -428,9 +438,7 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
   }
   EngProgram p = prog;
   p.slot = next_slot.fetch_add(1) % kBarSlots;
-  void* args[] = {&p};
-  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(eng_kernel),
-                                              dim3(grid), dim3(kEngThreads), args, 0, st);
+  cudaError_t e = launch_ex(eng_kernel, dim3(grid), dim3(kEngThreads), 0, st, true, p);
   count_launches(1);
   return e;
 }

@@ -51,7 +51,7 @@ struct alignas(16) EngTask {
 constexpr int kEngMaxTasks = 24;
 constexpr int kEngMaxPhases = 8;
 
-struct EngProgram {
+struct alignas(16) EngProgram {
   int ntasks = 0, nphases = 0;
   unsigned slot = 0;  // grid-barrier slot (set by eng_launch)
   int phase_begin[kEngMaxPhases + 1] = {};

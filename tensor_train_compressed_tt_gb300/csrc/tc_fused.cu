@@ -28,7 +28,9 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cstdlib>
 #include <mutex>
+#include <utility>
 
 #include "tc_fused.h"
 
@@ -155,6 +157,15 @@ __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(su32(bar)), "r"(c0), "r"(c1)
       : "memory");
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on
+// (their memory is visible afterwards), and let the next grid in the stream
+// be scheduled early.  Both are no-ops for a grid launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -386,8 +397,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
   if (warp == 1) tmem_alloc(&S.tmem_base);
+  pdl_wait();  // nothing a previous grid writes is touched before this point
+  pdl_trigger();
+  if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -585,8 +598,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
   if (warp == 1) tmem_alloc(&S.tmem_base);
+  pdl_wait();  // nothing a previous grid writes is touched before this point
+  pdl_trigger();
+  if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1059,6 +1074,44 @@ cudaError_t set_smem_attrs() {
   return err;
 }
 
+// Programmatic dependent launch is on unless TTC_NO_PDL is set (to 1).
+bool pdl_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = getenv("TTC_NO_PDL");
+    on = (e && e[0] && e[0] != '0') ? 0 : 1;
+  }
+  return on == 1;
+}
+
+// Launch with the programmatic-serialization attribute (and optionally as a
+// cooperative grid).  The kernels call pdl_wait() before reading anything a
+// predecessor may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      bool cooperative, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  int n = 0;
+  if (pdl_enabled()) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cooperative) {
+    attrs[n].id = cudaLaunchAttributeCooperative;
+    attrs[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -1112,9 +1165,9 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   a.Dc = at<float>(ws, off + t.Dc);
   a.y = static_cast<__nv_bfloat16*>(y);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
-  tt_fwd_kernel<<<grid, NTHREADS, kSmemFwd, st>>>(mx, mat, mbt, my, a);
+  cudaError_t e = launch_ex(tt_fwd_kernel, grid, NTHREADS, kSmemFwd, st, false, mx, mat, mbt, my, a);
   count_launches(1);
-  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
@@ -1146,9 +1199,10 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.dBc = at<float>(ws, off + t.dBc);
   a.dDc = at<float>(ws, off + t.dDc);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
-  tt_bwd_kernel<<<grid, NTHREADS, kSmemBwd, st>>>(mx, mdy, mat, mbm, manr, mdx, mdac, mdbc, a);
+  cudaError_t e = launch_ex(tt_bwd_kernel, grid, NTHREADS, kSmemBwd, st, false, mx, mdy, mat, mbm,
+                            manr, mdx, mdac, mdbc, a);
   count_launches(1);
-  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 }  // namespace ttc
@@ -1162,6 +1216,36 @@ extern "C" int ttc_timeline_read(void* host, size_t bytes) {
 extern "C" int ttc_timeline_units_read(void* host, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(host, ttc::g_tlu, bytes);
 }
+// Engine microbenchmark (timeline builds only): one program of `phases`
+// phases, each holding `ntasks` GEMM tasks of m x n x k (f32, all operands
+// in the given device buffer), or empty units when m == 0.
+extern "C" int ttc_probe_engine(int phases, int ntasks, int units_if_empty, long m, long n, long k,
+                                void* buf, int split) {
+  using namespace ttc;
+  EngBuilder b;
+  float* f = static_cast<float*>(buf);
+  for (int ph = 0; ph < phases; ++ph) {
+    b.begin_phase();
+    for (int t = 0; t < ntasks; ++t) {
+      EngTask* task = b.add();
+      if (m == 0) {
+        task->kind = 99;
+        task->units = units_if_empty;
+        continue;
+      }
+      GemmArgs g;
+      g.m = m; g.n = n; g.k = k;
+      g.A = f; g.sam = k; g.sak = 1;
+      g.B = f + m * k; g.sbk = n; g.sbn = 1;
+      g.C = f + m * k + k * n + (size_t)t * m * n; g.scm = n; g.scn = 1;
+      eng_gemm_task(task, g, split ? f + 4 * (m * k + k * n) + (size_t)t * m * n * 16 : nullptr,
+                    split ? (size_t)m * n * 16 : 0);
+    }
+  }
+  b.end();
+  return (int)eng_launch(b.p, 0);
+}
+
 extern "C" int ttc_timeline_units_clear(void) {
   static unsigned long long zero[256 * 8 * 3];
   return (int)cudaMemcpyToSymbol(ttc::g_tlu, zero, sizeof(zero));
