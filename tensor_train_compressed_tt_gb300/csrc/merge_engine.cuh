@@ -17,49 +17,36 @@ constexpr int kBarSlots = 64;
 static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
 static_assert(sizeof(EngProgram) % 16 == 0, "the program is copied in 16-byte pieces");
 
-// Two-level grid barrier state per slot: 16 group counters and a root
-// counter (each on its own 128-byte line) plus the generation word.
-constexpr int kBarGroup = 16;
-constexpr int kBarMaxGroups = 16;
+// Grid barrier: one monotonic 64-bit arrival counter per slot (own
+// 128-byte line).  A CTA's own atomicAdd tells it which barrier generation
+// it joined, so the target it waits for needs no extra read and the counter
+// never has to be reset: every launch on a slot uses the same grid size and
+// launches on one slot are serialised by their stream.
 struct EngBarSlot {
-  unsigned group[kBarMaxGroups][32];
-  unsigned root[32];
-  unsigned gen[32];
+  unsigned long long count;
+  unsigned long long pad[15];
 };
 __device__ EngBarSlot g_eng_bar[kBarSlots];
 
-// Grid-wide barrier, bounded: false if it timed out (error recorded).  Data
-// produced in one phase and read in a later one is read with L2-only loads
-// (__ldcg), so no stale L1 line can be observed across a barrier.
+// Bounded: false if it timed out (error recorded).  Data produced in one
+// phase and read in a later one is read with L2-only loads (__ldcg), so no
+// stale L1 line can be observed across a barrier.
 __device__ bool eng_grid_barrier(unsigned slot, unsigned nblocks, int* failed) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    EngBarSlot& B = g_eng_bar[slot];
-    volatile unsigned* gen = &B.gen[0];
-    const unsigned g0 = *gen;
+    unsigned long long* cnt = &g_eng_bar[slot].count;
     __threadfence();
-    const unsigned gi = blockIdx.x / kBarGroup;
-    const unsigned ngroups = (nblocks + kBarGroup - 1) / kBarGroup;
-    const unsigned gsize = min((unsigned)kBarGroup, nblocks - gi * kBarGroup);
-    bool last = false;
-    if (atomicAdd(&B.group[gi][0], 1u) == gsize - 1) {
-      atomicExch(&B.group[gi][0], 0u);
-      __threadfence();
-      if (atomicAdd(&B.root[0], 1u) == ngroups - 1) {
-        atomicExch(&B.root[0], 0u);
-        __threadfence();
-        atomicAdd(&B.gen[0], 1u);
-        last = true;
-      }
-    }
-    if (!last) {
-      const uint64_t t0 = gtimer();
-      while (*gen == g0) {
-        if (gtimer() - t0 > kTimeoutNs) {
-          record_error(TT_ERR_TIMEOUT, 100);
-          *failed = 1;
-          break;
-        }
+    const unsigned long long old = atomicAdd(cnt, 1ull);
+    const unsigned long long target = (old / nblocks + 1) * nblocks;
+    const uint64_t t0 = gtimer();
+    while (true) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(cnt) : "memory");
+      if (v >= target) break;
+      if (gtimer() - t0 > kTimeoutNs) {
+        record_error(TT_ERR_TIMEOUT, 100);
+        *failed = 1;
+        break;
       }
     }
     __threadfence();
@@ -91,7 +78,8 @@ __device__ __forceinline__ float eng_gather(const EngTask& t, const int* pos, in
 
 // One kET x kET output tile of C over one K slice.
 __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
-                              float (*Bs)[kET + 1], int* pos, float* ksc, float* csc) {
+                              float (*Bs)[kET + 1], int* pos, float* ksc, float* csc, int nu) {
+  (void)nu;
   if (t.pack_side || t.gather) eng_pos_map(t, pos);
   const GemmArgs& g = t.g;
   const int S = t.splits;
@@ -113,12 +101,13 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
     csc[tid] = (g.cscale && gn < g.n) ? g.cscale[(unsigned)gn % (unsigned)g.clen] : 1.f;
   }
   for (int64_t k0 = kb; k0 < ke; k0 += kEK) {
-    // the periodic scales of this K slice, one index computation per thread
+    // the K slice's periodic scales, loaded together with the operands
+    float kscv = 1.f;
     if (tid < kEK) {
       const int64_t gk = k0 + tid;
-      ksc[tid] = (g.kscale && gk < ke) ? g.kscale[(unsigned)gk % (unsigned)g.klen] : 1.f;
+      if (g.kscale && gk < ke) kscv = __ldcg(g.kscale + (unsigned)gk % (unsigned)g.klen);
     }
-    __syncthreads();
+    if (k0 == kb) TLU_STAMP(nu, 3);
     // coalesced loads: walk the operand's unit-stride index fastest (the
     // [kEK][kET+1] tiles are conflict-free either way).  All 2 x 16 loads of
     // a thread are issued before any is used, so they overlap in flight.
@@ -146,21 +135,24 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
         vb[e] = (t.gather && t.gather_op == 1) ? eng_gather(t, pos, f) : __ldcg(B + f);
       }
     }
+    if (tid < kEK) ksc[tid] = kscv;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
       const int idx = tid + e * kEngThreads;
       const int a_m = a_kfast ? idx / kEK : idx % kET;
       const int a_k = a_kfast ? idx % kEK : idx / kET;
-      As[a_k][a_m] = va[e] * ksc[a_k];
+      As[a_k][a_m] = va[e];
       const int b_n = b_kfast ? idx / kEK : idx % kET;
       const int b_k = b_kfast ? idx % kEK : idx / kET;
       Bs[b_k][b_n] = vb[e];
     }
     __syncthreads();
+    if (k0 == kb) TLU_STAMP(nu, 4);
     const int kn = (int)(ke - k0 < kEK ? ke - k0 : kEK);
 #pragma unroll 8
     for (int kk = 0; kk < kn; ++kk) {
-      const float a0 = As[kk][ty * 2], a1 = As[kk][ty * 2 + 1];
+      const float sk = ksc[kk];
+      const float a0 = As[kk][ty * 2] * sk, a1 = As[kk][ty * 2 + 1] * sk;
       const float b0 = Bs[kk][tx * 2], b1 = Bs[kk][tx * 2 + 1];
       acc[0][0] = fmaf(a0, b0, acc[0][0]);
       acc[0][1] = fmaf(a0, b1, acc[0][1]);
@@ -168,6 +160,7 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
       acc[1][1] = fmaf(a1, b1, acc[1][1]);
     }
     __syncthreads();
+    if (k0 == kb) TLU_STAMP(nu, 5);
   }
   float* C = static_cast<float*>(g.C);
 #pragma unroll
@@ -298,7 +291,13 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       }
 #endif
       switch (k.kind) {
-        case kEGemm: eng_gemm_unit(k, uu, As, Bs, pos, ksc, csc); break;
+        case kEGemm:
+#ifdef TTC_TIMELINE
+          eng_gemm_unit(k, uu, As, Bs, pos, ksc, csc, nu);
+#else
+          eng_gemm_unit(k, uu, As, Bs, pos, ksc, csc, 0);
+#endif
+          break;
         case kEGemmFinal: eng_gemm_final_unit(k, uu); break;
         case kEColdot: eng_coldot_unit(k, uu, red); break;
         case kEScale: eng_scale_unit(k, uu); break;
@@ -438,7 +437,14 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
   }
   EngProgram p = prog;
   p.slot = next_slot.fetch_add(1) % kBarSlots;
-  cudaError_t e = launch_ex(eng_kernel, dim3(grid), dim3(kEngThreads), 0, st, true, p);
+  int g = grid;
+  bool coop = true;
+#ifdef TTC_TIMELINE
+  // measurement builds only: grid size and launch kind from the environment
+  if (const char* e = getenv("TTC_ENG_GRID")) g = atoi(e) > 0 && atoi(e) < grid ? atoi(e) : grid;
+  if (getenv("TTC_ENG_NONCOOP")) coop = false;
+#endif
+  cudaError_t e = launch_ex(eng_kernel, dim3(g), dim3(kEngThreads), 0, st, coop, p);
   count_launches(1);
   return e;
 }

@@ -107,9 +107,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
 // -DTTC_TIMELINE for performance investigation; the default build has none.
 #ifdef TTC_TIMELINE
 __device__ unsigned long long g_tl[3][256][16];
-__device__ unsigned long long g_tlu[256][8][3];  // engine units: (phase*100+task, start, end)
+__device__ unsigned long long g_tlu[256][8][8];  // engine units: (phase*100+task, start, end, inner stamps)
 #define TL_STAMP(k, slot) (g_tl[(k)][blockIdx.x & 255][(slot)] = gtimer())
+#define TLU_STAMP(nu, slot) \
+  if (threadIdx.x == 0 && (nu) < 8) g_tlu[blockIdx.x & 255][(nu)][(slot)] = gtimer()
 #else
+#define TLU_STAMP(nu, slot) ((void)0)
 #define TL_STAMP(k, slot) ((void)0)
 #endif
 
@@ -1247,7 +1250,7 @@ extern "C" int ttc_probe_engine(int phases, int ntasks, int units_if_empty, long
 }
 
 extern "C" int ttc_timeline_units_clear(void) {
-  static unsigned long long zero[256 * 8 * 3];
+  static unsigned long long zero[256 * 8 * 8];
   return (int)cudaMemcpyToSymbol(ttc::g_tlu, zero, sizeof(zero));
 }
 #endif
