@@ -204,6 +204,164 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
   }
 }
 
+// kEChain unit: prefixes [p0, p0 + pb) of one side's chain and last-mode
+// indices [q0, q0 + sb).  One cooperative pass loads everything the unit
+// needs into shared memory (the C_0 rows of its prefixes, the inner cores
+// C_1..C_{L-2} whole, the C_{L-1}[:, q0:q0+sb, :] slice and the diagonals),
+// so the loads are all in flight together; the chain vectors are then
+// rebuilt from shared memory.  P_k rows are written once (by the units with
+// q0 == 0), the final rows go to `out` and, on the tensor-core path, to the
+// compacted bf16 operands.
+constexpr int kChainPB = 32;        // max prefixes per unit
+constexpr int kChainSmem = 40960;   // floats of dynamic shared memory per CTA
+
+__host__ __device__ inline int64_t chain_stage_floats(const ChainDesc& c) {
+  int64_t f = 2 * kChainPB * 64 + kChainPB * (TT_MAX_D + 1) + (int64_t)(c.L > 1 ? c.L - 1 : 0) * 64;
+  for (int k = 1; k <= c.L - 2; ++k) f += (int64_t)c.r[k] * c.s[k] * c.r[k + 1];
+  f += (int64_t)c.r[c.L - 1] * c.sb * c.r[c.L];
+  return f;
+}
+
+// Asynchronous 4-byte global -> shared copies: a thread issues all of its
+// copies without waiting, so a whole staging pass costs one round trip.
+// (Only read-only inputs of the launch are staged this way.)
+__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ void eng_chain_unit(const EngTask& t, int u, int* pos, float* dsm, int nu) {
+  (void)nu;
+  const ChainDesc& c = t.ch;
+  const int L = c.L;
+  const int pb = c.pb, sb = c.sb;
+  const int64_t p0 = (int64_t)(u / c.nsb) * pb;
+  const int q0 = (u % c.nsb) * sb;
+  const int np = (int)(c.nprefix - p0 < pb ? c.nprefix - p0 : pb);
+  const int sl = c.s[L - 1], rl1 = c.r[L - 1], rL = c.r[L];
+  const int nq = (sl - q0 < sb ? sl - q0 : sb);
+  // shared-memory layout
+  float* va = dsm;
+  float* vb = va + kChainPB * 64;
+  int* dig = reinterpret_cast<int*>(vb + kChainPB * 64);  // [pb][TT_MAX_D + 1] digits, alpha
+  float* dg = vb + kChainPB * 64 + kChainPB * (TT_MAX_D + 1);  // [L-1][64] diagonals
+  float* cs[TT_MAX_D] = {};                  // staged inner cores
+  float* cur = dg + (L > 1 ? L - 1 : 0) * 64;
+  for (int k = 1; k <= L - 2; ++k) {
+    cs[k] = cur;
+    cur += c.r[k] * c.s[k] * c.r[k + 1];
+  }
+  float* cf = cur;                           // [rl1][nq][rL] final slice
+  // prefix digits, 32-bit (prefix counts stay far below 2^31)
+  for (int pi = threadIdx.x; pi < np; pi += blockDim.x) {
+    unsigned rem = (unsigned)(p0 + pi);
+    for (int k = L - 2; k >= 0; --k) {
+      dig[pi * (TT_MAX_D + 1) + k] = (int)(rem % (unsigned)c.s[k]);
+      rem /= (unsigned)c.s[k];
+    }
+    dig[pi * (TT_MAX_D + 1) + TT_MAX_D] = (int)rem;  // alpha
+  }
+  __syncthreads();
+  // one asynchronous staging pass for everything the unit reads
+  const int r1 = c.r[1];
+  for (int e = threadIdx.x; e < np * r1; e += blockDim.x) {
+    const int pi = e / r1, col = e - (e / r1) * r1;
+    const int alpha = dig[pi * (TT_MAX_D + 1) + TT_MAX_D], d0 = dig[pi * (TT_MAX_D + 1)];
+    cp_async4(va + pi * 64 + col, c.core[0] + ((int64_t)(alpha * c.s[0] + d0) * r1 + col));
+  }
+  for (int k = 0; k < L - 1; ++k)
+    for (int e = threadIdx.x; e < c.r[k + 1]; e += blockDim.x) cp_async4(dg + k * 64 + e, c.diag[k] + e);
+  for (int k = 1; k <= L - 2; ++k) {
+    const int n = c.r[k] * c.s[k] * c.r[k + 1];
+    for (int e = threadIdx.x; e < n; e += blockDim.x) cp_async4(cs[k] + e, c.core[k] + e);
+  }
+  {
+    const int n = rl1 * nq * rL;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) {
+      const int col = e % rL;
+      const int qi = (e / rL) % nq;
+      const int b = e / (rL * nq);
+      cp_async4(cf + e, c.core[L - 1] + ((int64_t)b * sl + q0 + qi) * rL + col);
+    }
+  }
+  if (t.pack_side) compaction_map(t.s, t.rd, pos, nullptr, nullptr);
+  cp_async_wait_all();
+  __syncthreads();
+  TLU_STAMP(nu, 3);
+  TLU_STAMP(nu, 4);
+  // steps 1 .. L-2: v <- (v * E_{k-1}) . C_k[:, s_k, :]
+  for (int k = 1; k <= L - 2; ++k) {
+    const int rk = c.r[k], rk1 = c.r[k + 1], sk = c.s[k];
+    const float* Ek = dg + (k - 1) * 64;
+    for (int e = threadIdx.x; e < np * rk1; e += blockDim.x) {
+      const int pi = e / rk1, col = e - (e / rk1) * rk1;
+      const int* dd = dig + pi * (TT_MAX_D + 1);
+      int64_t row = dd[TT_MAX_D];
+      for (int kk = 0; kk <= k; ++kk) row = row * c.s[kk] + dd[kk];
+      const float* Ck = cs[k] + dd[k] * rk1 + col;
+      const float* v = va + pi * 64;
+      float a0 = 0.f, a1 = 0.f;
+      int b = 0;
+      for (; b + 1 < rk; b += 2) {
+        a0 = fmaf(v[b] * Ek[b], Ck[b * sk * rk1], a0);
+        a1 = fmaf(v[b + 1] * Ek[b + 1], Ck[(b + 1) * sk * rk1], a1);
+      }
+      if (b < rk) a0 = fmaf(v[b] * Ek[b], Ck[b * sk * rk1], a0);
+      const float acc = a0 + a1;
+      vb[pi * 64 + col] = acc;
+      if (q0 == 0 && c.prow[k]) c.prow[k][row * rk1 + col] = acc;
+    }
+    __syncthreads();
+    float* tmp = va;
+    va = vb;
+    vb = tmp;
+  }
+  TLU_STAMP(nu, 5);
+  // final rows (prefix, q) = (v * E_{L-2}) . C_{L-1}[:, q, :]
+  const float* EL = dg + (L - 2) * 64;
+  const int nout = np * nq * rL;
+  for (int e = threadIdx.x; e < nout; e += blockDim.x) {
+    const int col = e % rL;
+    const int qi = (e / rL) % nq;
+    const int pi = e / (rL * nq);
+    const float* v = va + pi * 64;
+    const float* Cq = cf + qi * rL + col;
+    float a0 = 0.f, a1 = 0.f;
+    int b = 0;
+    for (; b + 1 < rl1; b += 2) {
+      a0 = fmaf(v[b] * EL[b], Cq[b * nq * rL], a0);
+      a1 = fmaf(v[b + 1] * EL[b + 1], Cq[(b + 1) * nq * rL], a1);
+    }
+    if (b < rl1) a0 = fmaf(v[b] * EL[b], Cq[b * nq * rL], a0);
+    const float acc = a0 + a1;
+    const int64_t f = ((p0 + pi) * sl + q0 + qi) * rL + col;  // flat index into P_{L-1}
+    c.out[f] = acc;
+    if (t.pack_side) {
+      const __nv_bfloat16 bv = __float2bfloat16_rn(acc);
+      if (t.pack_side == 1) {  // A (N x rd): f = j * rd + a
+        const unsigned jj = (unsigned)f / (unsigned)t.rd;
+        const int cc = pos[(unsigned)f - jj * (unsigned)t.rd];
+        if (cc >= 0) {
+          static_cast<__nv_bfloat16*>(t.tc.Anr)[(size_t)jj * RP + cc] = bv;
+          static_cast<__nv_bfloat16*>(t.tc.At)[(size_t)cc * t.N + jj] = bv;
+        }
+      } else {  // B (rd x M): f = a * M + o
+        const unsigned a = (unsigned)f / (unsigned)t.M;
+        const int cc = pos[a];
+        if (cc >= 0) {
+          const unsigned o = (unsigned)f - a * (unsigned)t.M;
+          static_cast<__nv_bfloat16*>(t.tc.Bt)[(size_t)o * RP + cc] = bv;
+          static_cast<__nv_bfloat16*>(t.tc.Bm)[(size_t)cc * t.M + o] = bv;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
 __device__ void eng_gemm_final_unit(const EngTask& t, int u) {
   const GemmArgs& g = t.g;
   const int64_t i = (int64_t)u * kEngThreads + threadIdx.x;
@@ -253,6 +411,7 @@ __device__ void eng_scale_unit(const EngTask& t, int u) {
 }
 
 __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant__ EngProgram prog) {
+  extern __shared__ float eng_dsm[];  // kChainSmem floats, used by kEChain units
   __shared__ float As[kEK][kET + 1];
   __shared__ float Bs[kEK][kET + 1];
   __shared__ float red[32];
@@ -306,6 +465,13 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
           break;
         case kEDd:
           tc_dd_unit(k.tc, k.s, k.rd, k.out, k.acc);
+          break;
+        case kEChain:
+#ifdef TTC_TIMELINE
+          eng_chain_unit(k, uu, pos, eng_dsm, nu);
+#else
+          eng_chain_unit(k, uu, pos, eng_dsm, 0);
+#endif
           break;
         case kEUnpack:
           tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
@@ -416,6 +582,21 @@ void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const flo
   t->units = (int)ceil_div((L.N + L.M) * L.rd + L.rd, kPackPer);
 }
 
+bool eng_chain_task(EngTask* t, const ChainDesc& c) {
+  t->kind = kEChain;
+  t->ch = c;
+  // split the last mode when the last core is large, so that a unit stages
+  // only a slice of it
+  const int64_t last = (int64_t)c.r[c.L - 1] * c.s[c.L - 1] * c.r[c.L];
+  t->ch.sb = last > 4096 ? 1 : c.s[c.L - 1];
+  t->ch.nsb = (c.s[c.L - 1] + t->ch.sb - 1) / t->ch.sb;
+  t->ch.pb = kChainPB;
+  t->units = (int)(ceil_div(c.nprefix, kChainPB) * t->ch.nsb);
+  for (int k = 0; k <= c.L; ++k)
+    if (c.r[k] > 64) return false;
+  return chain_stage_floats(t->ch) <= kChainSmem;
+}
+
 void eng_gemm_final_task(EngTask* t, const EngTask& gemm) {
   t->kind = kEGemmFinal;
   t->g = gemm.g;
@@ -431,7 +612,11 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
     int dev = 0, sms = 0, per = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, eng_kernel, kEngThreads, 0);
+    if (cudaFuncSetAttribute(eng_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kChainSmem * sizeof(float))) != cudaSuccess)
+      return cudaErrorLaunchFailure;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, eng_kernel, kEngThreads,
+                                                  kChainSmem * sizeof(float));
     grid = sms * (per > 0 ? 1 : 0);
     if (grid <= 0) return cudaErrorLaunchFailure;
   }
@@ -444,7 +629,8 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
   if (const char* e = getenv("TTC_ENG_GRID")) g = atoi(e) > 0 && atoi(e) < grid ? atoi(e) : grid;
   if (getenv("TTC_ENG_NONCOOP")) coop = false;
 #endif
-  cudaError_t e = launch_ex(eng_kernel, dim3(g), dim3(kEngThreads), 0, st, coop, p);
+  cudaError_t e = launch_ex(eng_kernel, dim3(g), dim3(kEngThreads), kChainSmem * sizeof(float), st,
+                            coop, p);
   count_launches(1);
   return e;
 }

@@ -16,7 +16,26 @@ enum EngKind {
   kEScale = 3,     // out[i] (=|+=) in[i] * scale[i % len]
   kEPack = 4,      // tensor-core operands from A, B, D_d (+ zero gradient sums)
   kEUnpack = 5,    // compacted gradient sums -> dA, dB, dD_d
-  kEDd = 6         // compacted dD_d sum -> dD_d only
+  kEDd = 6,        // compacted dD_d sum -> dD_d only
+  kEChain = 7      // rows of one side's merged chain, recomputed per prefix
+};
+
+// One side of the chain for kEChain: cores C_0..C_{L-1} (C_k of shape
+// (r[k], s[k], r[k+1]), r[0] the left boundary), diagonals E_k between C_k
+// and C_{k+1}.  A prefix is (alpha, s_0..s_{L-2}); its P_k rows and the
+// s_{L-1} final rows of P_{L-1} (= A or B) are written.
+struct ChainDesc {
+  const float* core[TT_MAX_D] = {};
+  const float* diag[TT_MAX_D] = {};
+  float* prow[TT_MAX_D] = {};   // P_k buffers for 1 <= k <= L-2
+  float* out = nullptr;         // P_{L-1}
+  int r[TT_MAX_D + 1] = {};
+  int s[TT_MAX_D] = {};
+  int L = 0;
+  int pb = 1;                   // prefixes per unit
+  int sb = 1;                   // last-mode indices per unit
+  int nsb = 1;                  // number of last-mode blocks
+  int64_t nprefix = 0;
 };
 
 struct alignas(16) EngTask {
@@ -46,9 +65,10 @@ struct alignas(16) EngTask {
   //  gather 1/2: the operand that reads dA / dB (gather_op 0 = A, 1 = B)
   //    reads the compacted token sums tc.dAc / tc.dBc instead.
   int pack_side = 0, gather = 0, gather_op = 0, pad_only = 0;
+  ChainDesc ch;  // kEChain (pack_side selects the packing, s = D_d)
 };
 
-constexpr int kEngMaxTasks = 24;
+constexpr int kEngMaxTasks = 20;
 constexpr int kEngMaxPhases = 8;
 
 struct alignas(16) EngProgram {
@@ -70,6 +90,8 @@ struct EngBuilder {
 // Units for a GEMM task of the engine's tile size and a split-K count.
 void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap);
 void eng_gemm_final_task(EngTask* t, const EngTask& gemm);
+// false when the chain does not fit the unit's shared-memory staging
+bool eng_chain_task(EngTask* t, const ChainDesc& c);
 void eng_pack_task(EngTask* t, const LayerPlan& L, const float* A, const float* B,
                    const float* Dmid, const TcPtrs& tc, bool zero_grads, bool pad_only = false);
 void eng_dd_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,

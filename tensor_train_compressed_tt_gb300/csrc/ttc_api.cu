@@ -163,7 +163,9 @@ void chain_ptrs(const LayerPlan& L, const float* params, void* ws, const WsLayou
 // On the tensor-core path the GEMMs that produce A and B also write the
 // compacted bf16 operands, and the first phase writes the padding and the
 // metadata (and zeroes the token sums for a backward call).
-tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
+// Fallback for chains with an internal rank above 64: one GEMM phase per
+// chain step (grid barriers in between).
+tt_status run_merge_forward_gemm(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
                             const float** P, bool pack, bool zero_grads, cudaStream_t st) {
   chain_ptrs(L, params, ws, w, P);
   const float* Dmid = params + L.diag_off[L.d - 1];
@@ -200,6 +202,57 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
   if (b.p.nphases == 0) return TT_OK;
+  TT_CUDA(eng_launch(b.p, st));
+  return TT_OK;
+}
+
+tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
+                            const float** P, bool pack, bool zero_grads, cudaStream_t st) {
+  chain_ptrs(L, params, ws, w, P);
+  const float* Dmid = params + L.diag_off[L.d - 1];
+  const TcPtrs tc = pack ? tc_ptrs(L, ws, w.tc) : TcPtrs();
+  EngBuilder b;
+  b.begin_phase();
+  if (L.d == 1) {
+    if (pack) eng_pack_task(b.add(), L, P[0], P[1], Dmid, tc, zero_grads, false);
+  } else {
+    // one phase: each side's rows recomputed per prefix (no grid barrier);
+    // padding, metadata and the zeroed token sums come from the pack task
+    if (pack) eng_pack_task(b.add(), L, nullptr, nullptr, Dmid, tc, zero_grads, true);
+    for (int side = 0; side < 2; ++side) {
+      const int k0 = side == 0 ? 0 : L.d;
+      ChainDesc c;
+      c.L = L.d;
+      c.r[0] = L.r[k0];
+      int64_t np = side == 0 ? 1 : L.rd;
+      for (int k = 0; k < L.d; ++k) {
+        c.core[k] = params + L.core_off[k0 + k];
+        c.s[k] = L.s[k0 + k];
+        c.r[k + 1] = L.r[k0 + k + 1];
+        if (k < L.d - 1) {
+          c.diag[k] = params + L.diag_off[k0 + k];
+          np *= L.s[k0 + k];
+        }
+        if (k >= 1 && k <= L.d - 2) c.prow[k] = const_cast<float*>(P[k0 + k]);
+      }
+      c.out = const_cast<float*>(P[k0 + L.d - 1]);
+      c.nprefix = np;
+      EngTask* t = b.add();
+      if (!eng_chain_task(t, c))  // ranks above 64 or cores too large to stage
+        return run_merge_forward_gemm(L, params, ws, w, P, pack, zero_grads, st);
+      if (pack) {
+        t->pack_side = side + 1;
+        t->tc = tc;
+        t->s = Dmid;
+        t->rd = L.rd;
+        t->N = (int)L.N;
+        t->M = (int)L.M;
+      }
+    }
+  }
+  b.end();
+  if (b.overflow) return TT_ERR_UNSUPPORTED;
+  if (b.p.ntasks == 0) return TT_OK;
   TT_CUDA(eng_launch(b.p, st));
   return TT_OK;
 }

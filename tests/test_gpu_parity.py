@@ -186,3 +186,18 @@ def test_reuse_merge_matches_default(name):
         # atomically reduced token sums: equal up to summation order
         assert O.rel_err(g1.cpu().numpy(), g0.cpu().numpy()) <= 1e-5
         assert O.rel_err(g2.cpu().numpy(), g0.cpu().numpy()) <= 1e-5
+
+
+def test_internal_rank_above_64_uses_generic_merge():
+    """A link rank above 64 takes the generic (GEMM-phase) merge program."""
+    rng = np.random.Generator(np.random.PCG64(77))
+    for shape, act in [(synth.LayerShape((4, 3, 2), (2, 3, 4), (1, 4, 70, 6, 66, 4, 1)), "f32"),
+                       (synth.LayerShape((16, 8), (8, 16), (1, 16, 40, 72, 1)), "bf16")]:
+        li = synth.draw_layer(rng, shape, 0.3, "uniform")
+        T = 77
+        x = rng.standard_normal((T, shape.N)).astype(np.float32)
+        dy = rng.standard_normal((T, shape.M)).astype(np.float32)
+        if act == "bf16":
+            x, dy = synth.round_bf16(x), synth.round_bf16(dy)
+        compare(gpu_layer(shape, act, li, x, dy), oracle_layer(shape, li, x, dy), TOL[act],
+                f"{shape}")
