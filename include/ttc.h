@@ -94,7 +94,11 @@ tt_status tt_default_ranks(int d, const int* in_modes, const int* out_modes, int
                            int* ranks);
 
 /* Validate desc and build a plan (host only; no device work, no allocation on
- * the device).  *out is owned by the caller and freed with tt_destroy. */
+ * the device).  *out is owned by the caller and freed with tt_destroy.
+ * TT_ERR_INVALID_ARG for a malformed desc (a rank outside 1..4096 among
+ * them); TT_ERR_UNSUPPORTED for N or M above 2^20 or a merged intermediate
+ * (the packed parameters, a prefix product of the cores, the merged A or B)
+ * of 2^31 elements or more. */
 tt_status tt_plan(const tt_desc* desc, tt_plan_t** out);
 
 /* FFN pair y = TT_down(GELU(TT_up(x))) with the exact erf GELU; up's output

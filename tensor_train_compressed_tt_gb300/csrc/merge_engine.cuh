@@ -10,13 +10,15 @@
 namespace ttc {
 namespace {
 
-constexpr int kEngThreads = 256;
-constexpr int kET = 32;   // GEMM tile (kET x kET outputs per unit)
-constexpr int kEK = 128;  // K slice staged per iteration (all loads in flight at once)
+constexpr int kEngThreads = 512;
+constexpr int kEngWarps = kEngThreads / 32;
+constexpr int kGK = 512;    // GEMM: K extent staged per pass
+constexpr int kGLd = 36;    // GEMM: shared row stride (floats) of a staged [k][m] tile
+// GEMM unit dynamic shared memory: A and B tiles, K scales, k-group partials
+constexpr int kGemmSmem = 2 * kGK * kGLd + kGK + kEngThreads * 16;
 constexpr int kBarSlots = 64;
+constexpr int kMaxSplits = 32;  // split-K partials of one GEMM task
 static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
-static_assert(sizeof(EngProgram) % 16 == 0, "the program is copied in 16-byte pieces");
-
 // Grid barrier: one monotonic 64-bit arrival counter per slot (own
 // 128-byte line).  A CTA's own atomicAdd tells it which barrier generation
 // it joined, so the target it waits for needs no extra read and the counter
@@ -55,153 +57,230 @@ __device__ bool eng_grid_barrier(unsigned slot, unsigned nblocks, int* failed) {
   return *failed == 0;
 }
 
-// Compaction position of each middle-rank index (-1 if pruned), from D_d
-// (pack) or from the kept list (gather).
-__device__ void eng_pos_map(const EngTask& t, int* pos) {
-  compaction_map(t.s, t.rd, pos, nullptr, nullptr);
-}
-
-// Element f (flat index into dA (N x rd) or dB (rd x M)) read from the
-// compacted token sums.
+// Source of element f (flat index into dA (N x rd) or dB (rd x M)) in the
+// compacted token sums; null for a pruned rank (the element is 0).
 // (32-bit index arithmetic: N*rd and rd*M stay far below 2^31.)
-__device__ __forceinline__ float eng_gather(const EngTask& t, const int* pos, int64_t f64) {
+__device__ __forceinline__ const float* eng_gather_src(const EngTask& t, const int* pos,
+                                                       int64_t f64) {
   const unsigned f = (unsigned)f64;
   if (t.gather == 1) {
     const unsigned j = f / (unsigned)t.rd;
     const int c = pos[f - j * (unsigned)t.rd];
-    return c >= 0 ? __ldcg(t.tc.dAc + (size_t)j * RP + c) : 0.f;
+    return c >= 0 ? t.tc.dAc + (size_t)j * RP + c : nullptr;
   }
   const unsigned a = f / (unsigned)t.M;
   const int c = pos[a];
-  return c >= 0 ? __ldcg(t.tc.dBc + (size_t)(f - a * (unsigned)t.M) * RP + c) : 0.f;
+  return c >= 0 ? t.tc.dBc + (size_t)(f - a * (unsigned)t.M) * RP + c : nullptr;
 }
 
-// One kET x kET output tile of C over one K slice.
-__device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
-                              float (*Bs)[kET + 1], int* pos, float* ksc, float* csc, int nu) {
+// Asynchronous 4-byte global -> shared copies: a thread issues all of its
+// copies without waiting, so a whole staging pass costs one round trip.
+__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Issue the copies of one operand tile: element (r, k), r < rows (16 or 32),
+// k < kc, of the matrix whose element (r0 + r, k0 + k) is at G[(r0+r)*sr +
+// (k0+k)*sk] lands at S[k * kGLd + r]; rows at or past rlim are not
+// written.  A warp copies 32-element blocks laid out so that both the global
+// reads (unit-stride index fastest) and the shared writes (8 k x 4 rows hit
+// 32 distinct banks at row stride 36) are conflict-free.  Every thread keeps
+// one row and walks k with a fixed step, so the loop carries no divisions.
+// 32-bit offsets: the plan keeps every merge matrix below 2^31 elements.
+__device__ __forceinline__ void eng_stage(float* S, int rows, int kc, int r0, int k0, int rlim,
+                                          const float* G, int sr, int sk, const EngTask& t,
+                                          const int* pos, bool gather) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int rr, kk, step;
+  if (sk == 1 && sr != 1) {  // k fastest in memory: blocks of 8 k x 4 rows
+    const int lg = rows == 16 ? 2 : 3;  // log2(rows / 4)
+    rr = (warp & ((1 << lg) - 1)) * 4 + (lane >> 3);
+    kk = (warp >> lg) * 8 + (lane & 7);
+    step = (kEngWarps >> lg) * 8;
+  } else if (rows == 16) {  // rows fastest: blocks of 16 rows x 2 k
+    rr = lane & 15;
+    kk = warp * 2 + (lane >> 4);
+    step = kEngWarps * 2;
+  } else {  // rows fastest: blocks of 32 rows x 1 k
+    rr = lane;
+    kk = warp;
+    step = kEngWarps;
+  }
+  if (r0 + rr >= rlim) return;
+  float* dst = S + kk * kGLd + rr;
+  const int dstep = step * kGLd;
+  const int f0 = (r0 + rr) * sr + (k0 + kk) * sk;
+  const int finc = step * sk;
+  if (!gather) {
+    const float* src = G + f0;
+#pragma unroll 4
+    for (; kk < kc; kk += step, dst += dstep, src += finc) cp_async4(dst, src);
+    return;
+  }
+  // gathered operand: f = j * rd + a (dA: row j, compacted column pos[a] of
+  // dAc) or f = a * M + o (dB: row o, compacted column pos[a] of dBc); the
+  // quotient and remainder by D advance with f
+  const bool ga = t.gather == 1;
+  const unsigned D = ga ? (unsigned)t.rd : (unsigned)t.M;
+  unsigned q = (unsigned)f0 / D, rem = (unsigned)f0 - q * D;
+  const unsigned qi = (unsigned)finc / D, ri = (unsigned)finc - qi * D;
+  const float* base = ga ? t.tc.dAc : t.tc.dBc;
+#pragma unroll 4
+  for (; kk < kc; kk += step, dst += dstep) {
+    const int c = pos[ga ? rem : q];
+    const unsigned row = ga ? q : rem;
+    if (c >= 0) cp_async4(dst, base + (size_t)row * RP + c);
+    else *dst = 0.f;
+    rem += ri;
+    q += qi;
+    if (rem >= D) {
+      rem -= D;
+      ++q;
+    }
+  }
+}
+
+// One tm x tn output tile of C over one K split.  The whole K range (in
+// passes of kGK) is staged into shared memory with one round of
+// asynchronous copies; the kEngThreads threads then split K into
+// kEngThreads / (tm*tn/16) groups, each thread owning a 4 x 4 block of the tile, and the group
+// partials are summed in a fixed order (deterministic).  Tile counts and
+// the split length come from the host; the unit's own index arithmetic is
+// 32-bit shifts and masks.
+__device__ void eng_gemm_unit(const EngTask& t, int u, const int* pos, float* dsm, float* rsc,
+                              float* csc, int nu) {
   (void)nu;
-  if (t.pack_side || t.gather) eng_pos_map(t, pos);
+  TLU_STAMP(nu, 6);
   const GemmArgs& g = t.g;
-  const int S = t.splits;
-  const int tiles_n = (int)((g.n + kET - 1) / kET);
-  const int ks = u % S;
-  const int tile = u / S;
-  const int64_t m0 = (int64_t)(tile / tiles_n) * kET, n0 = (int64_t)(tile % tiles_n) * kET;
-  int64_t chunk = (g.k + S - 1) / S;
-  chunk = (chunk + kEK - 1) / kEK * kEK;
-  const int64_t kb = (int64_t)ks * chunk;
-  const int64_t ke = kb + chunk < g.k ? kb + chunk : g.k;
+  const int S = t.splits, TM = t.tm, TN = t.tn;
+  const int m = (int)g.m, n = (int)g.n, K = (int)g.k;
+  const int ks = S > 1 ? u % S : 0;
+  const int tile = S > 1 ? u / S : u;
+  const int ti = tile / t.tiles_n;
+  const int m0 = ti * TM, n0 = (tile - ti * t.tiles_n) * TN;
+  const int kb = ks * t.kchunk;
+  const int ke = kb + t.kchunk < K ? kb + t.kchunk : K;
   const float* A = static_cast<const float*>(g.A);
   const float* B = static_cast<const float*>(g.B);
-  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
-  float acc[2][2] = {};
-  // the periodic scales of this tile's columns, once per unit
-  if (tid < kET) {
-    const int64_t gn = n0 + tid;
-    csc[tid] = (g.cscale && gn < g.n) ? g.cscale[(unsigned)gn % (unsigned)g.clen] : 1.f;
+  float* As = dsm;
+  float* Bs = As + kGK * kGLd;
+  float* ksc = Bs + kGK * kGLd;
+  float* red = ksc + kGK;
+  const int tid = threadIdx.x;
+  const int lgtn4 = TN == 32 ? 3 : 2, lgtn = lgtn4 + 2;
+  const int lgG = (TM == 32 ? 3 : 2) + lgtn4;
+  const int kg = kEngThreads >> lgG;
+  const int grp = tid >> lgG, lid = tid & ((1 << lgG) - 1);
+  const int ty = lid >> lgtn4, tx = lid & ((1 << lgtn4) - 1);
+  const int mrem = m - m0 < TM ? m - m0 : TM;
+  const int nrem = n - n0 < TN ? n - n0 : TN;
+  const bool active = ty * 4 < mrem && tx * 4 < nrem;
+  const bool gA = t.gather && t.gather_op == 0, gB = t.gather && t.gather_op == 1;
+  // epilogue scales of this tile, copied together with the operands
+  if (tid < TM) {
+    if (g.rscale && tid < mrem) cp_async4(rsc + tid, g.rscale + m0 + tid);
+    else rsc[tid] = 1.f;
   }
-  for (int64_t k0 = kb; k0 < ke; k0 += kEK) {
-    // the K slice's periodic scales, loaded together with the operands
-    float kscv = 1.f;
-    if (tid < kEK) {
-      const int64_t gk = k0 + tid;
-      if (g.kscale && gk < ke) kscv = __ldcg(g.kscale + (unsigned)gk % (unsigned)g.klen);
+  if (tid >= 64 && tid < 64 + TN) {
+    const int j = tid - 64;
+    if (g.cscale && j < nrem) cp_async4(csc + j, g.cscale + (unsigned)(n0 + j) % (unsigned)g.clen);
+    else csc[j] = 1.f;
+  }
+  float acc[4][4] = {};
+  for (int k0 = kb; k0 < ke; k0 += kGK) {
+    const int kc = ke - k0 < kGK ? ke - k0 : kGK;
+    if (k0 != kb) __syncthreads();  // the previous pass's reads are done
+    if (k0 == kb) TLU_STAMP(nu, 7);
+    eng_stage(As, TM, kc, m0, k0, m, A, (int)g.sam, (int)g.sak, t, pos, gA);
+    eng_stage(Bs, TN, kc, n0, k0, n, B, (int)g.sbn, (int)g.sbk, t, pos, gB);
+    if (g.kscale) {
+      const unsigned kl = (unsigned)g.klen;
+      for (int k = tid; k < kc; k += kEngThreads)
+        cp_async4(ksc + k, g.kscale + (unsigned)(k0 + k) % kl);
     }
     if (k0 == kb) TLU_STAMP(nu, 3);
-    // coalesced loads: walk the operand's unit-stride index fastest (the
-    // [kEK][kET+1] tiles are conflict-free either way).  All 2 x 16 loads of
-    // a thread are issued before any is used, so they overlap in flight.
-    constexpr int kPer = (kET * kEK) / kEngThreads;
-    const bool a_kfast = g.sak == 1 && g.sam != 1;
-    const bool b_kfast = g.sbk == 1 && g.sbn != 1;
-    float va[kPer], vb[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int idx = tid + e * kEngThreads;
-      const int a_m = a_kfast ? idx / kEK : idx % kET;
-      const int a_k = a_kfast ? idx % kEK : idx / kET;
-      const int64_t gm = m0 + a_m, gk = k0 + a_k;
-      va[e] = 0.f;
-      if (gm < g.m && gk < ke) {
-        const int64_t f = gm * g.sam + gk * g.sak;
-        va[e] = (t.gather && t.gather_op == 0) ? eng_gather(t, pos, f) : __ldcg(A + f);
-      }
-      const int b_n = b_kfast ? idx / kEK : idx % kET;
-      const int b_k = b_kfast ? idx % kEK : idx / kET;
-      const int64_t gn = n0 + b_n, gk2 = k0 + b_k;
-      vb[e] = 0.f;
-      if (gn < g.n && gk2 < ke) {
-        const int64_t f = gk2 * g.sbk + gn * g.sbn;
-        vb[e] = (t.gather && t.gather_op == 1) ? eng_gather(t, pos, f) : __ldcg(B + f);
-      }
-    }
-    if (tid < kEK) ksc[tid] = kscv;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int idx = tid + e * kEngThreads;
-      const int a_m = a_kfast ? idx / kEK : idx % kET;
-      const int a_k = a_kfast ? idx % kEK : idx / kET;
-      As[a_k][a_m] = va[e];
-      const int b_n = b_kfast ? idx / kEK : idx % kET;
-      const int b_k = b_kfast ? idx % kEK : idx / kET;
-      Bs[b_k][b_n] = vb[e];
-    }
+    cp_async_wait_all();
     __syncthreads();
     if (k0 == kb) TLU_STAMP(nu, 4);
-    const int kn = (int)(ke - k0 < kEK ? ke - k0 : kEK);
-#pragma unroll 8
-    for (int kk = 0; kk < kn; ++kk) {
-      const float sk = ksc[kk];
-      const float a0 = As[kk][ty * 2] * sk, a1 = As[kk][ty * 2 + 1] * sk;
-      const float b0 = Bs[kk][tx * 2], b1 = Bs[kk][tx * 2 + 1];
-      acc[0][0] = fmaf(a0, b0, acc[0][0]);
-      acc[0][1] = fmaf(a0, b1, acc[0][1]);
-      acc[1][0] = fmaf(a1, b0, acc[1][0]);
-      acc[1][1] = fmaf(a1, b1, acc[1][1]);
-    }
-    __syncthreads();
-    if (k0 == kb) TLU_STAMP(nu, 5);
-  }
-  float* C = static_cast<float*>(g.C);
+    if (active) {
+      const int per = (kc + kg - 1) / kg;
+      const int k1 = grp * per;
+      const int k2 = k1 + per < kc ? k1 + per : kc;
+      const float* ap = As + ty * 4;
+      const float* bp = Bs + tx * 4;
+#pragma unroll 4
+      for (int k = k1; k < k2; ++k) {
+        float4 a = *reinterpret_cast<const float4*>(ap + k * kGLd);
+        const float4 b = *reinterpret_cast<const float4*>(bp + k * kGLd);
+        if (g.kscale) {
+          const float sc = ksc[k];
+          a.x *= sc; a.y *= sc; a.z *= sc; a.w *= sc;
+        }
+        const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int64_t gm = m0 + ty * 2 + i;
-    if (gm >= g.m) continue;
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int64_t gn = n0 + tx * 2 + j;
-      if (gn >= g.n) continue;
-      if (S > 1) {
-        t.partial[((int64_t)ks * g.m + gm) * g.n + gn] = acc[i][j];
-        continue;
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
       }
-      float v = acc[i][j] * csc[tx * 2 + j];
-      if (g.rscale) v *= g.rscale[gm];
-      const int64_t ci = gm * g.scm + gn * g.scn;
-      C[ci] = g.mode == kAccumulate ? __ldcg(C + ci) + v : v;
-      if (t.pack_side) {
-        // C is A (N x rd) or B (rd x M), row-major with scm = n, scn = 1
-        const __nv_bfloat16 b = __float2bfloat16_rn(v);
-        const unsigned cu = (unsigned)ci;
-        if (t.pack_side == 1) {
-          const unsigned jj = cu / (unsigned)t.rd;
-          const int c = pos[cu - jj * (unsigned)t.rd];
-          if (c >= 0) {
-            static_cast<__nv_bfloat16*>(t.tc.Anr)[(size_t)jj * RP + c] = b;
-            static_cast<__nv_bfloat16*>(t.tc.At)[(size_t)c * t.N + jj] = b;
-          }
-        } else {
-          const unsigned a = cu / (unsigned)t.M;
-          const int c = pos[a];
-          if (c >= 0) {
-            const unsigned o = cu - a * (unsigned)t.M;
-            static_cast<__nv_bfloat16*>(t.tc.Bt)[(size_t)o * RP + c] = b;
-            static_cast<__nv_bfloat16*>(t.tc.Bm)[(size_t)c * t.M + o] = b;
-          }
+    }
+  }
+  const int tsz = TM * TN;
+  if (active) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(red + grp * tsz + (ty * 4 + i) * TN + tx * 4) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  }
+  __syncthreads();
+  TLU_STAMP(nu, 5);
+  float* C = static_cast<float*>(g.C);
+  const int scm = (int)g.scm, scn = (int)g.scn;
+  for (int o = tid; o < tsz; o += kEngThreads) {
+    const int i = o >> lgtn, j = o & (TN - 1);
+    if (i >= mrem || j >= nrem) continue;
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < kEngThreads / 16; ++q)
+      if (q < kg) v += red[q * tsz + o];
+    const int gm = m0 + i, gn = n0 + j;
+    if (S > 1 && g.mode != kAtomic) {
+      t.partial[(ks * m + gm) * n + gn] = v;
+      continue;
+    }
+    v *= rsc[i] * csc[j];
+    const int ci = gm * scm + gn * scn;
+    if (g.mode == kAtomic) {  // each split adds its share into a zeroed C
+      atomicAdd(C + ci, v);
+      continue;
+    }
+    C[ci] = g.mode == kAccumulate ? __ldcg(C + ci) + v : v;
+    if (t.pack_side) {
+      // C is A (N x rd) or B (rd x M), row-major with scm = n, scn = 1
+      const __nv_bfloat16 b = __float2bfloat16_rn(v);
+      const unsigned cu = (unsigned)ci;
+      if (t.pack_side == 1) {
+        const unsigned jj = cu / (unsigned)t.rd;
+        const int c = pos[cu - jj * (unsigned)t.rd];
+        if (c >= 0) {
+          static_cast<__nv_bfloat16*>(t.tc.Anr)[(size_t)jj * RP + c] = b;
+          static_cast<__nv_bfloat16*>(t.tc.At)[(size_t)c * t.N + jj] = b;
+        }
+      } else {
+        const unsigned a = cu / (unsigned)t.M;
+        const int c = pos[a];
+        if (c >= 0) {
+          const unsigned oo = cu - a * (unsigned)t.M;
+          static_cast<__nv_bfloat16*>(t.tc.Bt)[(size_t)oo * RP + c] = b;
+          static_cast<__nv_bfloat16*>(t.tc.Bm)[(size_t)c * t.M + oo] = b;
         }
       }
     }
   }
+  __syncthreads();  // shared memory is reused by the next unit
 }
 
 // kEChain unit: prefixes [p0, p0 + pb) of one side's chain and last-mode
@@ -214,40 +293,54 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, float (*As)[kET + 1],
 // compacted bf16 operands.
 constexpr int kChainPB = 32;        // max prefixes per unit
 constexpr int kChainSmem = 40960;   // floats of dynamic shared memory per CTA
+constexpr int kVS = 65;             // shared row stride of the chain vectors (odd: no
+                                    // bank conflicts between prefixes)
 
 __host__ __device__ inline int64_t chain_stage_floats(const ChainDesc& c) {
-  int64_t f = 2 * kChainPB * 64 + kChainPB * (TT_MAX_D + 1) + (int64_t)(c.L > 1 ? c.L - 1 : 0) * 64;
+  int64_t f = 2 * kChainPB * kVS + kChainPB * (TT_MAX_D + 1) + kChainPB * TT_MAX_D +
+              (int64_t)(c.L > 1 ? c.L - 1 : 0) * 64;
   for (int k = 1; k <= c.L - 2; ++k) f += (int64_t)c.r[k] * c.s[k] * c.r[k + 1];
   f += (int64_t)c.r[c.L - 1] * c.sb * c.r[c.L];
   return f;
 }
 
-// Asynchronous 4-byte global -> shared copies: a thread issues all of its
-// copies without waiting, so a whole staging pass costs one round trip.
-// (Only read-only inputs of the launch are staged this way.)
-__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32(smem)), "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
+// Walks e = threadIdx.x, + kEngThreads, ... over a (rows x cols) grid as (r, c)
+// with one division up front instead of one per step.
+struct Walk2 {
+  int r, c, dr, dc, cols;
+  __device__ explicit Walk2(int cols_) : cols(cols_) {
+    r = (int)threadIdx.x / cols;
+    c = (int)threadIdx.x - r * cols;
+    dr = kEngThreads / cols;
+    dc = kEngThreads - dr * cols;
+  }
+  __device__ void next() {
+    r += dr;
+    c += dc;
+    if (c >= cols) {
+      c -= cols;
+      ++r;
+    }
+  }
+};
 
-__device__ void eng_chain_unit(const EngTask& t, int u, int* pos, float* dsm, int nu) {
+__device__ void eng_chain_unit(const EngTask& t, int u, const int* pos, float* dsm, int nu) {
   (void)nu;
   const ChainDesc& c = t.ch;
   const int L = c.L;
   const int pb = c.pb, sb = c.sb;
-  const int64_t p0 = (int64_t)(u / c.nsb) * pb;
+  const int tid = threadIdx.x;
+  const int p0 = (u / c.nsb) * pb;  // prefix counts stay below 2^31
   const int q0 = (u % c.nsb) * sb;
   const int np = (int)(c.nprefix - p0 < pb ? c.nprefix - p0 : pb);
   const int sl = c.s[L - 1], rl1 = c.r[L - 1], rL = c.r[L];
   const int nq = (sl - q0 < sb ? sl - q0 : sb);
   // shared-memory layout
-  float* va = dsm;
-  float* vb = va + kChainPB * 64;
-  int* dig = reinterpret_cast<int*>(vb + kChainPB * 64);  // [pb][TT_MAX_D + 1] digits, alpha
-  float* dg = vb + kChainPB * 64 + kChainPB * (TT_MAX_D + 1);  // [L-1][64] diagonals
+  float* va = dsm;                                              // [pb][kVS] chain vectors
+  float* vb = va + kChainPB * kVS;
+  int* dig = reinterpret_cast<int*>(vb + kChainPB * kVS);      // [pb][TT_MAX_D + 1] digits, alpha
+  int* rowk = dig + kChainPB * (TT_MAX_D + 1);                 // [pb][TT_MAX_D] P_k row of the prefix
+  float* dg = reinterpret_cast<float*>(rowk + kChainPB * TT_MAX_D);  // [L-1][64] diagonals
   float* cs[TT_MAX_D] = {};                  // staged inner cores
   float* cur = dg + (L > 1 ? L - 1 : 0) * 64;
   for (int k = 1; k <= L - 2; ++k) {
@@ -255,64 +348,67 @@ __device__ void eng_chain_unit(const EngTask& t, int u, int* pos, float* dsm, in
     cur += c.r[k] * c.s[k] * c.r[k + 1];
   }
   float* cf = cur;                           // [rl1][nq][rL] final slice
-  // prefix digits, 32-bit (prefix counts stay far below 2^31)
-  for (int pi = threadIdx.x; pi < np; pi += blockDim.x) {
+  // prefix digits and the flat P_k row of each prefix
+  for (int pi = tid; pi < np; pi += kEngThreads) {
     unsigned rem = (unsigned)(p0 + pi);
     for (int k = L - 2; k >= 0; --k) {
-      dig[pi * (TT_MAX_D + 1) + k] = (int)(rem % (unsigned)c.s[k]);
-      rem /= (unsigned)c.s[k];
+      const unsigned q = rem / (unsigned)c.s[k];
+      dig[pi * (TT_MAX_D + 1) + k] = (int)(rem - q * (unsigned)c.s[k]);
+      rem = q;
     }
     dig[pi * (TT_MAX_D + 1) + TT_MAX_D] = (int)rem;  // alpha
+    unsigned row = rem;
+    for (int k = 0; k <= L - 2; ++k) {
+      row = row * (unsigned)c.s[k] + (unsigned)dig[pi * (TT_MAX_D + 1) + k];
+      rowk[pi * TT_MAX_D + k] = (int)row;
+    }
   }
   __syncthreads();
   // one asynchronous staging pass for everything the unit reads
   const int r1 = c.r[1];
-  for (int e = threadIdx.x; e < np * r1; e += blockDim.x) {
-    const int pi = e / r1, col = e - (e / r1) * r1;
-    const int alpha = dig[pi * (TT_MAX_D + 1) + TT_MAX_D], d0 = dig[pi * (TT_MAX_D + 1)];
-    cp_async4(va + pi * 64 + col, c.core[0] + ((int64_t)(alpha * c.s[0] + d0) * r1 + col));
+  for (Walk2 w(r1); w.r < np; w.next()) {
+    const int* dd = dig + w.r * (TT_MAX_D + 1);
+    cp_async4(va + w.r * kVS + w.c, c.core[0] + (dd[TT_MAX_D] * c.s[0] + dd[0]) * r1 + w.c);
   }
   for (int k = 0; k < L - 1; ++k)
-    for (int e = threadIdx.x; e < c.r[k + 1]; e += blockDim.x) cp_async4(dg + k * 64 + e, c.diag[k] + e);
+    for (int e = tid; e < c.r[k + 1]; e += kEngThreads) cp_async4(dg + k * 64 + e, c.diag[k] + e);
   for (int k = 1; k <= L - 2; ++k) {
     const int n = c.r[k] * c.s[k] * c.r[k + 1];
-    for (int e = threadIdx.x; e < n; e += blockDim.x) cp_async4(cs[k] + e, c.core[k] + e);
+    for (int e = tid; e < n; e += kEngThreads) cp_async4(cs[k] + e, c.core[k] + e);
   }
   {
-    const int n = rl1 * nq * rL;
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      const int col = e % rL;
-      const int qi = (e / rL) % nq;
-      const int b = e / (rL * nq);
-      cp_async4(cf + e, c.core[L - 1] + ((int64_t)b * sl + q0 + qi) * rL + col);
-    }
+    const int w_ = nq * rL;  // one row b of the slice: C_{L-1}[b, q0:q0+nq, :], contiguous
+    const float* src = c.core[L - 1] + q0 * rL;
+    for (Walk2 w(w_); w.r < rl1; w.next()) cp_async4(cf + w.r * w_ + w.c, src + w.r * sl * rL + w.c);
   }
-  if (t.pack_side) compaction_map(t.s, t.rd, pos, nullptr, nullptr);
   cp_async_wait_all();
   __syncthreads();
   TLU_STAMP(nu, 3);
+  // the chain vectors carry the diagonal that follows them: v <- v * E_0
+  for (Walk2 w(r1); w.r < np; w.next()) va[w.r * kVS + w.c] *= dg[w.c];
+  __syncthreads();
   TLU_STAMP(nu, 4);
-  // steps 1 .. L-2: v <- (v * E_{k-1}) . C_k[:, s_k, :]
+  // steps 1 .. L-2: v <- v . C_k[:, d_k, :] (then times E_k); lanes walk
+  // the columns, so the P_k rows are written coalesced
   for (int k = 1; k <= L - 2; ++k) {
     const int rk = c.r[k], rk1 = c.r[k + 1], sk = c.s[k];
-    const float* Ek = dg + (k - 1) * 64;
-    for (int e = threadIdx.x; e < np * rk1; e += blockDim.x) {
-      const int pi = e / rk1, col = e - (e / rk1) * rk1;
-      const int* dd = dig + pi * (TT_MAX_D + 1);
-      int64_t row = dd[TT_MAX_D];
-      for (int kk = 0; kk <= k; ++kk) row = row * c.s[kk] + dd[kk];
-      const float* Ck = cs[k] + dd[k] * rk1 + col;
-      const float* v = va + pi * 64;
+    const float* Ek = dg + k * 64;
+    const int bstride = sk * rk1;
+    float* prow = (q0 == 0) ? c.prow[k] : nullptr;
+    for (Walk2 w(rk1); w.r < np; w.next()) {
+      const int pi = w.r, col = w.c;
+      const float* Ck = cs[k] + dig[pi * (TT_MAX_D + 1) + k] * rk1 + col;
+      const float* v = va + pi * kVS;
       float a0 = 0.f, a1 = 0.f;
       int b = 0;
       for (; b + 1 < rk; b += 2) {
-        a0 = fmaf(v[b] * Ek[b], Ck[b * sk * rk1], a0);
-        a1 = fmaf(v[b + 1] * Ek[b + 1], Ck[(b + 1) * sk * rk1], a1);
+        a0 = fmaf(v[b], Ck[b * bstride], a0);
+        a1 = fmaf(v[b + 1], Ck[(b + 1) * bstride], a1);
       }
-      if (b < rk) a0 = fmaf(v[b] * Ek[b], Ck[b * sk * rk1], a0);
+      if (b < rk) a0 = fmaf(v[b], Ck[b * bstride], a0);
       const float acc = a0 + a1;
-      vb[pi * 64 + col] = acc;
-      if (q0 == 0 && c.prow[k]) c.prow[k][row * rk1 + col] = acc;
+      vb[pi * kVS + col] = acc * Ek[col];
+      if (prow) prow[rowk[pi * TT_MAX_D + k] * rk1 + col] = acc;
     }
     __syncthreads();
     float* tmp = va;
@@ -320,27 +416,31 @@ __device__ void eng_chain_unit(const EngTask& t, int u, int* pos, float* dsm, in
     vb = tmp;
   }
   TLU_STAMP(nu, 5);
-  // final rows (prefix, q) = (v * E_{L-2}) . C_{L-1}[:, q, :]
-  const float* EL = dg + (L - 2) * 64;
-  const int nout = np * nq * rL;
-  for (int e = threadIdx.x; e < nout; e += blockDim.x) {
-    const int col = e % rL;
-    const int qi = (e / rL) % nq;
-    const int pi = e / (rL * nq);
-    const float* v = va + pi * 64;
-    const float* Cq = cf + qi * rL + col;
-    float a0 = 0.f, a1 = 0.f;
-    int b = 0;
-    for (; b + 1 < rl1; b += 2) {
-      a0 = fmaf(v[b] * EL[b], Cq[b * nq * rL], a0);
-      a1 = fmaf(v[b + 1] * EL[b + 1], Cq[(b + 1) * nq * rL], a1);
+  // final rows (prefix, q) = v . C_{L-1}[:, q, :].  Item (prefix group of
+  // four, z = q * rL + col): lanes walk z, along which both the staged slice
+  // and the output rows are contiguous, so the stores coalesce
+  const int zw = nq * rL;
+  const int npg = (np + 3) >> 2;
+  for (Walk2 w(zw); w.r < npg; w.next()) {
+    const int pi0 = w.r * 4, z = w.c;
+    const int npi = np - pi0 < 4 ? np - pi0 : 4;
+    const float* Cz = cf + z;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int b = 0; b < rl1; ++b) {
+      const float y = Cz[b * zw];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (i < npi) acc[i] = fmaf(va[(pi0 + i) * kVS + b], y, acc[i]);
     }
-    if (b < rl1) a0 = fmaf(v[b] * EL[b], Cq[b * nq * rL], a0);
-    const float acc = a0 + a1;
-    const int64_t f = ((p0 + pi) * sl + q0 + qi) * rL + col;  // flat index into P_{L-1}
-    c.out[f] = acc;
-    if (t.pack_side) {
-      const __nv_bfloat16 bv = __float2bfloat16_rn(acc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i >= npi) break;
+      const float v = acc[i];
+      const int f = ((p0 + pi0 + i) * sl + q0) * rL + z;  // flat index into P_{L-1}
+      c.out[f] = v;
+      if (!t.pack_side) continue;
+      const __nv_bfloat16 bv = __float2bfloat16_rn(v);
       if (t.pack_side == 1) {  // A (N x rd): f = j * rd + a
         const unsigned jj = (unsigned)f / (unsigned)t.rd;
         const int cc = pos[(unsigned)f - jj * (unsigned)t.rd];
@@ -367,8 +467,14 @@ __device__ void eng_gemm_final_unit(const EngTask& t, int u) {
   const int64_t i = (int64_t)u * kEngThreads + threadIdx.x;
   if (i >= g.m * g.n) return;
   const unsigned gm = (unsigned)i / (unsigned)g.n, gn = (unsigned)i - gm * (unsigned)g.n;
+  // all of the split partials in flight at once, summed in split order
+  float pv[kMaxSplits];
+#pragma unroll
+  for (int ks = 0; ks < kMaxSplits; ++ks)
+    pv[ks] = ks < t.splits ? __ldcg(t.partial + (int64_t)ks * g.m * g.n + i) : 0.f;
   float v = 0.f;
-  for (int ks = 0; ks < t.splits; ++ks) v += __ldcg(t.partial + (int64_t)ks * g.m * g.n + i);
+#pragma unroll
+  for (int ks = 0; ks < kMaxSplits; ++ks) v += pv[ks];
   if (g.rscale) v *= g.rscale[gm];
   if (g.cscale) v *= g.cscale[gn % (unsigned)g.clen];
   float* C = static_cast<float*>(g.C);
@@ -410,30 +516,32 @@ __device__ void eng_scale_unit(const EngTask& t, int u) {
   }
 }
 
+constexpr int kEngSmem = kGemmSmem > kChainSmem ? kGemmSmem : kChainSmem;
+
 __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant__ EngProgram prog) {
-  extern __shared__ float eng_dsm[];  // kChainSmem floats, used by kEChain units
-  __shared__ float As[kEK][kET + 1];
-  __shared__ float Bs[kEK][kET + 1];
+  extern __shared__ __align__(16) float eng_dsm[];  // kEngSmem floats: GEMM or chain staging
   __shared__ float red[32];
   __shared__ int pos[RP];
-  __shared__ float ksc[kEK];
-  __shared__ float csc[kET];
-  __shared__ __align__(16) EngProgram p;  // the whole program, copied once per CTA
+  __shared__ float rsc[32], csc[32];
+  // Tasks are read straight from the parameter space: every thread of a warp
+  // reads the same field, which the constant cache broadcasts.  (Copying
+  // the whole program to shared memory first costs several microseconds:
+  // per-lane addresses into parameter space serialise.)
+  const EngProgram& p = prog;
   __shared__ int failed;
   pdl_wait();  // params and workspace may be written by the previous grid
   pdl_trigger();
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(&prog);
-    uint4* dst = reinterpret_cast<uint4*>(&p);
-    for (int i = threadIdx.x; i < (int)(sizeof(EngProgram) / 16); i += blockDim.x) dst[i] = src[i];
-  }
   if (threadIdx.x == 0) {
     failed = 0;
     TL_STAMP(2, 0);
   }
+  // compaction map of D_d, once per CTA, for every gather / pack epilogue
+  if (prog.dmid) compaction_map(prog.dmid, prog.rd, pos, nullptr, nullptr);
   __syncthreads();
 #ifdef TTC_TIMELINE
   int nu = 0;
+#else
+  constexpr int nu = 0;
 #endif
   for (int ph = 0; ph < p.nphases; ++ph) {
     const int t0 = p.phase_begin[ph], t1 = p.phase_begin[ph + 1];
@@ -450,13 +558,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       }
 #endif
       switch (k.kind) {
-        case kEGemm:
-#ifdef TTC_TIMELINE
-          eng_gemm_unit(k, uu, As, Bs, pos, ksc, csc, nu);
-#else
-          eng_gemm_unit(k, uu, As, Bs, pos, ksc, csc, 0);
-#endif
-          break;
+        case kEGemm: eng_gemm_unit(k, uu, pos, eng_dsm, rsc, csc, nu); break;
         case kEGemmFinal: eng_gemm_final_unit(k, uu); break;
         case kEColdot: eng_coldot_unit(k, uu, red); break;
         case kEScale: eng_scale_unit(k, uu); break;
@@ -466,13 +568,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
         case kEDd:
           tc_dd_unit(k.tc, k.s, k.rd, k.out, k.acc);
           break;
-        case kEChain:
-#ifdef TTC_TIMELINE
-          eng_chain_unit(k, uu, pos, eng_dsm, nu);
-#else
-          eng_chain_unit(k, uu, pos, eng_dsm, 0);
-#endif
-          break;
+        case kEChain: eng_chain_unit(k, uu, pos, eng_dsm, nu); break;
         case kEUnpack:
           tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
           break;
@@ -518,27 +614,45 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 size_t eng_partial_floats(int64_t m, int64_t n, int64_t k) {
   (void)k;
-  return (size_t)(m * n) * 16;  // at most 16 K-splits
+  // splits happen only below 128 tiles of at most 32 x 32, with at most
+  // ceil(128 / tiles) splits: splits * m * n < 2 * 128 * 1024
+  const size_t full = (size_t)(m * n) * kMaxSplits;
+  const size_t bound = (size_t)2 * 128 * 1024;
+  return full < bound ? full : bound;
 }
 
-void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap) {
+void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap,
+                   bool atomic_splits) {
   t->kind = kEGemm;
   t->g = g;
-  const int64_t tiles = ceil_div(g.m, kET) * ceil_div(g.n, kET);
+  // 32 x 32 tiles, narrowed to 16 where a side is short or where the task
+  // would otherwise leave most of the grid idle
+  int tm = g.m <= 16 ? 16 : 32, tn = g.n <= 16 ? 16 : 32;
+  auto tiles = [&] { return ceil_div(g.m, tm) * ceil_div(g.n, tn); };
+  while (tiles() < 96 && (tm > 16 || tn > 16)) {
+    if (tm > 16 && (tm >= tn || tn == 16)) tm = 16;
+    else tn = 16;
+  }
+  t->tm = tm;
+  t->tn = tn;
   int64_t splits = 1;
-  // split long reductions so that a phase has a few units per SM and each
-  // unit still walks at least a few K slices
-  if (partial_ws && tiles < 256) {
-    const int64_t want = ceil_div(256, tiles);
-    const int64_t maxs = ceil_div(g.k, kEK);
+  // split long reductions so that a phase has about one unit per SM and
+  // each split keeps >= 48 of K: into partials that a later phase sums, or
+  // (atomic_splits, g.mode == kAtomic) straight into a zeroed C
+  const bool atomic = atomic_splits && g.mode == kAtomic;
+  if ((partial_ws || atomic) && tiles() < 128) {
+    const int64_t want = ceil_div(128, tiles());
+    const int64_t maxs = ceil_div(g.k, 48);
     splits = want < maxs ? want : maxs;
-    if (splits > 16) splits = 16;
-    if ((size_t)(splits * g.m * g.n) > partial_cap) splits = 1;
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    if (!atomic && (size_t)(splits * g.m * g.n) > partial_cap) splits = 1;
     if (splits < 1) splits = 1;
   }
   t->splits = (int)splits;
-  t->partial = splits > 1 ? partial_ws : nullptr;
-  t->units = (int)(tiles * splits);
+  t->partial = (splits > 1 && !atomic) ? partial_ws : nullptr;
+  t->units = (int)(tiles() * splits);
+  t->tiles_n = (int)ceil_div(g.n, tn);
+  t->kchunk = (int)ceil_div(g.k, splits);
 }
 
 void eng_dd_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
@@ -613,15 +727,25 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (cudaFuncSetAttribute(eng_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kChainSmem * sizeof(float))) != cudaSuccess)
+                             (int)(kEngSmem * sizeof(float))) != cudaSuccess)
       return cudaErrorLaunchFailure;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, eng_kernel, kEngThreads,
-                                                  kChainSmem * sizeof(float));
+                                                  kEngSmem * sizeof(float));
     grid = sms * (per > 0 ? 1 : 0);
     if (grid <= 0) return cudaErrorLaunchFailure;
   }
   EngProgram p = prog;
   p.slot = next_slot.fetch_add(1) % kBarSlots;
+  // the one D_d that the program's gather and pack epilogues compact by
+  p.dmid = nullptr;
+  for (int i = 0; i < p.ntasks; ++i) {
+    const EngTask& k = p.t[i];
+    if ((k.kind == kEGemm || k.kind == kEChain) && (k.gather || k.pack_side)) {
+      if (p.dmid && (p.dmid != k.s || p.rd != k.rd)) return cudaErrorInvalidValue;
+      p.dmid = k.s;
+      p.rd = k.rd;
+    }
+  }
   int g = grid;
   bool coop = true;
 #ifdef TTC_TIMELINE
@@ -629,7 +753,7 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
   if (const char* e = getenv("TTC_ENG_GRID")) g = atoi(e) > 0 && atoi(e) < grid ? atoi(e) : grid;
   if (getenv("TTC_ENG_NONCOOP")) coop = false;
 #endif
-  cudaError_t e = launch_ex(eng_kernel, dim3(g), dim3(kEngThreads), kChainSmem * sizeof(float), st,
+  cudaError_t e = launch_ex(eng_kernel, dim3(g), dim3(kEngThreads), kEngSmem * sizeof(float), st,
                             coop, p);
   count_launches(1);
   return e;

@@ -42,6 +42,9 @@ struct alignas(16) EngTask {
   int kind = 0;
   int units = 0;
   int splits = 1;       // kEGemm / kEGemmFinal
+  int tm = 32, tn = 32; // kEGemm output tile (16 or 32 each)
+  int tiles_n = 1;      // kEGemm: tiles along n
+  int kchunk = 0;       // kEGemm: K extent of one split
   int pad = 0;
   GemmArgs g;           // kEGemm / kEGemmFinal
   float* partial = nullptr;  // split-K partials [splits][m][n]
@@ -68,12 +71,15 @@ struct alignas(16) EngTask {
   ChainDesc ch;  // kEChain (pack_side selects the packing, s = D_d)
 };
 
-constexpr int kEngMaxTasks = 20;
+constexpr int kEngMaxTasks = 28;
 constexpr int kEngMaxPhases = 8;
 
 struct alignas(16) EngProgram {
   int ntasks = 0, nphases = 0;
   unsigned slot = 0;  // grid-barrier slot (set by eng_launch)
+  int rd = 0;         // middle rank of dmid
+  const float* dmid = nullptr;  // D_d whose compaction map the gather / pack
+                                // epilogues use (set by eng_launch)
   int phase_begin[kEngMaxPhases + 1] = {};
   EngTask t[kEngMaxTasks];
 };
@@ -88,7 +94,10 @@ struct EngBuilder {
 };
 
 // Units for a GEMM task of the engine's tile size and a split-K count.
-void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap);
+// atomic_splits: a kAtomic GEMM may be split along K, every split adding
+// into C (which must be zero before the phase).
+void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap,
+                   bool atomic_splits = false);
 void eng_gemm_final_task(EngTask* t, const EngTask& gemm);
 // false when the chain does not fit the unit's shared-memory staging
 bool eng_chain_task(EngTask* t, const ChainDesc& c);

@@ -1219,6 +1219,23 @@ extern "C" int ttc_timeline_read(void* host, size_t bytes) {
 extern "C" int ttc_timeline_units_read(void* host, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(host, ttc::g_tlu, bytes);
 }
+static cudaStream_t g_probe_stream = 0;
+extern "C" void ttc_probe_set_stream(void* st) { g_probe_stream = static_cast<cudaStream_t>(st); }
+// An empty kernel of the same parameter size as the engine, and one with none.
+__global__ void probe_big_param(const __grid_constant__ ttc::EngProgram p) {
+  if (threadIdx.x == 0 && p.ntasks == 12345) ttc::g_status.code = 1;
+}
+__global__ void probe_small_param(int v) {
+  if (threadIdx.x == 0 && v == 12345) ttc::g_status.code = 1;
+}
+extern "C" int ttc_probe_empty(int big, int coop, int grid, int threads, int smem) {
+  ttc::EngProgram p;
+  cudaFuncSetAttribute(probe_big_param, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaFuncSetAttribute(probe_small_param, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (big)
+    return (int)ttc::launch_ex(probe_big_param, dim3(grid), dim3(threads), smem, g_probe_stream, coop != 0, p);
+  return (int)ttc::launch_ex(probe_small_param, dim3(grid), dim3(threads), smem, g_probe_stream, coop != 0, 0);
+}
 // Engine microbenchmark (timeline builds only): one program of `phases`
 // phases, each holding `ntasks` GEMM tasks of m x n x k (f32, all operands
 // in the given device buffer), or empty units when m == 0.
@@ -1237,16 +1254,19 @@ extern "C" int ttc_probe_engine(int phases, int ntasks, int units_if_empty, long
         continue;
       }
       GemmArgs g;
+      // split == 2: every phase reads its own operands (no reuse of cached lines)
+      const size_t po = split == 2 ? (size_t)ph * (m * k + k * n + m * n) : 0;
       g.m = m; g.n = n; g.k = k;
-      g.A = f; g.sam = k; g.sak = 1;
-      g.B = f + m * k; g.sbk = n; g.sbn = 1;
-      g.C = f + m * k + k * n + (size_t)t * m * n; g.scm = n; g.scn = 1;
-      eng_gemm_task(task, g, split ? f + 4 * (m * k + k * n) + (size_t)t * m * n * 16 : nullptr,
-                    split ? (size_t)m * n * 16 : 0);
+      g.A = f + po; g.sam = k; g.sak = 1;
+      g.B = f + po + m * k; g.sbk = n; g.sbn = 1;
+      g.C = f + po + m * k + k * n + (size_t)t * m * n; g.scm = n; g.scn = 1;
+      const bool sp = split == 1;
+      eng_gemm_task(task, g, sp ? f + 4 * (m * k + k * n) + (size_t)t * m * n * 16 : nullptr,
+                    sp ? (size_t)m * n * 16 : 0);
     }
   }
   b.end();
-  return (int)eng_launch(b.p, 0);
+  return (int)eng_launch(b.p, g_probe_stream);
 }
 
 extern "C" int ttc_timeline_units_clear(void) {

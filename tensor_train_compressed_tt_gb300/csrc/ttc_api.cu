@@ -68,6 +68,12 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
     u *= p.s[k];
     p.U[k] = u;
   }
+  // the merge kernels index every matrix they touch in 32 bits: the packed
+  // parameters, each prefix product (U_k x r_{k+1}, A and B among them)
+  constexpr int64_t kMax32 = (int64_t)1 << 31;
+  if ((int64_t)p.n_floats >= kMax32) return TT_ERR_UNSUPPORTED;
+  for (int k = 0; k < p.K; ++k)
+    if (p.U[k] * p.r[k + 1] >= kMax32) return TT_ERR_UNSUPPORTED;
   *L = p;
   return TT_OK;
 }
@@ -76,7 +82,8 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
 struct WsLayout {
   size_t P[kMaxK] = {};  // merged chain prefixes (floats), 0 where aliased to params
   size_t dA = 0, dB = 0;
-  size_t q[4] = {};      // reverse-chain dQ ping-pong buffers (input side 0/1, output 2/3)
+  size_t q = 0;          // reverse-chain dQ buffers: step j of side s at q + (2j + s) * qstride
+  size_t qstride = 0;    // floats between dQ buffers
   size_t part[4] = {};   // split-K partials (input side 0/1, output 2/3)
   size_t part_cap = 0;   // floats per partial buffer
   size_t z = 0, dzp = 0; // SIMT token path intermediates
@@ -104,7 +111,8 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   }
   w->dA = take((size_t)L.N * L.rd * sizeof(float));
   w->dB = take((size_t)L.rd * L.M * sizeof(float));
-  for (int i = 0; i < 4; ++i) w->q[i] = take(qmax * sizeof(float));
+  w->qstride = align_up(qmax * sizeof(float), 256) / sizeof(float);
+  w->q = take(2 * (TT_MAX_D - 1) * w->qstride * sizeof(float));
   for (int i = 0; i < 4; ++i) w->part[i] = take(pmax * sizeof(float));
   w->part_cap = pmax;
   const bool tc = !simt_tokens && tc_supported(L) && L.act == TT_DT_BF16;
@@ -159,6 +167,28 @@ void chain_ptrs(const LayerPlan& L, const float* params, void* ws, const WsLayou
 }
 
 // ---- merge programs ---------------------------------------------------------
+// out[0 .. n) = 0 as one engine task.
+void eng_zero_task(EngBuilder& b, float* out, int64_t n) {
+  EngTask* z = b.add();
+  z->kind = kEScale;
+  z->n = n;
+  z->units = (int)((n + 1023) / 1024);
+  z->x = nullptr;
+  z->out = out;
+  z->acc = 0;
+}
+
+// dQ of reverse step j on side s (0 input, 1 output).  The steps j >= 1 and,
+// for chains of three or more cores a side, step 0 add their K splits
+// atomically: step 0's pair of buffers is zeroed by every merge that
+// precedes a backward (forward merge with zero_grads) and again by the
+// backward merge once read; the later steps are zeroed by the backward merge
+// in its first phase.
+float* dq_buf(void* ws, const WsLayout& w, int j, int side) {
+  return fptr(ws, w.q) + (size_t)(2 * j + side) * w.qstride;
+}
+
+
 // Forward merge: phase j computes P_j (input side) and P_{d+j} (output side).
 // On the tensor-core path the GEMMs that produce A and B also write the
 // compacted bf16 operands, and the first phase writes the padding and the
@@ -178,6 +208,7 @@ tt_status run_merge_forward_gemm(const LayerPlan& L, const float* params, void* 
   for (int j = 1; j < L.d; ++j) {
     b.begin_phase();
     if (pack && j == 1) eng_pack_task(b.add(), L, nullptr, nullptr, Dmid, tc, zero_grads, true);
+    if (zero_grads && j == 1 && L.d >= 3) eng_zero_task(b, dq_buf(ws, w, 0, 0), 2 * w.qstride);
     for (int k : {j, L.d + j}) {
       GemmArgs g;
       g.m = L.U[k - 1];
@@ -219,6 +250,7 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
     // one phase: each side's rows recomputed per prefix (no grid barrier);
     // padding, metadata and the zeroed token sums come from the pack task
     if (pack) eng_pack_task(b.add(), L, nullptr, nullptr, Dmid, tc, zero_grads, true);
+    if (zero_grads && L.d >= 3) eng_zero_task(b, dq_buf(ws, w, 0, 0), 2 * w.qstride);
     for (int side = 0; side < 2; ++side) {
       const int k0 = side == 0 ? 0 : L.d;
       ChainDesc c;
@@ -280,20 +312,24 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
     int k_first, k_last;
     const float* Y;
     const float* yscale;
-    int qi, pi;          // base index of q / part buffers
+    int qs, pi;          // side index of the dQ buffers, base index of part buffers
     int flip;
     EngTask pending;     // split GEMM whose partials the next phase reduces
     bool has_pending;
     const float* dQ;     // last dQ (for coldot in the next phase)
     int coldot_k;        // link whose dD the next phase computes (-1: none)
   } sides[2] = {{0, L.d - 1, dA, nullptr, 0, 0, 0, EngTask(), false, nullptr, -1},
-                {L.d, L.K - 1, dB, nullptr, 2, 2, 0, EngTask(), false, nullptr, -1}};
+                {L.d, L.K - 1, dB, nullptr, 1, 2, 0, EngTask(), false, nullptr, -1}};
   const int mode = acc ? kAccumulate : kStore;
   for (int j = 0; j <= steps; ++j) {
     b.begin_phase();
     if (unpack && steps > 0 && j == 0)
       eng_dd_task(b.add(), L, tc, params + L.diag_off[L.d - 1], dparams + L.diag_off[L.d - 1],
                   acc);
+    // dQ buffers of the steps after the first: zero before they are added to
+    if (j == 0 && steps >= 2) eng_zero_task(b, dq_buf(ws, w, 1, 0), 2 * (steps - 1) * w.qstride);
+    // step 0's pair, last read in phase 1: zero again for the next backward
+    if (j == 2) eng_zero_task(b, dq_buf(ws, w, 0, 0), 2 * w.qstride);
     for (Side& sd : sides) {
       // work left over from the previous step
       if (sd.has_pending) {
@@ -341,15 +377,17 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
           sd.pending = *t;
           sd.has_pending = true;
         }
-        float* dQ = fptr(ws, w.q[sd.qi + (sd.flip & 1)]);
+        float* dQ = dq_buf(ws, w, j, sd.qs);
+        const bool atomic_q = j >= 1 || steps >= 2;
         GemmArgs h;  // dQ = Y G_k^T
         h.m = U; h.n = rk; h.k = ncol;
         h.A = sd.Y; h.sam = ncol; h.sak = 1;
         h.kscale = sd.yscale; h.klen = rk1;
         h.B = params + L.core_off[k]; h.sbk = 1; h.sbn = ncol;
         h.C = dQ; h.scm = rk; h.scn = 1;
+        h.mode = atomic_q ? kAtomic : kStore;
         EngTask* th = b.add();
-        eng_gemm_task(th, h, nullptr, 0);
+        eng_gemm_task(th, h, nullptr, 0, atomic_q);
         if (gat) {
           th->gather = gat;
           th->gather_op = 0;
@@ -366,18 +404,9 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
       } else {
         if (rezero && &sd == &sides[0]) {
           // leave the token sums zeroed for the next backward that reuses
-          // this workspace's merge (they were last read before a barrier)
-          const float* bufs[3] = {tc.dAc, tc.dBc, tc.dDc};
-          const int64_t lens[3] = {L.N * 64, 64 * L.M, 64};
-          for (int q = 0; q < 3; ++q) {
-            EngTask* z = b.add();
-            z->kind = kEScale;
-            z->n = lens[q];
-            z->units = (int)((z->n + 1023) / 1024);
-            z->x = nullptr;
-            z->out = const_cast<float*>(bufs[q]);
-            z->acc = 0;
-          }
+          // this workspace's merge (they were last read before a barrier);
+          // dAc, dBc and dDc are adjacent
+          eng_zero_task(b, const_cast<float*>(tc.dAc), (L.N + L.M + 1) * 64);
         }
         // first core of the side
         EngTask* t = b.add();
