@@ -14,11 +14,13 @@ constexpr int kEngThreads = 512;
 constexpr int kEngWarps = kEngThreads / 32;
 constexpr int kGK = 512;    // GEMM: K extent staged per pass
 constexpr int kGLd = 36;    // GEMM: shared row stride (floats) of a staged [k][m] tile
-// GEMM unit dynamic shared memory: A and B tiles, K scales, k-group partials
-constexpr int kGemmSmem = 2 * kGK * kGLd + kGK + kEngThreads * 16;
+// GEMM unit dynamic shared memory: A and B tiles, K scales, k-group
+// partials, the folded coldot's operand tile and column sums
+constexpr int kGemmSmem = 2 * kGK * kGLd + kGK + kEngThreads * 16 + 32 * 32 + 32;
 constexpr int kBarSlots = 64;
 constexpr int kMaxSplits = 32;  // split-K partials of one GEMM task
 static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
+static_assert(kEngThreads == 512, "k-group shifts assume 512 threads");
 // Grid barrier: one monotonic 64-bit arrival counter per slot (own
 // 128-byte line).  A CTA's own atomicAdd tells it which barrier generation
 // it joined, so the target it waits for needs no extra read and the counter
@@ -144,6 +146,16 @@ __device__ __forceinline__ void eng_stage(float* S, int rows, int kc, int r0, in
   }
 }
 
+// The compaction map of D_d (pos[a]: compacted column of rank a, or -1),
+// built on first use by a unit of this CTA: a unit calls it after issuing its
+// own copies, so the load of D_d overlaps them.  Uniform across the CTA.
+__device__ __forceinline__ void ensure_pos(const EngProgram& p, int* pos, int* pos_ready) {
+  if (*pos_ready) return;
+  compaction_map(p.dmid, p.rd, pos, nullptr, nullptr);
+  if (threadIdx.x == 0) *pos_ready = 1;
+  __syncthreads();
+}
+
 // One tm x tn output tile of C over one K split.  The whole K range (in
 // passes of kGK) is staged into shared memory with one round of
 // asynchronous copies; the kEngThreads threads then split K into
@@ -151,16 +163,16 @@ __device__ __forceinline__ void eng_stage(float* S, int rows, int kc, int r0, in
 // partials are summed in a fixed order (deterministic).  Tile counts and
 // the split length come from the host; the unit's own index arithmetic is
 // 32-bit shifts and masks.
-__device__ void eng_gemm_unit(const EngTask& t, int u, const int* pos, float* dsm, float* rsc,
-                              float* csc, int nu) {
+__device__ void eng_gemm_unit(const EngProgram& prog, const EngTask& t, int u, int* pos,
+                              int* pos_ready, float* dsm, float* rsc, float* csc, int nu) {
   (void)nu;
   TLU_STAMP(nu, 6);
   const GemmArgs& g = t.g;
   const int S = t.splits, TM = t.tm, TN = t.tn;
   const int m = (int)g.m, n = (int)g.n, K = (int)g.k;
-  const int ks = S > 1 ? u % S : 0;
-  const int tile = S > 1 ? u / S : u;
-  const int ti = tile / t.tiles_n;
+  const int tile = (int)(((unsigned long long)(unsigned)u * t.div_s_mul) >> t.div_s_sh);
+  const int ks = u - tile * S;
+  const int ti = (int)(((unsigned long long)(unsigned)tile * t.div_n_mul) >> t.div_n_sh);
   const int m0 = ti * TM, n0 = (tile - ti * t.tiles_n) * TN;
   const int kb = ks * t.kchunk;
   const int ke = kb + t.kchunk < K ? kb + t.kchunk : K;
@@ -170,6 +182,8 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, const int* pos, float* ds
   float* Bs = As + kGK * kGLd;
   float* ksc = Bs + kGK * kGLd;
   float* red = ksc + kGK;
+  float* ptile = red + kEngThreads * 16;  // fold: P tile, laid out like red's first group
+  float* csum = ptile + 32 * 32;          // fold: column sums of P * v
   const int tid = threadIdx.x;
   const int lgtn4 = TN == 32 ? 3 : 2, lgtn = lgtn4 + 2;
   const int lgG = (TM == 32 ? 3 : 2) + lgtn4;
@@ -190,13 +204,26 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, const int* pos, float* ds
     if (g.cscale && j < nrem) cp_async4(csc + j, g.cscale + (unsigned)(n0 + j) % (unsigned)g.clen);
     else csc[j] = 1.f;
   }
+  const bool fold = t.fold_g != nullptr;
+  if (fold) {
+    for (int o = tid; o < TM * TN; o += kEngThreads) {
+      const int i = o >> (TN == 32 ? 5 : 4), j = o & (TN - 1);
+      if (i < mrem && j < nrem)
+        cp_async4(ptile + o, t.fold_p + (m0 + i) * (int)g.scm + (n0 + j) * (int)g.scn);
+    }
+    if (tid < TN) csum[tid] = 0.f;
+  }
   float acc[4][4] = {};
   for (int k0 = kb; k0 < ke; k0 += kGK) {
     const int kc = ke - k0 < kGK ? ke - k0 : kGK;
     if (k0 != kb) __syncthreads();  // the previous pass's reads are done
     if (k0 == kb) TLU_STAMP(nu, 7);
-    eng_stage(As, TM, kc, m0, k0, m, A, (int)g.sam, (int)g.sak, t, pos, gA);
-    eng_stage(Bs, TN, kc, n0, k0, n, B, (int)g.sbn, (int)g.sbk, t, pos, gB);
+    // the operand that needs no compaction map goes first
+    if (!gA) eng_stage(As, TM, kc, m0, k0, m, A, (int)g.sam, (int)g.sak, t, pos, false);
+    if (!gB) eng_stage(Bs, TN, kc, n0, k0, n, B, (int)g.sbn, (int)g.sbk, t, pos, false);
+    if (t.gather || t.pack_side) ensure_pos(prog, pos, pos_ready);
+    if (gA) eng_stage(As, TM, kc, m0, k0, m, A, (int)g.sam, (int)g.sak, t, pos, true);
+    if (gB) eng_stage(Bs, TN, kc, n0, k0, n, B, (int)g.sbn, (int)g.sbk, t, pos, true);
     if (g.kscale) {
       const unsigned kl = (unsigned)g.klen;
       for (int k = tid; k < kc; k += kEngThreads)
@@ -207,7 +234,7 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, const int* pos, float* ds
     __syncthreads();
     if (k0 == kb) TLU_STAMP(nu, 4);
     if (active) {
-      const int per = (kc + kg - 1) / kg;
+      const int per = (kc + kg - 1) >> (9 - lgG);  // kg = 2^(9 - lgG)
       const int k1 = grp * per;
       const int k2 = k1 + per < kc ? k1 + per : kc;
       const float* ap = As + ty * 4;
@@ -247,6 +274,11 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, const int* pos, float* ds
     for (int q = 0; q < kEngThreads / 16; ++q)
       if (q < kg) v += red[q * tsz + o];
     const int gm = m0 + i, gn = n0 + j;
+    if (fold) {  // last reverse step: the first core's dG and dD, no dQ
+      atomicAdd(t.fold_g + gm * scm + gn * scn, v * csc[j]);
+      if (csc[j] != 0.f) atomicAdd(&csum[j], ptile[o] * v);
+      continue;
+    }
     if (S > 1 && g.mode != kAtomic) {
       t.partial[(ks * m + gm) * n + gn] = v;
       continue;
@@ -279,6 +311,10 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, const int* pos, float* ds
         }
       }
     }
+  }
+  if (fold) {
+    __syncthreads();
+    if (tid < nrem && csc[tid] != 0.f) atomicAdd(t.fold_dd + n0 + tid, csum[tid]);
   }
   __syncthreads();  // shared memory is reused by the next unit
 }
@@ -324,7 +360,8 @@ struct Walk2 {
   }
 };
 
-__device__ void eng_chain_unit(const EngTask& t, int u, const int* pos, float* dsm, int nu) {
+__device__ void eng_chain_unit(const EngProgram& prog, const EngTask& t, int u, int* pos,
+                               int* pos_ready, float* dsm, int nu) {
   (void)nu;
   const ChainDesc& c = t.ch;
   const int L = c.L;
@@ -381,6 +418,7 @@ __device__ void eng_chain_unit(const EngTask& t, int u, const int* pos, float* d
     const float* src = c.core[L - 1] + q0 * rL;
     for (Walk2 w(w_); w.r < rl1; w.next()) cp_async4(cf + w.r * w_ + w.c, src + w.r * sl * rL + w.c);
   }
+  if (t.pack_side) ensure_pos(prog, pos, pos_ready);
   cp_async_wait_all();
   __syncthreads();
   TLU_STAMP(nu, 3);
@@ -533,10 +571,10 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
   pdl_trigger();
   if (threadIdx.x == 0) {
     failed = 0;
-    TL_STAMP(2, 0);
+    TL_STAMP(p.nphases == 1 ? 2 : 3, 0);
   }
-  // compaction map of D_d, once per CTA, for every gather / pack epilogue
-  if (prog.dmid) compaction_map(prog.dmid, prog.rd, pos, nullptr, nullptr);
+  __shared__ int pos_ready;  // the compaction map is built on first use
+  if (threadIdx.x == 0) pos_ready = 0;
   __syncthreads();
 #ifdef TTC_TIMELINE
   int nu = 0;
@@ -558,7 +596,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       }
 #endif
       switch (k.kind) {
-        case kEGemm: eng_gemm_unit(k, uu, pos, eng_dsm, rsc, csc, nu); break;
+        case kEGemm: eng_gemm_unit(p, k, uu, pos, &pos_ready, eng_dsm, rsc, csc, nu); break;
         case kEGemmFinal: eng_gemm_final_unit(k, uu); break;
         case kEColdot: eng_coldot_unit(k, uu, red); break;
         case kEScale: eng_scale_unit(k, uu); break;
@@ -568,7 +606,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
         case kEDd:
           tc_dd_unit(k.tc, k.s, k.rd, k.out, k.acc);
           break;
-        case kEChain: eng_chain_unit(k, uu, pos, eng_dsm, nu); break;
+        case kEChain: eng_chain_unit(p, k, uu, pos, &pos_ready, eng_dsm, nu); break;
         case kEUnpack:
           tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
           break;
@@ -580,9 +618,9 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       ++nu;
 #endif
     }
-    if (threadIdx.x == 0) TL_STAMP(2, 1 + 2 * ph);
+    if (threadIdx.x == 0) TL_STAMP(p.nphases == 1 ? 2 : 3, 1 + 2 * ph);
     if (ph + 1 < p.nphases && !eng_grid_barrier(p.slot, gridDim.x, &failed)) return;
-    if (threadIdx.x == 0) TL_STAMP(2, 2 + 2 * ph);
+    if (threadIdx.x == 0) TL_STAMP(p.nphases == 1 ? 2 : 3, 2 + 2 * ph);
   }
 }
 
@@ -590,7 +628,19 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
 
 // ---- host side -------------------------------------------------------------
 
+int eng_sm_count() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    sms = n > 0 ? n : 1;
+  }
+  return sms;
+}
+
 void EngBuilder::begin_phase() {
+  if (p.nphases > 0) balance(eng_sm_count());
   if (p.nphases >= kEngMaxPhases) {
     overflow = true;
     return;
@@ -608,7 +658,10 @@ EngTask* EngBuilder::add() {
   return &p.t[p.ntasks++];
 }
 
-void EngBuilder::end() { p.phase_begin[p.nphases] = p.ntasks; }
+void EngBuilder::end() {
+  if (p.nphases > 0) balance(eng_sm_count());
+  p.phase_begin[p.nphases] = p.ntasks;
+}
 
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -621,38 +674,99 @@ size_t eng_partial_floats(int64_t m, int64_t n, int64_t k) {
   return full < bound ? full : bound;
 }
 
+// x / d for 0 <= x < 2^31 as (x * mul) >> sh: with l = ceil(log2 d) and
+// mul = ceil(2^(31+l) / d), x * mul / 2^(31+l) exceeds x / d by less than
+// 2^31 / 2^(31+l) <= 1 / d, which never reaches the next integer.
+static void eng_divisor(int d, unsigned long long* mul, int* sh) {
+  int l = 0;
+  while ((1ll << l) < d) ++l;
+  const unsigned long long num = 1ull << (31 + l);
+  *mul = (num + (unsigned long long)d - 1) / (unsigned long long)d;
+  *sh = 31 + l;
+}
+
+// Tile (16 or 32 a side) and split choice: the configuration with the most
+// units not above max_units (ties: larger tiles, then fewer splits); if none
+// fits, the one with the fewest units.  A split keeps >= 48 of K.
+static void eng_gemm_config(EngTask* t, int max_units) {
+  const GemmArgs& g = t->g;
+  const bool atomic = t->atomic_splits && g.mode == kAtomic;
+  const bool can_split = atomic || t->partial != nullptr;
+  int64_t maxs = can_split ? ceil_div(g.k, 48) : 1;
+  if (maxs > kMaxSplits) maxs = kMaxSplits;
+  if (maxs < 1) maxs = 1;
+  int64_t fit_u = -1, min_u = -1;
+  int fit[3] = {32, 32, 1}, mn[3] = {32, 32, 1};
+  for (int tm : {32, 16}) {
+    if (tm == 32 && g.m <= 16) continue;
+    for (int tn : {32, 16}) {
+      if (tn == 32 && g.n <= 16) continue;
+      const int64_t tiles = ceil_div(g.m, tm) * ceil_div(g.n, tn);
+      for (int64_t s = 1; s <= maxs; ++s) {
+        if (s > 1 && !atomic && s * g.m * g.n > t->pcap) break;
+        const int64_t u = tiles * s;
+        if (u <= max_units && (u > fit_u || (u == fit_u && tm * tn > fit[0] * fit[1]))) {
+          fit_u = u;
+          fit[0] = tm; fit[1] = tn; fit[2] = (int)s;
+        }
+        if (min_u < 0 || u < min_u || (u == min_u && tm * tn > mn[0] * mn[1])) {
+          min_u = u;
+          mn[0] = tm; mn[1] = tn; mn[2] = (int)s;
+        }
+      }
+    }
+  }
+  const int* c = fit_u >= 0 ? fit : mn;
+  t->tm = c[0];
+  t->tn = c[1];
+  t->splits = c[2];
+  t->units = (int)(ceil_div(g.m, c[0]) * ceil_div(g.n, c[1]) * c[2]);
+  t->tiles_n = (int)ceil_div(g.n, c[1]);
+  t->kchunk = (int)ceil_div(g.k, c[2]);
+  eng_divisor(t->splits, &t->div_s_mul, &t->div_s_sh);
+  eng_divisor(t->tiles_n, &t->div_n_mul, &t->div_n_sh);
+}
+
 void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap,
-                   bool atomic_splits) {
+                   bool atomic_splits, int max_units) {
   t->kind = kEGemm;
   t->g = g;
-  // 32 x 32 tiles, narrowed to 16 where a side is short or where the task
-  // would otherwise leave most of the grid idle
-  int tm = g.m <= 16 ? 16 : 32, tn = g.n <= 16 ? 16 : 32;
-  auto tiles = [&] { return ceil_div(g.m, tm) * ceil_div(g.n, tn); };
-  while (tiles() < 96 && (tm > 16 || tn > 16)) {
-    if (tm > 16 && (tm >= tn || tn == 16)) tm = 16;
-    else tn = 16;
+  t->atomic_splits = atomic_splits ? 1 : 0;
+  // split-K partials (for a final task in a later phase) unless the splits
+  // add atomically; the device reads `partial` only when splits > 1
+  t->partial = (atomic_splits && g.mode == kAtomic) ? nullptr : partial_ws;
+  t->pcap = t->partial ? (int64_t)partial_cap : 0;
+  eng_gemm_config(t, max_units);
+}
+
+void EngBuilder::balance(int budget) {
+  const int t0 = p.phase_begin[p.nphases - 1];
+  // nothing to gain when even the narrowest configuration needs two waves
+  int64_t min_total = 0;
+  for (int i = t0; i < p.ntasks; ++i) {
+    EngTask probe = p.t[i];
+    if (probe.kind == kEGemm) eng_gemm_config(&probe, 0);
+    min_total += probe.units;
   }
-  t->tm = tm;
-  t->tn = tn;
-  int64_t splits = 1;
-  // split long reductions so that a phase has about one unit per SM and
-  // each split keeps >= 48 of K: into partials that a later phase sums, or
-  // (atomic_splits, g.mode == kAtomic) straight into a zeroed C
-  const bool atomic = atomic_splits && g.mode == kAtomic;
-  if ((partial_ws || atomic) && tiles() < 128) {
-    const int64_t want = ceil_div(128, tiles());
-    const int64_t maxs = ceil_div(g.k, 48);
-    splits = want < maxs ? want : maxs;
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    if (!atomic && (size_t)(splits * g.m * g.n) > partial_cap) splits = 1;
-    if (splits < 1) splits = 1;
+  if (min_total > budget) return;
+  for (int iter = 0; iter < 64; ++iter) {
+    int64_t total = 0;
+    for (int i = t0; i < p.ntasks; ++i) total += p.t[i].units;
+    if (total <= budget) return;
+    // shrink the GEMM task with the most units that can still shrink
+    int best = -1;
+    for (int i = t0; i < p.ntasks; ++i) {
+      EngTask& k = p.t[i];
+      if (k.kind != kEGemm || (best >= 0 && k.units <= p.t[best].units)) continue;
+      EngTask probe = k;
+      eng_gemm_config(&probe, 0);  // fewest units
+      if (probe.units < k.units) best = i;
+    }
+    if (best < 0) return;
+    EngTask& k = p.t[best];
+    const int64_t want = k.units - (total - budget);
+    eng_gemm_config(&k, (int)(want > 0 ? want : 0));
   }
-  t->splits = (int)splits;
-  t->partial = (splits > 1 && !atomic) ? partial_ws : nullptr;
-  t->units = (int)(tiles() * splits);
-  t->tiles_n = (int)ceil_div(g.n, tn);
-  t->kchunk = (int)ceil_div(g.k, splits);
 }
 
 void eng_dd_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,

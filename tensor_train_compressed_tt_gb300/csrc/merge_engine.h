@@ -45,7 +45,12 @@ struct alignas(16) EngTask {
   int tm = 32, tn = 32; // kEGemm output tile (16 or 32 each)
   int tiles_n = 1;      // kEGemm: tiles along n
   int kchunk = 0;       // kEGemm: K extent of one split
-  int pad = 0;
+  int atomic_splits = 0;  // kEGemm: K splits may add into C (mode kAtomic)
+  int64_t pcap = 0;     // kEGemm: floats of the split-K partial buffer `partial`
+  // kEGemm: division by splits and by tiles_n as a multiply and a shift
+  // (x / d == (x * mul) >> sh for 0 <= x < 2^31)
+  unsigned long long div_s_mul = 0, div_n_mul = 0;
+  int div_s_sh = 0, div_n_sh = 0;
   GemmArgs g;           // kEGemm / kEGemmFinal
   float* partial = nullptr;  // split-K partials [splits][m][n]
   // kEColdot / kEScale / pack / unpack operands
@@ -68,10 +73,17 @@ struct alignas(16) EngTask {
   //  gather 1/2: the operand that reads dA / dB (gather_op 0 = A, 1 = B)
   //    reads the compacted token sums tc.dAc / tc.dBc instead.
   int pack_side = 0, gather = 0, gather_op = 0, pad_only = 0;
+  //  fold_g: the GEMM is the last reverse step of a side, C = dQ is not
+  //    stored; each output v (row, c) adds v * cscale[c] to fold_g (the
+  //    first core's gradient, laid out like C) and fold_p[row, c] * v to
+  //    fold_dd[c] (dD of the first link, skipped where cscale[c] == 0).
+  float* fold_g = nullptr;
+  const float* fold_p = nullptr;
+  float* fold_dd = nullptr;
   ChainDesc ch;  // kEChain (pack_side selects the packing, s = D_d)
 };
 
-constexpr int kEngMaxTasks = 28;
+constexpr int kEngMaxTasks = 36;
 constexpr int kEngMaxPhases = 8;
 
 struct alignas(16) EngProgram {
@@ -88,16 +100,22 @@ struct alignas(16) EngProgram {
 struct EngBuilder {
   EngProgram p;
   bool overflow = false;
-  void begin_phase();
+  void begin_phase();  // also balances the phase before it
   EngTask* add();
-  void end();  // closes the last phase
+  void end();  // closes (and balances) the last phase
+  // Narrows the GEMM tasks of the last phase (larger tiles, fewer K splits)
+  // until its units fit one wave of `budget` CTAs, where possible.
+  void balance(int budget);
 };
 
 // Units for a GEMM task of the engine's tile size and a split-K count.
 // atomic_splits: a kAtomic GEMM may be split along K, every split adding
-// into C (which must be zero before the phase).
+// into C (which must be zero before the phase).  The tile and split choice
+// takes the most units up to max_units (EngBuilder::balance narrows it).
 void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap,
-                   bool atomic_splits = false);
+                   bool atomic_splits = false, int max_units = 128);
+// SMs of the current device (the engine's grid), cached after the first call.
+int eng_sm_count();
 void eng_gemm_final_task(EngTask* t, const EngTask& gemm);
 // false when the chain does not fit the unit's shared-memory staging
 bool eng_chain_task(EngTask* t, const ChainDesc& c);

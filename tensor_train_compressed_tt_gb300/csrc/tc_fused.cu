@@ -106,7 +106,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
 // Optional per-CTA timeline (global-timer stamps), compiled in only with
 // -DTTC_TIMELINE for performance investigation; the default build has none.
 #ifdef TTC_TIMELINE
-__device__ unsigned long long g_tl[3][256][16];
+__device__ unsigned long long g_tl[4][256][16];  // fwd, bwd, engine (1 phase), engine (more)
 __device__ unsigned long long g_tlu[256][8][8];  // engine units: (phase*100+task, start, end, inner stamps)
 #define TL_STAMP(k, slot) (g_tl[(k)][blockIdx.x & 255][(slot)] = gtimer())
 #define TLU_STAMP(nu, slot) \
@@ -336,6 +336,8 @@ struct BwdArgs {
   float* dAc;  // N x RP
   float* dBc;  // M x RP
   float* dDc;  // RP
+  float* zero;  // [0, zero_n) set to 0 (scratch the merge backward adds into)
+  int zero_n;
 };
 
 struct SmemCommon {
@@ -474,7 +476,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int s = it % NSTAGE_F;
           const int yb = yc & 1;
           if (!wait_bar(&S.x_empty[yb], ((yc >> 1) & 1) ^ 1, abort_flag, 5)) { ok = false; break; }
+          if (c < 3) TL_STAMP(0, 13 + c);  // y buffer free
           if (!wait_bar(&S.full[s], (it / NSTAGE_F) & 1, abort_flag, 6)) { ok = false; break; }
+          if (c < 3) TL_STAMP(0, 10 + c);  // Bt chunk in shared memory
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
@@ -519,6 +523,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int c = 0; c < p.nM; ++c, ++yc) {
         const int yb = yc & 1;
         if (!warp_wait(&S.x_full[yb], (yc >> 1) & 1, abort_flag, 9)) { ok = false; break; }
+        if (warp == 2 && lane == 0 && c < 3) TL_STAMP(0, 7 + c);  // y chunk in TMEM
         tc_fence_after();
         uint8_t* box = my_stg + (yc & 1) * STG;
         if (lane == 0) bulk_wait_read<1>();  // the store that used this box is done reading
@@ -571,10 +576,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1k(smem_raw);
   uint8_t* stages = base;
+  // z' (read by the phase-B MMAs) and dz (read by the phase-C MMAs) share
+  // one tile: dz is written once phase B's MMAs are done, the next tile's z'
+  // once phase C's are done
   uint8_t* zp_tile = base + NSTAGE_B * STAGE;
-  uint8_t* dz_tile = zp_tile + BOX;
-  uint8_t* staging = dz_tile + BOX;  // one box per epilogue warp
-  SmemCommon& S = *reinterpret_cast<SmemCommon*>(staging + NEPI * STG);
+  uint8_t* dz_tile = zp_tile;
+  uint8_t* staging = zp_tile + BOX;  // two boxes per epilogue warp
+  SmemCommon& S = *reinterpret_cast<SmemCommon*>(staging + NEPI * 2 * STG);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) TL_STAMP(1, 0);
 
@@ -605,6 +613,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   pdl_wait();  // nothing a previous grid writes is touched before this point
   pdl_trigger();
   if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_n; i += gridDim.x * blockDim.x)
+    p.zero[i] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -751,7 +761,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int row = 32 * q + lane;
     const uint32_t lane_off = (uint32_t)(32 * q) << 16;
     const int rprime = p.rinfo[0];
-    uint8_t* box = staging + (warp - 2) * STG;
+    uint8_t* my_stg = staging + (warp - 2) * 2 * STG;
+    int nst = 0;  // bulk operations this warp issued: they alternate between its two boxes
     int wc = 0, xc = 0, tl = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tl) {
       float z[32], v[32];
@@ -765,7 +776,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(&S.z_empty);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = z[j] * S.Dc[32 * h + j];
-      if (!warp_wait(&S.zp_empty, (tl & 1) ^ 1, abort_flag, 23)) break;
+      // the shared z'/dz tile is free once the previous tile's phase C is done
+      if (!warp_wait(&S.dz_empty, (tl & 1) ^ 1, abort_flag, 23)) break;
       st_tile_half(zp_tile, row, h, v);
       fence_async_smem();
       __syncwarp();
@@ -782,7 +794,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(&S.w_empty[wb]);
         // rows = outputs c*128 + 32q.., columns = compacted ranks 32h..
         if (32 * h < rprime && c * CH + 32 * q < p.M) {
-          if (lane == 0) bulk_wait_read<0>();
+          uint8_t* box = my_stg + (nst & 1) * STG;
+          if (lane == 0) bulk_wait_read<1>();  // the operation that used this box is done reading
           __syncwarp();
           stage_f32_32(box, lane, v);
           fence_async_smem();
@@ -791,6 +804,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tma_reduce_add(&tm_dbc, box, 32 * h, c * CH + 32 * q);
             bulk_commit();
           }
+          ++nst;
         }
       }
       if (!ok) break;
@@ -810,7 +824,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= S.Dc[32 * h + j];
-      if (!warp_wait(&S.dz_empty, (tl & 1) ^ 1, abort_flag, 26)) break;
+      // phase B's MMAs (readers of z' in the shared tile) are done
+      if (!warp_wait(&S.zp_empty, tl & 1, abort_flag, 26)) break;
       st_tile_half(dz_tile, row, h, v);
       fence_async_smem();
       __syncwarp();
@@ -821,7 +836,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int xb = xc & 1;
         if (!warp_wait(&S.x_full[xb], (xc >> 1) & 1, abort_flag, 27)) { ok = false; break; }
         tc_fence_after();
-        if (lane == 0) bulk_wait_read<0>();
+        const int col = c * CH + 64 * h;
+        const bool st_dx = col < p.N && (int64_t)tile * TILE + 32 * q < p.T;
+        uint8_t* box = my_stg + (nst & 1) * STG;
+        if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
 #pragma unroll
         for (int piece = 0; piece < 2; ++piece) {
@@ -833,12 +851,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&S.x_empty[xb]);
-          const int col = c * CH + 64 * h;
-          if (col < p.N && (int64_t)tile * TILE + 32 * q < p.T) {
+          if (st_dx) {
             tma_store(&tm_dx, box, col, tile * TILE + 32 * q);
             bulk_commit();
           }
         }
+        if (st_dx) ++nst;
         const int wb = wc & 1;
         if (!warp_wait(&S.w_full[wb], (wc >> 1) & 1, abort_flag, 28)) { ok = false; break; }
         tc_fence_after();
@@ -848,15 +866,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(&S.w_empty[wb]);
         // rows = features c*128 + 32q.., columns = compacted ranks 32h..
         if (32 * h < rprime && c * CH + 32 * q < p.N) {
-          if (lane == 0) bulk_wait_read<0>();
+          uint8_t* box2 = my_stg + (nst & 1) * STG;
+          if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
-          stage_f32_32(box, lane, v);
+          stage_f32_32(box2, lane, v);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add(&tm_dac, box, 32 * h, c * CH + 32 * q);
+            tma_reduce_add(&tm_dac, box2, 32 * h, c * CH + 32 * q);
             bulk_commit();
           }
+          ++nst;
         }
       }
       if (!ok) break;
@@ -876,7 +896,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // operand packing (compaction of the middle rank) and gradient unpacking,
 // run as units of the merge engine
 // ==========================================================================
-constexpr int kPackPer = 1024;  // elements per engine unit
+constexpr int kPackPer = 4096;  // elements per engine unit
 
 // Compaction of the middle rank, computed by the whole block in parallel:
 // pos[a] = position of a among the nonzero entries of D (or -1), kept[c] = a
@@ -1049,7 +1069,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
 }
 
 constexpr size_t kSmemFwd = NSTAGE_F * STAGE + BOX + NEPI * 2 * STG + sizeof(SmemCommon) + 1024;
-constexpr size_t kSmemBwd = NSTAGE_B * STAGE + 2 * BOX + NEPI * STG + sizeof(SmemCommon) + 1024;
+constexpr size_t kSmemBwd = NSTAGE_B * STAGE + BOX + NEPI * 2 * STG + sizeof(SmemCommon) + 1024;
 static_assert(kSmemFwd <= 227 * 1024, "forward smem");
 static_assert(kSmemBwd <= 227 * 1024, "backward smem");
 
@@ -1174,8 +1194,13 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
 }
 
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
-                      void* ws, size_t off, cudaStream_t st) {
-  if (T <= 0) return TT_OK;
+                      void* ws, size_t off, float* zero, size_t zero_n, cudaStream_t st) {
+  if (zero_n > 0x7FFFFFFF) return TT_ERR_UNSUPPORTED;
+  if (T <= 0) {
+    if (zero_n && cudaMemsetAsync(zero, 0, zero_n * sizeof(float), st) != cudaSuccess)
+      return TT_ERR_CUDA;
+    return TT_OK;
+  }
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
@@ -1201,6 +1226,8 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.dAc = at<float>(ws, off + t.dAc);
   a.dBc = at<float>(ws, off + t.dBc);
   a.dDc = at<float>(ws, off + t.dDc);
+  a.zero = zero;
+  a.zero_n = (int)zero_n;
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e = launch_ex(tt_bwd_kernel, grid, NTHREADS, kSmemBwd, st, false, mx, mdy, mat, mbm,
                             manr, mdx, mdac, mdbc, a);

@@ -32,7 +32,9 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
 
 // dx for T tokens and the token sums dAc, dBc, dDc (zeroed by the pack
 // phase); the merge engine's unpack phase turns these into dA, dB, dD_d.
+// zero[0, zero_n) is set to 0 on the way (scratch that the merge backward
+// then adds into), also when T == 0.
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
-                      void* ws, size_t ws_off, cudaStream_t st);
+                      void* ws, size_t ws_off, float* zero, size_t zero_n, cudaStream_t st);
 
 }  // namespace ttc

@@ -178,12 +178,7 @@ void eng_zero_task(EngBuilder& b, float* out, int64_t n) {
   z->acc = 0;
 }
 
-// dQ of reverse step j on side s (0 input, 1 output).  The steps j >= 1 and,
-// for chains of three or more cores a side, step 0 add their K splits
-// atomically: step 0's pair of buffers is zeroed by every merge that
-// precedes a backward (forward merge with zero_grads) and again by the
-// backward merge once read; the later steps are zeroed by the backward merge
-// in its first phase.
+// dQ scratch of reverse step j on side s (0 input, 1 output).
 float* dq_buf(void* ws, const WsLayout& w, int j, int side) {
   return fptr(ws, w.q) + (size_t)(2 * j + side) * w.qstride;
 }
@@ -208,7 +203,6 @@ tt_status run_merge_forward_gemm(const LayerPlan& L, const float* params, void* 
   for (int j = 1; j < L.d; ++j) {
     b.begin_phase();
     if (pack && j == 1) eng_pack_task(b.add(), L, nullptr, nullptr, Dmid, tc, zero_grads, true);
-    if (zero_grads && j == 1 && L.d >= 3) eng_zero_task(b, dq_buf(ws, w, 0, 0), 2 * w.qstride);
     for (int k : {j, L.d + j}) {
       GemmArgs g;
       g.m = L.U[k - 1];
@@ -250,7 +244,6 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
     // one phase: each side's rows recomputed per prefix (no grid barrier);
     // padding, metadata and the zeroed token sums come from the pack task
     if (pack) eng_pack_task(b.add(), L, nullptr, nullptr, Dmid, tc, zero_grads, true);
-    if (zero_grads && L.d >= 3) eng_zero_task(b, dq_buf(ws, w, 0, 0), 2 * w.qstride);
     for (int side = 0; side < 2; ++side) {
       const int k0 = side == 0 ? 0 : L.d;
       ChainDesc c;
@@ -294,7 +287,17 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
 //   dG_k = diag(D_{k-1}) P_{k-1}^T Y,  dQ = Y G_k^T,  dD_{k-1} = colsum(P_{k-1} * dQ)
 // with Y = dlast for the first step and Y = dQ_prev * D_k afterwards; the
 // first core gets dG = Y * D_{k_first}.  Both sides advance in lockstep, one
-// phase per step; split-K partials of dG_k are reduced in the next phase.
+// phase per step; split-K partials of the first step's dG are reduced in the
+// next phase.  With two or more steps a side, the last step's dQ GEMM writes
+// the first core's dG and dD straight from its epilogue (no phase of its
+// own), the later steps' dG add their K splits atomically, and every dQ is
+// added atomically into zeroed scratch: step 0's by the backward token pass
+// (dq0_zero_floats), the others' by phase 0, which also zeroes the gradient
+// slices that later phases add into (unless accumulating).
+size_t dq0_zero_floats(const LayerPlan& L, const WsLayout& w) {
+  return L.d >= 3 ? 2 * w.qstride : 0;
+}
+
 tt_status run_merge_backward(const LayerPlan& L, const float* params, const float** P,
                              const float* dA, const float* dB, float* dparams, bool acc,
                              bool unpack, bool rezero, void* ws, const WsLayout& w,
@@ -308,33 +311,47 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
     eng_unpack_task(b.add(), L, tc, params + L.diag_off[L.d - 1], fptr(ws, w.dA),
                     fptr(ws, w.dB), dparams + L.diag_off[L.d - 1], acc);
   }
+  const bool fold = steps >= 2;
+  const int nphases = fold ? steps : steps + 1;
   struct Side {
     int k_first, k_last;
     const float* Y;
     const float* yscale;
     int qs, pi;          // side index of the dQ buffers, base index of part buffers
     int flip;
-    EngTask pending;     // split GEMM whose partials the next phase reduces
-    bool has_pending;
+    int pending;         // task index of a split GEMM whose partials the next phase reduces
     const float* dQ;     // last dQ (for coldot in the next phase)
     int coldot_k;        // link whose dD the next phase computes (-1: none)
-  } sides[2] = {{0, L.d - 1, dA, nullptr, 0, 0, 0, EngTask(), false, nullptr, -1},
-                {L.d, L.K - 1, dB, nullptr, 1, 2, 0, EngTask(), false, nullptr, -1}};
+  } sides[2] = {{0, L.d - 1, dA, nullptr, 0, 0, 0, -1, nullptr, -1},
+                {L.d, L.K - 1, dB, nullptr, 1, 2, 0, -1, nullptr, -1}};
   const int mode = acc ? kAccumulate : kStore;
-  for (int j = 0; j <= steps; ++j) {
+  for (int j = 0; j < nphases; ++j) {
     b.begin_phase();
     if (unpack && steps > 0 && j == 0)
       eng_dd_task(b.add(), L, tc, params + L.diag_off[L.d - 1], dparams + L.diag_off[L.d - 1],
                   acc);
-    // dQ buffers of the steps after the first: zero before they are added to
-    if (j == 0 && steps >= 2) eng_zero_task(b, dq_buf(ws, w, 1, 0), 2 * (steps - 1) * w.qstride);
-    // step 0's pair, last read in phase 1: zero again for the next backward
-    if (j == 2) eng_zero_task(b, dq_buf(ws, w, 0, 0), 2 * w.qstride);
+    if (fold && j == 0) {
+      // dQ scratch of steps 1 .. steps-2 (step 0's was zeroed by the token pass)
+      if (steps >= 3) eng_zero_task(b, dq_buf(ws, w, 1, 0), 2 * (steps - 2) * w.qstride);
+      if (!acc) {
+        // gradients that later phases add into
+        for (const Side& sd : sides) {
+          for (int jj = 1; jj < steps; ++jj) {
+            const int k = sd.k_last - jj;
+            eng_zero_task(b, dparams + L.core_off[k], (int64_t)L.r[k] * L.s[k] * L.r[k + 1]);
+          }
+          const int kf = sd.k_first;
+          eng_zero_task(b, dparams + L.core_off[kf], (int64_t)L.r[kf] * L.s[kf] * L.r[kf + 1]);
+          eng_zero_task(b, dparams + L.diag_off[kf], L.r[kf + 1]);
+        }
+      }
+    }
     for (Side& sd : sides) {
       // work left over from the previous step
-      if (sd.has_pending) {
-        eng_gemm_final_task(b.add(), sd.pending);
-        sd.has_pending = false;
+      if (sd.pending >= 0) {  // the previous phase is balanced by now
+        const EngTask prev = b.p.t[sd.pending];
+        if (prev.splits > 1 && prev.partial) eng_gemm_final_task(b.add(), prev);
+        sd.pending = -1;
       }
       if (sd.coldot_k >= 0) {
         const int k = sd.coldot_k;  // dD_{k-1} from P_{k-1} and dQ_k
@@ -354,6 +371,8 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
         const int rk = L.r[k], rk1 = L.r[k + 1];
         const int64_t U = L.U[k - 1];
         const int64_t ncol = (int64_t)L.s[k] * rk1;
+        const bool last = j == steps - 1;
+        const int gat = (unpack && j == 0) ? (&sd == &sides[0] ? 1 : 2) : 0;
         GemmArgs g;  // dG_k
         g.m = rk; g.n = ncol; g.k = U;
         g.A = P[k - 1]; g.sam = 1; g.sak = rk;
@@ -361,10 +380,14 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
         g.rscale = params + L.diag_off[k - 1];
         g.cscale = sd.yscale; g.clen = rk1;
         g.C = dparams + L.core_off[k]; g.scm = ncol; g.scn = 1;
-        g.mode = mode;
         EngTask* t = b.add();
-        eng_gemm_task(t, g, fptr(ws, w.part[sd.pi + (sd.flip & 1)]), w.part_cap);
-        const int gat = (unpack && j == 0) ? (&sd == &sides[0] ? 1 : 2) : 0;
+        if (fold && j >= 1) {  // added into zeroed (or accumulated) dparams
+          g.mode = kAtomic;
+          eng_gemm_task(t, g, nullptr, 0, true);
+        } else {
+          g.mode = mode;
+          eng_gemm_task(t, g, fptr(ws, w.part[sd.pi + (sd.flip & 1)]), w.part_cap);
+        }
         if (gat) {  // read dA / dB straight from the compacted token sums
           t->gather = gat;
           t->gather_op = 1;
@@ -373,21 +396,30 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
           t->rd = L.rd;
           t->M = (int)L.M;
         }
-        if (t->splits > 1) {
-          sd.pending = *t;
-          sd.has_pending = true;
-        }
-        float* dQ = dq_buf(ws, w, j, sd.qs);
-        const bool atomic_q = j >= 1 || steps >= 2;
+        if (!b.overflow && t->partial) sd.pending = (int)(t - b.p.t);
         GemmArgs h;  // dQ = Y G_k^T
         h.m = U; h.n = rk; h.k = ncol;
         h.A = sd.Y; h.sam = ncol; h.sak = 1;
         h.kscale = sd.yscale; h.klen = rk1;
         h.B = params + L.core_off[k]; h.sbk = 1; h.sbn = ncol;
-        h.C = dQ; h.scm = rk; h.scn = 1;
-        h.mode = atomic_q ? kAtomic : kStore;
+        h.scm = rk; h.scn = 1;
         EngTask* th = b.add();
-        eng_gemm_task(th, h, nullptr, 0, atomic_q);
+        float* dQ = nullptr;
+        if (fold && last) {
+          // the first core: dG = dQ * D_{k_first}, dD_{k_first} = colsum(P_{k_first} * dQ)
+          const int kf = sd.k_first;
+          h.mode = kAtomic;
+          h.cscale = params + L.diag_off[kf]; h.clen = rk;
+          eng_gemm_task(th, h, nullptr, 0, true);
+          th->fold_g = dparams + L.core_off[kf];
+          th->fold_p = P[kf];
+          th->fold_dd = dparams + L.diag_off[kf];
+        } else {
+          dQ = dq_buf(ws, w, j, sd.qs);
+          h.C = dQ;
+          h.mode = fold ? kAtomic : kStore;
+          eng_gemm_task(th, h, nullptr, 0, fold);
+        }
         if (gat) {
           th->gather = gat;
           th->gather_op = 0;
@@ -397,18 +429,12 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
           th->M = (int)L.M;
         }
         sd.dQ = dQ;
-        sd.coldot_k = k;
+        sd.coldot_k = (fold && last) ? -1 : k;
         sd.Y = dQ;
         sd.yscale = params + L.diag_off[k - 1];
         sd.flip ^= 1;
       } else {
-        if (rezero && &sd == &sides[0]) {
-          // leave the token sums zeroed for the next backward that reuses
-          // this workspace's merge (they were last read before a barrier);
-          // dAc, dBc and dDc are adjacent
-          eng_zero_task(b, const_cast<float*>(tc.dAc), (L.N + L.M + 1) * 64);
-        }
-        // first core of the side
+        // (only without folding) first core of the side
         EngTask* t = b.add();
         t->kind = kEScale;
         t->n = (int64_t)L.r[sd.k_first] * L.s[sd.k_first] * L.r[sd.k_first + 1];
@@ -420,9 +446,16 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
         t->acc = acc ? 1 : 0;
       }
     }
+    if (rezero && j == nphases - 1 && (j >= 1 || steps == 0)) {
+      // leave the token sums zeroed for the next backward that reuses this
+      // workspace's merge (read only by an earlier phase: the first reverse
+      // step, or the unpack phase for order 2); dAc, dBc and dDc are adjacent
+      eng_zero_task(b, const_cast<float*>(tc.dAc), (L.N + L.M + 1) * 64);
+    }
   }
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
+  if (b.p.nphases == 0) return TT_OK;
   TT_CUDA(eng_launch(b.p, st));
   return TT_OK;
 }
@@ -542,10 +575,13 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
     if (s != TT_OK) return s;
   }
   prof_begin(kPhBwd, st);
-  if (tc)
-    s = tc_backward(L, T, x, dy, dx, ws, w.tc, st);
-  else
+  const size_t nz = dq0_zero_floats(L, w);
+  if (tc) {
+    s = tc_backward(L, T, x, dy, dx, ws, w.tc, dq_buf(ws, w, 0, 0), nz, st);
+  } else {
+    if (nz) TT_CUDA(cudaMemsetAsync(dq_buf(ws, w, 0, 0), 0, nz * sizeof(float), st));
     s = simt_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
+  }
   prof_end(kPhBwd, st);
   if (s != TT_OK) return s;
   prof_begin(kPhMergeBwd, st);
