@@ -477,6 +477,32 @@ def run_ours(args, w):
                             "us_per_interval": 1e3 * tot.value / n.value}
     ttc.lib().tt_profile_enable(0)
 
+    # ---- the rank-adaptive step (proximal update of one layer's packed
+    # parameters), timed on copies so the step's own buffers stay unchanged
+    rank_step = None
+    if not w.ffn:
+        pc = params[0].clone()
+        gc = dparams[0].clone()
+        n_up = 200
+        for _ in range(3):
+            ttc.check(ttc.tt_rank_update(mod.plan, pc.data_ptr(), gc.data_ptr(), 1e-3, 1e-3,
+                                         1e-3, sh), "tt_rank_update")
+        barrier()
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(stream)
+        for _ in range(n_up):
+            ttc.check(ttc.tt_rank_update(mod.plan, pc.data_ptr(), gc.data_ptr(), 1e-3, 1e-3,
+                                         1e-3, sh), "tt_rank_update")
+        r1.record(stream)
+        barrier()
+        us = 1e3 * r0.elapsed_time(r1) / n_up
+        nb = 12 * pc.numel()  # read params and dparams, write params (float32)
+        rank_step = {"us_per_call": us, "bytes_per_call": nb,
+                     "achieved_gbs": nb / (us * 1e-6) / 1e9, "bound": "latency",
+                     "note": "tt_rank_update, proximal step on one layer's packed "
+                             f"parameters ({pc.numel()} floats), back-to-back eager launches"}
+
     alg = algorithmic(w, T)
     peak, peak_kind = measured_peaks()
     bytes_of = {"forward_tokens": alg["fwd_bytes"], "backward_tokens": alg["bwd_bytes"]}
@@ -563,6 +589,7 @@ def run_ours(args, w):
                               "algorithmic_bytes": alg["bytes"], "algorithmic_flop": alg["flop"],
                               "peak_gbs": peak, "peak_kind": peak_kind},
             "phases_us": {k: round(v["us_per_interval"], 3) for k, v in phases.items()},
+            "rank_update": rank_step,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,

@@ -154,6 +154,34 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
                           float* dparams_up, float* dparams_down, void* ws, size_t ws_bytes,
                           void* stream);
 
+/* Rank-adaptive step [CoMERA project page, "Learn the ranks while
+ * training": the early-stage objective L(G, D) + gamma S_hat(D) + beta ||G||^2,
+ * with S_hat an l1 penalty on the diagonals (read here as sum_k |D_k|_1 over
+ * every internal link) and ||G||^2 = sum_k ||G_k||_F^2].  Works in place on
+ * one layer's packed params / dparams (the tt_param_layout layout, fp32,
+ * device pointers), enqueued on `stream`:
+ *   lr == 0: dparams += the penalty's sub-gradient:
+ *            dG_k += (2 beta) G_k,  dD_k += gamma sign(D_k), sign(0) = 0;
+ *            params untouched.
+ *   lr > 0:  one proximal gradient step on the whole objective:
+ *            G_k <- G_k - lr (dG_k + (2 beta) G_k),
+ *            D_k <- soft_threshold(D_k - lr dD_k, lr gamma),
+ *            soft_threshold(v, t) = sign(v) max(|v| - t, 0) (entries with
+ *            |v| <= t become exactly +0: pruned, and compacted out by the
+ *            next forward / backward); dparams untouched.
+ * Every step is one float32 operation, rounded to nearest, in the order
+ * written (no fused multiply-add).  TT_ERR_INVALID_ARG for a null pointer,
+ * an FFN plan (update each layer with its own single-layer plan), or a
+ * negative or non-finite gamma, beta or lr.  The CoMERA pages give no
+ * optimiser; this is the plainest step on the objective they state. */
+typedef struct tt_rank_opts {
+  float gamma; /* weight of the l1 penalty on the diagonals, >= 0 */
+  float beta;  /* weight of the squared l2 penalty on the cores, >= 0 */
+  float lr;    /* step size, >= 0; 0 selects the gradient-only form */
+} tt_rank_opts;
+tt_status tt_rank_update(const tt_plan_t* plan, float* params, float* dparams,
+                         const tt_rank_opts* opts, void* stream);
+
 /* Synchronise stream, then read and clear the status word of the current
  * device.  The word is sticky: it holds the first error any libttc kernel
  * on this device recorded since the last read.  Returns TT_OK,

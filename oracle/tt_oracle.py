@@ -346,3 +346,71 @@ def rel_err(out, ref) -> float:
     if den == 0.0:
         return 0.0 if num == 0.0 else float("inf")
     return num / den
+
+
+# ---------------------------------------------------------------------------
+# Rank-adaptive step (project page, "Learn the ranks while training": the
+# early-stage objective  L(G, D) + gamma * S_hat(D) + beta * ||G||^2, where
+# S_hat is an l1 penalty on the diagonals standing in for counting their
+# nonzeros, and beta ||G||^2 keeps the cores from growing).
+#
+# Reading (the pages print no formula for S_hat beyond "an l1 penalty on the
+# diagonals"): S_hat(D) = sum_k ||D_k||_1 over every internal link, and
+# ||G||^2 = sum_k ||G_k||_F^2 over every core.
+
+
+def penalty(cores, diags, gamma: float, beta: float) -> float:
+    """gamma * sum_k |D_k|_1 + beta * sum_k ||G_k||_F^2, in float64."""
+    s = sum(float(np.abs(np.asarray(e, F64)).sum()) for e in diags)
+    g = sum(float((np.asarray(c, F64) ** 2).sum()) for c in cores)
+    return gamma * s + beta * g
+
+
+def penalty_grads(cores, diags, gamma: float, beta: float):
+    """Sub-gradient of `penalty`: 2 beta G_k for the cores and gamma sign(D_k)
+    for the diagonals, with sign(0) = 0 (a pruned entry gets no push)."""
+    dC = [2.0 * beta * np.asarray(c, F64) for c in cores]
+    dE = [gamma * np.sign(np.asarray(e, F64)) for e in diags]
+    return dC, dE
+
+
+def soft_threshold(v, t):
+    """Proximal map of t |u|: argmin_u 0.5 (u - v)^2 + t |u|."""
+    v = np.asarray(v, F64)
+    return np.sign(v) * np.maximum(np.abs(v) - t, 0.0)
+
+
+def rank_update_f32(cores, diags, dcores, ddiags, gamma: float, beta: float, lr: float):
+    """The rank-adaptive step in float32 arithmetic, one rounding per
+    operation in the order below (the library applies the same operations
+    without contraction, so the two agree bit for bit; the zero / nonzero
+    decision of the threshold is a float32 comparison on both sides).
+
+    lr == 0: only the penalty's sub-gradient is added to the gradients,
+        dG <- dG + (2 beta) G,   dD <- dD + gamma sign(D).
+    lr > 0: one proximal gradient step on the whole objective,
+        G <- G - lr (dG + (2 beta) G),
+        D <- soft_threshold(D - lr dD, lr gamma),
+    so diagonal entries that reach zero are pruned (the next call compacts
+    them out).  Returns (cores, diags, dcores, ddiags) as float32 arrays."""
+    f = np.float32
+    b2 = f(2.0) * f(beta)
+    g, lr_, t = f(gamma), f(lr), f(lr) * f(gamma)
+    oc, od, odc, odd = [], [], [], []
+    for c, dc in zip(cores, dcores):
+        c = np.asarray(c, f); dc = np.asarray(dc, f)
+        grad = (dc + (b2 * c).astype(f)).astype(f)
+        if lr == 0:
+            oc.append(c.copy()); odc.append(grad)
+        else:
+            oc.append((c - (lr_ * grad).astype(f)).astype(f)); odc.append(dc.copy())
+    for e, de in zip(diags, ddiags):
+        e = np.asarray(e, f); de = np.asarray(de, f)
+        if lr == 0:
+            sgn = np.where(e > 0, g, np.where(e < 0, -g, f(0.0))).astype(f)
+            od.append(e.copy()); odd.append((de + sgn).astype(f))
+        else:
+            v = (e - (lr_ * de).astype(f)).astype(f)
+            out = np.where(v > t, (v - t).astype(f), np.where(v < -t, (v + t).astype(f), f(0.0)))
+            od.append(out.astype(f)); odd.append(de.copy())
+    return oc, od, odc, odd

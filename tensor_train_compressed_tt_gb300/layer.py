@@ -79,6 +79,14 @@ class TTLinear:
         return dx, dparams
 
 
+    def rank_update(self, params: torch.Tensor, dparams: torch.Tensor, gamma: float,
+                    beta: float, lr: float = 0.0, stream=None) -> None:
+        """In place: dparams += penalty sub-gradient (lr == 0), or one
+        proximal gradient step on params (lr > 0)."""
+        ttc.check(ttc.tt_rank_update(self.plan, _ptr(params), _ptr(dparams), gamma, beta, lr,
+                                     _stream(stream)), "tt_rank_update")
+
+
 class TTFFN:
     """y = TT_down(GELU(TT_up(x))), exact erf GELU, both layers through one plan."""
 

@@ -51,6 +51,14 @@ class tt_desc(ctypes.Structure):
     ]
 
 
+class tt_rank_opts(ctypes.Structure):
+    _fields_ = [
+        ("gamma", ctypes.c_float),
+        ("beta", ctypes.c_float),
+        ("lr", ctypes.c_float),
+    ]
+
+
 _lib = None
 _P = ctypes.c_void_p
 _SZ = ctypes.c_size_t
@@ -79,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "tt_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_forward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+            "tt_rank_update": [_P, _P, _P, _P, _P],
             "tt_get_device_status": [_P],
             "tt_status_string": [ctypes.c_int],
         }
@@ -210,6 +219,14 @@ def tt_ffn_backward(plan: Plan, T: int, x: int, dy: int, params_up: int, params_
     return lib().tt_ffn_backward(ctypes.c_void_p(plan.handle), int(T), x, dy, params_up,
                                  params_down, dx, dparams_up, dparams_down, ws,
                                  int(ws_bytes), stream)
+
+
+def tt_rank_update(plan: Plan, params: int, dparams: int, gamma: float, beta: float,
+                   lr: float, stream: int = 0) -> int:
+    """Penalty sub-gradient (lr == 0) or proximal step (lr > 0), in place."""
+    o = tt_rank_opts(float(gamma), float(beta), float(lr))
+    return lib().tt_rank_update(ctypes.c_void_p(plan.handle), params, dparams,
+                                ctypes.byref(o), stream)
 
 
 def tt_get_device_status(stream: int = 0) -> int:

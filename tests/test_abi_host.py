@@ -124,6 +124,17 @@ def test_argument_errors_return_before_any_launch(lib):
     assert ttc.tt_backward(plan, 64, fake, fake + 8, fake, fake, fake, fake, ws_need) == 1
     # a single-layer plan is not an FFN plan
     assert ttc.tt_ffn_forward(plan, 64, fake, fake, fake, fake, fake, ws_need) == 1
+    # rank step: null buffers, negative or non-finite weights, FFN plans
+    assert ttc.tt_rank_update(plan, 0, fake, 0.1, 0.1, 0.1) == 1
+    assert ttc.tt_rank_update(plan, fake, 0, 0.1, 0.1, 0.1) == 1
+    assert ttc.tt_rank_update(plan, fake, fake, -0.1, 0.1, 0.1) == 1
+    assert ttc.tt_rank_update(plan, fake, fake, 0.1, -0.1, 0.1) == 1
+    assert ttc.tt_rank_update(plan, fake, fake, 0.1, 0.1, -0.1) == 1
+    assert ttc.tt_rank_update(plan, fake, fake, float("nan"), 0.1, 0.1) == 1
+    assert ttc.tt_rank_update(plan, fake, fake, 0.1, float("inf"), 0.1) == 1
+    w = synth.WORKLOADS["ffn768_3072_bf16"]
+    ffn = ttc.tt_ffn_plan(_desc(w.layers[0]), _desc(w.layers[1]))
+    assert ttc.tt_rank_update(ffn, fake, fake, 0.1, 0.1, 0.1) == 1
 
 
 def test_status_strings(lib):

@@ -360,3 +360,93 @@ def test_bf16_rounding_is_round_to_nearest_even():
     ours = synth.round_bf16(v)
     ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float32).numpy()
     assert np.array_equal(ours, ref)
+
+
+# --- rank-adaptive step (early-stage objective) --------------------------------
+
+
+def test_penalty_gradient_matches_finite_differences():
+    """2 beta G and gamma sign(D) against central differences of the penalty
+    value (diagonal entries kept away from the kink at 0)."""
+    rng = np.random.Generator(np.random.PCG64(11))
+    shape = synth.LayerShape((2, 3), (3, 2), (1, 2, 3, 2, 1))
+    cores, diags = _random_tt(rng, shape)
+    gamma, beta, h = 0.3, 0.7, 1e-6
+    dC, dE = O.penalty_grads(cores, diags, gamma, beta)
+    for k, c in enumerate(cores):
+        for idx in [(0, 0, 0), tuple(s - 1 for s in c.shape)]:
+            cp = [x.copy() for x in cores]; cm = [x.copy() for x in cores]
+            cp[k][idx] += h; cm[k][idx] -= h
+            fd = (O.penalty(cp, diags, gamma, beta) - O.penalty(cm, diags, gamma, beta)) / (2 * h)
+            assert abs(fd - dC[k][idx]) <= 1e-6 * max(1.0, abs(fd))
+    for k, e in enumerate(diags):
+        for a in range(e.shape[0]):
+            ep = [x.copy() for x in diags]; em = [x.copy() for x in diags]
+            ep[k][a] += h; em[k][a] -= h
+            fd = (O.penalty(cores, ep, gamma, beta) - O.penalty(cores, em, gamma, beta)) / (2 * h)
+            assert abs(fd - dE[k][a]) <= 1e-6
+
+
+def test_soft_threshold_is_the_proximal_map():
+    """soft_threshold(v, t) minimises 0.5 (u - v)^2 + t |u| (brute force)."""
+    u = np.linspace(-4.0, 4.0, 160001)
+    for v in [-2.5, -0.6, -0.2, 0.0, 0.15, 0.9, 3.1]:
+        for t in [0.0, 0.25, 1.0]:
+            best = u[np.argmin(0.5 * (u - v) ** 2 + t * np.abs(u))]
+            assert abs(O.soft_threshold(v, t) - best) <= 1e-4
+
+
+def test_rank_update_f32_against_float64():
+    """The float32 step equals the float64 formulas within float32 rounding,
+    and the entries it prunes are exactly those with |D - lr dD| < lr gamma."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    shape = synth.LayerShape((3, 2), (2, 3), (1, 3, 2, 3, 1))
+    cores, diags = _random_tt(rng, shape)
+    cores = [c.astype(np.float32).astype(np.float64) for c in cores]
+    diags = [e.astype(np.float32).astype(np.float64) for e in diags]
+    dC = [rng.standard_normal(c.shape).astype(np.float32).astype(np.float64) for c in cores]
+    dE = [rng.standard_normal(e.shape).astype(np.float32).astype(np.float64) for e in diags]
+    gamma, beta = 0.5, 0.25
+    # gradient-only form
+    _, _, gc, ge = O.rank_update_f32(cores, diags, dC, dE, gamma, beta, 0.0)
+    pc, pe = O.penalty_grads(cores, diags, gamma, beta)
+    for a, b, c in zip(gc, dC, pc):
+        np.testing.assert_allclose(a, b + c, rtol=2e-6, atol=1e-6)
+    for a, b, c in zip(ge, dE, pe):
+        np.testing.assert_allclose(a, b + c, rtol=2e-6, atol=1e-6)
+    # proximal step (threshold lr * gamma = 0.8 prunes some entries)
+    lr, gamma = 1.0, 0.8
+    nc, ne, _, _ = O.rank_update_f32(cores, diags, dC, dE, gamma, beta, lr)
+    for a, c, g in zip(nc, cores, dC):
+        np.testing.assert_allclose(a, c - lr * (g + 2 * beta * c), rtol=2e-6, atol=2e-6)
+    pruned = 0
+    for a, e, g in zip(ne, diags, dE):
+        v = e - lr * g
+        ref = O.soft_threshold(v, lr * gamma)
+        far = np.abs(np.abs(v) - lr * gamma) > 1e-5
+        np.testing.assert_allclose(a[far], ref[far], rtol=2e-6, atol=2e-6)
+        assert np.all((a == 0)[far] == (np.abs(v) < lr * gamma)[far])
+        pruned += int(np.sum(a == 0))
+    assert pruned > 0  # the case exercises pruning
+
+
+def test_rank_update_prunes_to_the_truncated_tt():
+    """Entries the proximal step sets to zero drop their slices: the updated
+    layer equals its rank-truncated TT."""
+    rng = np.random.Generator(np.random.PCG64(13))
+    shape = synth.LayerShape((2, 3), (3, 2), (1, 2, 3, 2, 1))
+    cores, diags = _random_tt(rng, shape)
+    dC = [np.zeros_like(c) for c in cores]
+    dE = [np.zeros_like(e) for e in diags]
+    # a threshold between the smallest and largest |D| entries
+    allabs = np.sort(np.concatenate([np.abs(e) for e in diags]))
+    lr, gamma = 1.0, float(allabs[len(allabs) // 2])
+    nc, ne, _, _ = O.rank_update_f32(cores, diags, dC, dE, gamma, 0.0, lr)
+    nc = [c.astype(np.float64) for c in nc]
+    ne = [e.astype(np.float64) for e in ne]
+    assert any(np.any(e == 0) for e in ne)
+    tc, td, _ = O.truncate(nc, ne)
+    x = rng.standard_normal((3, shape.N))
+    d = len(shape.in_modes)
+    np.testing.assert_allclose(O.dense_forward(nc, ne, d, x), O.dense_forward(tc, td, d, x),
+                               rtol=1e-12, atol=1e-12)
