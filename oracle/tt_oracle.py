@@ -45,6 +45,7 @@ its exact erf form.
 
 from __future__ import annotations
 
+import itertools
 from typing import List, Sequence, Tuple
 
 import numpy as np
@@ -414,3 +415,131 @@ def rank_update_f32(cores, diags, dcores, ddiags, gamma: float, beta: float, lr:
             out = np.where(v > t, (v - t).astype(f), np.where(v < -t, (v + t).astype(f), f(0.0)))
             od.append(out.astype(f)); odd.append(de.copy())
     return oc, od, odc, odd
+
+
+# ---------------------------------------------------------------------------
+# TT-matrix (TTM) embedding table (project page: "Embedding tables, whose
+# shapes are very unbalanced, use the related tensor-train-matrix format";
+# poster digest, TT/TTM figure: each core F_k carries an index pair
+# (m_k, n_k)).  E (V x Dm), V = prod m_k, Dm = prod n_k, row index
+# i = (i_1..i_d) and column index j = (j_1..j_d) row-major:
+#
+#     E[i, j] = F_1[0, i_1, j_1, :] D_1 F_2[:, i_2, j_2, :] D_2 ... F_d[:, i_d, j_d, 0]
+#
+# A lookup returns the rows E[idx[b], :]; its backward, for the functional
+# L = <dout, rows>, gives every dF_k and dD_k (duplicated indices add up).
+
+
+def _row_digits(rows, row_modes):
+    rows = np.asarray(rows, np.int64)
+    dig = []
+    rem = rows.copy()
+    for m in reversed(row_modes):
+        dig.append(rem % m)
+        rem //= m
+    return list(reversed(dig))
+
+
+def ttm_table_bruteforce(cores, diags) -> np.ndarray:
+    """The whole table by the explicit sum over every rank index (tiny shapes)."""
+    d = len(cores)
+    m = [c.shape[1] for c in cores]
+    n = [c.shape[2] for c in cores]
+    V, Dm = int(np.prod(m)), int(np.prod(n))
+    E = np.zeros((V, Dm), F64)
+    ranges = [range(c.shape[3]) for c in cores[:-1]]
+    for i in range(V):
+        ii = np.unravel_index(i, m)
+        for j in range(Dm):
+            jj = np.unravel_index(j, n)
+            s = 0.0
+            for a in itertools.product(*ranges):
+                p = 1.0
+                prev = 0
+                for k in range(d):
+                    nxt = a[k] if k < d - 1 else 0
+                    p *= float(cores[k][prev, ii[k], jj[k], nxt])
+                    if k < d - 1:
+                        p *= float(diags[k][a[k]])
+                    prev = nxt
+                s += p
+            E[i, j] = s
+    return E
+
+
+def _ttm_prefix(cores, diags, dig, k_end):
+    """P (U, n_1..n_k flattened, r_k): the chain through cores 0..k_end-1,
+    with the diagonals between them but not the one after core k_end-1."""
+    U = dig[0].shape[0]
+    P = np.ones((U, 1, 1), F64)
+    for k in range(k_end):
+        if k > 0:
+            P = P * np.asarray(diags[k - 1], F64)[None, None, :]
+        Fk = np.asarray(cores[k], F64)[:, dig[k], :, :].transpose(1, 0, 2, 3)  # (U, r, n, r')
+        P = np.einsum("ulb,ubjc->uljc", P, Fk).reshape(U, -1, Fk.shape[3])
+    return P
+
+
+def _ttm_suffix(cores, diags, dig, k_begin):
+    """S (U, r_{k_begin}, n_{k_begin+1}..n_d flattened): the chain through
+    cores k_begin..d-1 (0-based), with the diagonals between them but not the
+    one before core k_begin."""
+    d = len(cores)
+    U = dig[0].shape[0]
+    S = np.ones((U, 1, 1), F64)
+    for k in range(d - 1, k_begin - 1, -1):
+        if k < d - 1:
+            S = np.asarray(diags[k], F64)[None, :, None] * S
+        Fk = np.asarray(cores[k], F64)[:, dig[k], :, :].transpose(1, 0, 2, 3)  # (U, r, n, r')
+        S = np.einsum("ubjc,ucr->ubjr", Fk, S).reshape(U, Fk.shape[1], -1)
+    return S
+
+
+def ttm_rows(cores, diags, rows) -> np.ndarray:
+    """Rows E[rows, :] by the chained contraction (float64)."""
+    m = [c.shape[1] for c in cores]
+    dig = _row_digits(rows, m)
+    P = _ttm_prefix(cores, diags, dig, len(cores))
+    return P[:, :, 0].copy()
+
+
+def ttm_lookup(cores, diags, idx) -> np.ndarray:
+    """out[b] = E[idx[b]]: each distinct row is computed once."""
+    uniq, inv = np.unique(np.asarray(idx, np.int64), return_inverse=True)
+    return ttm_rows(cores, diags, uniq)[inv]
+
+
+def ttm_lookup_backward(cores, diags, idx, dout, prune_convention=True):
+    """dF_k and dD_k of L = <dout, ttm_lookup(idx)>: gradients of repeated
+    indices are summed first (one gradient row per distinct index)."""
+    d = len(cores)
+    m = [c.shape[1] for c in cores]
+    uniq, inv = np.unique(np.asarray(idx, np.int64), return_inverse=True)
+    dR = np.zeros((uniq.size, np.asarray(dout).shape[1]), F64)
+    np.add.at(dR, inv, np.asarray(dout, F64))
+    dig = _row_digits(uniq, m)
+    U = uniq.size
+    dC = [np.zeros_like(np.asarray(c, F64)) for c in cores]
+    dE = [np.zeros(np.asarray(e).shape, F64) for e in diags]
+    for k in range(d):
+        Pl = _ttm_prefix(cores, diags, dig, k)          # (U, left, r_{k-1}) without D_{k-1}
+        if k > 0:
+            Pl = Pl * np.asarray(diags[k - 1], F64)[None, None, :]
+        Sr = _ttm_suffix(cores, diags, dig, k + 1)      # (U, r_k, right) without D_k
+        if k < d - 1:
+            Sr = np.asarray(diags[k], F64)[None, :, None] * Sr
+        nk = cores[k].shape[2]
+        G = dR.reshape(U, Pl.shape[1], nk, Sr.shape[2])
+        contrib = np.einsum("ulb,uljr,ucr->ubjc", Pl, G, Sr)   # (U, r_{k-1}, n_k, r_k)
+        acc = np.zeros((cores[k].shape[1],) + contrib.shape[1:], F64)
+        np.add.at(acc, dig[k], contrib)
+        dC[k] = acc.transpose(1, 0, 2, 3).copy()
+    for k in range(d - 1):
+        P = _ttm_prefix(cores, diags, dig, k + 1)      # through core k, no D_k
+        S = _ttm_suffix(cores, diags, dig, k + 1)      # from core k+1, no D_k
+        G = dR.reshape(U, P.shape[1], S.shape[2])
+        g = np.einsum("ulc,ulr,ucr->c", P, G, S)
+        if prune_convention:
+            g = np.where(np.asarray(diags[k]) == 0, 0.0, g)
+        dE[k] = g
+    return dC, dE

@@ -198,3 +198,91 @@ def unpack(shape: LayerShape, flat: np.ndarray):
         off += n
     assert off == flat.size, (off, flat.size)
     return cores, diags
+
+
+# ---------------------------------------------------------------------------
+# TT-matrix (TTM) embedding tables: E (V x Dm), V = prod m_k rows (the
+# vocabulary), Dm = prod n_k columns; cores F_k of shape (r_{k-1}, m_k, n_k,
+# r_k), r_0 = r_d = 1, with a diagonal on every internal link as for the TT
+# layers.  Packed like the TT layers: F_1..F_d row-major, then D_1..D_{d-1}.
+
+
+@dataclasses.dataclass(frozen=True)
+class TtmShape:
+    row_modes: Tuple[int, ...]   # m_1..m_d, V = prod
+    col_modes: Tuple[int, ...]   # n_1..n_d, Dm = prod
+    ranks: Tuple[int, ...]       # r_0..r_d, r_0 = r_d = 1
+
+    @property
+    def d(self) -> int:
+        return len(self.row_modes)
+
+    @property
+    def V(self) -> int:
+        return int(np.prod(self.row_modes))
+
+    @property
+    def Dm(self) -> int:
+        return int(np.prod(self.col_modes))
+
+    def core_shapes(self):
+        return [(self.ranks[k], self.row_modes[k], self.col_modes[k], self.ranks[k + 1])
+                for k in range(self.d)]
+
+    def diag_sizes(self):
+        return [self.ranks[k] for k in range(1, self.d)]
+
+
+@dataclasses.dataclass(frozen=True)
+class TtmWorkload:
+    name: str
+    shape: TtmShape
+    batch: int        # indices looked up per step
+    vocab: int        # indices are drawn from [0, vocab) (vocab <= V)
+    zipf_s: float     # P(rank k) proportional to 1 / (k + 1)^s
+    core_std: float
+    description: str = ""
+
+
+_TTM_BERT = TtmShape((32, 32, 32), (8, 8, 12), (1, 30, 30, 1))
+
+TTM_WORKLOADS = {
+    f"ttm_emb_{b // 1000}k": TtmWorkload(
+        f"ttm_emb_{b // 1000}k", _TTM_BERT, b, 30522, 1.0, 0.2,
+        description=f"TTM embedding 30522(->32768 as (32,32,32)) x 768 as (8,8,12), "
+                    f"ranks 30, D~U(0.5,1.5), {b} Zipf(1.0) indices, fp32")
+    for b in (10000, 20000, 40000)
+}
+
+
+@dataclasses.dataclass
+class TtmInputs:
+    cores: List[np.ndarray]   # float32 (r_{k-1}, m_k, n_k, r_k)
+    diags: List[np.ndarray]   # float32
+    idx: np.ndarray           # (B,) int32 row indices
+    dout: np.ndarray          # (B, Dm) float32 upstream gradient
+
+
+def zipf_indices(rng: np.random.Generator, n: int, vocab: int, s: float) -> np.ndarray:
+    """n indices in [0, vocab): frequency rank k has probability
+    proportional to 1/(k+1)^s (inverse-CDF sampling), and a seeded
+    permutation maps ranks to indices so frequent rows are spread out."""
+    w = 1.0 / np.arange(1, vocab + 1, dtype=np.float64) ** s
+    cdf = np.cumsum(w)
+    cdf /= cdf[-1]
+    perm = rng.permutation(vocab)
+    ranks = np.searchsorted(cdf, rng.random(n), side="right")
+    ranks = np.minimum(ranks, vocab - 1)
+    return perm[ranks].astype(np.int32)
+
+
+def draw_ttm(w: TtmWorkload, seed: int = 0, batch: Optional[int] = None) -> TtmInputs:
+    """Draw order: cores, diagonals, index permutation and indices, dout."""
+    B = w.batch if batch is None else int(batch)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cores = [(rng.standard_normal(cs) * w.core_std).astype(np.float32)
+             for cs in w.shape.core_shapes()]
+    diags = [rng.uniform(0.5, 1.5, n).astype(np.float32) for n in w.shape.diag_sizes()]
+    idx = zipf_indices(rng, B, w.vocab, w.zipf_s)
+    dout = rng.standard_normal((B, w.shape.Dm)).astype(np.float32)
+    return TtmInputs(cores, diags, idx, dout)
