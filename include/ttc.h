@@ -182,6 +182,54 @@ typedef struct tt_rank_opts {
 tt_status tt_rank_update(const tt_plan_t* plan, float* params, float* dparams,
                          const tt_rank_opts* opts, void* stream);
 
+/* ---- TT-matrix (TTM) embedding lookup ---------------------------------------
+ * [CoMERA project page, "Making small tensor operations fast on GPUs", bullet
+ * "Embedding lookup without repeated work": keep only the unique rows of a
+ * batch, contract neighbouring cores in pairs so each shared part is computed
+ * once, and assemble the rows with one batched product; the table is in
+ * tensor-train-matrix format (project page, "Learn the ranks while training";
+ * poster digest, TT/TTM figure)].
+ * The table E (V x Dm), V = prod m_k rows, Dm = prod n_k columns, is
+ *     E[i, j] = F_1[0, i_1, j_1, :] D_1 F_2[:, i_2, j_2, :] D_2 ... F_d[:, i_d, j_d, 0]
+ * with i = (i_1..i_d) and j = (j_1..j_d) row-major (first mode most
+ * significant).  Packed params: F_1..F_d, each (r_{k-1}, m_k, n_k, r_k)
+ * row-major, then D_1..D_{d-1}, fp32 (tt_param_layout describes a TTM plan
+ * too: d core offsets, d-1 diagonal offsets).  d is 2 or 3; ranks 1..64;
+ * n_1 n_2 r_2 <= 8192, r_1 n_2 r_2 <= 16384 and Dm <= 8192 (else
+ * TT_ERR_UNSUPPORTED). */
+typedef struct tt_ttm_desc {
+  int d;               /* 2 or 3 cores */
+  int row_modes[4];    /* m_1..m_d (the vocabulary V = prod m_k, <= 2^24) */
+  int col_modes[4];    /* n_1..n_d (the embedding width Dm = prod n_k) */
+  int ranks[5];        /* r_0..r_d, r_0 = r_d = 1 */
+  unsigned flags;      /* TT_ACCUMULATE (backward adds into dparams) */
+} tt_ttm_desc;
+tt_status tt_ttm_plan(const tt_ttm_desc* desc, tt_plan_t** out);
+
+/* out[b, :] = E[idx[b], :] for b < B (out: B x Dm fp32, row-major; idx:
+ * int32 device array).  Each distinct row and each distinct (i_1, i_2)
+ * prefix is computed once.  An index outside [0, V) is skipped (its output
+ * row is left unwritten) and recorded in the device status word
+ * (TT_ERR_DEVICE from tt_get_device_status).  Workspace: tt_workspace_size
+ * with T = B.  B == 0 is a no-op. */
+tt_status tt_ttm_lookup(const tt_plan_t* plan, int64_t B, const int32_t* idx,
+                        const float* params, float* out, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/* Gradients of L = <dout, lookup(idx)> (dout: B x Dm fp32): every dF_k and
+ * dD_k into dparams (overwritten, or added to under TT_ACCUMULATE); repeated
+ * indices add up.  dD_k[a] is 0 where D_k[a] == 0 (as for the TT layers).
+ * Recomputes the forward's unique rows; needs no state from a lookup call.
+ * Gradient sums are reduced with atomics (summation order not fixed). */
+tt_status tt_ttm_lookup_backward(const tt_plan_t* plan, int64_t B, const int32_t* idx,
+                                 const float* dout, const float* params, float* dparams,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* After a lookup or backward on ws (synchronises stream): the number of
+ * distinct rows and of distinct (i_1, i_2) prefixes of that batch. */
+tt_status tt_ttm_stats(const tt_plan_t* plan, const void* ws, int64_t* unique_rows,
+                       int64_t* unique_pairs, void* stream);
+
 /* Synchronise stream, then read and clear the status word of the current
  * device.  The word is sticky: it holds the first error any libttc kernel
  * on this device recorded since the last read.  Returns TT_OK,

@@ -680,6 +680,14 @@ static tt_status layout_out(const LayerPlan& L, size_t* core_off, size_t* diag_o
 tt_status tt_param_layout(const tt_plan_t* plan, size_t* core_off, size_t* diag_off,
                           size_t* n_floats) {
   if (!plan) return TT_ERR_INVALID_ARG;
+  if (plan->kind == 2) {  // TT-matrix table: d cores, d-1 diagonals
+    if (!core_off || !diag_off || !n_floats) return TT_ERR_INVALID_ARG;
+    const TtmPlan& P = plan->ttm;
+    for (int k = 0; k < P.d; ++k) core_off[k] = P.core_off[k];
+    for (int k = 0; k < P.d - 1; ++k) diag_off[k] = P.diag_off[k];
+    *n_floats = P.n_floats;
+    return TT_OK;
+  }
   return layout_out(plan->L[0], core_off, diag_off, n_floats);
 }
 
@@ -694,6 +702,9 @@ tt_status tt_workspace_size(const tt_plan_t* plan, int64_t T, size_t* bytes) {
   if (plan->kind == 0) {
     WsLayout w;
     *bytes = layer_layout(plan->L[0], T, 256, &w);
+  } else if (plan->kind == 2) {
+    if (T > 0x7FFFFFFF) return TT_ERR_INVALID_ARG;
+    *bytes = ttm_workspace_bytes(plan->ttm, T);
   } else {
     FfnLayout f;
     *bytes = ffn_layout(plan, T, &f);
@@ -828,10 +839,11 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
 tt_status tt_get_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return TT_ERR_CUDA;
-  DeviceStatus h{0, 0};
+  DeviceStatus h{0, 0}, e{0, 0};
   if (read_and_clear_device_status(&h) != cudaSuccess) return TT_ERR_CUDA;
+  if (read_and_clear_ttm_status(&e) != cudaSuccess) return TT_ERR_CUDA;
   if (h.code == TT_ERR_TIMEOUT) return TT_ERR_TIMEOUT;
-  if (h.code != 0) return TT_ERR_DEVICE;
+  if (h.code != 0 || e.code != 0) return TT_ERR_DEVICE;
   return TT_OK;
 }
 

@@ -32,9 +32,24 @@ struct LayerPlan {
 
 }  // namespace ttc
 
+namespace ttc {
+// TT-matrix embedding table: cores F_k (r_{k-1}, m_k, n_k, r_k), diagonals
+// D_1..D_{d-1}; a table of two cores runs as three with a unit third core.
+struct TtmPlan {
+  int d = 0;                      // 2 or 3
+  int m[3] = {1, 1, 1}, n[3] = {1, 1, 1}, r[4] = {1, 1, 1, 1};
+  int64_t V = 0, Dm = 0;          // rows (prod m), width (prod n)
+  int64_t npair = 0;              // distinct (i_1, i_2) prefixes: m_1 m_2
+  size_t core_off[3] = {}, diag_off[2] = {}, n_floats = 0;
+  unsigned flags = 0;
+};
+size_t ttm_workspace_bytes(const TtmPlan& P, int64_t B);
+}  // namespace ttc
+
 struct tt_plan_s {
-  int kind = 0;  // 0 = single layer, 1 = FFN pair
+  int kind = 0;  // 0 = single layer, 1 = FFN pair, 2 = TT-matrix embedding
   ttc::LayerPlan L[2];
+  ttc::TtmPlan ttm;
 };
 
 namespace ttc {
@@ -46,6 +61,8 @@ struct DeviceStatus {
 };
 // Copies the current device's status word to *out and zeroes it.
 cudaError_t read_and_clear_device_status(DeviceStatus* out);
+// The same for the embedding kernels' own word (ttm.cu).
+cudaError_t read_and_clear_ttm_status(DeviceStatus* out);
 
 // ---- measurement hooks (profile.cu) ---------------------------------------
 enum Phase { kPhMerge = 0, kPhFwd = 1, kPhBwd = 2, kPhMergeBwd = 3, kPhElem = 4 };

@@ -135,3 +135,50 @@ class TTFFN:
                                       _ptr(ws), ws.numel(), _stream(stream)),
                   "tt_ffn_backward")
         return dx, dp_up, dp_down
+
+
+class TTMEmbedding:
+    """TT-matrix embedding table: lookup of rows for int32 indices and its
+    backward into the packed cores/diagonals (float32)."""
+
+    def __init__(self, row_modes: Sequence[int], col_modes: Sequence[int],
+                 ranks: Sequence[int], accumulate: bool = False):
+        flags = ttc.TT_ACCUMULATE if accumulate else 0
+        self.desc = ttc.make_ttm_desc(row_modes, col_modes, ranks, flags)
+        self.plan = ttc.tt_ttm_plan(self.desc)
+        self.core_off, self.diag_off, self.n_params = ttc.tt_param_layout(self.plan)
+        self.V = 1
+        self.Dm = 1
+        for m in row_modes:
+            self.V *= m
+        for n in col_modes:
+            self.Dm *= n
+
+    def workspace(self, B: int, device="cuda") -> torch.Tensor:
+        return torch.empty(ttc.tt_workspace_size(self.plan, B), dtype=torch.uint8, device=device)
+
+    def lookup(self, idx: torch.Tensor, params: torch.Tensor, out=None, ws=None, stream=None):
+        B = idx.shape[0]
+        if out is None:
+            out = torch.empty((B, self.Dm), dtype=torch.float32, device=idx.device)
+        if ws is None:
+            ws = self.workspace(B, idx.device)
+        ttc.check(ttc.tt_ttm_lookup(self.plan, B, _ptr(idx), _ptr(params), _ptr(out), _ptr(ws),
+                                    ws.numel(), _stream(stream)), "tt_ttm_lookup")
+        return out
+
+    def backward(self, idx: torch.Tensor, dout: torch.Tensor, params: torch.Tensor,
+                 dparams=None, ws=None, stream=None):
+        B = idx.shape[0]
+        if dparams is None:
+            dparams = torch.empty(self.n_params, dtype=torch.float32, device=idx.device)
+        if ws is None:
+            ws = self.workspace(B, idx.device)
+        ttc.check(ttc.tt_ttm_lookup_backward(self.plan, B, _ptr(idx), _ptr(dout), _ptr(params),
+                                             _ptr(dparams), _ptr(ws), ws.numel(),
+                                             _stream(stream)), "tt_ttm_lookup_backward")
+        return dparams
+
+    def stats(self, ws: torch.Tensor, stream=None):
+        """(distinct rows, distinct (i_1, i_2) prefixes) of the last call on ws."""
+        return ttc.tt_ttm_stats(self.plan, _ptr(ws), _stream(stream))

@@ -51,6 +51,16 @@ class tt_desc(ctypes.Structure):
     ]
 
 
+class tt_ttm_desc(ctypes.Structure):
+    _fields_ = [
+        ("d", ctypes.c_int),
+        ("row_modes", ctypes.c_int * TT_MAX_D),
+        ("col_modes", ctypes.c_int * TT_MAX_D),
+        ("ranks", ctypes.c_int * (TT_MAX_D + 1)),
+        ("flags", ctypes.c_uint),
+    ]
+
+
 class tt_rank_opts(ctypes.Structure):
     _fields_ = [
         ("gamma", ctypes.c_float),
@@ -88,6 +98,10 @@ def lib() -> ctypes.CDLL:
             "tt_ffn_forward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_rank_update": [_P, _P, _P, _P, _P],
+            "tt_ttm_plan": [_P, _P],
+            "tt_ttm_lookup": [_P, _I64, _P, _P, _P, _P, _SZ, _P],
+            "tt_ttm_lookup_backward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
+            "tt_ttm_stats": [_P, _P, _P, _P, _P],
             "tt_get_device_status": [_P],
             "tt_status_string": [ctypes.c_int],
         }
@@ -174,7 +188,11 @@ def _layout(fn, args, d):
 
 
 def tt_param_layout(plan: Plan):
-    return _layout(lib().tt_param_layout, [ctypes.c_void_p(plan.handle)], plan.d[0])
+    core, diag, n = _layout(lib().tt_param_layout, [ctypes.c_void_p(plan.handle)], plan.d[0])
+    if plan.kind == "ttm":  # a TT-matrix table: d cores, d-1 diagonals
+        d = plan.d[0]
+        return core[:d], diag[:d - 1], n
+    return core, diag, n
 
 
 def tt_ffn_param_layout(plan: Plan, layer: int):
@@ -227,6 +245,45 @@ def tt_rank_update(plan: Plan, params: int, dparams: int, gamma: float, beta: fl
     o = tt_rank_opts(float(gamma), float(beta), float(lr))
     return lib().tt_rank_update(ctypes.c_void_p(plan.handle), params, dparams,
                                 ctypes.byref(o), stream)
+
+
+def make_ttm_desc(row_modes: Sequence[int], col_modes: Sequence[int], ranks: Sequence[int],
+                  flags: int = 0) -> tt_ttm_desc:
+    desc = tt_ttm_desc()
+    desc.d = len(row_modes)
+    for k in range(len(row_modes)):
+        desc.row_modes[k] = int(row_modes[k])
+        desc.col_modes[k] = int(col_modes[k])
+    for k, r in enumerate(ranks):
+        desc.ranks[k] = int(r)
+    desc.flags = int(flags)
+    return desc
+
+
+def tt_ttm_plan(desc: tt_ttm_desc) -> Plan:
+    h = ctypes.c_void_p()
+    _check(lib().tt_ttm_plan(ctypes.byref(desc), ctypes.byref(h)), "tt_ttm_plan")
+    return Plan(h.value, "ttm", (desc.d,))
+
+
+def tt_ttm_lookup(plan: Plan, B: int, idx: int, params: int, out: int, ws: int, ws_bytes: int,
+                  stream: int = 0) -> int:
+    return lib().tt_ttm_lookup(ctypes.c_void_p(plan.handle), int(B), idx, params, out, ws,
+                               int(ws_bytes), stream)
+
+
+def tt_ttm_lookup_backward(plan: Plan, B: int, idx: int, dout: int, params: int, dparams: int,
+                           ws: int, ws_bytes: int, stream: int = 0) -> int:
+    return lib().tt_ttm_lookup_backward(ctypes.c_void_p(plan.handle), int(B), idx, dout, params,
+                                        dparams, ws, int(ws_bytes), stream)
+
+
+def tt_ttm_stats(plan: Plan, ws: int, stream: int = 0):
+    u = ctypes.c_int64()
+    p = ctypes.c_int64()
+    _check(lib().tt_ttm_stats(ctypes.c_void_p(plan.handle), ws, ctypes.byref(u),
+                              ctypes.byref(p), stream), "tt_ttm_stats")
+    return u.value, p.value
 
 
 def tt_get_device_status(stream: int = 0) -> int:

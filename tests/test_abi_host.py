@@ -137,6 +137,40 @@ def test_argument_errors_return_before_any_launch(lib):
     assert ttc.tt_rank_update(ffn, fake, fake, 0.1, 0.1, 0.1) == 1
 
 
+def test_ttm_plan_and_argument_errors(lib):
+    plan = ttc.tt_ttm_plan(ttc.make_ttm_desc((32, 32, 32), (8, 8, 12), (1, 30, 30, 1)))
+    core, diag, n = ttc.tt_param_layout(plan)
+    t = synth.draw_ttm(synth.TTM_WORKLOADS["ttm_emb_10k"], batch=4)
+    assert n == synth.pack(t.cores, t.diags).size
+    assert core == [0, 7680, 238080] and diag == [249600, 249630]
+    a = ttc.tt_workspace_size(plan, 10000)
+    b = ttc.tt_workspace_size(plan, 40000)
+    assert 0 < a < b
+    for bad in [((32,), (8,), (1, 1)),                       # d = 1
+                ((32, 32, 32), (8, 8, 12), (2, 30, 30, 1)),  # r_0 != 1
+                ((32, 0, 32), (8, 8, 12), (1, 30, 30, 1))]:  # empty mode
+        with pytest.raises(ttc.TTError) as e:
+            ttc.tt_ttm_plan(ttc.make_ttm_desc(*bad))
+        assert e.value.code == 1
+    with pytest.raises(ttc.TTError) as e:   # rank above 64: no kernel
+        ttc.tt_ttm_plan(ttc.make_ttm_desc((32, 32), (8, 8), (1, 65, 1)))
+    assert e.value.code == 2
+    fake = 1 << 40
+    ws = ttc.tt_workspace_size(plan, 64)
+    assert ttc.tt_ttm_lookup(plan, 0, 0, 0, 0, 0, 0) == 0                    # B == 0
+    assert ttc.tt_ttm_lookup(plan, -1, fake, fake, fake, fake, ws) == 1
+    assert ttc.tt_ttm_lookup(plan, 64, 0, fake, fake, fake, ws) == 1         # NULL idx
+    assert ttc.tt_ttm_lookup(plan, 64, fake, fake, fake + 4, fake, ws) == 1  # misaligned out
+    assert ttc.tt_ttm_lookup(plan, 64, fake, fake, fake, fake, ws - 1) == 3  # small workspace
+    assert ttc.tt_ttm_lookup(plan, 64, fake, fake, fake, fake + 64, ws) == 3 # misaligned ws
+    assert ttc.tt_ttm_lookup_backward(plan, 64, fake, fake, 0, fake, fake, ws) == 1
+    # a TT-layer plan is not a table and the reverse
+    layer = ttc.tt_plan(_desc(synth.WORKLOADS["tt768_bf16"].layers[0]))
+    assert ttc.tt_ttm_lookup(layer, 64, fake, fake, fake, fake, ws) == 1
+    assert ttc.tt_forward(plan, 64, fake, fake, fake, fake, ws) == 1
+    assert ttc.tt_rank_update(plan, fake, fake, 0.1, 0.1, 0.1) == 1
+
+
 def test_status_strings(lib):
     for code, name in ttc.STATUS.items():
         assert ttc.tt_status_string(code).startswith(name)
