@@ -601,9 +601,279 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# TT-matrix embedding lookup (a second workload: lookup + backward per step)
+
+
+def ttm_oracle_step(inp):
+    from oracle import tt_oracle as O
+    import numpy as np
+    cores = [c.astype(np.float64) for c in inp.cores]
+    diags = [e.astype(np.float64) for e in inp.diags]
+    O.ttm_lookup(cores, diags, inp.idx)
+    O.ttm_lookup_backward(cores, diags, inp.idx, inp.dout)
+
+
+def time_ttm_oracle(w, sample, budget_s):
+    from tensor_train_compressed_tt_gb300 import synth
+    inp = synth.draw_ttm(w, seed=0, batch=sample)
+    ttm_oracle_step(inp)
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        ttm_oracle_step(inp)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return n * sample / el, n, el
+
+
+def run_ttm(args, w):
+    """Lookup + backward of a TT-matrix table per step (graph-replayed)."""
+    import numpy as np
+    import torch
+
+    from tensor_train_compressed_tt_gb300 import _build, synth, ttc
+    from tensor_train_compressed_tt_gb300.layer import TTMEmbedding
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(ttc.LIB_PATH):
+        _build.build()
+    B = args.tokens or w.batch
+    S = w.shape
+    inp0 = synth.draw_ttm(w, seed=rank, batch=B)
+    emb = TTMEmbedding(S.row_modes, S.col_modes, S.ranks)
+    params = torch.from_numpy(synth.pack(inp0.cores, inp0.diags)).to(dev)
+    dparams = torch.empty(emb.n_params, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    set_bytes = 4 * B * (2 * S.Dm + 1)
+    nsets = max(2, -(-2 * l2 // set_bytes) + 1)
+    sets = []
+    for i in range(nsets):
+        t = inp0 if i == 0 else synth.draw_ttm(w, seed=1000 * rank + i, batch=B)
+        sets.append((torch.from_numpy(t.idx).to(dev), torch.from_numpy(t.dout).to(dev),
+                     torch.empty((B, S.Dm), device=dev)))
+    ws = emb.workspace(B, dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    wsp, wsn = ws.data_ptr(), ws.numel()
+
+    def fwd(i, sh=sh):
+        idx, _, out = sets[i % nsets]
+        ttc.check(ttc.tt_ttm_lookup(emb.plan, B, idx.data_ptr(), params.data_ptr(),
+                                    out.data_ptr(), wsp, wsn, sh))
+
+    def bwd(i, sh=sh):
+        idx, dout, _ = sets[i % nsets]
+        ttc.check(ttc.tt_ttm_lookup_backward(emb.plan, B, idx.data_ptr(), dout.data_ptr(),
+                                             params.data_ptr(), dparams.data_ptr(), wsp, wsn,
+                                             sh))
+
+    def step(i, sh=sh):
+        fwd(i, sh)
+        bwd(i, sh)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    W = max(3, args.warmup)
+    for i in range(W):
+        step(i)
+    ttc.check(ttc.tt_get_device_status(sh), "device status after warm-up")
+    barrier()
+    uniq, pairs = emb.stats(ws)
+    graphs, graph_note, per_step = None, "eager", None
+    if not args.eager:
+        try:
+            graphs = []
+            for j in range(nsets):
+                g = torch.cuda.CUDAGraph()
+                c0 = ttc.lib().tt_launch_count()
+                with torch.cuda.graph(g):
+                    step(j, int(torch.cuda.current_stream().cuda_stream))
+                per_step = int(ttc.lib().tt_launch_count() - c0)
+                graphs.append(g)
+            for j in range(max(3, nsets)):
+                graphs[j % nsets].replay()
+            torch.cuda.synchronize(dev)
+            graph_note = "cuda_graph"
+        except Exception as e:
+            graphs, graph_note = None, f"eager (graph capture failed: {type(e).__name__}: {e})"
+            torch.cuda.synchronize(dev)
+
+    def run(i):
+        if graphs is not None:
+            graphs[i % nsets].replay()
+        else:
+            step(i)
+    if args.steps is None:
+        t0 = time.perf_counter()
+        for i in range(5):
+            run(i)
+        torch.cuda.synchronize(dev)
+        per = (time.perf_counter() - t0) / 5
+        K = int(min(100000, max(20, args.target_seconds / max(per, 1e-6))))
+        K = int(all_reduce_scalar(K, "min", dev))
+    else:
+        K = args.steps
+    barrier()
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    l0 = ttc.lib().tt_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for i in range(K):
+        run(i)
+    ev1.record(stream)
+    barrier()
+    launches = int(ttc.lib().tt_launch_count() - l0)
+    if graphs is not None:
+        launches = K * per_step
+    clk = clocks.stop()
+    ms = all_reduce_scalar(ev0.elapsed_time(ev1) / K, "max", dev)
+    ttc.check(ttc.tt_get_device_status(sh), "device status after timed region")
+
+    # each call on its own (eager), for the roofline of the dominant one
+    def timed(fn, n=50):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        barrier()
+        a.record(stream)
+        for i in range(n):
+            fn(i)
+        b.record(stream)
+        barrier()
+        return a.elapsed_time(b) / n * 1e-3
+    t_f, t_b = timed(fwd), timed(bwd)
+    peak, peak_kind = measured_peaks()
+    # algorithmic bytes: lookup writes B x Dm rows and reads the indices;
+    # backward reads dout and the indices (tables and gradients: < 1 MB)
+    by_f = 4 * B * (S.Dm + 1)
+    by_b = 4 * B * (S.Dm + 1)
+    dom, t_dom, by_dom = ("backward", t_b, by_b) if t_b >= t_f else ("lookup", t_f, by_f)
+    ach = by_dom / t_dom / 1e9
+    roof = {"bound": "hbm", "kernel": f"tt_ttm_{dom} (one call, several kernels)",
+            "achieved": ach, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": ach / peak, "traffic": None, "algorithmic_bytes_per_launch": by_dom}
+    value = whole_job_rate(B, world, ms)
+
+    e2e = None
+    if not args.no_e2e:
+        hi = torch.from_numpy(inp0.idx).pin_memory()
+        hd = torch.from_numpy(inp0.dout).pin_memory()
+        ho = torch.empty((B, S.Dm)).pin_memory()
+        hp = torch.empty(emb.n_params).pin_memory()
+        di, dd, do = sets[0]
+        Ke = 50
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(Ke):
+            di.copy_(hi, non_blocking=True)
+            dd.copy_(hd, non_blocking=True)
+            fwd(0)
+            bwd(0)
+            ho.copy_(do, non_blocking=True)
+            hp.copy_(dparams, non_blocking=True)
+        b.record(stream)
+        barrier()
+        ms_e = all_reduce_scalar(a.elapsed_time(b) / Ke, "max", dev)
+        e2e = {"value": whole_job_rate(B, world, ms_e), "unit": "tokens/s",
+               "h2d_bytes_per_step": hi.numel() * 4 + hd.numel() * 4,
+               "d2h_bytes_per_step": ho.numel() * 4 + hp.numel() * 4, "ms_per_step": ms_e,
+               "steps": Ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, el = time_ttm_oracle(w, min(B, 4000), 10.0)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{n} lookup+backward passes of the fp64 numpy oracle on "
+                         f"{min(B, 4000)} of the {B} indices ({el:.1f} s)"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "description": w.description, "tokens": B,
+                       "row_modes": list(S.row_modes), "col_modes": list(S.col_modes),
+                       "ranks": list(S.ranks), "distinct_rows": uniq, "distinct_prefixes": pairs,
+                       "l2": f"{nsets} rotating index/gradient/output sets of "
+                             f"{set_bytes / 1e6:.1f} MB (> 2x L2 of {l2 / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}", "launch": graph_note},
+            "lookup_us": t_f * 1e6, "backward_us": t_b * 1e6,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_ttm_reference(args, w):
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return
+    B = args.tokens or w.batch
+    K = args.steps if args.steps is not None else 20
+    W = args.warmup
+    rate, _, _ = time_ttm_oracle(w, min(B, 512), 1.0)
+    per_step = 120.0 / max(1, K + W)
+    sample = int(max(16, min(B, rate * per_step)))
+    from tensor_train_compressed_tt_gb300 import synth
+    inp = synth.draw_ttm(w, seed=0, batch=sample)
+    for _ in range(W):
+        ttm_oracle_step(inp)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        ttm_oracle_step(inp)
+    el = time.perf_counter() - t0
+    value = K * sample / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": 1e3 * el / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "tokens": B,
+                   "sample_tokens_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(),
+                         "kind": "oracle",
+                         "sample": f"{sample} of {B} indices per step, fp64 numpy oracle "
+                                   f"(distinct rows only), {K} steps"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from tensor_train_compressed_tt_gb300 import synth
+    if args.workload in synth.TTM_WORKLOADS:
+        w = synth.TTM_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            run_ttm_reference(args, w)
+        else:
+            run_ttm(args, w)
+        return
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

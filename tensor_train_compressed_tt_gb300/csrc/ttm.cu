@@ -8,14 +8,16 @@
 // table runs as a three-core one whose third core and second diagonal are a
 // single 1.
 //
-// Forward:  count -> scan -> pair products -> distinct rows -> scatter.
-// Backward: count -> scan (+ row chunks) -> fill (occurrence lists) -> pair
-//           products -> chunk sums of dout -> per distinct row: dF_3 and the
-//           pair-product gradients -> per pair: dF_1, dF_2, dD_1, dD_2.
+// Forward:  count -> tiled scan -> per prefix: pair product and its rows ->
+//           scatter.
+// Backward: count -> tiled scan (+ row chunks) -> fill (occurrence lists) ->
+//           chunk sums of dout -> per prefix: pair product, its rows' dF_3 and
+//           pair-product gradient, then dF_1, dF_2, dD_1, dD_2.
 // Sums over repeated indices and over rows sharing a prefix use atomics.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
 #include <new>
 
 #include "ttc.h"
@@ -58,8 +60,6 @@ struct TtmArgs {
   int* plist;     // [pcap] prefix of each slot
   int* counts;    // [4]: distinct rows, distinct prefixes, backward units
   int* occ;       // [B] occurrence lists
-  float* P;       // [pcap][nA][r2] pair products F_1 D_1 F_2 (without D_2)
-  float* dP;      // [pcap][nA][r2] gradient w.r.t. P * D_2
   float* rows;    // [ucap][Dm] distinct rows (forward) / [units][Dm] chunk sums (backward)
 };
 
@@ -75,73 +75,171 @@ __global__ void ttm_count_kernel(TtmArgs a, const int32_t* __restrict__ idx) {
   }
 }
 
-// Inclusive scan of 1024 per-thread values held in s (one block of 1024).
-__device__ void block_scan_1024(int* s, int t) {
-  for (int o = 1; o < 1024; o <<= 1) {
-    const int x = t >= o ? s[t - o] : 0;
-    __syncthreads();
-    s[t] += x;
-    __syncthreads();
+// Inclusive scans over the block (a multiple of 32 threads, at most 1024)
+// of three per-thread values (warp shuffles, then one warp over the warp
+// totals).  After the call w1[nw-1], w2[nw-1], w3[nw-1] hold the block
+// totals, nw = blockDim.x / 32.
+__device__ void block_scan3(int& x1, int& x2, int& x3, int* w1, int* w2, int* w3) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y1 = __shfl_up_sync(0xffffffffu, x1, o);
+    const int y2 = __shfl_up_sync(0xffffffffu, x2, o);
+    const int y3 = __shfl_up_sync(0xffffffffu, x3, o);
+    if (lane >= o) {
+      x1 += y1;
+      x2 += y2;
+      x3 += y3;
+    }
+  }
+  if (lane == 31) {
+    w1[warp] = x1;
+    w2[warp] = x2;
+    w3[warp] = x3;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int v1 = lane < nw ? w1[lane] : 0, v2 = lane < nw ? w2[lane] : 0;
+    int v3 = lane < nw ? w3[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y1 = __shfl_up_sync(0xffffffffu, v1, o);
+      const int y2 = __shfl_up_sync(0xffffffffu, v2, o);
+      const int y3 = __shfl_up_sync(0xffffffffu, v3, o);
+      if (lane >= o) {
+        v1 += y1;
+        v2 += y2;
+        v3 += y3;
+      }
+    }
+    if (lane < nw) {
+      w1[lane] = v1;
+      w2[lane] = v2;
+      w3[lane] = v3;
+    }
+  }
+  __syncthreads();
+  if (warp > 0) {
+    x1 += w1[warp - 1];
+    x2 += w2[warp - 1];
+    x3 += w3[warp - 1];
   }
 }
 
-// One block of 1024 threads: occurrence offsets, distinct-row slots, backward
-// units, and prefix slots, each an exclusive prefix sum over a contiguous
-// segment per thread.
-__global__ void __launch_bounds__(1024) ttm_scan_kernel(TtmArgs a) {
-  __shared__ int s1[1024], s2[1024], s3[1024];
-  const int t = threadIdx.x;
-  const int chunk = (a.V + 1023) / 1024;
-  const int lo = min(t * chunk, a.V), hi = min(lo + chunk, a.V);
-  int c = 0, f = 0, u = 0;
-  for (int v = lo; v < hi; ++v) {
-    const int x = a.cnt[v];
-    c += x;
-    f += x > 0;
-    u += (x + kChunk - 1) / kChunk;
-  }
-  s1[t] = c;
-  s2[t] = f;
-  s3[t] = u;
-  __syncthreads();
-  block_scan_1024(s1, t);
-  block_scan_1024(s2, t);
-  block_scan_1024(s3, t);
-  int ec = t ? s1[t - 1] : 0, ef = t ? s2[t - 1] : 0, eu = t ? s3[t - 1] : 0;
-  for (int v = lo; v < hi; ++v) {
-    const int x = a.cnt[v];
-    a.off[v] = ec;
-    ec += x;
-    if (x > 0) {
-      a.upos[v] = ef;
-      a.ulist[ef] = v;
-      a.uoff[ef] = eu;
-      const int nch = (x + kChunk - 1) / kChunk;
-      for (int k = 0; k < nch; ++k) a.unit_u[eu + k] = ef;
-      eu += nch;
-      ++ef;
+constexpr int kScanPer = 8;                    // elements per thread of a tile
+constexpr int kScanThreads = 256;
+constexpr int kScanTile = kScanThreads * kScanPer;
+
+// Per-thread sums over its kScanPer consecutive entries of a tile: rows give
+// (occurrences, distinct, backward units), prefixes give (used, 0, 0).
+__device__ void tile_sums(const TtmArgs& a, bool rows, int base, int n, int* c, int* f, int* u) {
+  const int lo = threadIdx.x * kScanPer, hi = min(lo + kScanPer, n);
+  *c = *f = *u = 0;
+  for (int i = lo; i < hi; ++i) {
+    const int x = rows ? a.cnt[base + i] : a.cnt_pair[base + i];
+    if (rows) {
+      *c += x;
+      *f += x > 0;
+      *u += (x + kChunk - 1) / kChunk;
+    } else {
+      *c += x != 0;
     }
   }
-  if (t == 1023) {
-    a.counts[0] = s2[1023];
-    a.counts[2] = s3[1023];
+}
+
+// Blocks [0, ntr) cover row tiles, [ntr, ntr + ntp) prefix tiles: each
+// writes its tile totals (tsum[3 * tile + 0..2]).
+__global__ void __launch_bounds__(kScanThreads) ttm_tile_sum_kernel(TtmArgs a, int ntr, int* tsum) {
+  __shared__ int w1[32], w2[32], w3[32];
+  const bool rows = (int)blockIdx.x < ntr;
+  const int tile = rows ? blockIdx.x : blockIdx.x - ntr;
+  const int base = tile * kScanTile;
+  const int n = min(kScanTile, (rows ? a.V : a.npair) - base);
+  int c, f, u;
+  tile_sums(a, rows, base, n, &c, &f, &u);
+  block_scan3(c, f, u, w1, w2, w3);
+  if (threadIdx.x == 0) {
+    const int nw = blockDim.x >> 5;
+    tsum[3 * blockIdx.x + 0] = w1[nw - 1];
+    tsum[3 * blockIdx.x + 1] = w2[nw - 1];
+    tsum[3 * blockIdx.x + 2] = w3[nw - 1];
   }
-  __syncthreads();
-  const int pch = (a.npair + 1023) / 1024;
-  const int plo = min(t * pch, a.npair), phi = min(plo + pch, a.npair);
-  f = 0;
-  for (int p = plo; p < phi; ++p) f += a.cnt_pair[p] != 0;
-  s2[t] = f;
-  __syncthreads();
-  block_scan_1024(s2, t);
-  ef = t ? s2[t - 1] : 0;
-  for (int p = plo; p < phi; ++p) {
-    if (a.cnt_pair[p]) {
-      a.pos_pair[p] = ef;
-      a.plist[ef++] = p;
+}
+
+// One block: exclusive prefix of the tile totals (rows and prefixes apart);
+// the grand totals go to counts[0..2].
+__global__ void __launch_bounds__(1024) ttm_tile_scan_kernel(TtmArgs a, int ntr, int ntp, int* tsum) {
+  __shared__ int w1[32], w2[32], w3[32];
+  for (int part = 0; part < 2; ++part) {
+    const int t0 = part == 0 ? 0 : ntr, nt = part == 0 ? ntr : ntp;
+    int carry_c = 0, carry_f = 0, carry_u = 0;
+    for (int base = 0; base < nt; base += 1024) {
+      const int i = base + threadIdx.x;
+      int c = 0, f = 0, u = 0;
+      if (i < nt) {
+        c = tsum[3 * (t0 + i)];
+        f = tsum[3 * (t0 + i) + 1];
+        u = tsum[3 * (t0 + i) + 2];
+      }
+      int ic = c, iff = f, iu = u;
+      block_scan3(ic, iff, iu, w1, w2, w3);
+      if (i < nt) {
+        tsum[3 * (t0 + i)] = carry_c + ic - c;
+        tsum[3 * (t0 + i) + 1] = carry_f + iff - f;
+        tsum[3 * (t0 + i) + 2] = carry_u + iu - u;
+      }
+      carry_c += w1[31];
+      carry_f += w2[31];
+      carry_u += w3[31];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      if (part == 0) {
+        a.counts[0] = carry_f;
+        a.counts[2] = carry_u;
+      } else {
+        a.counts[1] = carry_c;
+      }
     }
   }
-  if (t == 1023) a.counts[1] = s2[1023];
+}
+
+// Rescans each tile from its offset and writes: rows -> occurrence offsets,
+// distinct slots, row list, first backward unit and the unit list; prefixes
+// -> prefix slots and the prefix list.
+__global__ void __launch_bounds__(kScanThreads) ttm_tile_write_kernel(TtmArgs a, int ntr,
+                                                                     const int* tsum) {
+  __shared__ int w1[32], w2[32], w3[32];
+  const bool rows = (int)blockIdx.x < ntr;
+  const int tile = rows ? blockIdx.x : blockIdx.x - ntr;
+  const int base = tile * kScanTile;
+  const int n = min(kScanTile, (rows ? a.V : a.npair) - base);
+  int c, f, u;
+  tile_sums(a, rows, base, n, &c, &f, &u);
+  int ic = c, iff = f, iu = u;
+  block_scan3(ic, iff, iu, w1, w2, w3);
+  const int* off = tsum + 3 * blockIdx.x;
+  int ec = off[0] + ic - c, ef = off[1] + iff - f, eu = off[2] + iu - u;
+  const int lo = threadIdx.x * kScanPer, hi = min(lo + kScanPer, n);
+  for (int i = lo; i < hi; ++i) {
+    const int v = base + i;
+    if (rows) {
+      const int x = a.cnt[v];
+      a.off[v] = ec;
+      ec += x;
+      if (x > 0) {
+        a.upos[v] = ef;
+        a.ulist[ef] = v;
+        a.uoff[ef] = eu;
+        const int nch = (x + kChunk - 1) / kChunk;
+        for (int k = 0; k < nch; ++k) a.unit_u[eu + k] = ef;
+        eu += nch;
+        ++ef;
+      }
+    } else if (a.cnt_pair[v]) {
+      a.pos_pair[v] = ec;
+      a.plist[ec++] = v;
+    }
+  }
 }
 
 __global__ void ttm_fill_kernel(TtmArgs a, const int32_t* __restrict__ idx) {
@@ -152,65 +250,95 @@ __global__ void ttm_fill_kernel(TtmArgs a, const int32_t* __restrict__ idx) {
   }
 }
 
-// Pair products P[c][(j1, j2), e] = sum_b F_1[0, i1, j1, b] D_1[b] F_2[b, i2, j2, e]
-// for every used prefix p = i1 m2 + i2 (slot c); with zero_dp also dP[c] = 0.
-__global__ void ttm_pairs_kernel(TtmArgs a, int zero_dp) {
-  extern __shared__ float sm[];
-  const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2;
-  float* f1 = sm;             // [n1][r1], times D_1
-  float* f2 = f1 + n1 * r1;   // [r1][n2][r2]
-  const int Pn = a.counts[1];
-  const int nt = a.nA * r2;
-  for (int c = blockIdx.x; c < Pn; c += gridDim.x) {
-    const int p = a.plist[c];
-    const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
-    for (int e = threadIdx.x; e < n1 * r1; e += blockDim.x)
-      f1[e] = a.F1[i1 * n1 * r1 + e] * a.D1[e % r1];
-    const int w2 = n2 * r2;
-    for (int e = threadIdx.x; e < r1 * w2; e += blockDim.x) {
-      const int b = e / w2;
-      f2[e] = a.F2[(b * a.m2 + i2) * w2 + (e - b * w2)];
-    }
-    __syncthreads();
-    float* out = a.P + (size_t)c * nt;
-    for (int o = threadIdx.x; o < nt; o += blockDim.x) {
-      const int jA = o / r2, e = o - (o / r2) * r2;
-      const int j1 = jA / n2, j2 = jA - (jA / n2) * n2;
-      float acc = 0.f;
-      for (int b = 0; b < r1; ++b) acc = fmaf(f1[j1 * r1 + b], f2[(b * n2 + j2) * r2 + e], acc);
-      out[o] = acc;
-      if (zero_dp) a.dP[(size_t)c * nt + o] = 0.f;
-    }
-    __syncthreads();
+// Stages F_1[0, i1] (times D_1 when scale_d1) and F_2[:, i2] for prefix p,
+// and computes the pair product P[(j1, j2), e] = sum_b F_1[0, i1, j1, b] D_1[b]
+// F_2[b, i2, j2, e] into pt (times D_2[e] when scale_d2).  Ends synchronised.
+__device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, float* pt,
+                                 bool scale_d1, bool scale_d2) {
+  const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2, w2 = n2 * r2, nt = a.nA * r2;
+  const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
+  for (int e = threadIdx.x; e < n1 * r1; e += blockDim.x) f1[e] = a.F1[i1 * n1 * r1 + e];
+  for (int e = threadIdx.x; e < r1 * w2; e += blockDim.x) {
+    const int b = e / w2;
+    f2[e] = a.F2[(b * a.m2 + i2) * w2 + (e - b * w2)];
   }
+  __syncthreads();
+  // one thread per column (j2, e) of F_2's slice; up to 8 rows j1 at a time
+  // in registers, so each loaded F_2 value serves 8 products
+  for (int je = threadIdx.x; je < w2; je += blockDim.x) {
+    const int e = je % r2;
+    const float d2 = scale_d2 ? a.D2[e] : 1.f;
+    for (int j0 = 0; j0 < n1; j0 += 8) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int b = 0; b < r1; ++b) {
+        const float y = f2[b * w2 + je] * (scale_d1 ? a.D1[b] : 1.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (j0 + i < n1) acc[i] = fmaf(f1[(j0 + i) * r1 + b], y, acc[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (j0 + i < n1) pt[(j0 + i) * w2 + je] = acc[i] * d2;
+    }
+  }
+  __syncthreads();
 }
 
-// Distinct rows: row[(jA, j3)] = sum_e P[c][jA, e] D_2[e] F_3[e, i3, j3, 0].
-__global__ void ttm_rows_kernel(TtmArgs a) {
+// The used rows of prefix p (i3 with cnt[p m3 + i3] > 0) in increasing i3,
+// into list[0, *n), for i3 in [base, base + 256); ends synchronised.
+__device__ void used_rows(const TtmArgs& a, int p, int base, int* list, int* n) {
+  __shared__ int wc[8];
+  const int i3 = base + (int)threadIdx.x;
+  const bool use = threadIdx.x < 256 && i3 < a.m3 && a.cnt[p * a.m3 + i3] > 0;
+  const unsigned m = __ballot_sync(0xffffffffu, use);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0 && warp < 8) wc[warp] = __popc(m);
+  __syncthreads();
+  int before = 0, total = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) before += wc[w];
+    total += wc[w];
+  }
+  if (use) list[before + __popc(m & ((1u << lane) - 1u))] = i3;
+  if (threadIdx.x == 0) *n = total;
+  __syncthreads();
+}
+
+// Forward, one block of 256 threads per used prefix (slot c): its pair
+// product in shared memory, then its used rows, one warp per row:
+//   row[(jA, j3)] = sum_e P[jA, e] D_2[e] F_3[e, i3, j3, 0]  ->  rows[upos[v]].
+__global__ void __launch_bounds__(256) ttm_pair_rows_kernel(TtmArgs a) {
   extern __shared__ float sm[];
-  const int r2 = a.r2, n3 = a.n3, nt = a.nA * r2;
-  float* pt = sm;          // [nA][r2], times D_2
-  float* f3 = pt + nt;     // [r2][n3]
-  const int U = a.counts[0];
-  for (int u = blockIdx.x; u < U; u += gridDim.x) {
-    const int v = a.ulist[u];
-    const int pr = v / a.m3, i3 = v - (v / a.m3) * a.m3;
-    const int c = a.pos_pair[pr];
-    const float* P = a.P + (size_t)c * nt;
-    for (int o = threadIdx.x; o < nt; o += blockDim.x) pt[o] = P[o] * a.D2[o % r2];
-    for (int o = threadIdx.x; o < r2 * n3; o += blockDim.x) {
-      const int e = o / n3;
-      f3[o] = a.F3[(e * a.m3 + i3) * n3 + (o - e * n3)];
+  __shared__ int list[256];
+  __shared__ int nlist;
+  const int n3 = a.n3, r2 = a.r2, nt = a.nA * r2, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x;
+  if (c >= a.counts[1]) return;
+  float* f1 = sm;                           // [n1][r1]
+  float* f2 = f1 + a.n1 * a.r1;             // [r1][n2][r2]
+  float* pt = f2 + a.r1 * a.n2 * r2;        // [nA][r2], D_1 inside, times D_2
+  float* f3 = pt + nt + warp * r2 * n3;     // this warp's [r2][n3]
+  const int p = a.plist[c];
+  ttm_pair_product(a, p, f1, f2, pt, true, true);
+  for (int base = 0; base < a.m3; base += 256) {
+    used_rows(a, p, base, list, &nlist);
+    for (int k = warp; k < nlist; k += 8) {
+      const int i3 = list[k], v = p * a.m3 + i3;
+      for (int o = lane; o < r2 * n3; o += 32) {
+        const int e = o / n3;
+        f3[o] = a.F3[(e * a.m3 + i3) * n3 + (o - e * n3)];
+      }
+      __syncwarp();
+      float* row = a.rows + (size_t)a.upos[v] * a.Dm;
+      for (int j = lane; j < a.Dm; j += 32) {
+        const int jA = j / n3, j3 = j - (j / n3) * n3;
+        float acc = 0.f;
+        for (int e = 0; e < r2; ++e) acc = fmaf(pt[jA * r2 + e], f3[e * n3 + j3], acc);
+        row[j] = acc;
+      }
+      __syncwarp();
     }
-    __syncthreads();
-    float* row = a.rows + (size_t)u * a.Dm;
-    for (int j = threadIdx.x; j < a.Dm; j += blockDim.x) {
-      const int jA = j / n3, j3 = j - (j / n3) * n3;
-      float acc = 0.f;
-      for (int e = 0; e < r2; ++e) acc = fmaf(pt[jA * r2 + e], f3[e * n3 + j3], acc);
-      row[j] = acc;
-    }
-    __syncthreads();
+    __syncthreads();  // list is refilled next
   }
 }
 
@@ -241,132 +369,160 @@ __global__ void ttm_scatter_kernel(TtmArgs a, const int32_t* __restrict__ idx,
 }
 
 // Backward unit w: the sum of up to kChunk occurrence rows of dout for one
-// distinct row, into rows[w].
-__global__ void ttm_chunk_sum_kernel(TtmArgs a, const float* __restrict__ dout) {
-  const int C = a.counts[2];
-  for (int w = blockIdx.x; w < C; w += gridDim.x) {
-    const int u = a.unit_u[w];
-    const int k = w - a.uoff[u];
-    const int v = a.ulist[u];
-    const int o0 = a.off[v] + k * kChunk;
-    const int o1 = min(o0 + kChunk, a.off[v] + a.cnt[v]);
+// distinct row, into rows[w].  The occurrence list goes to shared memory
+// first so that all of a thread's loads are independent.
+__global__ void __launch_bounds__(256) ttm_chunk_sum_kernel(TtmArgs a,
+                                                            const float* __restrict__ dout) {
+  __shared__ int ob[kChunk];
+  const int w = blockIdx.x;
+  if (w >= a.counts[2]) return;
+  const int u = a.unit_u[w];
+  const int k = w - a.uoff[u];
+  const int v = a.ulist[u];
+  const int o0 = a.off[v] + k * kChunk;
+  const int n = min(kChunk, a.off[v] + a.cnt[v] - o0);
+  if ((int)threadIdx.x < n) ob[threadIdx.x] = a.occ[o0 + threadIdx.x];
+  __syncthreads();
+  if ((a.Dm & 3) == 0) {
+    const int q = a.Dm >> 2;
+    const float4* src = reinterpret_cast<const float4*>(dout);
+    float4* dst = reinterpret_cast<float4*>(a.rows) + (size_t)w * q;
+    for (int j = threadIdx.x; j < q; j += blockDim.x) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int o = 0; o < n; ++o) {
+        const float4 x = src[(size_t)ob[o] * q + j];
+        s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
+      }
+      dst[j] = s;
+    }
+  } else {
     float* dst = a.rows + (size_t)w * a.Dm;
     for (int j = threadIdx.x; j < a.Dm; j += blockDim.x) {
       float s = 0.f;
-      for (int o = o0; o < o1; ++o) s += dout[(size_t)a.occ[o] * a.Dm + j];
+#pragma unroll 8
+      for (int o = 0; o < n; ++o) s += dout[(size_t)ob[o] * a.Dm + j];
       dst[j] = s;
     }
   }
 }
 
-// Per distinct row: dR = sum of its chunk sums; then
-//   dF_3[e, i3, j3] += sum_jA P[c][jA, e] D_2[e] dR[jA, j3]
-//   dP[c][jA, e]    += sum_j3 dR[jA, j3] F_3[e, i3, j3]
-__global__ void ttm_row_grad_kernel(TtmArgs a, float* __restrict__ dF3) {
+// Backward, one block of 256 threads per used prefix (slot c).  Its used
+// rows go to one warp each: dR = the sum of the row's chunk sums,
+//   dF_3[e, i3, j3] += D_2[e] sum_jA P[jA, e] dR[jA, j3]   (P without D_2)
+//   dP[jA, e]       += sum_j3 dR[jA, j3] F_3[e, i3, j3]    (shared memory)
+// then back through P D_2 = F_1 D_1 F_2 D_2 for this prefix:
+//   dD_2[e] += sum_jA P[jA, e] dP[jA, e];  G = dP D_2
+//   dF_2[b, i2, j2, e] += D_1[b] sum_j1 F_1[i1, j1, b] G[(j1, j2), e]
+//   H[j1, b] = sum_{j2, e} G[(j1, j2), e] F_2[b, i2, j2, e]
+//   dF_1[0, i1, j1, b] += D_1[b] H[j1, b];  dD_1[b] += sum_j1 F_1[i1, j1, b] H[j1, b]
+// (dD entries of pruned ranks, D == 0, stay untouched).
+__global__ void __launch_bounds__(256) ttm_pair_backward_kernel(TtmArgs a, float* __restrict__ dF1,
+                                                                float* __restrict__ dF2,
+                                                                float* __restrict__ dF3,
+                                                                float* __restrict__ dD1,
+                                                                float* __restrict__ dD2) {
   extern __shared__ float sm[];
-  const int r2 = a.r2, n3 = a.n3, nt = a.nA * r2, Dm = a.Dm;
-  float* dR = sm;          // [Dm]
-  float* pt = dR + Dm;     // [nA][r2], times D_2
-  float* f3 = pt + nt;     // [r2][n3]
-  const int U = a.counts[0];
-  for (int u = blockIdx.x; u < U; u += gridDim.x) {
-    const int v = a.ulist[u];
-    const int pr = v / a.m3, i3 = v - (v / a.m3) * a.m3;
-    const int c = a.pos_pair[pr];
-    const int w0 = a.uoff[u], nch = (a.cnt[v] + kChunk - 1) / kChunk;
-    for (int j = threadIdx.x; j < Dm; j += blockDim.x) {
-      float s = 0.f;
-      for (int w = w0; w < w0 + nch; ++w) s += a.rows[(size_t)w * Dm + j];
-      dR[j] = s;
-    }
-    const float* P = a.P + (size_t)c * nt;
-    for (int o = threadIdx.x; o < nt; o += blockDim.x) pt[o] = P[o] * a.D2[o % r2];
-    for (int o = threadIdx.x; o < r2 * n3; o += blockDim.x) {
-      const int e = o / n3;
-      f3[o] = a.F3[(e * a.m3 + i3) * n3 + (o - e * n3)];
-    }
-    __syncthreads();
-    for (int o = threadIdx.x; o < r2 * n3; o += blockDim.x) {
-      const int e = o / n3, j3 = o - (o / n3) * n3;
-      float acc = 0.f;
-      for (int jA = 0; jA < a.nA; ++jA) acc = fmaf(pt[jA * r2 + e], dR[jA * n3 + j3], acc);
-      atomicAdd(dF3 + (e * a.m3 + i3) * n3 + j3, acc);
-    }
-    float* dP = a.dP + (size_t)c * nt;
-    for (int o = threadIdx.x; o < nt; o += blockDim.x) {
-      const int jA = o / r2, e = o - (o / r2) * r2;
-      float acc = 0.f;
-      for (int j3 = 0; j3 < n3; ++j3) acc = fmaf(dR[jA * n3 + j3], f3[e * n3 + j3], acc);
-      atomicAdd(dP + o, acc);
+  __shared__ int list[256];
+  __shared__ int nlist;
+  const int n1 = a.n1, n2 = a.n2, n3 = a.n3, r1 = a.r1, r2 = a.r2;
+  const int w2 = n2 * r2, nt = a.nA * r2, Dm = a.Dm;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x;
+  if (c >= a.counts[1]) return;
+  float* f1 = sm;                // [n1][r1] (without D_1)
+  float* f2 = f1 + n1 * r1;      // [r1][n2][r2]
+  float* pt = f2 + r1 * w2;      // [nA][r2] (D_1 inside, without D_2)
+  float* dP = pt + nt;           // [nA][r2]
+  float* H = dP + nt;            // [n1][r1]
+  float* dR = H + n1 * r1 + warp * (Dm + r2 * n3);   // this warp's [Dm]
+  float* f3 = dR + Dm;                               // this warp's [r2][n3]
+  const int p = a.plist[c];
+  const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
+  for (int o = threadIdx.x; o < nt; o += blockDim.x) dP[o] = 0.f;
+  ttm_pair_product(a, p, f1, f2, pt, true, false);
+  for (int base = 0; base < a.m3; base += 256) {
+    used_rows(a, p, base, list, &nlist);
+    for (int k = warp; k < nlist; k += 8) {
+      const int i3 = list[k], v = p * a.m3 + i3;
+      const int u = a.upos[v], w0 = a.uoff[u];
+      const int nch = (a.cnt[v] + kChunk - 1) / kChunk;
+      for (int j = lane; j < Dm; j += 32) {
+        float sacc = 0.f;
+        for (int w = w0; w < w0 + nch; ++w) sacc += a.rows[(size_t)w * Dm + j];
+        dR[j] = sacc;
+      }
+      for (int o = lane; o < r2 * n3; o += 32) {
+        const int e = o / n3;
+        f3[o] = a.F3[(e * a.m3 + i3) * n3 + (o - e * n3)];
+      }
+      __syncwarp();
+      for (int o = lane; o < r2 * n3; o += 32) {
+        const int e = o / n3, j3 = o - (o / n3) * n3;
+        float acc = 0.f;
+        for (int jA = 0; jA < a.nA; ++jA) acc = fmaf(pt[jA * r2 + e], dR[jA * n3 + j3], acc);
+        atomicAdd(dF3 + (e * a.m3 + i3) * n3 + j3, acc * a.D2[e]);
+      }
+      for (int o = lane; o < nt; o += 32) {
+        const int jA = o / r2, e = o - (o / r2) * r2;
+        float acc = 0.f;
+        for (int j3 = 0; j3 < n3; ++j3) acc = fmaf(dR[jA * n3 + j3], f3[e * n3 + j3], acc);
+        atomicAdd(dP + o, acc);  // shared memory: rows of this prefix in other warps
+      }
+      __syncwarp();
     }
     __syncthreads();
   }
-}
-
-// Per used prefix: back through P = F_1 D_1 F_2 and the D_2 scaling.
-__global__ void ttm_pair_grad_kernel(TtmArgs a, float* __restrict__ dF1, float* __restrict__ dF2,
-                                     float* __restrict__ dD1, float* __restrict__ dD2) {
-  extern __shared__ float sm[];
-  const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2, nt = a.nA * r2, w2 = n2 * r2;
-  float* f1 = sm;             // [n1][r1] (without D_1)
-  float* f2 = f1 + n1 * r1;   // [r1][n2][r2]
-  float* G = f2 + r1 * w2;    // [nA][r2] gradient w.r.t. P
-  float* H = G + nt;          // [n1][r1]
-  const int Pn = a.counts[1];
-  for (int c = blockIdx.x; c < Pn; c += gridDim.x) {
-    const int p = a.plist[c];
-    const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
-    for (int e = threadIdx.x; e < n1 * r1; e += blockDim.x) f1[e] = a.F1[i1 * n1 * r1 + e];
-    for (int e = threadIdx.x; e < r1 * w2; e += blockDim.x) {
-      const int b = e / w2;
-      f2[e] = a.F2[(b * a.m2 + i2) * w2 + (e - b * w2)];
+  for (int e = threadIdx.x; e < r2; e += blockDim.x) {
+    if (a.D2[e] == 0.f) continue;
+    float acc = 0.f;
+    for (int jA = 0; jA < a.nA; ++jA) acc = fmaf(pt[jA * r2 + e], dP[jA * r2 + e], acc);
+    atomicAdd(dD2 + e, acc);
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < nt; o += blockDim.x) dP[o] *= a.D2[o % r2];  // G
+  __syncthreads();
+  // dF_2: one thread per column (j2, e), G's column in registers (8 rows j1
+  // at a time)
+  for (int je = threadIdx.x; je < w2; je += blockDim.x) {
+    float* dst = dF2 + i2 * w2 + je;
+    for (int j0 = 0; j0 < n1; j0 += 8) {
+      float g[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = j0 + i < n1 ? dP[(j0 + i) * w2 + je] : 0.f;
+      for (int b = 0; b < r1; ++b) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (j0 + i < n1) acc = fmaf(f1[(j0 + i) * r1 + b], g[i], acc);
+        atomicAdd(dst + b * a.m2 * w2, acc * a.D1[b]);
+      }
     }
-    const float* dP = a.dP + (size_t)c * nt;
-    for (int o = threadIdx.x; o < nt; o += blockDim.x) G[o] = dP[o] * a.D2[o % r2];
-    __syncthreads();
-    // dD_2[e] += sum_jA P[jA, e] dP[jA, e]
-    const float* P = a.P + (size_t)c * nt;
-    for (int e = threadIdx.x; e < r2; e += blockDim.x) {
-      if (a.D2[e] == 0.f) continue;
-      float acc = 0.f;
-      for (int jA = 0; jA < a.nA; ++jA) acc = fmaf(P[jA * r2 + e], dP[jA * r2 + e], acc);
-      atomicAdd(dD2 + e, acc);
-    }
-    // dF_2[b, i2, j2, e] += sum_j1 F_1[i1, j1, b] D_1[b] G[(j1, j2), e]
-    for (int o = threadIdx.x; o < r1 * w2; o += blockDim.x) {
-      const int b = o / w2, je = o - (o / w2) * w2;
-      const float db = a.D1[b];
-      float acc = 0.f;
-      for (int j1 = 0; j1 < n1; ++j1) acc = fmaf(f1[j1 * r1 + b], G[j1 * w2 + je], acc);
-      atomicAdd(dF2 + (b * a.m2 + i2) * w2 + je, acc * db);
-    }
-    // H[j1, b] = sum_{j2, e} G[(j1, j2), e] F_2[b, i2, j2, e]
-    for (int o = threadIdx.x; o < n1 * r1; o += blockDim.x) {
-      const int j1 = o / r1, b = o - (o / r1) * r1;
-      float acc = 0.f;
-      for (int je = 0; je < w2; ++je) acc = fmaf(G[j1 * w2 + je], f2[b * w2 + je], acc);
-      H[o] = acc;
-    }
-    __syncthreads();
-    // dF_1[0, i1, j1, b] += D_1[b] H[j1, b];  dD_1[b] += sum_j1 F_1[i1, j1, b] H[j1, b]
-    for (int o = threadIdx.x; o < n1 * r1; o += blockDim.x)
-      atomicAdd(dF1 + i1 * n1 * r1 + o, a.D1[o % r1] * H[o]);
-    for (int b = threadIdx.x; b < r1; b += blockDim.x) {
-      if (a.D1[b] == 0.f) continue;
-      float acc = 0.f;
-      for (int j1 = 0; j1 < n1; ++j1) acc = fmaf(f1[j1 * r1 + b], H[j1 * r1 + b], acc);
-      atomicAdd(dD1 + b, acc);
-    }
-    __syncthreads();
+  }
+  for (int o = threadIdx.x; o < n1 * r1; o += blockDim.x) {
+    const int j1 = o / r1, b = o - (o / r1) * r1;
+    float acc = 0.f;
+    for (int je = 0; je < w2; ++je) acc = fmaf(dP[j1 * w2 + je], f2[b * w2 + je], acc);
+    H[o] = acc;
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < n1 * r1; o += blockDim.x)
+    atomicAdd(dF1 + i1 * n1 * r1 + o, a.D1[o % r1] * H[o]);
+  for (int b = threadIdx.x; b < r1; b += blockDim.x) {
+    if (a.D1[b] == 0.f) continue;
+    float acc = 0.f;
+    for (int j1 = 0; j1 < n1; ++j1) acc = fmaf(f1[j1 * r1 + b], H[j1 * r1 + b], acc);
+    atomicAdd(dD1 + b, acc);
   }
 }
 
 // ---- host side ---------------------------------------------------------------
 
 struct TtmWs {
-  size_t cnt, cursor, cnt_pair, off, upos, ulist, uoff, unit_u, pos_pair, plist, counts, occ, P,
-      dP, rows, end;
+  size_t cnt, cursor, cnt_pair, off, upos, ulist, uoff, unit_u, pos_pair, plist, counts, occ,
+      tsum, rows, end;
   int64_t ucap, pcap, unit_cap;
+  int ntr, ntp;  // scan tiles over the rows and over the prefixes
   size_t zero_bytes;  // cnt .. cnt_pair, zeroed per call
 };
 
@@ -377,7 +533,6 @@ TtmWs ttm_layout(const TtmPlan& P, int64_t B) {
   w.ucap = std::min<int64_t>(B, P.V);
   w.pcap = std::min<int64_t>(B, P.npair);
   w.unit_cap = w.ucap + B / kChunk + 1;
-  const int64_t nt = (int64_t)P.n[0] * P.n[1] * P.r[2];
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t r = o;
@@ -402,8 +557,9 @@ TtmWs ttm_layout(const TtmPlan& P, int64_t B) {
   w.pos_pair = take(4 * (size_t)P.npair);
   w.plist = take(4 * (size_t)w.pcap);
   w.occ = take(4 * (size_t)B);
-  w.P = take(4 * (size_t)(w.pcap * nt));
-  w.dP = take(4 * (size_t)(w.pcap * nt));
+  w.ntr = (int)((P.V + kScanTile - 1) / kScanTile);
+  w.ntp = (int)((P.npair + kScanTile - 1) / kScanTile);
+  w.tsum = take(4 * 3 * (size_t)(w.ntr + w.ntp));
   w.rows = take(4 * (size_t)(std::max(w.ucap, w.unit_cap) * P.Dm));
   w.end = o;
   return w;
@@ -419,12 +575,25 @@ struct Units {
   float* sink = nullptr;
 };
 
+// Device addresses of the unit core and the sink, looked up once per device
+// (the first call on a device should come before any stream capture).
 bool unit_ptrs(Units* u) {
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_ttm_one) != cudaSuccess) return false;
-  u->one = static_cast<float*>(p);
-  if (cudaGetSymbolAddress(&p, g_ttm_sink) != cudaSuccess) return false;
-  u->sink = static_cast<float*>(p);
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static Units cache[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev].one) {
+    void* p = nullptr;
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ttm_one) != cudaSuccess ||
+        cudaGetSymbolAddress(&q, g_ttm_sink) != cudaSuccess)
+      return false;
+    cache[dev].one = static_cast<float*>(p);
+    cache[dev].sink = static_cast<float*>(q);
+  }
+  *u = cache[dev];
   return true;
 }
 
@@ -456,8 +625,6 @@ TtmArgs make_args(const TtmPlan& P, int64_t B, const float* params, void* ws, co
   a.plist = at<int>(ws, w.plist);
   a.counts = at<int>(ws, w.counts);
   a.occ = at<int>(ws, w.occ);
-  a.P = at<float>(ws, w.P);
-  a.dP = at<float>(ws, w.dP);
   a.rows = at<float>(ws, w.rows);
   return a;
 }
@@ -473,29 +640,24 @@ int sm_count() {
   return n;
 }
 
-size_t pairs_smem(const TtmPlan& P) {
-  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * P.n[1] * P.r[2]);
+// Dynamic shared memory (bytes) of the per-prefix kernels.
+size_t pair_rows_smem(const TtmPlan& P) {
+  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * P.n[1] * P.r[2] + P.n[0] * P.n[1] * P.r[2] +
+                      8 * P.r[2] * P.n[2]);
 }
-size_t rows_smem(const TtmPlan& P) {
-  return 4 * (size_t)(P.n[0] * P.n[1] * P.r[2] + P.r[2] * P.n[2]);
-}
-size_t row_grad_smem(const TtmPlan& P) { return rows_smem(P) + 4 * (size_t)P.Dm; }
-size_t pair_grad_smem(const TtmPlan& P) {
-  return pairs_smem(P) + 4 * (size_t)(P.n[0] * P.n[1] * P.r[2] + P.n[0] * P.r[1]);
+size_t pair_backward_smem(const TtmPlan& P) {
+  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * P.n[1] * P.r[2] +
+                      2 * P.n[0] * P.n[1] * P.r[2] + P.n[0] * P.r[1] +
+                      8 * (P.Dm + P.r[2] * P.n[2]));
 }
 
 cudaError_t set_attrs() {
   static cudaError_t e = [] {
     const int big = kMaxSmemFloats * 4;
-    cudaError_t r = cudaFuncSetAttribute(ttm_pairs_kernel,
+    cudaError_t r = cudaFuncSetAttribute(ttm_pair_rows_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(ttm_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(ttm_row_grad_kernel,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, big);
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(ttm_pair_grad_kernel,
+      r = cudaFuncSetAttribute(ttm_pair_backward_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     return r;
   }();
@@ -507,17 +669,18 @@ cudaError_t set_attrs() {
     if ((call) != cudaSuccess) return TT_ERR_CUDA;     \
   } while (0)
 
-// count, scan (and, for the backward, fill), pair products
-tt_status ttm_prepare(const TtmPlan& P, int64_t B, const int32_t* idx, const TtmArgs& a,
-                      const TtmWs& w, void* ws, bool backward, cudaStream_t st) {
-  const int g = 2 * sm_count();
+// count and scan (and, for the backward, the occurrence lists)
+tt_status ttm_prepare(int64_t B, const int32_t* idx, const TtmArgs& a, const TtmWs& w, void* ws,
+                      bool backward, cudaStream_t st) {
   TTM_CUDA(cudaMemsetAsync(at<char>(ws, w.cnt), 0, w.zero_bytes, st));
   int gb = (int)std::min<int64_t>((B + 255) / 256, 4 * sm_count());
+  int* tsum = at<int>(ws, w.tsum);
   ttm_count_kernel<<<gb, 256, 0, st>>>(a, idx);
-  ttm_scan_kernel<<<1, 1024, 0, st>>>(a);
+  ttm_tile_sum_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
+  ttm_tile_scan_kernel<<<1, 1024, 0, st>>>(a, w.ntr, w.ntp, tsum);
+  ttm_tile_write_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
   if (backward) ttm_fill_kernel<<<gb, 256, 0, st>>>(a, idx);
-  ttm_pairs_kernel<<<g, 256, pairs_smem(P), st>>>(a, backward ? 1 : 0);
-  count_launches(backward ? 4 : 3);
+  count_launches(backward ? 5 : 4);
   TTM_CUDA(cudaGetLastError());
   return TT_OK;
 }
@@ -578,8 +741,8 @@ tt_status tt_ttm_plan(const tt_ttm_desc* desc, tt_plan_t** out) {
   P.n_floats = off;
   // shared-memory tiles of the kernels
   if ((int64_t)P.n[0] * P.n[1] * P.r[2] > 8192 || (int64_t)P.r[1] * P.n[1] * P.r[2] > 16384 ||
-      (int64_t)P.r[2] * P.n[2] > 8192 || pair_grad_smem(P) > 4 * (size_t)kMaxSmemFloats ||
-      row_grad_smem(P) > 4 * (size_t)kMaxSmemFloats)
+      (int64_t)P.r[2] * P.n[2] > 8192 || pair_rows_smem(P) > 4 * (size_t)kMaxSmemFloats ||
+      pair_backward_smem(P) > 4 * (size_t)kMaxSmemFloats)
     return TT_ERR_UNSUPPORTED;
   tt_plan_s* p = new (std::nothrow) tt_plan_s();
   if (!p) return TT_ERR_INVALID_ARG;
@@ -601,10 +764,9 @@ tt_status tt_ttm_lookup(const tt_plan_t* plan, int64_t B, const int32_t* idx, co
   if (set_attrs() != cudaSuccess || !unit_ptrs(&un)) return TT_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const TtmArgs a = make_args(P, B, params, ws, w, un);
-  tt_status s = ttm_prepare(P, B, idx, a, w, ws, false, st);
+  tt_status s = ttm_prepare(B, idx, a, w, ws, false, st);
   if (s != TT_OK) return s;
-  const int g = 2 * sm_count();
-  ttm_rows_kernel<<<g, 256, rows_smem(P), st>>>(a);
+  ttm_pair_rows_kernel<<<(unsigned)w.pcap, 256, pair_rows_smem(P), st>>>(a);
   ttm_scatter_kernel<<<4 * sm_count(), 256, 0, st>>>(a, idx, out);
   count_launches(2);
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
@@ -626,18 +788,17 @@ tt_status tt_ttm_lookup_backward(const tt_plan_t* plan, int64_t B, const int32_t
   Units un;
   if (set_attrs() != cudaSuccess || !unit_ptrs(&un)) return TT_ERR_CUDA;
   const TtmArgs a = make_args(P, B, params, ws, w, un);
-  tt_status s = ttm_prepare(P, B, idx, a, w, ws, true, st);
+  tt_status s = ttm_prepare(B, idx, a, w, ws, true, st);
   if (s != TT_OK) return s;
-  const int g = 2 * sm_count();
   float* dF1 = dparams + P.core_off[0];
   float* dF2 = dparams + P.core_off[1];
   float* dF3 = P.d == 3 ? dparams + P.core_off[2] : un.sink;
   float* dD1 = dparams + P.diag_off[0];
   float* dD2 = P.d == 3 ? dparams + P.diag_off[1] : un.sink + 32;
-  ttm_chunk_sum_kernel<<<4 * sm_count(), 256, 0, st>>>(a, dout);
-  ttm_row_grad_kernel<<<g, 256, row_grad_smem(P), st>>>(a, dF3);
-  ttm_pair_grad_kernel<<<g, 256, pair_grad_smem(P), st>>>(a, dF1, dF2, dD1, dD2);
-  count_launches(3);
+  ttm_chunk_sum_kernel<<<(unsigned)w.unit_cap, 256, 0, st>>>(a, dout);
+  ttm_pair_backward_kernel<<<(unsigned)w.pcap, 256, pair_backward_smem(P), st>>>(a, dF1, dF2, dF3,
+                                                                               dD1, dD2);
+  count_launches(2);
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
