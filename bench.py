@@ -29,7 +29,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "TT-linear fwd+bwd tokens/s on 1 GB300 and % of roofline; CPU-oracle speedup"
 DEFAULT_WORKLOAD = "tt768_bf16"
-ELEM = {"bf16": 2, "f32": 4}
+ELEM = {"bf16": 2, "f32": 4, "e4m3": 1}   # bytes of an x / dy element
+OUT_ELEM = {"bf16": 2, "f32": 4, "e4m3": 2}   # bytes of a y / dx element (E4M3 in, bf16 out)
 
 
 def parse():
@@ -66,11 +67,12 @@ def algorithmic(w, T):
     """FLOP and bytes of one fwd+bwd step, and bytes per token pass of each kernel.
 
     FLOP = 6 T r' (N + M) per layer (the merged contraction order: x A, z' B,
-    dy B^T, z'^T dy, dz A^T, x^T dz); bytes = e T (3N + 2M) per layer (x read
-    by both passes, y written, dy read, dx written).
+    dy B^T, z'^T dy, dz A^T, x^T dz); bytes = T (2N ei + M ei + M eo + N eo)
+    per layer (x read by both passes, dy read, y and dx written), ei / eo the
+    bytes of an input / output element (bf16: 2 / 2, E4M3 in, bf16 out: 1 / 2).
     """
-    import numpy as np
-    e = ELEM[w.act]
+    ei = ELEM[w.act]
+    eo = OUT_ELEM[w.act]
     flop = 0
     byt = 0
     fwd_b = 0
@@ -82,14 +84,12 @@ def algorithmic(w, T):
         flop += 6 * T * r * (L.N + L.M)
     if w.ffn:
         up, dn = w.layers
-        byt = e * T * (3 * up.N + 2 * dn.M)
-        fwd_b = e * T * (up.N + dn.M)
-        bwd_b = e * T * (2 * up.N + dn.M)
+        N, M = up.N, dn.M
     else:
-        L = w.layers[0]
-        byt = e * T * (3 * L.N + 2 * L.M)
-        fwd_b = e * T * (L.N + L.M)
-        bwd_b = e * T * (2 * L.N + L.M)
+        N, M = w.layers[0].N, w.layers[0].M
+    byt = T * (2 * N * ei + M * ei + M * eo + N * eo)
+    fwd_b = T * (N * ei + M * eo)
+    bwd_b = T * (N * ei + M * ei + N * eo)
     return {"flop": int(flop), "bytes": int(byt), "fwd_bytes": int(fwd_b),
             "bwd_bytes": int(bwd_b)}
 
@@ -316,8 +316,14 @@ def run_ours(args, w):
     if not os.path.exists(ttc.LIB_PATH):
         _build.build()
     T = args.tokens or w.tokens
-    dt = torch.bfloat16 if w.act == "bf16" else torch.float32
-    e = ELEM[w.act]
+    dt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.uint8}[w.act]
+    dto = torch.bfloat16 if w.act == "e4m3" else dt   # y and dx
+    ei, eo = ELEM[w.act], OUT_ELEM[w.act]
+
+    def to_act(a):   # float32 tensor -> the layer's input encoding
+        if w.act == "e4m3":
+            return a.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        return a.to(dt)
 
     # ---- setup: parameters and rotating activation sets larger than 2x L2
     inp0 = synth.draw(w, seed=rank, tokens=T)
@@ -336,20 +342,24 @@ def run_ours(args, w):
         n_par = [params[0].numel()]
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    set_bytes = e * T * (2 * N + 2 * M)
+    set_bytes = T * (N + M) * (ei + eo)
     nsets = max(2, -(-2 * l2 // set_bytes) + 1)
     sets = []
     for i in range(nsets):
         g = torch.Generator(device=dev)
         g.manual_seed(1000 * rank + i)
-        x = torch.randn((T, N), generator=g, device=dev, dtype=torch.float32).to(dt)
-        dy = torch.randn((T, M), generator=g, device=dev, dtype=torch.float32).to(dt)
-        y = torch.empty((T, M), device=dev, dtype=dt)
-        dx = torch.empty((T, N), device=dev, dtype=dt)
+        x = to_act(torch.randn((T, N), generator=g, device=dev, dtype=torch.float32))
+        dy = to_act(torch.randn((T, M), generator=g, device=dev, dtype=torch.float32))
+        y = torch.empty((T, M), device=dev, dtype=dto)
+        dx = torch.empty((T, N), device=dev, dtype=dto)
         sets.append((x, dy, y, dx))
     # the first set holds the seeded synthetic inputs of the workload
-    sets[0][0].copy_(torch.from_numpy(inp0.x).to(dev).to(dt))
-    sets[0][1].copy_(torch.from_numpy(inp0.dy).to(dev).to(dt))
+    if w.act == "e4m3":
+        sets[0][0].copy_(torch.from_numpy(synth.e4m3_bytes(inp0.x)).to(dev))
+        sets[0][1].copy_(torch.from_numpy(synth.e4m3_bytes(inp0.dy)).to(dev))
+    else:
+        sets[0][0].copy_(torch.from_numpy(inp0.x).to(dev).to(dt))
+        sets[0][1].copy_(torch.from_numpy(inp0.dy).to(dev).to(dt))
     dparams = [torch.empty(n, device=dev, dtype=torch.float32) for n in n_par]
     ws = mod.workspace(T, dev)
     stream = torch.cuda.current_stream(dev)
@@ -529,8 +539,8 @@ def run_ours(args, w):
         x, dy, y, dx = sets[0]
         hx = torch.empty(x.shape, dtype=dt, pin_memory=True)
         hdy = torch.empty(dy.shape, dtype=dt, pin_memory=True)
-        hy = torch.empty(y.shape, dtype=dt, pin_memory=True)
-        hdx = torch.empty(dx.shape, dtype=dt, pin_memory=True)
+        hy = torch.empty(y.shape, dtype=dto, pin_memory=True)
+        hdx = torch.empty(dx.shape, dtype=dto, pin_memory=True)
         hdp = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in n_par]
         hx.copy_(x)
         hdy.copy_(dy)
@@ -557,8 +567,8 @@ def run_ours(args, w):
         barrier()
         ems = all_reduce_scalar(a0.elapsed_time(a1) / Ke, "max", dev)
         e2e = {"value": whole_job_rate(T, world, ems), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(hx.numel() * e + hdy.numel() * e),
-               "d2h_bytes_per_step": int(hy.numel() * e + hdx.numel() * e + 4 * sum(n_par)),
+               "h2d_bytes_per_step": int(hx.numel() * ei + hdy.numel() * ei),
+               "d2h_bytes_per_step": int(hy.numel() * eo + hdx.numel() * eo + 4 * sum(n_par)),
                "ms_per_step": ems, "steps": Ke}
 
     # ---- oracle on the host cores (rank 0, N = 1 only)

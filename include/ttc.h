@@ -62,7 +62,13 @@ typedef enum tt_status {
   TT_ERR_DEVICE = 6       /* a device-side consistency check failed (device status) */
 } tt_status;
 
-typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1 } tt_dtype;
+/* Activation types.  TT_DT_E4M3: x and dy are one-byte OCP FP8 E4M3
+ * ("e4m3fn": bias 7, 3 mantissa bits, largest finite 448, NaN 0x7F/0xFF)
+ * codes, y and dx are bf16; the cores, diagonals and gradients stay fp32 and
+ * every product accumulates in fp32.  This is the FP8/FP32 mixed precision of
+ * the CoMERA poster digest (its FP8-mix speedup table and the mixed-precision
+ * DLRM results), read as FP8 storage of the activations. */
+typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1, TT_DT_E4M3 = 2 } tt_dtype;
 
 /* flags of tt_desc */
 #define TT_ACCUMULATE 1u /* backward adds into dparams instead of overwriting */
@@ -80,7 +86,7 @@ typedef struct tt_desc {
   int in_modes[TT_MAX_D];       /* n_1..n_d, each >= 1 */
   int out_modes[TT_MAX_D];      /* m_1..m_d, each >= 1 */
   int ranks[2 * TT_MAX_D + 1];  /* r_0..r_2d; r_0 = r_2d = 1, others >= 1 */
-  int act;                      /* tt_dtype of x, y, dx, dy */
+  int act;                      /* tt_dtype of x, y, dx, dy (E4M3: y, dx bf16) */
   unsigned flags;               /* TT_ACCUMULATE | TT_REUSE_MERGE */
 } tt_desc;
 
@@ -98,11 +104,14 @@ tt_status tt_default_ranks(int d, const int* in_modes, const int* out_modes, int
  * TT_ERR_INVALID_ARG for a malformed desc (a rank outside 1..4096 among
  * them); TT_ERR_UNSUPPORTED for N or M above 2^20 or a merged intermediate
  * (the packed parameters, a prefix product of the cores, the merged A or B)
- * of 2^31 elements or more. */
+ * of 2^31 elements or more; TT_ERR_UNSUPPORTED as well for an E4M3 layer
+ * outside the fused tensor-core kernels' shapes (N, M multiples of 16 and at
+ * least 128, middle rank r_d <= 64): E4M3 has no other path. */
 tt_status tt_plan(const tt_desc* desc, tt_plan_t** out);
 
 /* FFN pair y = TT_down(GELU(TT_up(x))) with the exact erf GELU; up's output
- * width must equal down's input width and both must use the same act type. */
+ * width must equal down's input width and both must use the same act type
+ * (F32 or BF16; E4M3 gives TT_ERR_UNSUPPORTED). */
 tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out);
 
 void tt_destroy(tt_plan_t* plan);

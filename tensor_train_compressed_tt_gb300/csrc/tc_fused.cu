@@ -20,6 +20,13 @@
 // [token][64 elements] tile is K-major for the token-side products and
 // MN-major for the weight-side ones).
 //
+// FP8 activations: with E4M3 x and dy (one byte an element) the same kernels
+// run with four more warps.  TMA brings each 128-token x 128-column E4M3 tile
+// into the second half of a stage's activation area; the converter warps
+// widen it in place to the two bf16 boxes the MMAs read (E4M3 values are
+// exact in bf16), so the tensor-core work and everything downstream is the
+// bf16 path's, and only the activation bytes read from HBM halve.
+//
 // Every mbarrier wait is bounded (global timer); on expiry the CTA records
 // TT_ERR_TIMEOUT in the per-device status word, raises a shared abort flag so
 // the other roles stop, waits (bounded) for its own copies and MMAs, frees its
@@ -27,6 +34,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cstdlib>
 #include <mutex>
@@ -58,6 +67,8 @@ constexpr int NSTAGE_B = 3;
 constexpr int NEPI = 8;              // epilogue warps
 constexpr int STG = 4096;            // one epilogue staging box: 32 rows x 128 bytes
 constexpr int NTHREADS = (2 + NEPI) * 32;
+constexpr int NCONV = 4;             // E4M3 -> bf16 converter warps (FP8 kernels)
+constexpr int NTHREADS_F8 = (2 + NEPI + NCONV) * 32;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 // TMEM columns
@@ -320,6 +331,47 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Two E4M3 codes (low byte first) -> two bf16 values (low half first).
+// Every E4M3 value is exact in f16, f32 and bf16, so no rounding happens.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pack_bf16(f.x, f.y);
+}
+
+// Widen the 128-row x 128-column E4M3 tile that TMA wrote (128-byte swizzle)
+// at st + BOX into the two [128][64] bf16 boxes at st and st + BOX.  Converter
+// warp cw owns rows 32cw .. 32cw + 31: the bf16 rows it writes into the second
+// box occupy exactly the bytes of the raw rows it read, so the warp reads all
+// of its raw bytes into registers, syncs, and only then writes.
+__device__ __forceinline__ void widen_e4m3_tile(uint8_t* st, int cw, int lane) {
+  const uint8_t* raw = st + BOX + cw * 32 * 128;
+  uint4 u[8];
+#pragma unroll
+  for (int n = 0; n < 8; ++n)
+    u[n] = *reinterpret_cast<const uint4*>(raw + (n * 32 + lane) * 16);
+  __syncwarp();
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+    const int unit = n * 32 + lane;      // physical 16-byte unit of the warp's rows
+    const int r = cw * 32 + (unit >> 3);
+    const int j = (unit & 7) ^ (r & 7);  // columns 16j .. 16j + 15
+    uint8_t* dst = st + (j >> 2) * BOX + r * 128;
+    const int k0 = 2 * (j & 3);          // their first bf16 16-byte chunk in that box
+    uint4 o0, o1;
+    o0.x = e4m3x2_to_bf16x2(u[n].x);
+    o0.y = e4m3x2_to_bf16x2(u[n].x >> 16);
+    o0.z = e4m3x2_to_bf16x2(u[n].y);
+    o0.w = e4m3x2_to_bf16x2(u[n].y >> 16);
+    o1.x = e4m3x2_to_bf16x2(u[n].z);
+    o1.y = e4m3x2_to_bf16x2(u[n].z >> 16);
+    o1.z = e4m3x2_to_bf16x2(u[n].w);
+    o1.w = e4m3x2_to_bf16x2(u[n].w >> 16);
+    *reinterpret_cast<uint4*>(dst + ((k0 ^ (r & 7)) << 4)) = o0;
+    *reinterpret_cast<uint4*>(dst + (((k0 + 1) ^ (r & 7)) << 4)) = o1;
+  }
+}
+
 struct FwdArgs {
   int64_t T;
   int N, M, nN, nM, ntiles;
@@ -344,6 +396,7 @@ struct SmemCommon {
   uint64_t full[4], empty[4];
   uint64_t z_full, z_empty, zp_full, zp_empty, dzp_full, dzp_empty, dz_full, dz_empty;
   uint64_t w_full[2], w_empty[2], x_full[2], x_empty[2];
+  uint64_t conv[4];  // FP8 kernels: stage s converted (and its operand loaded)
   uint64_t fin;
   uint32_t tmem_base;
   int abort_flag;
@@ -370,8 +423,10 @@ __device__ void tmem_free(uint32_t base) {
 
 // ==========================================================================
 // forward: y = ((x At^T) diag(Dc)) Bt^T per 128-token tile
+// (F8: x in E4M3, widened in shared memory by the converter warps)
 // ==========================================================================
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <bool F8>
+__global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     tt_fwd_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_at,
                   const __grid_constant__ CUtensorMap tm_bt,
@@ -398,6 +453,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&S.x_full[b], 1);
       mbar_init(&S.x_empty[b], NEPI);
     }
+    for (int s = 0; s < NSTAGE_F; ++s) mbar_init(&S.conv[s], NCONV);
     mbar_init(&S.fin, 1);
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -428,9 +484,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 1)) { ok = false; break; }
           uint8_t* st = stages + s * STAGE;
           if (c < p.nN) {
-            mbar_expect_tx(&S.full[s], STAGE);
-            tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
-            tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
+            if (F8) {  // one E4M3 box of 128 columns into the second bf16 box's bytes
+              mbar_expect_tx(&S.full[s], 2 * BOX);
+              tma_load(st + BOX, &tm_x, &S.full[s], c * CH, tok0);
+            } else {
+              mbar_expect_tx(&S.full[s], STAGE);
+              tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
+              tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
+            }
             tma_load(st + OPND, &tm_at, &S.full[s], c * CH, 0);
             tma_load(st + OPND + BOX / 2, &tm_at, &S.full[s], c * CH + 64, 0);
           } else {
@@ -449,6 +510,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t id_z = idesc(128, 64, 0, 0);
       const uint32_t id_y = idesc(128, 128, 0, 0);
       const uint32_t zp_addr = su32(zp_tile);
+      uint64_t* ready = F8 ? S.conv : S.full;  // a stage the MMAs may read
       int it = 0, yc = 0, tl = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
@@ -456,7 +518,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         for (int c = 0; c < p.nN; ++c, ++it) {
           const int s = it % NSTAGE_F;
-          if (!wait_bar(&S.full[s], (it / NSTAGE_F) & 1, abort_flag, 3)) { ok = false; break; }
+          if (!wait_bar(&ready[s], (it / NSTAGE_F) & 1, abort_flag, 3)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
@@ -477,7 +539,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int yb = yc & 1;
           if (!wait_bar(&S.x_empty[yb], ((yc >> 1) & 1) ^ 1, abort_flag, 5)) { ok = false; break; }
           if (c < 3) TL_STAMP(0, 13 + c);  // y buffer free
-          if (!wait_bar(&S.full[s], (it / NSTAGE_F) & 1, abort_flag, 6)) { ok = false; break; }
+          if (!wait_bar(&ready[s], (it / NSTAGE_F) & 1, abort_flag, 6)) { ok = false; break; }
           if (c < 3) TL_STAMP(0, 10 + c);  // Bt chunk in shared memory
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
@@ -494,6 +556,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       mma_commit(&S.fin);
       drain_bar(&S.fin, 0);
+    }
+  } else if (F8 && warp >= 2 + NEPI) {
+    // ---------------- converters: every chunk in the producer's order; x
+    // chunks are widened, operand-only chunks just pass through
+    const int cw = warp - 2 - NEPI;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
+      for (int c = 0; c < p.nN + p.nM; ++c, ++it) {
+        const int s = it % NSTAGE_F;
+        if (!warp_wait(&S.full[s], (it / NSTAGE_F) & 1, abort_flag, 40)) { ok = false; break; }
+        if (c < p.nN) {
+          widen_e4m3_tile(stages + s * STAGE, cw, lane);
+          fence_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(&S.conv[s]);
+      }
     }
   } else {
     // ---------------- epilogue: 8 warps, thread = (token row, column half)
@@ -563,8 +643,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 //   B  dz' = dy Bm^T ; dB^T += dy^T z'    (dy streamed, 128 outputs a chunk)
 //   C  dx  = dz Anr^T ; dA += x^T dz      (x streamed again)
 // with z' = z diag(Dc), dz = dz' diag(Dc), dDc += sum_t z * dz'.
+// (F8: x and dy in E4M3, widened in shared memory by the converter warps)
 // ==========================================================================
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <bool F8>
+__global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     tt_bwd_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_dy,
                   const __grid_constant__ CUtensorMap tm_at,
@@ -605,6 +687,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&S.x_full[b], 1);
       mbar_init(&S.x_empty[b], NEPI);
     }
+    for (int s = 0; s < NSTAGE_B; ++s) mbar_init(&S.conv[s], NCONV);
     mbar_init(&S.fin, 1);
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -637,23 +720,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t ph = (it / NSTAGE_B) & 1;
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 11)) { ok = false; break; }
           uint8_t* st = stages + s * STAGE;
-          mbar_expect_tx(&S.full[s], STAGE);
+          mbar_expect_tx(&S.full[s], F8 ? 2 * BOX : STAGE);
+          // activation tile: E4M3 as one box into the second bf16 box's bytes
+          const bool is_dy = c >= p.nN && c < p.nN + p.nM;
+          const CUtensorMap* act = is_dy ? &tm_dy : &tm_x;
+          const int col = (c < p.nN ? c : is_dy ? c - p.nN : c - p.nN - p.nM) * CH;
+          if (F8) {
+            tma_load(st + BOX, act, &S.full[s], col, tok0);
+          } else {
+            tma_load(st, act, &S.full[s], col, tok0);
+            tma_load(st + BOX, act, &S.full[s], col + 64, tok0);
+          }
           if (c < p.nN) {  // A
-            tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
-            tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
-            tma_load(st + OPND, &tm_at, &S.full[s], c * CH, 0);
-            tma_load(st + OPND + BOX / 2, &tm_at, &S.full[s], c * CH + 64, 0);
-          } else if (c < p.nN + p.nM) {  // B
-            const int o = (c - p.nN) * CH;
-            tma_load(st, &tm_dy, &S.full[s], o, tok0);
-            tma_load(st + BOX, &tm_dy, &S.full[s], o + 64, tok0);
-            tma_load(st + OPND, &tm_bm, &S.full[s], o, 0);
-            tma_load(st + OPND + BOX / 2, &tm_bm, &S.full[s], o + 64, 0);
+            tma_load(st + OPND, &tm_at, &S.full[s], col, 0);
+            tma_load(st + OPND + BOX / 2, &tm_at, &S.full[s], col + 64, 0);
+          } else if (is_dy) {  // B
+            tma_load(st + OPND, &tm_bm, &S.full[s], col, 0);
+            tma_load(st + OPND + BOX / 2, &tm_bm, &S.full[s], col + 64, 0);
           } else {  // C
-            const int f = (c - p.nN - p.nM) * CH;
-            tma_load(st, &tm_x, &S.full[s], f, tok0);
-            tma_load(st + BOX, &tm_x, &S.full[s], f + 64, tok0);
-            tma_load(st + OPND, &tm_anr, &S.full[s], 0, f);
+            tma_load(st + OPND, &tm_anr, &S.full[s], 0, col);
           }
           last_parity[s] = (int)ph;
         }
@@ -669,6 +754,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t id_x = idesc(128, 128, 0, 0);    // token x feature, K-major
       const uint32_t zp_addr = su32(zp_tile);
       const uint32_t dz_addr = su32(dz_tile);
+      uint64_t* ready = F8 ? S.conv : S.full;  // a stage the MMAs may read
       int it = 0, wc = 0, xc = 0, tl = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
@@ -677,7 +763,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         for (int c = 0; c < p.nN; ++c, ++it) {
           const int s = it % NSTAGE_B;
-          if (!wait_bar(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 13)) { ok = false; break; }
+          if (!wait_bar(&ready[s], (it / NSTAGE_B) & 1, abort_flag, 13)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
@@ -696,7 +782,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         for (int c = 0; c < p.nM; ++c, ++it, ++wc) {
           const int s = it % NSTAGE_B;
-          if (!wait_bar(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 15)) { ok = false; break; }
+          if (!wait_bar(&ready[s], (it / NSTAGE_B) & 1, abort_flag, 15)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
@@ -728,7 +814,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
         for (int c = 0; c < p.nN; ++c, ++it, ++xc, ++wc) {
           const int s = it % NSTAGE_B;
-          if (!wait_bar(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 19)) { ok = false; break; }
+          if (!wait_bar(&ready[s], (it / NSTAGE_B) & 1, abort_flag, 19)) { ok = false; break; }
           const int xb = xc & 1;
           if (!wait_bar(&S.x_empty[xb], ((xc >> 1) & 1) ^ 1, abort_flag, 20)) { ok = false; break; }
           tc_fence_after();
@@ -753,6 +839,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       mma_commit(&S.fin);
       drain_bar(&S.fin, 0);
+    }
+  } else if (F8 && warp >= 2 + NEPI) {
+    // ---------------- converters: every chunk (x, dy, x) in the producer's order
+    const int cw = warp - 2 - NEPI;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
+      for (int c = 0; c < nchunks; ++c, ++it) {
+        const int s = it % NSTAGE_B;
+        if (!warp_wait(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 41)) { ok = false; break; }
+        widen_e4m3_tile(stages + s * STAGE, cw, lane);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.conv[s]);
+      }
     }
   } else {
     // ---------------- epilogue
@@ -1050,18 +1151,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D tensor (outer x inner, row-major) of bf16 or f32, box
-// (box_outer x box_inner), 128-byte swizzle, zero fill outside the tensor.
+enum MapType { kMapBF16, kMapF32, kMapU8 };
+
+// 2-D tensor (outer x inner, row-major) of bf16, f32 or bytes (E4M3 codes),
+// box (box_outer x box_inner), 128-byte swizzle, zero fill outside the tensor.
 bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-              uint32_t box_outer, bool f32 = false) {
+              uint32_t box_outer, MapType type = kMapBF16) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const uint64_t esz = f32 ? 4 : 2;
+  const uint64_t esz = type == kMapF32 ? 4 : type == kMapU8 ? 1 : 2;
+  const CUtensorMapDataType dt = type == kMapF32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : type == kMapU8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * esz};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  CUresult r = fn(m, dt, 2,
                   const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1088,11 +1194,13 @@ cudaError_t set_smem_attrs() {
   static cudaError_t err = cudaErrorUnknown;
   static std::once_flag once;
   std::call_once(once, [] {
-    err = cudaFuncSetAttribute(tt_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kSmemFwd);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(tt_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBwd);
+    const std::pair<const void*, size_t> k[4] = {
+        {(const void*)tt_fwd_kernel<false>, kSmemFwd}, {(const void*)tt_fwd_kernel<true>, kSmemFwd},
+        {(const void*)tt_bwd_kernel<false>, kSmemBwd}, {(const void*)tt_bwd_kernel<true>, kSmemBwd}};
+    err = cudaSuccess;
+    for (int i = 0; i < 4 && err == cudaSuccess; ++i)
+      err = cudaFuncSetAttribute(k[i].first, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)k[i].second);
   });
   return err;
 }
@@ -1147,6 +1255,10 @@ bool tc_supported(const LayerPlan& L) {
          L.N <= (1 << 20) && L.M <= (1 << 20);
 }
 
+bool tc_f8_supported(const LayerPlan& L) {
+  return tc_supported(L) && L.N % 16 == 0 && L.M % 16 == 0;
+}
+
 size_t tc_operand_bytes(const LayerPlan& L) {
   return tc_supported(L) ? tc_layout(L).total : 256;
 }
@@ -1167,13 +1279,15 @@ TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t off) {
 }
 
 tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws, size_t off,
-                     cudaStream_t st) {
+                     bool f8, cudaStream_t st) {
   if (T <= 0) return TT_OK;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
+  if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
   CUtensorMap mx, mat, mbt, my;
-  if (!make_map(&mx, x, L.N, T, 64, TILE) ||
+  const bool mx_ok = f8 ? make_map(&mx, x, L.N, T, CH, TILE, kMapU8) : make_map(&mx, x, L.N, T, 64, TILE);
+  if (!mx_ok ||
       !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
       !make_map(&mbt, at<void>(ws, off + t.Bt), RP, L.M, 64, CH) ||
       !make_map(&my, y, L.M, T, 64, 32))
@@ -1188,14 +1302,17 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   a.Dc = at<float>(ws, off + t.Dc);
   a.y = static_cast<__nv_bfloat16*>(y);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
-  cudaError_t e = launch_ex(tt_fwd_kernel, grid, NTHREADS, kSmemFwd, st, false, mx, mat, mbt, my, a);
+  cudaError_t e =
+      f8 ? launch_ex(tt_fwd_kernel<true>, grid, NTHREADS_F8, kSmemFwd, st, false, mx, mat, mbt, my, a)
+         : launch_ex(tt_fwd_kernel<false>, grid, NTHREADS, kSmemFwd, st, false, mx, mat, mbt, my, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
-                      void* ws, size_t off, float* zero, size_t zero_n, cudaStream_t st) {
+                      void* ws, size_t off, float* zero, size_t zero_n, bool f8, cudaStream_t st) {
   if (zero_n > 0x7FFFFFFF) return TT_ERR_UNSUPPORTED;
+  if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
   if (T <= 0) {
     if (zero_n && cudaMemsetAsync(zero, 0, zero_n * sizeof(float), st) != cudaSuccess)
       return TT_ERR_CUDA;
@@ -1205,13 +1322,16 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
   CUtensorMap mx, mdy, mat, mbm, manr, mdx, mdac, mdbc;
-  if (!make_map(&mx, x, L.N, T, 64, TILE) || !make_map(&mdy, dy, L.M, T, 64, TILE) ||
+  const bool act_ok = f8 ? make_map(&mx, x, L.N, T, CH, TILE, kMapU8) &&
+                               make_map(&mdy, dy, L.M, T, CH, TILE, kMapU8)
+                         : make_map(&mx, x, L.N, T, 64, TILE) && make_map(&mdy, dy, L.M, T, 64, TILE);
+  if (!act_ok ||
       !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
       !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
       !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH) ||
       !make_map(&mdx, dx, L.N, T, 64, 32) ||
-      !make_map(&mdac, at<void>(ws, off + t.dAc), RP, L.N, 32, 32, true) ||
-      !make_map(&mdbc, at<void>(ws, off + t.dBc), RP, L.M, 32, 32, true))
+      !make_map(&mdac, at<void>(ws, off + t.dAc), RP, L.N, 32, 32, kMapF32) ||
+      !make_map(&mdbc, at<void>(ws, off + t.dBc), RP, L.M, 32, 32, kMapF32))
     return TT_ERR_CUDA;
   BwdArgs a;
   a.T = T;
@@ -1229,8 +1349,10 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.zero = zero;
   a.zero_n = (int)zero_n;
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
-  cudaError_t e = launch_ex(tt_bwd_kernel, grid, NTHREADS, kSmemBwd, st, false, mx, mdy, mat, mbm,
-                            manr, mdx, mdac, mdbc, a);
+  cudaError_t e = f8 ? launch_ex(tt_bwd_kernel<true>, grid, NTHREADS_F8, kSmemBwd, st, false, mx,
+                                 mdy, mat, mbm, manr, mdx, mdac, mdbc, a)
+                      : launch_ex(tt_bwd_kernel<false>, grid, NTHREADS, kSmemBwd, st, false, mx, mdy,
+                                  mat, mbm, manr, mdx, mdac, mdbc, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }

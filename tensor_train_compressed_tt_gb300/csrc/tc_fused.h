@@ -22,19 +22,26 @@ TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t ws_off);
 // True when the bf16 fused kernels handle this layer shape.
 bool tc_supported(const LayerPlan& L);
 
+// True when the E4M3-activation variants handle it too (row strides of x and
+// dy in bytes must be multiples of 16 for TMA).
+bool tc_f8_supported(const LayerPlan& L);
+
 // Bytes of workspace the fused path needs for its packed operands.
 size_t tc_operand_bytes(const LayerPlan& L);
 
 // y = ((x A) diag(D_d)) B for T tokens; the packed operands (written by the
-// merge engine's pack phase) are in the workspace at ws_off.
+// merge engine's pack phase) are in the workspace at ws_off.  x is bf16, or
+// E4M3 codes when f8; y is bf16.
 tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws,
-                     size_t ws_off, cudaStream_t st);
+                     size_t ws_off, bool f8, cudaStream_t st);
 
 // dx for T tokens and the token sums dAc, dBc, dDc (zeroed by the pack
 // phase); the merge engine's unpack phase turns these into dA, dB, dD_d.
 // zero[0, zero_n) is set to 0 on the way (scratch that the merge backward
-// then adds into), also when T == 0.
+// then adds into), also when T == 0.  x and dy are bf16, or E4M3 codes when
+// f8; dx is bf16.
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
-                      void* ws, size_t ws_off, float* zero, size_t zero_n, cudaStream_t st);
+                      void* ws, size_t ws_off, float* zero, size_t zero_n, bool f8,
+                      cudaStream_t st);
 
 }  // namespace ttc

@@ -24,7 +24,8 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
   if (!desc || !L) return TT_ERR_INVALID_ARG;
   const int d = desc->d;
   if (d < 1 || d > TT_MAX_D) return TT_ERR_INVALID_ARG;
-  if (desc->act != TT_DT_F32 && desc->act != TT_DT_BF16) return TT_ERR_INVALID_ARG;
+  if (desc->act != TT_DT_F32 && desc->act != TT_DT_BF16 && desc->act != TT_DT_E4M3)
+    return TT_ERR_INVALID_ARG;
   if (desc->flags & ~(TT_ACCUMULATE | TT_REUSE_MERGE)) return TT_ERR_INVALID_ARG;
   LayerPlan p;
   p.d = d;
@@ -115,7 +116,7 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   w->q = take(2 * (TT_MAX_D - 1) * w->qstride * sizeof(float));
   for (int i = 0; i < 4; ++i) w->part[i] = take(pmax * sizeof(float));
   w->part_cap = pmax;
-  const bool tc = !simt_tokens && tc_supported(L) && L.act == TT_DT_BF16;
+  const bool tc = !simt_tokens && tc_supported(L) && L.act != TT_DT_F32;
   w->z = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->dzp = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->tc = take(tc_operand_bytes(L));
@@ -461,7 +462,12 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
 }
 
 // ---- one layer ---------------------------------------------------------------
+// Output dtype of a layer: bf16 for E4M3 inputs, else the input dtype.
+int out_dtype(int act) { return act == TT_DT_E4M3 ? TT_DT_BF16 : act; }
+
+// The fused tensor-core kernels take bf16 or E4M3 inputs and write bf16.
 bool use_tc(const LayerPlan& L, int tx, int ty) {
+  if (tx == TT_DT_E4M3) return ty == TT_DT_BF16 && tc_f8_supported(L);
   return tx == TT_DT_BF16 && ty == TT_DT_BF16 && L.act == TT_DT_BF16 && tc_supported(L);
 }
 
@@ -469,6 +475,7 @@ tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, co
                         void* y, int ty, void* ws, const WsLayout& w, cudaStream_t st) {
   const float* P[kMaxK];
   const bool tc = use_tc(L, tx, ty);
+  if (!tc && tx == TT_DT_E4M3) return TT_ERR_UNSUPPORTED;  // E4M3 runs on the fused kernels only
   const bool reuse = (L.flags & TT_REUSE_MERGE) != 0;
   prof_begin(kPhMerge, st);
   tt_status s = run_merge_forward(L, params, ws, w, P, tc, reuse, st);
@@ -476,7 +483,7 @@ tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, co
   if (s != TT_OK) return s;
   prof_begin(kPhFwd, st);
   if (tc) {
-    s = tc_forward(L, T, x, y, ws, w.tc, st);
+    s = tc_forward(L, T, x, y, ws, w.tc, tx == TT_DT_E4M3, st);
   } else {
     const float* A = P[L.d - 1];   // N x rd
     const float* B = P[L.K - 1];   // rd x M
@@ -563,7 +570,8 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
                          int tdy, const float* params, void* dx, int tdx, float* dparams,
                          bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
   const float* P[kMaxK];
-  const bool tc = use_tc(L, tx, tdy) && tdx == TT_DT_BF16;
+  const bool tc = use_tc(L, tx, tdx) && tdy == tx;
+  if (!tc && (tx == TT_DT_E4M3 || tdy == TT_DT_E4M3)) return TT_ERR_UNSUPPORTED;
   const bool reuse = (L.flags & TT_REUSE_MERGE) != 0;
   tt_status s = TT_OK;
   if (reuse) {
@@ -577,7 +585,7 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   prof_begin(kPhBwd, st);
   const size_t nz = dq0_zero_floats(L, w);
   if (tc) {
-    s = tc_backward(L, T, x, dy, dx, ws, w.tc, dq_buf(ws, w, 0, 0), nz, st);
+    s = tc_backward(L, T, x, dy, dx, ws, w.tc, dq_buf(ws, w, 0, 0), nz, tx == TT_DT_E4M3, st);
   } else {
     if (nz) TT_CUDA(cudaMemsetAsync(dq_buf(ws, w, 0, 0), 0, nz * sizeof(float), st));
     s = simt_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
@@ -636,6 +644,7 @@ tt_status tt_plan(const tt_desc* desc, tt_plan_t** out) {
   LayerPlan L;
   tt_status s = build_layer(desc, &L);
   if (s != TT_OK) return s;
+  if (L.act == TT_DT_E4M3 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
   tt_plan_s* p = new (std::nothrow) tt_plan_s();
   if (!p) return TT_ERR_INVALID_ARG;
   p->kind = 0;
@@ -653,6 +662,7 @@ tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out) {
   s = build_layer(down, &b);
   if (s != TT_OK) return s;
   if (a.M != b.N || a.act != b.act || a.flags != b.flags) return TT_ERR_INVALID_ARG;
+  if (a.act == TT_DT_E4M3) return TT_ERR_UNSUPPORTED;  // the FFN pair runs in bf16 or f32
   // the two layers share workspace regions, so a merge cannot be kept
   // from the forward to the backward: TT_REUSE_MERGE has no effect here
   a.flags &= ~TT_REUSE_MERGE;
@@ -723,7 +733,8 @@ tt_status tt_forward(const tt_plan_t* plan, int64_t T, const void* x, const floa
   size_t need = layer_layout(L, T, 256, &w);
   tt_status s = check_ws(ws, ws_bytes, need);
   if (s != TT_OK) return s;
-  return layer_forward(L, T, x, L.act, params, y, L.act, ws, w, static_cast<cudaStream_t>(stream));
+  return layer_forward(L, T, x, L.act, params, y, out_dtype(L.act), ws, w,
+                       static_cast<cudaStream_t>(stream));
 }
 
 tt_status tt_backward(const tt_plan_t* plan, int64_t T, const void* x, const void* dy,
@@ -741,7 +752,8 @@ tt_status tt_backward(const tt_plan_t* plan, int64_t T, const void* x, const voi
   if (s != TT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool acc = (L.flags & TT_ACCUMULATE) != 0;
-  return layer_backward(L, T, x, L.act, dy, L.act, params, dx, L.act, dparams, acc, ws, w, st);
+  return layer_backward(L, T, x, L.act, dy, L.act, params, dx, out_dtype(L.act), dparams, acc, ws,
+                        w, st);
 }
 
 tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,

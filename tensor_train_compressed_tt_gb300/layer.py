@@ -13,6 +13,11 @@ import torch
 from . import ttc
 
 _DT = {torch.float32: ttc.TT_DT_F32, torch.bfloat16: ttc.TT_DT_BF16}
+# E4M3 activations: x / dy hold one-byte codes (a float8_e4m3fn tensor, or
+# uint8 holding the same bytes); y / dx come back in bf16.
+if hasattr(torch, "float8_e4m3fn"):
+    _DT[torch.float8_e4m3fn] = ttc.TT_DT_E4M3
+_DT[torch.uint8] = ttc.TT_DT_E4M3
 
 
 def _stream(stream: Optional[torch.cuda.Stream]) -> int:
@@ -34,6 +39,8 @@ class TTLinear:
         self.out_modes = tuple(out_modes)
         self.ranks = tuple(ranks)
         self.dtype = dtype
+        # dtype of y and dx
+        self.out_dtype = torch.bfloat16 if _DT[dtype] == ttc.TT_DT_E4M3 else dtype
         flags = (ttc.TT_ACCUMULATE if accumulate else 0) | \
             (ttc.TT_REUSE_MERGE if reuse_merge else 0)
         self.desc = ttc.make_desc(in_modes, out_modes, ranks, _DT[dtype], flags)
@@ -56,7 +63,7 @@ class TTLinear:
                 ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         T = x.shape[0]
         if y is None:
-            y = torch.empty((T, self.M), dtype=self.dtype, device=x.device)
+            y = torch.empty((T, self.M), dtype=self.out_dtype, device=x.device)
         if ws is None:
             ws = self.workspace(T, x.device)
         ttc.check(ttc.tt_forward(self.plan, T, _ptr(x), _ptr(params), _ptr(y), _ptr(ws),
@@ -68,7 +75,7 @@ class TTLinear:
                  ws: Optional[torch.Tensor] = None, stream=None):
         T = x.shape[0]
         if dx is None:
-            dx = torch.empty((T, self.N), dtype=self.dtype, device=x.device)
+            dx = torch.empty((T, self.N), dtype=self.out_dtype, device=x.device)
         if dparams is None:
             dparams = torch.empty(self.n_params, dtype=torch.float32, device=x.device)
         if ws is None:

@@ -16,7 +16,9 @@ Draw order for one layer: cores G_1..G_2d, diagonals D_1..D_{2d-1}, x, dy,
 all from one numpy PCG64 stream seeded with ``seed``.  "N(0, s)" means
 standard deviation s.  Activations drawn for a bf16 workload are rounded to
 the nearest bf16 value (round to nearest even) once, here, so both sides read
-identical numbers.
+identical numbers.  Activations of an e4m3 workload are rounded the same way
+to the nearest OCP FP8 E4M3 ("e4m3fn") value, saturating at +-448; the device
+receives the one-byte codes of those values.
 """
 
 from __future__ import annotations
@@ -65,7 +67,7 @@ class Workload:
     name: str
     layers: Tuple[LayerShape, ...]   # one layer, or (up, down) for the FFN pair
     tokens: int
-    act: str                         # "f32" or "bf16"
+    act: str                         # "f32", "bf16" or "e4m3" (x, dy; y and dx bf16)
     core_std: float
     x_std: float
     dy_std: float
@@ -102,6 +104,14 @@ WORKLOADS = {
         "pruned_half",
         description="TT linear 768x768, ranks 30, half of every D_k exactly zero, "
                     "16384 tokens, bf16"),
+    "tt768_e4m3": Workload(
+        "tt768_e4m3", (_L768_768,), 16384, "e4m3", 0.05, 1.0, 1.0, "uniform",
+        description="TT linear 768x768, modes (12,8,8)x(8,8,12), ranks 30, "
+                    "D~U(0.5,1.5), 16384 tokens, e4m3 x/dy, bf16 y/dx"),
+    "tt1024_4096_e4m3": Workload(
+        "tt1024_4096_e4m3", (_L1024_4096,), 32768, "e4m3", 0.03, 1.0, 1.0, "uniform",
+        description="TT linear 1024->4096, modes (8,8,16)x(16,16,16), ranks 64, "
+                    "32768 tokens, e4m3 x/dy, bf16 y/dx"),
     "tt1024_4096_bf16": Workload(
         "tt1024_4096_bf16", (_L1024_4096,), 32768, "bf16", 0.03, 1.0, 1.0, "uniform",
         description="TT linear 1024->4096, modes (8,8,16)x(16,16,16), ranks 64, "
@@ -119,6 +129,50 @@ def round_bf16(a: np.ndarray) -> np.ndarray:
     u = a.view(np.uint32).astype(np.uint64)
     u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
     return u.astype(np.uint32).view(np.float32)
+
+
+E4M3_MAX = 448.0
+
+
+def round_e4m3(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (ties to even), saturating at +-448.
+
+    E4M3 ("e4m3fn"): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+    bits, no infinities; the largest finite value is 1.75 * 2^8 = 448, the
+    smallest normal 2^-6, the subnormal step 2^-9.  Returns float32 values
+    exactly representable in E4M3.
+    """
+    v = np.asarray(a, dtype=np.float64)
+    m = np.minimum(np.abs(v), E4M3_MAX)
+    _, ex = np.frexp(np.maximum(m, 2.0 ** -6))
+    step = np.ldexp(1.0, ex - 1 - 3)          # 2^(e - 3), e = floor(log2 m) >= -6
+    r = np.round(m / step) * step               # numpy rounds halves to even
+    return (np.sign(v) * r).astype(np.float32)
+
+
+def e4m3_bytes(a: np.ndarray) -> np.ndarray:
+    """One-byte E4M3 codes of values that are already E4M3-representable."""
+    v = np.asarray(a, dtype=np.float64)
+    sign = np.signbit(v).astype(np.uint16) << 7
+    m = np.abs(v)
+    _, ex = np.frexp(np.maximum(m, 2.0 ** -6))
+    e = ex - 1
+    normal = m >= 2.0 ** -6
+    field = np.where(normal, (e + 7) * 8 + (m / np.ldexp(1.0, e) - 1.0) * 8, m / 2.0 ** -9)
+    code = np.rint(field).astype(np.uint16)
+    assert np.all(np.abs(field - code) == 0), "value not representable in E4M3"
+    return (sign | code).astype(np.uint8)
+
+
+def e4m3_values(codes: np.ndarray) -> np.ndarray:
+    """float32 values of one-byte E4M3 codes (NaN codes 0x7F / 0xFF included)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    s = np.where(c & 0x80, -1.0, 1.0)
+    E = (c >> 3) & 0xF
+    mt = c & 7
+    mag = np.where(E == 0, mt * 2.0 ** -9, np.ldexp(1.0 + mt / 8.0, E - 7))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return (s * mag).astype(np.float32)
 
 
 @dataclasses.dataclass
@@ -163,6 +217,9 @@ def draw(w: Workload, seed: int = 0, tokens: Optional[int] = None) -> WorkloadIn
     if w.act == "bf16":
         x = round_bf16(x)
         dy = round_bf16(dy)
+    elif w.act == "e4m3":
+        x = round_e4m3(x)
+        dy = round_e4m3(dy)
     return WorkloadInputs(layers, x, dy)
 
 

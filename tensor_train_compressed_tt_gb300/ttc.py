@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libttc.so")
 TT_MAX_D = 4
 TT_DT_F32 = 0
 TT_DT_BF16 = 1
+TT_DT_E4M3 = 2   # x, dy as one-byte FP8 E4M3 codes; y, dx bf16
 TT_ACCUMULATE = 1
 TT_REUSE_MERGE = 2
 

@@ -10,11 +10,15 @@ from oracle import tt_oracle as O
 from tensor_train_compressed_tt_gb300 import synth
 from tensor_train_compressed_tt_gb300.layer import TTFFN, TTLinear
 
-TOL = {"f32": 1e-4, "bf16": 2e-2}
-TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+# E4M3 inputs: the products run on bf16 tiles (the E4M3 values widened
+# exactly) with bf16 merged operands and bf16 outputs, so the bf16 bound holds.
+TOL = {"f32": 1e-4, "bf16": 2e-2, "e4m3": 2e-2}
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
 
 
 def to_dev(a: np.ndarray, act: str) -> torch.Tensor:
+    if act == "e4m3":   # one-byte codes of values that are E4M3-representable
+        return torch.from_numpy(synth.e4m3_bytes(a)).cuda()
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(TORCH_DT[act])
 
 

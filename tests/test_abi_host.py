@@ -81,6 +81,31 @@ def test_ffn_layout_and_validation(lib):
         ttc.tt_ffn_plan(_desc(up), _desc(dn, act=ttc.TT_DT_F32))
 
 
+def test_e4m3_plans(lib):
+    """E4M3 runs on the fused tensor-core kernels only: shapes they do not
+    take, and FFN pairs, are refused at plan time; the workspace is the bf16
+    plan's (no f32 token scratch)."""
+    shape = synth.WORKLOADS["tt768_e4m3"].layers[0]
+    plan = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_E4M3))
+    bf = ttc.tt_plan(_desc(shape))
+    for T in (0, 1, 16384):
+        assert ttc.tt_workspace_size(plan, T) == ttc.tt_workspace_size(bf, T)
+    bad = [synth.LayerShape((12, 8, 9), (8, 8, 12), (1, 12, 30, 30, 30, 12, 1)),  # N = 864 ok
+           synth.LayerShape((8, 17, 1), (8, 8, 12), (1, 8, 30, 30, 30, 12, 1)),   # N = 136
+           synth.LayerShape((4, 4, 4), (4, 4, 4), (1, 4, 8, 8, 8, 4, 1)),           # N < 128
+           synth.LayerShape((16, 16), (16, 16), (1, 16, 72, 16, 1))]                # r_d > 64
+    ttc.tt_plan(_desc(bad[0], act=ttc.TT_DT_E4M3))
+    for b in bad[1:]:
+        with pytest.raises(ttc.TTError) as e:
+            ttc.tt_plan(_desc(b, act=ttc.TT_DT_E4M3))
+        assert e.value.code == 2
+        ttc.tt_plan(_desc(b))   # the bf16 plan of the same shape is fine
+    up, dn = synth.WORKLOADS["ffn768_3072_bf16"].layers
+    with pytest.raises(ttc.TTError) as e:
+        ttc.tt_ffn_plan(_desc(up, act=ttc.TT_DT_E4M3), _desc(dn, act=ttc.TT_DT_E4M3))
+    assert e.value.code == 2
+
+
 @pytest.mark.parametrize("mutate", [
     lambda d: setattr(d, "d", 0),
     lambda d: setattr(d, "d", 5),

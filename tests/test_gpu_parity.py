@@ -1,7 +1,7 @@
 """GPU parity: libttc (through the C ABI) against the fp64 oracle.
 
 Tolerances (norm-wise relative error per output tensor): 1e-4 for f32
-activations, 2e-2 for bf16 activations with f32 accumulation; tensors whose
+activations, 2e-2 for bf16 or E4M3 activations with f32 accumulation; tensors whose
 reference is exactly zero (pruned slices, removed layers) must be exactly 0.
 """
 
@@ -24,7 +24,8 @@ def _built():
     _build.build()
 
 
-from parity_util import TOL, compare, gpu_ffn, gpu_layer, oracle_ffn, oracle_layer  # noqa: E402
+from parity_util import (TOL, TORCH_DT, compare, gpu_ffn, gpu_layer, oracle_ffn,  # noqa: E402
+                          oracle_layer, to_dev)
 
 
 def _run(name, tokens=None, seed=0):
@@ -159,7 +160,8 @@ def test_full_size_identities_tt1024_4096():
     assert O.rel_err(out["dx"][rows], sub["dx"]) <= TOL[w.act]
 
 
-@pytest.mark.parametrize("name", ["tt768_bf16", "pruned768_3072_bf16", "tiny64_f32"])
+@pytest.mark.parametrize("name", ["tt768_bf16", "pruned768_3072_bf16", "tiny64_f32",
+                                  "tt768_e4m3"])
 def test_reuse_merge_matches_default(name):
     """TT_REUSE_MERGE: backward after forward on the same workspace, twice."""
     import torch as th
@@ -167,10 +169,10 @@ def test_reuse_merge_matches_default(name):
     w = synth.WORKLOADS[name]
     inp = synth.draw(w, seed=3, tokens=min(w.tokens, 700))
     s = w.layers[0]
-    dt = th.bfloat16 if w.act == "bf16" else th.float32
+    dt = TORCH_DT[w.act]
     params = th.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
-    x = th.from_numpy(inp.x).cuda().to(dt)
-    dy = th.from_numpy(inp.dy).cuda().to(dt)
+    x = to_dev(inp.x, w.act)
+    dy = to_dev(inp.dy, w.act)
     ref = TTLinear(s.in_modes, s.out_modes, s.ranks, dt)
     y0 = ref.forward(x, params)
     dx0, g0 = ref.backward(x, dy, params)
@@ -201,3 +203,73 @@ def test_internal_rank_above_64_uses_generic_merge():
             x, dy = synth.round_bf16(x), synth.round_bf16(dy)
         compare(gpu_layer(shape, act, li, x, dy), oracle_layer(shape, li, x, dy), TOL[act],
                 f"{shape}")
+
+
+# ---- E4M3 activations ------------------------------------------------------
+
+@pytest.mark.parametrize("T", [1, 7, 300, 16384])
+def test_tt768_e4m3(T):
+    _run("tt768_e4m3", tokens=T)
+
+
+def test_tt1024_4096_e4m3():
+    _run("tt1024_4096_e4m3", tokens=4096)
+
+
+@pytest.mark.parametrize("name,T", [("tt768_e4m3", 1000), ("tt1024_4096_e4m3", 777)])
+def test_e4m3_equals_bf16_kernels_on_the_same_values(name, T):
+    """E4M3 values are exact in bf16, so the E4M3 kernels, which widen the tile
+    in shared memory, must give the bf16 kernels' y and dx bit for bit on the
+    same values (dparams: equal up to the order of the atomic token sums)."""
+    import torch as th
+    from tensor_train_compressed_tt_gb300.layer import TTLinear
+    w = synth.WORKLOADS[name]
+    inp = synth.draw(w, seed=5, tokens=T)
+    s = w.layers[0]
+    params = th.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
+    outs = []
+    for act in ("e4m3", "bf16"):
+        lay = TTLinear(s.in_modes, s.out_modes, s.ranks, TORCH_DT[act])
+        x, dy = to_dev(inp.x, act), to_dev(inp.dy, act)
+        y = lay.forward(x, params)
+        dx, g = lay.backward(x, dy, params)
+        th.cuda.synchronize()
+        outs.append((y, dx, g))
+    (y8, dx8, g8), (yb, dxb, gb) = outs
+    assert y8.dtype == th.bfloat16 and dx8.dtype == th.bfloat16
+    assert th.equal(y8, yb)
+    assert th.equal(dx8, dxb)
+    assert O.rel_err(g8.cpu().numpy(), gb.cpu().numpy()) <= 1e-5
+
+
+def test_full_size_e4m3_tt1024_4096():
+    """The benchmarked E4M3 configuration at its full 32768 tokens: the
+    <x,dx> = <G_k,dG_k> = <D_k,dD_k> = <dy,y> identities, and sampled rows of
+    y and dx against the oracle one token at a time."""
+    w = synth.WORKLOADS["tt1024_4096_e4m3"]
+    inp = synth.draw(w, seed=0)
+    shape = w.layers[0]
+    out = gpu_layer(shape, w.act, inp.layers[0], inp.x, inp.dy)
+    ref = float(np.sum(out["y"].astype(np.float64) * inp.dy))
+    scale = float(np.linalg.norm(out["y"])) * float(np.linalg.norm(inp.dy))
+    assert abs(float(np.sum(inp.x.astype(np.float64) * out["dx"])) - ref) <= 2e-2 * scale
+    for c, g in zip(inp.layers[0].cores, out["dcores"]):
+        assert abs(float(np.sum(c.astype(np.float64) * g)) - ref) <= 2e-2 * scale
+    for e, g in zip(inp.layers[0].diags, out["ddiags"]):
+        assert abs(float(np.sum(e.astype(np.float64) * g)) - ref) <= 2e-2 * scale
+    rows = np.random.default_rng(1).choice(inp.x.shape[0], 64, replace=False)
+    sub = oracle_layer(shape, inp.layers[0], inp.x[rows], inp.dy[rows])
+    assert O.rel_err(out["y"][rows], sub["y"]) <= TOL[w.act]
+    assert O.rel_err(out["dx"][rows], sub["dx"]) <= TOL[w.act]
+
+
+def test_tt768_e4m3_pruned():
+    """E4M3 inputs with half of every D_k exactly zero (compacted middle rank)."""
+    w = synth.WORKLOADS["tt768_e4m3"]
+    import dataclasses
+    wp = dataclasses.replace(w, diag="pruned_half")
+    inp = synth.draw(wp, seed=2, tokens=2000)
+    shape = wp.layers[0]
+    out = gpu_layer(shape, wp.act, inp.layers[0], inp.x, inp.dy)
+    ref = oracle_layer(shape, inp.layers[0], inp.x, inp.dy)
+    compare(out, ref, TOL["e4m3"], "tt768 e4m3 pruned")
