@@ -47,6 +47,8 @@ def parse():
                    help="launch every step from the host instead of replaying a CUDA graph")
     p.add_argument("--no-reuse", action="store_true",
                    help="re-merge the cores in the backward instead of reusing the forward's")
+    p.add_argument("--no-reuse-z", action="store_true",
+                   help="recompute z' = x A diag(D) in the backward instead of keeping the forward's")
     p.add_argument("--target-seconds", type=float, default=3.0,
                    help="timed-region length used when --steps is not given")
     return p.parse_args()
@@ -336,7 +338,8 @@ def run_ours(args, w):
         n_par = [p.numel() for p in params]
     else:
         L = w.layers[0]
-        mod = TTLinear(L.in_modes, L.out_modes, L.ranks, dt, reuse_merge=not args.no_reuse)
+        mod = TTLinear(L.in_modes, L.out_modes, L.ranks, dt, reuse_merge=not args.no_reuse,
+                       reuse_z=not (args.no_reuse or args.no_reuse_z))
         params = [torch.from_numpy(synth.pack(inp0.layers[0].cores, inp0.layers[0].diags)).to(dev)]
         N, M = L.N, L.M
         n_par = [params[0].numel()]
@@ -394,45 +397,52 @@ def run_ours(args, w):
     ttc.check(ttc.tt_get_device_status(sh), "device status after warm-up")
     barrier()
 
-    # One CUDA graph per rotating input set holds a whole fwd+bwd step, as
-    # the CoMERA pages capture their training step; --eager launches from
-    # the host every time instead.
-    graphs, graph_note, launches_per_step = None, "eager", None
+    # One CUDA graph holds one pass over the rotating input sets: nsets whole
+    # fwd+bwd steps in a row, as the CoMERA pages capture their training step
+    # in a graph.  Inside a graph consecutive steps keep the programmatic
+    # (PDL) edges between their kernels; --eager launches from the host every
+    # time instead.
+    graph, graph_note, launches_per_step = None, "eager", None
     if not args.eager:
         try:
-            graphs = []
-            for j in range(nsets):
-                g = torch.cuda.CUDAGraph()
-                c0 = ttc.lib().tt_launch_count()
-                with torch.cuda.graph(g):
-                    step(j, int(torch.cuda.current_stream().cuda_stream))
-                launches_per_step = int(ttc.lib().tt_launch_count() - c0)
-                graphs.append(g)
-            for j in range(max(3, nsets)):
-                graphs[j % nsets].replay()
+            g = torch.cuda.CUDAGraph()
+            c0 = ttc.lib().tt_launch_count()
+            with torch.cuda.graph(g):
+                cs = int(torch.cuda.current_stream().cuda_stream)
+                for j in range(nsets):
+                    step(j, cs)
+            launches_per_step = int(ttc.lib().tt_launch_count() - c0) // nsets
+            for _ in range(3):
+                g.replay()
             torch.cuda.synchronize(dev)
             ttc.check(ttc.tt_get_device_status(sh), "device status after graph warm-up")
-            graph_note = "cuda_graph"
+            graph = g
+            graph_note = f"cuda_graph ({nsets} steps per replay, one per rotating input set)"
         except Exception as e:  # capture unsupported: time the eager loop
-            graphs, graph_note = None, f"eager (graph capture failed: {type(e).__name__}: {e})"
+            graph, graph_note = None, f"eager (graph capture failed: {type(e).__name__}: {e})"
             torch.cuda.synchronize(dev)
 
     def run(i):
-        if graphs is not None:
-            graphs[i % nsets].replay()
+        """Step i; with the graph, a replay runs steps i .. i + nsets - 1."""
+        if graph is not None:
+            if i % nsets == 0:
+                graph.replay()
         else:
             step(i)
     # choose K for a timed region of about target-seconds when not given
     if args.steps is None:
+        n = 2 * nsets
         t0 = time.perf_counter()
-        for i in range(5):
+        for i in range(n):
             run(i)
         torch.cuda.synchronize(dev)
-        per = (time.perf_counter() - t0) / 5
+        per = (time.perf_counter() - t0) / n
         K = int(min(100000, max(20, args.target_seconds / max(per, 1e-6))))
         K = int(all_reduce_scalar(K, "min", dev))
     else:
         K = args.steps
+    if graph is not None:
+        K = -(-K // nsets) * nsets   # whole replays
     barrier()
 
     # ---- timed region
@@ -450,7 +460,7 @@ def run_ours(args, w):
     ev1.record(stream)
     barrier()
     launches = int(ttc.lib().tt_launch_count() - l0)
-    if graphs is not None:
+    if graph is not None:
         launches = K * launches_per_step  # replays launch without the host counter
     clk = clocks.stop()
     ms = all_reduce_scalar(ev0.elapsed_time(ev1) / K, "max", dev)
@@ -592,6 +602,7 @@ def run_ours(args, w):
                              f"(> 2x L2 of {l2 / 1e6:.0f} MB)",
                        "parallelism": f"replicas x{world}",
                        "reuse_merge": (not args.no_reuse) and not w.ffn,
+                       "reuse_z": not (args.no_reuse or args.no_reuse_z) and not w.ffn,
                        "launch": graph_note},
             "ms_per_step_eager": ms_eager,
             "roofline": roof,

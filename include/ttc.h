@@ -80,6 +80,14 @@ typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1, TT_DT_E4M3 = 2 } tt_dtype
  * workspace in between; then tt_backward skips re-merging the cores.  FFN
  * plans ignore it (their two layers share workspace regions). */
 #define TT_REUSE_MERGE 2u
+/* Implies TT_REUSE_MERGE.  On the tensor-core path (bf16 or E4M3 activations)
+ * the forward also keeps z' = (x A) diag(D_d) for every token in the
+ * workspace (bf16, T x 64 values: 128 more bytes a token, counted by
+ * tt_workspace_size), and the backward reads it instead of computing x A
+ * again, so it streams x once instead of twice.  The caller guarantees in
+ * addition that the backward gets the forward's x and T.  The f32 path and
+ * FFN plans ignore it. */
+#define TT_REUSE_Z 4u
 
 typedef struct tt_desc {
   int d;                        /* 1..TT_MAX_D: number of input (= output) modes */
@@ -87,7 +95,7 @@ typedef struct tt_desc {
   int out_modes[TT_MAX_D];      /* m_1..m_d, each >= 1 */
   int ranks[2 * TT_MAX_D + 1];  /* r_0..r_2d; r_0 = r_2d = 1, others >= 1 */
   int act;                      /* tt_dtype of x, y, dx, dy (E4M3: y, dx bf16) */
-  unsigned flags;               /* TT_ACCUMULATE | TT_REUSE_MERGE */
+  unsigned flags;               /* TT_ACCUMULATE | TT_REUSE_MERGE | TT_REUSE_Z */
 } tt_desc;
 
 typedef struct tt_plan_s tt_plan_t; /* opaque, immutable host object */

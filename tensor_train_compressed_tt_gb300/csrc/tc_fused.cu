@@ -263,6 +263,22 @@ __device__ __forceinline__ void st_tile_half(uint8_t* tile, int row, int h, cons
   }
 }
 
+// Inverse of st_tile_half: columns [32h, 32h+32) of row `row` as f32.
+__device__ __forceinline__ void ld_tile_half(const uint8_t* tile, int row, int h, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int chunk = (4 * h + q) ^ (row & 7);
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + row * 128 + chunk * 16);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      v[8 * q + 2 * i] = f.x;
+      v[8 * q + 2 * i + 1] = f.y;
+    }
+  }
+}
+
 __device__ __forceinline__ void tma_store(const CUtensorMap* map, const void* src, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
@@ -375,6 +391,7 @@ __device__ __forceinline__ void widen_e4m3_tile(uint8_t* st, int cw, int lane) {
 struct FwdArgs {
   int64_t T;
   int N, M, nN, nM, ntiles;
+  int save_z;  // also store each tile's z' (bf16 [T][64]) through tm_zs
   const float* Dc;
   __nv_bfloat16* y;
 };
@@ -390,6 +407,7 @@ struct BwdArgs {
   float* dDc;  // RP
   float* zero;  // [0, zero_n) set to 0 (scratch the merge backward adds into)
   int zero_n;
+  int use_z;    // read the forward's z' through tm_zs instead of computing x At^T
 };
 
 struct SmemCommon {
@@ -397,6 +415,7 @@ struct SmemCommon {
   uint64_t z_full, z_empty, zp_full, zp_empty, dzp_full, dzp_empty, dz_full, dz_empty;
   uint64_t w_full[2], w_empty[2], x_full[2], x_empty[2];
   uint64_t conv[4];  // FP8 kernels: stage s converted (and its operand loaded)
+  uint64_t zl_full;  // backward with a kept z': the z' tile has landed
   uint64_t fin;
   uint32_t tmem_base;
   int abort_flag;
@@ -430,7 +449,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     tt_fwd_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_at,
                   const __grid_constant__ CUtensorMap tm_bt,
-                  const __grid_constant__ CUtensorMap tm_y, FwdArgs p) {
+                  const __grid_constant__ CUtensorMap tm_y,
+                  const __grid_constant__ CUtensorMap tm_zs, FwdArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1k(smem_raw);
   uint8_t* stages = base;
@@ -534,6 +554,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         TL_STAMP(0, 2);
         if (!wait_bar(&S.zp_full, tl & 1, abort_flag, 4)) break;
         tc_fence_after();
+        if (p.save_z) {  // keep z' for the backward (rows past T are clipped)
+          tma_store(&tm_zs, zp_tile, 0, tile * TILE);
+          bulk_commit();
+        }
         for (int c = 0; c < p.nM; ++c, ++it, ++yc) {
           const int s = it % NSTAGE_F;
           const int yb = yc & 1;
@@ -551,9 +575,11 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           mma_commit(&S.x_full[yb]);
         }
         if (!ok) break;
+        if (p.save_z) bulk_wait_read<0>();  // the z' store has read the tile
         mma_commit(&S.zp_empty);
         TL_STAMP(0, 4);
       }
+      if (p.save_z) bulk_wait_all();
       mma_commit(&S.fin);
       drain_bar(&S.fin, 0);
     }
@@ -654,7 +680,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tm_anr,
                   const __grid_constant__ CUtensorMap tm_dx,
                   const __grid_constant__ CUtensorMap tm_dac,
-                  const __grid_constant__ CUtensorMap tm_dbc, BwdArgs p) {
+                  const __grid_constant__ CUtensorMap tm_dbc,
+                  const __grid_constant__ CUtensorMap tm_zs, BwdArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1k(smem_raw);
   uint8_t* stages = base;
@@ -688,6 +715,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       mbar_init(&S.x_empty[b], NEPI);
     }
     for (int s = 0; s < NSTAGE_B; ++s) mbar_init(&S.conv[s], NCONV);
+    mbar_init(&S.zl_full, 1);
     mbar_init(&S.fin, 1);
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -705,17 +733,25 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   if (threadIdx.x == 0) TL_STAMP(1, 1);
   volatile int* abort_flag = &S.abort_flag;
   const int nchunks = 2 * p.nN + p.nM;
+  // with the forward's z' kept, phase A (x At^T) is skipped: chunks start at B
+  const int cfirst = p.use_z ? p.nN : 0;
 
   if (warp == 0) {
-    // ---------------- TMA producer: A chunks, B chunks, C chunks per tile
+    // ---------------- TMA producer: (z' tile,) A chunks, B chunks, C chunks per tile
     if (lane == 0) {
-      int it = 0;
+      int it = 0, tl = 0;
       int last_parity[NSTAGE_B];
       for (int s = 0; s < NSTAGE_B; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
+      for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
         const int tok0 = tile * TILE;
-        for (int c = 0; c < nchunks; ++c, ++it) {
+        if (p.use_z) {
+          // the shared z'/dz tile is free once the previous tile's phase C is done
+          if (!wait_bar(&S.dz_empty, (tl & 1) ^ 1, abort_flag, 30)) break;
+          mbar_expect_tx(&S.zl_full, BOX);
+          tma_load(zp_tile, &tm_zs, &S.zl_full, 0, tok0);
+        }
+        for (int c = cfirst; c < nchunks; ++c, ++it) {
           const int s = it % NSTAGE_B;
           const uint32_t ph = (it / NSTAGE_B) & 1;
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 11)) { ok = false; break; }
@@ -745,6 +781,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       }
       for (int s = 0; s < NSTAGE_B; ++s)
         if (last_parity[s] >= 0) drain_bar(&S.full[s], (uint32_t)last_parity[s]);
+      if (p.use_z && tl > 0) drain_bar(&S.zl_full, (uint32_t)((tl - 1) & 1));
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer
@@ -759,9 +796,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
         // A: z = x At^T
-        if (!wait_bar(&S.z_empty, (tl & 1) ^ 1, abort_flag, 12)) break;
+        if (!p.use_z && !wait_bar(&S.z_empty, (tl & 1) ^ 1, abort_flag, 12)) break;
         tc_fence_after();
-        for (int c = 0; c < p.nN; ++c, ++it) {
+        for (int c = 0; c < p.nN && !p.use_z; ++c, ++it) {
           const int s = it % NSTAGE_B;
           if (!wait_bar(&ready[s], (it / NSTAGE_B) & 1, abort_flag, 13)) { ok = false; break; }
           tc_fence_after();
@@ -775,7 +812,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           mma_commit(&S.empty[s]);
         }
         if (!ok) break;
-        mma_commit(&S.z_full);
+        if (!p.use_z) mma_commit(&S.z_full);
         TL_STAMP(1, 2);
         // B: dz' = dy Bm^T, dB^T chunk = dy^T z'
         if (!wait_bar(&S.dzp_empty, (tl & 1) ^ 1, abort_flag, 14)) break;
@@ -791,8 +828,11 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
             for (int k = 0; k < 4; ++k)
               mma(tmem + B_DZP, kdesc(st + b * BOX) + 2 * k,
                   kdesc(st + OPND + b * (BOX / 2)) + 2 * k, id_r, (c | b | k) != 0);
-          if (c == 0) {
-            if (!wait_bar(&S.zp_full, tl & 1, abort_flag, 16)) { ok = false; break; }
+          if (c == 0) {  // z' written by the epilogue, or loaded from the forward's copy
+            if (!wait_bar(p.use_z ? &S.zl_full : &S.zp_full, tl & 1, abort_flag, 16)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
           }
           const int wb = wc & 1;
@@ -846,7 +886,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     int it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
-      for (int c = 0; c < nchunks; ++c, ++it) {
+      for (int c = cfirst; c < nchunks; ++c, ++it) {
         const int s = it % NSTAGE_B;
         if (!warp_wait(&S.full[s], (it / NSTAGE_B) & 1, abort_flag, 41)) { ok = false; break; }
         widen_e4m3_tile(stages + s * STAGE, cw, lane);
@@ -868,21 +908,23 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tl) {
       float z[32], v[32];
       bool ok = true;
-      // E1: z -> z' tile
-      if (!warp_wait(&S.z_full, tl & 1, abort_flag, 22)) break;
-      tc_fence_after();
-      tmem_ld32(tmem + lane_off + B_Z + 32 * h, z);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.z_empty);
+      if (!p.use_z) {
+        // E1: z -> z' tile
+        if (!warp_wait(&S.z_full, tl & 1, abort_flag, 22)) break;
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + B_Z + 32 * h, z);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.z_empty);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = z[j] * S.Dc[32 * h + j];
-      // the shared z'/dz tile is free once the previous tile's phase C is done
-      if (!warp_wait(&S.dz_empty, (tl & 1) ^ 1, abort_flag, 23)) break;
-      st_tile_half(zp_tile, row, h, v);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.zp_full);
+        for (int j = 0; j < 32; ++j) v[j] = z[j] * S.Dc[32 * h + j];
+        // the shared z'/dz tile is free once the previous tile's phase C is done
+        if (!warp_wait(&S.dz_empty, (tl & 1) ^ 1, abort_flag, 23)) break;
+        st_tile_half(zp_tile, row, h, v);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.zp_full);
+      }
       if (warp == 2 && lane == 0) TL_STAMP(1, 3);
       // E2: dB^T chunks (row = output index within the chunk)
       for (int c = 0; c < p.nM; ++c, ++wc) {
@@ -916,12 +958,21 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dzp_empty);
+      if (p.use_z) {
+        // z' of this thread's row from the loaded tile (read before dz
+        // overwrites the same bytes below); sum z' dz' / Dc = sum z dz'
+        if (!warp_wait(&S.zl_full, tl & 1, abort_flag, 31)) break;
+        ld_tile_half(zp_tile, row, h, z);
+      }
       {
         float pr[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) pr[j] = z[j] * v[j];
-        const float colsum = warp_transpose_sum(pr, lane);
-        if (32 * h + lane < rprime) atomicAdd(p.dDc + 32 * h + lane, colsum);
+        float colsum = warp_transpose_sum(pr, lane);
+        if (32 * h + lane < rprime) {
+          if (p.use_z) colsum = colsum / S.Dc[32 * h + lane];  // nonzero: compacted column
+          atomicAdd(p.dDc + 32 * h + lane, colsum);
+        }
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= S.Dc[32 * h + j];
@@ -1279,18 +1330,18 @@ TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t off) {
 }
 
 tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws, size_t off,
-                     bool f8, cudaStream_t st) {
+                     bool f8, void* zs, cudaStream_t st) {
   if (T <= 0) return TT_OK;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-  CUtensorMap mx, mat, mbt, my;
+  CUtensorMap mx, mat, mbt, my, mzs;
   const bool mx_ok = f8 ? make_map(&mx, x, L.N, T, CH, TILE, kMapU8) : make_map(&mx, x, L.N, T, 64, TILE);
   if (!mx_ok ||
       !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
       !make_map(&mbt, at<void>(ws, off + t.Bt), RP, L.M, 64, CH) ||
-      !make_map(&my, y, L.M, T, 64, 32))
+      !make_map(&my, y, L.M, T, 64, 32) || !make_map(&mzs, zs ? zs : y, RP, T, 64, TILE))
     return TT_ERR_CUDA;
   FwdArgs a;
   a.T = T;
@@ -1299,18 +1350,22 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   a.nN = (int)((L.N + CH - 1) / CH);
   a.nM = (int)((L.M + CH - 1) / CH);
   a.ntiles = (int)((T + TILE - 1) / TILE);
+  a.save_z = zs != nullptr;
   a.Dc = at<float>(ws, off + t.Dc);
   a.y = static_cast<__nv_bfloat16*>(y);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e =
-      f8 ? launch_ex(tt_fwd_kernel<true>, grid, NTHREADS_F8, kSmemFwd, st, false, mx, mat, mbt, my, a)
-         : launch_ex(tt_fwd_kernel<false>, grid, NTHREADS, kSmemFwd, st, false, mx, mat, mbt, my, a);
+      f8 ? launch_ex(tt_fwd_kernel<true>, grid, NTHREADS_F8, kSmemFwd, st, false, mx, mat, mbt, my,
+                     mzs, a)
+         : launch_ex(tt_fwd_kernel<false>, grid, NTHREADS, kSmemFwd, st, false, mx, mat, mbt, my,
+                     mzs, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
-                      void* ws, size_t off, float* zero, size_t zero_n, bool f8, cudaStream_t st) {
+                      void* ws, size_t off, float* zero, size_t zero_n, bool f8, const void* zs,
+                      cudaStream_t st) {
   if (zero_n > 0x7FFFFFFF) return TT_ERR_UNSUPPORTED;
   if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
   if (T <= 0) {
@@ -1321,7 +1376,7 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-  CUtensorMap mx, mdy, mat, mbm, manr, mdx, mdac, mdbc;
+  CUtensorMap mx, mdy, mat, mbm, manr, mdx, mdac, mdbc, mzs;
   const bool act_ok = f8 ? make_map(&mx, x, L.N, T, CH, TILE, kMapU8) &&
                                make_map(&mdy, dy, L.M, T, CH, TILE, kMapU8)
                          : make_map(&mx, x, L.N, T, 64, TILE) && make_map(&mdy, dy, L.M, T, 64, TILE);
@@ -1331,7 +1386,8 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
       !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH) ||
       !make_map(&mdx, dx, L.N, T, 64, 32) ||
       !make_map(&mdac, at<void>(ws, off + t.dAc), RP, L.N, 32, 32, kMapF32) ||
-      !make_map(&mdbc, at<void>(ws, off + t.dBc), RP, L.M, 32, 32, kMapF32))
+      !make_map(&mdbc, at<void>(ws, off + t.dBc), RP, L.M, 32, 32, kMapF32) ||
+      !make_map(&mzs, zs ? zs : dx, RP, T, 64, TILE))
     return TT_ERR_CUDA;
   BwdArgs a;
   a.T = T;
@@ -1348,11 +1404,12 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.dDc = at<float>(ws, off + t.dDc);
   a.zero = zero;
   a.zero_n = (int)zero_n;
+  a.use_z = zs != nullptr;
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e = f8 ? launch_ex(tt_bwd_kernel<true>, grid, NTHREADS_F8, kSmemBwd, st, false, mx,
-                                 mdy, mat, mbm, manr, mdx, mdac, mdbc, a)
+                                 mdy, mat, mbm, manr, mdx, mdac, mdbc, mzs, a)
                       : launch_ex(tt_bwd_kernel<false>, grid, NTHREADS, kSmemBwd, st, false, mx, mdy,
-                                  mat, mbm, manr, mdx, mdac, mdbc, a);
+                                  mat, mbm, manr, mdx, mdac, mdbc, mzs, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }

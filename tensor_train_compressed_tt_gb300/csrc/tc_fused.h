@@ -31,17 +31,19 @@ size_t tc_operand_bytes(const LayerPlan& L);
 
 // y = ((x A) diag(D_d)) B for T tokens; the packed operands (written by the
 // merge engine's pack phase) are in the workspace at ws_off.  x is bf16, or
-// E4M3 codes when f8; y is bf16.
+// E4M3 codes when f8; y is bf16.  With zs (256-byte aligned, T x 64 bf16) the
+// kernel also stores z' = (x A) diag(D_d) there, rank compacted and padded.
 tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws,
-                     size_t ws_off, bool f8, cudaStream_t st);
+                     size_t ws_off, bool f8, void* zs, cudaStream_t st);
 
 // dx for T tokens and the token sums dAc, dBc, dDc (zeroed by the pack
 // phase); the merge engine's unpack phase turns these into dA, dB, dD_d.
 // zero[0, zero_n) is set to 0 on the way (scratch that the merge backward
 // then adds into), also when T == 0.  x and dy are bf16, or E4M3 codes when
-// f8; dx is bf16.
+// f8; dx is bf16.  With zs, z' is read from the forward's copy there instead
+// of being recomputed from x.
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
                       void* ws, size_t ws_off, float* zero, size_t zero_n, bool f8,
-                      cudaStream_t st);
+                      const void* zs, cudaStream_t st);
 
 }  // namespace ttc

@@ -26,12 +26,13 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
   if (d < 1 || d > TT_MAX_D) return TT_ERR_INVALID_ARG;
   if (desc->act != TT_DT_F32 && desc->act != TT_DT_BF16 && desc->act != TT_DT_E4M3)
     return TT_ERR_INVALID_ARG;
-  if (desc->flags & ~(TT_ACCUMULATE | TT_REUSE_MERGE)) return TT_ERR_INVALID_ARG;
+  if (desc->flags & ~(TT_ACCUMULATE | TT_REUSE_MERGE | TT_REUSE_Z)) return TT_ERR_INVALID_ARG;
   LayerPlan p;
   p.d = d;
   p.K = 2 * d;
   p.act = desc->act;
   p.flags = desc->flags;
+  if (p.flags & TT_REUSE_Z) p.flags |= TT_REUSE_MERGE;  // the kept z' implies the kept merge
   p.N = 1;
   p.M = 1;
   for (int k = 0; k < d; ++k) {
@@ -89,6 +90,7 @@ struct WsLayout {
   size_t part_cap = 0;   // floats per partial buffer
   size_t z = 0, dzp = 0; // SIMT token path intermediates
   size_t tc = 0;         // tensor-core path operands
+  size_t zs = 0;         // z' kept by the forward for the backward (TT_REUSE_Z), bf16 [T][64]
   size_t end = 0;        // end of this layer's scratch
 };
 
@@ -120,6 +122,7 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   w->z = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->dzp = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->tc = take(tc_operand_bytes(L));
+  w->zs = take(tc && (L.flags & TT_REUSE_Z) ? (size_t)T * 64 * 2 : 0);
   w->end = off;
   return off;
 }
@@ -483,7 +486,8 @@ tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, co
   if (s != TT_OK) return s;
   prof_begin(kPhFwd, st);
   if (tc) {
-    s = tc_forward(L, T, x, y, ws, w.tc, tx == TT_DT_E4M3, st);
+    void* zs = (L.flags & TT_REUSE_Z) ? static_cast<char*>(ws) + w.zs : nullptr;
+    s = tc_forward(L, T, x, y, ws, w.tc, tx == TT_DT_E4M3, zs, st);
   } else {
     const float* A = P[L.d - 1];   // N x rd
     const float* B = P[L.K - 1];   // rd x M
@@ -585,7 +589,8 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   prof_begin(kPhBwd, st);
   const size_t nz = dq0_zero_floats(L, w);
   if (tc) {
-    s = tc_backward(L, T, x, dy, dx, ws, w.tc, dq_buf(ws, w, 0, 0), nz, tx == TT_DT_E4M3, st);
+    const void* zs = (L.flags & TT_REUSE_Z) ? static_cast<char*>(ws) + w.zs : nullptr;
+    s = tc_backward(L, T, x, dy, dx, ws, w.tc, dq_buf(ws, w, 0, 0), nz, tx == TT_DT_E4M3, zs, st);
   } else {
     if (nz) TT_CUDA(cudaMemsetAsync(dq_buf(ws, w, 0, 0), 0, nz * sizeof(float), st));
     s = simt_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
@@ -665,8 +670,8 @@ tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out) {
   if (a.act == TT_DT_E4M3) return TT_ERR_UNSUPPORTED;  // the FFN pair runs in bf16 or f32
   // the two layers share workspace regions, so a merge cannot be kept
   // from the forward to the backward: TT_REUSE_MERGE has no effect here
-  a.flags &= ~TT_REUSE_MERGE;
-  b.flags &= ~TT_REUSE_MERGE;
+  a.flags &= ~(TT_REUSE_MERGE | TT_REUSE_Z);
+  b.flags &= ~(TT_REUSE_MERGE | TT_REUSE_Z);
   tt_plan_s* p = new (std::nothrow) tt_plan_s();
   if (!p) return TT_ERR_INVALID_ARG;
   p->kind = 1;

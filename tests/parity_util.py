@@ -23,8 +23,11 @@ def to_dev(a: np.ndarray, act: str) -> torch.Tensor:
 
 
 def gpu_layer(shape: synth.LayerShape, act: str, li: synth.LayerInputs, x: np.ndarray,
-              dy: np.ndarray, accumulate: bool = False):
-    layer = TTLinear(shape.in_modes, shape.out_modes, shape.ranks, TORCH_DT[act], accumulate)
+              dy: np.ndarray, accumulate: bool = False, reuse_z: bool = False):
+    """Forward then backward on one workspace (reuse_z: the backward reads the
+    forward's kept z', as the benchmark's step does)."""
+    layer = TTLinear(shape.in_modes, shape.out_modes, shape.ranks, TORCH_DT[act], accumulate,
+                     reuse_z=reuse_z)
     params = torch.from_numpy(synth.pack(li.cores, li.diags)).cuda()
     xd, dyd = to_dev(x, act), to_dev(dy, act)
     T = x.shape[0]

@@ -81,6 +81,27 @@ def test_ffn_layout_and_validation(lib):
         ttc.tt_ffn_plan(_desc(up), _desc(dn, act=ttc.TT_DT_F32))
 
 
+def test_reuse_z_flag(lib):
+    """TT_REUSE_Z adds T x 64 bf16 of kept z' to the tensor-core plans'
+    workspace, implies TT_REUSE_MERGE, and leaves f32 and FFN plans alone."""
+    shape = synth.WORKLOADS["tt768_bf16"].layers[0]
+    for act in (ttc.TT_DT_BF16, ttc.TT_DT_E4M3):
+        base = ttc.tt_plan(_desc(shape, act=act))
+        kz = ttc.tt_plan(_desc(shape, act=act, flags=ttc.TT_REUSE_Z))
+        km = ttc.tt_plan(_desc(shape, act=act, flags=ttc.TT_REUSE_Z | ttc.TT_REUSE_MERGE))
+        for T in (1, 300, 16384):
+            extra = ttc.tt_workspace_size(kz, T) - ttc.tt_workspace_size(base, T)
+            assert T * 128 <= extra < T * 128 + 512
+            assert ttc.tt_workspace_size(km, T) == ttc.tt_workspace_size(kz, T)
+    f32 = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32))
+    f32z = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32, flags=ttc.TT_REUSE_Z))
+    assert ttc.tt_workspace_size(f32z, 1000) == ttc.tt_workspace_size(f32, 1000)
+    up, dn = synth.WORKLOADS["ffn768_3072_bf16"].layers
+    a = ttc.tt_ffn_plan(_desc(up), _desc(dn))
+    b = ttc.tt_ffn_plan(_desc(up, flags=ttc.TT_REUSE_Z), _desc(dn, flags=ttc.TT_REUSE_Z))
+    assert ttc.tt_workspace_size(a, 4096) == ttc.tt_workspace_size(b, 4096)
+
+
 def test_e4m3_plans(lib):
     """E4M3 runs on the fused tensor-core kernels only: shapes they do not
     take, and FFN pairs, are refused at plan time; the workspace is the bf16

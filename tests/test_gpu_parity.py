@@ -28,11 +28,11 @@ from parity_util import (TOL, TORCH_DT, compare, gpu_ffn, gpu_layer, oracle_ffn,
                           oracle_layer, to_dev)
 
 
-def _run(name, tokens=None, seed=0):
+def _run(name, tokens=None, seed=0, reuse_z=False):
     w = synth.WORKLOADS[name]
     inp = synth.draw(w, seed=seed, tokens=tokens)
     shape = w.layers[0]
-    out = gpu_layer(shape, w.act, inp.layers[0], inp.x, inp.dy)
+    out = gpu_layer(shape, w.act, inp.layers[0], inp.x, inp.dy, reuse_z=reuse_z)
     ref = oracle_layer(shape, inp.layers[0], inp.x, inp.dy)
     return compare(out, ref, TOL[w.act], f"{name} T={inp.x.shape[0]}")
 
@@ -273,3 +273,44 @@ def test_tt768_e4m3_pruned():
     out = gpu_layer(shape, wp.act, inp.layers[0], inp.x, inp.dy)
     ref = oracle_layer(shape, inp.layers[0], inp.x, inp.dy)
     compare(out, ref, TOL["e4m3"], "tt768 e4m3 pruned")
+
+
+# ---- TT_REUSE_Z: the backward reads the forward's z' -----------------------
+
+@pytest.mark.parametrize("name,T", [("tt768_bf16", 16384), ("tt768_e4m3", 16384),
+                                    ("tt768_bf16", 300), ("pruned768_3072_bf16", 1000),
+                                    ("tt1024_4096_bf16", 4096), ("tt1024_4096_e4m3", 777)])
+def test_reuse_z_against_oracle(name, T):
+    """Every output against the oracle, element by element, at the benchmark's
+    launch configuration (kept z') and full token count where listed."""
+    _run(name, tokens=T, reuse_z=True)
+
+
+@pytest.mark.parametrize("name", ["tt768_bf16", "tt768_e4m3", "pruned768_768_bf16"])
+def test_reuse_z_matches_recompute(name):
+    """y and dx are the recomputing path's bit for bit (the same z' tile feeds
+    the same MMAs); dparams agree to rounding: dD_d is summed from the bf16 z'
+    divided by D_d instead of the f32 z.  Two backward calls after one forward
+    read the same kept z'."""
+    import torch as th
+    from tensor_train_compressed_tt_gb300.layer import TTLinear
+    w = synth.WORKLOADS[name]
+    inp = synth.draw(w, seed=4, tokens=1000)
+    s = w.layers[0]
+    params = th.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
+    x, dy = to_dev(inp.x, w.act), to_dev(inp.dy, w.act)
+    ref = TTLinear(s.in_modes, s.out_modes, s.ranks, TORCH_DT[w.act])
+    y0 = ref.forward(x, params)
+    dx0, g0 = ref.backward(x, dy, params)
+    kz = TTLinear(s.in_modes, s.out_modes, s.ranks, TORCH_DT[w.act], reuse_z=True)
+    assert kz.workspace_bytes(1000) >= ref.workspace_bytes(1000) + 1000 * 128
+    ws = kz.workspace(1000)
+    y1 = kz.forward(x, params, ws=ws)
+    dx1, g1 = kz.backward(x, dy, params, ws=ws)
+    dx2, g2 = kz.backward(x, dy, params, ws=ws)
+    th.cuda.synchronize()
+    assert th.equal(y0, y1)
+    assert th.equal(dx0, dx1) and th.equal(dx0, dx2)
+    a0 = g0.cpu().numpy()
+    assert O.rel_err(g1.cpu().numpy(), a0) <= 1e-3
+    assert O.rel_err(g2.cpu().numpy(), g1.cpu().numpy()) <= 1e-5
