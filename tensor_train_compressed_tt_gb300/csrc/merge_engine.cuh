@@ -476,7 +476,7 @@ __device__ void eng_chain_unit(const EngProgram& prog, const EngTask& t, int u, 
       if (i >= npi) break;
       const float v = acc[i];
       const int f = ((p0 + pi0 + i) * sl + q0) * rL + z;  // flat index into P_{L-1}
-      c.out[f] = v;
+      if (c.out) c.out[f] = v;
       if (!t.pack_side) continue;
       const __nv_bfloat16 bv = __float2bfloat16_rn(v);
       if (t.pack_side == 1) {  // A (N x rd): f = j * rd + a

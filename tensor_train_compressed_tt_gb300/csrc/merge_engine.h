@@ -28,7 +28,7 @@ struct ChainDesc {
   const float* core[TT_MAX_D] = {};
   const float* diag[TT_MAX_D] = {};
   float* prow[TT_MAX_D] = {};   // P_k buffers for 1 <= k <= L-2
-  float* out = nullptr;         // P_{L-1}
+  float* out = nullptr;         // P_{L-1} (null: packed operands only)
   int r[TT_MAX_D + 1] = {};
   int s[TT_MAX_D] = {};
   int L = 0;

@@ -56,7 +56,7 @@ cudaError_t read_and_clear_device_status(DeviceStatus* out) {
 
 namespace {
 
-constexpr int TILE = 128;            // tokens per tile (MMA M)
+constexpr int TILE = 128;            // MMA M: rows of a token tile in shared memory and TMEM
 constexpr int RP = 64;               // padded rank (one 128-byte swizzle atom)
 constexpr int CH = 128;              // features / outputs per pipeline chunk
 constexpr int BOX = 16 * 1024;       // [128 rows][64 bf16] swizzled box
@@ -388,9 +388,13 @@ __device__ __forceinline__ void widen_e4m3_tile(uint8_t* st, int cw, int lane) {
   }
 }
 
+// A tile holds tt <= TILE tokens (a multiple of 16, chosen on the host so that
+// the tiles spread over every SM); rows tt .. TILE-1 of the shared-memory
+// activation boxes are zeroed once and never written by TMA, so they add
+// nothing to the token sums.
 struct FwdArgs {
   int64_t T;
-  int N, M, nN, nM, ntiles;
+  int N, M, nN, nM, ntiles, tt;
   int save_z;  // also store each tile's z' (bf16 [T][64]) through tm_zs
   const float* Dc;
   __nv_bfloat16* y;
@@ -398,7 +402,7 @@ struct FwdArgs {
 
 struct BwdArgs {
   int64_t T;
-  int N, M, nN, nM, ntiles;
+  int N, M, nN, nM, ntiles, tt;
   const float* Dc;
   const int* rinfo;  // [0] = r', [1..64] = kept index of each compacted column
   __nv_bfloat16* dx;
@@ -421,6 +425,28 @@ struct SmemCommon {
   int abort_flag;
   float Dc[RP];
 };
+
+// Chunk i of n visited in position c of a tile's phase.  The backward's
+// token sums are bulk-added into one [N or M][64] buffer by every CTA; with
+// the order rotated by the tile index, concurrent CTAs add into different
+// row blocks instead of all into the same one.
+__device__ __forceinline__ int rot_chunk(int c, int n, int tile) {
+  const int i = c + tile % n;
+  return i < n ? i : i - n;
+}
+
+// Zero rows [tt, TILE) of the stages' two activation boxes and of the z' tile.
+__device__ void zero_tail_rows(uint8_t* stages, int nstage, uint8_t* zp_tile, int tt) {
+  if (tt >= TILE) return;
+  const int per_box = (TILE - tt) * 8;  // 16-byte units
+  const int nbox = 2 * nstage + 1;
+  for (int i = threadIdx.x; i < nbox * per_box; i += blockDim.x) {
+    const int b = i / per_box, o = i - b * per_box;
+    uint8_t* bp = b < 2 * nstage ? stages + (b >> 1) * STAGE + (b & 1) * BOX : zp_tile;
+    *reinterpret_cast<uint4*>(bp + tt * 128 + o * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_async_smem();  // the MMAs read these rows through the async proxy
+}
 
 __device__ __forceinline__ uint8_t* align1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -450,6 +476,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tm_at,
                   const __grid_constant__ CUtensorMap tm_bt,
                   const __grid_constant__ CUtensorMap tm_y,
+                  const __grid_constant__ CUtensorMap tm_y16,
                   const __grid_constant__ CUtensorMap tm_zs, FwdArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1k(smem_raw);
@@ -482,6 +509,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   pdl_wait();  // nothing a previous grid writes is touched before this point
   pdl_trigger();
   if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
+  zero_tail_rows(stages, NSTAGE_F, zp_tile, p.tt);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -496,8 +524,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       int last_parity[NSTAGE_F];
       for (int s = 0; s < NSTAGE_F; ++s) last_parity[s] = -1;
       bool ok = true;
+      const uint32_t act_bytes = (uint32_t)p.tt * 128;  // one activation box of tt rows
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
-        const int tok0 = tile * TILE;
+        const int tok0 = tile * p.tt;
         for (int c = 0; ok && c < p.nN + p.nM; ++c, ++it) {
           const int s = it % NSTAGE_F;
           const uint32_t ph = (it / NSTAGE_F) & 1;
@@ -505,10 +534,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           uint8_t* st = stages + s * STAGE;
           if (c < p.nN) {
             if (F8) {  // one E4M3 box of 128 columns into the second bf16 box's bytes
-              mbar_expect_tx(&S.full[s], 2 * BOX);
+              mbar_expect_tx(&S.full[s], act_bytes + BOX);
               tma_load(st + BOX, &tm_x, &S.full[s], c * CH, tok0);
             } else {
-              mbar_expect_tx(&S.full[s], STAGE);
+              mbar_expect_tx(&S.full[s], 2 * act_bytes + BOX);
               tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
               tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
             }
@@ -555,7 +584,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         if (!wait_bar(&S.zp_full, tl & 1, abort_flag, 4)) break;
         tc_fence_after();
         if (p.save_z) {  // keep z' for the backward (rows past T are clipped)
-          tma_store(&tm_zs, zp_tile, 0, tile * TILE);
+          tma_store(&tm_zs, zp_tile, 0, tile * p.tt);
           bulk_commit();
         }
         for (int c = 0; c < p.nM; ++c, ++it, ++yc) {
@@ -645,8 +674,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         if (lane == 0) {
           mbar_arrive(&S.x_empty[yb]);
           const int col = c * CH + 64 * h;
-          if (col < p.M && (int64_t)tile * TILE + 32 * q < p.T)
-            tma_store(&tm_y, box, col, tile * TILE + 32 * q);
+          const int vq = p.tt - 32 * q;  // rows of this quadrant inside the tile
+          if (col < p.M && vq > 0 && (int64_t)tile * p.tt + 32 * q < p.T)
+            tma_store(vq >= 32 ? &tm_y : &tm_y16, box, col, tile * p.tt + 32 * q);
           bulk_commit();  // one group per chunk, empty if skipped: keeps the box ring in step
         }
       }
@@ -679,6 +709,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tm_bm,
                   const __grid_constant__ CUtensorMap tm_anr,
                   const __grid_constant__ CUtensorMap tm_dx,
+                  const __grid_constant__ CUtensorMap tm_dx16,
                   const __grid_constant__ CUtensorMap tm_dac,
                   const __grid_constant__ CUtensorMap tm_dbc,
                   const __grid_constant__ CUtensorMap tm_zs, BwdArgs p) {
@@ -726,6 +757,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_n; i += gridDim.x * blockDim.x)
     p.zero[i] = 0.f;
+  zero_tail_rows(stages, NSTAGE_B, zp_tile, p.tt);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -743,12 +775,13 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       int last_parity[NSTAGE_B];
       for (int s = 0; s < NSTAGE_B; ++s) last_parity[s] = -1;
       bool ok = true;
+      const uint32_t act_bytes = (uint32_t)p.tt * 128;  // one activation box of tt rows
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
-        const int tok0 = tile * TILE;
+        const int tok0 = tile * p.tt;
         if (p.use_z) {
           // the shared z'/dz tile is free once the previous tile's phase C is done
           if (!wait_bar(&S.dz_empty, (tl & 1) ^ 1, abort_flag, 30)) break;
-          mbar_expect_tx(&S.zl_full, BOX);
+          mbar_expect_tx(&S.zl_full, act_bytes);
           tma_load(zp_tile, &tm_zs, &S.zl_full, 0, tok0);
         }
         for (int c = cfirst; c < nchunks; ++c, ++it) {
@@ -756,11 +789,14 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           const uint32_t ph = (it / NSTAGE_B) & 1;
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 11)) { ok = false; break; }
           uint8_t* st = stages + s * STAGE;
-          mbar_expect_tx(&S.full[s], F8 ? 2 * BOX : STAGE);
+          mbar_expect_tx(&S.full[s], (F8 ? act_bytes : 2 * act_bytes) + BOX);
           // activation tile: E4M3 as one box into the second bf16 box's bytes
           const bool is_dy = c >= p.nN && c < p.nN + p.nM;
           const CUtensorMap* act = is_dy ? &tm_dy : &tm_x;
-          const int col = (c < p.nN ? c : is_dy ? c - p.nN : c - p.nN - p.nM) * CH;
+          const int col = (c < p.nN      ? c
+                           : is_dy       ? rot_chunk(c - p.nN, p.nM, tile)
+                                         : rot_chunk(c - p.nN - p.nM, p.nN, tile)) *
+                          CH;
           if (F8) {
             tma_load(st + BOX, act, &S.full[s], col, tok0);
           } else {
@@ -936,7 +972,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.w_empty[wb]);
         // rows = outputs c*128 + 32q.., columns = compacted ranks 32h..
-        if (32 * h < rprime && c * CH + 32 * q < p.M) {
+        const int cb = rot_chunk(c, p.nM, tile);  // the producer's order of dy chunks
+        if (32 * h < rprime && cb * CH + 32 * q < p.M) {
           uint8_t* box = my_stg + (nst & 1) * STG;
           if (lane == 0) bulk_wait_read<1>();  // the operation that used this box is done reading
           __syncwarp();
@@ -944,7 +981,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add(&tm_dbc, box, 32 * h, c * CH + 32 * q);
+            tma_reduce_add(&tm_dbc, box, 32 * h, cb * CH + 32 * q);
             bulk_commit();
           }
           ++nst;
@@ -988,8 +1025,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         const int xb = xc & 1;
         if (!warp_wait(&S.x_full[xb], (xc >> 1) & 1, abort_flag, 27)) { ok = false; break; }
         tc_fence_after();
-        const int col = c * CH + 64 * h;
-        const bool st_dx = col < p.N && (int64_t)tile * TILE + 32 * q < p.T;
+        const int cx = rot_chunk(c, p.nN, tile);  // the producer's order of phase-C x chunks
+        const int col = cx * CH + 64 * h;
+        const int vq = p.tt - 32 * q;  // rows of this quadrant inside the tile
+        const bool st_dx = col < p.N && vq > 0 && (int64_t)tile * p.tt + 32 * q < p.T;
         uint8_t* box = my_stg + (nst & 1) * STG;
         if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
@@ -1004,7 +1043,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         if (lane == 0) {
           mbar_arrive(&S.x_empty[xb]);
           if (st_dx) {
-            tma_store(&tm_dx, box, col, tile * TILE + 32 * q);
+            tma_store(vq >= 32 ? &tm_dx : &tm_dx16, box, col, tile * p.tt + 32 * q);
             bulk_commit();
           }
         }
@@ -1017,7 +1056,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.w_empty[wb]);
         // rows = features c*128 + 32q.., columns = compacted ranks 32h..
-        if (32 * h < rprime && c * CH + 32 * q < p.N) {
+        if (32 * h < rprime && cx * CH + 32 * q < p.N) {
           uint8_t* box2 = my_stg + (nst & 1) * STG;
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
@@ -1025,7 +1064,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add(&tm_dac, box2, 32 * h, c * CH + 32 * q);
+            tma_reduce_add(&tm_dac, box2, 32 * h, cx * CH + 32 * q);
             bulk_commit();
           }
           ++nst;
@@ -1256,6 +1295,25 @@ cudaError_t set_smem_attrs() {
   return err;
 }
 
+// Tokens per tile: the fewest tiles of at most TILE tokens that give every
+// SM the same number of waves, rounded up to a multiple of 16 (16 .. TILE).
+// At 16384 tokens on 152 SMs that is 112 tokens in 147 tiles rather than 128
+// in 128 (24 SMs idle).  TTC_TILE_TOKENS (16 .. 128, multiple of 16) fixes it.
+int tokens_per_tile(int64_t T) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char* e = getenv("TTC_TILE_TOKENS");
+    const int v = e ? atoi(e) : 0;
+    forced = (v >= 16 && v <= TILE && v % 16 == 0) ? v : 0;
+  }
+  if (forced) return forced;
+  const int64_t sms = num_sms();
+  const int64_t waves = (T + (int64_t)TILE * sms - 1) / ((int64_t)TILE * sms);
+  int64_t tt = (T + waves * sms - 1) / (waves * sms);
+  tt = (tt + 15) / 16 * 16;
+  return (int)(tt < 16 ? 16 : tt > TILE ? TILE : tt);
+}
+
 // Programmatic dependent launch is on unless TTC_NO_PDL is set (to 1).
 bool pdl_enabled() {
   static int on = -1;
@@ -1336,12 +1394,14 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-  CUtensorMap mx, mat, mbt, my, mzs;
-  const bool mx_ok = f8 ? make_map(&mx, x, L.N, T, CH, TILE, kMapU8) : make_map(&mx, x, L.N, T, 64, TILE);
+  const int tt = tokens_per_tile(T);
+  CUtensorMap mx, mat, mbt, my, my16, mzs;
+  const bool mx_ok = f8 ? make_map(&mx, x, L.N, T, CH, tt, kMapU8) : make_map(&mx, x, L.N, T, 64, tt);
   if (!mx_ok ||
       !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
       !make_map(&mbt, at<void>(ws, off + t.Bt), RP, L.M, 64, CH) ||
-      !make_map(&my, y, L.M, T, 64, 32) || !make_map(&mzs, zs ? zs : y, RP, T, 64, TILE))
+      !make_map(&my, y, L.M, T, 64, 32) || !make_map(&my16, y, L.M, T, 64, 16) ||
+      !make_map(&mzs, zs ? zs : y, RP, T, 64, tt))
     return TT_ERR_CUDA;
   FwdArgs a;
   a.T = T;
@@ -1349,16 +1409,17 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   a.M = (int)L.M;
   a.nN = (int)((L.N + CH - 1) / CH);
   a.nM = (int)((L.M + CH - 1) / CH);
-  a.ntiles = (int)((T + TILE - 1) / TILE);
+  a.tt = tt;
+  a.ntiles = (int)((T + tt - 1) / tt);
   a.save_z = zs != nullptr;
   a.Dc = at<float>(ws, off + t.Dc);
   a.y = static_cast<__nv_bfloat16*>(y);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e =
       f8 ? launch_ex(tt_fwd_kernel<true>, grid, NTHREADS_F8, kSmemFwd, st, false, mx, mat, mbt, my,
-                     mzs, a)
+                     my16, mzs, a)
          : launch_ex(tt_fwd_kernel<false>, grid, NTHREADS, kSmemFwd, st, false, mx, mat, mbt, my,
-                     mzs, a);
+                     my16, mzs, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
@@ -1376,18 +1437,19 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-  CUtensorMap mx, mdy, mat, mbm, manr, mdx, mdac, mdbc, mzs;
-  const bool act_ok = f8 ? make_map(&mx, x, L.N, T, CH, TILE, kMapU8) &&
-                               make_map(&mdy, dy, L.M, T, CH, TILE, kMapU8)
-                         : make_map(&mx, x, L.N, T, 64, TILE) && make_map(&mdy, dy, L.M, T, 64, TILE);
+  const int tt = tokens_per_tile(T);
+  CUtensorMap mx, mdy, mat, mbm, manr, mdx, mdx16, mdac, mdbc, mzs;
+  const bool act_ok = f8 ? make_map(&mx, x, L.N, T, CH, tt, kMapU8) &&
+                               make_map(&mdy, dy, L.M, T, CH, tt, kMapU8)
+                         : make_map(&mx, x, L.N, T, 64, tt) && make_map(&mdy, dy, L.M, T, 64, tt);
   if (!act_ok ||
       !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
       !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
       !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH) ||
-      !make_map(&mdx, dx, L.N, T, 64, 32) ||
+      !make_map(&mdx, dx, L.N, T, 64, 32) || !make_map(&mdx16, dx, L.N, T, 64, 16) ||
       !make_map(&mdac, at<void>(ws, off + t.dAc), RP, L.N, 32, 32, kMapF32) ||
       !make_map(&mdbc, at<void>(ws, off + t.dBc), RP, L.M, 32, 32, kMapF32) ||
-      !make_map(&mzs, zs ? zs : dx, RP, T, 64, TILE))
+      !make_map(&mzs, zs ? zs : dx, RP, T, 64, tt))
     return TT_ERR_CUDA;
   BwdArgs a;
   a.T = T;
@@ -1395,7 +1457,8 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.M = (int)L.M;
   a.nN = (int)((L.N + CH - 1) / CH);
   a.nM = (int)((L.M + CH - 1) / CH);
-  a.ntiles = (int)((T + TILE - 1) / TILE);
+  a.tt = tt;
+  a.ntiles = (int)((T + tt - 1) / tt);
   a.Dc = at<float>(ws, off + t.Dc);
   a.rinfo = at<int>(ws, off + t.rinfo);
   a.dx = static_cast<__nv_bfloat16*>(dx);
@@ -1407,9 +1470,9 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.use_z = zs != nullptr;
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e = f8 ? launch_ex(tt_bwd_kernel<true>, grid, NTHREADS_F8, kSmemBwd, st, false, mx,
-                                 mdy, mat, mbm, manr, mdx, mdac, mdbc, mzs, a)
+                                 mdy, mat, mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a)
                       : launch_ex(tt_bwd_kernel<false>, grid, NTHREADS, kSmemBwd, st, false, mx, mdy,
-                                  mat, mbm, manr, mdx, mdac, mdbc, mzs, a);
+                                  mat, mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }

@@ -264,7 +264,9 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
         }
         if (k >= 1 && k <= L.d - 2) c.prow[k] = const_cast<float*>(P[k0 + k]);
       }
-      c.out = const_cast<float*>(P[k0 + L.d - 1]);
+      // the f32 A / B are read only by the SIMT token path; the tensor-core
+      // path takes the packed bf16 operands alone
+      c.out = pack ? nullptr : const_cast<float*>(P[k0 + L.d - 1]);
       c.nprefix = np;
       EngTask* t = b.add();
       if (!eng_chain_task(t, c))  // ranks above 64 or cores too large to stage

@@ -41,7 +41,10 @@ def test_tiny64_f32():
     _run("tiny64_f32")
 
 
-@pytest.mark.parametrize("T", [1, 7, 128, 300, 16384])
+# Token counts cover every tile height the host picks (16 .. 128 tokens a
+# tile, so that tiles spread over all SMs): 16 (T <= 2432), 48 (6000),
+# 80 (10000), 112 (16384), 128 (18000) on 152 SMs, each with a ragged last tile.
+@pytest.mark.parametrize("T", [1, 7, 128, 300, 6000, 10000, 16384, 18000])
 def test_tt768_bf16(T):
     _run("tt768_bf16", tokens=T)
 
@@ -207,7 +210,7 @@ def test_internal_rank_above_64_uses_generic_merge():
 
 # ---- E4M3 activations ------------------------------------------------------
 
-@pytest.mark.parametrize("T", [1, 7, 300, 16384])
+@pytest.mark.parametrize("T", [1, 7, 300, 10000, 16384])
 def test_tt768_e4m3(T):
     _run("tt768_e4m3", tokens=T)
 
