@@ -4,6 +4,8 @@
 #pragma once
 
 #include <atomic>
+#include <cstdio>
+#include <cstdlib>
 
 #include "merge_engine.h"
 
@@ -299,14 +301,12 @@ __device__ void eng_gemm_unit(const EngProgram& prog, const EngTask& t, int u, i
         const int c = pos[cu - jj * (unsigned)t.rd];
         if (c >= 0) {
           static_cast<__nv_bfloat16*>(t.tc.Anr)[(size_t)jj * RP + c] = b;
-          static_cast<__nv_bfloat16*>(t.tc.At)[(size_t)c * t.N + jj] = b;
         }
       } else {
         const unsigned a = cu / (unsigned)t.M;
         const int c = pos[a];
         if (c >= 0) {
           const unsigned oo = cu - a * (unsigned)t.M;
-          static_cast<__nv_bfloat16*>(t.tc.Bt)[(size_t)oo * RP + c] = b;
           static_cast<__nv_bfloat16*>(t.tc.Bm)[(size_t)c * t.M + oo] = b;
         }
       }
@@ -482,16 +482,12 @@ __device__ void eng_chain_unit(const EngProgram& prog, const EngTask& t, int u, 
       if (t.pack_side == 1) {  // A (N x rd): f = j * rd + a
         const unsigned jj = (unsigned)f / (unsigned)t.rd;
         const int cc = pos[(unsigned)f - jj * (unsigned)t.rd];
-        if (cc >= 0) {
-          static_cast<__nv_bfloat16*>(t.tc.Anr)[(size_t)jj * RP + cc] = bv;
-          static_cast<__nv_bfloat16*>(t.tc.At)[(size_t)cc * t.N + jj] = bv;
-        }
+        if (cc >= 0) static_cast<__nv_bfloat16*>(t.tc.Anr)[(size_t)jj * RP + cc] = bv;
       } else {  // B (rd x M): f = a * M + o
         const unsigned a = (unsigned)f / (unsigned)t.M;
         const int cc = pos[a];
         if (cc >= 0) {
           const unsigned o = (unsigned)f - a * (unsigned)t.M;
-          static_cast<__nv_bfloat16*>(t.tc.Bt)[(size_t)o * RP + cc] = bv;
           static_cast<__nv_bfloat16*>(t.tc.Bm)[(size_t)cc * t.M + o] = bv;
         }
       }
@@ -544,8 +540,8 @@ __device__ void eng_coldot_unit(const EngTask& t, int c, float* red) {
 }
 
 __device__ void eng_scale_unit(const EngTask& t, int u) {
-  const int64_t base = (int64_t)u * 1024;
-  for (int e = threadIdx.x; e < 1024; e += blockDim.x) {
+  const int64_t base = (int64_t)u * t.chunk;
+  for (int e = threadIdx.x; e < t.chunk; e += blockDim.x) {
     const int64_t i = base + e;
     if (i >= t.n) break;
     float v = t.x ? __ldcg(t.x + i) : 0.f;
@@ -585,9 +581,16 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
     const int t0 = p.phase_begin[ph], t1 = p.phase_begin[ph + 1];
     int total = 0;
     for (int t = t0; t < t1; ++t) total += p.t[t].units;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-      int t = t0, uu = u;
-      while (uu >= p.t[t].units) uu -= p.t[t++].units;
+    // Units are dealt in waves of gridDim.x, costliest tasks first, and every
+    // other wave in reverse CTA order, so that the CTAs with the cheapest
+    // unit of one wave take the costliest of the next.
+    for (int w = 0; w * (int)gridDim.x < total; ++w) {
+      const int u = w * (int)gridDim.x +
+                    ((w & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+      if (u >= total) continue;
+      int o = t0, uu = u;
+      while (uu >= p.t[p.order[o]].units) uu -= p.t[p.order[o++]].units;
+      const int t = p.order[o];
       const EngTask& k = p.t[t];
 #ifdef TTC_TIMELINE
       if (threadIdx.x == 0 && nu < 8) {
@@ -741,14 +744,15 @@ void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t part
 
 void EngBuilder::balance(int budget) {
   const int t0 = p.phase_begin[p.nphases - 1];
-  // nothing to gain when even the narrowest configuration needs two waves
+  // aim at the fewest waves that the narrowest configuration allows
   int64_t min_total = 0;
   for (int i = t0; i < p.ntasks; ++i) {
     EngTask probe = p.t[i];
     if (probe.kind == kEGemm) eng_gemm_config(&probe, 0);
     min_total += probe.units;
   }
-  if (min_total > budget) return;
+  if (budget < 1) budget = 1;
+  if (min_total > budget) budget = (int)(ceil_div(min_total, budget) * budget);
   for (int iter = 0; iter < 64; ++iter) {
     int64_t total = 0;
     for (int i = t0; i < p.ntasks; ++i) total += p.t[i].units;
@@ -833,6 +837,39 @@ void eng_gemm_final_task(EngTask* t, const EngTask& gemm) {
   t->units = (int)ceil_div(gemm.g.m * gemm.g.n, kEngThreads);
 }
 
+// Rough cost of one unit of a task (arbitrary units, for ordering only): a
+// GEMM unit pays a staging round trip plus its tile's K extent; a chain unit
+// stages whole cores.
+static double eng_unit_cost(const EngTask& k) {
+  switch (k.kind) {
+    case kEGemm:
+      return 2000.0 + 0.25 * (double)k.kchunk * (k.tm + k.tn) + (k.fold_g ? 500.0 : 0.0) +
+             (k.gather || k.pack_side ? 500.0 : 0.0);
+    case kEChain: return 6000.0;
+    case kEGemmFinal: return 400.0 + 50.0 * k.splits;
+    case kEColdot: return 800.0;
+    case kEPack:
+    case kEUnpack:
+    case kEDd: return 800.0;
+    default: return 400.0;
+  }
+}
+
+static void eng_dump(const EngProgram& p) {
+  for (int ph = 0; ph < p.nphases; ++ph) {
+    fprintf(stderr, "engine phase %d\n", ph);
+    for (int o = p.phase_begin[ph]; o < p.phase_begin[ph + 1]; ++o) {
+      const EngTask& k = p.t[p.order[o]];
+      fprintf(stderr,
+              "  task %2d kind %d units %4d  m %lld n %lld k %lld  tile %dx%d splits %d kchunk %d"
+              "%s%s%s\n",
+              (int)p.order[o], k.kind, k.units, (long long)k.g.m, (long long)k.g.n,
+              (long long)k.g.k, k.tm, k.tn, k.splits, k.kchunk, k.fold_g ? " fold" : "",
+              k.gather ? " gather" : "", k.pack_side ? " pack" : "");
+    }
+  }
+}
+
 cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
   static std::atomic<unsigned> next_slot{0};
   static int grid = 0;
@@ -850,6 +887,22 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
   }
   EngProgram p = prog;
   p.slot = next_slot.fetch_add(1) % kBarSlots;
+  for (int ph = 0; ph < p.nphases; ++ph) {  // costliest units first, stable
+    const int a = p.phase_begin[ph], b = p.phase_begin[ph + 1];
+    for (int i = a; i < b; ++i) p.order[i] = (unsigned char)i;
+    for (int i = a + 1; i < b; ++i) {
+      const unsigned char v = p.order[i];
+      const double cv = eng_unit_cost(p.t[v]);
+      int j = i;
+      for (; j > a && eng_unit_cost(p.t[p.order[j - 1]]) < cv; --j) p.order[j] = p.order[j - 1];
+      p.order[j] = v;
+    }
+  }
+  static int dumps = 0;
+  if (getenv("TTC_ENG_DUMP") && dumps < 4) {
+    ++dumps;
+    eng_dump(p);
+  }
   // the one D_d that the program's gather and pack epilogues compact by
   p.dmid = nullptr;
   for (int i = 0; i < p.ntasks; ++i) {

@@ -60,6 +60,7 @@ struct alignas(16) EngTask {
   float* out = nullptr;
   int64_t n = 0, sx = 0, sy = 0;
   int len = 1, acc = 0;
+  int chunk = 1024;     // kEScale: elements per unit
   // pack / unpack (s = middle diagonal D_d, out = dD_d for unpack)
   const float* A = nullptr;
   const float* B = nullptr;
@@ -93,6 +94,9 @@ struct alignas(16) EngProgram {
   const float* dmid = nullptr;  // D_d whose compaction map the gather / pack
                                 // epilogues use (set by eng_launch)
   int phase_begin[kEngMaxPhases + 1] = {};
+  // units of a phase are dealt in this task order (set by eng_launch: the
+  // tasks with the costliest units first)
+  unsigned char order[kEngMaxTasks] = {};
   EngTask t[kEngMaxTasks];
 };
 
@@ -104,7 +108,8 @@ struct EngBuilder {
   EngTask* add();
   void end();  // closes (and balances) the last phase
   // Narrows the GEMM tasks of the last phase (larger tiles, fewer K splits)
-  // until its units fit one wave of `budget` CTAs, where possible.
+  // until its units fit the fewest waves of `budget` CTAs that its
+  // narrowest configuration allows (one wave where possible).
   void balance(int budget);
 };
 

@@ -11,11 +11,13 @@
 // Layout of the packed operands (bf16, rank padded to RP = 64 with zero rows
 // or columns; the middle rank is compacted to the nonzero entries of D_d, so
 // pruned ranks cost nothing but padding):
-//   At  (RP x N)  B operand of z  = x  . At^T   (K = features, K-major)
-//   Anr (N x RP)  B operand of dx = dz . Anr^T  (K = rank, K-major)
-//   Bm  (RP x M)  B operand of dz'= dy . Bm^T   (K = outputs, K-major)
-//   Bt  (M x RP)  B operand of y  = z' . Bt^T   (K = rank, K-major)
-// The weight-side products dA = x^T dz and dB^T = dy^T z' read the very same
+//   Anr (N x RP)  B operand of z  = x  . A     (K = features, MN-major)
+//                 and of dx = dz . Anr^T      (K = rank, K-major)
+//   Bm  (RP x M)  B operand of y  = z' . Bm    (K = rank, MN-major)
+//                 and of dz'= dy . Bm^T       (K = outputs, K-major)
+// Each is stored once, in the layout whose rows the merges write contiguously;
+// a 128-byte swizzled box of it serves as either operand major-ness.  The
+// weight-side products dA = x^T dz and dB^T = dy^T z' read the very same
 // x / dy / z' / dz tiles through MN-major descriptors (the 128-byte swizzled
 // [token][64 elements] tile is K-major for the token-side products and
 // MN-major for the weight-side ones).
@@ -473,8 +475,8 @@ __device__ void tmem_free(uint32_t base) {
 template <bool F8>
 __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     tt_fwd_kernel(const __grid_constant__ CUtensorMap tm_x,
-                  const __grid_constant__ CUtensorMap tm_at,
-                  const __grid_constant__ CUtensorMap tm_bt,
+                  const __grid_constant__ CUtensorMap tm_anr,
+                  const __grid_constant__ CUtensorMap tm_bm,
                   const __grid_constant__ CUtensorMap tm_y,
                   const __grid_constant__ CUtensorMap tm_y16,
                   const __grid_constant__ CUtensorMap tm_zs, FwdArgs p) {
@@ -541,11 +543,12 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
               tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
               tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
             }
-            tma_load(st + OPND, &tm_at, &S.full[s], c * CH, 0);
-            tma_load(st + OPND + BOX / 2, &tm_at, &S.full[s], c * CH + 64, 0);
+            tma_load(st + OPND, &tm_anr, &S.full[s], 0, c * CH);  // [128 features][64 ranks]
           } else {
             mbar_expect_tx(&S.full[s], BOX);
-            tma_load(st + OPND, &tm_bt, &S.full[s], 0, (c - p.nN) * CH);
+            // [64 ranks][128 outputs] as two boxes of 64 outputs
+            tma_load(st + OPND, &tm_bm, &S.full[s], (c - p.nN) * CH, 0);
+            tma_load(st + OPND + BOX / 2, &tm_bm, &S.full[s], (c - p.nN) * CH + 64, 0);
           }
           last_parity[s] = (int)ph;
         }
@@ -556,8 +559,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_z = idesc(128, 64, 0, 0);
-      const uint32_t id_y = idesc(128, 128, 0, 0);
+      const uint32_t id_z = idesc(128, 64, 0, 1);   // B = Anr rows, MN-major
+      const uint32_t id_y = idesc(128, 128, 0, 1);  // B = Bm rows, MN-major
       const uint32_t zp_addr = su32(zp_tile);
       uint64_t* ready = F8 ? S.conv : S.full;  // a stage the MMAs may read
       int it = 0, yc = 0, tl = 0;
@@ -574,8 +577,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           for (int b = 0; b < 2; ++b)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma(tmem + F_Z, kdesc(st + b * BOX) + 2 * k, kdesc(st + OPND + b * (BOX / 2)) + 2 * k,
-                  id_z, (c | b | k) != 0);
+              mma(tmem + F_Z, kdesc(st + b * BOX) + 2 * k,
+                  mndesc(st + OPND + b * (BOX / 2), 1024) + 128 * k, id_z, (c | b | k) != 0);
           mma_commit(&S.empty[s]);
         }
         if (!ok) break;
@@ -593,13 +596,13 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           if (!wait_bar(&S.x_empty[yb], ((yc >> 1) & 1) ^ 1, abort_flag, 5)) { ok = false; break; }
           if (c < 3) TL_STAMP(0, 13 + c);  // y buffer free
           if (!wait_bar(&ready[s], (it / NSTAGE_F) & 1, abort_flag, 6)) { ok = false; break; }
-          if (c < 3) TL_STAMP(0, 10 + c);  // Bt chunk in shared memory
+          if (c < 3) TL_STAMP(0, 10 + c);  // Bm chunk in shared memory
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma(tmem + F_Y + yb * 128, kdesc(zp_addr) + 2 * k, kdesc(st + OPND) + 2 * k, id_y,
-                k != 0);
+            mma(tmem + F_Y + yb * 128, kdesc(zp_addr) + 2 * k,
+                mndesc(st + OPND, BOX / 2) + 128 * k, id_y, k != 0);
           mma_commit(&S.empty[s]);
           mma_commit(&S.x_full[yb]);
         }
@@ -705,7 +708,6 @@ template <bool F8>
 __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     tt_bwd_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_dy,
-                  const __grid_constant__ CUtensorMap tm_at,
                   const __grid_constant__ CUtensorMap tm_bm,
                   const __grid_constant__ CUtensorMap tm_anr,
                   const __grid_constant__ CUtensorMap tm_dx,
@@ -803,9 +805,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
             tma_load(st, act, &S.full[s], col, tok0);
             tma_load(st + BOX, act, &S.full[s], col + 64, tok0);
           }
-          if (c < p.nN) {  // A
-            tma_load(st + OPND, &tm_at, &S.full[s], col, 0);
-            tma_load(st + OPND + BOX / 2, &tm_at, &S.full[s], col + 64, 0);
+          if (c < p.nN) {  // A: Anr rows of the chunk, read MN-major
+            tma_load(st + OPND, &tm_anr, &S.full[s], 0, col);
           } else if (is_dy) {  // B
             tma_load(st + OPND, &tm_bm, &S.full[s], col, 0);
             tma_load(st + OPND + BOX / 2, &tm_bm, &S.full[s], col + 64, 0);
@@ -823,6 +824,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_r = idesc(128, 64, 0, 0);     // token x rank, K-major
+      const uint32_t id_a = idesc(128, 64, 0, 1);     // token x rank, B = Anr rows MN-major
       const uint32_t id_w = idesc(128, 64, 1, 1);     // weight x rank, MN-major
       const uint32_t id_x = idesc(128, 128, 0, 0);    // token x feature, K-major
       const uint32_t zp_addr = su32(zp_tile);
@@ -843,8 +845,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           for (int b = 0; b < 2; ++b)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma(tmem + B_Z, kdesc(st + b * BOX) + 2 * k, kdesc(st + OPND + b * (BOX / 2)) + 2 * k,
-                  id_r, (c | b | k) != 0);
+              mma(tmem + B_Z, kdesc(st + b * BOX) + 2 * k,
+                  mndesc(st + OPND + b * (BOX / 2), 1024) + 128 * k, id_a, (c | b | k) != 0);
           mma_commit(&S.empty[s]);
         }
         if (!ok) break;
@@ -1128,10 +1130,8 @@ __device__ void tc_pack_unit(const float* __restrict__ A, const float* __restric
   __shared__ int rcount;
   compaction_map(Dmid, rd, nullptr, kept, &rcount);
   const int64_t nA = (int64_t)N * RP, nB = (int64_t)M * RP;
-  __nv_bfloat16* At = static_cast<__nv_bfloat16*>(p.At);
   __nv_bfloat16* Anr = static_cast<__nv_bfloat16*>(p.Anr);
   __nv_bfloat16* Bm = static_cast<__nv_bfloat16*>(p.Bm);
-  __nv_bfloat16* Bt = static_cast<__nv_bfloat16*>(p.Bt);
   for (int e = threadIdx.x; e < kPackPer; e += blockDim.x) {
     const int64_t i = (int64_t)unit * kPackPer + e;
     if (i < nA) {
@@ -1140,19 +1140,16 @@ __device__ void tc_pack_unit(const float* __restrict__ A, const float* __restric
         const float v = kept[c] >= 0 ? __ldcg(A + (int64_t)j * rd + kept[c]) : 0.f;
         const __nv_bfloat16 b = __float2bfloat16_rn(v);
         Anr[i] = b;
-        At[(int64_t)c * N + j] = b;
       }
       if (zero_grads) p.dAc[i] = 0.f;
     } else if (i < nA + nB) {
-      const int64_t k = i - nA;
-      const int o = (int)(k / RP), c = (int)(k % RP);
+      const int64_t k = i - nA;  // Bm [RP][M], walked in its own (row-major) order
+      const int c = (int)(k / M), o = (int)(k - (int64_t)c * M);
       if (!pad_only || kept[c] < 0) {
         const float v = kept[c] >= 0 ? __ldcg(B + (int64_t)kept[c] * M + o) : 0.f;
-        const __nv_bfloat16 b = __float2bfloat16_rn(v);
-        Bt[k] = b;
-        Bm[(int64_t)c * M + o] = b;
+        Bm[k] = __float2bfloat16_rn(v);
       }
-      if (zero_grads) p.dBc[k] = 0.f;
+      if (zero_grads) p.dBc[k] = 0.f;  // dBc has the same size, [M][RP]
     } else if (i < nA + nB + RP) {
       const int c = (int)(i - nA - nB);
       p.Dc[c] = kept[c] >= 0 ? Dmid[kept[c]] : 0.f;
@@ -1201,7 +1198,7 @@ __device__ void tc_unpack_unit(const TcPtrs& p, const float* Dmid, int rd, int N
 // host side
 // ==========================================================================
 struct TcLayout {
-  size_t At, Anr, Bm, Bt, Dc, rinfo, dAc, dBc, dDc, total;
+  size_t Anr, Bm, Dc, rinfo, dAc, dBc, dDc, total;
 };
 
 size_t al256(size_t v) { return (v + 255) / 256 * 256; }
@@ -1214,10 +1211,8 @@ TcLayout tc_layout(const LayerPlan& L) {
     o = al256(o + b);
     return r;
   };
-  t.At = take((size_t)RP * L.N * 2);
   t.Anr = take((size_t)L.N * RP * 2);
   t.Bm = take((size_t)RP * L.M * 2);
-  t.Bt = take((size_t)L.M * RP * 2);
   t.Dc = take(RP * 4);
   t.rinfo = take((RP + 1) * 4);
   t.dAc = take((size_t)L.N * RP * 4);
@@ -1375,10 +1370,8 @@ size_t tc_operand_bytes(const LayerPlan& L) {
 TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t off) {
   const TcLayout t = tc_layout(L);
   TcPtrs p;
-  p.At = at<void>(ws, off + t.At);
   p.Anr = at<void>(ws, off + t.Anr);
   p.Bm = at<void>(ws, off + t.Bm);
-  p.Bt = at<void>(ws, off + t.Bt);
   p.Dc = at<float>(ws, off + t.Dc);
   p.rinfo = at<int>(ws, off + t.rinfo);
   p.dAc = at<float>(ws, off + t.dAc);
@@ -1395,11 +1388,11 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
   const int tt = tokens_per_tile(T);
-  CUtensorMap mx, mat, mbt, my, my16, mzs;
+  CUtensorMap mx, manr, mbm, my, my16, mzs;
   const bool mx_ok = f8 ? make_map(&mx, x, L.N, T, CH, tt, kMapU8) : make_map(&mx, x, L.N, T, 64, tt);
   if (!mx_ok ||
-      !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
-      !make_map(&mbt, at<void>(ws, off + t.Bt), RP, L.M, 64, CH) ||
+      !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH) ||
+      !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
       !make_map(&my, y, L.M, T, 64, 32) || !make_map(&my16, y, L.M, T, 64, 16) ||
       !make_map(&mzs, zs ? zs : y, RP, T, 64, tt))
     return TT_ERR_CUDA;
@@ -1416,9 +1409,9 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   a.y = static_cast<__nv_bfloat16*>(y);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e =
-      f8 ? launch_ex(tt_fwd_kernel<true>, grid, NTHREADS_F8, kSmemFwd, st, false, mx, mat, mbt, my,
+      f8 ? launch_ex(tt_fwd_kernel<true>, grid, NTHREADS_F8, kSmemFwd, st, false, mx, manr, mbm, my,
                      my16, mzs, a)
-         : launch_ex(tt_fwd_kernel<false>, grid, NTHREADS, kSmemFwd, st, false, mx, mat, mbt, my,
+         : launch_ex(tt_fwd_kernel<false>, grid, NTHREADS, kSmemFwd, st, false, mx, manr, mbm, my,
                      my16, mzs, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
@@ -1438,12 +1431,11 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
   const int tt = tokens_per_tile(T);
-  CUtensorMap mx, mdy, mat, mbm, manr, mdx, mdx16, mdac, mdbc, mzs;
+  CUtensorMap mx, mdy, mbm, manr, mdx, mdx16, mdac, mdbc, mzs;
   const bool act_ok = f8 ? make_map(&mx, x, L.N, T, CH, tt, kMapU8) &&
                                make_map(&mdy, dy, L.M, T, CH, tt, kMapU8)
                          : make_map(&mx, x, L.N, T, 64, tt) && make_map(&mdy, dy, L.M, T, 64, tt);
   if (!act_ok ||
-      !make_map(&mat, at<void>(ws, off + t.At), L.N, RP, 64, RP) ||
       !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
       !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH) ||
       !make_map(&mdx, dx, L.N, T, 64, 32) || !make_map(&mdx16, dx, L.N, T, 64, 16) ||
@@ -1470,9 +1462,9 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.use_z = zs != nullptr;
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e = f8 ? launch_ex(tt_bwd_kernel<true>, grid, NTHREADS_F8, kSmemBwd, st, false, mx,
-                                 mdy, mat, mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a)
+                                 mdy, mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a)
                       : launch_ex(tt_bwd_kernel<false>, grid, NTHREADS, kSmemBwd, st, false, mx, mdy,
-                                  mat, mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a);
+                                  mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a);
   count_launches(1);
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }

@@ -7,10 +7,8 @@ namespace ttc {
 
 // Device addresses of the packed tensor-core operands and gradient sums.
 struct TcPtrs {
-  void* At = nullptr;    // bf16 [64][N]
   void* Anr = nullptr;   // bf16 [N][64]
   void* Bm = nullptr;    // bf16 [64][M]
-  void* Bt = nullptr;    // bf16 [M][64]
   float* Dc = nullptr;   // [64] compacted middle diagonal (0 past r')
   int* rinfo = nullptr;  // [0] = r', [1 + c] = original index of column c
   float* dAc = nullptr;  // [N][64] sum over tokens of x^T dz

@@ -176,7 +176,8 @@ void eng_zero_task(EngBuilder& b, float* out, int64_t n) {
   EngTask* z = b.add();
   z->kind = kEScale;
   z->n = n;
-  z->units = (int)((n + 1023) / 1024);
+  z->chunk = 8192;  // a unit's cost is mostly fixed: few large units keep a phase in one wave
+  z->units = (int)((n + z->chunk - 1) / z->chunk);
   z->x = nullptr;
   z->out = out;
   z->acc = 0;
