@@ -914,7 +914,10 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
     }
   }
   int g = grid;
-  bool coop = true;
+  // Only a grid barrier needs every CTA resident at once: a one-phase
+  // program launches as an ordinary grid, whose CTAs start as the previous
+  // grid's CTAs leave their SMs (with programmatic launch, before it ends).
+  bool coop = p.nphases > 1;
 #ifdef TTC_TIMELINE
   // measurement builds only: grid size and launch kind from the environment
   if (const char* e = getenv("TTC_ENG_GRID")) g = atoi(e) > 0 && atoi(e) < grid ? atoi(e) : grid;
