@@ -13,6 +13,8 @@
 // Backward: count -> tiled scan (+ row chunks) -> fill (occurrence lists) ->
 //           chunk sums of dout -> per prefix: pair product, its rows' dF_3 and
 //           pair-product gradient, then dF_1, dF_2, dD_1, dD_2.
+// The per-row contractions of a prefix run as small dense GEMMs over batches
+// of its used rows, register-blocked, from shared memory.
 // Sums over repeated indices and over rows sharing a prefix use atomics.
 #include <cuda_runtime.h>
 
@@ -250,6 +252,19 @@ __global__ void ttm_fill_kernel(TtmArgs a, const int32_t* __restrict__ idx) {
   }
 }
 
+// Asynchronous 4-byte global -> shared copies: a thread issues all of its
+// staging copies before waiting, so a staging pass costs one round trip
+// instead of one per element.
+__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<unsigned>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Stages F_1[0, i1] (times D_1 when scale_d1) and F_2[:, i2] for prefix p,
 // and computes the pair product P[(j1, j2), e] = sum_b F_1[0, i1, j1, b] D_1[b]
 // F_2[b, i2, j2, e] into pt (times D_2[e] when scale_d2).  Ends synchronised.
@@ -257,11 +272,12 @@ __device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, 
                                  bool scale_d1, bool scale_d2) {
   const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2, w2 = n2 * r2, nt = a.nA * r2;
   const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
-  for (int e = threadIdx.x; e < n1 * r1; e += blockDim.x) f1[e] = a.F1[i1 * n1 * r1 + e];
-  for (int e = threadIdx.x; e < r1 * w2; e += blockDim.x) {
-    const int b = e / w2;
-    f2[e] = a.F2[(b * a.m2 + i2) * w2 + (e - b * w2)];
+  for (int e = threadIdx.x; e < n1 * r1; e += blockDim.x) cp_async4(f1 + e, a.F1 + i1 * n1 * r1 + e);
+  for (int b = 0; b < r1; ++b) {  // row b of the slice is contiguous in F_2
+    const float* src = a.F2 + (b * a.m2 + i2) * w2;
+    for (int e = threadIdx.x; e < w2; e += blockDim.x) cp_async4(f2 + b * w2 + e, src + e);
   }
+  cp_async_wait_all();
   __syncthreads();
   // one thread per column (j2, e) of F_2's slice; up to 8 rows j1 at a time
   // in registers, so each loaded F_2 value serves 8 products
@@ -304,41 +320,114 @@ __device__ void used_rows(const TtmArgs& a, int p, int base, int* list, int* n) 
   __syncthreads();
 }
 
+// C(m, n) = sum_k A(m, k) B(k, n) for one block, operands in shared memory,
+// each thread holding a 4 x 4 tile of C in registers (8 loads feed 16 FMAs).
+// K runs as k1 < K1 outer, k2 < K2 inner:
+//   A(m, k1, k2) = A[m am + k1 ak1 + k2 ak2]
+//   B(k1, k2, n) = B[(n / nq) bq + (n % nq) bn + k1 bk1 + k2 bk2]
+// A thread's rows are m_t, m_t + TM, ... and its columns n_t, n_t + TN, ...
+// (TM, TN: thread rows and columns), so the lanes of a warp read consecutive
+// columns.  epi(m, n, c) receives every output once.
+struct BlockGemm {
+  int M, N, K1, K2;
+  int am, ak1, ak2;
+  int nq, bq, bn, bk1, bk2;
+};
+
+template <typename Epi>
+__device__ void block_gemm(const float* __restrict__ A, const float* __restrict__ B,
+                           const BlockGemm& g, Epi epi) {
+  const int TM = (g.M + 3) >> 2, TN = (g.N + 3) >> 2;
+  for (int t = threadIdx.x; t < TM * TN; t += blockDim.x) {
+    const int mt = t / TN, nt = t - mt * TN;
+    int ao[4], bo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = mt + i * TM;
+      ao[i] = (m < g.M ? m : 0) * g.am;
+      const int n0 = nt + i * TN, n = n0 < g.N ? n0 : 0;
+      const int q = n / g.nq;
+      bo[i] = q * g.bq + (n - q * g.nq) * g.bn;
+    }
+    float acc[4][4] = {};
+    for (int k1 = 0; k1 < g.K1; ++k1) {
+      const float* a1 = A + k1 * g.ak1;
+      const float* b1 = B + k1 * g.bk1;
+      for (int k2 = 0; k2 < g.K2; ++k2) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          av[i] = a1[ao[i] + k2 * g.ak2];
+          bv[i] = b1[bo[i] + k2 * g.bk2];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[i][c] = fmaf(av[i], bv[c], acc[i][c]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (mt + i * TM < g.M && nt + c * TN < g.N) epi(mt + i * TM, nt + c * TN, acc[i][c]);
+  }
+}
+
+constexpr int kRowBatch = 8;  // used rows of a prefix handled together
+
+// f3b[e][k n3 + j3] = F_3[e, i3_k, j3] for the kb rows i3_k of a batch (each
+// (e, k) run of n3 floats is contiguous in F_3); ends with the copies landed
+// (the caller synchronises the block).
+__device__ void stage_f3(const TtmArgs& a, const int* i3s, int kb, float* f3b, int FP) {
+  const int n3 = a.n3, runs = a.r2 * kb;
+  for (int o = threadIdx.x; o < runs * n3; o += blockDim.x) {
+    const int run = o / n3, j3 = o - run * n3;
+    const int e = run / kb, k = run - e * kb;
+    cp_async4(f3b + e * FP + k * n3 + j3, a.F3 + (e * a.m3 + i3s[k]) * n3 + j3);
+  }
+  cp_async_wait_all();
+}
+
 // Forward, one block of 256 threads per used prefix (slot c): its pair
-// product in shared memory, then its used rows, one warp per row:
-//   row[(jA, j3)] = sum_e P[jA, e] D_2[e] F_3[e, i3, j3, 0]  ->  rows[upos[v]].
-__global__ void __launch_bounds__(256) ttm_pair_rows_kernel(TtmArgs a) {
+// product P (with D_2) in shared memory, then its used rows kRowBatch at a
+// time as one block GEMM,
+//   row_k[(jA, j3)] = sum_e P[jA, e] F_3[e, i3_k, j3]  ->  rows[upos[v_k]],
+// with M = n1 n2, N = (rows of the batch) n3, K = r2.
+__global__ void __launch_bounds__(256, 2) ttm_pair_rows_kernel(TtmArgs a) {
   extern __shared__ float sm[];
   __shared__ int list[256];
   __shared__ int nlist;
-  const int n3 = a.n3, r2 = a.r2, nt = a.nA * r2, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ long long rbase[kRowBatch];
+  const int n3 = a.n3, r2 = a.r2, nt = a.nA * r2;
+  const int FP = kRowBatch * n3;            // row pitch of the staged F_3 slices
   const int c = blockIdx.x;
   if (c >= a.counts[1]) return;
   float* f1 = sm;                           // [n1][r1]
   float* f2 = f1 + a.n1 * a.r1;             // [r1][n2][r2]
   float* pt = f2 + a.r1 * a.n2 * r2;        // [nA][r2], D_1 inside, times D_2
-  float* f3 = pt + nt + warp * r2 * n3;     // this warp's [r2][n3]
+  float* f3b = pt + nt;                     // [r2][kRowBatch n3]: F_3[:, i3_k, :] side by side
   const int p = a.plist[c];
   ttm_pair_product(a, p, f1, f2, pt, true, true);
   for (int base = 0; base < a.m3; base += 256) {
     used_rows(a, p, base, list, &nlist);
-    for (int k = warp; k < nlist; k += 8) {
-      const int i3 = list[k], v = p * a.m3 + i3;
-      for (int o = lane; o < r2 * n3; o += 32) {
-        const int e = o / n3;
-        f3[o] = a.F3[(e * a.m3 + i3) * n3 + (o - e * n3)];
-      }
-      __syncwarp();
-      float* row = a.rows + (size_t)a.upos[v] * a.Dm;
-      for (int j = lane; j < a.Dm; j += 32) {
-        const int jA = j / n3, j3 = j - (j / n3) * n3;
-        float acc = 0.f;
-        for (int e = 0; e < r2; ++e) acc = fmaf(pt[jA * r2 + e], f3[e * n3 + j3], acc);
-        row[j] = acc;
-      }
-      __syncwarp();
+    for (int k0 = 0; k0 < nlist; k0 += kRowBatch) {
+      const int kb = min(kRowBatch, nlist - k0);
+      if ((int)threadIdx.x < kb)
+        rbase[threadIdx.x] = (long long)a.upos[p * a.m3 + list[k0 + threadIdx.x]] * a.Dm;
+      stage_f3(a, list + k0, kb, f3b, FP);
+      __syncthreads();
+      BlockGemm g;
+      g.M = a.nA; g.N = kb * n3; g.K1 = 1; g.K2 = r2;
+      g.am = r2; g.ak1 = 0; g.ak2 = 1;
+      g.nq = 1 << 30; g.bq = 0; g.bn = 1; g.bk1 = 0; g.bk2 = FP;
+      float* rows = a.rows;
+      block_gemm(pt, f3b, g, [&](int jA, int n, float v) {
+        const int k = n / n3;
+        rows[rbase[k] + jA * n3 + (n - k * n3)] = v;
+      });
+      __syncthreads();  // f3b and rbase are refilled next
     }
-    __syncthreads();  // list is refilled next
   }
 }
 
@@ -408,16 +497,17 @@ __global__ void __launch_bounds__(256) ttm_chunk_sum_kernel(TtmArgs a,
 }
 
 // Backward, one block of 256 threads per used prefix (slot c).  Its used
-// rows go to one warp each: dR = the sum of the row's chunk sums,
-//   dF_3[e, i3, j3] += D_2[e] sum_jA P[jA, e] dR[jA, j3]   (P without D_2)
-//   dP[jA, e]       += sum_j3 dR[jA, j3] F_3[e, i3, j3]    (shared memory)
+// rows, kRowBatch at a time: dR_k = the sum of row k's chunk sums, then two
+// block GEMMs over the batch,
+//   dF_3[e, i3_k, j3] += D_2[e] sum_jA P[jA, e] dR_k[jA, j3]   (P without D_2)
+//   dP[jA, e]         += sum_{k, j3} dR_k[jA, j3] F_3[e, i3_k, j3]
 // then back through P D_2 = F_1 D_1 F_2 D_2 for this prefix:
 //   dD_2[e] += sum_jA P[jA, e] dP[jA, e];  G = dP D_2
 //   dF_2[b, i2, j2, e] += D_1[b] sum_j1 F_1[i1, j1, b] G[(j1, j2), e]
 //   H[j1, b] = sum_{j2, e} G[(j1, j2), e] F_2[b, i2, j2, e]
 //   dF_1[0, i1, j1, b] += D_1[b] H[j1, b];  dD_1[b] += sum_j1 F_1[i1, j1, b] H[j1, b]
 // (dD entries of pruned ranks, D == 0, stay untouched).
-__global__ void __launch_bounds__(256) ttm_pair_backward_kernel(TtmArgs a, float* __restrict__ dF1,
+__global__ void __launch_bounds__(256, 2) ttm_pair_backward_kernel(TtmArgs a, float* __restrict__ dF1,
                                                                 float* __restrict__ dF2,
                                                                 float* __restrict__ dF3,
                                                                 float* __restrict__ dD1,
@@ -425,9 +515,10 @@ __global__ void __launch_bounds__(256) ttm_pair_backward_kernel(TtmArgs a, float
   extern __shared__ float sm[];
   __shared__ int list[256];
   __shared__ int nlist;
+  __shared__ int ri3[kRowBatch], rw0[kRowBatch], rnch[kRowBatch];
   const int n1 = a.n1, n2 = a.n2, n3 = a.n3, r1 = a.r1, r2 = a.r2;
   const int w2 = n2 * r2, nt = a.nA * r2, Dm = a.Dm;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int FP = kRowBatch * n3;
   const int c = blockIdx.x;
   if (c >= a.counts[1]) return;
   float* f1 = sm;                // [n1][r1] (without D_1)
@@ -435,43 +526,59 @@ __global__ void __launch_bounds__(256) ttm_pair_backward_kernel(TtmArgs a, float
   float* pt = f2 + r1 * w2;      // [nA][r2] (D_1 inside, without D_2)
   float* dP = pt + nt;           // [nA][r2]
   float* H = dP + nt;            // [n1][r1]
-  float* dR = H + n1 * r1 + warp * (Dm + r2 * n3);   // this warp's [Dm]
-  float* f3 = dR + Dm;                               // this warp's [r2][n3]
+  float* dRb = H + n1 * r1;      // [kRowBatch][Dm]
+  float* f3b = dRb + kRowBatch * Dm;  // [r2][kRowBatch n3]
   const int p = a.plist[c];
   const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
   for (int o = threadIdx.x; o < nt; o += blockDim.x) dP[o] = 0.f;
   ttm_pair_product(a, p, f1, f2, pt, true, false);
   for (int base = 0; base < a.m3; base += 256) {
     used_rows(a, p, base, list, &nlist);
-    for (int k = warp; k < nlist; k += 8) {
-      const int i3 = list[k], v = p * a.m3 + i3;
-      const int u = a.upos[v], w0 = a.uoff[u];
-      const int nch = (a.cnt[v] + kChunk - 1) / kChunk;
-      for (int j = lane; j < Dm; j += 32) {
-        float sacc = 0.f;
-        for (int w = w0; w < w0 + nch; ++w) sacc += a.rows[(size_t)w * Dm + j];
-        dR[j] = sacc;
+    for (int k0 = 0; k0 < nlist; k0 += kRowBatch) {
+      const int kb = min(kRowBatch, nlist - k0);
+      if ((int)threadIdx.x < kb) {
+        const int i3 = list[k0 + threadIdx.x], v = p * a.m3 + i3;
+        ri3[threadIdx.x] = i3;
+        rw0[threadIdx.x] = a.uoff[a.upos[v]];
+        rnch[threadIdx.x] = (a.cnt[v] + kChunk - 1) / kChunk;
       }
-      for (int o = lane; o < r2 * n3; o += 32) {
-        const int e = o / n3;
-        f3[o] = a.F3[(e * a.m3 + i3) * n3 + (o - e * n3)];
+      __syncthreads();
+      // dR_k: the first chunk sum copied asynchronously, further chunks
+      // (rows seen more than kChunk times) added after it has landed
+      for (int k = 0; k < kb; ++k) {
+        const float* src = a.rows + (size_t)rw0[k] * Dm;
+        for (int j = threadIdx.x; j < Dm; j += blockDim.x) cp_async4(dRb + k * Dm + j, src + j);
       }
-      __syncwarp();
-      for (int o = lane; o < r2 * n3; o += 32) {
-        const int e = o / n3, j3 = o - (o / n3) * n3;
-        float acc = 0.f;
-        for (int jA = 0; jA < a.nA; ++jA) acc = fmaf(pt[jA * r2 + e], dR[jA * n3 + j3], acc);
-        atomicAdd(dF3 + (e * a.m3 + i3) * n3 + j3, acc * a.D2[e]);
+      stage_f3(a, ri3, kb, f3b, FP);
+      __syncthreads();
+      for (int k = 0; k < kb; ++k) {
+        if (rnch[k] <= 1) continue;
+        const float* src = a.rows + (size_t)rw0[k] * Dm;
+        for (int j = threadIdx.x; j < Dm; j += blockDim.x) {
+          float sacc = dRb[k * Dm + j];
+          for (int w = 1; w < rnch[k]; ++w) sacc += src[(size_t)w * Dm + j];
+          dRb[k * Dm + j] = sacc;
+        }
       }
-      for (int o = lane; o < nt; o += 32) {
-        const int jA = o / r2, e = o - (o / r2) * r2;
-        float acc = 0.f;
-        for (int j3 = 0; j3 < n3; ++j3) acc = fmaf(dR[jA * n3 + j3], f3[e * n3 + j3], acc);
-        atomicAdd(dP + o, acc);  // shared memory: rows of this prefix in other warps
-      }
-      __syncwarp();
+      __syncthreads();
+      BlockGemm g3;  // dF_3 slices: M = r2 (e), N = kb n3 ((k, j3)), K = nA
+      g3.M = r2; g3.N = kb * n3; g3.K1 = 1; g3.K2 = a.nA;
+      g3.am = 1; g3.ak1 = 0; g3.ak2 = r2;
+      g3.nq = n3; g3.bq = Dm; g3.bn = 1; g3.bk1 = 0; g3.bk2 = n3;
+      const float* D2 = a.D2;
+      const int m3 = a.m3;
+      block_gemm(pt, dRb, g3, [&](int e, int n, float v) {
+        const int k = n / n3;
+        atomicAdd(dF3 + (e * m3 + ri3[k]) * n3 + (n - k * n3), v * D2[e]);
+      });
+      BlockGemm gp;  // dP: M = nA (jA), N = r2 (e), K = (k, j3)
+      gp.M = a.nA; gp.N = r2; gp.K1 = kb; gp.K2 = n3;
+      gp.am = n3; gp.ak1 = Dm; gp.ak2 = 1;
+      gp.nq = 1 << 30; gp.bq = 0; gp.bn = FP; gp.bk1 = n3; gp.bk2 = 1;
+      // every dP entry has one owner thread (the same in every batch)
+      block_gemm(dRb, f3b, gp, [&](int jA, int e, float v) { dP[jA * r2 + e] += v; });
+      __syncthreads();  // dRb, f3b and the row metadata are refilled next
     }
-    __syncthreads();
   }
   for (int e = threadIdx.x; e < r2; e += blockDim.x) {
     if (a.D2[e] == 0.f) continue;
@@ -643,12 +750,12 @@ int sm_count() {
 // Dynamic shared memory (bytes) of the per-prefix kernels.
 size_t pair_rows_smem(const TtmPlan& P) {
   return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * P.n[1] * P.r[2] + P.n[0] * P.n[1] * P.r[2] +
-                      8 * P.r[2] * P.n[2]);
+                      P.r[2] * kRowBatch * P.n[2]);
 }
 size_t pair_backward_smem(const TtmPlan& P) {
   return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * P.n[1] * P.r[2] +
-                      2 * P.n[0] * P.n[1] * P.r[2] + P.n[0] * P.r[1] +
-                      8 * (P.Dm + P.r[2] * P.n[2]));
+                      2 * P.n[0] * P.n[1] * P.r[2] + P.n[0] * P.r[1] + kRowBatch * P.Dm +
+                      P.r[2] * kRowBatch * P.n[2]);
 }
 
 cudaError_t set_attrs() {
