@@ -265,17 +265,28 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Shared-memory row pitches chosen against bank conflicts: an odd pitch for
+// the F_2 slice rows (read across rows by the H product) and the staged F_3
+// slices (read across e by the dP product), and a dR row pitch congruent to
+// n3 mod 32, so that consecutive (row, j3) columns fall in consecutive banks.
+__host__ __device__ inline int f2_pitch(int n2, int r2) { return (n2 * r2) | 1; }
+__host__ __device__ inline int f3_pitch(int kb, int n3) { return (kb * n3) | 1; }
+__host__ __device__ inline int dr_pitch(int Dm, int n3) {
+  return Dm + (((n3 - Dm) % 32) + 32) % 32;
+}
+
 // Stages F_1[0, i1] (times D_1 when scale_d1) and F_2[:, i2] for prefix p,
 // and computes the pair product P[(j1, j2), e] = sum_b F_1[0, i1, j1, b] D_1[b]
 // F_2[b, i2, j2, e] into pt (times D_2[e] when scale_d2).  Ends synchronised.
 __device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, float* pt,
                                  bool scale_d1, bool scale_d2) {
   const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2, w2 = n2 * r2, nt = a.nA * r2;
+  const int F2P = f2_pitch(n2, r2);
   const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
   for (int e = threadIdx.x; e < n1 * r1; e += blockDim.x) cp_async4(f1 + e, a.F1 + i1 * n1 * r1 + e);
   for (int b = 0; b < r1; ++b) {  // row b of the slice is contiguous in F_2
     const float* src = a.F2 + (b * a.m2 + i2) * w2;
-    for (int e = threadIdx.x; e < w2; e += blockDim.x) cp_async4(f2 + b * w2 + e, src + e);
+    for (int e = threadIdx.x; e < w2; e += blockDim.x) cp_async4(f2 + b * F2P + e, src + e);
   }
   cp_async_wait_all();
   __syncthreads();
@@ -287,7 +298,7 @@ __device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, 
     for (int j0 = 0; j0 < n1; j0 += 8) {
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int b = 0; b < r1; ++b) {
-        const float y = f2[b * w2 + je] * (scale_d1 ? a.D1[b] : 1.f);
+        const float y = f2[b * F2P + je] * (scale_d1 ? a.D1[b] : 1.f);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (j0 + i < n1) acc[i] = fmaf(f1[(j0 + i) * r1 + b], y, acc[i]);
@@ -400,12 +411,12 @@ __global__ void __launch_bounds__(256, 2) ttm_pair_rows_kernel(TtmArgs a) {
   __shared__ int nlist;
   __shared__ long long rbase[kRowBatch];
   const int n3 = a.n3, r2 = a.r2, nt = a.nA * r2;
-  const int FP = kRowBatch * n3;            // row pitch of the staged F_3 slices
+  const int FP = f3_pitch(kRowBatch, n3);   // row pitch of the staged F_3 slices
   const int c = blockIdx.x;
   if (c >= a.counts[1]) return;
   float* f1 = sm;                           // [n1][r1]
   float* f2 = f1 + a.n1 * a.r1;             // [r1][n2][r2]
-  float* pt = f2 + a.r1 * a.n2 * r2;        // [nA][r2], D_1 inside, times D_2
+  float* pt = f2 + a.r1 * f2_pitch(a.n2, r2);  // [nA][r2], D_1 inside, times D_2
   float* f3b = pt + nt;                     // [r2][kRowBatch n3]: F_3[:, i3_k, :] side by side
   const int p = a.plist[c];
   ttm_pair_product(a, p, f1, f2, pt, true, true);
@@ -518,16 +529,16 @@ __global__ void __launch_bounds__(256, 2) ttm_pair_backward_kernel(TtmArgs a, fl
   __shared__ int ri3[kRowBatch], rw0[kRowBatch], rnch[kRowBatch];
   const int n1 = a.n1, n2 = a.n2, n3 = a.n3, r1 = a.r1, r2 = a.r2;
   const int w2 = n2 * r2, nt = a.nA * r2, Dm = a.Dm;
-  const int FP = kRowBatch * n3;
+  const int FP = f3_pitch(kRowBatch, n3), F2P = f2_pitch(n2, r2), DP = dr_pitch(Dm, n3);
   const int c = blockIdx.x;
   if (c >= a.counts[1]) return;
   float* f1 = sm;                // [n1][r1] (without D_1)
-  float* f2 = f1 + n1 * r1;      // [r1][n2][r2]
-  float* pt = f2 + r1 * w2;      // [nA][r2] (D_1 inside, without D_2)
+  float* f2 = f1 + n1 * r1;      // [r1][n2 r2], row pitch F2P
+  float* pt = f2 + r1 * F2P;     // [nA][r2] (D_1 inside, without D_2)
   float* dP = pt + nt;           // [nA][r2]
   float* H = dP + nt;            // [n1][r1]
-  float* dRb = H + n1 * r1;      // [kRowBatch][Dm]
-  float* f3b = dRb + kRowBatch * Dm;  // [r2][kRowBatch n3]
+  float* dRb = H + n1 * r1;      // [kRowBatch][Dm], row pitch DP
+  float* f3b = dRb + kRowBatch * DP;  // [r2][kRowBatch n3], row pitch FP
   const int p = a.plist[c];
   const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
   for (int o = threadIdx.x; o < nt; o += blockDim.x) dP[o] = 0.f;
@@ -547,7 +558,7 @@ __global__ void __launch_bounds__(256, 2) ttm_pair_backward_kernel(TtmArgs a, fl
       // (rows seen more than kChunk times) added after it has landed
       for (int k = 0; k < kb; ++k) {
         const float* src = a.rows + (size_t)rw0[k] * Dm;
-        for (int j = threadIdx.x; j < Dm; j += blockDim.x) cp_async4(dRb + k * Dm + j, src + j);
+        for (int j = threadIdx.x; j < Dm; j += blockDim.x) cp_async4(dRb + k * DP + j, src + j);
       }
       stage_f3(a, ri3, kb, f3b, FP);
       __syncthreads();
@@ -555,16 +566,16 @@ __global__ void __launch_bounds__(256, 2) ttm_pair_backward_kernel(TtmArgs a, fl
         if (rnch[k] <= 1) continue;
         const float* src = a.rows + (size_t)rw0[k] * Dm;
         for (int j = threadIdx.x; j < Dm; j += blockDim.x) {
-          float sacc = dRb[k * Dm + j];
+          float sacc = dRb[k * DP + j];
           for (int w = 1; w < rnch[k]; ++w) sacc += src[(size_t)w * Dm + j];
-          dRb[k * Dm + j] = sacc;
+          dRb[k * DP + j] = sacc;
         }
       }
       __syncthreads();
       BlockGemm g3;  // dF_3 slices: M = r2 (e), N = kb n3 ((k, j3)), K = nA
       g3.M = r2; g3.N = kb * n3; g3.K1 = 1; g3.K2 = a.nA;
       g3.am = 1; g3.ak1 = 0; g3.ak2 = r2;
-      g3.nq = n3; g3.bq = Dm; g3.bn = 1; g3.bk1 = 0; g3.bk2 = n3;
+      g3.nq = n3; g3.bq = DP; g3.bn = 1; g3.bk1 = 0; g3.bk2 = n3;
       const float* D2 = a.D2;
       const int m3 = a.m3;
       block_gemm(pt, dRb, g3, [&](int e, int n, float v) {
@@ -573,7 +584,7 @@ __global__ void __launch_bounds__(256, 2) ttm_pair_backward_kernel(TtmArgs a, fl
       });
       BlockGemm gp;  // dP: M = nA (jA), N = r2 (e), K = (k, j3)
       gp.M = a.nA; gp.N = r2; gp.K1 = kb; gp.K2 = n3;
-      gp.am = n3; gp.ak1 = Dm; gp.ak2 = 1;
+      gp.am = n3; gp.ak1 = DP; gp.ak2 = 1;
       gp.nq = 1 << 30; gp.bq = 0; gp.bn = FP; gp.bk1 = n3; gp.bk2 = 1;
       // every dP entry has one owner thread (the same in every batch)
       block_gemm(dRb, f3b, gp, [&](int jA, int e, float v) { dP[jA * r2 + e] += v; });
@@ -609,7 +620,7 @@ __global__ void __launch_bounds__(256, 2) ttm_pair_backward_kernel(TtmArgs a, fl
   for (int o = threadIdx.x; o < n1 * r1; o += blockDim.x) {
     const int j1 = o / r1, b = o - (o / r1) * r1;
     float acc = 0.f;
-    for (int je = 0; je < w2; ++je) acc = fmaf(dP[j1 * w2 + je], f2[b * w2 + je], acc);
+    for (int je = 0; je < w2; ++je) acc = fmaf(dP[j1 * w2 + je], f2[b * F2P + je], acc);
     H[o] = acc;
   }
   __syncthreads();
@@ -749,13 +760,14 @@ int sm_count() {
 
 // Dynamic shared memory (bytes) of the per-prefix kernels.
 size_t pair_rows_smem(const TtmPlan& P) {
-  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * P.n[1] * P.r[2] + P.n[0] * P.n[1] * P.r[2] +
-                      P.r[2] * kRowBatch * P.n[2]);
+  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * f2_pitch(P.n[1], P.r[2]) +
+                      P.n[0] * P.n[1] * P.r[2] + P.r[2] * f3_pitch(kRowBatch, P.n[2]));
 }
 size_t pair_backward_smem(const TtmPlan& P) {
-  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * P.n[1] * P.r[2] +
-                      2 * P.n[0] * P.n[1] * P.r[2] + P.n[0] * P.r[1] + kRowBatch * P.Dm +
-                      P.r[2] * kRowBatch * P.n[2]);
+  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * f2_pitch(P.n[1], P.r[2]) +
+                      2 * P.n[0] * P.n[1] * P.r[2] + P.n[0] * P.r[1] +
+                      kRowBatch * dr_pitch((int)P.Dm, P.n[2]) +
+                      P.r[2] * f3_pitch(kRowBatch, P.n[2]));
 }
 
 cudaError_t set_attrs() {
