@@ -385,7 +385,7 @@ __device__ void block_gemm(const float* __restrict__ A, const float* __restrict_
   }
 }
 
-constexpr int kRowBatch = 8;  // used rows of a prefix handled together
+constexpr int kRowBatch = 6;  // used rows of a prefix handled together (3 blocks an SM fit)
 
 // f3b[e][k n3 + j3] = F_3[e, i3_k, j3] for the kb rows i3_k of a batch (each
 // (e, k) run of n3 floats is contiguous in F_3); ends with the copies landed
@@ -405,7 +405,7 @@ __device__ void stage_f3(const TtmArgs& a, const int* i3s, int kb, float* f3b, i
 // time as one block GEMM,
 //   row_k[(jA, j3)] = sum_e P[jA, e] F_3[e, i3_k, j3]  ->  rows[upos[v_k]],
 // with M = n1 n2, N = (rows of the batch) n3, K = r2.
-__global__ void __launch_bounds__(256, 2) ttm_pair_rows_kernel(TtmArgs a) {
+__global__ void __launch_bounds__(256, 3) ttm_pair_rows_kernel(TtmArgs a) {
   extern __shared__ float sm[];
   __shared__ int list[256];
   __shared__ int nlist;
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(256) ttm_chunk_sum_kernel(TtmArgs a,
 //   H[j1, b] = sum_{j2, e} G[(j1, j2), e] F_2[b, i2, j2, e]
 //   dF_1[0, i1, j1, b] += D_1[b] H[j1, b];  dD_1[b] += sum_j1 F_1[i1, j1, b] H[j1, b]
 // (dD entries of pruned ranks, D == 0, stay untouched).
-__global__ void __launch_bounds__(256, 2) ttm_pair_backward_kernel(TtmArgs a, float* __restrict__ dF1,
+__global__ void __launch_bounds__(256, 3) ttm_pair_backward_kernel(TtmArgs a, float* __restrict__ dF1,
                                                                 float* __restrict__ dF2,
                                                                 float* __restrict__ dF3,
                                                                 float* __restrict__ dD1,
@@ -778,6 +778,14 @@ cudaError_t set_attrs() {
     if (r == cudaSuccess)
       r = cudaFuncSetAttribute(ttm_pair_backward_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    // all of the unified L1 / shared memory as shared memory, so that several
+    // blocks of these kernels fit an SM
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(ttm_pair_rows_kernel,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(ttm_pair_backward_kernel,
+                               cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     return r;
   }();
   return e;
