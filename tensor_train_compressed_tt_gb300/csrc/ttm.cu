@@ -442,28 +442,21 @@ __global__ void __launch_bounds__(256, 3) ttm_pair_rows_kernel(TtmArgs a) {
   }
 }
 
-// out[b, :] = rows[upos[idx[b]], :], four floats at a time when Dm % 4 == 0.
+// out[b, :] = rows[upos[idx[b]], :]: one warp per index (one lookup of its
+// row), the lanes copying the row four floats at a time when Dm % 4 == 0.
 __global__ void ttm_scatter_kernel(TtmArgs a, const int32_t* __restrict__ idx,
                                    float* __restrict__ out) {
-  if ((a.Dm & 3) == 0) {
-    const int q = a.Dm >> 2;
-    const int64_t n = (int64_t)a.B * q;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-      const int b = (int)(i / q), j = (int)(i - (int64_t)b * q);
-      const int v = idx[b];
-      if (v < 0 || v >= a.V) continue;
-      reinterpret_cast<float4*>(out)[i] =
-          reinterpret_cast<const float4*>(a.rows)[(size_t)a.upos[v] * q + j];
-    }
-  } else {
-    const int64_t n = (int64_t)a.B * a.Dm;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-      const int b = (int)(i / a.Dm), j = (int)(i - (int64_t)b * a.Dm);
-      const int v = idx[b];
-      if (v < 0 || v >= a.V) continue;
-      out[i] = a.rows[(size_t)a.upos[v] * a.Dm + j];
+  const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+  for (int b = blockIdx.x * wpb + (threadIdx.x >> 5); b < a.B; b += gridDim.x * wpb) {
+    const int v = idx[b];
+    if (v < 0 || v >= a.V) continue;
+    const size_t src = (size_t)a.upos[v] * a.Dm, dst = (size_t)b * a.Dm;
+    if ((a.Dm & 3) == 0) {
+      const float4* s4 = reinterpret_cast<const float4*>(a.rows + src);
+      float4* d4 = reinterpret_cast<float4*>(out + dst);
+      for (int j = lane; j < (a.Dm >> 2); j += 32) d4[j] = s4[j];
+    } else {
+      for (int j = lane; j < a.Dm; j += 32) out[dst + j] = a.rows[src + j];
     }
   }
 }
@@ -894,7 +887,8 @@ tt_status tt_ttm_lookup(const tt_plan_t* plan, int64_t B, const int32_t* idx, co
   tt_status s = ttm_prepare(B, idx, a, w, ws, false, st);
   if (s != TT_OK) return s;
   ttm_pair_rows_kernel<<<(unsigned)w.pcap, 256, pair_rows_smem(P), st>>>(a);
-  ttm_scatter_kernel<<<4 * sm_count(), 256, 0, st>>>(a, idx, out);
+  ttm_scatter_kernel<<<(unsigned)std::min<int64_t>((B + 7) / 8, 32 * sm_count()), 256, 0, st>>>(
+      a, idx, out);
   count_launches(2);
   return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
