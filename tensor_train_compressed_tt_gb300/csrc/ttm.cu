@@ -916,7 +916,9 @@ tt_status tt_ttm_lookup_backward(const tt_plan_t* plan, int64_t B, const int32_t
   float* dF3 = P.d == 3 ? dparams + P.core_off[2] : un.sink;
   float* dD1 = dparams + P.diag_off[0];
   float* dD2 = P.d == 3 ? dparams + P.diag_off[1] : un.sink + 32;
-  ttm_chunk_sum_kernel<<<(unsigned)w.unit_cap, 256, 0, st>>>(a, dout);
+  // one thread per float4 column of a row (192 for Dm = 768): no idle lanes
+  const int cthreads = (P.Dm % 4 == 0) ? (int)std::min<int64_t>(256, (P.Dm / 4 + 31) / 32 * 32) : 256;
+  ttm_chunk_sum_kernel<<<(unsigned)w.unit_cap, cthreads, 0, st>>>(a, dout);
   ttm_pair_backward_kernel<<<(unsigned)w.pcap, 256, pair_backward_smem(P), st>>>(a, dF1, dF2, dF3,
                                                                                dD1, dD2);
   count_launches(2);
