@@ -413,7 +413,7 @@ struct BwdArgs {
   float* dDc;  // RP
   float* zero;  // [0, zero_n) set to 0 (scratch the merge backward adds into)
   int zero_n;
-  int use_z;    // read the forward's z' through tm_zs instead of computing x At^T
+  int use_z;    // read the forward's z' through tm_zs instead of computing x A
 };
 
 struct SmemCommon {
@@ -469,7 +469,7 @@ __device__ void tmem_free(uint32_t base) {
 }
 
 // ==========================================================================
-// forward: y = ((x At^T) diag(Dc)) Bt^T per 128-token tile
+// forward: y = ((x A) diag(Dc)) B per tile of up to 128 tokens
 // (F8: x in E4M3, widened in shared memory by the converter warps)
 // ==========================================================================
 template <bool F8>
@@ -697,8 +697,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
 }
 
 // ==========================================================================
-// backward: per 128-token tile
-//   A  z   = x At^T                       (x streamed, 128 features a chunk)
+// backward: per tile of up to 128 tokens
+//   A  z   = x A                          (x streamed, 128 features a chunk;
+//                                          skipped when the forward's z' is kept)
 //   B  dz' = dy Bm^T ; dB^T += dy^T z'    (dy streamed, 128 outputs a chunk)
 //   C  dx  = dz Anr^T ; dA += x^T dz      (x streamed again)
 // with z' = z diag(Dc), dz = dz' diag(Dc), dDc += sum_t z * dz'.
@@ -767,7 +768,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   if (threadIdx.x == 0) TL_STAMP(1, 1);
   volatile int* abort_flag = &S.abort_flag;
   const int nchunks = 2 * p.nN + p.nM;
-  // with the forward's z' kept, phase A (x At^T) is skipped: chunks start at B
+  // with the forward's z' kept, phase A (x A) is skipped: chunks start at B
   const int cfirst = p.use_z ? p.nN : 0;
 
   if (warp == 0) {
@@ -833,7 +834,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       int it = 0, wc = 0, xc = 0, tl = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
-        // A: z = x At^T
+        // A: z = x A
         if (!p.use_z && !wait_bar(&S.z_empty, (tl & 1) ^ 1, abort_flag, 12)) break;
         tc_fence_after();
         for (int c = 0; c < p.nN && !p.use_z; ++c, ++it) {
