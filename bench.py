@@ -332,7 +332,8 @@ def run_ours(args, w):
     if w.ffn:
         up, dn = w.layers
         mod = TTFFN((up.in_modes, up.out_modes, up.ranks), (dn.in_modes, dn.out_modes, dn.ranks),
-                    dt)
+                    dt, reuse_merge=not args.no_reuse,
+                    reuse_z=not (args.no_reuse or args.no_reuse_z))
         params = [torch.from_numpy(synth.pack(l.cores, l.diags)).to(dev) for l in inp0.layers]
         N, M = up.N, dn.M
         n_par = [p.numel() for p in params]
@@ -601,8 +602,8 @@ def run_ours(args, w):
                        "l2": f"{nsets} rotating input/output sets of {set_bytes / 1e6:.1f} MB "
                              f"(> 2x L2 of {l2 / 1e6:.0f} MB)",
                        "parallelism": f"replicas x{world}",
-                       "reuse_merge": (not args.no_reuse) and not w.ffn,
-                       "reuse_z": not (args.no_reuse or args.no_reuse_z) and not w.ffn,
+                       "reuse_merge": not args.no_reuse,
+                       "reuse_z": not (args.no_reuse or args.no_reuse_z) and w.act != "f32",
                        "launch": graph_note},
             "ms_per_step_eager": ms_eager,
             "roofline": roof,

@@ -77,16 +77,18 @@ typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1, TT_DT_E4M3 = 2 } tt_dtype
  * (the forward keeps its intermediate results for the backward pass).  The
  * caller guarantees that a tt_forward call with the same plan, the same
  * params and the same workspace came before, with nothing else using the
- * workspace in between; then tt_backward skips re-merging the cores.  FFN
- * plans ignore it (their two layers share workspace regions). */
+ * workspace in between; then tt_backward skips re-merging the cores.  In an
+ * FFN plan (both descs must carry the same flags) each layer then keeps its
+ * merges in a workspace region of its own. */
 #define TT_REUSE_MERGE 2u
 /* Implies TT_REUSE_MERGE.  On the tensor-core path (bf16 or E4M3 activations)
  * the forward also keeps z' = (x A) diag(D_d) for every token in the
  * workspace (bf16, T x 64 values: 128 more bytes a token, counted by
  * tt_workspace_size), and the backward reads it instead of computing x A
  * again, so it streams x once instead of twice.  The caller guarantees in
- * addition that the backward gets the forward's x and T.  The f32 path and
- * FFN plans ignore it. */
+ * addition that the backward gets the forward's x and T.  The f32 path
+ * ignores it.  In a bf16 FFN plan the backward also takes h = TT_up(x) and
+ * GELU(h) from the forward's workspace instead of recomputing them. */
 #define TT_REUSE_Z 4u
 
 typedef struct tt_desc {

@@ -138,10 +138,14 @@ bool ffn_tc(const tt_plan_s* p) {
   return p->L[0].act == TT_DT_BF16 && tc_supported(p->L[0]) && tc_supported(p->L[1]);
 }
 
+// Without the reuse flags the two layers' scratch shares one region; with
+// them each layer keeps its merges (and z') from the forward in a region of
+// its own.
 size_t ffn_layout(const tt_plan_s* p, int64_t T, FfnLayout* f) {
   const bool tc = ffn_tc(p);
+  const bool keep = (p->L[0].flags & TT_REUSE_MERGE) != 0;
   size_t e0 = layer_layout(p->L[0], T, 256, &f->up, !tc);
-  size_t e1 = layer_layout(p->L[1], T, 256, &f->down, !tc);
+  size_t e1 = layer_layout(p->L[1], T, keep ? align_up(e0, 256) : 256, &f->down, !tc);
   size_t off = align_up(e0 > e1 ? e0 : e1, 256);
   const size_t hb = (size_t)T * p->L[0].M * (tc ? 2 : sizeof(float));
   f->h = off;
@@ -671,10 +675,6 @@ tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out) {
   if (s != TT_OK) return s;
   if (a.M != b.N || a.act != b.act || a.flags != b.flags) return TT_ERR_INVALID_ARG;
   if (a.act == TT_DT_E4M3) return TT_ERR_UNSUPPORTED;  // the FFN pair runs in bf16 or f32
-  // the two layers share workspace regions, so a merge cannot be kept
-  // from the forward to the backward: TT_REUSE_MERGE has no effect here
-  a.flags &= ~(TT_REUSE_MERGE | TT_REUSE_Z);
-  b.flags &= ~(TT_REUSE_MERGE | TT_REUSE_Z);
   tt_plan_s* p = new (std::nothrow) tt_plan_s();
   if (!p) return TT_ERR_INVALID_ARG;
   p->kind = 1;
@@ -819,7 +819,9 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
   float* a = fptr(ws, f.a);
   float* da = fptr(ws, f.da);
   if (ffn_tc(plan)) {
-    if (T > 0) {
+    // h = up(x) and a = GELU(h) are the forward's, still in the workspace,
+    // under TT_REUSE_Z (same x); otherwise they are recomputed here
+    if (T > 0 && !(U.flags & TT_REUSE_Z)) {
       s = layer_forward(U, T, x, TT_DT_BF16, params_up, h, TT_DT_BF16, ws, f.up, st);
       if (s != TT_OK) return s;
       prof_begin(kPhElem, st);

@@ -98,8 +98,10 @@ class TTFFN:
     """y = TT_down(GELU(TT_up(x))), exact erf GELU, both layers through one plan."""
 
     def __init__(self, up: Sequence[Sequence[int]], down: Sequence[Sequence[int]],
-                 dtype: torch.dtype = torch.bfloat16, accumulate: bool = False):
-        flags = ttc.TT_ACCUMULATE if accumulate else 0
+                 dtype: torch.dtype = torch.bfloat16, accumulate: bool = False,
+                 reuse_merge: bool = False, reuse_z: bool = False):
+        flags = (ttc.TT_ACCUMULATE if accumulate else 0) | \
+            (ttc.TT_REUSE_MERGE if reuse_merge else 0) | (ttc.TT_REUSE_Z if reuse_z else 0)
         self.dtype = dtype
         self.up_desc = ttc.make_desc(up[0], up[1], up[2], _DT[dtype], flags)
         self.down_desc = ttc.make_desc(down[0], down[1], down[2], _DT[dtype], flags)

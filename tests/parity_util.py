@@ -69,10 +69,12 @@ def compare(out, ref, tol, label=""):
     return errs
 
 
-def gpu_ffn(w: synth.Workload, inp: synth.WorkloadInputs):
+def gpu_ffn(w: synth.Workload, inp: synth.WorkloadInputs, reuse_z: bool = False):
+    """Forward then backward on one workspace (reuse_z: the backward takes the
+    forward's merges, z', h and GELU(h), as the benchmark's step does)."""
     up, dn = w.layers
     ffn = TTFFN((up.in_modes, up.out_modes, up.ranks), (dn.in_modes, dn.out_modes, dn.ranks),
-                TORCH_DT[w.act])
+                TORCH_DT[w.act], reuse_z=reuse_z)
     pu = torch.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
     pd = torch.from_numpy(synth.pack(inp.layers[1].cores, inp.layers[1].diags)).cuda()
     xd, dyd = to_dev(inp.x, w.act), to_dev(inp.dy, w.act)

@@ -83,7 +83,7 @@ def test_ffn_layout_and_validation(lib):
 
 def test_reuse_z_flag(lib):
     """TT_REUSE_Z adds T x 64 bf16 of kept z' to the tensor-core plans'
-    workspace, implies TT_REUSE_MERGE, and leaves f32 and FFN plans alone."""
+    workspace, implies TT_REUSE_MERGE, and leaves f32 plans alone."""
     shape = synth.WORKLOADS["tt768_bf16"].layers[0]
     for act in (ttc.TT_DT_BF16, ttc.TT_DT_E4M3):
         base = ttc.tt_plan(_desc(shape, act=act))
@@ -96,10 +96,13 @@ def test_reuse_z_flag(lib):
     f32 = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32))
     f32z = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32, flags=ttc.TT_REUSE_Z))
     assert ttc.tt_workspace_size(f32z, 1000) == ttc.tt_workspace_size(f32, 1000)
+    # FFN: with the reuse flags each layer keeps its own region (merges, z')
     up, dn = synth.WORKLOADS["ffn768_3072_bf16"].layers
     a = ttc.tt_ffn_plan(_desc(up), _desc(dn))
     b = ttc.tt_ffn_plan(_desc(up, flags=ttc.TT_REUSE_Z), _desc(dn, flags=ttc.TT_REUSE_Z))
-    assert ttc.tt_workspace_size(a, 4096) == ttc.tt_workspace_size(b, 4096)
+    assert ttc.tt_workspace_size(b, 4096) >= ttc.tt_workspace_size(a, 4096) + 2 * 4096 * 128
+    with pytest.raises(ttc.TTError):   # the two layers must carry the same flags
+        ttc.tt_ffn_plan(_desc(up, flags=ttc.TT_REUSE_Z), _desc(dn))
 
 
 def test_e4m3_plans(lib):

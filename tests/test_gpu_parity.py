@@ -70,10 +70,11 @@ def test_tt1024_4096(T):
     _run("tt1024_4096_bf16", tokens=T)
 
 
-def test_ffn_pair():
+@pytest.mark.parametrize("reuse_z", [False, True])
+def test_ffn_pair(reuse_z):
     w = synth.WORKLOADS["ffn768_3072_bf16"]
     inp = synth.draw(w, seed=0, tokens=1000)
-    out, gu, gd = gpu_ffn(w, inp)
+    out, gu, gd = gpu_ffn(w, inp, reuse_z=reuse_z)
     ref, ru, rd = oracle_ffn(w, inp)
     tol = TOL[w.act]
     assert O.rel_err(out["y"], ref["y"]) <= tol
@@ -317,3 +318,33 @@ def test_reuse_z_matches_recompute(name):
     a0 = g0.cpu().numpy()
     assert O.rel_err(g1.cpu().numpy(), a0) <= 1e-3
     assert O.rel_err(g2.cpu().numpy(), g1.cpu().numpy()) <= 1e-5
+
+
+def test_ffn_reuse_matches_recompute():
+    """FFN with the forward's merges, z', h and GELU(h) kept: y and dx are the
+    recomputing path's bit for bit; dparams agree to rounding; a second
+    backward after one forward gives the same."""
+    import torch as th
+    from tensor_train_compressed_tt_gb300.layer import TTFFN
+    w = synth.WORKLOADS["ffn768_3072_bf16"]
+    inp = synth.draw(w, seed=6, tokens=700)
+    up, dn = w.layers
+    pu = th.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
+    pd = th.from_numpy(synth.pack(inp.layers[1].cores, inp.layers[1].diags)).cuda()
+    x, dy = to_dev(inp.x, w.act), to_dev(inp.dy, w.act)
+    outs = []
+    for keep in (False, True):
+        f = TTFFN((up.in_modes, up.out_modes, up.ranks), (dn.in_modes, dn.out_modes, dn.ranks),
+                  TORCH_DT[w.act], reuse_z=keep)
+        ws = f.workspace(700)
+        y = f.forward(x, pu, pd, ws=ws)
+        dx, gu, gd = f.backward(x, dy, pu, pd, ws=ws)
+        dx2, gu2, gd2 = f.backward(x, dy, pu, pd, ws=ws)
+        th.cuda.synchronize()
+        assert th.equal(dx, dx2)
+        assert O.rel_err(gu2.cpu().numpy(), gu.cpu().numpy()) <= 1e-5
+        outs.append((y, dx, gu, gd))
+    (y0, dx0, gu0, gd0), (y1, dx1, gu1, gd1) = outs
+    assert th.equal(y0, y1) and th.equal(dx0, dx1)
+    assert O.rel_err(gu1.cpu().numpy(), gu0.cpu().numpy()) <= 1e-3
+    assert O.rel_err(gd1.cpu().numpy(), gd0.cpu().numpy()) <= 1e-3
