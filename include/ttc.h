@@ -119,7 +119,8 @@ tt_status tt_default_ranks(int d, const int* in_modes, const int* out_modes, int
  * least 128, middle rank r_d <= 64): E4M3 has no other path. */
 tt_status tt_plan(const tt_desc* desc, tt_plan_t** out);
 
-/* FFN pair y = TT_down(GELU(TT_up(x))) with the exact erf GELU; up's output
+/* FFN pair y = TT_down(GELU(TT_up(x))) with the erf GELU h Phi(h) (erf to
+ * within 1.5e-7, Abramowitz and Stegun 7.1.26); up's output
  * width must equal down's input width and both must use the same act type
  * (F32 or BF16; E4M3 gives TT_ERR_UNSUPPORTED). */
 tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out);

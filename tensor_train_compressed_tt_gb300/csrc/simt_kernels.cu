@@ -168,13 +168,35 @@ __global__ void scale_periodic_kernel(int64_t n, const float* in, const float* s
   }
 }
 
-__device__ __forceinline__ float gelu_f(float h) {
-  return 0.5f * h * (1.f + erff(h * 0.70710678118654752f));
+// The normal CDF Phi(h) = (1 + erf(h / sqrt 2)) / 2 with erf from
+// Abramowitz and Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+//   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
+//   t = 1 / (1 + p x),  x >= 0,  |error| <= 1.5e-7,
+// (odd in x).  exp(-x^2) = exp(-h^2 / 2) is also the density's exponential,
+// so GELU' = Phi + h phi costs one exponential.  The error is about one ulp
+// of fp32 at 1, far below the rounding of a bf16 result.
+struct NormalParts {
+  float Phi, phi;
+};
+__device__ __forceinline__ NormalParts normal_parts(float h) {
+  const float x = fabsf(h) * 0.70710678118654752f;
+  const float t = __frcp_rn(fmaf(0.3275911f, x, 1.f));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  const float e = __expf(-x * x);           // exp(-h^2 / 2)
+  const float q = 0.5f * poly * e;          // (1 - erf(x)) / 2 = Phi(-|h|)
+  NormalParts r;
+  r.Phi = h >= 0.f ? 1.f - q : q;
+  r.phi = 0.39894228040143268f * e;         // exp(-h^2 / 2) / sqrt(2 pi)
+  return r;
 }
+__device__ __forceinline__ float gelu_f(float h) { return h * normal_parts(h).Phi; }
 __device__ __forceinline__ float gelu_grad_f(float h) {
-  float Phi = 0.5f * (1.f + erff(h * 0.70710678118654752f));
-  float phi = 0.39894228040143268f * expf(-0.5f * h * h);
-  return fmaf(h, phi, Phi);
+  const NormalParts n = normal_parts(h);
+  return fmaf(h, n.phi, n.Phi);
 }
 
 template <typename TO>
@@ -190,34 +212,60 @@ __global__ void gelu_bwd_kernel(int64_t n, const float* h, float* da) {
     da[i] *= gelu_grad_f(h[i]);
 }
 
-// bf16 in / bf16 out, 8 elements per thread (n is a multiple of 8)
-__global__ void gelu_fwd_bf16_kernel(int64_t n8, const uint4* __restrict__ h, uint4* a) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    uint4 u = h[i];
-    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&u);
+// bf16 in / bf16 out, 8 elements (one 16-byte word) at a time; each thread
+// issues the loads of kWords words before using any, so that enough bytes
+// are in flight per SM to run at the HBM rate.
+constexpr int kWords = 4;
+
+__device__ __forceinline__ uint4 gelu8(uint4 u) {
+  __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(p[k]);
-      p[k] = __floats2bfloat162_rn(gelu_f(f.x), gelu_f(f.y));
-    }
-    a[i] = u;
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(p[k]);
+    p[k] = __floats2bfloat162_rn(gelu_f(f.x), gelu_f(f.y));
+  }
+  return u;
+}
+__device__ __forceinline__ uint4 gelu_grad8(uint4 uh, uint4 ud) {
+  const __nv_bfloat162* ph = reinterpret_cast<const __nv_bfloat162*>(&uh);
+  __nv_bfloat162* pd = reinterpret_cast<__nv_bfloat162*>(&ud);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 fh = __bfloat1622float2(ph[k]);
+    const float2 fd = __bfloat1622float2(pd[k]);
+    pd[k] = __floats2bfloat162_rn(fd.x * gelu_grad_f(fh.x), fd.y * gelu_grad_f(fh.y));
+  }
+  return ud;
+}
+
+__global__ void gelu_fwd_bf16_kernel(int64_t n8, const uint4* __restrict__ h, uint4* a) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n8;
+       i0 += stride * kWords) {
+    uint4 u[kWords];
+#pragma unroll
+    for (int w = 0; w < kWords; ++w)
+      if (i0 + w * stride < n8) u[w] = h[i0 + w * stride];
+#pragma unroll
+    for (int w = 0; w < kWords; ++w)
+      if (i0 + w * stride < n8) a[i0 + w * stride] = gelu8(u[w]);
   }
 }
 
 __global__ void gelu_bwd_bf16_kernel(int64_t n8, const uint4* __restrict__ h, uint4* da) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    uint4 uh = h[i], ud = da[i];
-    const __nv_bfloat162* ph = reinterpret_cast<const __nv_bfloat162*>(&uh);
-    __nv_bfloat162* pd = reinterpret_cast<__nv_bfloat162*>(&ud);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < n8;
+       i0 += stride * kWords) {
+    uint4 uh[kWords], ud[kWords];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 fh = __bfloat1622float2(ph[k]);
-      const float2 fd = __bfloat1622float2(pd[k]);
-      pd[k] = __floats2bfloat162_rn(fd.x * gelu_grad_f(fh.x), fd.y * gelu_grad_f(fh.y));
-    }
-    da[i] = ud;
+    for (int w = 0; w < kWords; ++w)
+      if (i0 + w * stride < n8) {
+        uh[w] = h[i0 + w * stride];
+        ud[w] = da[i0 + w * stride];
+      }
+#pragma unroll
+    for (int w = 0; w < kWords; ++w)
+      if (i0 + w * stride < n8) da[i0 + w * stride] = gelu_grad8(uh[w], ud[w]);
   }
 }
 
@@ -277,7 +325,7 @@ cudaError_t gelu_fwd(int64_t n, const float* h, void* a, int ta, cudaStream_t st
 cudaError_t gelu_fwd_bf16(int64_t n, const void* h, void* a, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   if (n % 8) return cudaErrorInvalidValue;
-  gelu_fwd_bf16_kernel<<<grid_for(n / 8, 256), 256, 0, st>>>(
+  gelu_fwd_bf16_kernel<<<grid_for((n / 8 + kWords - 1) / kWords, 256), 256, 0, st>>>(
       n / 8, static_cast<const uint4*>(h), static_cast<uint4*>(a));
   count_launches(1);
   return cudaGetLastError();
@@ -286,7 +334,7 @@ cudaError_t gelu_fwd_bf16(int64_t n, const void* h, void* a, cudaStream_t st) {
 cudaError_t gelu_bwd_bf16(int64_t n, const void* h, void* da, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   if (n % 8) return cudaErrorInvalidValue;
-  gelu_bwd_bf16_kernel<<<grid_for(n / 8, 256), 256, 0, st>>>(
+  gelu_bwd_bf16_kernel<<<grid_for((n / 8 + kWords - 1) / kWords, 256), 256, 0, st>>>(
       n / 8, static_cast<const uint4*>(h), static_cast<uint4*>(da));
   count_launches(1);
   return cudaGetLastError();

@@ -348,3 +348,24 @@ def test_ffn_reuse_matches_recompute():
     assert th.equal(y0, y1) and th.equal(dx0, dx1)
     assert O.rel_err(gu1.cpu().numpy(), gu0.cpu().numpy()) <= 1e-3
     assert O.rel_err(gd1.cpu().numpy(), gd0.cpu().numpy()) <= 1e-3
+
+
+@pytest.mark.parametrize("act", ["f32", "bf16"])
+def test_ffn_pair_small(act):
+    """A small FFN pair on both token paths (f32: SIMT GEMMs and the f32 GELU
+    kernels; bf16: tensor-core kernels), 300 tokens, against the oracle."""
+    import dataclasses
+    up = synth.LayerShape((8, 16), (16, 16), (1, 8, 12, 16, 1))
+    dn = synth.LayerShape((16, 16), (8, 16), (1, 16, 12, 8, 1))
+    w = dataclasses.replace(synth.WORKLOADS["ffn768_3072_bf16"], name=f"ffn_small_{act}",
+                            layers=(up, dn), tokens=300, act=act, core_std=0.2)
+    inp = synth.draw(w, seed=8)
+    out, gu, gd = gpu_ffn(w, inp)
+    ref, ru, rd = oracle_ffn(w, inp)
+    tol = TOL[act]
+    assert O.rel_err(out["y"], ref["y"]) <= tol
+    assert O.rel_err(out["dx"], ref["dx"]) <= tol
+    for (a, b) in list(zip(gu[0], ru[0])) + list(zip(gd[0], rd[0])):
+        assert O.rel_err(a, b) <= tol
+    for (a, b) in list(zip(gu[1], ru[1])) + list(zip(gd[1], rd[1])):
+        assert O.rel_err(a, b) <= tol
