@@ -77,7 +77,8 @@ typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1, TT_DT_E4M3 = 2 } tt_dtype
  * (the forward keeps its intermediate results for the backward pass).  The
  * caller guarantees that a tt_forward call with the same plan, the same
  * params and the same workspace came before, with nothing else using the
- * workspace in between; then tt_backward skips re-merging the cores.  In an
+ * workspace in between; then tt_backward skips re-merging the cores (a
+ * backward of T == 0 tokens ignores the flag: a forward of none does no work).  In an
  * FFN plan (both descs must carry the same flags) each layer then keeps its
  * merges in a workspace region of its own. */
 #define TT_REUSE_MERGE 2u

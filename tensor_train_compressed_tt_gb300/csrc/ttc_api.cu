@@ -583,7 +583,8 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   const float* P[kMaxK];
   const bool tc = use_tc(L, tx, tdx) && tdy == tx;
   if (!tc && (tx == TT_DT_E4M3 || tdy == TT_DT_E4M3)) return TT_ERR_UNSUPPORTED;
-  const bool reuse = (L.flags & TT_REUSE_MERGE) != 0;
+  // a forward of no tokens is a no-op that leaves nothing to reuse
+  const bool reuse = (L.flags & TT_REUSE_MERGE) != 0 && T > 0;
   tt_status s = TT_OK;
   if (reuse) {
     chain_ptrs(L, params, ws, w, P);
@@ -596,7 +597,7 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   prof_begin(kPhBwd, st);
   const size_t nz = dq0_zero_floats(L, w);
   if (tc) {
-    const void* zs = (L.flags & TT_REUSE_Z) ? static_cast<char*>(ws) + w.zs : nullptr;
+    const void* zs = (L.flags & TT_REUSE_Z) && reuse ? static_cast<char*>(ws) + w.zs : nullptr;
     s = tc_backward(L, T, x, dy, dx, ws, w.tc, dq_buf(ws, w, 0, 0), nz, tx == TT_DT_E4M3, zs, st);
   } else {
     if (nz) TT_CUDA(cudaMemsetAsync(dq_buf(ws, w, 0, 0), 0, nz * sizeof(float), st));

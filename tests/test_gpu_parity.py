@@ -102,10 +102,13 @@ def test_random_small_shapes(d, act):
         compare(out, ref, TOL[act], f"d={d} {shape} T={T}")
 
 
-def test_zero_tokens_backward_gives_zero_gradients():
+@pytest.mark.parametrize("reuse_z", [False, True])
+def test_zero_tokens_backward_gives_zero_gradients(reuse_z):
+    """T = 0: zero gradients, also with the reuse flags (a forward of no
+    tokens leaves nothing to reuse)."""
     w = synth.WORKLOADS["tt768_bf16"]
     inp = synth.draw(w, seed=0, tokens=1)
-    out = gpu_layer(w.layers[0], w.act, inp.layers[0], inp.x[:0], inp.dy[:0])
+    out = gpu_layer(w.layers[0], w.act, inp.layers[0], inp.x[:0], inp.dy[:0], reuse_z=reuse_z)
     assert out["y"].shape == (0, w.layers[0].M)
     assert all(np.all(g == 0) for g in out["dcores"])
     assert all(np.all(g == 0) for g in out["ddiags"])
