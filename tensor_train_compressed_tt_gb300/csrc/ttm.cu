@@ -280,7 +280,7 @@ __host__ __device__ inline int dr_pitch(int Dm, int n3) {
 // F_2[b, i2, j2, e] into pt (times D_2[e] when scale_d2).  Ends synchronised.
 __device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, float* pt,
                                  bool scale_d1, bool scale_d2) {
-  const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2, w2 = n2 * r2, nt = a.nA * r2;
+  const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2, w2 = n2 * r2;
   const int F2P = f2_pitch(n2, r2);
   const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
   for (int e = threadIdx.x; e < n1 * r1; e += blockDim.x) cp_async4(f1 + e, a.F1 + i1 * n1 * r1 + e);
