@@ -370,21 +370,25 @@ def run_ours(args, w):
     sh = int(stream.cuda_stream)
     wsp, wsn = ws.data_ptr(), ws.numel()
 
-    def step(i, sh=sh):
-        x, dy, y, dx = sets[i % nsets]
+    def run_step(x, dy, y, dx, dps, sh):
+        """One fwd+bwd step through the C ABI on the given device buffers."""
         if w.ffn:
             ttc.check(ttc.tt_ffn_forward(mod.plan, T, x.data_ptr(), params[0].data_ptr(),
                                          params[1].data_ptr(), y.data_ptr(), wsp, wsn, sh))
             ttc.check(ttc.tt_ffn_backward(mod.plan, T, x.data_ptr(), dy.data_ptr(),
                                           params[0].data_ptr(), params[1].data_ptr(),
-                                          dx.data_ptr(), dparams[0].data_ptr(),
-                                          dparams[1].data_ptr(), wsp, wsn, sh))
+                                          dx.data_ptr(), dps[0].data_ptr(),
+                                          dps[1].data_ptr(), wsp, wsn, sh))
         else:
             ttc.check(ttc.tt_forward(mod.plan, T, x.data_ptr(), params[0].data_ptr(),
                                      y.data_ptr(), wsp, wsn, sh))
             ttc.check(ttc.tt_backward(mod.plan, T, x.data_ptr(), dy.data_ptr(),
                                       params[0].data_ptr(), dx.data_ptr(),
-                                      dparams[0].data_ptr(), wsp, wsn, sh))
+                                      dps[0].data_ptr(), wsp, wsn, sh))
+
+    def step(i, sh=sh):
+        x, dy, y, dx = sets[i % nsets]
+        run_step(x, dy, y, dx, dparams, sh)
 
     def barrier():
         if world > 1:
@@ -547,40 +551,67 @@ def run_ours(args, w):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        x, dy, y, dx = sets[0]
-        hx = torch.empty(x.shape, dtype=dt, pin_memory=True)
-        hdy = torch.empty(dy.shape, dtype=dt, pin_memory=True)
-        hy = torch.empty(y.shape, dtype=dto, pin_memory=True)
-        hdx = torch.empty(dx.shape, dtype=dto, pin_memory=True)
+        # Every step copies its inputs in from pinned host memory and its
+        # results (y, dx, dparams) out, as an input pipeline would: the copies
+        # run on their own streams into two alternating device buffer sets, so
+        # step i+1's host->device copy and step i-1's device->host copy
+        # overlap step i's kernels.
+        x0, dy0, y0, dx0 = sets[0]
+        hx = torch.empty(x0.shape, dtype=dt, pin_memory=True)
+        hdy = torch.empty(dy0.shape, dtype=dt, pin_memory=True)
+        hy = torch.empty(y0.shape, dtype=dto, pin_memory=True)
+        hdx = torch.empty(dx0.shape, dtype=dto, pin_memory=True)
         hdp = [torch.empty(n, dtype=torch.float32, pin_memory=True) for n in n_par]
-        hx.copy_(x)
-        hdy.copy_(dy)
+        hx.copy_(x0)
+        hdy.copy_(dy0)
+        dparams2 = [torch.empty(n, device=dev, dtype=torch.float32) for n in n_par]
+        bufs = [sets[0] + (dparams,), sets[1] + (dparams2,)]
+        s_in = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
         Ke = max(3, min(K, 200))
 
-        def e2e_step():
-            x.copy_(hx, non_blocking=True)
-            dy.copy_(hdy, non_blocking=True)
-            step(0)
-            hy.copy_(y, non_blocking=True)
-            hdx.copy_(dx, non_blocking=True)
-            for hp, dp in zip(hdp, dparams):
-                hp.copy_(dp, non_blocking=True)
+        def e2e_step(i):
+            j = i % 2
+            x, dy, y, dx, dps = bufs[j]
+            s_in.wait_event(ev_done[j])          # the step that last read set j is done
+            with torch.cuda.stream(s_in):
+                x.copy_(hx, non_blocking=True)
+                dy.copy_(hdy, non_blocking=True)
+            ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            stream.wait_event(ev_out[j])         # set j's last results are read out
+            run_step(x, dy, y, dx, dps, sh)
+            ev_done[j].record(stream)
+            s_out.wait_event(ev_done[j])
+            with torch.cuda.stream(s_out):
+                hy.copy_(y, non_blocking=True)
+                hdx.copy_(dx, non_blocking=True)
+                for hp, dp in zip(hdp, dps):
+                    hp.copy_(dp, non_blocking=True)
+            ev_out[j].record(s_out)
 
-        for _ in range(3):
-            e2e_step()
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
         barrier()
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for _ in range(Ke):
-            e2e_step()
+        s_in.wait_event(a0)
+        for i in range(Ke):
+            e2e_step(i)
+        stream.wait_event(ev_out[(Ke - 1) % 2])  # the last step's results are on the host
         a1.record(stream)
         barrier()
         ems = all_reduce_scalar(a0.elapsed_time(a1) / Ke, "max", dev)
         e2e = {"value": whole_job_rate(T, world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": int(hx.numel() * ei + hdy.numel() * ei),
                "d2h_bytes_per_step": int(hy.numel() * eo + hdx.numel() * eo + 4 * sum(n_par)),
-               "ms_per_step": ems, "steps": Ke}
+               "ms_per_step": ems, "steps": Ke,
+               "pipeline": "copies on their own streams, two device buffer sets"}
 
     # ---- oracle on the host cores (rank 0, N = 1 only)
     cpu = None
