@@ -265,21 +265,64 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+constexpr int kRowBatch = 5;  // used rows of a prefix handled together (3 blocks an SM fit)
+
 // Shared-memory row pitches chosen against bank conflicts: an odd pitch for
-// the F_2 slice rows (read across rows by the H product) and the staged F_3
-// slices (read across e by the dP product), and a dR row pitch congruent to
-// n3 mod 32, so that consecutive (row, j3) columns fall in consecutive banks.
+// the F_2 slice rows (read across rows by the H product, scalar loads); for
+// tiles read four floats at a time along their rows, a multiple of 4 whose
+// quarter is odd, so that the 16-byte reads of eight consecutive rows fall on
+// eight different bank quads; and a dR row pitch congruent to n3 mod 32, so
+// that consecutive (row, j3) columns fall in consecutive banks.
 __host__ __device__ inline int f2_pitch(int n2, int r2) { return (n2 * r2) | 1; }
-__host__ __device__ inline int f3_pitch(int kb, int n3) { return (kb * n3) | 1; }
+__host__ __device__ inline int pad4(int x) { return (x + 3) & ~3; }
+__host__ __device__ inline int vec_pitch(int x) {
+  const int p = pad4(x);
+  return (p / 4) % 2 ? p : p + 4;
+}
 __host__ __device__ inline int dr_pitch(int Dm, int n3) {
   return Dm + (((n3 - Dm) % 32) + 32) % 32;
+}
+
+// Shared-memory tiles (float offsets, each start a multiple of 4) of the
+// per-prefix kernels:
+//   f1 [n1][r1] | f2 [r1][n2 r2] pitch F2P | pt [n1 n2][PTP] (P; columns
+//   r2 .. K2P-1 zero) | forward: f3 [kRowBatch n3][F3P] (F_3 slices, e along
+//   the rows; columns r2 .. K2P-1 zero) | backward: dP [n1 n2][r2], H [n1][r1],
+//   dR [kRowBatch][DP], f3 [r2][F3P] (e down the rows)
+struct TtmSmem {
+  int F2P, PTP, K2P, F3P, DP;
+  int f1, f2, pt, dP, H, dR, f3, total;
+};
+__host__ __device__ inline TtmSmem ttm_smem(int n1, int n2, int n3, int r1, int r2, int Dm,
+                                            bool backward) {
+  TtmSmem t;
+  t.F2P = f2_pitch(n2, r2);
+  t.K2P = pad4(r2);
+  t.PTP = vec_pitch(r2);
+  t.F3P = backward ? vec_pitch(kRowBatch * n3) : vec_pitch(r2);
+  t.DP = dr_pitch(Dm, n3);
+  int o = 0;
+  t.f1 = o; o = pad4(o + n1 * r1);
+  t.f2 = o; o = pad4(o + r1 * t.F2P);
+  t.pt = o; o = pad4(o + n1 * n2 * t.PTP);
+  t.dP = t.H = t.dR = 0;
+  if (backward) {
+    t.dP = o; o = pad4(o + n1 * n2 * r2);
+    t.H = o; o = pad4(o + n1 * r1);
+    t.dR = o; o = pad4(o + kRowBatch * t.DP);
+    t.f3 = o; o = pad4(o + r2 * t.F3P);
+  } else {
+    t.f3 = o; o = pad4(o + kRowBatch * n3 * t.F3P);
+  }
+  t.total = o;
+  return t;
 }
 
 // Stages F_1[0, i1] (times D_1 when scale_d1) and F_2[:, i2] for prefix p,
 // and computes the pair product P[(j1, j2), e] = sum_b F_1[0, i1, j1, b] D_1[b]
 // F_2[b, i2, j2, e] into pt (times D_2[e] when scale_d2).  Ends synchronised.
 __device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, float* pt,
-                                 bool scale_d1, bool scale_d2) {
+                                 int PTP, bool scale_d1, bool scale_d2) {
   const int n1 = a.n1, n2 = a.n2, r1 = a.r1, r2 = a.r2, w2 = n2 * r2;
   const int F2P = f2_pitch(n2, r2);
   const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
@@ -293,7 +336,8 @@ __device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, 
   // one thread per column (j2, e) of F_2's slice; up to 8 rows j1 at a time
   // in registers, so each loaded F_2 value serves 8 products
   for (int je = threadIdx.x; je < w2; je += blockDim.x) {
-    const int e = je % r2;
+    const int j2 = je / r2, e = je - j2 * r2;
+    float* dst = pt + j2 * PTP + e;          // P[(j1, j2), e] at ((j1 n2 + j2) PTP + e)
     const float d2 = scale_d2 ? a.D2[e] : 1.f;
     for (int j0 = 0; j0 < n1; j0 += 8) {
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -305,7 +349,7 @@ __device__ void ttm_pair_product(const TtmArgs& a, int p, float* f1, float* f2, 
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        if (j0 + i < n1) pt[(j0 + i) * w2 + je] = acc[i] * d2;
+        if (j0 + i < n1) dst[(j0 + i) * n2 * PTP] = acc[i] * d2;
     }
   }
   __syncthreads();
@@ -385,7 +429,68 @@ __device__ void block_gemm(const float* __restrict__ A, const float* __restrict_
   }
 }
 
-constexpr int kRowBatch = 6;  // used rows of a prefix handled together (3 blocks an SM fit)
+
+// block_gemm for operands read four floats at a time along K: K2 a multiple
+// of 4, ak2 = bk2 = 1, every other stride a multiple of 4 and A, B 16-byte
+// aligned.
+template <typename Epi>
+__device__ void block_gemm4(const float* __restrict__ A, const float* __restrict__ B,
+                            const BlockGemm& g, Epi epi) {
+  const int TM = (g.M + 3) >> 2, TN = (g.N + 3) >> 2;
+  for (int t = threadIdx.x; t < TM * TN; t += blockDim.x) {
+    const int mt = t / TN, nt = t - mt * TN;
+    int ao[4], bo[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = mt + i * TM;
+      ao[i] = (m < g.M ? m : 0) * g.am;
+      const int n0 = nt + i * TN, n = n0 < g.N ? n0 : 0;
+      const int q = n / g.nq;
+      bo[i] = q * g.bq + (n - q * g.nq) * g.bn;
+    }
+    float acc[4][4] = {};
+    for (int k1 = 0; k1 < g.K1; ++k1) {
+      const float* a1 = A + k1 * g.ak1;
+      const float* b1 = B + k1 * g.bk1;
+      for (int k2 = 0; k2 < g.K2; k2 += 4) {
+        float4 av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          av[i] = *reinterpret_cast<const float4*>(a1 + ao[i] + k2);
+          bv[i] = *reinterpret_cast<const float4*>(b1 + bo[i] + k2);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float x = acc[i][c];
+            x = fmaf(av[i].x, bv[c].x, x);
+            x = fmaf(av[i].y, bv[c].y, x);
+            x = fmaf(av[i].z, bv[c].z, x);
+            x = fmaf(av[i].w, bv[c].w, x);
+            acc[i][c] = x;
+          }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (mt + i * TM < g.M && nt + c * TN < g.N) epi(mt + i * TM, nt + c * TN, acc[i][c]);
+  }
+}
+
+// f3t[k n3 + j3][e] = F_3[e, i3_k, j3] for the kb rows i3_k of a batch (e
+// along the rows, pitch F3P); ends with the copies landed.
+__device__ void stage_f3t(const TtmArgs& a, const int* i3s, int kb, float* f3t, int F3P) {
+  const int n3 = a.n3, w = kb * n3;
+  for (int o = threadIdx.x; o < a.r2 * w; o += blockDim.x) {
+    const int e = o / w, rem = o - e * w;
+    const int k = rem / n3, j3 = rem - k * n3;
+    cp_async4(f3t + rem * F3P + e, a.F3 + (e * a.m3 + i3s[k]) * n3 + j3);
+  }
+  cp_async_wait_all();
+}
 
 // f3b[e][k n3 + j3] = F_3[e, i3_k, j3] for the kb rows i3_k of a batch (each
 // (e, k) run of n3 floats is contiguous in F_3); ends with the copies landed
@@ -402,42 +507,50 @@ __device__ void stage_f3(const TtmArgs& a, const int* i3s, int kb, float* f3b, i
 
 // Forward, one block of 256 threads per used prefix (slot c): its pair
 // product P (with D_2) in shared memory, then its used rows kRowBatch at a
-// time as one block GEMM,
+// time as one block GEMM read four floats at a time,
 //   row_k[(jA, j3)] = sum_e P[jA, e] F_3[e, i3_k, j3]  ->  rows[upos[v_k]],
-// with M = n1 n2, N = (rows of the batch) n3, K = r2.
+// with M = n1 n2, N = (rows of the batch) n3, K = r2 padded with zeros to a
+// multiple of 4.
 __global__ void __launch_bounds__(256, 3) ttm_pair_rows_kernel(TtmArgs a) {
-  extern __shared__ float sm[];
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
   __shared__ int list[256];
   __shared__ int nlist;
   __shared__ long long rbase[kRowBatch];
-  const int n3 = a.n3, r2 = a.r2, nt = a.nA * r2;
-  const int FP = f3_pitch(kRowBatch, n3);   // row pitch of the staged F_3 slices
+  const int n3 = a.n3, r2 = a.r2;
+  const TtmSmem L = ttm_smem(a.n1, a.n2, n3, a.r1, r2, a.Dm, false);
   const int c = blockIdx.x;
   if (c >= a.counts[1]) return;
-  float* f1 = sm;                           // [n1][r1]
-  float* f2 = f1 + a.n1 * a.r1;             // [r1][n2][r2]
-  float* pt = f2 + a.r1 * f2_pitch(a.n2, r2);  // [nA][r2], D_1 inside, times D_2
-  float* f3b = pt + nt;                     // [r2][kRowBatch n3]: F_3[:, i3_k, :] side by side
+  float* f1 = sm + L.f1;
+  float* f2 = sm + L.f2;
+  float* pt = sm + L.pt;                    // [nA][PTP], D_1 inside, times D_2
+  float* f3t = sm + L.f3;                   // [kRowBatch n3][F3P]: F_3[:, i3_k, j3] along rows
+  // the K padding columns r2 .. K2P-1 of P and of the F_3 slices stay zero
+  const int padw = L.K2P - r2;
+  for (int o = threadIdx.x; o < a.nA * padw; o += blockDim.x)
+    pt[(o / padw) * L.PTP + r2 + o % padw] = 0.f;
+  for (int o = threadIdx.x; o < kRowBatch * n3 * padw; o += blockDim.x)
+    f3t[(o / padw) * L.F3P + r2 + o % padw] = 0.f;
   const int p = a.plist[c];
-  ttm_pair_product(a, p, f1, f2, pt, true, true);
+  ttm_pair_product(a, p, f1, f2, pt, L.PTP, true, true);  // ends synchronised
   for (int base = 0; base < a.m3; base += 256) {
     used_rows(a, p, base, list, &nlist);
     for (int k0 = 0; k0 < nlist; k0 += kRowBatch) {
       const int kb = min(kRowBatch, nlist - k0);
       if ((int)threadIdx.x < kb)
         rbase[threadIdx.x] = (long long)a.upos[p * a.m3 + list[k0 + threadIdx.x]] * a.Dm;
-      stage_f3(a, list + k0, kb, f3b, FP);
+      stage_f3t(a, list + k0, kb, f3t, L.F3P);
       __syncthreads();
       BlockGemm g;
-      g.M = a.nA; g.N = kb * n3; g.K1 = 1; g.K2 = r2;
-      g.am = r2; g.ak1 = 0; g.ak2 = 1;
-      g.nq = 1 << 30; g.bq = 0; g.bn = 1; g.bk1 = 0; g.bk2 = FP;
+      g.M = a.nA; g.N = kb * n3; g.K1 = 1; g.K2 = L.K2P;
+      g.am = L.PTP; g.ak1 = 0; g.ak2 = 1;
+      g.nq = 1 << 30; g.bq = 0; g.bn = L.F3P; g.bk1 = 0; g.bk2 = 1;
       float* rows = a.rows;
-      block_gemm(pt, f3b, g, [&](int jA, int n, float v) {
+      block_gemm4(pt, f3t, g, [&](int jA, int n, float v) {
         const int k = n / n3;
         rows[rbase[k] + jA * n3 + (n - k * n3)] = v;
       });
-      __syncthreads();  // f3b and rbase are refilled next
+      __syncthreads();  // f3t and rbase are refilled next
     }
   }
 }
@@ -516,26 +629,30 @@ __global__ void __launch_bounds__(256, 3) ttm_pair_backward_kernel(TtmArgs a, fl
                                                                 float* __restrict__ dF3,
                                                                 float* __restrict__ dD1,
                                                                 float* __restrict__ dD2) {
-  extern __shared__ float sm[];
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
   __shared__ int list[256];
   __shared__ int nlist;
   __shared__ int ri3[kRowBatch], rw0[kRowBatch], rnch[kRowBatch];
   const int n1 = a.n1, n2 = a.n2, n3 = a.n3, r1 = a.r1, r2 = a.r2;
   const int w2 = n2 * r2, nt = a.nA * r2, Dm = a.Dm;
-  const int FP = f3_pitch(kRowBatch, n3), F2P = f2_pitch(n2, r2), DP = dr_pitch(Dm, n3);
+  const TtmSmem L = ttm_smem(n1, n2, n3, r1, r2, Dm, true);
+  const int FP = L.F3P, F2P = L.F2P, DP = L.DP, PTP = L.PTP;
   const int c = blockIdx.x;
   if (c >= a.counts[1]) return;
-  float* f1 = sm;                // [n1][r1] (without D_1)
-  float* f2 = f1 + n1 * r1;      // [r1][n2 r2], row pitch F2P
-  float* pt = f2 + r1 * F2P;     // [nA][r2] (D_1 inside, without D_2)
-  float* dP = pt + nt;           // [nA][r2]
-  float* H = dP + nt;            // [n1][r1]
-  float* dRb = H + n1 * r1;      // [kRowBatch][Dm], row pitch DP
-  float* f3b = dRb + kRowBatch * DP;  // [r2][kRowBatch n3], row pitch FP
+  float* f1 = sm + L.f1;    // [n1][r1] (without D_1)
+  float* f2 = sm + L.f2;    // [r1][n2 r2], row pitch F2P
+  float* pt = sm + L.pt;    // [nA][PTP] (D_1 inside, without D_2)
+  float* dP = sm + L.dP;    // [nA][r2]
+  float* H = sm + L.H;      // [n1][r1]
+  float* dRb = sm + L.dR;   // [kRowBatch][Dm], row pitch DP
+  float* f3b = sm + L.f3;   // [r2][kRowBatch n3], row pitch FP
+  // the dP product reads four floats at a time along (k, j3) when n3 allows
+  const bool vec = n3 % 4 == 0;
   const int p = a.plist[c];
   const int i1 = p / a.m2, i2 = p - (p / a.m2) * a.m2;
   for (int o = threadIdx.x; o < nt; o += blockDim.x) dP[o] = 0.f;
-  ttm_pair_product(a, p, f1, f2, pt, true, false);
+  ttm_pair_product(a, p, f1, f2, pt, PTP, true, false);
   for (int base = 0; base < a.m3; base += 256) {
     used_rows(a, p, base, list, &nlist);
     for (int k0 = 0; k0 < nlist; k0 += kRowBatch) {
@@ -567,7 +684,7 @@ __global__ void __launch_bounds__(256, 3) ttm_pair_backward_kernel(TtmArgs a, fl
       __syncthreads();
       BlockGemm g3;  // dF_3 slices: M = r2 (e), N = kb n3 ((k, j3)), K = nA
       g3.M = r2; g3.N = kb * n3; g3.K1 = 1; g3.K2 = a.nA;
-      g3.am = 1; g3.ak1 = 0; g3.ak2 = r2;
+      g3.am = 1; g3.ak1 = 0; g3.ak2 = PTP;
       g3.nq = n3; g3.bq = DP; g3.bn = 1; g3.bk1 = 0; g3.bk2 = n3;
       const float* D2 = a.D2;
       const int m3 = a.m3;
@@ -580,14 +697,18 @@ __global__ void __launch_bounds__(256, 3) ttm_pair_backward_kernel(TtmArgs a, fl
       gp.am = n3; gp.ak1 = DP; gp.ak2 = 1;
       gp.nq = 1 << 30; gp.bq = 0; gp.bn = FP; gp.bk1 = n3; gp.bk2 = 1;
       // every dP entry has one owner thread (the same in every batch)
-      block_gemm(dRb, f3b, gp, [&](int jA, int e, float v) { dP[jA * r2 + e] += v; });
+      auto add_dp = [&](int jA, int e, float v) { dP[jA * r2 + e] += v; };
+      if (vec)
+        block_gemm4(dRb, f3b, gp, add_dp);
+      else
+        block_gemm(dRb, f3b, gp, add_dp);
       __syncthreads();  // dRb, f3b and the row metadata are refilled next
     }
   }
   for (int e = threadIdx.x; e < r2; e += blockDim.x) {
     if (a.D2[e] == 0.f) continue;
     float acc = 0.f;
-    for (int jA = 0; jA < a.nA; ++jA) acc = fmaf(pt[jA * r2 + e], dP[jA * r2 + e], acc);
+    for (int jA = 0; jA < a.nA; ++jA) acc = fmaf(pt[jA * PTP + e], dP[jA * r2 + e], acc);
     atomicAdd(dD2 + e, acc);
   }
   __syncthreads();
@@ -753,14 +874,10 @@ int sm_count() {
 
 // Dynamic shared memory (bytes) of the per-prefix kernels.
 size_t pair_rows_smem(const TtmPlan& P) {
-  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * f2_pitch(P.n[1], P.r[2]) +
-                      P.n[0] * P.n[1] * P.r[2] + P.r[2] * f3_pitch(kRowBatch, P.n[2]));
+  return 4 * (size_t)ttm_smem(P.n[0], P.n[1], P.n[2], P.r[1], P.r[2], (int)P.Dm, false).total;
 }
 size_t pair_backward_smem(const TtmPlan& P) {
-  return 4 * (size_t)(P.n[0] * P.r[1] + P.r[1] * f2_pitch(P.n[1], P.r[2]) +
-                      2 * P.n[0] * P.n[1] * P.r[2] + P.n[0] * P.r[1] +
-                      kRowBatch * dr_pitch((int)P.Dm, P.n[2]) +
-                      P.r[2] * f3_pitch(kRowBatch, P.n[2]));
+  return 4 * (size_t)ttm_smem(P.n[0], P.n[1], P.n[2], P.r[1], P.r[2], (int)P.Dm, true).total;
 }
 
 cudaError_t set_attrs() {
