@@ -55,3 +55,20 @@ def test_single_process_is_identity():
     import bench
     assert bench.all_reduce_scalar(3.25, "max") == 3.25
     assert bench.whole_job_rate(100, 1, 1.0) == pytest.approx(1e5)
+
+
+def test_algorithmic_bytes_per_activation_type():
+    """The roofline's algorithmic bytes: x read by both passes, dy read, y and
+    dx written, at the bytes of an input element (E4M3: 1) and of an output
+    element (bf16: 2)."""
+    import bench
+    from tensor_train_compressed_tt_gb300 import synth
+    T, N, M = 16384, 768, 768
+    bf = bench.algorithmic(synth.WORKLOADS["tt768_bf16"], T)
+    f8 = bench.algorithmic(synth.WORKLOADS["tt768_e4m3"], T)
+    assert bf["bytes"] == 2 * T * (3 * N + 2 * M)
+    assert bf["fwd_bytes"] == 2 * T * (N + M) and bf["bwd_bytes"] == 2 * T * (2 * N + M)
+    assert f8["bytes"] == T * (2 * N + M + 2 * (M + N))
+    assert f8["fwd_bytes"] == T * (N + 2 * M) and f8["bwd_bytes"] == T * (N + M + 2 * N)
+    r = 30
+    assert bf["flop"] == f8["flop"] == 6 * T * r * (N + M)
