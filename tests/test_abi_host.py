@@ -223,3 +223,12 @@ def test_ttm_plan_and_argument_errors(lib):
 def test_status_strings(lib):
     for code, name in ttc.STATUS.items():
         assert ttc.tt_status_string(code).startswith(name)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No CPU fallback: without libttc.so the binding raises instead of
+    computing anything."""
+    monkeypatch.setattr(ttc, "LIB_PATH", str(tmp_path / "absent" / "libttc.so"))
+    monkeypatch.setattr(ttc, "_lib", None)   # both restored after the test
+    with pytest.raises(RuntimeError, match="not found"):
+        ttc.lib()
