@@ -55,7 +55,7 @@ extern "C" {
 typedef enum tt_status {
   TT_OK = 0,
   TT_ERR_INVALID_ARG = 1, /* bad descriptor, NULL or misaligned pointer, T < 0 */
-  TT_ERR_UNSUPPORTED = 2, /* valid layer this build has no kernel for */
+  TT_ERR_UNSUPPORTED = 2, /* valid layer the library has no kernel for */
   TT_ERR_WORKSPACE = 3,   /* workspace missing or smaller than tt_workspace_size */
   TT_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   TT_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (device status) */
