@@ -49,8 +49,10 @@ def parse():
                    help="re-merge the cores in the backward instead of reusing the forward's")
     p.add_argument("--no-reuse-z", action="store_true",
                    help="recompute z' = x A diag(D) in the backward instead of keeping the forward's")
-    p.add_argument("--target-seconds", type=float, default=3.0,
-                   help="timed-region length used when --steps is not given")
+    p.add_argument("--oracle-rate", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--target-seconds", type=float, default=1.5,
+                   help="the K-step timed region is repeated until the repeats last this "
+                        "long (and at least 50 times)")
     return p.parse_args()
 
 
@@ -200,7 +202,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -213,8 +215,9 @@ class ClockSampler:
         if self.thread:
             self.thread.join(timeout=2)
         sm, mx, reasons = [], [], set()
+        self.samples = []   # (host time, SM MHz)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -223,6 +226,7 @@ class ClockSampler:
                 mx.append(float(parts[1]))
             except ValueError:
                 continue
+            self.samples.append((t, sm[-1]))
             for nm, v in zip(names, parts[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
@@ -230,7 +234,116 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         sm_sorted = sorted(sm)
         return {"sm_mhz": sm_sorted[len(sm_sorted) // 2], "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "interval_ms": 100}
+
+    def binned(self, windows, ms_per_step, nbins=8):
+        """The timed repeats split into nbins consecutive groups: per group its
+        median ms a step and the median SM clock sampled inside it."""
+        out = []
+        R = len(windows)
+        if R == 0:
+            return out
+        for b in range(nbins):
+            lo, hi = b * R // nbins, (b + 1) * R // nbins
+            if hi <= lo:
+                continue
+            t0, t1 = windows[lo][0], windows[hi - 1][1]
+            mhz = sorted(v for t, v in getattr(self, "samples", []) if t0 <= t <= t1)
+            ms = sorted(ms_per_step[lo:hi])
+            out.append({"repeats": [lo, hi], "ms_per_step": ms[len(ms) // 2],
+                        "sm_mhz": mhz[len(mhz) // 2] if mhz else None, "clock_samples": len(mhz)})
+        return out
+
+
+def timed_repeats(run, K, barrier, stream, min_seconds, min_repeats=50, max_repeats=20000):
+    """Time R repeats of the K-step region, each bracketed by a barrier and a
+    device synchronise on both sides and timed by CUDA events on the launching
+    stream; R >= min_repeats and the repeats together last >= min_seconds.
+    Returns the per-repeat ms a step and the host time window of each repeat."""
+    import torch
+    evs, windows = [], []
+    t_start = time.perf_counter()
+    r = 0
+    while r < max_repeats:
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
+        a.record(stream)
+        for i in range(K):
+            run(i)
+        b.record(stream)
+        barrier()
+        windows.append((h0, time.perf_counter()))
+        evs.append((a, b))
+        r += 1
+        if r >= min_repeats and time.perf_counter() - t_start >= min_seconds:
+            break
+    return [a.elapsed_time(b) / K for a, b in evs], windows
+
+
+def spread(ms):
+    """Median and spread of per-repeat times (ms a step)."""
+    v = sorted(ms)
+    n = len(v)
+    q = lambda f: v[min(n - 1, int(f * (n - 1) + 0.5))]
+    return {"repeats": n, "median": q(0.5), "min": v[0], "p10": q(0.1), "p90": q(0.9),
+            "max": v[-1]}
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() in ("Model name", "Model"):
+                v = ln.split(":", 1)[1].strip()
+                if v and not v.isdigit():
+                    return v
+        vendor = [ln.split(":", 1)[1].strip() for ln in out.splitlines()
+                  if ln.startswith("Vendor ID")]
+        if vendor:
+            return vendor[0]
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def single_thread_rate(workload, sample, budget_s):
+    """The oracle's rate on one host core: a fresh interpreter (exec, not a
+    fork of this process) with every BLAS thread pool set to one thread.
+    Returns (tokens/s, passes, seconds) or None."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+              "BLIS_NUM_THREADS", "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-rate",
+                            "--workload", workload, "--tokens", str(sample),
+                            "--target-seconds", str(budget_s)],
+                           env=env, capture_output=True, text=True, timeout=10 * budget_s + 120)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return d["rate"], d["passes"], d["seconds"]
+    except Exception:
+        return None
+
+
+def oracle_rate_main(args):
+    """--oracle-rate: print the oracle's rate on this process's threads."""
+    from tensor_train_compressed_tt_gb300 import synth
+    if args.workload in synth.TTM_WORKLOADS:
+        rate, n, el = time_ttm_oracle(synth.TTM_WORKLOADS[args.workload], args.tokens,
+                                      args.target_seconds)
+    else:
+        rate, n, el = time_oracle(synth.WORKLOADS[args.workload], args.tokens, args.target_seconds)
+    print(json.dumps({"rate": rate, "passes": n, "seconds": el}), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -434,18 +547,10 @@ def run_ours(args, w):
                 graph.replay()
         else:
             step(i)
-    # choose K for a timed region of about target-seconds when not given
-    if args.steps is None:
-        n = 2 * nsets
-        t0 = time.perf_counter()
-        for i in range(n):
-            run(i)
-        torch.cuda.synchronize(dev)
-        per = (time.perf_counter() - t0) / n
-        K = int(min(100000, max(20, args.target_seconds / max(per, 1e-6))))
-        K = int(all_reduce_scalar(K, "min", dev))
-    else:
-        K = args.steps
+    # K steps a timed region (whole graph replays); the region is repeated
+    # until the repeats last target-seconds (at least 50 of them), and the
+    # median repeat gives ms_per_step
+    K = args.steps if args.steps is not None else 20
     if graph is not None:
         K = -(-K // nsets) * nsets   # whole replays
     barrier()
@@ -456,19 +561,15 @@ def run_ours(args, w):
     clocks.start()
     time.sleep(0.3)
     l0 = ttc.lib().tt_launch_count()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    ev0.record(stream)
-    for i in range(K):
-        run(i)
-    ev1.record(stream)
-    barrier()
-    launches = int(ttc.lib().tt_launch_count() - l0)
+    rep_ms, windows = timed_repeats(run, K, barrier, stream, args.target_seconds)
+    launches = int(ttc.lib().tt_launch_count() - l0) // len(rep_ms)
     if graph is not None:
         launches = K * launches_per_step  # replays launch without the host counter
     clk = clocks.stop()
-    ms = all_reduce_scalar(ev0.elapsed_time(ev1) / K, "max", dev)
+    if clk is not None:
+        clk["by_repeat_group"] = clocks.binned(windows, rep_ms)
+    rep = spread(rep_ms)
+    ms = all_reduce_scalar(rep["median"], "max", dev)
     ttc.check(ttc.tt_get_device_status(sh), "device status after timed region")
 
     # the same steps launched eagerly, for reference
@@ -618,15 +719,22 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         sample = min(T, 2048)
         rate, n, el = time_oracle(w, sample, 10.0)
+        one = single_thread_rate(w.name, min(T, 512), 8.0)
         cpu = {"value": rate, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+               "cpu_model": cpu_model(), "nproc": os.cpu_count(),
                "sample": f"{n} fwd+bwd passes of the fp64 numpy oracle on {sample} of the "
-                         f"{T} tokens ({el:.1f} s)"}
+                         f"{T} tokens ({el:.1f} s)",
+               "single_thread": None if one is None else
+               {"value": one[0], "unit": "tokens/s", "cores": 1,
+                "sample": f"{one[1]} passes on {min(T, 512)} tokens ({one[2]:.1f} s)"}}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.act, "data": "synthetic",
+            "timing": dict(rep, note="ms_per_step is the median over repeats of the K-step "
+                                     "region, max over ranks"),
             "config": {"workload": w.name, "description": w.description, "tokens": T,
                        "modes": [list(L.modes) for L in w.layers],
                        "ranks": [list(L.ranks) for L in w.layers],
@@ -769,35 +877,22 @@ def run_ttm(args, w):
             graphs[i % nsets].replay()
         else:
             step(i)
-    if args.steps is None:
-        t0 = time.perf_counter()
-        for i in range(5):
-            run(i)
-        torch.cuda.synchronize(dev)
-        per = (time.perf_counter() - t0) / 5
-        K = int(min(100000, max(20, args.target_seconds / max(per, 1e-6))))
-        K = int(all_reduce_scalar(K, "min", dev))
-    else:
-        K = args.steps
+    K = args.steps if args.steps is not None else 20
     barrier()
     uuid = getattr(props, "uuid", None)
     clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
     clocks.start()
     time.sleep(0.3)
     l0 = ttc.lib().tt_launch_count()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    ev0.record(stream)
-    for i in range(K):
-        run(i)
-    ev1.record(stream)
-    barrier()
-    launches = int(ttc.lib().tt_launch_count() - l0)
+    rep_ms, windows = timed_repeats(run, K, barrier, stream, args.target_seconds)
+    launches = int(ttc.lib().tt_launch_count() - l0) // len(rep_ms)
     if graphs is not None:
         launches = K * per_step
     clk = clocks.stop()
-    ms = all_reduce_scalar(ev0.elapsed_time(ev1) / K, "max", dev)
+    if clk is not None:
+        clk["by_repeat_group"] = clocks.binned(windows, rep_ms)
+    rep = spread(rep_ms)
+    ms = all_reduce_scalar(rep["median"], "max", dev)
     ttc.check(ttc.tt_get_device_status(sh), "device status after timed region")
 
     # each call on its own (eager), for the roofline of the dominant one
@@ -854,14 +949,21 @@ def run_ttm(args, w):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, el = time_ttm_oracle(w, min(B, 4000), 10.0)
+        one = single_thread_rate(w.name, min(B, 1000), 8.0)
         cpu = {"value": rate, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+               "cpu_model": cpu_model(), "nproc": os.cpu_count(),
                "sample": f"{n} lookup+backward passes of the fp64 numpy oracle on "
-                         f"{min(B, 4000)} of the {B} indices ({el:.1f} s)"}
+                         f"{min(B, 4000)} of the {B} indices ({el:.1f} s)",
+               "single_thread": None if one is None else
+               {"value": one[0], "unit": "tokens/s", "cores": 1,
+                "sample": f"{one[1]} passes on {min(B, 1000)} indices ({one[2]:.1f} s)"}}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "timing": dict(rep, note="ms_per_step is the median over repeats of the K-step "
+                                     "region, max over ranks"),
             "config": {"workload": w.name, "description": w.description, "tokens": B,
                        "row_modes": list(S.row_modes), "col_modes": list(S.col_modes),
                        "ranks": list(S.ranks), "distinct_rows": uniq, "distinct_prefixes": pairs,
@@ -919,6 +1021,9 @@ def run_ttm_reference(args, w):
 
 def main():
     args = parse()
+    if args.oracle_rate:
+        oracle_rate_main(args)
+        return
     from tensor_train_compressed_tt_gb300 import synth
     if args.workload in synth.TTM_WORKLOADS:
         w = synth.TTM_WORKLOADS[args.workload]

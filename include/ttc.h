@@ -24,7 +24,16 @@
  *
  * Conventions for every call:
  *  - All device pointers are plain CUDA device addresses owned by the caller.
- *    The library allocates no device memory; it uses the caller's workspace.
+ *    The library allocates no device memory at run time; it uses the
+ *    caller's workspace.  It does hold a few module-scope device arrays,
+ *    which every GPU that loads the library keeps until the process exits,
+ *    whether or not it calls the functions that use them: the
+ *    tt_forward_noalloc scratch (32 MiB), the status words and the TT-matrix
+ *    lookup's unit constants (a few bytes).
+ *  - Calls on different streams may overlap on the GPU when each has its own
+ *    workspace: everything a call writes (grid-barrier counters included)
+ *    lives in its workspace or its outputs.  Calls that share a workspace
+ *    must be ordered (one stream, or events).
  *  - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
  *    Calls only enqueue work; none synchronises, except
  *    tt_get_device_status.

@@ -3,7 +3,6 @@
 // with the tensor-core kernels (one device translation unit).
 #pragma once
 
-#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 
@@ -19,28 +18,20 @@ constexpr int kGLd = 36;    // GEMM: shared row stride (floats) of a staged [k][
 // GEMM unit dynamic shared memory: A and B tiles, K scales, k-group
 // partials, the folded coldot's operand tile and column sums
 constexpr int kGemmSmem = 2 * kGK * kGLd + kGK + kEngThreads * 16 + 32 * 32 + 32;
-constexpr int kBarSlots = 64;
 constexpr int kMaxSplits = 32;  // split-K partials of one GEMM task
 static_assert(sizeof(EngProgram) <= 30000, "engine program exceeds the kernel parameter limit");
 static_assert(kEngThreads == 512, "k-group shifts assume 512 threads");
-// Grid barrier: one monotonic 64-bit arrival counter per slot (own
-// 128-byte line).  A CTA's own atomicAdd tells it which barrier generation
-// it joined, so the target it waits for needs no extra read and the counter
-// never has to be reset: every launch on a slot uses the same grid size and
-// launches on one slot are serialised by their stream.
-struct EngBarSlot {
-  unsigned long long count;
-  unsigned long long pad[15];
-};
-__device__ EngBarSlot g_eng_bar[kBarSlots];
+// Grid barrier: a monotonic 64-bit arrival counter that belongs to one call
+// (zeroed in stream order before the launch).  A CTA's own atomicAdd tells it
+// which barrier generation it joined, so the target it waits for needs no
+// extra read.
 
 // Bounded: false if it timed out (error recorded).  Data produced in one
 // phase and read in a later one is read with L2-only loads (__ldcg), so no
 // stale L1 line can be observed across a barrier.
-__device__ bool eng_grid_barrier(unsigned slot, unsigned nblocks, int* failed) {
+__device__ bool eng_grid_barrier(unsigned long long* cnt, unsigned nblocks, int* failed) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned long long* cnt = &g_eng_bar[slot].count;
     __threadfence();
     const unsigned long long old = atomicAdd(cnt, 1ull);
     const unsigned long long target = (old / nblocks + 1) * nblocks;
@@ -622,7 +613,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
 #endif
     }
     if (threadIdx.x == 0) TL_STAMP(p.nphases == 1 ? 2 : 3, 1 + 2 * ph);
-    if (ph + 1 < p.nphases && !eng_grid_barrier(p.slot, gridDim.x, &failed)) return;
+    if (ph + 1 < p.nphases && !eng_grid_barrier(p.bar, gridDim.x, &failed)) return;
     if (threadIdx.x == 0) TL_STAMP(p.nphases == 1 ? 2 : 3, 2 + 2 * ph);
   }
 }
@@ -631,16 +622,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
 
 // ---- host side -------------------------------------------------------------
 
-int eng_sm_count() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    sms = n > 0 ? n : 1;
-  }
-  return sms;
-}
+int eng_sm_count() { return device_sms(); }
 
 void EngBuilder::begin_phase() {
   if (p.nphases > 0) balance(eng_sm_count());
@@ -871,22 +853,21 @@ static void eng_dump(const EngProgram& p) {
 }
 
 cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
-  static std::atomic<unsigned> next_slot{0};
-  static int grid = 0;
-  if (!grid) {
-    int dev = 0, sms = 0, per = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaFuncSetAttribute(eng_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kEngSmem * sizeof(float))) != cudaSuccess)
-      return cudaErrorLaunchFailure;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, eng_kernel, kEngThreads,
-                                                  kEngSmem * sizeof(float));
-    grid = sms * (per > 0 ? 1 : 0);
-    if (grid <= 0) return cudaErrorLaunchFailure;
-  }
+  // the shared-memory opt-in and the occupancy check, once per device
+  static PerDevice setup;
+  cudaError_t se = setup.get([] {
+    int per = 0;
+    cudaError_t e = cudaFuncSetAttribute(eng_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kEngSmem * sizeof(float)));
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, eng_kernel, kEngThreads,
+                                                        kEngSmem * sizeof(float));
+    return e != cudaSuccess ? e : per > 0 ? cudaSuccess : cudaErrorLaunchFailure;
+  });
+  if (se != cudaSuccess) return se;
+  const int grid = device_sms();
+  if (prog.nphases > 1 && !prog.bar) return cudaErrorInvalidValue;
   EngProgram p = prog;
-  p.slot = next_slot.fetch_add(1) % kBarSlots;
   for (int ph = 0; ph < p.nphases; ++ph) {  // costliest units first, stable
     const int a = p.phase_begin[ph], b = p.phase_begin[ph + 1];
     for (int i = a; i < b; ++i) p.order[i] = (unsigned char)i;

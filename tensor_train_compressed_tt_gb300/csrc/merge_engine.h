@@ -89,7 +89,12 @@ constexpr int kEngMaxPhases = 8;
 
 struct alignas(16) EngProgram {
   int ntasks = 0, nphases = 0;
-  unsigned slot = 0;  // grid-barrier slot (set by eng_launch)
+  // Grid-barrier arrival counter of this call (a 64-bit word on its own
+  // 256-byte line of the caller's workspace).  A program of more than one
+  // phase needs it, zeroed in stream order before the launch; every call
+  // has its own, so calls on different streams with different workspaces
+  // never share one.
+  unsigned long long* bar = nullptr;
   int rd = 0;         // middle rank of dmid
   const float* dmid = nullptr;  // D_d whose compaction map the gather / pack
                                 // epilogues use (set by eng_launch)
@@ -131,7 +136,9 @@ void eng_dd_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* 
 void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
                      float* dA, float* dB, float* dDout, bool acc);
 
-// Launch (cooperative, one CTA per SM).  Returns cudaSuccess or the error.
+// Launch (cooperative when it has more than one phase: one CTA per SM).
+// Returns cudaSuccess or the error; cudaErrorInvalidValue for a program of
+// several phases without a barrier counter.
 cudaError_t eng_launch(const EngProgram& p, cudaStream_t st);
 
 // Bytes of split-K partial scratch a GEMM of this shape may use.

@@ -1265,30 +1265,20 @@ constexpr size_t kSmemBwd = NSTAGE_B * STAGE + BOX + NEPI * 2 * STG + sizeof(Sme
 static_assert(kSmemFwd <= 227 * 1024, "forward smem");
 static_assert(kSmemBwd <= 227 * 1024, "backward smem");
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int num_sms() { return device_sms(); }
 
 cudaError_t set_smem_attrs() {
-  static cudaError_t err = cudaErrorUnknown;
-  static std::once_flag once;
-  std::call_once(once, [] {
+  static PerDevice once;
+  return once.get([] {
     const std::pair<const void*, size_t> k[4] = {
         {(const void*)tt_fwd_kernel<false>, kSmemFwd}, {(const void*)tt_fwd_kernel<true>, kSmemFwd},
         {(const void*)tt_bwd_kernel<false>, kSmemBwd}, {(const void*)tt_bwd_kernel<true>, kSmemBwd}};
-    err = cudaSuccess;
+    cudaError_t err = cudaSuccess;
     for (int i = 0; i < 4 && err == cudaSuccess; ++i)
       err = cudaFuncSetAttribute(k[i].first, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)k[i].second);
+    return err;
   });
-  return err;
 }
 
 // Tokens per tile: the fewest tiles of at most TILE tokens that give every
@@ -1528,6 +1518,9 @@ extern "C" int ttc_probe_engine(int phases, int ntasks, int units_if_empty, long
     }
   }
   b.end();
+  // the barrier counter: one zeroed line past the operands
+  b.p.bar = reinterpret_cast<unsigned long long*>(f + 8 * (m * k + k * n + m * n) + 64 * ntasks * m * n);
+  cudaMemsetAsync(b.p.bar, 0, 256, g_probe_stream);
   return (int)eng_launch(b.p, g_probe_stream);
 }
 

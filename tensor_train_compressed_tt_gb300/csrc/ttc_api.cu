@@ -84,6 +84,8 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
 struct WsLayout {
   size_t P[kMaxK] = {};  // merged chain prefixes (floats), 0 where aliased to params
   size_t dA = 0, dB = 0;
+  size_t bar = 0;        // grid-barrier counter of the merge programs (one 256-byte line,
+                         // directly before q: the backward token pass zeroes both at once)
   size_t q = 0;          // reverse-chain dQ buffers: step j of side s at q + (2j + s) * qstride
   size_t qstride = 0;    // floats between dQ buffers
   size_t part[4] = {};   // split-K partials (input side 0/1, output 2/3)
@@ -115,6 +117,7 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   w->dA = take((size_t)L.N * L.rd * sizeof(float));
   w->dB = take((size_t)L.rd * L.M * sizeof(float));
   w->qstride = align_up(qmax * sizeof(float), 256) / sizeof(float);
+  w->bar = take(256);
   w->q = take(2 * (TT_MAX_D - 1) * w->qstride * sizeof(float));
   for (int i = 0; i < 4; ++i) w->part[i] = take(pmax * sizeof(float));
   w->part_cap = pmax;
@@ -236,6 +239,8 @@ tt_status run_merge_forward_gemm(const LayerPlan& L, const float* params, void* 
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
   if (b.p.nphases == 0) return TT_OK;
+  b.p.bar = reinterpret_cast<unsigned long long*>(fptr(ws, w.bar));
+  if (b.p.nphases > 1) TT_CUDA(cudaMemsetAsync(b.p.bar, 0, 256, st));
   TT_CUDA(eng_launch(b.p, st));
   return TT_OK;
 }
@@ -307,6 +312,13 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
 // slices that later phases add into (unless accumulating).
 size_t dq0_zero_floats(const LayerPlan& L, const WsLayout& w) {
   return L.d >= 3 ? 2 * w.qstride : 0;
+}
+
+// What the backward token pass zeroes on its way: the merge program's
+// grid-barrier line and the step-0 dQ scratch right after it.
+float* bwd_zero_ptr(void* ws, const WsLayout& w) { return fptr(ws, w.bar); }
+size_t bwd_zero_floats(const LayerPlan& L, const WsLayout& w) {
+  return (w.q - w.bar) / sizeof(float) + dq0_zero_floats(L, w);
 }
 
 tt_status run_merge_backward(const LayerPlan& L, const float* params, const float** P,
@@ -467,6 +479,8 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
   if (b.p.nphases == 0) return TT_OK;
+  // zeroed by the backward token pass that comes before in the stream
+  b.p.bar = reinterpret_cast<unsigned long long*>(fptr(ws, w.bar));
   TT_CUDA(eng_launch(b.p, st));
   return TT_OK;
 }
@@ -595,12 +609,12 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
     if (s != TT_OK) return s;
   }
   prof_begin(kPhBwd, st);
-  const size_t nz = dq0_zero_floats(L, w);
+  const size_t nz = bwd_zero_floats(L, w);
   if (tc) {
     const void* zs = (L.flags & TT_REUSE_Z) && reuse ? static_cast<char*>(ws) + w.zs : nullptr;
-    s = tc_backward(L, T, x, dy, dx, ws, w.tc, dq_buf(ws, w, 0, 0), nz, tx == TT_DT_E4M3, zs, st);
+    s = tc_backward(L, T, x, dy, dx, ws, w.tc, bwd_zero_ptr(ws, w), nz, tx == TT_DT_E4M3, zs, st);
   } else {
-    if (nz) TT_CUDA(cudaMemsetAsync(dq_buf(ws, w, 0, 0), 0, nz * sizeof(float), st));
+    TT_CUDA(cudaMemsetAsync(bwd_zero_ptr(ws, w), 0, nz * sizeof(float), st));
     s = simt_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
   }
   prof_end(kPhBwd, st);

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "ttc.h"
 
 namespace ttc {
@@ -53,6 +55,36 @@ struct tt_plan_s {
 };
 
 namespace ttc {
+
+// ---- per-device set-up ------------------------------------------------------
+// Kernel attributes (the shared-memory opt-in, the carveout) and occupancy
+// figures belong to one device; a process that drives several GPUs needs them
+// once on each.  A PerDevice runs its set-up step once for every device it is
+// used on, with that device current, and keeps the result.
+constexpr int kMaxDevices = 64;
+class PerDevice {
+ public:
+  template <typename F>
+  cudaError_t get(F&& fn) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+      return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!done_[dev]) {
+      res_[dev] = fn();
+      done_[dev] = true;
+    }
+    return res_[dev];
+  }
+
+ private:
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+  cudaError_t res_[kMaxDevices] = {};
+};
+// Streaming multiprocessors of the current device (cached per device; 1 if
+// the query fails).
+int device_sms();
 
 // ---- device status word (one per GPU, module-scope device variable) -------
 struct DeviceStatus {

@@ -881,7 +881,8 @@ size_t pair_backward_smem(const TtmPlan& P) {
 }
 
 cudaError_t set_attrs() {
-  static cudaError_t e = [] {
+  static PerDevice once;
+  return once.get([] {
     const int big = kMaxSmemFloats * 4;
     cudaError_t r = cudaFuncSetAttribute(ttm_pair_rows_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, big);
@@ -897,8 +898,7 @@ cudaError_t set_attrs() {
       r = cudaFuncSetAttribute(ttm_pair_backward_kernel,
                                cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     return r;
-  }();
-  return e;
+  });
 }
 
 #define TTM_CUDA(call)                                 \

@@ -186,6 +186,31 @@ def test_argument_errors_return_before_any_launch(lib):
     assert ttc.tt_rank_update(ffn, fake, fake, 0.1, 0.1, 0.1) == 1
 
 
+def test_noalloc_rejections_before_any_launch(lib):
+    """tt_forward_noalloc checks everything on the host first: a layer whose
+    scratch would exceed the library's fixed 32 MiB array gets
+    TT_ERR_WORKSPACE, an FFN plan or T < 0 TT_ERR_INVALID_ARG, T == 0 is a
+    no-op; none of these touches a device."""
+    limit = 32 << 20
+    fake = 1 << 40
+    shape = synth.WORKLOADS["tt1024_4096_bf16"].layers[0]
+    for act, flags in ((ttc.TT_DT_BF16, ttc.TT_REUSE_Z), (ttc.TT_DT_F32, 0)):
+        plan = ttc.tt_plan(_desc(shape, act=act, flags=flags))
+        T = 1024
+        while ttc.tt_workspace_size(plan, T) <= limit:
+            T *= 2
+        assert ttc.tt_forward_noalloc(plan, T, fake, fake, fake) == 3
+        assert ttc.tt_workspace_size(plan, 257) <= limit
+    plan = ttc.tt_plan(_desc(shape))
+    assert ttc.tt_forward_noalloc(plan, 0, 0, 0, 0) == 0
+    assert ttc.tt_forward_noalloc(plan, -1, fake, fake, fake) == 1
+    w = synth.WORKLOADS["ffn768_3072_bf16"]
+    ffn = ttc.tt_ffn_plan(_desc(w.layers[0]), _desc(w.layers[1]))
+    assert ttc.tt_forward_noalloc(ffn, 64, fake, fake, fake) == 1
+    table = ttc.tt_ttm_plan(ttc.make_ttm_desc((32, 32, 32), (8, 8, 12), (1, 30, 30, 1)))
+    assert ttc.tt_forward_noalloc(table, 64, fake, fake, fake) == 1
+
+
 def test_ttm_plan_and_argument_errors(lib):
     plan = ttc.tt_ttm_plan(ttc.make_ttm_desc((32, 32, 32), (8, 8, 12), (1, 30, 30, 1)))
     core, diag, n = ttc.tt_param_layout(plan)

@@ -59,21 +59,30 @@ def test_pruned_equals_truncated(name):
     tc, td, _ = O.truncate(inp.layers[0].cores, inp.layers[0].diags)
     tshape = synth.LayerShape(shape.in_modes, shape.out_modes,
                               tuple([1] + [len(e) for e in td] + [1]))
+    # the truncated layer really is smaller: every link keeps nnz(D_k) ranks
+    assert all(len(e) == np.count_nonzero(f) < f.size
+               for e, f in zip(td, inp.layers[0].diags) if f.size > 1)
     out_t = gpu_layer(tshape, w.act, synth.LayerInputs(tc, td), inp.x, inp.dy)
     out_z = gpu_layer(shape, w.act, inp.layers[0], inp.x, inp.dy)
     assert O.rel_err(out_z["y"], out_t["y"]) <= TOL[w.act]
     assert O.rel_err(out_z["dx"], out_t["dx"]) <= TOL[w.act]
 
 
-@pytest.mark.parametrize("T", [4096])
-def test_tt1024_4096(T):
-    _run("tt1024_4096_bf16", tokens=T)
+@pytest.mark.parametrize("T,reuse_z", [(4096, False), (16384, False), (32768, True)])
+def test_tt1024_4096(T, reuse_z):
+    """The 1024 -> 4096 rank-64 layer at each token count of its sweep, every
+    output tensor (y, dx, each dG_k and dD_k) element by element against the
+    oracle; 32768 tokens in the benchmark's launch configuration (kept z')."""
+    _run("tt1024_4096_bf16", tokens=T, reuse_z=reuse_z)
 
 
-@pytest.mark.parametrize("reuse_z", [False, True])
-def test_ffn_pair(reuse_z):
+@pytest.mark.parametrize("reuse_z,T", [(False, 1000), (True, 1000), (True, 16384)])
+def test_ffn_pair(reuse_z, T):
+    """The FFN pair against the oracle: y, dx and every dG_k, dD_k of both
+    layers; 16384 tokens is the configured size, in the benchmark's launch
+    configuration (the backward reusing the forward's work)."""
     w = synth.WORKLOADS["ffn768_3072_bf16"]
-    inp = synth.draw(w, seed=0, tokens=1000)
+    inp = synth.draw(w, seed=0, tokens=T)
     out, gu, gd = gpu_ffn(w, inp, reuse_z=reuse_z)
     ref, ru, rd = oracle_ffn(w, inp)
     tol = TOL[w.act]

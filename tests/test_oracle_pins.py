@@ -174,6 +174,12 @@ def test_zeroed_diagonal_equals_truncated_tt(rng, d):
         if e.size > 1:
             e[rng.permutation(e.size)[: e.size // 2]] = 0.0
     tc, td, kept = O.truncate(cores, diags)
+    # the truncation really removed the zeroed slices: every link keeps
+    # exactly nnz(D_k) ranks, and at least one link lost some
+    for k, e in enumerate(diags):
+        assert len(kept[k]) == np.count_nonzero(e) == td[k].size
+        assert tc[k].shape[2] == tc[k + 1].shape[0] == np.count_nonzero(e)
+    assert sum(len(kk) for kk in kept) < sum(e.size for e in diags)
     x = rng.standard_normal((4, shape.N))
     dy = rng.standard_normal((4, shape.M))
     y = O.chained_forward(cores, diags, d, x)
@@ -203,6 +209,53 @@ def test_zeroed_diagonal_equals_truncated_tt(rng, d):
     for k in range(K - 1):
         assert np.all(dE[k][diags[k] == 0.0] == 0.0)
         assert O.rel_err(dE[k][kept[k]], dEt[k]) < 1e-12
+
+
+def test_truncate_hand_built_example():
+    """A hand-built order-2 chain (d = 1: cores (1,2,3), (3,2,1)) with D_1 =
+    (2, 0, -1): the truncation keeps ranks 0 and 2 only, i.e. columns 0 and 2
+    of G_1's last axis, rows 0 and 2 of G_2's first axis, and D_1 = (2, -1)."""
+    G1 = np.arange(6, dtype=np.float64).reshape(1, 2, 3) + 1.0      # values 1..6
+    G2 = np.arange(6, dtype=np.float64).reshape(3, 2, 1) + 10.0     # values 10..15
+    D1 = np.array([2.0, 0.0, -1.0])
+    tc, td, kept = O.truncate([G1, G2], [D1])
+    assert kept[0].tolist() == [0, 2]
+    assert td[0].tolist() == [2.0, -1.0]
+    assert tc[0].shape == (1, 2, 2) and tc[1].shape == (2, 2, 1)
+    # G1[0, s, :] = (1,2,3) / (4,5,6) -> keep columns 0 and 2
+    assert tc[0][0].tolist() == [[1.0, 3.0], [4.0, 6.0]]
+    # G2[:, s, 0] rows 0 and 2: (10, 11) and (14, 15)
+    assert tc[1][:, :, 0].tolist() == [[10.0, 11.0], [14.0, 15.0]]
+    # the layer itself: W[i, j] = sum_a G1[0,j,a] D1[a] G2[a,i,0], written out
+    W = np.array([[sum(G1[0, j, a] * D1[a] * G2[a, i, 0] for a in range(3)) for j in range(2)]
+                  for i in range(2)])
+    assert np.array_equal(O.dense_weight(tc, td, 1), W)
+    # an all-zero link truncates to rank 0 on that link
+    tz, dz, kz = O.truncate([G1, G2], [np.zeros(3)])
+    assert kz[0].size == 0 and tz[0].shape == (1, 2, 0) and tz[1].shape == (0, 2, 1)
+
+
+def test_rel_err_hand_values():
+    """The comparison metric every parity test uses: ||out - ref|| / ||ref||
+    (Frobenius, over all elements), checked on values computed by hand."""
+    # difference (0, 1) against a reference of norm sqrt 2
+    assert O.rel_err([1.0, 2.0], [1.0, 1.0]) == pytest.approx(1.0 / np.sqrt(2.0), rel=1e-15)
+    # divides by the reference's norm, not the output's: |2 - 1| / |1| = 1 (not 1/2)
+    assert O.rel_err([2.0, 0.0], [1.0, 0.0]) == 1.0
+    # the difference, not the sum: equal tensors give exactly 0
+    assert O.rel_err([1.0, -3.0], [1.0, -3.0]) == 0.0
+    # a 2-norm over all elements, not a max: (1,1,1,1) vs (0,0,0,2) -> 2 / 2
+    assert O.rel_err([1.0, 1.0, 1.0, 1.0], [0.0, 0.0, 0.0, 2.0]) == 1.0
+    # every element of a 3-D tensor counts: one 3-4-5 difference in 24 entries
+    ref = np.zeros((2, 3, 4))
+    ref[1, 2, 3] = 5.0
+    out = ref.copy()
+    out[0, 0, 0] = 3.0
+    out[1, 1, 1] = 4.0
+    assert O.rel_err(out, ref) == 1.0
+    # zero reference: 0 for a zero output, infinity otherwise
+    assert O.rel_err([0.0, 0.0], [0.0, 0.0]) == 0.0
+    assert O.rel_err([0.0, 1e-30], [0.0, 0.0]) == float("inf")
 
 
 def test_all_zero_link_removes_layer(rng):
