@@ -1463,6 +1463,7 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
 }  // namespace ttc
 
 #include "merge_engine.cuh"
+#include "ffn_fused.cuh"
 
 #ifdef TTC_TIMELINE
 extern "C" int ttc_timeline_read(void* host, size_t bytes) {

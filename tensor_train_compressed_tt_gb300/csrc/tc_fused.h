@@ -44,4 +44,27 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
                       void* ws, size_t ws_off, float* zero, size_t zero_n, bool f8,
                       const void* zs, cudaStream_t st);
 
+// ---- fused FFN pair (ffn_fused.cuh) -------------------------------------------
+// True when both layers run on the tensor-core kernels and up's output width
+// is down's input width.
+bool ffn_tc_supported(const LayerPlan& U, const LayerPlan& D);
+
+// y = TT_down(GELU(TT_up(x))) for T tokens, x and y bf16, with the hidden
+// activations kept on the SM; each layer's packed operands are in the
+// workspace at off1 / off2.  With zs1 and zs2 (T x 64 bf16 each) z1' and z2'
+// are kept there for the backward.  y may be null when zs1 and zs2 are given:
+// then only z1' and z2' are computed.
+tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x, void* y,
+                         void* ws, size_t off1, size_t off2, void* zs1, void* zs2,
+                         cudaStream_t st);
+
+// dx and both layers' token sums (dAc, dBc, dDc, zeroed beforehand) for T
+// tokens from x, dy and the forward's z1', z2' (zs1, zs2); h, GELU(h), da and
+// dh are recomputed per hidden chunk on the SM.  zero1[0, n1) and zero2[0, n2)
+// are set to 0 on the way (the merge backward's scratch), also when T == 0.
+tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x,
+                          const void* dy, void* dx, void* ws, size_t off1, size_t off2,
+                          const void* zs1, const void* zs2, float* zero1, size_t n1,
+                          float* zero2, size_t n2, cudaStream_t st);
+
 }  // namespace ttc

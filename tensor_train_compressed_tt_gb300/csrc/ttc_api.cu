@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -99,7 +100,7 @@ struct WsLayout {
 size_t chain_len(const LayerPlan& L, int k) { return (size_t)L.U[k] * L.r[k + 1]; }
 
 size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
-                    bool simt_tokens = false) {
+                    bool simt_tokens = false, bool keep_z = false) {
   size_t off = align_up(base, 256);
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -125,7 +126,7 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   w->z = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->dzp = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->tc = take(tc_operand_bytes(L));
-  w->zs = take(tc && (L.flags & TT_REUSE_Z) ? (size_t)T * 64 * 2 : 0);
+  w->zs = take(tc && (keep_z || (L.flags & TT_REUSE_Z)) ? (size_t)T * 64 * 2 : 0);
   w->end = off;
   return off;
 }
@@ -141,10 +142,31 @@ bool ffn_tc(const tt_plan_s* p) {
   return p->L[0].act == TT_DT_BF16 && tc_supported(p->L[0]) && tc_supported(p->L[1]);
 }
 
+// A bf16 FFN pair whose layers both fit the tensor-core kernels runs fused:
+// h, GELU(h), da and dh never leave the SM.  TTC_FFN_UNFUSED=1 selects the
+// layer-by-layer path instead (a measurement aid).
+bool ffn_fused(const tt_plan_s* p) {
+  static int off = -1;
+  if (off < 0) {
+    const char* e = getenv("TTC_FFN_UNFUSED");
+    off = (e && e[0] && e[0] != '0') ? 1 : 0;
+  }
+  return !off && ffn_tc(p) && ffn_tc_supported(p->L[0], p->L[1]);
+}
+
 // Without the reuse flags the two layers' scratch shares one region; with
 // them each layer keeps its merges (and z') from the forward in a region of
 // its own.
 size_t ffn_layout(const tt_plan_s* p, int64_t T, FfnLayout* f) {
+  if (ffn_fused(p)) {
+    // both layers' operands at once, and their z' (T x 64 bf16 each), which
+    // the backward reads: no T x hidden buffers
+    size_t e0 = layer_layout(p->L[0], T, 256, &f->up, false, true);
+    size_t e1 = layer_layout(p->L[1], T, align_up(e0, 256), &f->down, false, true);
+    f->h = f->a = f->da = 0;
+    f->end = align_up(e1, 256);
+    return f->end;
+  }
   const bool tc = ffn_tc(p);
   const bool keep = (p->L[0].flags & TT_REUSE_MERGE) != 0;
   size_t e0 = layer_layout(p->L[0], T, 256, &f->up, !tc);
@@ -796,6 +818,22 @@ tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,
   const LayerPlan& D = plan->L[1];
   float* h = fptr(ws, f.h);
   float* a = fptr(ws, f.a);
+  if (ffn_fused(plan)) {
+    const bool reuse = (U.flags & TT_REUSE_MERGE) != 0;
+    const float* P[kMaxK];
+    prof_begin(kPhMerge, st);
+    s = run_merge_forward(U, params_up, ws, f.up, P, true, reuse, st);
+    if (s == TT_OK) s = run_merge_forward(D, params_down, ws, f.down, P, true, reuse, st);
+    prof_end(kPhMerge, st);
+    if (s != TT_OK) return s;
+    const bool keep = (U.flags & TT_REUSE_Z) != 0;
+    prof_begin(kPhFwd, st);
+    s = ffn_tc_forward(U, D, T, x, y, ws, f.up.tc, f.down.tc,
+                       keep ? static_cast<char*>(ws) + f.up.zs : nullptr,
+                       keep ? static_cast<char*>(ws) + f.down.zs : nullptr, st);
+    prof_end(kPhFwd, st);
+    return s;
+  }
   if (ffn_tc(plan)) {
     s = layer_forward(U, T, x, TT_DT_BF16, params_up, h, TT_DT_BF16, ws, f.up, st);
     if (s != TT_OK) return s;
@@ -833,6 +871,45 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
   float* h = fptr(ws, f.h);
   float* a = fptr(ws, f.a);
   float* da = fptr(ws, f.da);
+  if (ffn_fused(plan)) {
+    // the merges: the forward's (TT_REUSE_MERGE, tokens to reuse), else now
+    const bool reuse = (U.flags & TT_REUSE_MERGE) != 0 && T > 0;
+    const float* PU[kMaxK];
+    const float* PD[kMaxK];
+    if (reuse) {
+      chain_ptrs(U, params_up, ws, f.up, PU);
+      chain_ptrs(D, params_down, ws, f.down, PD);
+    } else {
+      prof_begin(kPhMerge, st);
+      s = run_merge_forward(U, params_up, ws, f.up, PU, true, true, st);
+      if (s == TT_OK) s = run_merge_forward(D, params_down, ws, f.down, PD, true, true, st);
+      prof_end(kPhMerge, st);
+      if (s != TT_OK) return s;
+    }
+    // z1' and z2': the forward's under TT_REUSE_Z, else computed here
+    void* zs1 = static_cast<char*>(ws) + f.up.zs;
+    void* zs2 = static_cast<char*>(ws) + f.down.zs;
+    if (T > 0 && !((U.flags & TT_REUSE_Z) && reuse)) {
+      prof_begin(kPhFwd, st);
+      s = ffn_tc_forward(U, D, T, x, nullptr, ws, f.up.tc, f.down.tc, zs1, zs2, st);
+      prof_end(kPhFwd, st);
+      if (s != TT_OK) return s;
+    }
+    prof_begin(kPhBwd, st);
+    s = ffn_tc_backward(U, D, T, x, dy, dx, ws, f.up.tc, f.down.tc, zs1, zs2,
+                        bwd_zero_ptr(ws, f.up), bwd_zero_floats(U, f.up), bwd_zero_ptr(ws, f.down),
+                        bwd_zero_floats(D, f.down), st);
+    prof_end(kPhBwd, st);
+    if (s != TT_OK) return s;
+    prof_begin(kPhMergeBwd, st);
+    s = run_merge_backward(D, params_down, PD, fptr(ws, f.down.dA), fptr(ws, f.down.dB),
+                           dparams_down, acc, true, reuse, ws, f.down, st);
+    if (s == TT_OK)
+      s = run_merge_backward(U, params_up, PU, fptr(ws, f.up.dA), fptr(ws, f.up.dB), dparams_up,
+                             acc, true, reuse, ws, f.up, st);
+    prof_end(kPhMergeBwd, st);
+    return s;
+  }
   if (ffn_tc(plan)) {
     // h = up(x) and a = GELU(h) are the forward's, still in the workspace,
     // under TT_REUSE_Z (same x); otherwise they are recomputed here

@@ -96,11 +96,16 @@ def test_reuse_z_flag(lib):
     f32 = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32))
     f32z = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32, flags=ttc.TT_REUSE_Z))
     assert ttc.tt_workspace_size(f32z, 1000) == ttc.tt_workspace_size(f32, 1000)
-    # FFN: with the reuse flags each layer keeps its own region (merges, z')
+    # FFN (fused bf16 pair): each layer always has a region of its own and its
+    # z' (T x 64 bf16), which the backward reads; no T x hidden buffers
     up, dn = synth.WORKLOADS["ffn768_3072_bf16"].layers
     a = ttc.tt_ffn_plan(_desc(up), _desc(dn))
     b = ttc.tt_ffn_plan(_desc(up, flags=ttc.TT_REUSE_Z), _desc(dn, flags=ttc.TT_REUSE_Z))
-    assert ttc.tt_workspace_size(b, 4096) >= ttc.tt_workspace_size(a, 4096) + 2 * 4096 * 128
+    for T in (1, 4096, 16384):
+        assert ttc.tt_workspace_size(b, T) == ttc.tt_workspace_size(a, T)
+        assert 2 * T * 128 <= ttc.tt_workspace_size(a, T) - ttc.tt_workspace_size(a, 0) \
+            < 2 * T * 128 + 2048
+    assert ttc.tt_workspace_size(a, 16384) < 16384 * up.M * 2   # h never stored
     with pytest.raises(ttc.TTError):   # the two layers must carry the same flags
         ttc.tt_ffn_plan(_desc(up, flags=ttc.TT_REUSE_Z), _desc(dn))
 
