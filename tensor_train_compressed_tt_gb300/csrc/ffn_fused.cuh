@@ -55,6 +55,15 @@ __device__ __forceinline__ void gelu_tanh_grad(float u, float da, float& a, floa
   g = da * d;
 }
 
+// Per-warp stamps of CTA 0 (timeline builds only): [kernel][warp][slot]
+#ifdef TTC_TIMELINE
+__device__ unsigned long long g_tlw[2][16][32];
+#define TLW(k, slot) \
+  if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (slot) < 32) g_tlw[(k)][threadIdx.x >> 5][(slot)] = gtimer()
+#else
+#define TLW(k, slot) ((void)0)
+#endif
+
 struct FfnFwdArgs {
   int64_t T;
   int nN, nH, nM, ntiles;
@@ -159,7 +168,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
             tma_load(st + OPND, &tm_anr1, &S.full[s], 0, c * CH);
           } else if (c < p.nN + p.nH) {
-            const int hc = c - p.nN;
+            // chunk order rotated by the tile index: concurrent CTAs read
+            // different operand chunks instead of all the same lines of L2
+            const int hc = rot_chunk(c - p.nN, p.nH, tile);
             mbar_expect_tx(&S.full[s], 2 * BOX);
             tma_load(st, &tm_anr2, &S.full[s], 0, hc * CH);  // [128 hidden][64 ranks]
             tma_load(st + OPND, &tm_bm1, &S.full[s], hc * CH, 0);
@@ -213,40 +224,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!wait_bar(&S.z2_empty, (tl & 1) ^ 1, abort_flag, 54)) break;
         const int ih = it;
-        for (int c = 0; c <= p.nH; ++c) {
-          if (c < p.nH) {
-            const int s = (ih + c) % FFN_NST_F;
-            const int hb = hc & 1;
-            if (!wait_bar(&S.full[s], ((ih + c) / FFN_NST_F) & 1, abort_flag, 55)) { ok = false; break; }
-            if (!wait_bar(&S.h_empty[hb], ((hc >> 1) & 1) ^ 1, abort_flag, 56)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t st = su32(stages + s * STAGE);
-            for (int k = 0; k < p.kb1; ++k)
-              mma(tmem + FF_H + hb * 128, kdesc(zp_addr) + 2 * k,
-                  mndesc(st + OPND, BOX / 2) + 128 * k, id_h, k != 0);
-            mma_commit(&S.h_full[hb]);
-            ++hc;
-            if (c == p.nH - 1) {  // the z1' tile's last reader is issued
-              if (p.save_z) bulk_wait_read<0>();
-              mma_commit(&S.zp_empty);
-            }
+        // h_c = z1' B1[:, c] into H buffer c & 1, issued two chunks ahead of
+        // the z2 product that consumes GELU(h_c), so the epilogue finds the
+        // next h ready when it finishes a chunk
+        auto issue_h = [&](int c) -> bool {
+          const int s = (ih + c) % FFN_NST_F;
+          const int hb = hc & 1;
+          if (!wait_bar(&S.full[s], ((ih + c) / FFN_NST_F) & 1, abort_flag, 55)) return false;
+          if (!wait_bar(&S.h_empty[hb], ((hc >> 1) & 1) ^ 1, abort_flag, 56)) return false;
+          tc_fence_after();
+          const uint32_t st = su32(stages + s * STAGE);
+          for (int k = 0; k < p.kb1; ++k)
+            mma(tmem + FF_H + hb * 128, kdesc(zp_addr) + 2 * k,
+                mndesc(st + OPND, BOX / 2) + 128 * k, id_h, k != 0);
+          mma_commit(&S.h_full[hb]);
+          if (tl == 0 && c < 8) TLW(0, 2 * c);
+          ++hc;
+          if (c == p.nH - 1) {  // the z1' tile's last reader is issued
+            if (p.save_z) bulk_wait_read<0>();
+            mma_commit(&S.zp_empty);
           }
-          if (c >= 1) {
-            const int cp = c - 1;
-            const int s = (ih + cp) % FFN_NST_F;
-            if (!wait_bar(&S.a_full, ac & 1, abort_flag, 57)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t st = su32(stages + s * STAGE);
+          return true;
+        };
+        if (!issue_h(0) || (p.nH > 1 && !issue_h(1))) break;
+        for (int c = 0; c < p.nH; ++c) {
+          const int s = (ih + c) % FFN_NST_F;
+          if (!wait_bar(&S.a_full, ac & 1, abort_flag, 57)) { ok = false; break; }
+          if (tl == 0 && c < 8) TLW(0, 2 * c + 1);
+          tc_fence_after();
+          const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
-            for (int b = 0; b < 2; ++b)
+          for (int b = 0; b < 2; ++b)
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma(tmem + FF_Z2, kdesc(at_addr + b * BOX) + 2 * k,
-                    mndesc(st + b * (BOX / 2), 1024) + 128 * k, id_z, (cp | b | k) != 0);
-            mma_commit(&S.a_empty);
-            mma_commit(&S.empty[s]);
-            ++ac;
-          }
+            for (int k = 0; k < 4; ++k)
+              mma(tmem + FF_Z2, kdesc(at_addr + b * BOX) + 2 * k,
+                  mndesc(st + b * (BOX / 2), 1024) + 128 * k, id_z, (c | b | k) != 0);
+          mma_commit(&S.a_empty);
+          mma_commit(&S.empty[s]);
+          ++ac;
+          if (c + 2 < p.nH && !issue_h(c + 2)) { ok = false; break; }
         }
         if (!ok) break;
         it = ih + p.nH;
@@ -313,6 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int hb = hc & 1;
         if (!warp_wait(&S.h_full[hb], (hc >> 1) & 1, abort_flag, 64)) { ok = false; break; }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(0, 2 + 3 * c);
+        if (tl == 0 && c < 8) TLW(0, 4 * c);
         tc_fence_after();
         tmem_ld32(tmem + lane_off + FF_H + hb * 128 + 64 * h, v);
         tmem_ld32(tmem + lane_off + FF_H + hb * 128 + 64 * h + 32, w);
@@ -326,13 +343,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           w[j] = gelu_tanh(w[j]);
         }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(0, 3 + 3 * c);
+        if (tl == 0 && c < 8) TLW(0, 4 * c + 1);
         if (!warp_wait(&S.a_empty, (ac & 1) ^ 1, abort_flag, 65)) { ok = false; break; }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(0, 4 + 3 * c);
+        if (tl == 0 && c < 8) TLW(0, 4 * c + 2);
         st_tile_half(atile + h * BOX, row, 0, v);
         st_tile_half(atile + h * BOX, row, 1, w);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.a_full);
+        if (tl == 0 && c < 8) TLW(0, 4 * c + 3);
         ++ac;
       }
       if (!ok) break;
@@ -601,6 +621,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c = 0; c < p.nM; ++c, ++it) {
           const int s = it % FFN_NST_B;
           if (!wait_bar(&S.full[s], (it / FFN_NST_B) & 1, abort_flag, 75)) { ok = false; break; }
+          if (tl == 0 && c < 6) TLW(1, 24 + c);
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
@@ -620,8 +641,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok) break;
         mma_commit(&S.dzp2_full);
         mma_commit(&S.zp2_free);
+        if (tl == 0) TLW(1, 30);
         // hidden chunks
         if (!wait_bar(&S.dz2_full, tl & 1, abort_flag, 76)) break;
+        if (tl == 0) TLW(1, 31);
         if (!wait_bar(&S.dz1p_empty, (tl & 1) ^ 1, abort_flag, 77)) break;
         tc_fence_after();
         const int ih = it;
@@ -629,7 +652,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         auto issue_hd = [&](int c) -> bool {
           const int s = (ih + c) % FFN_NST_B;
           if (!wait_bar(&S.full[s], ((ih + c) / FFN_NST_B) & 1, abort_flag, 78)) return false;
+          if (tl == 0 && c < 4) TLW(1, 16 + c);
           if (!wait_bar(&S.hd_empty, (hdc & 1) ^ 1, abort_flag, 79)) return false;
+          if (tl == 0 && c < 4) TLW(1, 20 + c);
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
           for (int k = 0; k < p.kb1; ++k)
@@ -637,6 +662,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int k = 0; k < p.kb2; ++k)
             mma(tmem + FB_DA, kdesc(z2a) + 2 * k, kdesc(st) + 2 * k, id_n, k != 0);
           mma_commit(&S.hd_full);
+          if (tl == 0 && c < 8) TLW(1, 2 * c);
           ++hdc;
           return true;
         };
@@ -644,21 +670,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c = 0; c < p.nH; ++c) {
           if (c + 1 < p.nH && !issue_hd(c + 1)) { ok = false; break; }
           if (!wait_bar(&S.ad_full, adc & 1, abort_flag, 80)) { ok = false; break; }
+          if (tl == 0 && c < 8) TLW(1, 2 * c + 1);
           tc_fence_after();
           const int s = (ih + c) % FFN_NST_B;
           const uint32_t st = su32(stages + s * STAGE);
-          uint32_t wcol;
-          if (!w_take(wcol)) { ok = false; break; }
-#pragma unroll
-          for (int k = 0; k < 8; ++k)   // dA2 chunk = a_c^T dz2
-            mma(wcol, mndesc(ata, BOX) + 128 * k, mndesc(z2a, 1024) + 128 * k, id_w, k != 0);
-          w_done();
 #pragma unroll
           for (int b = 0; b < 2; ++b)   // dz1' += dh_c B1[:, c]^T
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma(tmem + FB_DZ1P, kdesc(dha + b * BOX) + 2 * k,
                   kdesc(st + OPND + b * (BOX / 2)) + 2 * k, id_r, (c | b | k) != 0);
+          uint32_t wcol;
+          if (!w_take(wcol)) { ok = false; break; }
+#pragma unroll
+          for (int k = 0; k < 8; ++k)   // dA2 chunk = a_c^T dz2
+            mma(wcol, mndesc(ata, BOX) + 128 * k, mndesc(z2a, 1024) + 128 * k, id_w, k != 0);
+          w_done();
           if (!w_take(wcol)) { ok = false; break; }
 #pragma unroll
           for (int k = 0; k < 8; ++k)   // dB1^T chunk = dh_c^T z1'
@@ -772,6 +799,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float h0[32], h1[32], d0[32], d1[32];
         if (!warp_wait(&S.hd_full, hdc & 1, abort_flag, 88)) { ok = false; break; }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(1, 2 + 3 * c);
+        if (tl == 0 && c < 8) TLW(1, 4 * c);
         tc_fence_after();
         tmem_ld32(tmem + lane_off + FB_H + 64 * h, h0);
         tmem_ld32(tmem + lane_off + FB_H + 64 * h + 32, h1);
@@ -795,15 +823,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           pd1[j] = pack_bf16(g0, g1);
         }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(1, 3 + 3 * c);
-        if (c > 0) {  // the previous chunk's dA2 and dB1^T products are done by now
-          const int cb = rot_chunk(c - 1, p.nH, tile) * CH;
-          if (!drain_w(&tm_dac2, cb, p.H, r2) || !drain_w(&tm_dbc1, cb, p.H, r1)) {
-            ok = false;
-            break;
-          }
-        }
+        if (tl == 0 && c < 8) TLW(1, 4 * c + 1);
         if (!warp_wait(&S.ad_empty, (adc & 1) ^ 1, abort_flag, 89)) { ok = false; break; }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(1, 4 + 3 * c);
+        if (tl == 0 && c < 8) TLW(1, 4 * c + 2);
         st_tile_half_u(atile + h * BOX, row, 0, pa0);
         st_tile_half_u(atile + h * BOX, row, 1, pa1);
         st_tile_half_u(dhtile + h * BOX, row, 0, pd0);
@@ -811,7 +834,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.ad_full);
+        if (tl == 0 && c < 8) TLW(1, 4 * c + 3);
         ++adc;
+        if (c > 0) {  // the previous chunk's dA2 and dB1^T products
+          const int cb = rot_chunk(c - 1, p.nH, tile) * CH;
+          if (!drain_w(&tm_dac2, cb, p.H, r2) || !drain_w(&tm_dbc1, cb, p.H, r1)) {
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) break;
       {
@@ -992,3 +1023,9 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
 }
 
 }  // namespace ttc
+
+#ifdef TTC_TIMELINE
+extern "C" int ttc_timeline_warps_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, ttc::g_tlw, bytes);
+}
+#endif

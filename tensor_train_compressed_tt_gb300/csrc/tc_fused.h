@@ -44,6 +44,20 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
                       void* ws, size_t ws_off, float* zero, size_t zero_n, bool f8,
                       const void* zs, cudaStream_t st);
 
+// ---- single-launch f32 path for small layers (small_f32.cu) -----------------
+// True when one CTA's shared memory holds the whole pass for T tokens (f32
+// activations, T <= 4096).
+bool small_f32_supported(const LayerPlan& L, int64_t T);
+// y = x W^T in one launch.  pout[k] (k < 2d, null entries skipped, pout itself
+// may be null) receives the prefix product ending at core k, for a backward
+// that reuses this forward's merge.
+tt_status small_f32_forward(const LayerPlan& L, int64_t T, const void* x, const float* params,
+                            void* y, float* const* pout, cudaStream_t st);
+// dx and dparams (overwritten, or added to when acc) in one launch.
+tt_status small_f32_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy,
+                             const float* params, void* dx, float* dparams, bool acc,
+                             cudaStream_t st);
+
 // ---- fused FFN pair (ffn_fused.cuh) -------------------------------------------
 // True when both layers run on the tensor-core kernels and up's output width
 // is down's input width.

@@ -517,9 +517,29 @@ bool use_tc(const LayerPlan& L, int tx, int ty) {
   return tx == TT_DT_BF16 && ty == TT_DT_BF16 && L.act == TT_DT_BF16 && tc_supported(L);
 }
 
+// Small f32 layers run as one launch per pass (merges, token products and
+// gradients in one CTA's shared memory).
+bool use_small(const LayerPlan& L, int64_t T, int tx, int ty) {
+  return tx == TT_DT_F32 && ty == TT_DT_F32 && small_f32_supported(L, T);
+}
+
 tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, const float* params,
                         void* y, int ty, void* ws, const WsLayout& w, cudaStream_t st) {
   const float* P[kMaxK];
+  if (use_small(L, T, tx, ty)) {
+    // with TT_REUSE_MERGE the prefix products go where the merge engine
+    // would have left them (the backward may take another path)
+    float* pout[kMaxK] = {};
+    if (L.flags & TT_REUSE_MERGE) {
+      chain_ptrs(L, params, ws, w, P);
+      for (int k = 0; k < L.K; ++k)
+        if (k != 0 && k != L.d) pout[k] = const_cast<float*>(P[k]);
+    }
+    prof_begin(kPhFwd, st);
+    tt_status s = small_f32_forward(L, T, x, params, y, pout, st);
+    prof_end(kPhFwd, st);
+    return s;
+  }
   const bool tc = use_tc(L, tx, ty);
   if (!tc && tx == TT_DT_E4M3) return TT_ERR_UNSUPPORTED;  // E4M3 runs on the fused kernels only
   const bool reuse = (L.flags & TT_REUSE_MERGE) != 0;
@@ -617,6 +637,12 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
                          int tdy, const float* params, void* dx, int tdx, float* dparams,
                          bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
   const float* P[kMaxK];
+  if (tdy == TT_DT_F32 && use_small(L, T, tx, tdx)) {
+    prof_begin(kPhBwd, st);
+    tt_status s = small_f32_backward(L, T, x, dy, params, dx, dparams, acc, st);
+    prof_end(kPhBwd, st);
+    return s;
+  }
   const bool tc = use_tc(L, tx, tdx) && tdy == tx;
   if (!tc && (tx == TT_DT_E4M3 || tdy == TT_DT_E4M3)) return TT_ERR_UNSUPPORTED;
   // a forward of no tokens is a no-op that leaves nothing to reuse
