@@ -100,6 +100,18 @@ typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1, TT_DT_E4M3 = 2 } tt_dtype
  * ignores it.  In a bf16 FFN plan the backward also takes h = TT_up(x) and
  * GELU(h) from the forward's workspace instead of recomputing them. */
 #define TT_REUSE_Z 4u
+/* Bit-reproducible gradients: the same inputs give the same dx and dparams
+ * bit for bit, run after run, on a given GPU model.  Every sum over tokens
+ * is taken in a fixed order: 128-token tiles, each CTA adding its tiles in
+ * order into a slot of its own (TMA bulk add with completion awaited between
+ * tiles), the slots then summed in CTA order by one more kernel; the merge
+ * backward runs without atomic K splits (split partials reduced in split
+ * order, one more engine phase); the f32 path reduces without atomics; a
+ * bf16 FFN pair runs layer by layer.  Costs workspace (up to 160 slots of
+ * (N + M + 4) x 64 floats, counted by tt_workspace_size) and time.  The
+ * CoMERA pages do not discuss reproducibility; this is the training
+ * requirement of a library boundary. */
+#define TT_DETERMINISTIC 8u
 
 typedef struct tt_desc {
   int d;                        /* 1..TT_MAX_D: number of input (= output) modes */
@@ -107,7 +119,7 @@ typedef struct tt_desc {
   int out_modes[TT_MAX_D];      /* m_1..m_d, each >= 1 */
   int ranks[2 * TT_MAX_D + 1];  /* r_0..r_2d; r_0 = r_2d = 1, others >= 1 */
   int act;                      /* tt_dtype of x, y, dx, dy (E4M3: y, dx bf16) */
-  unsigned flags;               /* TT_ACCUMULATE | TT_REUSE_MERGE | TT_REUSE_Z */
+  unsigned flags;               /* TT_ACCUMULATE | TT_REUSE_MERGE | TT_REUSE_Z | TT_DETERMINISTIC */
 } tt_desc;
 
 typedef struct tt_plan_s tt_plan_t; /* opaque, immutable host object */

@@ -414,6 +414,12 @@ struct BwdArgs {
   float* zero;  // [0, zero_n) set to 0 (scratch the merge backward adds into)
   int zero_n;
   int use_z;    // read the forward's z' through tm_zs instead of computing x A
+  // Fixed summation order: the token sums go to this CTA's own slot (rows
+  // blockIdx.x * N of tm_dac, blockIdx.x * M of tm_dbc; dDslot[blockIdx.x][4
+  // quadrants][64]), stored by the CTA's first tile and added to by its later
+  // ones, each tile's bulk operations completed before the next tile's.
+  int det;
+  float* dDslot;
 };
 
 struct SmemCommon {
@@ -984,7 +990,11 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add(&tm_dbc, box, 32 * h, cb * CH + 32 * q);
+            if (p.det && tl == 0)
+              tma_store(&tm_dbc, box, 32 * h, blockIdx.x * p.M + cb * CH + 32 * q);
+            else
+              tma_reduce_add(&tm_dbc, box, 32 * h,
+                             (p.det ? blockIdx.x * p.M : 0) + cb * CH + 32 * q);
             bulk_commit();
           }
           ++nst;
@@ -1011,7 +1021,12 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         float colsum = warp_transpose_sum(pr, lane);
         if (32 * h + lane < rprime) {
           if (p.use_z) colsum = colsum / S.Dc[32 * h + lane];  // nonzero: compacted column
-          atomicAdd(p.dDc + 32 * h + lane, colsum);
+          if (p.det) {  // this lane alone owns the entry of its CTA and quadrant
+            float* e = p.dDslot + ((size_t)blockIdx.x * 4 + q) * RP + 32 * h + lane;
+            *e = tl == 0 ? colsum : *e + colsum;
+          } else {
+            atomicAdd(p.dDc + 32 * h + lane, colsum);
+          }
         }
       }
 #pragma unroll
@@ -1067,13 +1082,19 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add(&tm_dac, box2, 32 * h, cx * CH + 32 * q);
+            if (p.det && tl == 0)
+              tma_store(&tm_dac, box2, 32 * h, blockIdx.x * p.N + cx * CH + 32 * q);
+            else
+              tma_reduce_add(&tm_dac, box2, 32 * h,
+                             (p.det ? blockIdx.x * p.N : 0) + cx * CH + 32 * q);
             bulk_commit();
           }
           ++nst;
         }
       }
       if (!ok) break;
+      // the next tile's adds into this CTA's slot come after this tile's
+      if (p.det && lane == 0) bulk_wait_all();
       if (warp == 2 && lane == 0) TL_STAMP(1, 6);
     }
     if (lane == 0) bulk_wait_all();
@@ -1084,6 +1105,36 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   tc_fence_after();
   if (threadIdx.x == 0) TL_STAMP(1, 7);
   if (warp == 1) tmem_free(tmem);
+}
+
+// ==========================================================================
+// fixed-order sum of the per-CTA token-sum slots (TT_DETERMINISTIC)
+//   dAc[i] = sum_k slotA[k][i], dBc[i] = sum_k slotB[k][i],
+//   dDc[c] = sum_k sum_q slotD[k][q][c], k = 0 .. G-1 in order
+// ==========================================================================
+__global__ void det_sum_kernel(const float* __restrict__ slotA, const float* __restrict__ slotB,
+                               const float* __restrict__ slotD, int G, int64_t nA, int64_t nB,
+                               float* dAc, float* dBc, float* dDc) {
+  pdl_wait();  // the token kernel's slots are complete
+  pdl_trigger();
+  const int64_t n = nA + nB + RP;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    if (i < nA) {
+      for (int k = 0; k < G; ++k) v += __ldcg(slotA + (int64_t)k * nA + i);
+      dAc[i] = v;
+    } else if (i < nA + nB) {
+      const int64_t j = i - nA;
+      for (int k = 0; k < G; ++k) v += __ldcg(slotB + (int64_t)k * nB + j);
+      dBc[j] = v;
+    } else {
+      const int c = (int)(i - nA - nB);
+      for (int k = 0; k < G; ++k)
+        for (int q = 0; q < 4; ++q) v += __ldcg(slotD + ((int64_t)k * 4 + q) * RP + c);
+      dDc[c] = v;
+    }
+  }
 }
 
 // ==========================================================================
@@ -1410,7 +1461,7 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
 
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
                       void* ws, size_t off, float* zero, size_t zero_n, bool f8, const void* zs,
-                      cudaStream_t st) {
+                      const DetSlots* det, cudaStream_t st) {
   if (zero_n > 0x7FFFFFFF) return TT_ERR_UNSUPPORTED;
   if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
   if (T <= 0) {
@@ -1421,7 +1472,10 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
-  const int tt = tokens_per_tile(T);
+  if (det && (det->count < 1 || (int64_t)det->count * (L.N > L.M ? L.N : L.M) > 0x7FFFFFFF))
+    return TT_ERR_UNSUPPORTED;
+  // a fixed summation order wants a fixed token blocking: 128-token tiles
+  const int tt = det ? TILE : tokens_per_tile(T);
   CUtensorMap mx, mdy, mbm, manr, mdx, mdx16, mdac, mdbc, mzs;
   const bool act_ok = f8 ? make_map(&mx, x, L.N, T, CH, tt, kMapU8) &&
                                make_map(&mdy, dy, L.M, T, CH, tt, kMapU8)
@@ -1430,8 +1484,10 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
       !make_map(&mbm, at<void>(ws, off + t.Bm), L.M, RP, 64, RP) ||
       !make_map(&manr, at<void>(ws, off + t.Anr), RP, L.N, 64, CH) ||
       !make_map(&mdx, dx, L.N, T, 64, 32) || !make_map(&mdx16, dx, L.N, T, 64, 16) ||
-      !make_map(&mdac, at<void>(ws, off + t.dAc), RP, L.N, 32, 32, kMapF32) ||
-      !make_map(&mdbc, at<void>(ws, off + t.dBc), RP, L.M, 32, 32, kMapF32) ||
+      !make_map(&mdac, det ? det->a : at<void>(ws, off + t.dAc), RP,
+                L.N * (det ? det->count : 1), 32, 32, kMapF32) ||
+      !make_map(&mdbc, det ? det->b : at<void>(ws, off + t.dBc), RP,
+                L.M * (det ? det->count : 1), 32, 32, kMapF32) ||
       !make_map(&mzs, zs ? zs : dx, RP, T, 64, tt))
     return TT_ERR_CUDA;
   BwdArgs a;
@@ -1451,13 +1507,26 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.zero = zero;
   a.zero_n = (int)zero_n;
   a.use_z = zs != nullptr;
+  a.det = det ? 1 : 0;
+  a.dDslot = det ? det->d : nullptr;
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+  if (det && grid > det->count) grid = det->count;
   cudaError_t e = f8 ? launch_ex(tt_bwd_kernel<true>, grid, NTHREADS_F8, kSmemBwd, st, false, mx,
                                  mdy, mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a)
                       : launch_ex(tt_bwd_kernel<false>, grid, NTHREADS, kSmemBwd, st, false, mx, mdy,
                                   mbm, manr, mdx, mdx16, mdac, mdbc, mzs, a);
   count_launches(1);
-  return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  if (e != cudaSuccess) return TT_ERR_CUDA;
+  if (det) {  // the slots of the `grid` CTAs, summed in CTA order
+    const int64_t nA = L.N * RP, nB = L.M * RP;
+    const int blocks = (int)((nA + nB + RP + 255) / 256 < 4 * num_sms() ? (nA + nB + RP + 255) / 256
+                                                                        : 4 * num_sms());
+    e = launch_ex(det_sum_kernel, blocks, 256, 0, st, false, (const float*)det->a,
+                  (const float*)det->b, (const float*)det->d, grid, nA, nB, a.dAc, a.dBc, a.dDc);
+    count_launches(1);
+    if (e != cudaSuccess) return TT_ERR_CUDA;
+  }
+  return TT_OK;
 }
 
 }  // namespace ttc

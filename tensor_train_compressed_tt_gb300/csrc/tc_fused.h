@@ -35,14 +35,25 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
                      size_t ws_off, bool f8, void* zs, cudaStream_t st);
 
 // dx for T tokens and the token sums dAc, dBc, dDc (zeroed by the pack
-// phase); the merge engine's unpack phase turns these into dA, dB, dD_d.
+// phase, or, with det, written in a fixed order from per-CTA slots by one
+// more kernel); the merge engine's unpack phase turns these into dA, dB, dD_d.
 // zero[0, zero_n) is set to 0 on the way (scratch that the merge backward
 // then adds into), also when T == 0.  x and dy are bf16, or E4M3 codes when
 // f8; dx is bf16.  With zs, z' is read from the forward's copy there instead
 // of being recomputed from x.
+// TT_DETERMINISTIC: per-CTA slots of the token sums (count CTAs at most):
+// a [count][N][64], b [count][M][64], d [count][4][64] floats.
+struct DetSlots {
+  float* a = nullptr;
+  float* b = nullptr;
+  float* d = nullptr;
+  int count = 0;
+};
+constexpr int kDetMaxSlots = 160;
+
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
                       void* ws, size_t ws_off, float* zero, size_t zero_n, bool f8,
-                      const void* zs, cudaStream_t st);
+                      const void* zs, const DetSlots* det, cudaStream_t st);
 
 // ---- single-launch f32 path for small layers (small_f32.cu) -----------------
 // True when one CTA's shared memory holds the whole pass for T tokens (f32

@@ -27,7 +27,8 @@ tt_status build_layer(const tt_desc* desc, LayerPlan* L) {
   if (d < 1 || d > TT_MAX_D) return TT_ERR_INVALID_ARG;
   if (desc->act != TT_DT_F32 && desc->act != TT_DT_BF16 && desc->act != TT_DT_E4M3)
     return TT_ERR_INVALID_ARG;
-  if (desc->flags & ~(TT_ACCUMULATE | TT_REUSE_MERGE | TT_REUSE_Z)) return TT_ERR_INVALID_ARG;
+  if (desc->flags & ~(TT_ACCUMULATE | TT_REUSE_MERGE | TT_REUSE_Z | TT_DETERMINISTIC))
+    return TT_ERR_INVALID_ARG;
   LayerPlan p;
   p.d = d;
   p.K = 2 * d;
@@ -94,6 +95,8 @@ struct WsLayout {
   size_t z = 0, dzp = 0; // SIMT token path intermediates
   size_t tc = 0;         // tensor-core path operands
   size_t zs = 0;         // z' kept by the forward for the backward (TT_REUSE_Z), bf16 [T][64]
+  size_t det = 0;        // TT_DETERMINISTIC: per-CTA token-sum slots (det_slots of them)
+  int det_slots = 0;
   size_t end = 0;        // end of this layer's scratch
 };
 
@@ -127,6 +130,14 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   w->dzp = take(tc ? 0 : (size_t)T * L.rd * sizeof(float));
   w->tc = take(tc_operand_bytes(L));
   w->zs = take(tc && (keep_z || (L.flags & TT_REUSE_Z)) ? (size_t)T * 64 * 2 : 0);
+  // one slot per CTA of the backward token pass (128-token tiles, at most
+  // kDetMaxSlots CTAs): [N + M + 4][64] floats each
+  w->det_slots = 0;
+  if (tc && (L.flags & TT_DETERMINISTIC)) {
+    const int64_t tiles = (T + 127) / 128;
+    w->det_slots = (int)(tiles < kDetMaxSlots ? (tiles > 0 ? tiles : 1) : kDetMaxSlots);
+  }
+  w->det = take((size_t)w->det_slots * (size_t)(L.N + L.M + 4) * 64 * sizeof(float));
   w->end = off;
   return off;
 }
@@ -151,7 +162,9 @@ bool ffn_fused(const tt_plan_s* p) {
     const char* e = getenv("TTC_FFN_UNFUSED");
     off = (e && e[0] && e[0] != '0') ? 1 : 0;
   }
-  return !off && ffn_tc(p) && ffn_tc_supported(p->L[0], p->L[1]);
+  // TT_DETERMINISTIC: layer by layer, each with its fixed-order token sums
+  return !off && !(p->L[0].flags & TT_DETERMINISTIC) && ffn_tc(p) &&
+         ffn_tc_supported(p->L[0], p->L[1]);
 }
 
 // Without the reuse flags the two layers' scratch shares one region; with
@@ -356,7 +369,10 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
     eng_unpack_task(b.add(), L, tc, params + L.diag_off[L.d - 1], fptr(ws, w.dA),
                     fptr(ws, w.dB), dparams + L.diag_off[L.d - 1], acc);
   }
-  const bool fold = steps >= 2;
+  // the folded last step adds into the first core's gradient with atomics;
+  // TT_DETERMINISTIC takes the unfolded program (split partials reduced in
+  // split order, dD by column sums)
+  const bool fold = steps >= 2 && !(L.flags & TT_DETERMINISTIC);
   const int nphases = fold ? steps : steps + 1;
   struct Side {
     int k_first, k_last;
@@ -621,14 +637,15 @@ tt_status simt_backward_tokens(const LayerPlan& L, int64_t T, const void* x, int
   bb.A = x; bb.sam = 1; bb.sak = L.N; bb.ta = tx;
   bb.B = dzp; bb.sbk = L.rd; bb.sbn = 1;
   bb.cscale = Dm; bb.clen = L.rd;
-  bb.C = dA; bb.scm = L.rd; bb.scn = 1; bb.mode = kAtomic;
+  const int sum_mode = (L.flags & TT_DETERMINISTIC) ? kStore : kAtomic;  // kStore: whole K a thread
+  bb.C = dA; bb.scm = L.rd; bb.scn = 1; bb.mode = sum_mode;
   TT_CUDA(gemm_simt(bb, st));
   GemmArgs c;  // dB = diag(D) z^T dy
   c.m = L.rd; c.n = L.M; c.k = T;
   c.A = z; c.sam = 1; c.sak = L.rd;
   c.rscale = Dm;
   c.B = dy; c.sbk = L.M; c.sbn = 1; c.tb = tdy;
-  c.C = dB; c.scm = L.M; c.scn = 1; c.mode = kAtomic;
+  c.C = dB; c.scm = L.M; c.scn = 1; c.mode = sum_mode;
   TT_CUDA(gemm_simt(c, st));
   return TT_OK;
 }
@@ -660,7 +677,15 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   const size_t nz = bwd_zero_floats(L, w);
   if (tc) {
     const void* zs = (L.flags & TT_REUSE_Z) && reuse ? static_cast<char*>(ws) + w.zs : nullptr;
-    s = tc_backward(L, T, x, dy, dx, ws, w.tc, bwd_zero_ptr(ws, w), nz, tx == TT_DT_E4M3, zs, st);
+    DetSlots det;
+    if (w.det_slots) {
+      det.count = w.det_slots;
+      det.a = fptr(ws, w.det);
+      det.b = det.a + (size_t)w.det_slots * L.N * 64;
+      det.d = det.b + (size_t)w.det_slots * L.M * 64;
+    }
+    s = tc_backward(L, T, x, dy, dx, ws, w.tc, bwd_zero_ptr(ws, w), nz, tx == TT_DT_E4M3, zs,
+                    w.det_slots ? &det : nullptr, st);
   } else {
     TT_CUDA(cudaMemsetAsync(bwd_zero_ptr(ws, w), 0, nz * sizeof(float), st));
     s = simt_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);

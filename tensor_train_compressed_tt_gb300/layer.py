@@ -34,7 +34,8 @@ class TTLinear:
 
     def __init__(self, in_modes: Sequence[int], out_modes: Sequence[int],
                  ranks: Sequence[int], dtype: torch.dtype = torch.bfloat16,
-                 accumulate: bool = False, reuse_merge: bool = False, reuse_z: bool = False):
+                 accumulate: bool = False, reuse_merge: bool = False, reuse_z: bool = False,
+                 deterministic: bool = False):
         self.in_modes = tuple(in_modes)
         self.out_modes = tuple(out_modes)
         self.ranks = tuple(ranks)
@@ -42,7 +43,8 @@ class TTLinear:
         # dtype of y and dx
         self.out_dtype = torch.bfloat16 if _DT[dtype] == ttc.TT_DT_E4M3 else dtype
         flags = (ttc.TT_ACCUMULATE if accumulate else 0) | \
-            (ttc.TT_REUSE_MERGE if reuse_merge else 0) | (ttc.TT_REUSE_Z if reuse_z else 0)
+            (ttc.TT_REUSE_MERGE if reuse_merge else 0) | (ttc.TT_REUSE_Z if reuse_z else 0) | \
+            (ttc.TT_DETERMINISTIC if deterministic else 0)
         self.desc = ttc.make_desc(in_modes, out_modes, ranks, _DT[dtype], flags)
         self.plan = ttc.tt_plan(self.desc)
         self.core_off, self.diag_off, self.n_params = ttc.tt_param_layout(self.plan)
@@ -99,9 +101,10 @@ class TTFFN:
 
     def __init__(self, up: Sequence[Sequence[int]], down: Sequence[Sequence[int]],
                  dtype: torch.dtype = torch.bfloat16, accumulate: bool = False,
-                 reuse_merge: bool = False, reuse_z: bool = False):
+                 reuse_merge: bool = False, reuse_z: bool = False, deterministic: bool = False):
         flags = (ttc.TT_ACCUMULATE if accumulate else 0) | \
-            (ttc.TT_REUSE_MERGE if reuse_merge else 0) | (ttc.TT_REUSE_Z if reuse_z else 0)
+            (ttc.TT_REUSE_MERGE if reuse_merge else 0) | (ttc.TT_REUSE_Z if reuse_z else 0) | \
+            (ttc.TT_DETERMINISTIC if deterministic else 0)
         self.dtype = dtype
         self.up_desc = ttc.make_desc(up[0], up[1], up[2], _DT[dtype], flags)
         self.down_desc = ttc.make_desc(down[0], down[1], down[2], _DT[dtype], flags)

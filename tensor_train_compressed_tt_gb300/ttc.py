@@ -24,6 +24,7 @@ TT_DT_E4M3 = 2   # x, dy as one-byte FP8 E4M3 codes; y, dx bf16
 TT_ACCUMULATE = 1
 TT_REUSE_MERGE = 2
 TT_REUSE_Z = 4   # forward keeps z' for the backward (implies TT_REUSE_MERGE)
+TT_DETERMINISTIC = 8   # bit-reproducible gradients (fixed summation order)
 
 STATUS = {
     0: "TT_OK",

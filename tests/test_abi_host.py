@@ -110,6 +110,21 @@ def test_reuse_z_flag(lib):
         ttc.tt_ffn_plan(_desc(up, flags=ttc.TT_REUSE_Z), _desc(dn))
 
 
+def test_deterministic_flag_workspace(lib):
+    """TT_DETERMINISTIC adds one token-sum slot per CTA of the backward
+    (128-token tiles, at most 160) to the tensor-core plans' workspace."""
+    shape = synth.WORKLOADS["tt768_bf16"].layers[0]
+    base = ttc.tt_plan(_desc(shape))
+    det = ttc.tt_plan(_desc(shape, flags=ttc.TT_DETERMINISTIC))
+    slot = (shape.N + shape.M + 4) * 64 * 4
+    for T, slots in ((1, 1), (300, 3), (16384, 128), (10 ** 6, 160)):
+        extra = ttc.tt_workspace_size(det, T) - ttc.tt_workspace_size(base, T)
+        assert slots * slot <= extra < slots * slot + 512
+    f32 = ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32, flags=ttc.TT_DETERMINISTIC))
+    assert ttc.tt_workspace_size(f32, 999) == ttc.tt_workspace_size(
+        ttc.tt_plan(_desc(shape, act=ttc.TT_DT_F32)), 999)
+
+
 def test_e4m3_plans(lib):
     """E4M3 runs on the fused tensor-core kernels only: shapes they do not
     take, and FFN pairs, are refused at plan time; the workspace is the bf16
@@ -144,6 +159,7 @@ def test_e4m3_plans(lib):
     lambda d: d.in_modes.__setitem__(1, 0),
     lambda d: setattr(d, "act", 7),
     lambda d: setattr(d, "flags", 0x80),
+    lambda d: setattr(d, "flags", 0x10),
 ])
 def test_invalid_descriptors_rejected(lib, mutate):
     shape = synth.WORKLOADS["tt768_bf16"].layers[0]
