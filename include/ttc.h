@@ -272,6 +272,31 @@ tt_status tt_ttm_lookup_backward(const tt_plan_t* plan, int64_t B, const int32_t
 tt_status tt_ttm_stats(const tt_plan_t* plan, const void* ws, int64_t* unique_rows,
                        int64_t* unique_pairs, void* stream);
 
+/* ---- the device-side error path ---------------------------------------------
+ * Every wait inside the library's kernels (on a TMA transfer, on another warp
+ * of the CTA, on a grid barrier) is bounded: after the limit it records
+ * TT_ERR_TIMEOUT in the device status word, tells the CTA's other warps to
+ * stop, waits (bounded) for its own copies and MMAs, frees its tensor memory
+ * and returns, leaving the context usable.  Not part of the CoMERA method. */
+
+/* The limit of those waits on the current device, in nanoseconds of the
+ * global timer (default 2e9, at least 1000).  Applies to kernels launched
+ * afterwards; call it with no library work in flight on the device and
+ * outside stream capture.  TT_ERR_INVALID_ARG below 1000 ns. */
+tt_status tt_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook: the next launch on the current device of the named kernel skips
+ * one arrival in its first CTA, so that a bounded wait of that launch runs
+ * out (the launch then reports TT_ERR_TIMEOUT through tt_get_device_status
+ * and its outputs are undefined).  It faults nothing and hangs nothing: it is
+ * for testing the error path above.  Same calling rules as
+ * tt_set_wait_limit_ns. */
+#define TT_DEBUG_NONE 0
+#define TT_DEBUG_FWD_TOKENS 1    /* forward token kernel: first stage never loaded */
+#define TT_DEBUG_BWD_TOKENS 2    /* backward token kernel: first stage never loaded */
+#define TT_DEBUG_MERGE_BARRIER 3 /* merge engine (programs of 2+ phases): one grid-barrier arrival */
+tt_status tt_debug_skip_arrival(int site);
+
 /* Synchronise stream, then read and clear the status word of the current
  * device.  The word is sticky: it holds the first error any libttc kernel
  * on this device recorded since the last read.  Returns TT_OK,

@@ -33,17 +33,22 @@ __device__ bool eng_grid_barrier(unsigned long long* cnt, unsigned nblocks, int*
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned long long old = atomicAdd(cnt, 1ull);
-    const unsigned long long target = (old / nblocks + 1) * nblocks;
-    const uint64_t t0 = gtimer();
-    while (true) {
-      unsigned long long v;
-      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(cnt) : "memory");
-      if (v >= target) break;
-      if (gtimer() - t0 > kTimeoutNs) {
-        record_error(TT_ERR_TIMEOUT, 100);
-        *failed = 1;
-        break;
+    // test hook: the first CTA does not arrive, so the others' waits run out
+    const bool skip = blockIdx.x == 0 && debug_take(TT_DEBUG_MERGE_BARRIER);
+    if (!skip) {
+      const unsigned long long old = atomicAdd(cnt, 1ull);
+      const unsigned long long target = (old / nblocks + 1) * nblocks;
+      const uint64_t t0 = gtimer();
+      const uint64_t limit = *(volatile unsigned long long*)&g_wait_limit_ns;
+      while (true) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(cnt) : "memory");
+        if (v >= target) break;
+        if (gtimer() - t0 > limit) {
+          record_error(TT_ERR_TIMEOUT, 100);
+          *failed = 1;
+          break;
+        }
       }
     }
     __threadfence();

@@ -48,6 +48,11 @@
 namespace ttc {
 
 __device__ DeviceStatus g_status;
+// Limit of every bounded device wait (ns on the global timer), and the test
+// hook that makes one arrival go missing (tt_set_wait_limit_ns,
+// tt_debug_skip_arrival).
+__device__ unsigned long long g_wait_limit_ns = 2000000000ull;
+__device__ int g_debug_skip = 0;
 
 cudaError_t read_and_clear_device_status(DeviceStatus* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(DeviceStatus));
@@ -71,7 +76,6 @@ constexpr int STG = 4096;            // one epilogue staging box: 32 rows x 128 
 constexpr int NTHREADS = (2 + NEPI) * 32;
 constexpr int NCONV = 4;             // E4M3 -> bf16 converter warps (FP8 kernels)
 constexpr int NTHREADS_F8 = (2 + NEPI + NCONV) * 32;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 // TMEM columns
 constexpr uint32_t F_Z = 0, F_Y = 128;                       // forward
@@ -133,14 +137,20 @@ __device__ void record_error(unsigned code, unsigned where) {
   if (atomicCAS(&g_status.code, 0u, code) == 0u) atomicExch(&g_status.detail, where);
 }
 
+// True (once) when the test hook asks this launch to skip one arrival.
+__device__ __forceinline__ bool debug_take(int site) {
+  return *(volatile int*)&g_debug_skip == site && atomicCAS(&g_debug_skip, site, 0) == site;
+}
+
 // Wait for the phase of the given parity; false if aborted or timed out.
 __device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile int* abort_flag,
                                          unsigned where) {
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = gtimer();
+  const uint64_t limit = *(volatile unsigned long long*)&g_wait_limit_ns;
   while (!mbar_try_wait(b, parity)) {
     if (*abort_flag) return false;
-    if (gtimer() - t0 > kTimeoutNs) {
+    if (gtimer() - t0 > limit) {
       *abort_flag = 1;
       record_error(TT_ERR_TIMEOUT, where);
       return false;
@@ -161,8 +171,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, volatile
 // Drain wait used on the way out: bounded, ignores the abort flag.
 __device__ __forceinline__ void drain_bar(uint64_t* b, uint32_t parity) {
   const uint64_t t0 = gtimer();
+  const uint64_t limit = *(volatile unsigned long long*)&g_wait_limit_ns / 4;
   while (!mbar_try_wait(b, parity)) {
-    if (gtimer() - t0 > kTimeoutNs / 4) return;
+    if (gtimer() - t0 > limit) return;
   }
 }
 
@@ -533,12 +544,15 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       for (int s = 0; s < NSTAGE_F; ++s) last_parity[s] = -1;
       bool ok = true;
       const uint32_t act_bytes = (uint32_t)p.tt * 128;  // one activation box of tt rows
+      // test hook: the first CTA leaves its first stage unloaded
+      const bool skip_first = blockIdx.x == 0 && debug_take(TT_DEBUG_FWD_TOKENS);
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
         const int tok0 = tile * p.tt;
         for (int c = 0; ok && c < p.nN + p.nM; ++c, ++it) {
           const int s = it % NSTAGE_F;
           const uint32_t ph = (it / NSTAGE_F) & 1;
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 1)) { ok = false; break; }
+          if (skip_first && it == 0) continue;
           uint8_t* st = stages + s * STAGE;
           if (c < p.nN) {
             if (F8) {  // one E4M3 box of 128 columns into the second bf16 box's bytes
@@ -785,6 +799,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       for (int s = 0; s < NSTAGE_B; ++s) last_parity[s] = -1;
       bool ok = true;
       const uint32_t act_bytes = (uint32_t)p.tt * 128;  // one activation box of tt rows
+      // test hook: the first CTA leaves its first stage unloaded
+      const bool skip_first = blockIdx.x == 0 && debug_take(TT_DEBUG_BWD_TOKENS);
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
         const int tok0 = tile * p.tt;
         if (p.use_z) {
@@ -797,6 +813,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           const int s = it % NSTAGE_B;
           const uint32_t ph = (it / NSTAGE_B) & 1;
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 11)) { ok = false; break; }
+          if (skip_first && it == 0) continue;
           uint8_t* st = stages + s * STAGE;
           mbar_expect_tx(&S.full[s], (F8 ? act_bytes : 2 * act_bytes) + BOX);
           // activation tile: E4M3 as one box into the second bf16 box's bytes
@@ -1530,6 +1547,19 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
 }
 
 }  // namespace ttc
+
+extern "C" tt_status tt_set_wait_limit_ns(uint64_t ns) {
+  if (ns < 1000) return TT_ERR_INVALID_ARG;
+  const unsigned long long v = ns;
+  return cudaMemcpyToSymbol(ttc::g_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? TT_OK
+                                                                              : TT_ERR_CUDA;
+}
+
+extern "C" tt_status tt_debug_skip_arrival(int site) {
+  if (site < 0 || site > TT_DEBUG_MERGE_BARRIER) return TT_ERR_INVALID_ARG;
+  return cudaMemcpyToSymbol(ttc::g_debug_skip, &site, sizeof(site)) == cudaSuccess ? TT_OK
+                                                                                  : TT_ERR_CUDA;
+}
 
 #include "merge_engine.cuh"
 #include "ffn_fused.cuh"

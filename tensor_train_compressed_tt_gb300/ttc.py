@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
             "tt_ttm_lookup_backward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ttm_stats": [_P, _P, _P, _P, _P],
             "tt_get_device_status": [_P],
+            "tt_set_wait_limit_ns": [ctypes.c_uint64],
+            "tt_debug_skip_arrival": [ctypes.c_int],
             "tt_status_string": [ctypes.c_int],
         }
         for name, args in sigs.items():
@@ -291,6 +293,22 @@ def tt_ttm_stats(plan: Plan, ws: int, stream: int = 0):
 
 def tt_get_device_status(stream: int = 0) -> int:
     return lib().tt_get_device_status(stream)
+
+
+TT_DEBUG_NONE = 0
+TT_DEBUG_FWD_TOKENS = 1
+TT_DEBUG_BWD_TOKENS = 2
+TT_DEBUG_MERGE_BARRIER = 3
+
+
+def tt_set_wait_limit_ns(ns: int) -> int:
+    """Limit of the kernels' bounded waits on the current device (ns)."""
+    return lib().tt_set_wait_limit_ns(int(ns))
+
+
+def tt_debug_skip_arrival(site: int) -> int:
+    """Test hook: the next launch of `site` skips one arrival in its first CTA."""
+    return lib().tt_debug_skip_arrival(int(site))
 
 
 def tt_status_string(code: int) -> str:
