@@ -120,6 +120,9 @@ def whole_job_rate(tokens_per_rank, world, step_ms_max):
     return world * tokens_per_rank / (step_ms_max * 1e-3)
 
 
+SM_MAX_MHZ = 2070   # GB300 maximum SM clock
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -588,24 +591,57 @@ def run_ours(args, w):
     barrier()
     ms_eager = all_reduce_scalar(e0.elapsed_time(e1) / Ke, "max", dev)
 
-    # ---- per-phase CUDA-event timing of the library's kernels (same steps)
+    # ---- per-phase CUDA-event timing of the library's kernels (same steps):
+    # the library brackets each kernel phase with events on the launching
+    # stream.  Eagerly launched, the events also take in the host's launch
+    # latency; inside a replayed graph (event-record nodes) they time each
+    # kernel from the end of the node before it, as the timed region runs them.
+    import ctypes
+
+    def read_phases(acc):
+        for ph in range(5):
+            tot = ctypes.c_double()
+            n = ctypes.c_int64()
+            ttc.check(ttc.lib().tt_profile_phase(ph, ctypes.byref(tot), ctypes.byref(n)))
+            name = ttc.lib().tt_profile_phase_name(ph)
+            name = name.decode() if isinstance(name, bytes) else str(name)
+            if n.value:
+                a = acc.setdefault(name, {"ms_total": 0.0, "intervals": 0})
+                a["ms_total"] += tot.value
+                a["intervals"] += n.value
+        for a in acc.values():
+            a["us_per_interval"] = 1e3 * a["ms_total"] / a["intervals"]
+        return acc
+
     ttc.lib().tt_profile_enable(1)
     barrier()
     for i in range(K):
         step(i)
     barrier()
-    phases = {}
-    import ctypes
-    for ph in range(5):
-        tot = ctypes.c_double()
-        n = ctypes.c_int64()
-        ttc.check(ttc.lib().tt_profile_phase(ph, ctypes.byref(tot), ctypes.byref(n)))
-        name = ttc.lib().tt_profile_phase_name(ph)
-        name = name.decode() if isinstance(name, bytes) else str(name)
-        if n.value:
-            phases[name] = {"ms_total": tot.value, "intervals": n.value,
-                            "us_per_interval": 1e3 * tot.value / n.value}
+    phases_eager = read_phases({})
     ttc.lib().tt_profile_enable(0)
+    phases, phase_note = phases_eager, "eager launches with events between them"
+    if graph is not None:
+        try:
+            ttc.lib().tt_profile_enable(1)
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp):
+                cs = int(torch.cuda.current_stream().cuda_stream)
+                for j in range(nsets):
+                    step(j, cs)
+            ttc.lib().tt_profile_enable(0)
+            gp.replay()
+            torch.cuda.synchronize(dev)
+            acc = {}
+            for _ in range(max(10, K // nsets)):
+                gp.replay()
+                torch.cuda.synchronize(dev)
+                read_phases(acc)
+            phases, phase_note = acc, "graph replays with event-record nodes around each phase"
+        except Exception as e:  # keep the eager figures
+            ttc.lib().tt_profile_enable(0)
+            phase_note = f"eager ({type(e).__name__} in the graph pass: {e})"
+            torch.cuda.synchronize(dev)
 
     # ---- the rank-adaptive step (proximal update of one layer's packed
     # parameters), timed on copies so the step's own buffers stay unchanged
@@ -674,13 +710,32 @@ def run_ours(args, w):
     roof = None
     if dom is not None:
         per_launch_s = phases[dom]["us_per_interval"] * 1e-6
-        if w.ffn:
+        fused_ffn = w.ffn and not args.deterministic
+        if w.ffn and not fused_ffn:
             per_launch_s *= 2  # two layers bracketed per pass; bytes cover the pair
-        ach = bytes_of[dom] / per_launch_s / 1e9
-        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,
-                "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / peak,
-                "traffic": traffic_for(dom, w.name),
-                "algorithmic_bytes_per_launch": bytes_of[dom]}
+        if fused_ffn:
+            # The fused pair's floor is not HBM: every hidden activation takes
+            # one tanh on the special-function units (GELU in the forward, GELU
+            # and GELU' in the backward), T x H evaluations a launch, against
+            # 16 a clock per SM at the maximum SM clock.
+            H = w.layers[0].M
+            evals = T * H
+            sfu_peak = 16 * props.multi_processor_count * SM_MAX_MHZ * 1e6
+            ach = evals / per_launch_s
+            roof = {"bound": "alu", "kernel": dom, "achieved": ach / 1e9, "peak": sfu_peak / 1e9,
+                    "peak_kind": "derived: 16 special-function results a clock per SM x "
+                                 f"{props.multi_processor_count} SMs x {SM_MAX_MHZ} MHz",
+                    "unit": "G tanh/s", "frac": ach / sfu_peak, "traffic": None,
+                    "algorithmic_evals_per_launch": evals, "duration_us": per_launch_s * 1e6,
+                    "hbm_frac": bytes_of[dom] / per_launch_s / 1e9 / peak,
+                    "timing": phase_note}
+        else:
+            ach = bytes_of[dom] / per_launch_s / 1e9
+            roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,
+                    "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / peak,
+                    "traffic": traffic_for(dom, w.name),
+                    "algorithmic_bytes_per_launch": bytes_of[dom],
+                    "duration_us": per_launch_s * 1e6, "timing": phase_note}
     if launch_floor is not None:
         # launch-bound: the achieved step rate against the 1-token step rate
         roof = {"bound": "launch", "kernel": "whole step", "achieved": 1e3 / ms,
@@ -793,6 +848,8 @@ def run_ours(args, w):
                               "algorithmic_bytes": alg["bytes"], "algorithmic_flop": alg["flop"],
                               "peak_gbs": peak, "peak_kind": peak_kind},
             "phases_us": {k: round(v["us_per_interval"], 3) for k, v in phases.items()},
+            "phases_us_eager": {k: round(v["us_per_interval"], 3) for k, v in phases_eager.items()},
+            "phases_timing": phase_note,
             "rank_update": rank_step,
             "launch_floor": launch_floor,
             "cpu_baseline": cpu,

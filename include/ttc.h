@@ -314,7 +314,9 @@ const char* tt_status_string(tt_status s);
 #define TT_NUM_PHASES 5
 void tt_profile_enable(int on); /* on != 0: clear records and start; 0: stop */
 /* Synchronise on the recorded events and return the summed milliseconds and
- * the number of bracketed intervals of one phase since the last enable. */
+ * the number of bracketed intervals of one phase since the last enable.
+ * Calls captured into a CUDA graph record external event nodes: after each
+ * replay of that graph this returns the times of that replay. */
 tt_status tt_profile_phase(int phase, double* total_ms, int64_t* intervals);
 const char* tt_profile_phase_name(int phase);
 /* Total kernels this library has launched in this process (monotonic). */

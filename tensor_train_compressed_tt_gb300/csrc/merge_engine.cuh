@@ -144,13 +144,15 @@ __device__ __forceinline__ void eng_stage(float* S, int rows, int kc, int r0, in
   }
 }
 
-// The compaction map of D_d (pos[a]: compacted column of rank a, or -1),
-// built on first use by a unit of this CTA: a unit calls it after issuing its
-// own copies, so the load of D_d overlaps them.  Uniform across the CTA.
-__device__ __forceinline__ void ensure_pos(const EngProgram& p, int* pos, int* pos_ready) {
-  if (*pos_ready) return;
-  compaction_map(p.dmid, p.rd, pos, nullptr, nullptr);
-  if (threadIdx.x == 0) *pos_ready = 1;
+// The compaction map of the task's D_d (pos[a]: compacted column of rank a,
+// or -1), built when a unit of this CTA first needs it (again when a unit of
+// a task with another D_d, another layer, follows): a unit calls it after
+// issuing its own copies, so the load of D_d overlaps them.  Uniform across
+// the CTA.
+__device__ __forceinline__ void ensure_pos(const EngTask& t, int* pos, const float** pos_of) {
+  if (*pos_of == t.s) return;  // the map of this task's D_d is the one in pos
+  compaction_map(t.s, t.rd, pos, nullptr, nullptr);
+  if (threadIdx.x == 0) *pos_of = t.s;
   __syncthreads();
 }
 
@@ -161,8 +163,8 @@ __device__ __forceinline__ void ensure_pos(const EngProgram& p, int* pos, int* p
 // partials are summed in a fixed order (deterministic).  Tile counts and
 // the split length come from the host; the unit's own index arithmetic is
 // 32-bit shifts and masks.
-__device__ void eng_gemm_unit(const EngProgram& prog, const EngTask& t, int u, int* pos,
-                              int* pos_ready, float* dsm, float* rsc, float* csc, int nu) {
+__device__ void eng_gemm_unit(const EngTask& t, int u, int* pos, const float** pos_of, float* dsm,
+                              float* rsc, float* csc, int nu) {
   (void)nu;
   TLU_STAMP(nu, 6);
   const GemmArgs& g = t.g;
@@ -219,7 +221,7 @@ __device__ void eng_gemm_unit(const EngProgram& prog, const EngTask& t, int u, i
     // the operand that needs no compaction map goes first
     if (!gA) eng_stage(As, TM, kc, m0, k0, m, A, (int)g.sam, (int)g.sak, t, pos, false);
     if (!gB) eng_stage(Bs, TN, kc, n0, k0, n, B, (int)g.sbn, (int)g.sbk, t, pos, false);
-    if (t.gather || t.pack_side) ensure_pos(prog, pos, pos_ready);
+    if (t.gather || t.pack_side) ensure_pos(t, pos, pos_of);
     if (gA) eng_stage(As, TM, kc, m0, k0, m, A, (int)g.sam, (int)g.sak, t, pos, true);
     if (gB) eng_stage(Bs, TN, kc, n0, k0, n, B, (int)g.sbn, (int)g.sbk, t, pos, true);
     if (g.kscale) {
@@ -356,8 +358,8 @@ struct Walk2 {
   }
 };
 
-__device__ void eng_chain_unit(const EngProgram& prog, const EngTask& t, int u, int* pos,
-                               int* pos_ready, float* dsm, int nu) {
+__device__ void eng_chain_unit(const EngTask& t, int u, int* pos, const float** pos_of,
+                               float* dsm, int nu) {
   (void)nu;
   const ChainDesc& c = t.ch;
   const int L = c.L;
@@ -414,7 +416,7 @@ __device__ void eng_chain_unit(const EngProgram& prog, const EngTask& t, int u, 
     const float* src = c.core[L - 1] + q0 * rL;
     for (Walk2 w(w_); w.r < rl1; w.next()) cp_async4(cf + w.r * w_ + w.c, src + w.r * sl * rL + w.c);
   }
-  if (t.pack_side) ensure_pos(prog, pos, pos_ready);
+  if (t.pack_side) ensure_pos(t, pos, pos_of);
   cp_async_wait_all();
   __syncthreads();
   TLU_STAMP(nu, 3);
@@ -565,8 +567,8 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
     failed = 0;
     TL_STAMP(p.nphases == 1 ? 2 : 3, 0);
   }
-  __shared__ int pos_ready;  // the compaction map is built on first use
-  if (threadIdx.x == 0) pos_ready = 0;
+  __shared__ const float* pos_of;  // the D_d whose compaction map pos holds
+  if (threadIdx.x == 0) pos_of = nullptr;
   __syncthreads();
 #ifdef TTC_TIMELINE
   int nu = 0;
@@ -595,7 +597,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       }
 #endif
       switch (k.kind) {
-        case kEGemm: eng_gemm_unit(p, k, uu, pos, &pos_ready, eng_dsm, rsc, csc, nu); break;
+        case kEGemm: eng_gemm_unit(k, uu, pos, &pos_of, eng_dsm, rsc, csc, nu); break;
         case kEGemmFinal: eng_gemm_final_unit(k, uu); break;
         case kEColdot: eng_coldot_unit(k, uu, red); break;
         case kEScale: eng_scale_unit(k, uu); break;
@@ -605,7 +607,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
         case kEDd:
           tc_dd_unit(k.tc, k.s, k.rd, k.out, k.acc);
           break;
-        case kEChain: eng_chain_unit(p, k, uu, pos, &pos_ready, eng_dsm, nu); break;
+        case kEChain: eng_chain_unit(k, uu, pos, &pos_of, eng_dsm, nu); break;
         case kEUnpack:
           tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
           break;
@@ -888,16 +890,6 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
   if (getenv("TTC_ENG_DUMP") && dumps < 4) {
     ++dumps;
     eng_dump(p);
-  }
-  // the one D_d that the program's gather and pack epilogues compact by
-  p.dmid = nullptr;
-  for (int i = 0; i < p.ntasks; ++i) {
-    const EngTask& k = p.t[i];
-    if ((k.kind == kEGemm || k.kind == kEChain) && (k.gather || k.pack_side)) {
-      if (p.dmid && (p.dmid != k.s || p.rd != k.rd)) return cudaErrorInvalidValue;
-      p.dmid = k.s;
-      p.rd = k.rd;
-    }
   }
   int g = grid;
   // Only a grid barrier needs every CTA resident at once: a one-phase

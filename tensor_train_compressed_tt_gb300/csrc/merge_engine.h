@@ -84,7 +84,7 @@ struct alignas(16) EngTask {
   ChainDesc ch;  // kEChain (pack_side selects the packing, s = D_d)
 };
 
-constexpr int kEngMaxTasks = 36;
+constexpr int kEngMaxTasks = 46;  // two order-6 layers (an FFN pair) in one program
 constexpr int kEngMaxPhases = 8;
 
 struct alignas(16) EngProgram {
@@ -95,9 +95,6 @@ struct alignas(16) EngProgram {
   // has its own, so calls on different streams with different workspaces
   // never share one.
   unsigned long long* bar = nullptr;
-  int rd = 0;         // middle rank of dmid
-  const float* dmid = nullptr;  // D_d whose compaction map the gather / pack
-                                // epilogues use (set by eng_launch)
   int phase_begin[kEngMaxPhases + 1] = {};
   // units of a phase are dealt in this task order (set by eng_launch: the
   // tasks with the costliest units first)

@@ -35,11 +35,21 @@ const char* kNames[TT_NUM_PHASES] = {"merge", "forward_tokens", "backward_tokens
 
 }  // namespace
 
+// Inside a stream capture the record becomes an event-record node of the
+// graph (external), so that every replay stamps it; otherwise a plain record.
+void record(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
+
 void prof_begin(int phase, cudaStream_t st) {
   if (!g_on) return;
   cudaEvent_t e = take_event();
   if (!e) return;
-  cudaEventRecord(e, st);
+  record(e, st);
   g_open_phase = phase;
   g_open_start = e;
 }
@@ -48,7 +58,7 @@ void prof_end(int phase, cudaStream_t st) {
   if (!g_on || g_open_phase != phase || !g_open_start) return;
   cudaEvent_t e = take_event();
   if (!e) return;
-  cudaEventRecord(e, st);
+  record(e, st);
   g_records.push_back({phase, g_open_start, e});
   g_open_phase = -1;
   g_open_start = nullptr;

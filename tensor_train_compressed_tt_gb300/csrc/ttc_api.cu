@@ -280,13 +280,15 @@ tt_status run_merge_forward_gemm(const LayerPlan& L, const float* params, void* 
   return TT_OK;
 }
 
-tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
-                            const float** P, bool pack, bool zero_grads, cudaStream_t st) {
+// The one-phase chain program of one layer's forward merge, added to the
+// builder's current phase; false when a chain does not fit the chain units
+// (ranks above 64 or cores too large to stage): then the GEMM-phase program
+// below serves.
+bool add_merge_forward(EngBuilder& b, const LayerPlan& L, const float* params, void* ws,
+                       const WsLayout& w, const float** P, bool pack, bool zero_grads) {
   chain_ptrs(L, params, ws, w, P);
   const float* Dmid = params + L.diag_off[L.d - 1];
   const TcPtrs tc = pack ? tc_ptrs(L, ws, w.tc) : TcPtrs();
-  EngBuilder b;
-  b.begin_phase();
   if (L.d == 1) {
     if (pack) eng_pack_task(b.add(), L, P[0], P[1], Dmid, tc, zero_grads, false);
   } else {
@@ -313,19 +315,57 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
       // path takes the packed bf16 operands alone
       c.out = pack ? nullptr : const_cast<float*>(P[k0 + L.d - 1]);
       c.nprefix = np;
-      EngTask* t = b.add();
-      if (!eng_chain_task(t, c))  // ranks above 64 or cores too large to stage
-        return run_merge_forward_gemm(L, params, ws, w, P, pack, zero_grads, st);
+      EngTask t;
+      if (!eng_chain_task(&t, c)) return false;  // ranks above 64 or cores too large to stage
       if (pack) {
-        t->pack_side = side + 1;
-        t->tc = tc;
-        t->s = Dmid;
-        t->rd = L.rd;
-        t->N = (int)L.N;
-        t->M = (int)L.M;
+        t.pack_side = side + 1;
+        t.tc = tc;
+        t.s = Dmid;
+        t.rd = L.rd;
+        t.N = (int)L.N;
+        t.M = (int)L.M;
       }
+      *b.add() = t;
     }
   }
+  return true;
+}
+
+bool chain_merge_fits(const LayerPlan& L, const float* params, void* ws, const WsLayout& w) {
+  EngBuilder probe;
+  probe.begin_phase();
+  const float* P[kMaxK];
+  return add_merge_forward(probe, L, params, ws, w, P, false, false) && !probe.overflow;
+}
+
+tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, const WsLayout& w,
+                            const float** P, bool pack, bool zero_grads, cudaStream_t st) {
+  if (!chain_merge_fits(L, params, ws, w))
+    return run_merge_forward_gemm(L, params, ws, w, P, pack, zero_grads, st);
+  EngBuilder b;
+  b.begin_phase();
+  add_merge_forward(b, L, params, ws, w, P, pack, zero_grads);
+  b.end();
+  if (b.overflow) return TT_ERR_UNSUPPORTED;
+  if (b.p.ntasks == 0) return TT_OK;
+  TT_CUDA(eng_launch(b.p, st));
+  return TT_OK;
+}
+
+// Both layers' forward merges of an FFN pair in one launch where they fit
+// the chain units (else one launch each).
+tt_status run_merge_forward2(const LayerPlan& U, const float* pu, const WsLayout& wu,
+                             const float** PU, const LayerPlan& D, const float* pd,
+                             const WsLayout& wd, const float** PD, void* ws, bool zero_grads,
+                             cudaStream_t st) {
+  if (!chain_merge_fits(U, pu, ws, wu) || !chain_merge_fits(D, pd, ws, wd)) {
+    tt_status s = run_merge_forward(U, pu, ws, wu, PU, true, zero_grads, st);
+    return s != TT_OK ? s : run_merge_forward(D, pd, ws, wd, PD, true, zero_grads, st);
+  }
+  EngBuilder b;
+  b.begin_phase();
+  add_merge_forward(b, U, pu, ws, wu, PU, true, zero_grads);
+  add_merge_forward(b, D, pd, ws, wd, PD, true, zero_grads);
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
   if (b.p.ntasks == 0) return TT_OK;
@@ -356,24 +396,19 @@ size_t bwd_zero_floats(const LayerPlan& L, const WsLayout& w) {
   return (w.q - w.bar) / sizeof(float) + dq0_zero_floats(L, w);
 }
 
-tt_status run_merge_backward(const LayerPlan& L, const float* params, const float** P,
-                             const float* dA, const float* dB, float* dparams, bool acc,
-                             bool unpack, bool rezero, void* ws, const WsLayout& w,
-                             cudaStream_t st) {
-  EngBuilder b;
-  const int steps = L.d - 1;
-  const TcPtrs tc = unpack ? tc_ptrs(L, ws, w.tc) : TcPtrs();
-  if (unpack && steps == 0) {
-    // order 2: the merges are the cores themselves; unpack in full first
-    b.begin_phase();
-    eng_unpack_task(b.add(), L, tc, params + L.diag_off[L.d - 1], fptr(ws, w.dA),
-                    fptr(ws, w.dB), dparams + L.diag_off[L.d - 1], acc);
-  }
-  // the folded last step adds into the first core's gradient with atomics;
-  // TT_DETERMINISTIC takes the unfolded program (split partials reduced in
-  // split order, dD by column sums)
-  const bool fold = steps >= 2 && !(L.flags & TT_DETERMINISTIC);
-  const int nphases = fold ? steps : steps + 1;
+// The merge-backward program of one layer, built phase by phase so that the
+// programs of several layers (the two of an FFN pair) can share one launch.
+struct MergeBwd {
+  const LayerPlan& L;
+  const float* params;
+  const float** P;
+  float* dparams;
+  bool acc, unpack, rezero;
+  void* ws;
+  const WsLayout& w;
+  int steps = 0, pre = 0, nphases = 0;
+  bool fold = false;
+  TcPtrs tc;
   struct Side {
     int k_first, k_last;
     const float* Y;
@@ -383,11 +418,36 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
     int pending;         // task index of a split GEMM whose partials the next phase reduces
     const float* dQ;     // last dQ (for coldot in the next phase)
     int coldot_k;        // link whose dD the next phase computes (-1: none)
-  } sides[2] = {{0, L.d - 1, dA, nullptr, 0, 0, 0, -1, nullptr, -1},
-                {L.d, L.K - 1, dB, nullptr, 1, 2, 0, -1, nullptr, -1}};
-  const int mode = acc ? kAccumulate : kStore;
-  for (int j = 0; j < nphases; ++j) {
-    b.begin_phase();
+  } sides[2];
+
+  MergeBwd(const LayerPlan& L_, const float* params_, const float** P_, const float* dA,
+           const float* dB, float* dparams_, bool acc_, bool unpack_, bool rezero_, void* ws_,
+           const WsLayout& w_)
+      : L(L_), params(params_), P(P_), dparams(dparams_), acc(acc_), unpack(unpack_),
+        rezero(rezero_), ws(ws_), w(w_) {
+    steps = L.d - 1;
+    tc = unpack ? tc_ptrs(L, ws, w.tc) : TcPtrs();
+    // order 2: the merges are the cores themselves; unpack in full first
+    pre = (unpack && steps == 0) ? 1 : 0;
+    // the folded last step adds into the first core's gradient with atomics;
+    // TT_DETERMINISTIC takes the unfolded program (split partials reduced in
+    // split order, dD by column sums)
+    fold = steps >= 2 && !(L.flags & TT_DETERMINISTIC);
+    nphases = pre + (fold ? steps : steps + 1);
+    sides[0] = {0, L.d - 1, dA, nullptr, 0, 0, 0, -1, nullptr, -1};
+    sides[1] = {L.d, L.K - 1, dB, nullptr, 1, 2, 0, -1, nullptr, -1};
+  }
+
+  // The tasks of phase jj (the builder's current phase).
+  void add_phase(EngBuilder& b, int jj) {
+    if (jj < pre) {
+      eng_unpack_task(b.add(), L, tc, params + L.diag_off[L.d - 1], fptr(ws, w.dA),
+                      fptr(ws, w.dB), dparams + L.diag_off[L.d - 1], acc);
+      return;
+    }
+    const int j = jj - pre;
+    const int last_phase = nphases - pre - 1;
+    const int mode = acc ? kAccumulate : kStore;
     if (unpack && steps > 0 && j == 0)
       eng_dd_task(b.add(), L, tc, params + L.diag_off[L.d - 1], dparams + L.diag_off[L.d - 1],
                   acc);
@@ -397,8 +457,8 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
       if (!acc) {
         // gradients that later phases add into
         for (const Side& sd : sides) {
-          for (int jj = 1; jj < steps; ++jj) {
-            const int k = sd.k_last - jj;
+          for (int jj2 = 1; jj2 < steps; ++jj2) {
+            const int k = sd.k_last - jj2;
             eng_zero_task(b, dparams + L.core_off[k], (int64_t)L.r[k] * L.s[k] * L.r[k + 1]);
           }
           const int kf = sd.k_first;
@@ -507,20 +567,41 @@ tt_status run_merge_backward(const LayerPlan& L, const float* params, const floa
         t->acc = acc ? 1 : 0;
       }
     }
-    if (rezero && j == nphases - 1 && (j >= 1 || steps == 0)) {
+    if (rezero && j == last_phase && (j >= 1 || steps == 0)) {
       // leave the token sums zeroed for the next backward that reuses this
       // workspace's merge (read only by an earlier phase: the first reverse
       // step, or the unpack phase for order 2); dAc, dBc and dDc are adjacent
       eng_zero_task(b, const_cast<float*>(tc.dAc), (L.N + L.M + 1) * 64);
     }
   }
+};
+
+tt_status run_merge_backward_multi(MergeBwd* const* layers, int n, cudaStream_t st) {
+  EngBuilder b;
+  const int nph = layers[0]->nphases;
+  for (int i = 1; i < n; ++i)
+    if (layers[i]->nphases != nph || layers[i]->pre != layers[0]->pre) return TT_ERR_UNSUPPORTED;
+  for (int j = 0; j < nph; ++j) {
+    b.begin_phase();
+    for (int i = 0; i < n; ++i) layers[i]->add_phase(b, j);
+  }
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
   if (b.p.nphases == 0) return TT_OK;
-  // zeroed by the backward token pass that comes before in the stream
-  b.p.bar = reinterpret_cast<unsigned long long*>(fptr(ws, w.bar));
+  // one barrier line serves the program: the first layer's, zeroed by the
+  // backward token pass that comes before in the stream
+  b.p.bar = reinterpret_cast<unsigned long long*>(fptr(layers[0]->ws, layers[0]->w.bar));
   TT_CUDA(eng_launch(b.p, st));
   return TT_OK;
+}
+
+tt_status run_merge_backward(const LayerPlan& L, const float* params, const float** P,
+                             const float* dA, const float* dB, float* dparams, bool acc,
+                             bool unpack, bool rezero, void* ws, const WsLayout& w,
+                             cudaStream_t st) {
+  MergeBwd m(L, params, P, dA, dB, dparams, acc, unpack, rezero, ws, w);
+  MergeBwd* one = &m;
+  return run_merge_backward_multi(&one, 1, st);
 }
 
 // ---- one layer ---------------------------------------------------------------
@@ -872,9 +953,9 @@ tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,
   if (ffn_fused(plan)) {
     const bool reuse = (U.flags & TT_REUSE_MERGE) != 0;
     const float* P[kMaxK];
+    const float* P2[kMaxK];
     prof_begin(kPhMerge, st);
-    s = run_merge_forward(U, params_up, ws, f.up, P, true, reuse, st);
-    if (s == TT_OK) s = run_merge_forward(D, params_down, ws, f.down, P, true, reuse, st);
+    s = run_merge_forward2(U, params_up, f.up, P, D, params_down, f.down, P2, ws, reuse, st);
     prof_end(kPhMerge, st);
     if (s != TT_OK) return s;
     const bool keep = (U.flags & TT_REUSE_Z) != 0;
@@ -932,8 +1013,7 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
       chain_ptrs(D, params_down, ws, f.down, PD);
     } else {
       prof_begin(kPhMerge, st);
-      s = run_merge_forward(U, params_up, ws, f.up, PU, true, true, st);
-      if (s == TT_OK) s = run_merge_forward(D, params_down, ws, f.down, PD, true, true, st);
+      s = run_merge_forward2(U, params_up, f.up, PU, D, params_down, f.down, PD, ws, true, st);
       prof_end(kPhMerge, st);
       if (s != TT_OK) return s;
     }
@@ -953,6 +1033,9 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
     prof_end(kPhBwd, st);
     if (s != TT_OK) return s;
     prof_begin(kPhMergeBwd, st);
+    // one launch per layer: each layer's reverse chain alone fills a wave a
+    // phase, and the second launch starts as the first's CTAs leave (one
+    // program of both layers measured slower: two waves a phase)
     s = run_merge_backward(D, params_down, PD, fptr(ws, f.down.dA), fptr(ws, f.down.dB),
                            dparams_down, acc, true, reuse, ws, f.down, st);
     if (s == TT_OK)
