@@ -664,10 +664,39 @@ def run_ours(args, w):
         barrier()
         us = 1e3 * r0.elapsed_time(r1) / n_up
         nb = 12 * pc.numel()  # read params and dparams, write params (float32)
+        # the same step fused into the backward's merge program: the added
+        # time of tt_backward_rank_update over tt_backward (gradient form, so
+        # the parameters stay as they are)
+        x0, dy0, _, dx0 = sets[0]
+
+        def bwd_time(fused, n=50):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            barrier()
+            a.record(stream)
+            for _ in range(n):
+                if fused:
+                    ttc.check(ttc.tt_backward_rank_update(
+                        mod.plan, T, x0.data_ptr(), dy0.data_ptr(), pc.data_ptr(), dx0.data_ptr(),
+                        gc.data_ptr(), 1e-3, 1e-3, 0.0, wsp, wsn, sh))
+                else:
+                    ttc.check(ttc.tt_backward(mod.plan, T, x0.data_ptr(), dy0.data_ptr(),
+                                              pc.data_ptr(), dx0.data_ptr(), gc.data_ptr(), wsp,
+                                              wsn, sh))
+            b.record(stream)
+            barrier()
+            return 1e3 * a.elapsed_time(b) / n
+        ttc.check(ttc.tt_forward(mod.plan, T, x0.data_ptr(), pc.data_ptr(), sets[0][2].data_ptr(),
+                                 wsp, wsn, sh))
+        t_b, t_bf = bwd_time(False), bwd_time(True)
         rank_step = {"us_per_call": us, "bytes_per_call": nb,
                      "achieved_gbs": nb / (us * 1e-6) / 1e9, "bound": "latency",
                      "note": "tt_rank_update, proximal step on one layer's packed "
-                             f"parameters ({pc.numel()} floats), back-to-back eager launches"}
+                             f"parameters ({pc.numel()} floats), back-to-back eager launches",
+                     "fused_added_us": t_bf - t_b, "backward_us": t_b,
+                     "backward_with_step_us": t_bf,
+                     "fused_note": "tt_backward_rank_update (the step as the last phase of the "
+                                   "merge program) against tt_backward, eager, 50 calls each"}
 
     alg = algorithmic(w, T)
     peak, peak_kind = measured_peaks()

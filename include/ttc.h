@@ -224,6 +224,19 @@ typedef struct tt_rank_opts {
 tt_status tt_rank_update(const tt_plan_t* plan, float* params, float* dparams,
                          const tt_rank_opts* opts, void* stream);
 
+/* tt_backward followed by tt_rank_update on the same params / dparams, with
+ * the step run as the last phase of the backward's merge program (after a
+ * grid barrier that follows every read of params) instead of a launch of its
+ * own: the early-stage objective's gradient (lr == 0: dparams = dL/dparams +
+ * the penalty's sub-gradient) or one proximal step (lr > 0: params updated in
+ * place, dparams = dL/dparams).  Arguments and errors as tt_backward and
+ * tt_rank_update (params is written when lr > 0); a single-layer plan only.
+ * The result equals the two calls in a row. */
+tt_status tt_backward_rank_update(const tt_plan_t* plan, int64_t T, const void* x,
+                                  const void* dy, float* params, void* dx, float* dparams,
+                                  const tt_rank_opts* opts, void* ws, size_t ws_bytes,
+                                  void* stream);
+
 /* ---- TT-matrix (TTM) embedding lookup ---------------------------------------
  * [CoMERA project page, "Making small tensor operations fast on GPUs", bullet
  * "Embedding lookup without repeated work": keep only the unique rows of a

@@ -548,6 +548,15 @@ __device__ void eng_scale_unit(const EngTask& t, int u) {
   }
 }
 
+__device__ void eng_rank_unit(const EngTask& t, int u) {
+  const int64_t base = (int64_t)u * t.chunk;
+  for (int e = threadIdx.x; e < t.chunk; e += blockDim.x) {
+    const int64_t i = base + e;
+    if (i >= t.n) break;
+    rank_step_elem(t.out, t.dA, (int)i, i < t.len, t.rk);
+  }
+}
+
 constexpr int kEngSmem = kGemmSmem > kChainSmem ? kGemmSmem : kChainSmem;
 
 __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant__ EngProgram prog) {
@@ -608,6 +617,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
           tc_dd_unit(k.tc, k.s, k.rd, k.out, k.acc);
           break;
         case kEChain: eng_chain_unit(k, uu, pos, &pos_of, eng_dsm, nu); break;
+        case kERank: eng_rank_unit(k, uu); break;
         case kEUnpack:
           tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
           break;
@@ -801,6 +811,18 @@ void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const flo
   t->out = dDout;
   t->acc = acc ? 1 : 0;
   t->units = (int)ceil_div((L.N + L.M) * L.rd + L.rd, kPackPer);
+}
+
+void eng_rank_task(EngTask* t, const LayerPlan& L, float* params, float* dparams,
+                   const RankStep& r) {
+  t->kind = kERank;
+  t->out = params;
+  t->dA = dparams;
+  t->n = (int64_t)L.n_floats;
+  t->len = (int)L.diag_off[0];  // the cores come first
+  t->rk = r;
+  t->chunk = 4096;
+  t->units = (int)ceil_div(t->n, t->chunk);
 }
 
 bool eng_chain_task(EngTask* t, const ChainDesc& c) {

@@ -4,6 +4,7 @@
 // over all CTAs and a bounded grid barrier separates phases.
 #pragma once
 
+#include "rank_step.cuh"
 #include "tc_fused.h"
 #include "ttc_internal.h"
 
@@ -17,7 +18,8 @@ enum EngKind {
   kEPack = 4,      // tensor-core operands from A, B, D_d (+ zero gradient sums)
   kEUnpack = 5,    // compacted gradient sums -> dA, dB, dD_d
   kEDd = 6,        // compacted dD_d sum -> dD_d only
-  kEChain = 7      // rows of one side's merged chain, recomputed per prefix
+  kEChain = 7,     // rows of one side's merged chain, recomputed per prefix
+  kERank = 8       // the rank-adaptive step over one layer's packed parameters
 };
 
 // One side of the chain for kEChain: cores C_0..C_{L-1} (C_k of shape
@@ -82,6 +84,7 @@ struct alignas(16) EngTask {
   const float* fold_p = nullptr;
   float* fold_dd = nullptr;
   ChainDesc ch;  // kEChain (pack_side selects the packing, s = D_d)
+  RankStep rk;   // kERank: out = params, dA = dparams, n = floats, len = core floats
 };
 
 constexpr int kEngMaxTasks = 46;  // two order-6 layers (an FFN pair) in one program
@@ -132,6 +135,9 @@ void eng_dd_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* 
                  float* dDout, bool acc);
 void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
                      float* dA, float* dB, float* dDout, bool acc);
+// The rank-adaptive step (rank_step_elem) over the packed params / dparams.
+void eng_rank_task(EngTask* t, const LayerPlan& L, float* params, float* dparams,
+                   const RankStep& r);
 
 // Launch (cooperative when it has more than one phase: one CTA per SM).
 // Returns cudaSuccess or the error; cudaErrorInvalidValue for a program of

@@ -8,6 +8,7 @@
 #include <new>
 
 #include "merge_engine.h"
+#include "rank_step.cuh"
 #include "tc_fused.h"
 #include "ttc_internal.h"
 
@@ -409,6 +410,9 @@ struct MergeBwd {
   int steps = 0, pre = 0, nphases = 0;
   bool fold = false;
   TcPtrs tc;
+  // the rank-adaptive step as one more phase, after every read of params
+  const RankStep* rank = nullptr;
+  float* params_mut = nullptr;
   struct Side {
     int k_first, k_last;
     const float* Y;
@@ -585,6 +589,15 @@ tt_status run_merge_backward_multi(MergeBwd* const* layers, int n, cudaStream_t 
     b.begin_phase();
     for (int i = 0; i < n; ++i) layers[i]->add_phase(b, j);
   }
+  bool any_rank = false;
+  for (int i = 0; i < n; ++i) any_rank |= layers[i]->rank != nullptr;
+  if (any_rank) {
+    b.begin_phase();
+    for (int i = 0; i < n; ++i)
+      if (layers[i]->rank)
+        eng_rank_task(b.add(), layers[i]->L, layers[i]->params_mut, layers[i]->dparams,
+                      *layers[i]->rank);
+  }
   b.end();
   if (b.overflow) return TT_ERR_UNSUPPORTED;
   if (b.p.nphases == 0) return TT_OK;
@@ -598,8 +611,11 @@ tt_status run_merge_backward_multi(MergeBwd* const* layers, int n, cudaStream_t 
 tt_status run_merge_backward(const LayerPlan& L, const float* params, const float** P,
                              const float* dA, const float* dB, float* dparams, bool acc,
                              bool unpack, bool rezero, void* ws, const WsLayout& w,
-                             cudaStream_t st) {
+                             cudaStream_t st, const RankStep* rank = nullptr,
+                             float* params_mut = nullptr) {
   MergeBwd m(L, params, P, dA, dB, dparams, acc, unpack, rezero, ws, w);
+  m.rank = rank;
+  m.params_mut = params_mut;
   MergeBwd* one = &m;
   return run_merge_backward_multi(&one, 1, st);
 }
@@ -733,12 +749,15 @@ tt_status simt_backward_tokens(const LayerPlan& L, int64_t T, const void* x, int
 
 tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, const void* dy,
                          int tdy, const float* params, void* dx, int tdx, float* dparams,
-                         bool acc, void* ws, const WsLayout& w, cudaStream_t st) {
+                         bool acc, void* ws, const WsLayout& w, cudaStream_t st,
+                         const RankStep* rank = nullptr, float* params_mut = nullptr) {
   const float* P[kMaxK];
   if (tdy == TT_DT_F32 && use_small(L, T, tx, tdx)) {
     prof_begin(kPhBwd, st);
     tt_status s = small_f32_backward(L, T, x, dy, params, dx, dparams, acc, st);
     prof_end(kPhBwd, st);
+    if (s == TT_OK && rank)  // one CTA did the rest; the step is one more launch
+      TT_CUDA(rank_update_launch(L, params_mut, dparams, *rank, st));
     return s;
   }
   const bool tc = use_tc(L, tx, tdx) && tdy == tx;
@@ -775,7 +794,7 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   if (s != TT_OK) return s;
   prof_begin(kPhMergeBwd, st);
   s = run_merge_backward(L, params, P, fptr(ws, w.dA), fptr(ws, w.dB), dparams, acc, tc,
-                         tc && reuse, ws, w, st);
+                         tc && reuse, ws, w, st, rank, params_mut);
   prof_end(kPhMergeBwd, st);
   return s;
 }
@@ -931,6 +950,28 @@ tt_status tt_backward(const tt_plan_t* plan, int64_t T, const void* x, const voi
   const bool acc = (L.flags & TT_ACCUMULATE) != 0;
   return layer_backward(L, T, x, L.act, dy, L.act, params, dx, out_dtype(L.act), dparams, acc, ws,
                         w, st);
+}
+
+tt_status tt_backward_rank_update(const tt_plan_t* plan, int64_t T, const void* x,
+                                  const void* dy, float* params, void* dx, float* dparams,
+                                  const tt_rank_opts* opts, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (!plan || plan->kind != 0 || T < 0) return TT_ERR_INVALID_ARG;
+  const LayerPlan& L = plan->L[0];
+  RankStep r;
+  if (!rank_step_from(opts, &r)) return TT_ERR_INVALID_ARG;
+  if (!params || !dparams || !aligned(params, 4) || !aligned(dparams, 4))
+    return TT_ERR_INVALID_ARG;
+  if (T > 0 && (!act_aligned(x) || !act_aligned(dy) || !act_aligned(dx)))
+    return TT_ERR_INVALID_ARG;
+  WsLayout w;
+  size_t need = layer_layout(L, T, 256, &w);
+  tt_status s = check_ws(ws, ws_bytes, need);
+  if (s != TT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool acc = (L.flags & TT_ACCUMULATE) != 0;
+  return layer_backward(L, T, x, L.act, dy, L.act, params, dx, out_dtype(L.act), dparams, acc, ws,
+                        w, st, &r, params);
 }
 
 tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,

@@ -96,6 +96,14 @@ cudaError_t read_and_clear_device_status(DeviceStatus* out);
 // The same for the embedding kernels' own word (ttm.cu).
 cudaError_t read_and_clear_ttm_status(DeviceStatus* out);
 
+// ---- rank-adaptive step (rank_update.cu) ------------------------------------
+// One elementwise launch of the step over a layer's packed params / dparams.
+struct RankStep;
+cudaError_t rank_update_launch(const LayerPlan& L, float* params, float* dparams,
+                               const RankStep& r, cudaStream_t st);
+// The step's weights from tt_rank_opts (false for negative or non-finite ones).
+bool rank_step_from(const tt_rank_opts* opts, RankStep* r);
+
 // ---- measurement hooks (profile.cu) ---------------------------------------
 enum Phase { kPhMerge = 0, kPhFwd = 1, kPhBwd = 2, kPhMergeBwd = 3, kPhElem = 4 };
 void prof_begin(int phase, cudaStream_t st);

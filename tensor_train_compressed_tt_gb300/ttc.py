@@ -101,6 +101,7 @@ def lib() -> ctypes.CDLL:
             "tt_ffn_forward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_rank_update": [_P, _P, _P, _P, _P],
+            "tt_backward_rank_update": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ttm_plan": [_P, _P],
             "tt_ttm_lookup": [_P, _I64, _P, _P, _P, _P, _SZ, _P],
             "tt_ttm_lookup_backward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
@@ -250,6 +251,15 @@ def tt_rank_update(plan: Plan, params: int, dparams: int, gamma: float, beta: fl
     o = tt_rank_opts(float(gamma), float(beta), float(lr))
     return lib().tt_rank_update(ctypes.c_void_p(plan.handle), params, dparams,
                                 ctypes.byref(o), stream)
+
+
+def tt_backward_rank_update(plan: Plan, T: int, x: int, dy: int, params: int, dx: int,
+                            dparams: int, gamma: float, beta: float, lr: float, ws: int,
+                            ws_bytes: int, stream: int = 0) -> int:
+    """tt_backward then the rank-adaptive step, the step inside the merge program."""
+    o = tt_rank_opts(float(gamma), float(beta), float(lr))
+    return lib().tt_backward_rank_update(ctypes.c_void_p(plan.handle), int(T), x, dy, params, dx,
+                                         dparams, ctypes.byref(o), ws, int(ws_bytes), stream)
 
 
 def make_ttm_desc(row_modes: Sequence[int], col_modes: Sequence[int], ranks: Sequence[int],

@@ -205,6 +205,15 @@ def test_argument_errors_return_before_any_launch(lib):
     w = synth.WORKLOADS["ffn768_3072_bf16"]
     ffn = ttc.tt_ffn_plan(_desc(w.layers[0]), _desc(w.layers[1]))
     assert ttc.tt_rank_update(ffn, fake, fake, 0.1, 0.1, 0.1) == 1
+    # backward with the fused step: the step's weights and the plan kind first
+    assert ttc.tt_backward_rank_update(plan, 64, fake, fake, fake, fake, fake, -1.0, 0.1, 0.1,
+                                       fake, ws_need) == 1
+    assert ttc.tt_backward_rank_update(plan, 64, fake, fake, fake, fake, fake, 0.1, float("nan"),
+                                       0.1, fake, ws_need) == 1
+    assert ttc.tt_backward_rank_update(ffn, 64, fake, fake, fake, fake, fake, 0.1, 0.1, 0.1,
+                                       fake, ws_need) == 1
+    assert ttc.tt_backward_rank_update(plan, 64, fake, fake, fake, fake, fake, 0.1, 0.1, 0.1,
+                                       fake, ws_need - 1) == 3
 
 
 def test_noalloc_rejections_before_any_launch(lib):

@@ -84,3 +84,51 @@ def test_pruned_by_the_step_equals_truncated_tt():
     out_t = gpu_layer(ts, w.act, synth.LayerInputs(tc, td), inp.x, inp.dy)
     assert O.rel_err(out["y"], out_t["y"]) <= TOL[w.act]
     assert O.rel_err(out["dx"], out_t["dx"]) <= TOL[w.act]
+
+
+@pytest.mark.parametrize("name,T", [("tt768_bf16", 2000), ("pruned768_3072_bf16", 700),
+                                    ("tiny64_f32", 16), ("tt1024_4096_bf16", 1000)])
+@pytest.mark.parametrize("gamma,beta,lr", [(0.05, 0.01, 0.0), (0.6, 0.02, 1.0)])
+def test_backward_with_fused_rank_step_equals_the_two_calls(name, T, gamma, beta, lr):
+    """tt_backward_rank_update (the step as the last phase of the backward's
+    merge program) gives the bits of tt_backward then tt_rank_update, and its
+    step is the oracle's float32 step on the gradients it produced.  The
+    plans are deterministic, so the two backward passes sum in one order."""
+    from tensor_train_compressed_tt_gb300 import ttc
+    from parity_util import TORCH_DT, to_dev
+    w = synth.WORKLOADS[name]
+    s = w.layers[0]
+    inp = synth.draw(w, seed=31, tokens=T)
+    act = {"bf16": ttc.TT_DT_BF16, "f32": ttc.TT_DT_F32}[w.act]
+    plan = ttc.tt_plan(ttc.make_desc(s.in_modes, s.out_modes, s.ranks, act,
+                                     ttc.TT_DETERMINISTIC))
+    x, dy = to_dev(inp.x, w.act), to_dev(inp.dy, w.act)
+    p0 = torch.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
+    st = torch.cuda.current_stream().cuda_stream
+    ws = torch.empty(ttc.tt_workspace_size(plan, T), dtype=torch.uint8, device="cuda")
+    outs = []
+    for fused in (False, True):
+        p = p0.clone()
+        g = torch.empty_like(p0)
+        dx = torch.empty((T, s.N), dtype=TORCH_DT[w.act], device="cuda")
+        if fused:
+            ttc.check(ttc.tt_backward_rank_update(plan, T, x.data_ptr(), dy.data_ptr(),
+                                                  p.data_ptr(), dx.data_ptr(), g.data_ptr(),
+                                                  gamma, beta, lr, ws.data_ptr(), ws.numel(), st))
+        else:
+            ttc.check(ttc.tt_backward(plan, T, x.data_ptr(), dy.data_ptr(), p.data_ptr(),
+                                      dx.data_ptr(), g.data_ptr(), ws.data_ptr(), ws.numel(), st))
+            grad = g.clone()
+            ttc.check(ttc.tt_rank_update(plan, p.data_ptr(), g.data_ptr(), gamma, beta, lr, st))
+        torch.cuda.synchronize()
+        outs.append((p, g, dx))
+    (p1, g1, dx1), (p2, g2, dx2) = outs
+    assert torch.equal(dx1, dx2)
+    assert torch.equal(p1, p2) and torch.equal(g1, g2)
+    # the step itself against the oracle, on the gradients the backward produced
+    gc, gd = synth.unpack(s, grad.cpu().numpy())
+    oc, od, odc, odd = O.rank_update_f32(inp.layers[0].cores, inp.layers[0].diags, gc, gd,
+                                         gamma, beta, lr)
+    assert np.array_equal(_bits(p2.cpu().numpy()), _bits(synth.pack(oc, od)))
+    assert np.array_equal(_bits(g2.cpu().numpy()), _bits(synth.pack(odc, odd)))
+    assert ttc.tt_get_device_status(st) == 0
