@@ -1149,6 +1149,172 @@ def run_ttm_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# The TT layers of one encoder block (Q, K, V, O and the FFN pair) as one step
+
+
+def encoder_oracle_step(inp):
+    from oracle import tt_oracle as O
+    import numpy as np
+
+    def f64(li):
+        return ([c.astype(np.float64) for c in li.cores], [e.astype(np.float64) for e in li.diags])
+    xin = {"q": inp.x, "k": inp.x, "v": inp.x, "o": inp.xo}
+    for nm in ("q", "k", "v", "o"):
+        c, d = f64(inp.layers[nm])
+        O.chained_forward(c, d, 3, xin[nm])
+        O.chained_backward(c, d, 3, xin[nm], inp.dy[nm])
+    up, dn = f64(inp.layers["up"]), f64(inp.layers["down"])
+    O.ffn_forward(up, dn, 3, 3, inp.xf)
+    O.ffn_backward(up, dn, 3, 3, inp.xf, inp.dy["ffn"])
+
+
+def run_encoder(args):
+    import torch
+
+    from tensor_train_compressed_tt_gb300 import _build, synth, ttc
+    from tensor_train_compressed_tt_gb300.encoder import TTEncoderBlock
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not os.path.exists(ttc.LIB_PATH):
+        _build.build()
+    T = args.tokens or 16384
+    inp = synth.draw_encoder(T, seed=rank)
+    blk = TTEncoderBlock(deterministic=args.deterministic)
+    params = {nm: torch.from_numpy(synth.pack(li.cores, li.diags)).to(dev)
+              for nm, li in inp.layers.items()}
+    b = blk.buffers(T, dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    set_bytes = T * 768 * 2 * 8 + 10 * T * 768 * 2   # 8 inputs, 10 outputs of 768 columns, bf16
+    nsets = max(2, -(-2 * l2 // set_bytes) + 1)
+    sets = []
+    for i in range(nsets):
+        if i == 0:
+            d = lambda a: torch.from_numpy(a).to(dev).bfloat16()  # noqa: E731
+            sets.append((d(inp.x), d(inp.xo), d(inp.xf), {k: d(v) for k, v in inp.dy.items()}))
+            continue
+        g = torch.Generator(device=dev)
+        g.manual_seed(1000 * rank + i)
+        r = lambda: torch.randn((T, 768), generator=g, device=dev).bfloat16()  # noqa: E731
+        sets.append((r(), r(), r(), {k: r() for k in ("q", "k", "v", "o", "ffn")}))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        x, xo, xf, dy = sets[i % nsets]
+        blk.step(x, xo, xf, dy, params, b)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    W = max(3, args.warmup)
+    for i in range(W):
+        step(i)
+    ttc.check(ttc.tt_get_device_status(int(stream.cuda_stream)), "device status after warm-up")
+    barrier()
+    graph, note, per_step = None, "eager", None
+    if not args.eager:
+        g = torch.cuda.CUDAGraph()
+        c0 = ttc.lib().tt_launch_count()
+        with torch.cuda.graph(g):
+            for j in range(nsets):
+                step(j)
+        per_step = int(ttc.lib().tt_launch_count() - c0) // nsets
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        graph, note = g, f"cuda_graph ({nsets} block steps per replay, one per input set)"
+
+    def run(i):
+        if graph is not None:
+            if i % nsets == 0:
+                graph.replay()
+        else:
+            step(i)
+    K = args.steps if args.steps is not None else 8
+    if graph is not None:
+        K = -(-K // nsets) * nsets
+    barrier()
+    uuid = getattr(props, "uuid", None)
+    clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    l0 = ttc.lib().tt_launch_count()
+    rep_ms, windows = timed_repeats(run, K, barrier, stream, args.target_seconds)
+    launches = int(ttc.lib().tt_launch_count() - l0) // len(rep_ms)
+    if graph is not None:
+        launches = K * per_step
+    clk = clocks.stop()
+    if clk is not None:
+        clk["by_repeat_group"] = clocks.binned(windows, rep_ms)
+    rep = spread(rep_ms)
+    ms = all_reduce_scalar(rep["median"], "max", dev)
+    ttc.check(ttc.tt_get_device_status(int(stream.cuda_stream)), "device status after timing")
+    peak, peak_kind = measured_peaks()
+    # summed algorithmic work of the block's TT layers: per layer x read by
+    # both passes, dy read, y and dx written (bf16), and 6 T r (N + M) FLOP
+    byts, flop = 0, 0
+    for nm in ("q", "k", "v", "o"):
+        sh = synth.ENCODER_LAYERS[nm]
+        byts += 2 * T * (3 * sh.N + 2 * sh.M)
+        flop += 6 * T * sh.ranks[sh.d] * (sh.N + sh.M)
+    byts += 2 * T * (3 * 768 + 2 * 768)   # the FFN pair: x, y, dy, dx of the pair
+    for nm in ("up", "down"):
+        sh = synth.ENCODER_LAYERS[nm]
+        flop += 6 * T * sh.ranks[sh.d] * (sh.N + sh.M)
+    t_roof = byts / (peak * 1e9)
+    value = whole_job_rate(T, world, ms)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        small = synth.draw_encoder(256, seed=0)
+        encoder_oracle_step(small)
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 10.0:
+            encoder_oracle_step(small)
+            n += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": n * 256 / el, "unit": "tokens/s", "cores": oracle_threads(),
+               "kind": "oracle", "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+               "sample": f"{n} block steps of the fp64 numpy oracle on 256 of the {T} tokens "
+                         f"({el:.1f} s)"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "timing": dict(rep, note="ms_per_step is the median over repeats of the K-step "
+                                     "region, max over ranks"),
+            "config": {"workload": "encoder768_bf16",
+                       "description": "the TT layers of one encoder block: Q, K, V, O "
+                                      "(768x768, ranks 30) and the GELU FFN pair "
+                                      "768->3072->768, fwd+bwd of all, 16384 tokens, bf16",
+                       "tokens": T, "parallelism": f"replicas x{world}", "launch": note,
+                       "deterministic": bool(args.deterministic),
+                       "l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.0f} MB"},
+            "roofline": {"bound": "hbm", "kernel": "whole block step (summed)",
+                         "achieved": byts / (ms * 1e-3) / 1e9, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": t_roof / (ms * 1e-3), "traffic": None,
+                         "algorithmic_bytes_per_step": byts},
+            "roofline_step": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3),
+                              "algorithmic_bytes": byts, "algorithmic_flop": flop,
+                              "peak_gbs": peak, "peak_kind": peak_kind},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.oracle_rate:
@@ -1161,6 +1327,13 @@ def main():
             run_ttm_reference(args, w)
         else:
             run_ttm(args, w)
+        return
+    if args.workload == "encoder768_bf16":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the reference arm times single workloads; use --workload"}))
+        else:
+            run_encoder(args)
         return
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -223,6 +223,44 @@ def draw(w: Workload, seed: int = 0, tokens: Optional[int] = None) -> WorkloadIn
     return WorkloadInputs(layers, x, dy)
 
 
+# ---------------------------------------------------------------------------
+# The TT layers of one transformer encoder block (the project page's
+# six-encoder model, "Results": the attention projections Q, K, V, O at
+# 768 x 768 and the feed-forward pair 768 -> 3072 -> 768, every one a
+# rank-30 TT as in the rank table "Internal tensor-train ranks of each layer
+# in one encoder block").  Q, K and V read the same input x; O reads the
+# attention output and the FFN pair the block's middle activations, for which
+# independent synthetic tensors stand in (the attention itself is not a TT
+# layer).  Distributions as "tt768_bf16": cores N(0, 0.05), D ~ U(0.5, 1.5),
+# activations and upstream gradients bf16 N(0, 1).
+
+ENCODER_LAYERS = {"q": _L768_768, "k": _L768_768, "v": _L768_768, "o": _L768_768,
+                  "up": _L768_3072, "down": _L3072_768}
+
+
+@dataclasses.dataclass
+class EncoderInputs:
+    layers: dict        # name -> LayerInputs ("q", "k", "v", "o", "up", "down")
+    x: np.ndarray       # (T, 768): input of Q, K and V
+    xo: np.ndarray      # (T, 768): input of O (stands in for the attention output)
+    xf: np.ndarray      # (T, 768): input of the FFN pair
+    dy: dict            # "q", "k", "v", "o", "ffn" -> (T, 768) upstream gradients
+
+
+def draw_encoder(tokens: int = 16384, seed: int = 0) -> EncoderInputs:
+    """The block's inputs, from one seeded stream: the layers' cores and
+    diagonals in the order q, k, v, o, up, down, then x, xo, xf, then the
+    upstream gradients of q, k, v, o and the FFN pair."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    layers = {nm: draw_layer(rng, sh, 0.05, "uniform") for nm, sh in ENCODER_LAYERS.items()}
+
+    def act(n):
+        return round_bf16(rng.standard_normal((tokens, n)).astype(np.float32))
+    x, xo, xf = act(768), act(768), act(768)
+    dy = {nm: act(768) for nm in ("q", "k", "v", "o", "ffn")}
+    return EncoderInputs(layers, x, xo, xf, dy)
+
+
 def random_shape(rng: np.random.Generator, d: int, max_mode: int = 4,
                  max_rank: int = 4) -> LayerShape:
     """A small random TT shape for sweep tests (ranks not capped: any r >= 1 is a TT)."""
