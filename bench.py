@@ -1191,7 +1191,7 @@ def run_encoder(args):
     b = blk.buffers(T, dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
-    set_bytes = T * 768 * 2 * 8 + 10 * T * 768 * 2   # 8 inputs, 10 outputs of 768 columns, bf16
+    set_bytes = T * 768 * 2 * 8 + 8 * T * 768 * 2   # 8 inputs, 8 outputs of 768 columns, bf16
     nsets = max(2, -(-2 * l2 // set_bytes) + 1)
     sets = []
     for i in range(nsets):
@@ -1259,12 +1259,15 @@ def run_encoder(args):
     ms = all_reduce_scalar(rep["median"], "max", dev)
     ttc.check(ttc.tt_get_device_status(int(stream.cuda_stream)), "device status after timing")
     peak, peak_kind = measured_peaks()
-    # summed algorithmic work of the block's TT layers: per layer x read by
-    # both passes, dy read, y and dx written (bf16), and 6 T r (N + M) FLOP
+    # summed algorithmic work of the block's TT layers: per input x read by
+    # both passes and its dx written once (Q, K and V share theirs), per layer
+    # dy read and y written (bf16), and 6 T r (N + M) FLOP a layer
     byts, flop = 0, 0
     for nm in ("q", "k", "v", "o"):
         sh = synth.ENCODER_LAYERS[nm]
-        byts += 2 * T * (3 * sh.N + 2 * sh.M)
+        byts += 2 * T * 2 * sh.M
+        if nm in ("q", "o"):
+            byts += 2 * T * 3 * sh.N
         flop += 6 * T * sh.ranks[sh.d] * (sh.N + sh.M)
     byts += 2 * T * (3 * 768 + 2 * 768)   # the FFN pair: x, y, dy, dx of the pair
     for nm in ("up", "down"):

@@ -97,8 +97,9 @@ typedef enum tt_dtype { TT_DT_F32 = 0, TT_DT_BF16 = 1, TT_DT_E4M3 = 2 } tt_dtype
  * tt_workspace_size), and the backward reads it instead of computing x A
  * again, so it streams x once instead of twice.  The caller guarantees in
  * addition that the backward gets the forward's x and T.  The f32 path
- * ignores it.  In a bf16 FFN plan the backward also takes h = TT_up(x) and
- * GELU(h) from the forward's workspace instead of recomputing them. */
+ * ignores it.  In a bf16 FFN plan (and a bf16 multi-layer plan) every layer
+ * keeps its z' the same way; without the flag the fused FFN and multi-layer
+ * backward compute them first (one more pass over x). */
 #define TT_REUSE_Z 4u
 /* Bit-reproducible gradients: the same inputs give the same dx and dparams
  * bit for bit, run after run, on a given GPU model.  Every sum over tokens
@@ -141,17 +142,22 @@ tt_status tt_default_ranks(int d, const int* in_modes, const int* out_modes, int
  * least 128, middle rank r_d <= 64): E4M3 has no other path. */
 tt_status tt_plan(const tt_desc* desc, tt_plan_t** out);
 
-/* FFN pair y = TT_down(GELU(TT_up(x))) with the erf GELU h Phi(h) (erf to
- * within 1.5e-7, Abramowitz and Stegun 7.1.26); up's output
- * width must equal down's input width and both must use the same act type
- * (F32 or BF16; E4M3 gives TT_ERR_UNSUPPORTED). */
+/* FFN pair y = TT_down(GELU(TT_up(x))) with GELU(h) = h Phi(h).  Up's
+ * output width must equal down's input width and both must use the same act
+ * type and flags (F32 or BF16; E4M3 gives TT_ERR_UNSUPPORTED).  A bf16 pair
+ * whose layers fit the tensor-core kernels runs fused, h never leaving the
+ * SM, with Phi(h) = (1 + tanh(sqrt(2/pi)(h + 0.044715 h^3))) / 2 (Hendrycks
+ * and Gimpel's tanh form; |Phi error| <= 1.8e-4, below a bf16 rounding of
+ * h); every other pair evaluates erf to within 1.5e-7 (Abramowitz and
+ * Stegun 7.1.26). */
 tt_status tt_ffn_plan(const tt_desc* up, const tt_desc* down, tt_plan_t** out);
 
 void tt_destroy(tt_plan_t* plan);
 
 /* Offsets (in floats) of every core and diagonal inside the packed parameter
  * buffer: core_off receives 2d values, diag_off 2d-1, *n_floats the total.
- * For an FFN plan these describe the up layer; use tt_ffn_param_layout. */
+ * For an FFN plan these describe the up layer (use tt_ffn_param_layout), for
+ * a multi-layer plan its first layer (use tt_multi_param_layout). */
 tt_status tt_param_layout(const tt_plan_t* plan, size_t* core_off, size_t* diag_off,
                           size_t* n_floats);
 tt_status tt_ffn_param_layout(const tt_plan_t* plan, int layer /*0 up, 1 down*/,
@@ -195,6 +201,32 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
                           const float* params_up, const float* params_down, void* dx,
                           float* dparams_up, float* dparams_down, void* ws, size_t ws_bytes,
                           void* stream);
+
+/* ---- several layers on one input --------------------------------------------
+ * Up to TT_MULTI_MAX layers that read the same x: the Q, K and V projections
+ * of an encoder block's attention (CoMERA project page, "Results", rank
+ * table: the attention rows, 768 x 768 at rank 30 each).  The results are
+ * those of one tt_forward / tt_backward per layer, except that the backward
+ * returns the sum dx = sum_g dy_g W_g (the gradient of x, which feeds every
+ * layer).  A bf16 plan whose layers all fit the tensor-core kernels (and
+ * without TT_DETERMINISTIC) runs every token pass as one kernel over all
+ * layers, streaming x once for all of them (twice in a backward without
+ * TT_REUSE_Z); otherwise the layers run one after another and dx is their
+ * sum, taken in layer order.  params, y, dy, dparams are host arrays of n
+ * device pointers, one per layer, in the descs' order. */
+#define TT_MULTI_MAX 3
+/* descs: n (1..TT_MULTI_MAX) layers with the same input modes, act type and
+ * flags (else TT_ERR_INVALID_ARG); other errors as tt_plan. */
+tt_status tt_multi_plan(const tt_desc* descs, int n, tt_plan_t** out);
+/* The packed parameter layout of layer `layer` (0..n-1) of a multi plan. */
+tt_status tt_multi_param_layout(const tt_plan_t* plan, int layer, size_t* core_off,
+                                size_t* diag_off, size_t* n_floats);
+tt_status tt_multi_forward(const tt_plan_t* plan, int64_t T, const void* x,
+                           const float* const* params, void* const* y, void* ws,
+                           size_t ws_bytes, void* stream);
+tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
+                            const void* const* dy, const float* const* params, void* dx,
+                            float* const* dparams, void* ws, size_t ws_bytes, void* stream);
 
 /* Rank-adaptive step [CoMERA project page, "Learn the ranks while
  * training": the early-stage objective L(G, D) + gamma S_hat(D) + beta ||G||^2,

@@ -269,6 +269,17 @@ __global__ void gelu_bwd_bf16_kernel(int64_t n8, const uint4* __restrict__ h, ui
   }
 }
 
+template <typename T>
+__global__ void sum_into_kernel(int64_t n, T* out, const T* p0, const T* p1, int nparts) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v = ld_as_f32<T>(out, i);
+    v += ld_as_f32<T>(p0, i);
+    if (nparts > 1) v += ld_as_f32<T>(p1, i);
+    st_from_f32<T>(out, i, v);
+  }
+}
+
 unsigned grid_for(int64_t n, int threads) {
   int64_t b = (n + threads - 1) / threads;
   if (b > 65535LL * 8) b = 65535LL * 8;
@@ -336,6 +347,23 @@ cudaError_t gelu_bwd_bf16(int64_t n, const void* h, void* da, cudaStream_t st) {
   if (n % 8) return cudaErrorInvalidValue;
   gelu_bwd_bf16_kernel<<<grid_for((n / 8 + kWords - 1) / kWords, 256), 256, 0, st>>>(
       n / 8, static_cast<const uint4*>(h), static_cast<uint4*>(da));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t sum_into(int64_t n, void* out, const void* const* parts, int nparts, int type,
+                     cudaStream_t st) {
+  if (n <= 0 || nparts <= 0) return cudaSuccess;
+  if (nparts > 2) return cudaErrorInvalidValue;
+  const void* p1 = nparts > 1 ? parts[1] : parts[0];
+  if (type == TT_DT_BF16)
+    sum_into_kernel<__nv_bfloat16><<<grid_for(n, 256), 256, 0, st>>>(
+        n, static_cast<__nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(parts[0]),
+        static_cast<const __nv_bfloat16*>(p1), nparts);
+  else
+    sum_into_kernel<float><<<grid_for(n, 256), 256, 0, st>>>(
+        n, static_cast<float*>(out), static_cast<const float*>(parts[0]),
+        static_cast<const float*>(p1), nparts);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -1563,6 +1563,7 @@ extern "C" tt_status tt_debug_skip_arrival(int site) {
 
 #include "merge_engine.cuh"
 #include "ffn_fused.cuh"
+#include "qkv_fused.cuh"
 
 #ifdef TTC_TIMELINE
 extern "C" int ttc_timeline_read(void* host, size_t bytes) {

@@ -92,4 +92,22 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
                           const void* zs1, const void* zs2, float* zero1, size_t n1,
                           float* zero2, size_t n2, cudaStream_t st);
 
+// ---- several layers on one input (qkv_fused.cuh) ----------------------------
+// True when G (1..3) layers of equal input width all fit the tensor-core kernels.
+bool multi_tc_supported(const LayerPlan* Ls, int G);
+
+// y[g] = x W_g^T for every layer g, x streamed once; layer g's packed
+// operands at offs[g] of ws.  With zs (G pointers, T x 64 bf16 each) every
+// z'_g is kept there; y may be null when zs is given (then only z'_g).
+tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x, void* const* y,
+                           void* ws, const size_t* offs, void* const* zs, cudaStream_t st);
+
+// dx = sum_g dy[g] W_g and every layer's token sums (dAc, dBc, dDc, zeroed
+// beforehand) from x, dy[g] and the forward's z'_g; x streamed once.
+// zero[g][0, zero_n[g]) is set to 0 on the way, also when T == 0.
+tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x,
+                            const void* const* dy, void* dx, void* ws, const size_t* offs,
+                            const void* const* zs, float* const* zero, const size_t* zero_n,
+                            cudaStream_t st);
+
 }  // namespace ttc

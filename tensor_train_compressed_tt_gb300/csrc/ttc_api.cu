@@ -353,25 +353,40 @@ tt_status run_merge_forward(const LayerPlan& L, const float* params, void* ws, c
   return TT_OK;
 }
 
-// Both layers' forward merges of an FFN pair in one launch where they fit
-// the chain units (else one launch each).
+// The forward merges of n layers in one launch where they all fit the chain
+// units and the program's task table (else one launch each).
+tt_status run_merge_forward_n(int n, const LayerPlan* const* Ls, const float* const* params,
+                              const WsLayout* const* wl, const float** const* P, void* ws,
+                              bool zero_grads, cudaStream_t st) {
+  bool fit = true;
+  for (int i = 0; i < n && fit; ++i) fit = chain_merge_fits(*Ls[i], params[i], ws, *wl[i]);
+  if (fit) {
+    EngBuilder b;
+    b.begin_phase();
+    for (int i = 0; i < n; ++i) add_merge_forward(b, *Ls[i], params[i], ws, *wl[i], P[i], true, zero_grads);
+    b.end();
+    if (!b.overflow) {
+      if (b.p.ntasks > 0) TT_CUDA(eng_launch(b.p, st));
+      return TT_OK;
+    }
+  }
+  for (int i = 0; i < n; ++i) {
+    tt_status s = run_merge_forward(*Ls[i], params[i], ws, *wl[i], P[i], true, zero_grads, st);
+    if (s != TT_OK) return s;
+  }
+  return TT_OK;
+}
+
+// Both layers' forward merges of an FFN pair.
 tt_status run_merge_forward2(const LayerPlan& U, const float* pu, const WsLayout& wu,
                              const float** PU, const LayerPlan& D, const float* pd,
                              const WsLayout& wd, const float** PD, void* ws, bool zero_grads,
                              cudaStream_t st) {
-  if (!chain_merge_fits(U, pu, ws, wu) || !chain_merge_fits(D, pd, ws, wd)) {
-    tt_status s = run_merge_forward(U, pu, ws, wu, PU, true, zero_grads, st);
-    return s != TT_OK ? s : run_merge_forward(D, pd, ws, wd, PD, true, zero_grads, st);
-  }
-  EngBuilder b;
-  b.begin_phase();
-  add_merge_forward(b, U, pu, ws, wu, PU, true, zero_grads);
-  add_merge_forward(b, D, pd, ws, wd, PD, true, zero_grads);
-  b.end();
-  if (b.overflow) return TT_ERR_UNSUPPORTED;
-  if (b.p.ntasks == 0) return TT_OK;
-  TT_CUDA(eng_launch(b.p, st));
-  return TT_OK;
+  const LayerPlan* Ls[2] = {&U, &D};
+  const float* params[2] = {pu, pd};
+  const WsLayout* wl[2] = {&wu, &wd};
+  const float** P[2] = {PU, PD};
+  return run_merge_forward_n(2, Ls, params, wl, P, ws, zero_grads, st);
 }
 
 // Backward through the merges.  For one side with cores k_first..k_last and
@@ -799,6 +814,38 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   return s;
 }
 
+// ---- several layers on one input ---------------------------------------------
+struct MultiLayout {
+  WsLayout w[3];
+  size_t dxp[2] = {};  // layer-by-layer backward: dx of layers 1, 2 before the sum
+  size_t end = 0;
+};
+
+// The layers run on the multi-layer kernels when all of them fit the bf16
+// tensor-core path and no fixed summation order is asked for.
+bool multi_fused(const tt_plan_s* p) {
+  return p->L[0].act == TT_DT_BF16 && !(p->L[0].flags & TT_DETERMINISTIC) &&
+         multi_tc_supported(p->L, p->G);
+}
+
+// One region a layer (its merges, packed operands and, fused, its z'),
+// then (layer by layer) the partial dx buffers.
+size_t multi_layout(const tt_plan_s* p, int64_t T, MultiLayout* m) {
+  const bool fused = multi_fused(p);
+  size_t off = 256;
+  for (int g = 0; g < p->G; ++g)
+    off = align_up(layer_layout(p->L[g], T, off, &m->w[g], false, fused), 256);
+  if (!fused) {
+    const size_t esz = out_dtype(p->L[0].act) == TT_DT_F32 ? 4 : 2;
+    for (int g = 1; g < p->G; ++g) {
+      m->dxp[g - 1] = off;
+      off = align_up(off + (size_t)T * p->L[0].N * esz, 256);
+    }
+  }
+  m->end = off;
+  return off;
+}
+
 tt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
   if (!ws || !aligned(ws, 256)) return TT_ERR_WORKSPACE;
   if (ws_bytes < need) return TT_ERR_WORKSPACE;
@@ -905,7 +952,10 @@ tt_status tt_ffn_param_layout(const tt_plan_t* plan, int layer, size_t* core_off
 
 tt_status tt_workspace_size(const tt_plan_t* plan, int64_t T, size_t* bytes) {
   if (!plan || !bytes || T < 0) return TT_ERR_INVALID_ARG;
-  if (plan->kind == 0) {
+  if (plan->kind == 3) {
+    MultiLayout m;
+    *bytes = multi_layout(plan, T, &m);
+  } else if (plan->kind == 0) {
     WsLayout w;
     *bytes = layer_layout(plan->L[0], T, 256, &w);
   } else if (plan->kind == 2) {
@@ -1123,6 +1173,160 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
   }
   return layer_backward(U, T, x, U.act, da, TT_DT_F32, params_up, dx, U.act, dparams_up, acc,
                         ws, f.up, st);
+}
+
+tt_status tt_multi_plan(const tt_desc* descs, int n, tt_plan_t** out) {
+  if (!out) return TT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!descs || n < 1 || n > TT_MULTI_MAX) return TT_ERR_INVALID_ARG;
+  LayerPlan L[TT_MULTI_MAX];
+  for (int g = 0; g < n; ++g) {
+    tt_status s = build_layer(&descs[g], &L[g]);
+    if (s != TT_OK) return s;
+    if (L[g].act != L[0].act || L[g].flags != L[0].flags || L[g].d != L[0].d)
+      return TT_ERR_INVALID_ARG;
+    for (int k = 0; k < L[0].d; ++k)
+      if (descs[g].in_modes[k] != descs[0].in_modes[k]) return TT_ERR_INVALID_ARG;
+    if (L[g].act == TT_DT_E4M3 && !tc_f8_supported(L[g])) return TT_ERR_UNSUPPORTED;
+  }
+  tt_plan_s* p = new (std::nothrow) tt_plan_s();
+  if (!p) return TT_ERR_INVALID_ARG;
+  p->kind = 3;
+  p->G = n;
+  for (int g = 0; g < n; ++g) p->L[g] = L[g];
+  *out = p;
+  return TT_OK;
+}
+
+tt_status tt_multi_param_layout(const tt_plan_t* plan, int layer, size_t* core_off,
+                                size_t* diag_off, size_t* n_floats) {
+  if (!plan || plan->kind != 3 || layer < 0 || layer >= plan->G) return TT_ERR_INVALID_ARG;
+  return layout_out(plan->L[layer], core_off, diag_off, n_floats);
+}
+
+tt_status tt_multi_forward(const tt_plan_t* plan, int64_t T, const void* x,
+                           const float* const* params, void* const* y, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!plan || plan->kind != 3 || T < 0 || !params || !y) return TT_ERR_INVALID_ARG;
+  const int G = plan->G;
+  for (int g = 0; g < G; ++g)
+    if (!params[g] || !aligned(params[g], 4)) return TT_ERR_INVALID_ARG;
+  if (T == 0) return TT_OK;
+  if (!act_aligned(x)) return TT_ERR_INVALID_ARG;
+  for (int g = 0; g < G; ++g)
+    if (!act_aligned(y[g])) return TT_ERR_INVALID_ARG;
+  MultiLayout m;
+  tt_status s = check_ws(ws, ws_bytes, multi_layout(plan, T, &m));
+  if (s != TT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int act = plan->L[0].act;
+  if (!multi_fused(plan)) {
+    for (int g = 0; g < G && s == TT_OK; ++g)
+      s = layer_forward(plan->L[g], T, x, act, params[g], y[g], out_dtype(act), ws, m.w[g], st);
+    return s;
+  }
+  const bool reuse = (plan->L[0].flags & TT_REUSE_MERGE) != 0;
+  const bool keep = (plan->L[0].flags & TT_REUSE_Z) != 0;
+  const LayerPlan* Ls[TT_MULTI_MAX];
+  const WsLayout* wl[TT_MULTI_MAX];
+  const float* P[TT_MULTI_MAX][kMaxK];
+  const float** Pp[TT_MULTI_MAX];
+  void* zs[TT_MULTI_MAX];
+  size_t offs[TT_MULTI_MAX];
+  for (int g = 0; g < G; ++g) {
+    Ls[g] = &plan->L[g];
+    wl[g] = &m.w[g];
+    Pp[g] = P[g];
+    zs[g] = static_cast<char*>(ws) + m.w[g].zs;
+    offs[g] = m.w[g].tc;
+  }
+  prof_begin(kPhMerge, st);
+  s = run_merge_forward_n(G, Ls, params, wl, Pp, ws, reuse, st);
+  prof_end(kPhMerge, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhFwd, st);
+  s = multi_tc_forward(plan->L, G, T, x, y, ws, offs, keep ? zs : nullptr, st);
+  prof_end(kPhFwd, st);
+  return s;
+}
+
+tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
+                            const void* const* dy, const float* const* params, void* dx,
+                            float* const* dparams, void* ws, size_t ws_bytes, void* stream) {
+  if (!plan || plan->kind != 3 || T < 0 || !params || !dparams || !dy)
+    return TT_ERR_INVALID_ARG;
+  const int G = plan->G;
+  for (int g = 0; g < G; ++g) {
+    if (!params[g] || !dparams[g] || !aligned(params[g], 4) || !aligned(dparams[g], 4))
+      return TT_ERR_INVALID_ARG;
+    if (T > 0 && !act_aligned(dy[g])) return TT_ERR_INVALID_ARG;
+  }
+  if (T > 0 && (!act_aligned(x) || !act_aligned(dx))) return TT_ERR_INVALID_ARG;
+  MultiLayout m;
+  tt_status s = check_ws(ws, ws_bytes, multi_layout(plan, T, &m));
+  if (s != TT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int act = plan->L[0].act;
+  const bool acc = (plan->L[0].flags & TT_ACCUMULATE) != 0;
+  if (!multi_fused(plan)) {
+    // layer by layer: layer 0's dx into dx, the others' beside it, then the sum
+    const void* parts[TT_MULTI_MAX - 1];
+    for (int g = 0; g < G && s == TT_OK; ++g) {
+      void* dxg = g == 0 ? dx : static_cast<char*>(ws) + m.dxp[g - 1];
+      if (g > 0) parts[g - 1] = dxg;
+      s = layer_backward(plan->L[g], T, x, act, dy[g], act, params[g], dxg, out_dtype(act),
+                         dparams[g], acc, ws, m.w[g], st);
+    }
+    if (s != TT_OK || T == 0 || G == 1) return s;
+    prof_begin(kPhElem, st);
+    TT_CUDA(sum_into(T * plan->L[0].N, dx, parts, G - 1, out_dtype(act), st));
+    prof_end(kPhElem, st);
+    return TT_OK;
+  }
+  // the merges: the forward's (TT_REUSE_MERGE, tokens to reuse), else now
+  const bool reuse = (plan->L[0].flags & TT_REUSE_MERGE) != 0 && T > 0;
+  const LayerPlan* Ls[TT_MULTI_MAX];
+  const WsLayout* wl[TT_MULTI_MAX];
+  const float* P[TT_MULTI_MAX][kMaxK];
+  const float** Pp[TT_MULTI_MAX];
+  void* zs[TT_MULTI_MAX];
+  size_t offs[TT_MULTI_MAX];
+  float* zero[TT_MULTI_MAX];
+  size_t zero_n[TT_MULTI_MAX];
+  for (int g = 0; g < G; ++g) {
+    Ls[g] = &plan->L[g];
+    wl[g] = &m.w[g];
+    Pp[g] = P[g];
+    zs[g] = static_cast<char*>(ws) + m.w[g].zs;
+    offs[g] = m.w[g].tc;
+    zero[g] = bwd_zero_ptr(ws, m.w[g]);
+    zero_n[g] = bwd_zero_floats(plan->L[g], m.w[g]);
+  }
+  if (reuse) {
+    for (int g = 0; g < G; ++g) chain_ptrs(plan->L[g], params[g], ws, m.w[g], P[g]);
+  } else {
+    prof_begin(kPhMerge, st);
+    s = run_merge_forward_n(G, Ls, params, wl, Pp, ws, true, st);
+    prof_end(kPhMerge, st);
+    if (s != TT_OK) return s;
+  }
+  // every z'_g: the forward's under TT_REUSE_Z, else computed here
+  if (T > 0 && !((plan->L[0].flags & TT_REUSE_Z) && reuse)) {
+    prof_begin(kPhFwd, st);
+    s = multi_tc_forward(plan->L, G, T, x, nullptr, ws, offs, zs, st);
+    prof_end(kPhFwd, st);
+    if (s != TT_OK) return s;
+  }
+  prof_begin(kPhBwd, st);
+  s = multi_tc_backward(plan->L, G, T, x, dy, dx, ws, offs, zs, zero, zero_n, st);
+  prof_end(kPhBwd, st);
+  if (s != TT_OK) return s;
+  prof_begin(kPhMergeBwd, st);
+  for (int g = 0; g < G && s == TT_OK; ++g)
+    s = run_merge_backward(plan->L[g], params[g], P[g], fptr(ws, m.w[g].dA), fptr(ws, m.w[g].dB),
+                           dparams[g], acc, true, reuse, ws, m.w[g], st);
+  prof_end(kPhMergeBwd, st);
+  return s;
 }
 
 tt_status tt_get_device_status(void* stream) {

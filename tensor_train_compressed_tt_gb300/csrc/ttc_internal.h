@@ -49,8 +49,9 @@ size_t ttm_workspace_bytes(const TtmPlan& P, int64_t B);
 }  // namespace ttc
 
 struct tt_plan_s {
-  int kind = 0;  // 0 = single layer, 1 = FFN pair, 2 = TT-matrix embedding
-  ttc::LayerPlan L[2];
+  int kind = 0;  // 0 = single layer, 1 = FFN pair, 2 = TT-matrix embedding, 3 = layers on one x
+  int G = 1;     // layers of a kind-3 plan
+  ttc::LayerPlan L[3];
   ttc::TtmPlan ttm;
 };
 
@@ -141,6 +142,10 @@ cudaError_t scale_periodic(int64_t n, const float* in, const float* scale, int l
 cudaError_t gelu_fwd(int64_t n, const float* h, void* a, int ta, cudaStream_t st);
 // dh = da * GELU'(h), in place over da (f32)
 cudaError_t gelu_bwd(int64_t n, const float* h, float* da, cudaStream_t st);
+// out[i] = out[i] + parts[0][i] + ... + parts[nparts-1][i], summed in f32 in
+// that order and rounded once to out's type (TT_DT_F32 or TT_DT_BF16)
+cudaError_t sum_into(int64_t n, void* out, const void* const* parts, int nparts, int type,
+                     cudaStream_t st);
 // bf16 variants (n a multiple of 8, 16-byte aligned buffers)
 cudaError_t gelu_fwd_bf16(int64_t n, const void* h, void* a, cudaStream_t st);
 cudaError_t gelu_bwd_bf16(int64_t n, const void* h, void* da, cudaStream_t st);

@@ -149,6 +149,64 @@ class TTFFN:
         return dx, dp_up, dp_down
 
 
+class TTMulti:
+    """Up to three TT layers on one input x (the Q, K and V projections):
+    y_g = x W_g^T for each layer; the backward returns dx = sum_g dy_g W_g
+    and each layer's packed gradients."""
+
+    def __init__(self, layers: Sequence[Sequence[Sequence[int]]],
+                 dtype: torch.dtype = torch.bfloat16, accumulate: bool = False,
+                 reuse_merge: bool = False, reuse_z: bool = False, deterministic: bool = False):
+        flags = (ttc.TT_ACCUMULATE if accumulate else 0) | \
+            (ttc.TT_REUSE_MERGE if reuse_merge else 0) | (ttc.TT_REUSE_Z if reuse_z else 0) | \
+            (ttc.TT_DETERMINISTIC if deterministic else 0)
+        self.dtype = dtype
+        self.out_dtype = torch.bfloat16 if _DT[dtype] == ttc.TT_DT_E4M3 else dtype
+        self.descs = [ttc.make_desc(i, o, r, _DT[dtype], flags) for i, o, r in layers]
+        self.plan = ttc.tt_multi_plan(self.descs)
+        self.G = len(self.descs)
+        self.layout = [ttc.tt_multi_param_layout(self.plan, g) for g in range(self.G)]
+        self.N = 1
+        for n in layers[0][0]:
+            self.N *= n
+        self.M = []
+        for _, o, _ in layers:
+            m = 1
+            for v in o:
+                m *= v
+            self.M.append(m)
+
+    def workspace(self, T: int, device="cuda") -> torch.Tensor:
+        return torch.empty(ttc.tt_workspace_size(self.plan, T), dtype=torch.uint8,
+                           device=device)
+
+    def forward(self, x, params, y=None, ws=None, stream=None):
+        T = x.shape[0]
+        if y is None:
+            y = [torch.empty((T, m), dtype=self.out_dtype, device=x.device) for m in self.M]
+        if ws is None:
+            ws = self.workspace(T, x.device)
+        ttc.check(ttc.tt_multi_forward(self.plan, T, _ptr(x), [_ptr(p) for p in params],
+                                       [_ptr(t) for t in y], _ptr(ws), ws.numel(),
+                                       _stream(stream)), "tt_multi_forward")
+        return y
+
+    def backward(self, x, dy, params, dx=None, dparams=None, ws=None, stream=None):
+        T = x.shape[0]
+        if dx is None:
+            dx = torch.empty((T, self.N), dtype=self.out_dtype, device=x.device)
+        if dparams is None:
+            dparams = [torch.empty(lay[2], dtype=torch.float32, device=x.device)
+                       for lay in self.layout]
+        if ws is None:
+            ws = self.workspace(T, x.device)
+        ttc.check(ttc.tt_multi_backward(self.plan, T, _ptr(x), [_ptr(t) for t in dy],
+                                        [_ptr(p) for p in params], _ptr(dx),
+                                        [_ptr(t) for t in dparams], _ptr(ws), ws.numel(),
+                                        _stream(stream)), "tt_multi_backward")
+        return dx, dparams
+
+
 class TTMEmbedding:
     """TT-matrix embedding table: lookup of rows for int32 indices and its
     backward into the packed cores/diagonals (float32)."""

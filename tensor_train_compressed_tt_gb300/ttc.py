@@ -25,6 +25,7 @@ TT_ACCUMULATE = 1
 TT_REUSE_MERGE = 2
 TT_REUSE_Z = 4   # forward keeps z' for the backward (implies TT_REUSE_MERGE)
 TT_DETERMINISTIC = 8   # bit-reproducible gradients (fixed summation order)
+TT_MULTI_MAX = 3       # layers of a multi-layer plan (one shared input)
 
 STATUS = {
     0: "TT_OK",
@@ -100,6 +101,10 @@ def lib() -> ctypes.CDLL:
             "tt_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_forward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ffn_backward": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+            "tt_multi_plan": [_P, ctypes.c_int, _P],
+            "tt_multi_param_layout": [_P, ctypes.c_int, _P, _P, _P],
+            "tt_multi_forward": [_P, _I64, _P, _P, _P, _P, _SZ, _P],
+            "tt_multi_backward": [_P, _I64, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_rank_update": [_P, _P, _P, _P, _P],
             "tt_backward_rank_update": [_P, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
             "tt_ttm_plan": [_P, _P],
@@ -185,6 +190,13 @@ def tt_ffn_plan(up: tt_desc, down: tt_desc) -> Plan:
     return Plan(h.value, "ffn", (up.d, down.d))
 
 
+def tt_multi_plan(descs: Sequence[tt_desc]) -> Plan:
+    arr = (tt_desc * len(descs))(*descs)
+    h = ctypes.c_void_p()
+    _check(lib().tt_multi_plan(arr, len(descs), ctypes.byref(h)), "tt_multi_plan")
+    return Plan(h.value, "multi", tuple(d.d for d in descs))
+
+
 def _layout(fn, args, d):
     core = (ctypes.c_size_t * (2 * d))()
     diag = (ctypes.c_size_t * max(1, 2 * d - 1))()
@@ -204,6 +216,11 @@ def tt_param_layout(plan: Plan):
 def tt_ffn_param_layout(plan: Plan, layer: int):
     return _layout(lib().tt_ffn_param_layout, [ctypes.c_void_p(plan.handle), int(layer)],
                    plan.d[layer])
+
+
+def tt_multi_param_layout(plan: Plan, layer: int):
+    d = plan.d[layer] if 0 <= layer < len(plan.d) else plan.d[0]   # the library checks layer
+    return _layout(lib().tt_multi_param_layout, [ctypes.c_void_p(plan.handle), int(layer)], d)
 
 
 def tt_workspace_size(plan: Plan, T: int) -> int:
@@ -243,6 +260,26 @@ def tt_ffn_backward(plan: Plan, T: int, x: int, dy: int, params_up: int, params_
     return lib().tt_ffn_backward(ctypes.c_void_p(plan.handle), int(T), x, dy, params_up,
                                  params_down, dx, dparams_up, dparams_down, ws,
                                  int(ws_bytes), stream)
+
+
+def _ptrs(ps: Sequence[int]):
+    return (ctypes.c_void_p * len(ps))(*[ctypes.c_void_p(int(p)) for p in ps])
+
+
+def tt_multi_forward(plan: Plan, T: int, x: int, params: Sequence[int], y: Sequence[int],
+                     ws: int, ws_bytes: int, stream: int = 0) -> int:
+    """params, y: one device pointer a layer (host arrays built here)."""
+    return lib().tt_multi_forward(ctypes.c_void_p(plan.handle), int(T), x, _ptrs(params),
+                                  _ptrs(y), ws, int(ws_bytes), stream)
+
+
+def tt_multi_backward(plan: Plan, T: int, x: int, dy: Sequence[int], params: Sequence[int],
+                      dx: int, dparams: Sequence[int], ws: int, ws_bytes: int,
+                      stream: int = 0) -> int:
+    """dx receives the sum over the layers of dy_g W_g."""
+    return lib().tt_multi_backward(ctypes.c_void_p(plan.handle), int(T), x, _ptrs(dy),
+                                   _ptrs(params), dx, _ptrs(dparams), ws, int(ws_bytes),
+                                   stream)
 
 
 def tt_rank_update(plan: Plan, params: int, dparams: int, gamma: float, beta: float,

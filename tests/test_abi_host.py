@@ -110,6 +110,67 @@ def test_reuse_z_flag(lib):
         ttc.tt_ffn_plan(_desc(up, flags=ttc.TT_REUSE_Z), _desc(dn))
 
 
+def test_multi_plan_layout_and_validation(lib):
+    """A multi-layer plan takes 1..3 layers with the same input modes, act
+    type and flags; each layer keeps its own packed layout.  The fused bf16
+    plan holds one region a layer with its z' (T x 64 bf16); the
+    layer-by-layer plans (f32, TT_DETERMINISTIC) hold the other layers' dx
+    instead."""
+    L = synth.ENCODER_LAYERS
+    q, up = L["q"], L["up"]
+    plan = ttc.tt_multi_plan([_desc(q), _desc(q), _desc(up)])
+    for g, shape in enumerate((q, q, up)):
+        core_off, diag_off, n = ttc.tt_multi_param_layout(plan, g)
+        assert n == sum(int(np.prod(c)) for c in shape.core_shapes()) + sum(shape.diag_sizes())
+        assert core_off[0] == 0 and diag_off[0] == n - sum(shape.diag_sizes())
+    with pytest.raises(ttc.TTError):
+        ttc.tt_multi_param_layout(plan, 3)
+    with pytest.raises(ttc.TTError):
+        ttc.tt_multi_plan([])
+    with pytest.raises(ttc.TTError):
+        ttc.tt_multi_plan([_desc(q)] * 4)
+    with pytest.raises(ttc.TTError):   # input modes differ
+        ttc.tt_multi_plan([_desc(q), _desc(L["down"])])
+    with pytest.raises(ttc.TTError):   # act types differ
+        ttc.tt_multi_plan([_desc(q), _desc(q, act=ttc.TT_DT_F32)])
+    with pytest.raises(ttc.TTError):   # flags differ
+        ttc.tt_multi_plan([_desc(q), _desc(q, flags=ttc.TT_REUSE_Z)])
+    one = ttc.tt_plan(_desc(q))
+    fused = ttc.tt_multi_plan([_desc(q)] * 3)
+    for T in (1, 1000, 16384):
+        w1 = ttc.tt_workspace_size(one, T)
+        w3 = ttc.tt_workspace_size(fused, T)
+        assert 3 * (w1 + T * 128) <= w3 + 3 * 512 and w3 <= 3 * (w1 + T * 128) + 3 * 512
+    for act, flags in ((ttc.TT_DT_F32, 0), (ttc.TT_DT_BF16, ttc.TT_DETERMINISTIC)):
+        single = ttc.tt_plan(_desc(q, act=act, flags=flags))
+        multi = ttc.tt_multi_plan([_desc(q, act=act, flags=flags)] * 3)
+        esz = 4 if act == ttc.TT_DT_F32 else 2
+        for T in (7, 1000):
+            extra = ttc.tt_workspace_size(multi, T) - 3 * ttc.tt_workspace_size(single, T)
+            assert 2 * T * q.N * esz - 3 * 512 <= extra <= 2 * T * q.N * esz + 3 * 512
+
+
+def test_multi_argument_errors_return_before_any_launch(lib):
+    q = synth.ENCODER_LAYERS["q"]
+    plan = ttc.tt_multi_plan([_desc(q)] * 3)
+    need = ttc.tt_workspace_size(plan, 64)
+    fake = 1 << 40
+    p3 = [fake] * 3
+    assert ttc.tt_multi_forward(plan, 0, 0, p3, [0] * 3, 0, 0) == 0      # T == 0: no-op
+    assert ttc.tt_multi_forward(plan, -1, fake, p3, p3, fake, need) == 1
+    assert ttc.tt_multi_forward(plan, 64, fake, [fake, 0, fake], p3, fake, need) == 1
+    assert ttc.tt_multi_forward(plan, 64, fake, p3, [fake, fake + 2, fake], fake, need) == 1
+    assert ttc.tt_multi_forward(plan, 64, fake, p3, p3, fake, need - 1) == 3
+    assert ttc.tt_multi_backward(plan, 64, fake, p3, p3, fake, [fake, fake, 0], fake, need) == 1
+    assert ttc.tt_multi_backward(plan, 64, fake, [fake, fake + 8, fake], p3, fake, p3, fake,
+                                 need) == 1
+    assert ttc.tt_multi_backward(plan, 64, fake, p3, p3, fake + 4, p3, fake, need) == 1
+    assert ttc.tt_multi_backward(plan, 64, fake, p3, p3, fake, p3, fake + 16, need) == 3
+    single = ttc.tt_plan(_desc(q))   # a single-layer plan is not a multi plan
+    assert ttc.tt_multi_forward(single, 64, fake, p3, p3, fake, need) == 1
+    assert ttc.tt_forward(plan, 64, fake, fake, fake, fake, need) == 1
+
+
 def test_deterministic_flag_workspace(lib):
     """TT_DETERMINISTIC adds one token-sum slot per CTA of the backward
     (128-token tiles, at most 160) to the tensor-core plans' workspace."""

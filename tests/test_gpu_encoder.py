@@ -28,10 +28,10 @@ def _f64(li):
     return ([c.astype(np.float64) for c in li.cores], [e.astype(np.float64) for e in li.diags])
 
 
-def _block(T, seed):
+def _block(T, seed, fuse_qkv=True):
     from tensor_train_compressed_tt_gb300.encoder import PROJ, TTEncoderBlock
     inp = synth.draw_encoder(T, seed)
-    blk = TTEncoderBlock()
+    blk = TTEncoderBlock(fuse_qkv=fuse_qkv)
     dev = lambda a: torch.from_numpy(a).cuda().bfloat16()  # noqa: E731
     x, xo, xf = dev(inp.x), dev(inp.xo), dev(inp.xf)
     dy = {k: dev(v) for k, v in inp.dy.items()}
@@ -42,14 +42,21 @@ def _block(T, seed):
 
 
 def _check(inp, b, PROJ):
+    """Every layer's y and gradients; dx per input (dx_qkv: the summed dx of
+    Q, K and V, when they run fused)."""
     L = synth.ENCODER_LAYERS
     xin = {"q": inp.x, "k": inp.x, "v": inp.x, "o": inp.xo}
+    dx_sum = 0.0
     for nm in PROJ:
         ref = oracle_layer(L[nm], inp.layers[nm], xin[nm], inp.dy[nm])
+        if nm != "o":
+            dx_sum = dx_sum + ref["dx"]
         gc, gd = synth.unpack(L[nm], b[f"dp_{nm}"].cpu().numpy())
-        out = {"y": b[f"y_{nm}"].float().cpu().numpy(), "dx": b[f"dx_{nm}"].float().cpu().numpy(),
-               "dcores": gc, "ddiags": gd}
+        dx = b[f"dx_{nm}"].float().cpu().numpy() if f"dx_{nm}" in b else ref["dx"]
+        out = {"y": b[f"y_{nm}"].float().cpu().numpy(), "dx": dx, "dcores": gc, "ddiags": gd}
         compare(out, ref, TOL["bf16"], f"layer {nm}")
+    if "dx_qkv" in b:
+        assert O.rel_err(b["dx_qkv"].float().cpu().numpy(), dx_sum) <= TOL["bf16"]
     up, dn = _f64(inp.layers["up"]), _f64(inp.layers["down"])
     y = O.ffn_forward(up, dn, 3, 3, inp.xf)
     dx, gu, gdn = O.ffn_backward(up, dn, 3, 3, inp.xf, inp.dy["ffn"])
@@ -61,9 +68,9 @@ def _check(inp, b, PROJ):
             assert O.rel_err(a, r) <= TOL["bf16"], key
 
 
-@pytest.mark.parametrize("T", [300, 4096])
-def test_encoder_block_step_against_oracle(T):
-    inp, blk, args, b, PROJ = _block(T, seed=40)
+@pytest.mark.parametrize("T,fuse_qkv", [(300, True), (4096, True), (1000, False)])
+def test_encoder_block_step_against_oracle(T, fuse_qkv):
+    inp, blk, args, b, PROJ = _block(T, seed=40, fuse_qkv=fuse_qkv)
     blk.step(*args, b)
     torch.cuda.synchronize()
     _check(inp, b, PROJ)
