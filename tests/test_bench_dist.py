@@ -1,7 +1,10 @@
-"""The benchmark's multi-rank bookkeeping on CPU (gloo, world size 2).
+"""Multi-rank paths on CPU (gloo, world size 2).
 
-Each rank runs its own replica; the step time is the slowest rank's and the
-value counts the tokens of every rank.
+The benchmark's bookkeeping: each rank runs its own replica; the step time is
+the slowest rank's and the value counts the tokens of every rank.  And the
+one exchange a data-parallel training step needs: the token sums behind
+dparams are linear in the tokens, so one all-reduce (sum) of the replicas'
+packed dparams gives the gradient of the whole batch.
 """
 
 import os
@@ -49,6 +52,66 @@ def test_two_gloo_ranks_reduce_like_the_benchmark():
     for rank, ms, k, tot, rate in res:
         assert ms == 2.5 and k == 93 and tot == 3
         assert rate == pytest.approx(2 * 16384 / 2.5e-3)
+
+
+def _grad_worker(rank, world, port, q):
+    """Rank r takes rows r::world of one seeded batch, runs the oracle's
+    backward on them, all-reduces its packed dparams (and reassembles dx by
+    all-gather) over gloo."""
+    import numpy as np
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from oracle import tt_oracle as O
+    from tensor_train_compressed_tt_gb300 import synth
+    w = synth.WORKLOADS["tiny64_f32"]
+    inp = synth.draw(w, seed=7, tokens=24)
+    sh = w.layers[0]
+    li = inp.layers[0]
+    cores = [c.astype(np.float64) for c in li.cores]
+    diags = [e.astype(np.float64) for e in li.diags]
+    xs, dys = inp.x[rank::world], inp.dy[rank::world]
+    dx, dC, dE = O.chained_backward(cores, diags, sh.d, xs, dys)
+    flat = torch.from_numpy(synth.pack([c.astype(np.float32) for c in dC],
+                                       [e.astype(np.float32) for e in dE]).astype(np.float64))
+    dist.all_reduce(flat, op=dist.ReduceOp.SUM)
+    parts = [torch.zeros(dx.shape, dtype=torch.float64) for _ in range(world)]
+    dist.all_gather(parts, torch.from_numpy(np.ascontiguousarray(dx)))
+    q.put((rank, flat.numpy(), [p.numpy() for p in parts]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_all_reduced_dparams_equal_the_whole_batch_gradient():
+    import numpy as np
+    from oracle import tt_oracle as O
+    from tensor_train_compressed_tt_gb300 import synth
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_grad_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted((q.get(timeout=120) for _ in range(world)), key=lambda t: t[0])
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    w = synth.WORKLOADS["tiny64_f32"]
+    inp = synth.draw(w, seed=7, tokens=24)
+    sh, li = w.layers[0], inp.layers[0]
+    cores = [c.astype(np.float64) for c in li.cores]
+    diags = [e.astype(np.float64) for e in li.diags]
+    dx, dC, dE = O.chained_backward(cores, diags, sh.d, inp.x, inp.dy)
+    whole = synth.pack([c.astype(np.float32) for c in dC], [e.astype(np.float32) for e in dE])
+    for rank, flat, parts in res:
+        # the float32 packing of each half rounds once more than the whole's
+        assert O.rel_err(flat, whole) <= 1e-6
+        dx_all = np.empty_like(dx)
+        for r, part in enumerate(parts):
+            dx_all[r::world] = part
+        assert O.rel_err(dx_all, dx) <= 1e-12
+    assert np.array_equal(res[0][1], res[1][1])
 
 
 def test_single_process_is_identity():
