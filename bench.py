@@ -49,6 +49,8 @@ def parse():
                    help="re-merge the cores in the backward instead of reusing the forward's")
     p.add_argument("--no-reuse-z", action="store_true",
                    help="recompute z' = x A diag(D) in the backward instead of keeping the forward's")
+    p.add_argument("--no-fuse-qkv", action="store_true",
+                   help="encoder block: Q, K and V as three single-layer plans")
     p.add_argument("--deterministic", action="store_true",
                    help="TT_DETERMINISTIC: fixed-order (bit-reproducible) gradient sums")
     p.add_argument("--oracle-rate", action="store_true", help=argparse.SUPPRESS)
@@ -1185,7 +1187,7 @@ def run_encoder(args):
         _build.build()
     T = args.tokens or 16384
     inp = synth.draw_encoder(T, seed=rank)
-    blk = TTEncoderBlock(deterministic=args.deterministic)
+    blk = TTEncoderBlock(deterministic=args.deterministic, fuse_qkv=not args.no_fuse_qkv)
     params = {nm: torch.from_numpy(synth.pack(li.cores, li.diags)).to(dev)
               for nm, li in inp.layers.items()}
     b = blk.buffers(T, dev)
@@ -1301,6 +1303,7 @@ def run_encoder(args):
                                       "768->3072->768, fwd+bwd of all, 16384 tokens, bf16",
                        "tokens": T, "parallelism": f"replicas x{world}", "launch": note,
                        "deterministic": bool(args.deterministic),
+                       "qkv": "separate plans" if args.no_fuse_qkv else "one multi-layer plan",
                        "l2": f"{nsets} rotating input sets of {set_bytes / 1e6:.0f} MB"},
             "roofline": {"bound": "hbm", "kernel": "whole block step (summed)",
                          "achieved": byts / (ms * 1e-3) / 1e9, "peak": peak,

@@ -436,9 +436,8 @@ struct FfnBwdArgs {
   const int* rinfo2;
   float* dDc1;        // token sums of z1 * dz1' and z2 * dz2'
   float* dDc2;
-  float* zero1;       // [0, zero1_n) and [0, zero2_n) set to 0 on the way (scratch the
-  float* zero2;       // merge backward of each layer adds into)
-  int zero1_n, zero2_n;
+  ZeroList zero;      // ranges set to 0 on the way (what each layer's merge backward
+                      // adds into)
 };
 
 struct FfnBwdSmem {
@@ -532,10 +531,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     S.Dc1[threadIdx.x] = p.Dc1[threadIdx.x];
     S.Dc2[threadIdx.x] = p.Dc2[threadIdx.x];
   }
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero1_n; i += gridDim.x * blockDim.x)
-    p.zero1[i] = 0.f;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero2_n; i += gridDim.x * blockDim.x)
-    p.zero2[i] = 0.f;
+  zero_list(p.zero);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -969,14 +965,10 @@ tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, cons
 
 tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x,
                           const void* dy, void* dx, void* ws, size_t off1, size_t off2,
-                          const void* zs1, const void* zs2, float* zero1, size_t n1,
-                          float* zero2, size_t n2, cudaStream_t st) {
-  if (n1 > 0x7FFFFFFF || n2 > 0x7FFFFFFF || !ffn_tc_supported(U, D)) return TT_ERR_UNSUPPORTED;
-  if (T <= 0) {
-    if (n1 && cudaMemsetAsync(zero1, 0, n1 * sizeof(float), st) != cudaSuccess) return TT_ERR_CUDA;
-    if (n2 && cudaMemsetAsync(zero2, 0, n2 * sizeof(float), st) != cudaSuccess) return TT_ERR_CUDA;
-    return TT_OK;
-  }
+                          const void* zs1, const void* zs2, const ZeroList& zero,
+                          cudaStream_t st) {
+  if (!ffn_tc_supported(U, D)) return TT_ERR_UNSUPPORTED;
+  if (T <= 0) return zero_list_memset(zero, st) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   if (set_ffn_attrs() != cudaSuccess) return TT_ERR_CUDA;
   const TcLayout t1 = tc_layout(U), t2 = tc_layout(D);
@@ -1010,10 +1002,7 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
   a.rinfo2 = at<int>(ws, off2 + t2.rinfo);
   a.dDc1 = at<float>(ws, off1 + t1.dDc);
   a.dDc2 = at<float>(ws, off2 + t2.dDc);
-  a.zero1 = zero1;
-  a.zero1_n = (int)n1;
-  a.zero2 = zero2;
-  a.zero2_n = (int)n2;
+  a.zero = zero;
   const int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e = launch_ex(ffn_bwd_kernel, grid, NTHREADS, kSmemFfnBwd, st, false, mx, mdy,
                             manr1, mbm1, manr2, mbm2, mdx, mdac1, mdbc1, mdac2, mdbc2, mzs1, mzs2,

@@ -315,8 +315,7 @@ struct QkvBwdArgs {
   const float* Dc[kMaxGroups];
   const int* rinfo[kMaxGroups];
   float* dDc[kMaxGroups];
-  float* zero[kMaxGroups];   // each layer's merge scratch, set to 0 on the way
-  int zero_n[kMaxGroups];
+  ZeroList zero;             // ranges set to 0 on the way (what the merges add into)
 };
 
 // TMEM columns of the backward
@@ -391,10 +390,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   pdl_wait();
   pdl_trigger();
   for (int i = threadIdx.x; i < p.G * RP; i += blockDim.x) S.Dc[i / RP][i % RP] = p.Dc[i / RP][i % RP];
-  for (int g = 0; g < p.G; ++g)
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_n[g];
-         i += gridDim.x * blockDim.x)
-      p.zero[g][i] = 0.f;
+  zero_list(p.zero);
   zero_tail_boxes(act, 2 * QKV_NACT, ztiles, kMaxGroups, p.tt);
   tc_fence_before();
   __syncthreads();
@@ -744,17 +740,9 @@ tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x,
 
 tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x,
                             const void* const* dy, void* dx, void* ws, const size_t* offs,
-                            const void* const* zs, float* const* zero, const size_t* zero_n,
-                            cudaStream_t st) {
+                            const void* const* zs, const ZeroList& zero, cudaStream_t st) {
   if (!multi_tc_supported(Ls, G)) return TT_ERR_UNSUPPORTED;
-  for (int g = 0; g < G; ++g)
-    if (zero_n[g] > 0x7FFFFFFF) return TT_ERR_UNSUPPORTED;
-  if (T <= 0) {
-    for (int g = 0; g < G; ++g)
-      if (zero_n[g] && cudaMemsetAsync(zero[g], 0, zero_n[g] * sizeof(float), st) != cudaSuccess)
-        return TT_ERR_CUDA;
-    return TT_OK;
-  }
+  if (T <= 0) return zero_list_memset(zero, st) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   if (set_qkv_attrs() != cudaSuccess) return TT_ERR_CUDA;
   CUtensorMap mx, mdx, mdx16, mdy[kMaxGroups], manr[kMaxGroups], mbm[kMaxGroups], mdac[kMaxGroups],
@@ -786,9 +774,8 @@ tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x
     a.Dc[g] = at<float>(ws, offs[gg] + t.Dc);
     a.rinfo[g] = at<int>(ws, offs[gg] + t.rinfo);
     a.dDc[g] = at<float>(ws, offs[gg] + t.dDc);
-    a.zero[g] = g < G ? zero[g] : nullptr;
-    a.zero_n[g] = g < G ? (int)zero_n[g] : 0;
   }
+  a.zero = zero;
   const int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
   cudaError_t e = launch_ex(qkv_bwd_kernel, grid, NTHREADS, kSmemQkvBwd, st, false, mx, mdy[0],
                             mdy[1], mdy[2], manr[0], manr[1], manr[2], mbm[0], mbm[1], mbm[2],

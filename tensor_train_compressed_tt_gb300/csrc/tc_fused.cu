@@ -422,8 +422,7 @@ struct BwdArgs {
   float* dAc;  // N x RP
   float* dBc;  // M x RP
   float* dDc;  // RP
-  float* zero;  // [0, zero_n) set to 0 (scratch the merge backward adds into)
-  int zero_n;
+  ZeroList zero;  // ranges set to 0 on the way (what the merge backward adds into)
   int use_z;    // read the forward's z' through tm_zs instead of computing x A
   // Fixed summation order: the token sums go to this CTA's own slot (rows
   // blockIdx.x * N of tm_dac, blockIdx.x * M of tm_dbc; dDslot[blockIdx.x][4
@@ -455,6 +454,13 @@ __device__ __forceinline__ int rot_chunk(int c, int n, int tile) {
 }
 
 // Zero rows [tt, TILE) of the stages' two activation boxes and of the z' tile.
+// Every range of the list set to 0, grid-stride over the whole grid.
+__device__ void zero_list(const ZeroList& z) {
+  const int stride = gridDim.x * blockDim.x;
+  for (int r = 0; r < z.count; ++r)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < z.n[r]; i += stride) z.p[r][i] = 0.f;
+}
+
 __device__ void zero_tail_rows(uint8_t* stages, int nstage, uint8_t* zp_tile, int tt) {
   if (tt >= TILE) return;
   const int per_box = (TILE - tt) * 8;  // 16-byte units
@@ -778,8 +784,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   pdl_wait();  // nothing a previous grid writes is touched before this point
   pdl_trigger();
   if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.zero_n; i += gridDim.x * blockDim.x)
-    p.zero[i] = 0.f;
+  zero_list(p.zero);
   zero_tail_rows(stages, NSTAGE_B, zp_tile, p.tt);
   tc_fence_before();
   __syncthreads();
@@ -1476,16 +1481,19 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 
-tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
-                      void* ws, size_t off, float* zero, size_t zero_n, bool f8, const void* zs,
-                      const DetSlots* det, cudaStream_t st) {
-  if (zero_n > 0x7FFFFFFF) return TT_ERR_UNSUPPORTED;
-  if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
-  if (T <= 0) {
-    if (zero_n && cudaMemsetAsync(zero, 0, zero_n * sizeof(float), st) != cudaSuccess)
-      return TT_ERR_CUDA;
-    return TT_OK;
+cudaError_t zero_list_memset(const ZeroList& z, cudaStream_t st) {
+  for (int r = 0; r < z.count; ++r) {
+    cudaError_t e = cudaMemsetAsync(z.p[r], 0, (size_t)z.n[r] * sizeof(float), st);
+    if (e != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
+                      void* ws, size_t off, const ZeroList& zero, bool f8, const void* zs,
+                      const DetSlots* det, cudaStream_t st) {
+  if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
+  if (T <= 0) return zero_list_memset(zero, st) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   const TcLayout t = tc_layout(L);
   if (set_smem_attrs() != cudaSuccess) return TT_ERR_CUDA;
@@ -1522,7 +1530,6 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   a.dBc = at<float>(ws, off + t.dBc);
   a.dDc = at<float>(ws, off + t.dDc);
   a.zero = zero;
-  a.zero_n = (int)zero_n;
   a.use_z = zs != nullptr;
   a.det = det ? 1 : 0;
   a.dDslot = det ? det->d : nullptr;

@@ -34,11 +34,30 @@ size_t tc_operand_bytes(const LayerPlan& L);
 tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws,
                      size_t ws_off, bool f8, void* zs, cudaStream_t st);
 
+// Ranges of floats a backward token kernel sets to zero on its way: scratch
+// that the merge backward then adds into, and the gradients that its
+// one-phase program adds into.  Also zeroed when there are no tokens.
+constexpr int kMaxZero = 6;
+struct ZeroList {
+  float* p[kMaxZero] = {};
+  int n[kMaxZero] = {};
+  int count = 0;
+  // false when the list is full or the range is 2^31 floats or more
+  bool add(float* ptr, size_t len) {
+    if (!len) return true;
+    if (count >= kMaxZero || len > 0x7FFFFFFF) return false;
+    p[count] = ptr;
+    n[count++] = (int)len;
+    return true;
+  }
+};
+// cudaMemsetAsync of every range (the no-token case)
+cudaError_t zero_list_memset(const ZeroList& z, cudaStream_t st);
+
 // dx for T tokens and the token sums dAc, dBc, dDc (zeroed by the pack
 // phase, or, with det, written in a fixed order from per-CTA slots by one
 // more kernel); the merge engine's unpack phase turns these into dA, dB, dD_d.
-// zero[0, zero_n) is set to 0 on the way (scratch that the merge backward
-// then adds into), also when T == 0.  x and dy are bf16, or E4M3 codes when
+// The ranges of `zero` are set to 0 on the way, also when T == 0.  x and dy are bf16, or E4M3 codes when
 // f8; dx is bf16.  With zs, z' is read from the forward's copy there instead
 // of being recomputed from x.
 // TT_DETERMINISTIC: per-CTA slots of the token sums (count CTAs at most):
@@ -52,7 +71,7 @@ struct DetSlots {
 constexpr int kDetMaxSlots = 160;
 
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
-                      void* ws, size_t ws_off, float* zero, size_t zero_n, bool f8,
+                      void* ws, size_t ws_off, const ZeroList& zero, bool f8,
                       const void* zs, const DetSlots* det, cudaStream_t st);
 
 // ---- single-launch f32 path for small layers (small_f32.cu) -----------------
@@ -85,12 +104,12 @@ tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, cons
 
 // dx and both layers' token sums (dAc, dBc, dDc, zeroed beforehand) for T
 // tokens from x, dy and the forward's z1', z2' (zs1, zs2); h, GELU(h), da and
-// dh are recomputed per hidden chunk on the SM.  zero1[0, n1) and zero2[0, n2)
+// dh are recomputed per hidden chunk on the SM.  The ranges of `zero`
 // are set to 0 on the way (the merge backward's scratch), also when T == 0.
 tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x,
                           const void* dy, void* dx, void* ws, size_t off1, size_t off2,
-                          const void* zs1, const void* zs2, float* zero1, size_t n1,
-                          float* zero2, size_t n2, cudaStream_t st);
+                          const void* zs1, const void* zs2, const ZeroList& zero,
+                          cudaStream_t st);
 
 // ---- several layers on one input (qkv_fused.cuh) ----------------------------
 // True when G (1..3) layers of equal input width all fit the tensor-core kernels.
@@ -104,10 +123,9 @@ tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x,
 
 // dx = sum_g dy[g] W_g and every layer's token sums (dAc, dBc, dDc, zeroed
 // beforehand) from x, dy[g] and the forward's z'_g; x streamed once.
-// zero[g][0, zero_n[g]) is set to 0 on the way, also when T == 0.
+// The ranges of `zero` are set to 0 on the way, also when T == 0.
 tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x,
                             const void* const* dy, void* dx, void* ws, const size_t* offs,
-                            const void* const* zs, float* const* zero, const size_t* zero_n,
-                            cudaStream_t st);
+                            const void* const* zs, const ZeroList& zero, cudaStream_t st);
 
 }  // namespace ttc

@@ -412,6 +412,12 @@ size_t bwd_zero_floats(const LayerPlan& L, const WsLayout& w) {
   return (w.q - w.bar) / sizeof(float) + dq0_zero_floats(L, w);
 }
 
+// What the backward token pass zeroes on its way: the merge program's
+// grid-barrier line and the step-0 dQ scratch right after it.
+bool bwd_zero_add(ZeroList* z, const LayerPlan& L, void* ws, const WsLayout& w) {
+  return z->add(bwd_zero_ptr(ws, w), bwd_zero_floats(L, w));
+}
+
 // The merge-backward program of one layer, built phase by phase so that the
 // programs of several layers (the two of an FFN pair) can share one launch.
 struct MergeBwd {
@@ -789,7 +795,8 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
     if (s != TT_OK) return s;
   }
   prof_begin(kPhBwd, st);
-  const size_t nz = bwd_zero_floats(L, w);
+  ZeroList zl;
+  if (!bwd_zero_add(&zl, L, ws, w)) return TT_ERR_UNSUPPORTED;
   if (tc) {
     const void* zs = (L.flags & TT_REUSE_Z) && reuse ? static_cast<char*>(ws) + w.zs : nullptr;
     DetSlots det;
@@ -799,10 +806,10 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
       det.b = det.a + (size_t)w.det_slots * L.N * 64;
       det.d = det.b + (size_t)w.det_slots * L.M * 64;
     }
-    s = tc_backward(L, T, x, dy, dx, ws, w.tc, bwd_zero_ptr(ws, w), nz, tx == TT_DT_E4M3, zs,
+    s = tc_backward(L, T, x, dy, dx, ws, w.tc, zl, tx == TT_DT_E4M3, zs,
                     w.det_slots ? &det : nullptr, st);
   } else {
-    TT_CUDA(cudaMemsetAsync(bwd_zero_ptr(ws, w), 0, nz * sizeof(float), st));
+    TT_CUDA(zero_list_memset(zl, st));
     s = simt_backward_tokens(L, T, x, tx, dy, tdy, params, P, dx, tdx, dparams, acc, ws, w, st);
   }
   prof_end(kPhBwd, st);
@@ -1118,9 +1125,10 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
       if (s != TT_OK) return s;
     }
     prof_begin(kPhBwd, st);
-    s = ffn_tc_backward(U, D, T, x, dy, dx, ws, f.up.tc, f.down.tc, zs1, zs2,
-                        bwd_zero_ptr(ws, f.up), bwd_zero_floats(U, f.up), bwd_zero_ptr(ws, f.down),
-                        bwd_zero_floats(D, f.down), st);
+    ZeroList zl;
+    if (!bwd_zero_add(&zl, U, ws, f.up) || !bwd_zero_add(&zl, D, ws, f.down))
+      return TT_ERR_UNSUPPORTED;
+    s = ffn_tc_backward(U, D, T, x, dy, dx, ws, f.up.tc, f.down.tc, zs1, zs2, zl, st);
     prof_end(kPhBwd, st);
     if (s != TT_OK) return s;
     prof_begin(kPhMergeBwd, st);
@@ -1291,16 +1299,14 @@ tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
   const float** Pp[TT_MULTI_MAX];
   void* zs[TT_MULTI_MAX];
   size_t offs[TT_MULTI_MAX];
-  float* zero[TT_MULTI_MAX];
-  size_t zero_n[TT_MULTI_MAX];
+  ZeroList zl;
   for (int g = 0; g < G; ++g) {
     Ls[g] = &plan->L[g];
     wl[g] = &m.w[g];
     Pp[g] = P[g];
     zs[g] = static_cast<char*>(ws) + m.w[g].zs;
     offs[g] = m.w[g].tc;
-    zero[g] = bwd_zero_ptr(ws, m.w[g]);
-    zero_n[g] = bwd_zero_floats(plan->L[g], m.w[g]);
+    if (!bwd_zero_add(&zl, plan->L[g], ws, m.w[g])) return TT_ERR_UNSUPPORTED;
   }
   if (reuse) {
     for (int g = 0; g < G; ++g) chain_ptrs(plan->L[g], params[g], ws, m.w[g], P[g]);
@@ -1318,7 +1324,7 @@ tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
     if (s != TT_OK) return s;
   }
   prof_begin(kPhBwd, st);
-  s = multi_tc_backward(plan->L, G, T, x, dy, dx, ws, offs, zs, zero, zero_n, st);
+  s = multi_tc_backward(plan->L, G, T, x, dy, dx, ws, offs, zs, zl, st);
   prof_end(kPhBwd, st);
   if (s != TT_OK) return s;
   prof_begin(kPhMergeBwd, st);

@@ -42,12 +42,12 @@ def short_limit():
 from parity_util import TOL, compare, gpu_layer, oracle_layer  # noqa: E402
 
 
-def _layer_inputs(name, T, seed):
+def _layer_inputs(name, T, seed, **flags):
     from tensor_train_compressed_tt_gb300.layer import TTLinear
     w = synth.WORKLOADS[name]
     inp = synth.draw(w, seed=seed, tokens=T)
     s = w.layers[0]
-    lay = TTLinear(s.in_modes, s.out_modes, s.ranks, torch.bfloat16)
+    lay = TTLinear(s.in_modes, s.out_modes, s.ranks, torch.bfloat16, **flags)
     params = torch.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
     x = torch.from_numpy(inp.x).cuda().bfloat16()
     dy = torch.from_numpy(inp.dy).cuda().bfloat16()
@@ -83,15 +83,27 @@ def test_token_kernel_wait_runs_out(short_limit, site, T):
     _then_ordinary_call_is_correct(ttc)
 
 
-def test_merge_grid_barrier_wait_runs_out(short_limit):
-    """The backward merge of an order-6 layer is a two-phase engine program:
-    its first CTA skips the grid-barrier arrival and the others' waits run out."""
+@pytest.mark.parametrize("program", ["default", "deterministic", "rank_step"])
+def test_merge_grid_barrier_wait_runs_out(short_limit, program):
+    """Engine programs of more than one phase: the backward merge of an
+    order-6 layer (two phases), its deterministic form (one phase a reverse
+    step, then the first cores) and the backward merge with the rank-adaptive
+    step (the step a phase of its own).  The first CTA skips a grid-barrier
+    arrival and the others' waits run out."""
     ttc = short_limit
     st = torch.cuda.current_stream().cuda_stream
-    _, _, lay, params, x, dy = _layer_inputs("tt768_bf16", 512, seed=22)
+    det = program == "deterministic"
+    _, _, lay, params, x, dy = _layer_inputs("tt768_bf16", 512, seed=22, deterministic=det)
     ws = lay.workspace(512)
+    dx = torch.empty_like(x)
+    dp = torch.empty_like(params)
     ttc.check(ttc.tt_debug_skip_arrival(ttc.TT_DEBUG_MERGE_BARRIER), "hook")
-    lay.backward(x, dy, params, ws=ws)
+    if program != "rank_step":
+        lay.backward(x, dy, params, dx=dx, dparams=dp, ws=ws)
+    else:
+        ttc.tt_backward_rank_update(lay.plan, 512, x.data_ptr(), dy.data_ptr(),
+                                    params.data_ptr(), dx.data_ptr(), dp.data_ptr(), 0.01, 0.01,
+                                    0.0, ws.data_ptr(), ws.numel(), st)
     assert ttc.tt_get_device_status(st) == 5
     _then_ordinary_call_is_correct(ttc)
 
