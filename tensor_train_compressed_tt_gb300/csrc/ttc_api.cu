@@ -402,8 +402,12 @@ tt_status run_merge_forward2(const LayerPlan& U, const float* pu, const WsLayout
 // (dq0_zero_floats), the others' by phase 0, which also zeroes the gradient
 // slices that later phases add into (unless accumulating).
 size_t dq0_zero_floats(const LayerPlan& L, const WsLayout& w) {
-  return L.d >= 3 ? 2 * w.qstride : 0;
+  return L.d >= 3 ? 2 * (size_t)(L.d - 2) * w.qstride : 0;  // steps 0 .. d-3, both sides
 }
+
+// The backward merge folds its last reverse step into the first core's
+// gradient (atomics), for order 6 and up without TT_DETERMINISTIC.
+bool merge_fold(const LayerPlan& L) { return L.d >= 3 && !(L.flags & TT_DETERMINISTIC); }
 
 // What the backward token pass zeroes on its way: the merge program's
 // grid-barrier line and the step-0 dQ scratch right after it.
@@ -413,9 +417,13 @@ size_t bwd_zero_floats(const LayerPlan& L, const WsLayout& w) {
 }
 
 // What the backward token pass zeroes on its way: the merge program's
-// grid-barrier line and the step-0 dQ scratch right after it.
-bool bwd_zero_add(ZeroList* z, const LayerPlan& L, void* ws, const WsLayout& w) {
-  return z->add(bwd_zero_ptr(ws, w), bwd_zero_floats(L, w));
+// grid-barrier line and the dQ scratch right after it, and (folded merge,
+// not accumulating) the whole of dparams, whose parts the merge's later
+// phases add into.
+bool bwd_zero_add(ZeroList* z, const LayerPlan& L, void* ws, const WsLayout& w, float* dparams,
+                  bool acc) {
+  if (!z->add(bwd_zero_ptr(ws, w), bwd_zero_floats(L, w))) return false;
+  return acc || !merge_fold(L) || z->add(dparams, L.n_floats);
 }
 
 // The merge-backward program of one layer, built phase by phase so that the
@@ -457,7 +465,7 @@ struct MergeBwd {
     // the folded last step adds into the first core's gradient with atomics;
     // TT_DETERMINISTIC takes the unfolded program (split partials reduced in
     // split order, dD by column sums)
-    fold = steps >= 2 && !(L.flags & TT_DETERMINISTIC);
+    fold = merge_fold(L);
     nphases = pre + (fold ? steps : steps + 1);
     sides[0] = {0, L.d - 1, dA, nullptr, 0, 0, 0, -1, nullptr, -1};
     sides[1] = {L.d, L.K - 1, dB, nullptr, 1, 2, 0, -1, nullptr, -1};
@@ -476,22 +484,8 @@ struct MergeBwd {
     if (unpack && steps > 0 && j == 0)
       eng_dd_task(b.add(), L, tc, params + L.diag_off[L.d - 1], dparams + L.diag_off[L.d - 1],
                   acc);
-    if (fold && j == 0) {
-      // dQ scratch of steps 1 .. steps-2 (step 0's was zeroed by the token pass)
-      if (steps >= 3) eng_zero_task(b, dq_buf(ws, w, 1, 0), 2 * (steps - 2) * w.qstride);
-      if (!acc) {
-        // gradients that later phases add into
-        for (const Side& sd : sides) {
-          for (int jj2 = 1; jj2 < steps; ++jj2) {
-            const int k = sd.k_last - jj2;
-            eng_zero_task(b, dparams + L.core_off[k], (int64_t)L.r[k] * L.s[k] * L.r[k + 1]);
-          }
-          const int kf = sd.k_first;
-          eng_zero_task(b, dparams + L.core_off[kf], (int64_t)L.r[kf] * L.s[kf] * L.r[kf + 1]);
-          eng_zero_task(b, dparams + L.diag_off[kf], L.r[kf + 1]);
-        }
-      }
-    }
+    // (folded: the dQ scratch and, unless accumulating, dparams were zeroed
+    // by the backward token pass, see bwd_zero_add)
     for (Side& sd : sides) {
       // work left over from the previous step
       if (sd.pending >= 0) {  // the previous phase is balanced by now
@@ -796,7 +790,7 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   }
   prof_begin(kPhBwd, st);
   ZeroList zl;
-  if (!bwd_zero_add(&zl, L, ws, w)) return TT_ERR_UNSUPPORTED;
+  if (!bwd_zero_add(&zl, L, ws, w, dparams, acc)) return TT_ERR_UNSUPPORTED;
   if (tc) {
     const void* zs = (L.flags & TT_REUSE_Z) && reuse ? static_cast<char*>(ws) + w.zs : nullptr;
     DetSlots det;
@@ -1126,7 +1120,8 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
     }
     prof_begin(kPhBwd, st);
     ZeroList zl;
-    if (!bwd_zero_add(&zl, U, ws, f.up) || !bwd_zero_add(&zl, D, ws, f.down))
+    if (!bwd_zero_add(&zl, U, ws, f.up, dparams_up, acc) ||
+        !bwd_zero_add(&zl, D, ws, f.down, dparams_down, acc))
       return TT_ERR_UNSUPPORTED;
     s = ffn_tc_backward(U, D, T, x, dy, dx, ws, f.up.tc, f.down.tc, zs1, zs2, zl, st);
     prof_end(kPhBwd, st);
@@ -1306,7 +1301,7 @@ tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
     Pp[g] = P[g];
     zs[g] = static_cast<char*>(ws) + m.w[g].zs;
     offs[g] = m.w[g].tc;
-    if (!bwd_zero_add(&zl, plan->L[g], ws, m.w[g])) return TT_ERR_UNSUPPORTED;
+    if (!bwd_zero_add(&zl, plan->L[g], ws, m.w[g], dparams[g], acc)) return TT_ERR_UNSUPPORTED;
   }
   if (reuse) {
     for (int g = 0; g < G; ++g) chain_ptrs(plan->L[g], params[g], ws, m.w[g], P[g]);
@@ -1328,9 +1323,30 @@ tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
   prof_end(kPhBwd, st);
   if (s != TT_OK) return s;
   prof_begin(kPhMergeBwd, st);
-  for (int g = 0; g < G && s == TT_OK; ++g)
-    s = run_merge_backward(plan->L[g], params[g], P[g], fptr(ws, m.w[g].dA), fptr(ws, m.w[g].dB),
-                           dparams[g], acc, true, reuse, ws, m.w[g], st);
+  // the layers' programs in one launch where they fit one (a launch each
+  // otherwise, or with TTC_MULTI_MERGE_SPLIT=1, a measurement aid)
+  static int split = -1;
+  if (split < 0) {
+    const char* e = getenv("TTC_MULTI_MERGE_SPLIT");
+    split = (e && e[0] && e[0] != '0') ? 1 : 0;
+  }
+  s = TT_ERR_UNSUPPORTED;
+  if (!split && G > 1) {
+    MergeBwd* mb[TT_MULTI_MAX] = {};
+    alignas(MergeBwd) unsigned char store[TT_MULTI_MAX][sizeof(MergeBwd)];
+    for (int g = 0; g < G; ++g)
+      mb[g] = new (store[g]) MergeBwd(plan->L[g], params[g], P[g], fptr(ws, m.w[g].dA),
+                                      fptr(ws, m.w[g].dB), dparams[g], acc, true, reuse, ws,
+                                      m.w[g]);
+    s = run_merge_backward_multi(mb, G, st);
+    for (int g = 0; g < G; ++g) mb[g]->~MergeBwd();
+  }
+  if (s == TT_ERR_UNSUPPORTED) {  // nothing was launched
+    s = TT_OK;
+    for (int g = 0; g < G && s == TT_OK; ++g)
+      s = run_merge_backward(plan->L[g], params[g], P[g], fptr(ws, m.w[g].dA),
+                             fptr(ws, m.w[g].dB), dparams[g], acc, true, reuse, ws, m.w[g], st);
+  }
   prof_end(kPhMergeBwd, st);
   return s;
 }
