@@ -70,6 +70,7 @@ struct FfnFwdArgs {
   int kb1, kb2;     // 16-wide K blocks that cover the middle ranks (the rest is zero padding)
   int save_z;       // keep z1' and z2' (bf16 [T][64] each) for the backward
   int M;
+  int prefetch_x;   // x of the first stages requested before the dependency wait
   const float* Dc1;
   const float* Dc2;
 };
@@ -132,9 +133,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&S.fin, 1);
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < fwd_prefetched(p, FFN_NST_F); ++s) {  // x of the first chunks
+      uint8_t* st = stages + s * STAGE;
+      mbar_expect_tx(&S.full[s], 3 * BOX);
+      tma_load(st, &tm_x, &S.full[s], s * CH, blockIdx.x * TILE);
+      tma_load(st + BOX, &tm_x, &S.full[s], s * CH + 64, blockIdx.x * TILE);
+    }
   }
   if (warp == 1) tmem_alloc(&S.tmem_base);
-  pdl_wait();  // nothing a previous grid writes is touched before this point
+  pdl_wait();  // nothing a previous grid writes is touched before this point (but x above)
   pdl_trigger();
   if (threadIdx.x < RP) {
     S.Dc1[threadIdx.x] = p.Dc1[threadIdx.x];
@@ -155,6 +162,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int last_parity[FFN_NST_F];
       for (int s = 0; s < FFN_NST_F; ++s) last_parity[s] = -1;
       bool ok = true;
+      const int npre = fwd_prefetched(p, FFN_NST_F);  // x already requested
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
         const int tok0 = tile * TILE;
         for (int c = 0; c < nitems; ++c, ++it) {
@@ -162,7 +170,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t ph = (it / FFN_NST_F) & 1;
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 50)) { ok = false; break; }
           uint8_t* st = stages + s * STAGE;
-          if (c < p.nN) {
+          if (it < npre) {
+            tma_load(st + OPND, &tm_anr1, &S.full[s], 0, c * CH);
+          } else if (c < p.nN) {
             mbar_expect_tx(&S.full[s], 3 * BOX);
             tma_load(st, &tm_x, &S.full[s], c * CH, tok0);
             tma_load(st + BOX, &tm_x, &S.full[s], c * CH + 64, tok0);
@@ -925,7 +935,7 @@ bool ffn_tc_supported(const LayerPlan& U, const LayerPlan& D) {
 
 tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x, void* y,
                          void* ws, size_t off1, size_t off2, void* zs1, void* zs2,
-                         cudaStream_t st) {
+                         bool prefetch_x, cudaStream_t st) {
   if (T <= 0) return TT_OK;
   if (T > (int64_t)0x7FFFFFFF - TILE || !ffn_tc_supported(U, D)) return TT_ERR_UNSUPPORTED;
   if (!y && (!zs1 || !zs2)) return TT_ERR_INVALID_ARG;
@@ -954,6 +964,7 @@ tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, cons
   a.kb2 = kblocks(D.rd);
   a.save_z = (zs1 && zs2) ? 1 : 0;
   a.M = (int)D.M;
+  a.prefetch_x = prefetch_x && pdl_enabled() ? 1 : 0;
   a.Dc1 = at<float>(ws, off1 + t1.Dc);
   a.Dc2 = at<float>(ws, off2 + t2.Dc);
   const int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();

@@ -29,6 +29,7 @@ struct QkvFwdArgs {
   int M[kMaxGroups];
   int kb[kMaxGroups];
   int save_z;
+  int prefetch_x;  // x of the first chunks requested before the dependency wait
   const float* Dc[kMaxGroups];
 };
 
@@ -116,9 +117,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&S.fin, 1);
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int s = 0; s < fwd_prefetched(p, QKV_NACT); ++s) {  // x of the first chunks
+      uint8_t* st = act + s * ACT_STAGE;
+      mbar_expect_tx(&S.a_full[s], 2 * (uint32_t)p.tt * 128);
+      tma_load(st, &tm_x, &S.a_full[s], s * CH, blockIdx.x * p.tt);
+      tma_load(st + BOX, &tm_x, &S.a_full[s], s * CH + 64, blockIdx.x * p.tt);
+    }
   }
   if (warp == 1) tmem_alloc(&S.tmem_base);
-  pdl_wait();
+  pdl_wait();  // nothing a previous grid writes is touched before this point (but x above)
   pdl_trigger();
   for (int i = threadIdx.x; i < p.G * RP; i += blockDim.x) S.Dc[i / RP][i % RP] = p.Dc[i / RP][i % RP];
   zero_tail_boxes(act, 2 * QKV_NACT, zp_tile, 1, p.tt);
@@ -146,6 +153,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         return true;
       };
       const uint32_t act_bytes = (uint32_t)p.tt * 128;  // one activation box of tt rows
+      const int npre = fwd_prefetched(p, QKV_NACT);     // x already requested
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
         const int tok0 = tile * p.tt;
         for (int c = 0; ok && c < p.nN; ++c) {
@@ -153,9 +161,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t ph = (ia / QKV_NACT) & 1;
           if (!wait_bar(&S.a_empty[s], ph ^ 1, abort_flag, 121)) { ok = false; break; }
           uint8_t* st = act + s * ACT_STAGE;
-          mbar_expect_tx(&S.a_full[s], 2 * act_bytes);
-          tma_load(st, &tm_x, &S.a_full[s], c * CH, tok0);
-          tma_load(st + BOX, &tm_x, &S.a_full[s], c * CH + 64, tok0);
+          if (ia >= npre) {
+            mbar_expect_tx(&S.a_full[s], 2 * act_bytes);
+            tma_load(st, &tm_x, &S.a_full[s], c * CH, tok0);
+            tma_load(st + BOX, &tm_x, &S.a_full[s], c * CH + 64, tok0);
+          }
           lpa[s] = (int)ph;
           ++ia;
           for (int g = 0; g < p.G; ++g) {
@@ -696,7 +706,8 @@ bool multi_tc_supported(const LayerPlan* Ls, int G) {
 }
 
 tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x, void* const* y,
-                           void* ws, const size_t* offs, void* const* zs, cudaStream_t st) {
+                           void* ws, const size_t* offs, void* const* zs, bool prefetch_x,
+                           cudaStream_t st) {
   if (T <= 0) return TT_OK;
   if (T > (int64_t)0x7FFFFFFF - TILE || !multi_tc_supported(Ls, G)) return TT_ERR_UNSUPPORTED;
   if (set_qkv_attrs() != cudaSuccess) return TT_ERR_CUDA;
@@ -710,6 +721,7 @@ tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x,
   a.tt = tokens_per_tile(T);
   a.ntiles = (int)((T + a.tt - 1) / a.tt);
   a.save_z = keep ? 1 : 0;
+  a.prefetch_x = prefetch_x && pdl_enabled() ? 1 : 0;
   if (!make_map(&mx, x, Ls[0].N, T, 64, a.tt)) return TT_ERR_CUDA;
   for (int g = 0; g < kMaxGroups; ++g) {
     const int gg = g < G ? g : 0;  // unused slots repeat layer 0's maps

@@ -409,6 +409,9 @@ struct FwdArgs {
   int64_t T;
   int N, M, nN, nM, ntiles, tt;
   int save_z;  // also store each tile's z' (bf16 [T][64]) through tm_zs
+  // the grid before this one is the merge of the same call, which does not
+  // write x: the first stages' x boxes are requested before the dependency wait
+  int prefetch_x;
   const float* Dc;
   __nv_bfloat16* y;
 };
@@ -459,6 +462,13 @@ __device__ void zero_list(const ZeroList& z) {
   const int stride = gridDim.x * blockDim.x;
   for (int r = 0; r < z.count; ++r)
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < z.n[r]; i += stride) z.p[r][i] = 0.f;
+}
+
+// Stages whose x boxes a forward kernel requests before its dependency wait.
+template <typename Args>
+__device__ __forceinline__ int fwd_prefetched(const Args& p, int nstage) {
+  if (!p.prefetch_x || (int)blockIdx.x >= p.ntiles) return 0;
+  return p.nN < nstage ? p.nN : nstage;
 }
 
 __device__ void zero_tail_rows(uint8_t* stages, int nstage, uint8_t* zp_tile, int tt) {
@@ -529,9 +539,24 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
     mbar_init(&S.fin, 1);
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // x of the first tile's first chunks (rows 0..tt-1 of the activation
+    // boxes; zero_tail_rows below writes the other rows)
+    for (int s = 0; s < fwd_prefetched(p, NSTAGE_F); ++s) {
+      uint8_t* st = stages + s * STAGE;
+      const uint32_t act_bytes = (uint32_t)p.tt * 128;
+      const int tok0 = blockIdx.x * p.tt;
+      if (F8) {
+        mbar_expect_tx(&S.full[s], act_bytes + BOX);
+        tma_load(st + BOX, &tm_x, &S.full[s], s * CH, tok0);
+      } else {
+        mbar_expect_tx(&S.full[s], 2 * act_bytes + BOX);
+        tma_load(st, &tm_x, &S.full[s], s * CH, tok0);
+        tma_load(st + BOX, &tm_x, &S.full[s], s * CH + 64, tok0);
+      }
+    }
   }
   if (warp == 1) tmem_alloc(&S.tmem_base);
-  pdl_wait();  // nothing a previous grid writes is touched before this point
+  pdl_wait();  // nothing a previous grid writes is touched before this point (but x above)
   pdl_trigger();
   if (threadIdx.x < RP) S.Dc[threadIdx.x] = p.Dc[threadIdx.x];
   zero_tail_rows(stages, NSTAGE_F, zp_tile, p.tt);
@@ -552,6 +577,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       const uint32_t act_bytes = (uint32_t)p.tt * 128;  // one activation box of tt rows
       // test hook: the first CTA leaves its first stage unloaded
       const bool skip_first = blockIdx.x == 0 && debug_take(TT_DEBUG_FWD_TOKENS);
+      const int npre = fwd_prefetched(p, NSTAGE_F);  // x already requested
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x) {
         const int tok0 = tile * p.tt;
         for (int c = 0; ok && c < p.nN + p.nM; ++c, ++it) {
@@ -560,7 +586,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 1)) { ok = false; break; }
           if (skip_first && it == 0) continue;
           uint8_t* st = stages + s * STAGE;
-          if (c < p.nN) {
+          if (it < npre) {
+            tma_load(st + OPND, &tm_anr, &S.full[s], 0, c * CH);
+          } else if (c < p.nN) {
             if (F8) {  // one E4M3 box of 128 columns into the second bf16 box's bytes
               mbar_expect_tx(&S.full[s], act_bytes + BOX);
               tma_load(st + BOX, &tm_x, &S.full[s], c * CH, tok0);
@@ -1445,7 +1473,7 @@ TcPtrs tc_ptrs(const LayerPlan& L, void* ws, size_t off) {
 }
 
 tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws, size_t off,
-                     bool f8, void* zs, cudaStream_t st) {
+                     bool f8, void* zs, bool prefetch_x, cudaStream_t st) {
   if (T <= 0) return TT_OK;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
   if (f8 && !tc_f8_supported(L)) return TT_ERR_UNSUPPORTED;
@@ -1469,6 +1497,7 @@ tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void
   a.tt = tt;
   a.ntiles = (int)((T + tt - 1) / tt);
   a.save_z = zs != nullptr;
+  a.prefetch_x = prefetch_x && pdl_enabled() ? 1 : 0;
   a.Dc = at<float>(ws, off + t.Dc);
   a.y = static_cast<__nv_bfloat16*>(y);
   int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();

@@ -31,8 +31,11 @@ size_t tc_operand_bytes(const LayerPlan& L);
 // merge engine's pack phase) are in the workspace at ws_off.  x is bf16, or
 // E4M3 codes when f8; y is bf16.  With zs (256-byte aligned, T x 64 bf16) the
 // kernel also stores z' = (x A) diag(D_d) there, rank compacted and padded.
+// prefetch_x: the launch right before this one on the stream is the merge of
+// the same call, which does not write x; the kernel then requests its first
+// x boxes before waiting for that grid.
 tt_status tc_forward(const LayerPlan& L, int64_t T, const void* x, void* y, void* ws,
-                     size_t ws_off, bool f8, void* zs, cudaStream_t st);
+                     size_t ws_off, bool f8, void* zs, bool prefetch_x, cudaStream_t st);
 
 // Ranges of floats a backward token kernel sets to zero on its way: scratch
 // that the merge backward then adds into, and the gradients that its
@@ -100,7 +103,7 @@ bool ffn_tc_supported(const LayerPlan& U, const LayerPlan& D);
 // then only z1' and z2' are computed.
 tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x, void* y,
                          void* ws, size_t off1, size_t off2, void* zs1, void* zs2,
-                         cudaStream_t st);
+                         bool prefetch_x, cudaStream_t st);
 
 // dx and both layers' token sums (dAc, dBc, dDc, zeroed beforehand) for T
 // tokens from x, dy and the forward's z1', z2' (zs1, zs2); h, GELU(h), da and
@@ -119,7 +122,8 @@ bool multi_tc_supported(const LayerPlan* Ls, int G);
 // operands at offs[g] of ws.  With zs (G pointers, T x 64 bf16 each) every
 // z'_g is kept there; y may be null when zs is given (then only z'_g).
 tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x, void* const* y,
-                           void* ws, const size_t* offs, void* const* zs, cudaStream_t st);
+                           void* ws, const size_t* offs, void* const* zs, bool prefetch_x,
+                           cudaStream_t st);
 
 // dx = sum_g dy[g] W_g and every layer's token sums (dAc, dBc, dDc, zeroed
 // beforehand) from x, dy[g] and the forward's z'_g; x streamed once.

@@ -678,7 +678,7 @@ tt_status layer_forward(const LayerPlan& L, int64_t T, const void* x, int tx, co
   prof_begin(kPhFwd, st);
   if (tc) {
     void* zs = (L.flags & TT_REUSE_Z) ? static_cast<char*>(ws) + w.zs : nullptr;
-    s = tc_forward(L, T, x, y, ws, w.tc, tx == TT_DT_E4M3, zs, st);
+    s = tc_forward(L, T, x, y, ws, w.tc, tx == TT_DT_E4M3, zs, true, st);  // after the merge
   } else {
     const float* A = P[L.d - 1];   // N x rd
     const float* B = P[L.K - 1];   // rd x M
@@ -1054,7 +1054,7 @@ tt_status tt_ffn_forward(const tt_plan_t* plan, int64_t T, const void* x,
     prof_begin(kPhFwd, st);
     s = ffn_tc_forward(U, D, T, x, y, ws, f.up.tc, f.down.tc,
                        keep ? static_cast<char*>(ws) + f.up.zs : nullptr,
-                       keep ? static_cast<char*>(ws) + f.down.zs : nullptr, st);
+                       keep ? static_cast<char*>(ws) + f.down.zs : nullptr, true, st);
     prof_end(kPhFwd, st);
     return s;
   }
@@ -1114,7 +1114,7 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
     void* zs2 = static_cast<char*>(ws) + f.down.zs;
     if (T > 0 && !((U.flags & TT_REUSE_Z) && reuse)) {
       prof_begin(kPhFwd, st);
-      s = ffn_tc_forward(U, D, T, x, nullptr, ws, f.up.tc, f.down.tc, zs1, zs2, st);
+      s = ffn_tc_forward(U, D, T, x, nullptr, ws, f.up.tc, f.down.tc, zs1, zs2, !reuse, st);
       prof_end(kPhFwd, st);
       if (s != TT_OK) return s;
     }
@@ -1248,7 +1248,7 @@ tt_status tt_multi_forward(const tt_plan_t* plan, int64_t T, const void* x,
   prof_end(kPhMerge, st);
   if (s != TT_OK) return s;
   prof_begin(kPhFwd, st);
-  s = multi_tc_forward(plan->L, G, T, x, y, ws, offs, keep ? zs : nullptr, st);
+  s = multi_tc_forward(plan->L, G, T, x, y, ws, offs, keep ? zs : nullptr, true, st);
   prof_end(kPhFwd, st);
   return s;
 }
@@ -1314,7 +1314,7 @@ tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
   // every z'_g: the forward's under TT_REUSE_Z, else computed here
   if (T > 0 && !((plan->L[0].flags & TT_REUSE_Z) && reuse)) {
     prof_begin(kPhFwd, st);
-    s = multi_tc_forward(plan->L, G, T, x, nullptr, ws, offs, zs, st);
+    s = multi_tc_forward(plan->L, G, T, x, nullptr, ws, offs, zs, !reuse, st);
     prof_end(kPhFwd, st);
     if (s != TT_OK) return s;
   }
