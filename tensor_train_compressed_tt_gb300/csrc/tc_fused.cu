@@ -126,11 +126,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
 __device__ unsigned long long g_tl[4][256][16];  // fwd, bwd, engine (1 phase), engine (more)
 __device__ unsigned long long g_tlu[256][8][8];  // engine units: (phase*100+task, start, end, inner stamps)
 #define TL_STAMP(k, slot) (g_tl[(k)][blockIdx.x & 255][(slot)] = gtimer())
+// per-warp stamps of the backward token kernel's CTA 0: [warp][slot]
+__device__ unsigned long long g_tlk[16][48];
+#define TLK(slot) \
+  if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (slot) < 48) g_tlk[threadIdx.x >> 5][(slot)] = gtimer()
 #define TLU_STAMP(nu, slot) \
   if (threadIdx.x == 0 && (nu) < 8) g_tlu[blockIdx.x & 255][(nu)][(slot)] = gtimer()
 #else
 #define TLU_STAMP(nu, slot) ((void)0)
 #define TL_STAMP(k, slot) ((void)0)
+#define TLK(slot) ((void)0)
 #endif
 
 __device__ void record_error(unsigned code, unsigned where) {
@@ -464,6 +469,15 @@ __device__ void zero_list(const ZeroList& z) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < z.n[r]; i += stride) z.p[r][i] = 0.f;
 }
 
+// The compacted middle rank r' (the nonzero entries of Dc come first) and the
+// 16-wide K blocks of the rank dimension that cover it (at least one).
+__device__ __forceinline__ int compacted_rank(const float* Dc) {
+  int r = 0;
+  while (r < RP && Dc[r] != 0.f) ++r;
+  return r;
+}
+__device__ __forceinline__ int rank_kblocks(int r) { return r > 0 ? (r + 15) >> 4 : 1; }
+
 // Stages whose x boxes a forward kernel requests before its dependency wait.
 template <typename Args>
 __device__ __forceinline__ int fwd_prefetched(const Args& p, int nstage) {
@@ -617,6 +631,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       const uint32_t id_y = idesc(128, 128, 0, 1);  // B = Bm rows, MN-major
       const uint32_t zp_addr = su32(zp_tile);
       uint64_t* ready = F8 ? S.conv : S.full;  // a stage the MMAs may read
+      const int kb = rank_kblocks(compacted_rank(S.Dc));  // z' columns past r' are 0
       int it = 0, yc = 0, tl = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.ntiles; tile += gridDim.x, ++tl) {
@@ -653,8 +668,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           if (c < 3) TL_STAMP(0, 10 + c);  // Bm chunk in shared memory
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < kb; ++k)
             mma(tmem + F_Y + yb * 128, kdesc(zp_addr) + 2 * k,
                 mndesc(st + OPND, BOX / 2) + 128 * k, id_y, k != 0);
           mma_commit(&S.empty[s]);
@@ -846,6 +860,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           const int s = it % NSTAGE_B;
           const uint32_t ph = (it / NSTAGE_B) & 1;
           if (!wait_bar(&S.empty[s], ph ^ 1, abort_flag, 11)) { ok = false; break; }
+          if (tl == 0) TLK(it);  // stage free, load issued
           if (skip_first && it == 0) continue;
           uint8_t* st = stages + s * STAGE;
           mbar_expect_tx(&S.full[s], (F8 ? act_bytes : 2 * act_bytes) + BOX);
@@ -880,7 +895,11 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_r = idesc(128, 64, 0, 0);     // token x rank, K-major
+      // dz' = dy Bm^T needs only the compacted ranks: N = 32 when r' <= 32
+      // (Bm rows past r' are zero); dx = dz Anr^T only the K blocks that cover r'
+      const int rprime = compacted_rank(S.Dc);
+      const int kb = rank_kblocks(rprime);
+      const uint32_t id_r = idesc(128, rprime <= 32 ? 32 : 64, 0, 0);  // token x rank, K-major
       const uint32_t id_a = idesc(128, 64, 0, 1);     // token x rank, B = Anr rows MN-major
       const uint32_t id_w = idesc(128, 64, 1, 1);     // weight x rank, MN-major
       const uint32_t id_x = idesc(128, 128, 0, 0);    // token x feature, K-major
@@ -915,6 +934,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         for (int c = 0; c < p.nM; ++c, ++it, ++wc) {
           const int s = it % NSTAGE_B;
           if (!wait_bar(&ready[s], (it / NSTAGE_B) & 1, abort_flag, 15)) { ok = false; break; }
+          if (tl == 0) TLK(2 * c);  // dy chunk c in shared memory
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
 #pragma unroll
@@ -932,6 +952,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           }
           const int wb = wc & 1;
           if (!wait_bar(&S.w_empty[wb], ((wc >> 1) & 1) ^ 1, abort_flag, 17)) { ok = false; break; }
+          if (tl == 0) TLK(2 * c + 1);  // W buffer free
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
@@ -954,8 +975,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
           if (!wait_bar(&S.x_empty[xb], ((xc >> 1) & 1) ^ 1, abort_flag, 20)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < kb; ++k)
             mma(tmem + B_X + xb * 128, kdesc(dz_addr) + 2 * k, kdesc(st + OPND) + 2 * k, id_x,
                 k != 0);
           mma_commit(&S.x_full[xb]);
@@ -1025,11 +1045,13 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       for (int c = 0; c < p.nM; ++c, ++wc) {
         const int wb = wc & 1;
         if (!warp_wait(&S.w_full[wb], (wc >> 1) & 1, abort_flag, 24)) { ok = false; break; }
+        if (tl == 0) TLK(2 * c);  // W chunk c in TMEM
         tc_fence_after();
         tmem_ld32(tmem + lane_off + B_W + wb * 64 + 32 * h, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.w_empty[wb]);
+        if (tl == 0) TLK(2 * c + 1);  // released
         // rows = outputs c*128 + 32q.., columns = compacted ranks 32h..
         const int cb = rot_chunk(c, p.nM, tile);  // the producer's order of dy chunks
         if (32 * h < rprime && cb * CH + 32 * q < p.M) {
@@ -1051,10 +1073,15 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
         }
       }
       if (!ok) break;
-      // E3: dz' -> dDc, dz tile
+      // E3: dz' -> dDc, dz tile (columns 32.. are not computed when r' <= 32)
       if (!warp_wait(&S.dzp_full, tl & 1, abort_flag, 25)) break;
+      if (tl == 0) TLK(20);
       tc_fence_after();
       tmem_ld32(tmem + lane_off + B_DZP + 32 * h, v);
+      if (32 * h >= rprime) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dzp_empty);
@@ -1087,11 +1114,13 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dz_full);
+      if (tl == 0) TLK(21);
       if (warp == 2 && lane == 0) TL_STAMP(1, 5);
       // E4: dx chunks (row = token), dA chunks (row = feature within the chunk)
       for (int c = 0; c < p.nN; ++c, ++xc, ++wc) {
         const int xb = xc & 1;
         if (!warp_wait(&S.x_full[xb], (xc >> 1) & 1, abort_flag, 27)) { ok = false; break; }
+        if (tl == 0) TLK(22 + 2 * c);  // dx chunk c in TMEM
         tc_fence_after();
         const int cx = rot_chunk(c, p.nN, tile);  // the producer's order of phase-C x chunks
         const int col = cx * CH + 64 * h;
@@ -1607,6 +1636,9 @@ extern "C" int ttc_timeline_read(void* host, size_t bytes) {
 }
 extern "C" int ttc_timeline_units_read(void* host, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(host, ttc::g_tlu, bytes);
+}
+extern "C" int ttc_timeline_bwd_warps_read(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, ttc::g_tlk, bytes);
 }
 static cudaStream_t g_probe_stream = 0;
 extern "C" void ttc_probe_set_stream(void* st) { g_probe_stream = static_cast<cudaStream_t>(st); }
