@@ -35,24 +35,29 @@ __device__ __forceinline__ float tanh_hw(float x) {
 constexpr float kGeluK = 0.79788456080286536f;                 // sqrt(2 / pi)
 constexpr float kGeluKC = 0.79788456080286536f * 0.044715f;    // sqrt(2 / pi) * 0.044715
 
-// GELU(u) = u Phi(u), Phi(u) ~ (1 + tanh(k (u + c u^3))) / 2
-__device__ __forceinline__ float gelu_tanh(float u) {
-  const float t = tanh_hw(u * fmaf(kGeluKC, u * u, kGeluK));
-  const float hu = 0.5f * u;
-  return fmaf(hu, t, hu);
+// GELU(u) = u Phi(u), Phi(u) ~ (1 + tanh(k (u + c u^3))) / 2, and with it
+// g = da * GELU'(u) of the same approximation,
+// GELU'(u) = (1 + t) / 2 + (u / 2)(1 - t^2) k (1 + 3 c u^2), t = tanh(k (u + c u^3)).
+// Both for a pair of elements in packed f32x2 arithmetic (two FMAs an
+// instruction on this architecture, each rounded as a scalar FMA); the tanh
+// stays one special-function operation an element.
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float2 gelu_tanh2(float2 u) {
+  const float2 arg = __fmul2_rn(u, __ffma2_rn(f2(kGeluKC), __fmul2_rn(u, u), f2(kGeluK)));
+  const float2 t = make_float2(tanh_hw(arg.x), tanh_hw(arg.y));
+  const float2 hu = __fmul2_rn(f2(0.5f), u);
+  return __ffma2_rn(hu, t, hu);
 }
-
-// a = GELU(u) and g = da * GELU'(u) of the same approximation:
-// GELU'(u) = (1 + t) / 2 + (u / 2)(1 - t^2) k (1 + 3 c u^2)
-__device__ __forceinline__ void gelu_tanh_grad(float u, float da, float& a, float& g) {
-  const float u2 = u * u;
-  const float t = tanh_hw(u * fmaf(kGeluKC, u2, kGeluK));
-  const float hu = 0.5f * u;
-  a = fmaf(hu, t, hu);
-  const float dq = fmaf(3.f * kGeluKC, u2, kGeluK);  // d/du of k (u + c u^3)
-  const float omt = fmaf(-t, t, 1.f);
-  const float d = fmaf(hu * omt, dq, fmaf(0.5f, t, 0.5f));
-  g = da * d;
+__device__ __forceinline__ void gelu_tanh_grad2(float2 u, float2 da, float2& a, float2& g) {
+  const float2 u2 = __fmul2_rn(u, u);
+  const float2 arg = __fmul2_rn(u, __ffma2_rn(f2(kGeluKC), u2, f2(kGeluK)));
+  const float2 t = make_float2(tanh_hw(arg.x), tanh_hw(arg.y));
+  const float2 hu = __fmul2_rn(f2(0.5f), u);
+  a = __ffma2_rn(hu, t, hu);
+  const float2 dq = __ffma2_rn(f2(3.f * kGeluKC), u2, f2(kGeluK));
+  const float2 omt = __ffma2_rn(make_float2(-t.x, -t.y), t, f2(1.f));
+  const float2 d = __ffma2_rn(__fmul2_rn(hu, omt), dq, __ffma2_rn(f2(0.5f), t, f2(0.5f)));
+  g = __fmul2_rn(da, d);
 }
 
 // Per-warp stamps of CTA 0 (timeline builds only): [kernel][warp][slot]
@@ -348,9 +353,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) mbar_arrive(&S.h_empty[hb]);
         ++hc;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = gelu_tanh(v[j]);
-          w[j] = gelu_tanh(w[j]);
+        for (int j = 0; j < 32; j += 2) {
+          const float2 gv = gelu_tanh2(make_float2(v[j], v[j + 1]));
+          const float2 gw = gelu_tanh2(make_float2(w[j], w[j + 1]));
+          v[j] = gv.x;
+          v[j + 1] = gv.y;
+          w[j] = gw.x;
+          w[j + 1] = gw.y;
         }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(0, 3 + 3 * c);
         if (tl == 0 && c < 8) TLW(0, 4 * c + 1);
@@ -818,15 +827,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t pa0[16], pa1[16], pd0[16], pd1[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float a0, a1, g0, g1;
-          gelu_tanh_grad(h0[2 * j], d0[2 * j], a0, g0);
-          gelu_tanh_grad(h0[2 * j + 1], d0[2 * j + 1], a1, g1);
-          pa0[j] = pack_bf16(a0, a1);
-          pd0[j] = pack_bf16(g0, g1);
-          gelu_tanh_grad(h1[2 * j], d1[2 * j], a0, g0);
-          gelu_tanh_grad(h1[2 * j + 1], d1[2 * j + 1], a1, g1);
-          pa1[j] = pack_bf16(a0, a1);
-          pd1[j] = pack_bf16(g0, g1);
+          float2 a, g;
+          gelu_tanh_grad2(make_float2(h0[2 * j], h0[2 * j + 1]),
+                          make_float2(d0[2 * j], d0[2 * j + 1]), a, g);
+          pa0[j] = pack_bf16(a.x, a.y);
+          pd0[j] = pack_bf16(g.x, g.y);
+          gelu_tanh_grad2(make_float2(h1[2 * j], h1[2 * j + 1]),
+                          make_float2(d1[2 * j], d1[2 * j + 1]), a, g);
+          pa1[j] = pack_bf16(a.x, a.y);
+          pd1[j] = pack_bf16(g.x, g.y);
         }
         if (warp == 2 && lane == 0 && tl == 0 && c < 3) TL_STAMP(1, 3 + 3 * c);
         if (tl == 0 && c < 8) TLW(1, 4 * c + 1);
