@@ -62,9 +62,9 @@ __device__ __forceinline__ void gelu_tanh_grad2(float2 u, float2 da, float2& a, 
 
 // Per-warp stamps of CTA 0 (timeline builds only): [kernel][warp][slot]
 #ifdef TTC_TIMELINE
-__device__ unsigned long long g_tlw[2][16][32];
+__device__ unsigned long long g_tlw[2][16][48];
 #define TLW(k, slot) \
-  if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (slot) < 32) g_tlw[(k)][threadIdx.x >> 5][(slot)] = gtimer()
+  if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (slot) < 48) g_tlw[(k)][threadIdx.x >> 5][(slot)] = gtimer()
 #else
 #define TLW(k, slot) ((void)0)
 #endif
@@ -73,6 +73,7 @@ struct FfnFwdArgs {
   int64_t T;
   int nN, nH, nM, ntiles;
   int kb1, kb2;     // 16-wide K blocks that cover the middle ranks (the rest is zero padding)
+  int nr;           // MMA width of the rank dimension: 32 when both middle ranks are <= 32, else 64
   int save_z;       // keep z1' and z2' (bf16 [T][64] each) for the backward
   int M;
   int prefetch_x;   // x of the first stages requested before the dependency wait
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_z = idesc(128, 64, 0, 1);   // B = rows [K][64 ranks], MN-major
+      const uint32_t id_z = idesc(128, p.nr, 0, 1);  // B = rows [K][64 ranks], MN-major
       const uint32_t id_h = idesc(128, 128, 0, 1);  // B = [64 ranks][128 columns], MN-major
       const uint32_t zp_addr = su32(zp);
       const uint32_t at_addr = su32(atile);
@@ -326,12 +327,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!warp_wait(&S.z1_full, tl & 1, abort_flag, 61)) break;
       if (warp == 2 && lane == 0 && tl == 0) TL_STAMP(0, 1);
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + FF_Z1 + 32 * h, v);
+      if (32 * h < p.nr) tmem_ld32(tmem + lane_off + FF_Z1 + 32 * h, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.z1_empty);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= S.Dc1[32 * h + j];
+      for (int j = 0; j < 32; ++j) v[j] = 32 * h < p.nr ? v[j] * S.Dc1[32 * h + j] : 0.f;
       if (!warp_wait(&S.zp_empty, 1, abort_flag, 62)) break;
       st_tile_half(zp, row, h, v);
       fence_async_smem();
@@ -379,12 +380,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!warp_wait(&S.z2_full, tl & 1, abort_flag, 66)) break;
       if (warp == 2 && lane == 0 && tl == 0) TL_STAMP(0, 11);
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + FF_Z2 + 32 * h, v);
+      if (32 * h < p.nr) tmem_ld32(tmem + lane_off + FF_Z2 + 32 * h, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.z2_empty);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= S.Dc2[32 * h + j];
+      for (int j = 0; j < 32; ++j) v[j] = 32 * h < p.nr ? v[j] * S.Dc2[32 * h + j] : 0.f;
       if (!warp_wait(&S.zp_empty, 0, abort_flag, 67)) break;
       st_tile_half(zp, row, h, v);
       fence_async_smem();
@@ -448,6 +449,7 @@ struct FfnBwdArgs {
   int64_t T;
   int nN, nH, nM, ntiles;
   int kb1, kb2;
+  int nr;  // as in FfnFwdArgs; 32 also splits each W drain to one warp half
   int N, H, M;
   const float* Dc1;
   const float* Dc2;
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&S.ad_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.w_full[b], 1);
-      mbar_init(&S.w_empty[b], NEPI);
+      mbar_init(&S.w_empty[b], p.nr == 32 ? NEPI / 2 : NEPI);
       mbar_init(&S.x_full[b], 1);
       mbar_init(&S.x_empty[b], NEPI);
     }
@@ -608,8 +610,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_r = idesc(128, 64, 0, 0);    // token x rank, both K-major
-      const uint32_t id_w = idesc(128, 64, 1, 1);    // weight x rank, both MN-major
+      const uint32_t id_r = idesc(128, p.nr, 0, 0);  // token x rank, both K-major
+      const uint32_t id_w = idesc(128, p.nr, 1, 1);  // weight x rank, both MN-major
       const uint32_t id_n = idesc(128, 128, 0, 0);   // token x 128 columns, K = rank
       const uint32_t id_h = idesc(128, 128, 0, 1);   // token x 128 columns, B MN-major
       const uint32_t z1a = su32(zt1), z2a = su32(zt2);
@@ -668,8 +670,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int s = (ih + c) % FFN_NST_B;
           if (!wait_bar(&S.full[s], ((ih + c) / FFN_NST_B) & 1, abort_flag, 78)) return false;
           if (tl == 0 && c < 4) TLW(1, 16 + c);
+          if (tl == 0 && c >= 4 && c < 8) TLW(1, 32 + 3 * (c - 4));
           if (!wait_bar(&S.hd_empty, (hdc & 1) ^ 1, abort_flag, 79)) return false;
           if (tl == 0 && c < 4) TLW(1, 20 + c);
+          if (tl == 0 && c >= 4 && c < 8) TLW(1, 33 + 3 * (c - 4));
           tc_fence_after();
           const uint32_t st = su32(stages + s * STAGE);
           for (int k = 0; k < p.kb1; ++k)
@@ -708,6 +712,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           w_done();
           mma_commit(&S.ad_empty);
           mma_commit(&S.empty[s]);
+          if (tl == 0 && c >= 4 && c < 8) TLW(1, 34 + 3 * (c - 4));
           ++adc;
         }
         if (!ok) break;
@@ -750,25 +755,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint8_t* box = staging + (warp - 2) * STG;
     int wc = 0, xc = 0, hdc = 0, adc = 0, tl = 0;
     // drain the next W buffer: 32 rank columns of 32 weight rows, bulk-added
-    // into the token sum `map` at (row0 + 32 q, 32 h) when row0 + 32 q < nrows
+    // into the token sum `map` at (row0 + 32 q, col0) when row0 + 32 q < nrows.
+    // 64 rank columns: every warp drains every buffer, half h its columns 32 h..;
+    // 32 rank columns: buffer b is drained by the warps of half b alone, so the
+    // two W products of a hidden chunk are drained side by side
     auto drain_w = [&](const CUtensorMap* map, int row0, int nrows, int rprime) -> bool {
       float v[32];
       const int wb = wc & 1;
+      const int col0 = p.nr == 32 ? 0 : 32 * h;
+      if (p.nr == 32 && wb != h) {
+        ++wc;
+        return true;
+      }
       if (!warp_wait(&S.w_full[wb], (wc >> 1) & 1, abort_flag, 84)) return false;
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + FB_W + wb * 64 + 32 * h, v);
+      tmem_ld32(tmem + lane_off + FB_W + wb * 64 + col0, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.w_empty[wb]);
       ++wc;
-      if (32 * h < rprime && row0 + 32 * q < nrows) {
+      if (col0 < rprime && row0 + 32 * q < nrows) {
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         stage_f32_32(box, lane, v);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add(map, box, 32 * h, row0 + 32 * q);
+          tma_reduce_add(map, box, col0, row0 + 32 * q);
           bulk_commit();
         }
       }
@@ -794,7 +807,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!warp_wait(&S.dzp2_full, tl & 1, abort_flag, 85)) break;
       if (warp == 2 && lane == 0 && tl == 0) TL_STAMP(1, 1);
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + FB_DZ2P + 32 * h, v);
+      if (32 * h < p.nr) {
+        tmem_ld32(tmem + lane_off + FB_DZ2P + 32 * h, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;  // rank columns the MMAs left out
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dzp2_empty);
@@ -858,6 +876,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             break;
           }
         }
+        if (tl == 0 && c < 8) TLW(1, 32 + c);
       }
       if (!ok) break;
       {
@@ -868,7 +887,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!warp_wait(&S.dz1p_full, tl & 1, abort_flag, 90)) break;
       if (warp == 2 && lane == 0 && tl == 0) TL_STAMP(1, 11);
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + FB_DZ1P + 32 * h, v);
+      if (32 * h < p.nr) {
+        tmem_ld32(tmem + lane_off + FB_DZ1P + 32 * h, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dz1p_empty);
@@ -971,6 +995,7 @@ tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, cons
   a.ntiles = (int)((T + TILE - 1) / TILE);
   a.kb1 = kblocks(U.rd);
   a.kb2 = kblocks(D.rd);
+  a.nr = U.rd <= 32 && D.rd <= 32 ? 32 : 64;
   a.save_z = (zs1 && zs2) ? 1 : 0;
   a.M = (int)D.M;
   a.prefetch_x = prefetch_x && pdl_enabled() ? 1 : 0;
@@ -1013,6 +1038,7 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
   a.ntiles = (int)((T + TILE - 1) / TILE);
   a.kb1 = kblocks(U.rd);
   a.kb2 = kblocks(D.rd);
+  a.nr = U.rd <= 32 && D.rd <= 32 ? 32 : 64;
   a.N = (int)U.N;
   a.H = (int)U.M;
   a.M = (int)D.M;

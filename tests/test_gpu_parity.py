@@ -362,14 +362,16 @@ def test_ffn_reuse_matches_recompute():
     assert O.rel_err(gd1.cpu().numpy(), gd0.cpu().numpy()) <= 1e-3
 
 
-@pytest.mark.parametrize("act", ["f32", "bf16"])
-def test_ffn_pair_small(act):
+@pytest.mark.parametrize("act,rmid", [("f32", 12), ("bf16", 12), ("bf16", 40)])
+def test_ffn_pair_small(act, rmid):
     """A small FFN pair on both token paths (f32: SIMT GEMMs and the f32 GELU
-    kernels; bf16: tensor-core kernels), 300 tokens, against the oracle."""
+    kernels; bf16: tensor-core kernels), 300 tokens, against the oracle.  A
+    middle rank of 12 takes the fused kernels' 32-wide rank products, 40 the
+    64-wide ones."""
     import dataclasses
-    up = synth.LayerShape((8, 16), (16, 16), (1, 8, 12, 16, 1))
-    dn = synth.LayerShape((16, 16), (8, 16), (1, 16, 12, 8, 1))
-    w = dataclasses.replace(synth.WORKLOADS["ffn768_3072_bf16"], name=f"ffn_small_{act}",
+    up = synth.LayerShape((8, 16), (16, 16), (1, 8, rmid, 16, 1))
+    dn = synth.LayerShape((16, 16), (8, 16), (1, 16, rmid, 8, 1))
+    w = dataclasses.replace(synth.WORKLOADS["ffn768_3072_bf16"], name=f"ffn_small_{act}_{rmid}",
                             layers=(up, dn), tokens=300, act=act, core_std=0.2)
     inp = synth.draw(w, seed=8)
     out, gu, gd = gpu_ffn(w, inp)
