@@ -1189,30 +1189,77 @@ __global__ void __launch_bounds__(F8 ? NTHREADS_F8 : NTHREADS, 1)
 // ==========================================================================
 // fixed-order sum of the per-CTA token-sum slots (TT_DETERMINISTIC)
 //   dAc[i] = sum_k slotA[k][i], dBc[i] = sum_k slotB[k][i],
-//   dDc[c] = sum_k sum_q slotD[k][q][c], k = 0 .. G-1 in order
+//   dDc[c] = sum_{k, q} slotD[k][q][c]
+// The slots of one output are split into four fixed ranges of k; each range
+// is summed in increasing k by its own quarter of the block (eight slots in
+// flight a thread, four floats a load), and the four partial sums are added
+// in range order: the same order, and so the same bits, on every call.
+// Columns at or past `wcol` of a 64-wide row (ranks the layer does not have:
+// the token kernel writes no slot entry there) come out 0 without a read.
 // ==========================================================================
-__global__ void det_sum_kernel(const float* __restrict__ slotA, const float* __restrict__ slotB,
-                               const float* __restrict__ slotD, int G, int64_t nA, int64_t nB,
-                               float* dAc, float* dBc, float* dDc) {
+__device__ __forceinline__ void add4(float4& s, const float4 v) {
+  s.x += v.x;
+  s.y += v.y;
+  s.z += v.z;
+  s.w += v.w;
+}
+
+constexpr int kDetCols = 64;  // float4 columns a block handles at a time (x 4 ranges = 256 threads)
+
+__global__ void __launch_bounds__(4 * kDetCols) det_sum_kernel(
+    const float* __restrict__ slotA, const float* __restrict__ slotB,
+    const float* __restrict__ slotD, int G, int64_t nA, int64_t nB, int wcol, float* dAc,
+    float* dBc, float* dDc) {
   pdl_wait();  // the token kernel's slots are complete
   pdl_trigger();
-  const int64_t n = nA + nB + RP;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    float v = 0.f;
-    if (i < nA) {
-      for (int k = 0; k < G; ++k) v += __ldcg(slotA + (int64_t)k * nA + i);
-      dAc[i] = v;
-    } else if (i < nA + nB) {
-      const int64_t j = i - nA;
-      for (int k = 0; k < G; ++k) v += __ldcg(slotB + (int64_t)k * nB + j);
-      dBc[j] = v;
-    } else {
-      const int c = (int)(i - nA - nB);
-      for (int k = 0; k < G; ++k)
-        for (int q = 0; q < 4; ++q) v += __ldcg(slotD + ((int64_t)k * 4 + q) * RP + c);
-      dDc[c] = v;
+  __shared__ float4 part[4][kDetCols];
+  const int kg = (int)threadIdx.x / kDetCols, vc = (int)threadIdx.x % kDetCols;
+  const int64_t nvA = nA / 4, nvB = nB / 4, nvD = RP / 4, nv = nvA + nvB + nvD;
+  for (int64_t v0 = (int64_t)blockIdx.x * kDetCols; v0 < nv; v0 += (int64_t)gridDim.x * kDetCols) {
+    const int64_t v = v0 + vc;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* base = nullptr;
+    int64_t stride = 0;  // float4s from one slot to the next
+    int cnt = 0;         // slots summed (0: a column past wcol)
+    if (4 * (int)(v % (RP / 4)) >= wcol) {
+      // nA and nB are whole 64-wide rows, so v % 16 is the column in every region
+    } else if (v < nvA) {
+      base = reinterpret_cast<const float4*>(slotA) + v;
+      stride = nvA;
+      cnt = G;
+    } else if (v < nvA + nvB) {
+      base = reinterpret_cast<const float4*>(slotB) + (v - nvA);
+      stride = nvB;
+      cnt = G;
+    } else if (v < nv) {
+      base = reinterpret_cast<const float4*>(slotD) + (v - nvA - nvB);
+      stride = nvD;  // slots (k, q) in k-major order
+      cnt = 4 * G;
     }
+    const int k0 = (int)((int64_t)cnt * kg / 4), k1 = (int)((int64_t)cnt * (kg + 1) / 4);
+    int k = k0;
+    for (; k + 8 <= k1; k += 8) {
+      float4 r[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r[j] = __ldcg(base + (int64_t)(k + j) * stride);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) add4(s, r[j]);
+    }
+    for (; k < k1; ++k) add4(s, __ldcg(base + (int64_t)k * stride));
+    part[kg][vc] = s;
+    __syncthreads();
+    if (kg == 0 && v < nv) {
+      float4 t = part[0][vc];
+      add4(t, part[1][vc]);
+      add4(t, part[2][vc]);
+      add4(t, part[3][vc]);
+      float* out = v < nvA ? dAc + 4 * v : v < nvA + nvB ? dBc + 4 * (v - nvA) : dDc + 4 * (v - nvA - nvB);
+      out[0] = t.x;
+      out[1] = t.y;
+      out[2] = t.z;
+      out[3] = t.w;
+    }
+    __syncthreads();
   }
 }
 
@@ -1601,10 +1648,13 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   if (e != cudaSuccess) return TT_ERR_CUDA;
   if (det) {  // the slots of the `grid` CTAs, summed in CTA order
     const int64_t nA = L.N * RP, nB = L.M * RP;
-    const int blocks = (int)((nA + nB + RP + 255) / 256 < 4 * num_sms() ? (nA + nB + RP + 255) / 256
-                                                                        : 4 * num_sms());
-    e = launch_ex(det_sum_kernel, blocks, 256, 0, st, false, (const float*)det->a,
-                  (const float*)det->b, (const float*)det->d, grid, nA, nB, a.dAc, a.dBc, a.dDc);
+    const int64_t cols = (nA + nB + RP) / 4;
+    const int blocks = (int)((cols + kDetCols - 1) / kDetCols < 8 * num_sms()
+                                 ? (cols + kDetCols - 1) / kDetCols
+                                 : 8 * num_sms());
+    e = launch_ex(det_sum_kernel, blocks, 4 * kDetCols, 0, st, false, (const float*)det->a,
+                  (const float*)det->b, (const float*)det->d, grid, nA, nB, L.rd <= 32 ? 32 : RP,
+                  a.dAc, a.dBc, a.dDc);
     count_launches(1);
     if (e != cudaSuccess) return TT_ERR_CUDA;
   }
