@@ -459,6 +459,13 @@ struct FfnBwdArgs {
   float* dDc2;
   ZeroList zero;      // ranges set to 0 on the way (what each layer's merge backward
                       // adds into)
+  // TT_DETERMINISTIC: every token sum goes to this CTA's own slot (rows
+  // blockIdx.x * rows.. of the four dA / dB maps; dD into dDslot[CTA][quadrant]),
+  // stored by the CTA's first tile and added to by its later ones in tile
+  // order; the slots are then summed in CTA order
+  int det;
+  float* dDslot1;
+  float* dDslot2;
 };
 
 struct FfnBwdSmem {
@@ -781,7 +788,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add(map, box, col0, row0 + 32 * q);
+          const int r = (p.det ? (int)blockIdx.x * nrows : 0) + row0 + 32 * q;
+          if (p.det && tl == 0)
+            tma_store(map, box, col0, r);
+          else
+            tma_reduce_add(map, box, col0, r);
           bulk_commit();
         }
       }
@@ -789,12 +800,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // column sums over this warp's 32 rows of z' dz' / Dc: the token sum of z dz'
     auto dd_sum = [&](const float (&z)[32], const float (&v)[32], const float* Dc, float* out,
-                      int rprime) {
+                      float* slot, int rprime) {
       float pr[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) pr[j] = z[j] * v[j];
       const float colsum = warp_transpose_sum(pr, lane);
-      if (32 * h + lane < rprime) atomicAdd(out + 32 * h + lane, colsum / Dc[32 * h + lane]);
+      if (32 * h + lane < rprime) {
+        const float d = colsum / Dc[32 * h + lane];
+        if (p.det) {  // this lane alone owns the entry of its CTA and quadrant
+          float* e = slot + ((size_t)blockIdx.x * 4 + q) * RP + 32 * h + lane;
+          *e = tl == 0 ? d : *e + d;
+        } else {
+          atomicAdd(out + 32 * h + lane, d);
+        }
+      }
     };
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++tl) {
       float z[32], v[32];
@@ -818,7 +837,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(&S.dzp2_empty);
       if (!warp_wait(&S.zl_full, tl & 1, abort_flag, 86)) break;
       ld_tile_half(zt2, row, h, z);
-      dd_sum(z, v, S.Dc2, p.dDc2, r2);
+      dd_sum(z, v, S.Dc2, p.dDc2, p.dDslot2, r2);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= S.Dc2[32 * h + j];
       if (!warp_wait(&S.zp2_free, tl & 1, abort_flag, 87)) break;
@@ -897,7 +916,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.dz1p_empty);
       ld_tile_half(zt1, row, h, z);
-      dd_sum(z, v, S.Dc1, p.dDc1, r1);
+      dd_sum(z, v, S.Dc1, p.dDc1, p.dDslot1, r1);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= S.Dc1[32 * h + j];
       __syncwarp();
@@ -934,6 +953,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (!ok) break;
       if (warp == 2 && lane == 0 && tl == 0) TL_STAMP(1, 12);
+      // the next tile's adds into this CTA's slots come after this tile's
+      if (p.det && lane == 0) bulk_wait_all();
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -1011,10 +1032,17 @@ tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, cons
 tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x,
                           const void* dy, void* dx, void* ws, size_t off1, size_t off2,
                           const void* zs1, const void* zs2, const ZeroList& zero,
-                          cudaStream_t st) {
+                          const DetSlots* det1, const DetSlots* det2, cudaStream_t st) {
   if (!ffn_tc_supported(U, D)) return TT_ERR_UNSUPPORTED;
   if (T <= 0) return zero_list_memset(zero, st) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
+  if ((det1 == nullptr) != (det2 == nullptr)) return TT_ERR_INVALID_ARG;
+  const bool det = det1 != nullptr;
+  if (det && (det1->count < 1 || det2->count != det1->count ||
+              (int64_t)det1->count * (U.M > U.N ? U.M : U.N) > 0x7FFFFFFF ||
+              (int64_t)det1->count * (D.M > D.N ? D.M : D.N) > 0x7FFFFFFF))
+    return TT_ERR_UNSUPPORTED;
+  const int64_t nslot = det ? det1->count : 1;
   if (set_ffn_attrs() != cudaSuccess) return TT_ERR_CUDA;
   const TcLayout t1 = tc_layout(U), t2 = tc_layout(D);
   CUtensorMap mx, mdy, manr1, mbm1, manr2, mbm2, mdx, mdac1, mdbc1, mdac2, mdbc2, mzs1, mzs2;
@@ -1024,10 +1052,14 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
       !make_map(&manr2, at<void>(ws, off2 + t2.Anr), RP, D.N, 64, CH) ||
       !make_map(&mbm2, at<void>(ws, off2 + t2.Bm), D.M, RP, 64, RP) ||
       !make_map(&mdx, dx, U.N, T, 64, 32) ||
-      !make_map(&mdac1, at<void>(ws, off1 + t1.dAc), RP, U.N, 32, 32, kMapF32) ||
-      !make_map(&mdbc1, at<void>(ws, off1 + t1.dBc), RP, U.M, 32, 32, kMapF32) ||
-      !make_map(&mdac2, at<void>(ws, off2 + t2.dAc), RP, D.N, 32, 32, kMapF32) ||
-      !make_map(&mdbc2, at<void>(ws, off2 + t2.dBc), RP, D.M, 32, 32, kMapF32) ||
+      !make_map(&mdac1, det ? det1->a : at<void>(ws, off1 + t1.dAc), RP, U.N * nslot, 32, 32,
+                kMapF32) ||
+      !make_map(&mdbc1, det ? det1->b : at<void>(ws, off1 + t1.dBc), RP, U.M * nslot, 32, 32,
+                kMapF32) ||
+      !make_map(&mdac2, det ? det2->a : at<void>(ws, off2 + t2.dAc), RP, D.N * nslot, 32, 32,
+                kMapF32) ||
+      !make_map(&mdbc2, det ? det2->b : at<void>(ws, off2 + t2.dBc), RP, D.M * nslot, 32, 32,
+                kMapF32) ||
       !make_map(&mzs1, zs1, RP, T, 64, TILE) || !make_map(&mzs2, zs2, RP, T, 64, TILE))
     return TT_ERR_CUDA;
   FfnBwdArgs a;
@@ -1038,7 +1070,9 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
   a.ntiles = (int)((T + TILE - 1) / TILE);
   a.kb1 = kblocks(U.rd);
   a.kb2 = kblocks(D.rd);
-  a.nr = U.rd <= 32 && D.rd <= 32 ? 32 : 64;
+  // (a deterministic pass keeps every W drain on the same warp from tile to
+  // tile: the 64-wide products, whose drains split by column half)
+  a.nr = !det && U.rd <= 32 && D.rd <= 32 ? 32 : 64;
   a.N = (int)U.N;
   a.H = (int)U.M;
   a.M = (int)D.M;
@@ -1049,12 +1083,25 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
   a.dDc1 = at<float>(ws, off1 + t1.dDc);
   a.dDc2 = at<float>(ws, off2 + t2.dDc);
   a.zero = zero;
-  const int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+  a.det = det ? 1 : 0;
+  a.dDslot1 = det ? det1->d : nullptr;
+  a.dDslot2 = det ? det2->d : nullptr;
+  int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+  if (det && grid > det1->count) grid = det1->count;
   cudaError_t e = launch_ex(ffn_bwd_kernel, grid, NTHREADS, kSmemFfnBwd, st, false, mx, mdy,
                             manr1, mbm1, manr2, mbm2, mdx, mdac1, mdbc1, mdac2, mdbc2, mzs1, mzs2,
                             a);
   count_launches(1);
-  return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+  if (e != cudaSuccess) return TT_ERR_CUDA;
+  if (det) {  // each layer's slots of the `grid` CTAs, summed in CTA order
+    e = det_sum_launch(U, *det1, grid, at<float>(ws, off1 + t1.dAc), at<float>(ws, off1 + t1.dBc),
+                       a.dDc1, st);
+    if (e == cudaSuccess)
+      e = det_sum_launch(D, *det2, grid, at<float>(ws, off2 + t2.dAc),
+                         at<float>(ws, off2 + t2.dBc), a.dDc2, st);
+    if (e != cudaSuccess) return TT_ERR_CUDA;
+  }
+  return TT_OK;
 }
 
 }  // namespace ttc

@@ -1594,6 +1594,22 @@ cudaError_t zero_list_memset(const ZeroList& z, cudaStream_t st) {
   return cudaSuccess;
 }
 
+// The fixed-order sums (TT_DETERMINISTIC) of one layer's token-sum slots,
+// filled by the `grid` CTAs of a token pass, into its dAc, dBc and dDc.
+cudaError_t det_sum_launch(const LayerPlan& L, const DetSlots& det, int grid, float* dAc,
+                           float* dBc, float* dDc, cudaStream_t st) {
+  const int64_t nA = L.N * RP, nB = L.M * RP;
+  const int64_t cols = (nA + nB + RP) / 4;
+  const int blocks = (int)((cols + kDetCols - 1) / kDetCols < 8 * num_sms()
+                               ? (cols + kDetCols - 1) / kDetCols
+                               : 8 * num_sms());
+  const cudaError_t e = launch_ex(det_sum_kernel, blocks, 4 * kDetCols, 0, st, false,
+                                  (const float*)det.a, (const float*)det.b, (const float*)det.d,
+                                  grid, nA, nB, L.rd <= 32 ? 32 : RP, dAc, dBc, dDc);
+  count_launches(1);
+  return e;
+}
+
 tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* dy, void* dx,
                       void* ws, size_t off, const ZeroList& zero, bool f8, const void* zs,
                       const DetSlots* det, cudaStream_t st) {
@@ -1647,15 +1663,7 @@ tt_status tc_backward(const LayerPlan& L, int64_t T, const void* x, const void* 
   count_launches(1);
   if (e != cudaSuccess) return TT_ERR_CUDA;
   if (det) {  // the slots of the `grid` CTAs, summed in CTA order
-    const int64_t nA = L.N * RP, nB = L.M * RP;
-    const int64_t cols = (nA + nB + RP) / 4;
-    const int blocks = (int)((cols + kDetCols - 1) / kDetCols < 8 * num_sms()
-                                 ? (cols + kDetCols - 1) / kDetCols
-                                 : 8 * num_sms());
-    e = launch_ex(det_sum_kernel, blocks, 4 * kDetCols, 0, st, false, (const float*)det->a,
-                  (const float*)det->b, (const float*)det->d, grid, nA, nB, L.rd <= 32 ? 32 : RP,
-                  a.dAc, a.dBc, a.dDc);
-    count_launches(1);
+    e = det_sum_launch(L, *det, grid, a.dAc, a.dBc, a.dDc, st);
     if (e != cudaSuccess) return TT_ERR_CUDA;
   }
   return TT_OK;

@@ -109,10 +109,17 @@ tt_status ffn_tc_forward(const LayerPlan& U, const LayerPlan& D, int64_t T, cons
 // tokens from x, dy and the forward's z1', z2' (zs1, zs2); h, GELU(h), da and
 // dh are recomputed per hidden chunk on the SM.  The ranges of `zero`
 // are set to 0 on the way (the merge backward's scratch), also when T == 0.
+// With det1 and det2 (TT_DETERMINISTIC, the up and down layer's slots) the
+// token sums go through per-CTA slots summed in CTA order instead.
 tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, const void* x,
                           const void* dy, void* dx, void* ws, size_t off1, size_t off2,
                           const void* zs1, const void* zs2, const ZeroList& zero,
-                          cudaStream_t st);
+                          const DetSlots* det1, const DetSlots* det2, cudaStream_t st);
+
+// The fixed-order sums of one layer's token-sum slots, filled by the `grid`
+// CTAs of a deterministic token pass, into its dAc, dBc and dDc.
+cudaError_t det_sum_launch(const LayerPlan& L, const DetSlots& det, int grid, float* dAc,
+                           float* dBc, float* dDc, cudaStream_t st);
 
 // ---- several layers on one input (qkv_fused.cuh) ----------------------------
 // True when G (1..3) layers of equal input width all fit the tensor-core kernels.

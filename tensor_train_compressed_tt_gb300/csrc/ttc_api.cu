@@ -143,6 +143,19 @@ size_t layer_layout(const LayerPlan& L, int64_t T, size_t base, WsLayout* w,
   return off;
 }
 
+// The TT_DETERMINISTIC token-sum slots of a layer's workspace region:
+// det_slots x [N][64] for dA, then x [M][64] for dB, then x [4][64] for dD.
+DetSlots det_slots(const LayerPlan& L, void* ws, const WsLayout& w) {
+  DetSlots d;
+  if (w.det_slots) {
+    d.count = w.det_slots;
+    d.a = reinterpret_cast<float*>(static_cast<char*>(ws) + w.det);
+    d.b = d.a + (size_t)w.det_slots * L.N * 64;
+    d.d = d.b + (size_t)w.det_slots * L.M * 64;
+  }
+  return d;
+}
+
 struct FfnLayout {
   WsLayout up, down;
   size_t h = 0, a = 0, da = 0, end = 0;
@@ -155,17 +168,16 @@ bool ffn_tc(const tt_plan_s* p) {
 }
 
 // A bf16 FFN pair whose layers both fit the tensor-core kernels runs fused:
-// h, GELU(h), da and dh never leave the SM.  TTC_FFN_UNFUSED=1 selects the
-// layer-by-layer path instead (a measurement aid).
+// h, GELU(h), da and dh never leave the SM (under TT_DETERMINISTIC too, the
+// token sums then going through per-CTA slots).  TTC_FFN_UNFUSED=1 selects
+// the layer-by-layer path instead (a measurement aid).
 bool ffn_fused(const tt_plan_s* p) {
   static int off = -1;
   if (off < 0) {
     const char* e = getenv("TTC_FFN_UNFUSED");
     off = (e && e[0] && e[0] != '0') ? 1 : 0;
   }
-  // TT_DETERMINISTIC: layer by layer, each with its fixed-order token sums
-  return !off && !(p->L[0].flags & TT_DETERMINISTIC) && ffn_tc(p) &&
-         ffn_tc_supported(p->L[0], p->L[1]);
+  return !off && ffn_tc(p) && ffn_tc_supported(p->L[0], p->L[1]);
 }
 
 // Without the reuse flags the two layers' scratch shares one region; with
@@ -793,13 +805,7 @@ tt_status layer_backward(const LayerPlan& L, int64_t T, const void* x, int tx, c
   if (!bwd_zero_add(&zl, L, ws, w, dparams, acc)) return TT_ERR_UNSUPPORTED;
   if (tc) {
     const void* zs = (L.flags & TT_REUSE_Z) && reuse ? static_cast<char*>(ws) + w.zs : nullptr;
-    DetSlots det;
-    if (w.det_slots) {
-      det.count = w.det_slots;
-      det.a = fptr(ws, w.det);
-      det.b = det.a + (size_t)w.det_slots * L.N * 64;
-      det.d = det.b + (size_t)w.det_slots * L.M * 64;
-    }
+    const DetSlots det = det_slots(L, ws, w);
     s = tc_backward(L, T, x, dy, dx, ws, w.tc, zl, tx == TT_DT_E4M3, zs,
                     w.det_slots ? &det : nullptr, st);
   } else {
@@ -1123,7 +1129,10 @@ tt_status tt_ffn_backward(const tt_plan_t* plan, int64_t T, const void* x, const
     if (!bwd_zero_add(&zl, U, ws, f.up, dparams_up, acc) ||
         !bwd_zero_add(&zl, D, ws, f.down, dparams_down, acc))
       return TT_ERR_UNSUPPORTED;
-    s = ffn_tc_backward(U, D, T, x, dy, dx, ws, f.up.tc, f.down.tc, zs1, zs2, zl, st);
+    const DetSlots det1 = det_slots(U, ws, f.up), det2 = det_slots(D, ws, f.down);
+    const bool det = f.up.det_slots && f.down.det_slots;
+    s = ffn_tc_backward(U, D, T, x, dy, dx, ws, f.up.tc, f.down.tc, zs1, zs2, zl,
+                        det ? &det1 : nullptr, det ? &det2 : nullptr, st);
     prof_end(kPhBwd, st);
     if (s != TT_OK) return s;
     prof_begin(kPhMergeBwd, st);

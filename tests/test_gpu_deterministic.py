@@ -95,21 +95,35 @@ def test_f32_token_path_is_bit_identical():
         assert O.rel_err(a, b) <= 1e-4
 
 
-def test_ffn_pair_is_bit_identical():
+@pytest.mark.parametrize("T", [2000, 20000])
+def test_ffn_pair_is_bit_identical(T):
+    """The fused FFN kernels with per-CTA slots: bit-identical runs, and the
+    oracle's gradients.  20000 tokens are more 128-token tiles than SMs, so
+    some CTAs add a second tile into their slots."""
     from tensor_train_compressed_tt_gb300.layer import TTFFN
+    from parity_util import oracle_ffn
     w = synth.WORKLOADS["ffn768_3072_bf16"]
-    inp = synth.draw(w, seed=3, tokens=2000)
+    inp = synth.draw(w, seed=3, tokens=T)
     up, dn = w.layers
     pu = torch.from_numpy(synth.pack(inp.layers[0].cores, inp.layers[0].diags)).cuda()
     pd = torch.from_numpy(synth.pack(inp.layers[1].cores, inp.layers[1].diags)).cuda()
     x, dy = to_dev(inp.x, w.act), to_dev(inp.dy, w.act)
     f = TTFFN((up.in_modes, up.out_modes, up.ranks), (dn.in_modes, dn.out_modes, dn.ranks),
               TORCH_DT[w.act], reuse_z=True, deterministic=True)
-    ws = f.workspace(2000)
+    ws = f.workspace(T)
     res = []
     for _ in range(3):
-        f.forward(x, pu, pd, ws=ws)
-        res.append(tuple(t.clone() for t in f.backward(x, dy, pu, pd, ws=ws)))
+        y = f.forward(x, pu, pd, ws=ws).clone()
+        res.append((y,) + tuple(t.clone() for t in f.backward(x, dy, pu, pd, ws=ws)))
     torch.cuda.synchronize()
     for r in res[1:]:
         assert all(torch.equal(a, b) for a, b in zip(r, res[0]))
+    y, dx, gu, gd = res[0]
+    ref, ru, rd = oracle_ffn(w, inp)
+    tol = TOL[w.act]
+    assert O.rel_err(y.float().cpu().numpy(), ref["y"]) <= tol
+    assert O.rel_err(dx.float().cpu().numpy(), ref["dx"]) <= tol
+    for sh, g, r in ((up, gu, ru), (dn, gd, rd)):
+        gc, gdg = synth.unpack(sh, g.cpu().numpy())
+        for a, b in list(zip(gc, r[0])) + list(zip(gdg, r[1])):
+            assert O.rel_err(a, b) <= tol
