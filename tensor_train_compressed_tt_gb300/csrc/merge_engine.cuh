@@ -325,13 +325,15 @@ __device__ void eng_gemm_unit(const EngTask& t, int u, int* pos, const float** p
 // rebuilt from shared memory.  P_k rows are written once (by the units with
 // q0 == 0), the final rows go to `out` and, on the tensor-core path, to the
 // compacted bf16 operands.
-constexpr int kChainPB = 32;        // max prefixes per unit
+constexpr int kChainPB = 32;        // prefixes per unit, unless the phase balancing widens it
+constexpr int kChainPBMax = 128;    // the widest unit the balancing makes
 constexpr int kChainSmem = 40960;   // floats of dynamic shared memory per CTA
 constexpr int kVS = 65;             // shared row stride of the chain vectors (odd: no
                                     // bank conflicts between prefixes)
 
 __host__ __device__ inline int64_t chain_stage_floats(const ChainDesc& c) {
-  int64_t f = 2 * kChainPB * kVS + kChainPB * (TT_MAX_D + 1) + kChainPB * TT_MAX_D +
+  const int64_t pb = c.pb;
+  int64_t f = 2 * pb * kVS + pb * (TT_MAX_D + 1) + pb * TT_MAX_D +
               (int64_t)(c.L > 1 ? c.L - 1 : 0) * 64;
   for (int k = 1; k <= c.L - 2; ++k) f += (int64_t)c.r[k] * c.s[k] * c.r[k + 1];
   f += (int64_t)c.r[c.L - 1] * c.sb * c.r[c.L];
@@ -372,10 +374,10 @@ __device__ void eng_chain_unit(const EngTask& t, int u, int* pos, const float** 
   const int nq = (sl - q0 < sb ? sl - q0 : sb);
   // shared-memory layout
   float* va = dsm;                                              // [pb][kVS] chain vectors
-  float* vb = va + kChainPB * kVS;
-  int* dig = reinterpret_cast<int*>(vb + kChainPB * kVS);      // [pb][TT_MAX_D + 1] digits, alpha
-  int* rowk = dig + kChainPB * (TT_MAX_D + 1);                 // [pb][TT_MAX_D] P_k row of the prefix
-  float* dg = reinterpret_cast<float*>(rowk + kChainPB * TT_MAX_D);  // [L-1][64] diagonals
+  float* vb = va + pb * kVS;
+  int* dig = reinterpret_cast<int*>(vb + pb * kVS);            // [pb][TT_MAX_D + 1] digits, alpha
+  int* rowk = dig + pb * (TT_MAX_D + 1);                       // [pb][TT_MAX_D] P_k row of the prefix
+  float* dg = reinterpret_cast<float*>(rowk + pb * TT_MAX_D);  // [L-1][64] diagonals
   float* cs[TT_MAX_D] = {};                  // staged inner cores
   float* cur = dg + (L > 1 ? L - 1 : 0) * 64;
   for (int k = 1; k <= L - 2; ++k) {
@@ -611,7 +613,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
         case kEColdot: eng_coldot_unit(k, uu, red); break;
         case kEScale: eng_scale_unit(k, uu); break;
         case kEPack:
-          tc_pack_unit(k.A, k.B, k.s, k.rd, k.N, k.M, k.tc, k.zero, k.pad_only, uu);
+          tc_pack_unit(k.A, k.B, k.s, k.rd, k.N, k.M, k.tc, k.zero, k.pad_only, k.chunk, uu);
           break;
         case kEDd:
           tc_dd_unit(k.tc, k.s, k.rd, k.out, k.acc);
@@ -619,7 +621,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
         case kEChain: eng_chain_unit(k, uu, pos, &pos_of, eng_dsm, nu); break;
         case kERank: eng_rank_unit(k, uu); break;
         case kEUnpack:
-          tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, uu);
+          tc_unpack_unit(k.tc, k.s, k.rd, k.N, k.M, k.dA, k.dB, k.out, k.acc, k.chunk, uu);
           break;
         default: break;
       }
@@ -741,6 +743,38 @@ void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t part
   eng_gemm_config(t, max_units);
 }
 
+// One step wider for a task whose units are latency-bound: a chain task
+// takes twice the prefixes a unit (while its staging fits the shared memory),
+// a pack or unpack task twice the elements.  False when the task can not
+// widen or its unit count would not drop.
+static bool eng_widen(EngTask* t) {
+  if (t->kind == kEChain) {
+    ChainDesc c = t->ch;
+    if (2 * c.pb > kChainPBMax || c.pb >= c.nprefix) return false;
+    c.pb *= 2;
+    if (chain_stage_floats(c) > kChainSmem) return false;
+    const int units = (int)(ceil_div(c.nprefix, c.pb) * c.nsb);
+    if (units >= t->units) return false;
+    t->ch = c;
+    t->units = units;
+    return true;
+  }
+  if (t->kind == kEPack || t->kind == kEUnpack) {
+    if (2 * t->chunk > kPackPerMax) return false;
+    const int w = t->kind == kEPack ? RP : t->rd;
+    const int64_t n = ((int64_t)t->N + t->M) * w + w;
+    const int units = (int)ceil_div(n, 2 * t->chunk);
+    if (units >= t->units) return false;
+    t->chunk *= 2;
+    t->units = units;
+    return true;
+  }
+  return false;
+}
+
+// The phase's units in as few waves of `budget` CTAs as the task shapes allow:
+// GEMM tasks re-tiled; chain, pack and unpack tasks widened (their units are
+// latency-bound, so fewer waves of somewhat longer units finish sooner).
 void EngBuilder::balance(int budget) {
   const int t0 = p.phase_begin[p.nphases - 1];
   // aim at the fewest waves that the narrowest configuration allows
@@ -748,27 +782,39 @@ void EngBuilder::balance(int budget) {
   for (int i = t0; i < p.ntasks; ++i) {
     EngTask probe = p.t[i];
     if (probe.kind == kEGemm) eng_gemm_config(&probe, 0);
+    while (eng_widen(&probe)) {
+    }
     min_total += probe.units;
   }
   if (budget < 1) budget = 1;
   if (min_total > budget) budget = (int)(ceil_div(min_total, budget) * budget);
-  for (int iter = 0; iter < 64; ++iter) {
+  for (int iter = 0; iter < 256; ++iter) {
     int64_t total = 0;
     for (int i = t0; i < p.ntasks; ++i) total += p.t[i].units;
     if (total <= budget) return;
-    // shrink the GEMM task with the most units that can still shrink
+    // shrink the task with the most units that can still shrink
     int best = -1;
     for (int i = t0; i < p.ntasks; ++i) {
       EngTask& k = p.t[i];
-      if (k.kind != kEGemm || (best >= 0 && k.units <= p.t[best].units)) continue;
+      if (best >= 0 && k.units <= p.t[best].units) continue;
       EngTask probe = k;
-      eng_gemm_config(&probe, 0);  // fewest units
-      if (probe.units < k.units) best = i;
+      bool can = false;
+      if (k.kind == kEGemm) {
+        eng_gemm_config(&probe, 0);  // fewest units
+        can = probe.units < k.units;
+      } else {
+        can = eng_widen(&probe);
+      }
+      if (can) best = i;
     }
     if (best < 0) return;
     EngTask& k = p.t[best];
-    const int64_t want = k.units - (total - budget);
-    eng_gemm_config(&k, (int)(want > 0 ? want : 0));
+    if (k.kind == kEGemm) {
+      const int64_t want = k.units - (total - budget);
+      eng_gemm_config(&k, (int)(want > 0 ? want : 0));
+    } else {
+      eng_widen(&k);
+    }
   }
 }
 
@@ -795,7 +841,8 @@ void eng_pack_task(EngTask* t, const LayerPlan& L, const float* A, const float* 
   t->M = (int)L.M;
   t->tc = tc;
   t->zero = zero_grads ? 1 : 0;
-  t->units = (int)ceil_div((L.N + L.M) * RP + RP, kPackPer);
+  t->chunk = kPackPer;
+  t->units = (int)ceil_div((L.N + L.M) * RP + RP, t->chunk);
 }
 
 void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const float* Dmid,
@@ -810,7 +857,8 @@ void eng_unpack_task(EngTask* t, const LayerPlan& L, const TcPtrs& tc, const flo
   t->dB = dB;
   t->out = dDout;
   t->acc = acc ? 1 : 0;
-  t->units = (int)ceil_div((L.N + L.M) * L.rd + L.rd, kPackPer);
+  t->chunk = kPackPer;
+  t->units = (int)ceil_div((L.N + L.M) * L.rd + L.rd, t->chunk);
 }
 
 void eng_rank_task(EngTask* t, const LayerPlan& L, float* params, float* dparams,

@@ -62,7 +62,7 @@ struct alignas(16) EngTask {
   float* out = nullptr;
   int64_t n = 0, sx = 0, sy = 0;
   int len = 1, acc = 0;
-  int chunk = 1024;     // kEScale: elements per unit
+  int chunk = 1024;     // kEScale, kERank, kEPack, kEUnpack: elements per unit
   // pack / unpack (s = middle diagonal D_d, out = dD_d for unpack)
   const float* A = nullptr;
   const float* B = nullptr;

@@ -1267,7 +1267,8 @@ __global__ void __launch_bounds__(4 * kDetCols) det_sum_kernel(
 // operand packing (compaction of the middle rank) and gradient unpacking,
 // run as units of the merge engine
 // ==========================================================================
-constexpr int kPackPer = 4096;  // elements per engine unit
+constexpr int kPackPer = 4096;      // elements per engine unit, unless the phase balancing widens it
+constexpr int kPackPerMax = 16384;  // the widest unit the balancing makes
 
 // Compaction of the middle rank, computed by the whole block in parallel:
 // pos[a] = position of a among the nonzero entries of D (or -1), kept[c] = a
@@ -1303,15 +1304,15 @@ __device__ void compaction_map(const float* __restrict__ D, int rd, int* pos, in
 // merge GEMMs' epilogues write the compacted columns themselves.
 __device__ void tc_pack_unit(const float* __restrict__ A, const float* __restrict__ B,
                              const float* __restrict__ Dmid, int rd, int N, int M,
-                             const TcPtrs& p, int zero_grads, int pad_only, int unit) {
+                             const TcPtrs& p, int zero_grads, int pad_only, int chunk, int unit) {
   __shared__ int kept[RP];
   __shared__ int rcount;
   compaction_map(Dmid, rd, nullptr, kept, &rcount);
   const int64_t nA = (int64_t)N * RP, nB = (int64_t)M * RP;
   __nv_bfloat16* Anr = static_cast<__nv_bfloat16*>(p.Anr);
   __nv_bfloat16* Bm = static_cast<__nv_bfloat16*>(p.Bm);
-  for (int e = threadIdx.x; e < kPackPer; e += blockDim.x) {
-    const int64_t i = (int64_t)unit * kPackPer + e;
+  for (int e = threadIdx.x; e < chunk; e += blockDim.x) {
+    const int64_t i = (int64_t)unit * chunk + e;
     if (i < nA) {
       const int j = (int)(i / RP), c = (int)(i % RP);
       if (!pad_only || kept[c] < 0) {
@@ -1351,12 +1352,12 @@ __device__ void tc_dd_unit(const TcPtrs& p, const float* Dmid, int rd, float* dD
 }
 
 __device__ void tc_unpack_unit(const TcPtrs& p, const float* Dmid, int rd, int N, int M,
-                               float* dA, float* dB, float* dDout, int acc, int unit) {
+                               float* dA, float* dB, float* dDout, int acc, int chunk, int unit) {
   __shared__ int pos[RP];
   compaction_map(Dmid, rd, pos, nullptr, nullptr);
   const int64_t nA = (int64_t)N * rd, nB = (int64_t)rd * M;
-  for (int e = threadIdx.x; e < kPackPer; e += blockDim.x) {
-    const int64_t i = (int64_t)unit * kPackPer + e;
+  for (int e = threadIdx.x; e < chunk; e += blockDim.x) {
+    const int64_t i = (int64_t)unit * chunk + e;
     if (i < nA) {
       const int j = (int)(i / rd), a = (int)(i % rd);
       dA[i] = pos[a] >= 0 ? __ldcg(p.dAc + (int64_t)j * RP + pos[a]) : 0.f;
