@@ -743,6 +743,24 @@ void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t part
   eng_gemm_config(t, max_units);
 }
 
+// Rough cost of one unit of a task (about nanoseconds: for ordering the units
+// and for the balancing's cap): a GEMM unit pays a staging round trip plus
+// its tile's K extent; a chain unit stages whole cores.
+static double eng_unit_cost(const EngTask& k) {
+  switch (k.kind) {
+    case kEGemm:
+      return 2000.0 + 0.25 * (double)k.kchunk * (k.tm + k.tn) + (k.fold_g ? 500.0 : 0.0) +
+             (k.gather || k.pack_side ? 500.0 : 0.0);
+    case kEChain: return 6000.0;
+    case kEGemmFinal: return 400.0 + 50.0 * k.splits;
+    case kEColdot: return 800.0;
+    case kEPack:
+    case kEUnpack:
+    case kEDd: return 800.0;
+    default: return 400.0;
+  }
+}
+
 // One step wider for a task whose units are latency-bound: a chain task
 // takes twice the prefixes a unit (while its staging fits the shared memory),
 // a pack or unpack task twice the elements.  False when the task can not
@@ -774,9 +792,16 @@ static bool eng_widen(EngTask* t) {
 
 // The phase's units in as few waves of `budget` CTAs as the task shapes allow:
 // GEMM tasks re-tiled; chain, pack and unpack tasks widened (their units are
-// latency-bound, so fewer waves of somewhat longer units finish sooner).
+// latency-bound, so fewer waves of somewhat longer units finish sooner).  A
+// GEMM is not re-tiled into units longer (by the cost model) than the
+// phase's longest unit that nothing can shorten, and at least 8 us: one long
+// unit (a whole K of 1024 on one CTA) would outlast the waves it saves.
 void EngBuilder::balance(int budget) {
   const int t0 = p.phase_begin[p.nphases - 1];
+  double cap = 8000.0;
+  bool frozen[kEngMaxTasks] = {};
+  for (int i = t0; i < p.ntasks; ++i)
+    if (p.t[i].kind != kEGemm && eng_unit_cost(p.t[i]) > cap) cap = eng_unit_cost(p.t[i]);
   // aim at the fewest waves that the narrowest configuration allows
   int64_t min_total = 0;
   for (int i = t0; i < p.ntasks; ++i) {
@@ -796,7 +821,7 @@ void EngBuilder::balance(int budget) {
     int best = -1;
     for (int i = t0; i < p.ntasks; ++i) {
       EngTask& k = p.t[i];
-      if (best >= 0 && k.units <= p.t[best].units) continue;
+      if (frozen[i] || (best >= 0 && k.units <= p.t[best].units)) continue;
       EngTask probe = k;
       bool can = false;
       if (k.kind == kEGemm) {
@@ -810,8 +835,22 @@ void EngBuilder::balance(int budget) {
     if (best < 0) return;
     EngTask& k = p.t[best];
     if (k.kind == kEGemm) {
+      const EngTask before = k;
       const int64_t want = k.units - (total - budget);
       eng_gemm_config(&k, (int)(want > 0 ? want : 0));
+      if (eng_unit_cost(k) > cap && eng_unit_cost(k) > eng_unit_cost(before)) {
+        // the fewest units whose cost stays under the cap, then no further
+        k = before;
+        for (int w = (int)(want > 0 ? want : 0) + 1; w < before.units; ++w) {
+          EngTask probe = before;
+          eng_gemm_config(&probe, w);
+          if (probe.units < before.units && eng_unit_cost(probe) <= cap) {
+            k = probe;
+            break;
+          }
+        }
+        frozen[best] = true;
+      }
     } else {
       eng_widen(&k);
     }
@@ -894,24 +933,6 @@ void eng_gemm_final_task(EngTask* t, const EngTask& gemm) {
   t->splits = gemm.splits;
   t->partial = gemm.partial;
   t->units = (int)ceil_div(gemm.g.m * gemm.g.n, kEngThreads);
-}
-
-// Rough cost of one unit of a task (arbitrary units, for ordering only): a
-// GEMM unit pays a staging round trip plus its tile's K extent; a chain unit
-// stages whole cores.
-static double eng_unit_cost(const EngTask& k) {
-  switch (k.kind) {
-    case kEGemm:
-      return 2000.0 + 0.25 * (double)k.kchunk * (k.tm + k.tn) + (k.fold_g ? 500.0 : 0.0) +
-             (k.gather || k.pack_side ? 500.0 : 0.0);
-    case kEChain: return 6000.0;
-    case kEGemmFinal: return 400.0 + 50.0 * k.splits;
-    case kEColdot: return 800.0;
-    case kEPack:
-    case kEUnpack:
-    case kEDd: return 800.0;
-    default: return 400.0;
-  }
 }
 
 static void eng_dump(const EngProgram& p) {
