@@ -289,7 +289,8 @@ typedef struct tt_ttm_desc {
   int row_modes[4];    /* m_1..m_d (the vocabulary V = prod m_k, <= 2^24) */
   int col_modes[4];    /* n_1..n_d (the embedding width Dm = prod n_k) */
   int ranks[5];        /* r_0..r_d, r_0 = r_d = 1 */
-  unsigned flags;      /* TT_ACCUMULATE (backward adds into dparams) */
+  unsigned flags;      /* TT_ACCUMULATE (backward adds into dparams),
+                          TT_REUSE_MERGE (see tt_ttm_lookup_backward) */
 } tt_ttm_desc;
 tt_status tt_ttm_plan(const tt_ttm_desc* desc, tt_plan_t** out);
 
@@ -307,6 +308,11 @@ tt_status tt_ttm_lookup(const tt_plan_t* plan, int64_t B, const int32_t* idx,
  * dD_k into dparams (overwritten, or added to under TT_ACCUMULATE); repeated
  * indices add up.  dD_k[a] is 0 where D_k[a] == 0 (as for the TT layers).
  * Recomputes the forward's unique rows; needs no state from a lookup call.
+ * Under TT_REUSE_MERGE it also takes the batch's distinct rows and prefixes
+ * from the workspace instead of finding them again: the caller guarantees
+ * that a tt_ttm_lookup with the same plan, the same idx and B and the same
+ * workspace came before, with nothing but such backward calls using the
+ * workspace in between.
  * Gradient sums are reduced with atomics (summation order not fixed). */
 tt_status tt_ttm_lookup_backward(const tt_plan_t* plan, int64_t B, const int32_t* idx,
                                  const float* dout, const float* params, float* dparams,

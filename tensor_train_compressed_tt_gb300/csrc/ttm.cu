@@ -244,11 +244,19 @@ __global__ void __launch_bounds__(kScanThreads) ttm_tile_write_kernel(TtmArgs a,
   }
 }
 
+// Occurrence lists: occ[off[v] ..] = the positions b with idx[b] == v.  A
+// position beyond the row's count (counts of another batch, kept in the
+// workspace by a lookup whose indices differ: a broken TT_REUSE_MERGE
+// promise) is not written, and the status word records the error.
 __global__ void ttm_fill_kernel(TtmArgs a, const int32_t* __restrict__ idx) {
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.B; b += gridDim.x * blockDim.x) {
     const int v = idx[b];
     if (v < 0 || v >= a.V) continue;
-    a.occ[a.off[v] + atomicAdd(a.cursor + v, 1)] = b;
+    const int k = atomicAdd(a.cursor + v, 1);
+    if (k < a.cnt[v])
+      a.occ[a.off[v] + k] = b;
+    else
+      ttm_error(3);
   }
 }
 
@@ -907,17 +915,28 @@ cudaError_t set_attrs() {
   } while (0)
 
 // count and scan (and, for the backward, the occurrence lists)
+// The batch's bookkeeping: occurrence counts, distinct rows and prefixes,
+// their slots and the backward units; with `backward` also the occurrence
+// lists.  `reuse`: the counts, slots and units are the lookup's of the same
+// batch, still in the workspace, and only the occurrence lists are built
+// (from zeroed fill cursors).
 tt_status ttm_prepare(int64_t B, const int32_t* idx, const TtmArgs& a, const TtmWs& w, void* ws,
-                      bool backward, cudaStream_t st) {
-  TTM_CUDA(cudaMemsetAsync(at<char>(ws, w.cnt), 0, w.zero_bytes, st));
+                      bool backward, bool reuse, cudaStream_t st) {
   int gb = (int)std::min<int64_t>((B + 255) / 256, 4 * sm_count());
-  int* tsum = at<int>(ws, w.tsum);
-  ttm_count_kernel<<<gb, 256, 0, st>>>(a, idx);
-  ttm_tile_sum_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
-  ttm_tile_scan_kernel<<<1, 1024, 0, st>>>(a, w.ntr, w.ntp, tsum);
-  ttm_tile_write_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
-  if (backward) ttm_fill_kernel<<<gb, 256, 0, st>>>(a, idx);
-  count_launches(backward ? 5 : 4);
+  if (!reuse) {
+    TTM_CUDA(cudaMemsetAsync(at<char>(ws, w.cnt), 0, w.zero_bytes, st));
+    int* tsum = at<int>(ws, w.tsum);
+    ttm_count_kernel<<<gb, 256, 0, st>>>(a, idx);
+    ttm_tile_sum_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
+    ttm_tile_scan_kernel<<<1, 1024, 0, st>>>(a, w.ntr, w.ntp, tsum);
+    ttm_tile_write_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
+    count_launches(4);
+  }
+  if (backward) {
+    if (reuse) TTM_CUDA(cudaMemsetAsync(a.cursor, 0, (size_t)a.V * sizeof(int), st));
+    ttm_fill_kernel<<<gb, 256, 0, st>>>(a, idx);
+    count_launches(1);
+  }
   TTM_CUDA(cudaGetLastError());
   return TT_OK;
 }
@@ -943,7 +962,7 @@ tt_status tt_ttm_plan(const tt_ttm_desc* desc, tt_plan_t** out) {
   if (!out) return TT_ERR_INVALID_ARG;
   *out = nullptr;
   if (!desc || (desc->d != 2 && desc->d != 3)) return TT_ERR_INVALID_ARG;
-  if (desc->flags & ~TT_ACCUMULATE) return TT_ERR_INVALID_ARG;
+  if (desc->flags & ~(TT_ACCUMULATE | TT_REUSE_MERGE)) return TT_ERR_INVALID_ARG;
   const int d = desc->d;
   TtmPlan P;
   P.d = d;
@@ -1001,7 +1020,7 @@ tt_status tt_ttm_lookup(const tt_plan_t* plan, int64_t B, const int32_t* idx, co
   if (set_attrs() != cudaSuccess || !unit_ptrs(&un)) return TT_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const TtmArgs a = make_args(P, B, params, ws, w, un);
-  tt_status s = ttm_prepare(B, idx, a, w, ws, false, st);
+  tt_status s = ttm_prepare(B, idx, a, w, ws, false, false, st);
   if (s != TT_OK) return s;
   ttm_pair_rows_kernel<<<(unsigned)w.pcap, 256, pair_rows_smem(P), st>>>(a);
   ttm_scatter_kernel<<<(unsigned)std::min<int64_t>((B + 7) / 8, 32 * sm_count()), 256, 0, st>>>(
@@ -1026,7 +1045,7 @@ tt_status tt_ttm_lookup_backward(const tt_plan_t* plan, int64_t B, const int32_t
   Units un;
   if (set_attrs() != cudaSuccess || !unit_ptrs(&un)) return TT_ERR_CUDA;
   const TtmArgs a = make_args(P, B, params, ws, w, un);
-  tt_status s = ttm_prepare(B, idx, a, w, ws, true, st);
+  tt_status s = ttm_prepare(B, idx, a, w, ws, true, (P.flags & TT_REUSE_MERGE) != 0, st);
   if (s != TT_OK) return s;
   float* dF1 = dparams + P.core_off[0];
   float* dF2 = dparams + P.core_off[1];

@@ -212,8 +212,10 @@ class TTMEmbedding:
     backward into the packed cores/diagonals (float32)."""
 
     def __init__(self, row_modes: Sequence[int], col_modes: Sequence[int],
-                 ranks: Sequence[int], accumulate: bool = False):
-        flags = ttc.TT_ACCUMULATE if accumulate else 0
+                 ranks: Sequence[int], accumulate: bool = False, reuse: bool = False):
+        # reuse: backward() takes the batch's distinct rows from the lookup()
+        # of the same indices on the same workspace (TT_REUSE_MERGE)
+        flags = (ttc.TT_ACCUMULATE if accumulate else 0) | (ttc.TT_REUSE_MERGE if reuse else 0)
         self.desc = ttc.make_ttm_desc(row_modes, col_modes, ranks, flags)
         self.plan = ttc.tt_ttm_plan(self.desc)
         self.core_off, self.diag_off, self.n_params = ttc.tt_param_layout(self.plan)

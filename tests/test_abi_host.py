@@ -320,6 +320,13 @@ def test_ttm_plan_and_argument_errors(lib):
     with pytest.raises(ttc.TTError) as e:   # rank above 64: no kernel
         ttc.tt_ttm_plan(ttc.make_ttm_desc((32, 32), (8, 8), (1, 65, 1)))
     assert e.value.code == 2
+    # TT_ACCUMULATE and TT_REUSE_MERGE are a TTM plan's flags; TT_REUSE_Z is not
+    flags = ttc.TT_ACCUMULATE | ttc.TT_REUSE_MERGE
+    ttc.tt_ttm_plan(ttc.make_ttm_desc((32, 32, 32), (8, 8, 12), (1, 30, 30, 1), flags))
+    with pytest.raises(ttc.TTError) as e:
+        ttc.tt_ttm_plan(ttc.make_ttm_desc((32, 32, 32), (8, 8, 12), (1, 30, 30, 1),
+                                          ttc.TT_REUSE_Z))
+    assert e.value.code == 1
     fake = 1 << 40
     ws = ttc.tt_workspace_size(plan, 64)
     assert ttc.tt_ttm_lookup(plan, 0, 0, 0, 0, 0, 0) == 0                    # B == 0

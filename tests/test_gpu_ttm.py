@@ -28,9 +28,10 @@ def _built():
     _build.build()
 
 
-def _run(shape, cores, diags, idx, dout, accumulate=False, base=None):
+def _run(shape, cores, diags, idx, dout, accumulate=False, base=None, reuse=False):
     from tensor_train_compressed_tt_gb300.layer import TTMEmbedding
-    emb = TTMEmbedding(shape.row_modes, shape.col_modes, shape.ranks, accumulate=accumulate)
+    emb = TTMEmbedding(shape.row_modes, shape.col_modes, shape.ranks, accumulate=accumulate,
+                       reuse=reuse)
     p = torch.from_numpy(synth.pack(cores, diags)).cuda()
     i = torch.from_numpy(np.asarray(idx, np.int32)).cuda()
     g = torch.from_numpy(np.asarray(dout, np.float32)).cuda()
@@ -45,8 +46,8 @@ def _run(shape, cores, diags, idx, dout, accumulate=False, base=None):
     return out.cpu().numpy(), dp.cpu().numpy(), stats_f, stats_b
 
 
-def _check(shape, cores, diags, idx, dout, label):
-    out, dp, sf, sb = _run(shape, cores, diags, idx, dout)
+def _check(shape, cores, diags, idx, dout, label, reuse=False):
+    out, dp, sf, sb = _run(shape, cores, diags, idx, dout, reuse=reuse)
     c64 = [c.astype(np.float64) for c in cores]
     d64 = [e.astype(np.float64) for e in diags]
     ref = O.ttm_lookup(c64, d64, idx)
@@ -95,11 +96,35 @@ def test_small_tables(m, n, r):
         _check(shape, cores, diags, idx, dout, f"{m}x{n} r{r} B={B}")
 
 
-@pytest.mark.parametrize("name", ["ttm_emb_10k", "ttm_emb_40k"])
-def test_workloads(name):
+@pytest.mark.parametrize("name,reuse", [("ttm_emb_10k", False), ("ttm_emb_40k", False),
+                                        ("ttm_emb_40k", True)])
+def test_workloads(name, reuse):
+    """reuse: the backward takes the lookup's distinct rows and prefixes from
+    the workspace (TT_REUSE_MERGE), as the benchmark's step runs it."""
     w = synth.TTM_WORKLOADS[name]
     t = synth.draw_ttm(w)
-    _check(w.shape, t.cores, t.diags, t.idx, t.dout, name)
+    _check(w.shape, t.cores, t.diags, t.idx, t.dout, name, reuse=reuse)
+
+
+def test_reused_bookkeeping_twice_in_a_row():
+    """Two backward calls after one lookup under TT_REUSE_MERGE give the same
+    gradients as a backward that finds the distinct rows itself."""
+    from tensor_train_compressed_tt_gb300.layer import TTMEmbedding
+    w = synth.TTM_WORKLOADS["ttm_emb_10k"]
+    t = synth.draw_ttm(w, seed=9, batch=3000)
+    S = w.shape
+    p = torch.from_numpy(synth.pack(t.cores, t.diags)).cuda()
+    i = torch.from_numpy(t.idx).cuda()
+    g = torch.from_numpy(t.dout).cuda()
+    plain = TTMEmbedding(S.row_modes, S.col_modes, S.ranks)
+    ref = plain.backward(i, g, p, ws=plain.workspace(3000))
+    emb = TTMEmbedding(S.row_modes, S.col_modes, S.ranks, reuse=True)
+    ws = emb.workspace(3000)
+    emb.lookup(i, p, ws=ws)
+    for _ in range(2):
+        dp = emb.backward(i, g, p, ws=ws)
+        torch.cuda.synchronize()
+        assert O.rel_err(dp.cpu().numpy(), ref.cpu().numpy()) <= 1e-5
 
 
 def test_accumulate_adds_into_dparams():
