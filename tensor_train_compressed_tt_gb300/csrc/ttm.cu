@@ -595,7 +595,14 @@ __global__ void __launch_bounds__(256) ttm_chunk_sum_kernel(TtmArgs a,
   const int v = a.ulist[u];
   const int o0 = a.off[v] + k * kChunk;
   const int n = min(kChunk, a.off[v] + a.cnt[v] - o0);
-  if ((int)threadIdx.x < n) ob[threadIdx.x] = a.occ[o0 + threadIdx.x];
+  if ((int)threadIdx.x < n) {
+    int b = a.occ[o0 + threadIdx.x];
+    if ((unsigned)b >= (unsigned)a.B) {  // a list left unfilled (a broken reuse promise)
+      ttm_error(4);
+      b = 0;
+    }
+    ob[threadIdx.x] = b;
+  }
   __syncthreads();
   if ((a.Dm & 3) == 0) {
     const int q = a.Dm >> 2;
