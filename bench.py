@@ -399,6 +399,30 @@ def run_reference(args, w):
 # our arm
 
 
+def gelu_rates(nsm, dev, stream):
+    """Evaluations a second of the fused FFN kernels' GELU (index 0) and
+    GELU + GELU' (index 1) arithmetic, from tt_gelu_rate timed with CUDA
+    events: a microbenchmark of the elementwise term on every SM."""
+    import torch
+    from tensor_train_compressed_tt_gb300 import ttc
+    blocks, iters = 8 * nsm, 2000
+    out = torch.empty(blocks * 256, device=dev)
+    sh = int(stream.cuda_stream)
+    rates = []
+    for mode in (0, 1):
+        ttc.check(ttc.lib().tt_gelu_rate(mode, iters, blocks, out.data_ptr(), sh), "tt_gelu_rate")
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            ttc.check(ttc.lib().tt_gelu_rate(mode, iters, blocks, out.data_ptr(), sh),
+                      "tt_gelu_rate")
+        b.record(stream)
+        b.synchronize()
+        rates.append(3 * blocks * 256 * 16 * iters / (a.elapsed_time(b) * 1e-3))
+    return rates
+
+
 def traffic_for(phase_name, workload):
     """DRAM bytes per launch from the committed ncu summary, if still current."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -760,6 +784,17 @@ def run_ours(args, w):
                     "algorithmic_evals_per_launch": evals, "duration_us": per_launch_s * 1e6,
                     "hbm_frac": bytes_of[dom] / per_launch_s / 1e9 / peak,
                     "timing": phase_note}
+            # the GELU term measured: the kernels' own packed GELU (forward)
+            # and GELU + GELU' (backward) arithmetic, in registers on every SM
+            rates = gelu_rates(props.multi_processor_count, dev, stream)
+            gm = {"unit": "G evaluations/s", "note": "tt_gelu_rate: 8 blocks of 256 threads an "
+                  "SM, 16 values a thread, 2000 rounds, CUDA events; floor = T x 3072 / rate"}
+            for nm, mode in (("forward_tokens", 0), ("backward_tokens", 1)):
+                floor_s = evals / rates[mode]
+                gm[nm] = {"rate": rates[mode] / 1e9, "floor_us": floor_s * 1e6}
+                if nm in phases:
+                    gm[nm]["frac"] = floor_s / (phases[nm]["us_per_interval"] * 1e-6)
+            roof["gelu_measured"] = gm
         else:
             ach = bytes_of[dom] / per_launch_s / 1e9
             roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak,

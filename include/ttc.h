@@ -372,6 +372,13 @@ tt_status tt_profile_phase(int phase, double* total_ms, int64_t* intervals);
 const char* tt_profile_phase_name(int phase);
 /* Total kernels this library has launched in this process (monotonic). */
 uint64_t tt_launch_count(void);
+/* Throughput probe of the fused FFN kernels' GELU arithmetic: `blocks`
+ * blocks of 256 threads each carry 16 values through `iters` rounds of the
+ * same packed tanh-form GELU (mode 0) or GELU and GELU' (mode 1), in
+ * registers, and write one float each to out (device, blocks * 256 floats).
+ * Evaluations = blocks * 256 * 16 * iters; time it with CUDA events on
+ * `stream`. */
+tt_status tt_gelu_rate(int mode, int iters, int blocks, float* out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -60,6 +60,39 @@ __device__ __forceinline__ void gelu_tanh_grad2(float2 u, float2 da, float2& a, 
   g = __fmul2_rn(da, d);
 }
 
+// Throughput probe of the fused FFN kernels' GELU arithmetic (a measurement
+// hook): every thread carries eight pairs of values through `iters` rounds of
+// GELU (mode 0, the forward's) or GELU and GELU' (mode 1, the backward's),
+// each result feeding the next round, entirely in registers, and writes one
+// sum so that nothing is dropped.  16 evaluations a thread a round.
+__global__ void __launch_bounds__(256) gelu_rate_kernel(int mode, int iters, float* out) {
+  float2 v[8], w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float base = (float)((threadIdx.x * 8 + j) % 61) * 0.1f - 3.f;  // in [-3, 3]
+    v[j] = make_float2(base, base + 0.05f);
+    w[j] = make_float2(1.f, 0.5f);
+  }
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (mode == 0) {
+        const float2 a = gelu_tanh2(v[j]);
+        v[j] = __ffma2_rn(a, f2(0.9f), f2(-0.2f));  // stays in about [-3, 3]
+      } else {
+        float2 a, g;
+        gelu_tanh_grad2(v[j], w[j], a, g);
+        v[j] = __ffma2_rn(a, f2(0.9f), f2(-0.2f));
+        w[j] = __ffma2_rn(g, f2(0.5f), f2(0.5f));
+      }
+    }
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) sum += v[j].x + v[j].y + w[j].x + w[j].y;
+  out[blockIdx.x * blockDim.x + threadIdx.x] = sum;
+}
+
 // Per-warp stamps of CTA 0 (timeline builds only): [kernel][warp][slot]
 #ifdef TTC_TIMELINE
 __device__ unsigned long long g_tlw[2][16][48];
@@ -1105,6 +1138,13 @@ tt_status ffn_tc_backward(const LayerPlan& U, const LayerPlan& D, int64_t T, con
 }
 
 }  // namespace ttc
+
+extern "C" tt_status tt_gelu_rate(int mode, int iters, int blocks, float* out, void* stream) {
+  if ((mode != 0 && mode != 1) || iters < 1 || blocks < 1 || !out) return TT_ERR_INVALID_ARG;
+  ttc::gelu_rate_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(mode, iters, out);
+  ttc::count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? TT_OK : TT_ERR_CUDA;
+}
 
 #ifdef TTC_TIMELINE
 extern "C" int ttc_timeline_warps_read(void* host, size_t bytes) {

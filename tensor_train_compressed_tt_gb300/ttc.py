@@ -130,6 +130,8 @@ def lib() -> ctypes.CDLL:
         L.tt_profile_phase_name.restype = ctypes.c_char_p
         L.tt_launch_count.argtypes = []
         L.tt_launch_count.restype = ctypes.c_uint64
+        L.tt_gelu_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P]
+        L.tt_gelu_rate.restype = ctypes.c_int
         _lib = L
     return _lib
 
