@@ -326,6 +326,11 @@ struct QkvBwdArgs {
   const int* rinfo[kMaxGroups];
   float* dDc[kMaxGroups];
   ZeroList zero;             // ranges set to 0 on the way (what the merges add into)
+  // TT_DETERMINISTIC: every token sum goes to this CTA's own slot (rows
+  // blockIdx.x * rows.. of each dA / dB map; dD into dDslot[g][CTA][quadrant]),
+  // stored by the CTA's first tile and added to by its later ones in tile order
+  int det;
+  float* dDslot[kMaxGroups];
 };
 
 // TMEM columns of the backward
@@ -592,7 +597,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_reduce_add(map, box, 32 * h, row0 + 32 * q);
+          const int r = (p.det ? (int)blockIdx.x * nrows : 0) + row0 + 32 * q;
+          if (p.det && tl == 0)
+            tma_store(map, box, 32 * h, r);
+          else
+            tma_reduce_add(map, box, 32 * h, r);
           bulk_commit();
         }
       }
@@ -623,8 +632,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) pr[j] = z[j] * v[j];
           const float colsum = warp_transpose_sum(pr, lane);
-          if (32 * h + lane < rp[g])
-            atomicAdd(p.dDc[g] + 32 * h + lane, colsum / S.Dc[g][32 * h + lane]);
+          if (32 * h + lane < rp[g]) {
+            const float d = colsum / S.Dc[g][32 * h + lane];
+            if (p.det) {  // this lane alone owns the entry of its CTA and quadrant
+              float* e = p.dDslot[g] + ((size_t)blockIdx.x * 4 + q) * RP + 32 * h + lane;
+              *e = tl == 0 ? d : *e + d;
+            } else {
+              atomicAdd(p.dDc[g] + 32 * h + lane, d);
+            }
+          }
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= S.Dc[g][32 * h + j];
@@ -667,6 +683,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok) break;
       }
       if (!ok) break;
+      // the next tile's adds into this CTA's slots come after this tile's
+      if (p.det && lane == 0) bulk_wait_all();
     }
     if (lane == 0) bulk_wait_all();
   }
@@ -752,10 +770,17 @@ tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x,
 
 tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x,
                             const void* const* dy, void* dx, void* ws, const size_t* offs,
-                            const void* const* zs, const ZeroList& zero, cudaStream_t st) {
+                            const void* const* zs, const ZeroList& zero, const DetSlots* det,
+                            cudaStream_t st) {
   if (!multi_tc_supported(Ls, G)) return TT_ERR_UNSUPPORTED;
   if (T <= 0) return zero_list_memset(zero, st) == cudaSuccess ? TT_OK : TT_ERR_CUDA;
   if (T > (int64_t)0x7FFFFFFF - TILE) return TT_ERR_UNSUPPORTED;
+  if (det)
+    for (int g = 0; g < G; ++g)
+      if (det[g].count < 1 || det[g].count != det[0].count ||
+          (int64_t)det[g].count * (Ls[g].N > Ls[g].M ? Ls[g].N : Ls[g].M) > 0x7FFFFFFF)
+        return TT_ERR_UNSUPPORTED;
+  const int64_t nslot = det ? det[0].count : 1;
   if (set_qkv_attrs() != cudaSuccess) return TT_ERR_CUDA;
   CUtensorMap mx, mdx, mdx16, mdy[kMaxGroups], manr[kMaxGroups], mbm[kMaxGroups], mdac[kMaxGroups],
       mdbc[kMaxGroups], mzs[kMaxGroups];
@@ -764,7 +789,8 @@ tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x
   a.G = G;
   a.N = (int)Ls[0].N;
   a.nN = (int)((Ls[0].N + CH - 1) / CH);
-  a.tt = tokens_per_tile(T);
+  // a fixed summation order wants a fixed token blocking: 128-token tiles
+  a.tt = det ? TILE : tokens_per_tile(T);
   a.ntiles = (int)((T + a.tt - 1) / a.tt);
   if (!make_map(&mx, x, Ls[0].N, T, 64, a.tt) || !make_map(&mdx, dx, Ls[0].N, T, 64, 32) ||
       !make_map(&mdx16, dx, Ls[0].N, T, 64, 16))
@@ -776,8 +802,10 @@ tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x
     if (!make_map(&mdy[g], dy[gg], L.M, T, 64, a.tt) ||
         !make_map(&manr[g], at<void>(ws, offs[gg] + t.Anr), RP, L.N, 64, CH) ||
         !make_map(&mbm[g], at<void>(ws, offs[gg] + t.Bm), L.M, RP, 64, RP) ||
-        !make_map(&mdac[g], at<void>(ws, offs[gg] + t.dAc), RP, L.N, 32, 32, kMapF32) ||
-        !make_map(&mdbc[g], at<void>(ws, offs[gg] + t.dBc), RP, L.M, 32, 32, kMapF32) ||
+        !make_map(&mdac[g], det ? det[gg].a : at<void>(ws, offs[gg] + t.dAc), RP, L.N * nslot,
+                  32, 32, kMapF32) ||
+        !make_map(&mdbc[g], det ? det[gg].b : at<void>(ws, offs[gg] + t.dBc), RP, L.M * nslot,
+                  32, 32, kMapF32) ||
         !make_map(&mzs[g], zs[gg], RP, T, 64, a.tt))
       return TT_ERR_CUDA;
     a.nM[g] = (int)((L.M + CH - 1) / CH);
@@ -786,14 +814,24 @@ tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x
     a.Dc[g] = at<float>(ws, offs[gg] + t.Dc);
     a.rinfo[g] = at<int>(ws, offs[gg] + t.rinfo);
     a.dDc[g] = at<float>(ws, offs[gg] + t.dDc);
+    a.dDslot[g] = det ? det[gg].d : nullptr;
   }
   a.zero = zero;
-  const int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+  a.det = det ? 1 : 0;
+  int grid = a.ntiles < num_sms() ? a.ntiles : num_sms();
+  if (det && grid > det[0].count) grid = det[0].count;
   cudaError_t e = launch_ex(qkv_bwd_kernel, grid, NTHREADS, kSmemQkvBwd, st, false, mx, mdy[0],
                             mdy[1], mdy[2], manr[0], manr[1], manr[2], mbm[0], mbm[1], mbm[2],
                             mdx, mdx16, mdac[0], mdac[1], mdac[2], mdbc[0], mdbc[1], mdbc[2], mzs[0],
                             mzs[1], mzs[2], a);
   count_launches(1);
+  if (e != cudaSuccess) return TT_ERR_CUDA;
+  if (det)  // each layer's slots of the `grid` CTAs, summed in CTA order
+    for (int g = 0; g < G && e == cudaSuccess; ++g) {
+      const TcLayout t = tc_layout(Ls[g]);
+      e = det_sum_launch(Ls[g], det[g], grid, at<float>(ws, offs[g] + t.dAc),
+                         at<float>(ws, offs[g] + t.dBc), a.dDc[g], st);
+    }
   return e == cudaSuccess ? TT_OK : TT_ERR_CUDA;
 }
 

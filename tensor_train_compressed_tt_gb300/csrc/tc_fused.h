@@ -134,9 +134,12 @@ tt_status multi_tc_forward(const LayerPlan* Ls, int G, int64_t T, const void* x,
 
 // dx = sum_g dy[g] W_g and every layer's token sums (dAc, dBc, dDc, zeroed
 // beforehand) from x, dy[g] and the forward's z'_g; x streamed once.
-// The ranges of `zero` are set to 0 on the way, also when T == 0.
+// The ranges of `zero` are set to 0 on the way, also when T == 0.  With det
+// (TT_DETERMINISTIC, one DetSlots a layer) the token sums go through per-CTA
+// slots summed in CTA order instead.
 tt_status multi_tc_backward(const LayerPlan* Ls, int G, int64_t T, const void* x,
                             const void* const* dy, void* dx, void* ws, const size_t* offs,
-                            const void* const* zs, const ZeroList& zero, cudaStream_t st);
+                            const void* const* zs, const ZeroList& zero, const DetSlots* det,
+                            cudaStream_t st);
 
 }  // namespace ttc

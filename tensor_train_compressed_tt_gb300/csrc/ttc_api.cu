@@ -829,10 +829,9 @@ struct MultiLayout {
 };
 
 // The layers run on the multi-layer kernels when all of them fit the bf16
-// tensor-core path and no fixed summation order is asked for.
+// tensor-core path (under TT_DETERMINISTIC too: per-CTA token-sum slots).
 bool multi_fused(const tt_plan_s* p) {
-  return p->L[0].act == TT_DT_BF16 && !(p->L[0].flags & TT_DETERMINISTIC) &&
-         multi_tc_supported(p->L, p->G);
+  return p->L[0].act == TT_DT_BF16 && multi_tc_supported(p->L, p->G);
 }
 
 // One region a layer (its merges, packed operands and, fused, its z'),
@@ -1328,7 +1327,13 @@ tt_status tt_multi_backward(const tt_plan_t* plan, int64_t T, const void* x,
     if (s != TT_OK) return s;
   }
   prof_begin(kPhBwd, st);
-  s = multi_tc_backward(plan->L, G, T, x, dy, dx, ws, offs, zs, zl, st);
+  DetSlots det[TT_MULTI_MAX];
+  bool use_det = true;
+  for (int g = 0; g < G; ++g) {
+    det[g] = det_slots(plan->L[g], ws, m.w[g]);
+    use_det &= m.w[g].det_slots > 0;
+  }
+  s = multi_tc_backward(plan->L, G, T, x, dy, dx, ws, offs, zs, zl, use_det ? det : nullptr, st);
   prof_end(kPhBwd, st);
   if (s != TT_OK) return s;
   prof_begin(kPhMergeBwd, st);

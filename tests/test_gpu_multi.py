@@ -100,14 +100,21 @@ def test_fused_forward_equals_single_layer_kernel():
         assert torch.equal(y1, ys[g]), g
 
 
-def test_layer_by_layer_paths():
-    """f32 activations and TT_DETERMINISTIC run the layers one after another
-    and sum dx in layer order; the deterministic one is bit-reproducible."""
+def test_layer_by_layer_path():
+    """f32 activations run the layers one after another and sum dx in layer
+    order."""
     tiny = synth.WORKLOADS["tiny64_f32"].layers[0]
     shapes = [tiny] * 3
     _, lis, x, dys, _, ys, dx, dps = _run(shapes, 16, seed=64, act="f32")
     _check(shapes, lis, x, dys, ys, dx, dps, TOL["f32"])
-    m, lis, x, dys, (xd, dyd, params, ws), ys, dx, dps = _run(QKV, 1000, seed=65,
+
+
+@pytest.mark.parametrize("T", [1000, 20000])
+def test_deterministic_fused(T):
+    """TT_DETERMINISTIC on the fused Q/K/V kernels: per-CTA token-sum slots
+    summed in CTA order, bit-reproducible, and the oracle's gradients.  20000
+    tokens are more 128-token tiles than SMs (a second tile on some CTAs)."""
+    m, lis, x, dys, (xd, dyd, params, ws), ys, dx, dps = _run(QKV, T, seed=65,
                                                               deterministic=True)
     _check(QKV, lis, x, dys, ys, dx, dps, TOL["bf16"])
     dx2, dps2 = m.backward(xd, dyd, params, ws=ws)
