@@ -5,6 +5,8 @@ activations, 2e-2 for bf16 or E4M3 activations with f32 accumulation; tensors wh
 reference is exactly zero (pruned slices, removed layers) must be exactly 0.
 """
 
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -360,6 +362,34 @@ def test_ffn_reuse_matches_recompute():
     assert th.equal(y0, y1) and th.equal(dx0, dx1)
     assert O.rel_err(gu1.cpu().numpy(), gu0.cpu().numpy()) <= 1e-3
     assert O.rel_err(gd1.cpu().numpy(), gd0.cpu().numpy()) <= 1e-3
+
+
+@pytest.mark.parametrize("T,reuse_z", [(1, True), (127, False), (129, True)])
+def test_ffn_pair_edge_token_counts(T, reuse_z):
+    """The fused FFN kernels on one token, on one token short of a 128-token
+    tile and one past it: y, dx and every gradient of both layers."""
+    w = synth.WORKLOADS["ffn768_3072_bf16"]
+    inp = synth.draw(w, seed=21 + T, tokens=T)
+    out, gu, gd = gpu_ffn(w, inp, reuse_z=reuse_z)
+    ref, ru, rd = oracle_ffn(w, inp)
+    tol = TOL[w.act]
+    assert O.rel_err(out["y"], ref["y"]) <= tol
+    assert O.rel_err(out["dx"], ref["dx"]) <= tol
+    for (a, b) in (list(zip(gu[0], ru[0])) + list(zip(gd[0], rd[0])) + list(zip(gu[1], ru[1])) +
+                   list(zip(gd[1], rd[1]))):
+        assert O.rel_err(a, b) <= tol
+
+
+@pytest.mark.parametrize("reuse_z", [False, True])
+def test_ffn_pair_zero_tokens(reuse_z):
+    """T = 0 through the FFN plan: y is empty and every gradient exactly 0."""
+    w = synth.WORKLOADS["ffn768_3072_bf16"]
+    inp = synth.draw(w, seed=0, tokens=1)
+    inp0 = dataclasses.replace(inp, x=inp.x[:0], dy=inp.dy[:0])
+    out, gu, gd = gpu_ffn(w, inp0, reuse_z=reuse_z)
+    assert out["y"].shape == (0, w.layers[1].M)
+    for g in list(gu[0]) + list(gu[1]) + list(gd[0]) + list(gd[1]):
+        assert np.all(g == 0)
 
 
 @pytest.mark.parametrize("act,rmid", [("f32", 12), ("bf16", 12), ("bf16", 40)])
