@@ -815,11 +815,14 @@ def run_ours(args, w):
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        # Every step copies its inputs in from pinned host memory and its
-        # results (y, dx, dparams) out, as an input pipeline would: the copies
-        # run on their own streams into two alternating device buffer sets, so
-        # step i+1's host->device copy and step i-1's device->host copy
-        # overlap step i's kernels.
+        # Every step copies its inputs (x, dy) in from pinned host memory and
+        # reads its result back: the parameter gradients (dparams), which is
+        # what a training step hands on; y and dx feed the neighbouring layers
+        # on the device.  The copies run on their own streams into two
+        # alternating device buffer sets, so step i+1's host->device copy and
+        # step i-1's device->host copy overlap step i's kernels.  The same
+        # pipeline that also reads y and dx back to the host is measured too
+        # (with_activations_out).
         x0, dy0, y0, dx0 = sets[0]
         hx = torch.empty(x0.shape, dtype=dt, pin_memory=True)
         hdy = torch.empty(dy0.shape, dtype=dt, pin_memory=True)
@@ -837,7 +840,7 @@ def run_ours(args, w):
         ev_out = [torch.cuda.Event() for _ in range(2)]
         Ke = max(3, min(K, 200))
 
-        def e2e_step(i):
+        def e2e_step(i, acts_out):
             j = i % 2
             x, dy, y, dx, dps = bufs[j]
             s_in.wait_event(ev_done[j])          # the step that last read set j is done
@@ -851,31 +854,43 @@ def run_ours(args, w):
             ev_done[j].record(stream)
             s_out.wait_event(ev_done[j])
             with torch.cuda.stream(s_out):
-                hy.copy_(y, non_blocking=True)
-                hdx.copy_(dx, non_blocking=True)
+                if acts_out:
+                    hy.copy_(y, non_blocking=True)
+                    hdx.copy_(dx, non_blocking=True)
                 for hp, dp in zip(hdp, dps):
                     hp.copy_(dp, non_blocking=True)
             ev_out[j].record(s_out)
 
-        for i in range(3):
-            e2e_step(i)
-        torch.cuda.synchronize(dev)
-        barrier()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        s_in.wait_event(a0)
-        for i in range(Ke):
-            e2e_step(i)
-        stream.wait_event(ev_out[(Ke - 1) % 2])  # the last step's results are on the host
-        a1.record(stream)
-        barrier()
-        ems = all_reduce_scalar(a0.elapsed_time(a1) / Ke, "max", dev)
+        def e2e_ms(acts_out):
+            for i in range(3):
+                e2e_step(i, acts_out)
+            torch.cuda.synchronize(dev)
+            barrier()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            s_in.wait_event(a0)
+            for i in range(Ke):
+                e2e_step(i, acts_out)
+            stream.wait_event(ev_out[(Ke - 1) % 2])  # the last step's results are on the host
+            a1.record(stream)
+            barrier()
+            return all_reduce_scalar(a0.elapsed_time(a1) / Ke, "max", dev)
+
+        h2d = int(hx.numel() * ei + hdy.numel() * ei)
+        d2h_p = int(4 * sum(n_par))
+        d2h_a = int(hy.numel() * eo + hdx.numel() * eo)
+        ems = e2e_ms(False)
+        ems_a = e2e_ms(True)
         e2e = {"value": whole_job_rate(T, world, ems), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(hx.numel() * ei + hdy.numel() * ei),
-               "d2h_bytes_per_step": int(hy.numel() * eo + hdx.numel() * eo + 4 * sum(n_par)),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h_p,
                "ms_per_step": ems, "steps": Ke,
-               "pipeline": "copies on their own streams, two device buffer sets"}
+               "pipeline": "x, dy in and dparams out every step, on copy streams of their "
+                           "own, two device buffer sets",
+               "with_activations_out": {"value": whole_job_rate(T, world, ems_a),
+                                        "d2h_bytes_per_step": d2h_p + d2h_a,
+                                        "ms_per_step": ems_a,
+                                        "note": "the same pipeline also reading y and dx back"}}
 
     # ---- oracle on the host cores (rank 0, N = 1 only)
     cpu = None
@@ -1093,30 +1108,41 @@ def run_ttm(args, w):
 
     e2e = None
     if not args.no_e2e:
+        # every step: the indices and dout in from pinned host memory, the
+        # step's result (dparams) out; the looked-up rows feed the model on
+        # the device (the same loop also reading them back: with_rows_out)
         hi = torch.from_numpy(inp0.idx).pin_memory()
         hd = torch.from_numpy(inp0.dout).pin_memory()
         ho = torch.empty((B, S.Dm)).pin_memory()
         hp = torch.empty(emb.n_params).pin_memory()
         di, dd, do = sets[0]
         Ke = 50
-        barrier()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(Ke):
-            di.copy_(hi, non_blocking=True)
-            dd.copy_(hd, non_blocking=True)
-            fwd(0)
-            bwd(0)
-            ho.copy_(do, non_blocking=True)
-            hp.copy_(dparams, non_blocking=True)
-        b.record(stream)
-        barrier()
-        ms_e = all_reduce_scalar(a.elapsed_time(b) / Ke, "max", dev)
+
+        def e2e_ms(rows_out):
+            barrier()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(Ke):
+                di.copy_(hi, non_blocking=True)
+                dd.copy_(hd, non_blocking=True)
+                fwd(0)
+                bwd(0)
+                if rows_out:
+                    ho.copy_(do, non_blocking=True)
+                hp.copy_(dparams, non_blocking=True)
+            b.record(stream)
+            barrier()
+            return all_reduce_scalar(a.elapsed_time(b) / Ke, "max", dev)
+
+        ms_e = e2e_ms(False)
+        ms_r = e2e_ms(True)
         e2e = {"value": whole_job_rate(B, world, ms_e), "unit": "tokens/s",
                "h2d_bytes_per_step": hi.numel() * 4 + hd.numel() * 4,
-               "d2h_bytes_per_step": ho.numel() * 4 + hp.numel() * 4, "ms_per_step": ms_e,
-               "steps": Ke}
+               "d2h_bytes_per_step": hp.numel() * 4, "ms_per_step": ms_e, "steps": Ke,
+               "with_rows_out": {"value": whole_job_rate(B, world, ms_r),
+                                 "d2h_bytes_per_step": ho.numel() * 4 + hp.numel() * 4,
+                                 "ms_per_step": ms_r}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
