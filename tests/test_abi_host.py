@@ -141,13 +141,18 @@ def test_multi_plan_layout_and_validation(lib):
         w1 = ttc.tt_workspace_size(one, T)
         w3 = ttc.tt_workspace_size(fused, T)
         assert 3 * (w1 + T * 128) <= w3 + 3 * 512 and w3 <= 3 * (w1 + T * 128) + 3 * 512
-    for act, flags in ((ttc.TT_DT_F32, 0), (ttc.TT_DT_BF16, ttc.TT_DETERMINISTIC)):
+    # the layer-by-layer backward (f32) keeps the dx of layers 2 and 3 before
+    # the sum; the fused bf16 kernels, deterministic or not, sum dx on the SM
+    def extra(act, flags, T):
         single = ttc.tt_plan(_desc(q, act=act, flags=flags))
         multi = ttc.tt_multi_plan([_desc(q, act=act, flags=flags)] * 3)
-        esz = 4 if act == ttc.TT_DT_F32 else 2
-        for T in (7, 1000):
-            extra = ttc.tt_workspace_size(multi, T) - 3 * ttc.tt_workspace_size(single, T)
-            assert 2 * T * q.N * esz - 3 * 512 <= extra <= 2 * T * q.N * esz + 3 * 512
+        return ttc.tt_workspace_size(multi, T) - 3 * ttc.tt_workspace_size(single, T)
+
+    for T in (7, 1000):
+        e = extra(ttc.TT_DT_F32, 0, T)
+        assert 2 * T * q.N * 4 - 3 * 512 <= e <= 2 * T * q.N * 4 + 3 * 512
+        assert extra(ttc.TT_DT_BF16, ttc.TT_DETERMINISTIC, T) == extra(ttc.TT_DT_BF16, 0, T)
+    assert extra(ttc.TT_DT_BF16, ttc.TT_DETERMINISTIC, 1000) < 2 * 1000 * q.N * 2
 
 
 def test_multi_argument_errors_return_before_any_launch(lib):
