@@ -1343,6 +1343,40 @@ def run_encoder(args):
         flop += 6 * T * sh.ranks[sh.d] * (sh.N + sh.M)
     t_roof = byts / (peak * 1e9)
     value = whole_job_rate(T, world, ms)
+    # end to end: every step copies the block's eight inputs (x, xo, xf and the
+    # five upstream gradients) in from pinned host memory and reads every
+    # layer's dparams back, in stream order with the kernels
+    e2e = None
+    if not args.no_e2e:
+        x0, xo0, xf0, dy0 = sets[0]
+        dev_in = [x0, xo0, xf0] + [dy0[k] for k in sorted(dy0)]
+        host_in = [t.cpu().pin_memory() for t in dev_in]
+        dps = [b[k] for k in sorted(b) if k.startswith("dp_")]
+        host_dp = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dps]
+        Ke = 8
+
+        def e2e_run():
+            for hi, di in zip(host_in, dev_in):
+                di.copy_(hi, non_blocking=True)
+            blk.step(x0, xo0, xf0, dy0, params, b)
+            for hd, dd in zip(host_dp, dps):
+                hd.copy_(dd, non_blocking=True)
+
+        e2e_run()
+        barrier()
+        ea = torch.cuda.Event(enable_timing=True)
+        eb = torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        for _ in range(Ke):
+            e2e_run()
+        eb.record(stream)
+        barrier()
+        ems = all_reduce_scalar(ea.elapsed_time(eb) / Ke, "max", dev)
+        e2e = {"value": whole_job_rate(T, world, ems), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_dp),
+               "ms_per_step": ems, "steps": Ke,
+               "pipeline": "inputs in and dparams out every step, in stream order"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         small = synth.draw_encoder(256, seed=0)
@@ -1379,7 +1413,7 @@ def run_encoder(args):
             "roofline_step": {"t_roof_us": t_roof * 1e6, "frac": t_roof / (ms * 1e-3),
                               "algorithmic_bytes": byts, "algorithmic_flop": flop,
                               "peak_gbs": peak, "peak_kind": peak_kind},
-            "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches, "clocks": clk,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
