@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 #include <new>
 
@@ -38,6 +39,16 @@ __device__ float g_ttm_sink[64];                        // their gradients (disc
 __device__ void ttm_error(unsigned where) {
   if (atomicCAS(&g_ttm_status.code, 0u, (unsigned)TT_ERR_DEVICE) == 0u)
     atomicExch(&g_ttm_status.detail, where);
+}
+
+// The bookkeeping kernels (count, tile sums, scan, tile write, fill) are
+// launched with programmatic dependent launch: each waits for the grid
+// before it in the stream (whose writes it may read) first thing, then lets
+// the next grid start its own launch.  The per-prefix kernels and the row
+// kernels are ordinary launches (measured slower with it).
+__device__ __forceinline__ void ttm_pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 struct TtmArgs {
@@ -66,6 +77,7 @@ struct TtmArgs {
 };
 
 __global__ void ttm_count_kernel(TtmArgs a, const int32_t* __restrict__ idx) {
+  ttm_pdl_enter();
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.B; b += gridDim.x * blockDim.x) {
     const int v = idx[b];
     if (v < 0 || v >= a.V) {
@@ -151,6 +163,7 @@ __device__ void tile_sums(const TtmArgs& a, bool rows, int base, int n, int* c, 
 // Blocks [0, ntr) cover row tiles, [ntr, ntr + ntp) prefix tiles: each
 // writes its tile totals (tsum[3 * tile + 0..2]).
 __global__ void __launch_bounds__(kScanThreads) ttm_tile_sum_kernel(TtmArgs a, int ntr, int* tsum) {
+  ttm_pdl_enter();
   __shared__ int w1[32], w2[32], w3[32];
   const bool rows = (int)blockIdx.x < ntr;
   const int tile = rows ? blockIdx.x : blockIdx.x - ntr;
@@ -170,6 +183,7 @@ __global__ void __launch_bounds__(kScanThreads) ttm_tile_sum_kernel(TtmArgs a, i
 // One block: exclusive prefix of the tile totals (rows and prefixes apart);
 // the grand totals go to counts[0..2].
 __global__ void __launch_bounds__(1024) ttm_tile_scan_kernel(TtmArgs a, int ntr, int ntp, int* tsum) {
+  ttm_pdl_enter();
   __shared__ int w1[32], w2[32], w3[32];
   for (int part = 0; part < 2; ++part) {
     const int t0 = part == 0 ? 0 : ntr, nt = part == 0 ? ntr : ntp;
@@ -210,6 +224,7 @@ __global__ void __launch_bounds__(1024) ttm_tile_scan_kernel(TtmArgs a, int ntr,
 // -> prefix slots and the prefix list.
 __global__ void __launch_bounds__(kScanThreads) ttm_tile_write_kernel(TtmArgs a, int ntr,
                                                                      const int* tsum) {
+  ttm_pdl_enter();
   __shared__ int w1[32], w2[32], w3[32];
   const bool rows = (int)blockIdx.x < ntr;
   const int tile = rows ? blockIdx.x : blockIdx.x - ntr;
@@ -249,6 +264,7 @@ __global__ void __launch_bounds__(kScanThreads) ttm_tile_write_kernel(TtmArgs a,
 // workspace by a lookup whose indices differ: a broken TT_REUSE_MERGE
 // promise) is not written, and the status word records the error.
 __global__ void ttm_fill_kernel(TtmArgs a, const int32_t* __restrict__ idx) {
+  ttm_pdl_enter();
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < a.B; b += gridDim.x * blockDim.x) {
     const int v = idx[b];
     if (v < 0 || v >= a.V) continue;
@@ -916,6 +932,32 @@ cudaError_t set_attrs() {
   });
 }
 
+bool ttm_pdl_on() {
+  static int on = -1;
+  if (on < 0) {
+    const char* e = getenv("TTC_NO_PDL");
+    on = (e && e[0] && e[0] != '0') ? 0 : 1;
+  }
+  return on == 1;
+}
+
+// Launch with the programmatic-serialization attribute (TTC_NO_PDL=1: without).
+template <typename... KArgs, typename... Args>
+cudaError_t ttm_launch(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = ttm_pdl_on() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 #define TTM_CUDA(call)                                 \
   do {                                                 \
     if ((call) != cudaSuccess) return TT_ERR_CUDA;     \
@@ -933,15 +975,15 @@ tt_status ttm_prepare(int64_t B, const int32_t* idx, const TtmArgs& a, const Ttm
   if (!reuse) {
     TTM_CUDA(cudaMemsetAsync(at<char>(ws, w.cnt), 0, w.zero_bytes, st));
     int* tsum = at<int>(ws, w.tsum);
-    ttm_count_kernel<<<gb, 256, 0, st>>>(a, idx);
-    ttm_tile_sum_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
-    ttm_tile_scan_kernel<<<1, 1024, 0, st>>>(a, w.ntr, w.ntp, tsum);
-    ttm_tile_write_kernel<<<w.ntr + w.ntp, kScanThreads, 0, st>>>(a, w.ntr, tsum);
+    TTM_CUDA(ttm_launch(ttm_count_kernel, gb, 256, 0, st, a, idx));
+    TTM_CUDA(ttm_launch(ttm_tile_sum_kernel, w.ntr + w.ntp, kScanThreads, 0, st, a, w.ntr, tsum));
+    TTM_CUDA(ttm_launch(ttm_tile_scan_kernel, 1, 1024, 0, st, a, w.ntr, w.ntp, tsum));
+    TTM_CUDA(ttm_launch(ttm_tile_write_kernel, w.ntr + w.ntp, kScanThreads, 0, st, a, w.ntr, tsum));
     count_launches(4);
   }
   if (backward) {
     if (reuse) TTM_CUDA(cudaMemsetAsync(a.cursor, 0, (size_t)a.V * sizeof(int), st));
-    ttm_fill_kernel<<<gb, 256, 0, st>>>(a, idx);
+    TTM_CUDA(ttm_launch(ttm_fill_kernel, gb, 256, 0, st, a, idx));
     count_launches(1);
   }
   TTM_CUDA(cudaGetLastError());
