@@ -289,7 +289,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-constexpr int kRowBatch = 5;  // used rows of a prefix handled together (3 blocks an SM fit)
+constexpr int kRowBatch = 5;  // used rows of a prefix handled together (4 blocks an SM fit)
 
 // Shared-memory row pitches chosen against bank conflicts: an odd pitch for
 // the F_2 slice rows (read across rows by the H product, scalar loads); for
@@ -535,7 +535,7 @@ __device__ void stage_f3(const TtmArgs& a, const int* i3s, int kb, float* f3b, i
 //   row_k[(jA, j3)] = sum_e P[jA, e] F_3[e, i3_k, j3]  ->  rows[upos[v_k]],
 // with M = n1 n2, N = (rows of the batch) n3, K = r2 padded with zeros to a
 // multiple of 4.
-__global__ void __launch_bounds__(256, 3) ttm_pair_rows_kernel(TtmArgs a) {
+__global__ void __launch_bounds__(256, 4) ttm_pair_rows_kernel(TtmArgs a) {
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   __shared__ int list[256];
@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(256) ttm_chunk_sum_kernel(TtmArgs a,
 //   H[j1, b] = sum_{j2, e} G[(j1, j2), e] F_2[b, i2, j2, e]
 //   dF_1[0, i1, j1, b] += D_1[b] H[j1, b];  dD_1[b] += sum_j1 F_1[i1, j1, b] H[j1, b]
 // (dD entries of pruned ranks, D == 0, stay untouched).
-__global__ void __launch_bounds__(256, 3) ttm_pair_backward_kernel(TtmArgs a, float* __restrict__ dF1,
+__global__ void __launch_bounds__(256, 4) ttm_pair_backward_kernel(TtmArgs a, float* __restrict__ dF1,
                                                                 float* __restrict__ dF2,
                                                                 float* __restrict__ dF3,
                                                                 float* __restrict__ dD1,
