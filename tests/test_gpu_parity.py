@@ -43,10 +43,12 @@ def test_tiny64_f32():
     _run("tiny64_f32")
 
 
-# Token counts cover every tile height the host picks (16 .. 128 tokens a
-# tile, so that tiles spread over all SMs): 16 (T <= 2432), 48 (6000),
-# 80 (10000), 112 (16384), 128 (18000) on 152 SMs, each with a ragged last tile.
-@pytest.mark.parametrize("T", [1, 7, 128, 300, 6000, 10000, 16384, 18000])
+# Token counts cover the tile heights the host picks for one wave (16 .. 128
+# tokens a tile) on 152 SMs: 16 (T <= 2432), 48 (6000), 80 (10000), 96
+# (14000), and full 128-token tiles from three quarters of the SMs up (16384:
+# 128 tiles, 18000: 141), each with a ragged last tile; two waves (112) run
+# in the 1024 -> 4096 test at 32768 tokens.
+@pytest.mark.parametrize("T", [1, 7, 128, 300, 6000, 10000, 14000, 16384, 18000])
 def test_tt768_bf16(T):
     _run("tt768_bf16", tokens=T)
 
