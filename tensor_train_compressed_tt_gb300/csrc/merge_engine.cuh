@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <cstdlib>
 
+#include <vector>
+
 #include "merge_engine.h"
 
 namespace ttc {
@@ -689,6 +691,19 @@ static void eng_divisor(int d, unsigned long long* mul, int* sh) {
   *sh = 31 + l;
 }
 
+// Sets a GEMM task's tile (tm x tn) and split count, and what follows.
+static void eng_gemm_set(EngTask* t, int tm, int tn, int splits) {
+  const GemmArgs& g = t->g;
+  t->tm = tm;
+  t->tn = tn;
+  t->splits = splits;
+  t->units = (int)(ceil_div(g.m, tm) * ceil_div(g.n, tn) * splits);
+  t->tiles_n = (int)ceil_div(g.n, tn);
+  t->kchunk = (int)ceil_div(g.k, splits);
+  eng_divisor(t->splits, &t->div_s_mul, &t->div_s_sh);
+  eng_divisor(t->tiles_n, &t->div_n_mul, &t->div_n_sh);
+}
+
 // Tile (16 or 32 a side) and split choice: the configuration with the most
 // units not above max_units (ties: larger tiles, then fewer splits); if none
 // fits, the one with the fewest units.  A split keeps >= 48 of K.
@@ -721,14 +736,38 @@ static void eng_gemm_config(EngTask* t, int max_units) {
     }
   }
   const int* c = fit_u >= 0 ? fit : mn;
-  t->tm = c[0];
-  t->tn = c[1];
-  t->splits = c[2];
-  t->units = (int)(ceil_div(g.m, c[0]) * ceil_div(g.n, c[1]) * c[2]);
-  t->tiles_n = (int)ceil_div(g.n, c[1]);
-  t->kchunk = (int)ceil_div(g.k, c[2]);
-  eng_divisor(t->splits, &t->div_s_mul, &t->div_s_sh);
-  eng_divisor(t->tiles_n, &t->div_n_mul, &t->div_n_sh);
+  eng_gemm_set(t, c[0], c[1], c[2]);
+}
+
+// Every configuration eng_gemm_config may choose for t (at most
+// kEngMaxConfigs): tile, splits, units and unit cost.
+struct EngCfg {
+  int tm, tn, splits, units;
+  double cost;
+};
+constexpr int kEngMaxConfigs = 4 * kMaxSplits;
+static double eng_unit_cost(const EngTask& k);
+static int eng_gemm_configs(const EngTask& t, EngCfg* out) {
+  const GemmArgs& g = t.g;
+  const bool atomic = t.atomic_splits && g.mode == kAtomic;
+  const bool can_split = atomic || t.partial != nullptr;
+  int64_t maxs = can_split ? ceil_div(g.k, 48) : 1;
+  if (maxs > kMaxSplits) maxs = kMaxSplits;
+  if (maxs < 1) maxs = 1;
+  int n = 0;
+  EngTask tmp = t;
+  for (int tm : {32, 16}) {
+    if (tm == 32 && g.m <= 16) continue;
+    for (int tn : {32, 16}) {
+      if (tn == 32 && g.n <= 16) continue;
+      for (int64_t sp = 1; sp <= maxs && n < kEngMaxConfigs; ++sp) {
+        if (sp > 1 && !atomic && sp * g.m * g.n > t.pcap) break;
+        eng_gemm_set(&tmp, tm, tn, (int)sp);
+        out[n++] = {tm, tn, (int)sp, tmp.units, eng_unit_cost(tmp)};
+      }
+    }
+  }
+  return n;
 }
 
 void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t partial_cap,
@@ -812,11 +851,12 @@ void EngBuilder::balance(int budget) {
     min_total += probe.units;
   }
   if (budget < 1) budget = 1;
+  const bool one_wave = min_total <= budget;
   if (min_total > budget) budget = (int)(ceil_div(min_total, budget) * budget);
   for (int iter = 0; iter < 256; ++iter) {
     int64_t total = 0;
     for (int i = t0; i < p.ntasks; ++i) total += p.t[i].units;
-    if (total <= budget) return;
+    if (total <= budget) break;
     // shrink the task with the most units that can still shrink
     int best = -1;
     for (int i = t0; i < p.ntasks; ++i) {
@@ -832,7 +872,7 @@ void EngBuilder::balance(int budget) {
       }
       if (can) best = i;
     }
-    if (best < 0) return;
+    if (best < 0) break;
     EngTask& k = p.t[best];
     if (k.kind == kEGemm) {
       const EngTask before = k;
@@ -854,6 +894,74 @@ void EngBuilder::balance(int budget) {
     } else {
       eng_widen(&k);
     }
+  }
+  if (one_wave) refine(budget);
+}
+
+// In a phase of one unit a CTA the phase lasts as long as its costliest
+// unit: while that unit is a GEMM's, give that task a finer configuration
+// (more units, each cheaper) if the phase still fits `budget` units, making
+// room where needed by coarsening other GEMM tasks as far as their units stay
+// below the new maximum.  Stops when no step lowers the maximum.
+void EngBuilder::refine(int budget) {
+  const int t0 = p.phase_begin[p.nphases - 1];
+  std::vector<EngCfg> cfgs((size_t)(p.ntasks - t0) * kEngMaxConfigs);
+  std::vector<int> ncfg((size_t)(p.ntasks - t0));
+  for (int iter = 0; iter < 16; ++iter) {
+    int64_t total = 0;
+    int hi = -1;
+    for (int i = t0; i < p.ntasks; ++i) {
+      total += p.t[i].units;
+      if (hi < 0 || eng_unit_cost(p.t[i]) > eng_unit_cost(p.t[hi])) hi = i;
+    }
+    if (hi < 0 || p.t[hi].kind != kEGemm || total > budget) return;
+    const double cmax = eng_unit_cost(p.t[hi]);
+    double others = 0.0;  // the costliest unit of every other task
+    for (int i = t0; i < p.ntasks; ++i)
+      if (i != hi && eng_unit_cost(p.t[i]) > others) others = eng_unit_cost(p.t[i]);
+    for (int i = t0; i < p.ntasks; ++i)
+      ncfg[i - t0] = p.t[i].kind == kEGemm
+                         ? eng_gemm_configs(p.t[i], &cfgs[(size_t)(i - t0) * kEngMaxConfigs])
+                         : 0;
+    const EngCfg* cfg = &cfgs[(size_t)(hi - t0) * kEngMaxConfigs];
+    double best_max = cmax;
+    int best_c = -1;
+    int best_sub[kEngMaxTasks];  // per other task its new configuration (-1: unchanged)
+    for (int c = 0; c < ncfg[hi - t0]; ++c) {
+      if (cfg[c].units <= p.t[hi].units) continue;
+      const double newmax = cfg[c].cost > others ? cfg[c].cost : others;
+      if (newmax >= best_max) continue;
+      // units to free elsewhere: the GEMM tasks coarsened to their fewest
+      // units whose cost stays at or below newmax
+      int64_t need = total - p.t[hi].units + cfg[c].units - budget;
+      int sub[kEngMaxTasks];
+      for (int i = t0; i < p.ntasks; ++i) sub[i] = -1;
+      for (int i = t0; i < p.ntasks && need > 0; ++i) {
+        if (i == hi) continue;
+        const EngCfg* alt = &cfgs[(size_t)(i - t0) * kEngMaxConfigs];
+        int pick = -1;
+        for (int a2 = 0; a2 < ncfg[i - t0]; ++a2)
+          if (alt[a2].units < p.t[i].units && alt[a2].cost <= newmax &&
+              (pick < 0 || alt[a2].units < alt[pick].units))
+            pick = a2;
+        if (pick >= 0) {
+          need -= p.t[i].units - alt[pick].units;
+          sub[i] = pick;
+        }
+      }
+      if (need > 0) continue;
+      best_max = newmax;
+      best_c = c;
+      for (int i = t0; i < p.ntasks; ++i) best_sub[i] = sub[i];
+    }
+    if (best_c < 0) return;
+    const EngCfg h = cfg[best_c];
+    for (int i = t0; i < p.ntasks; ++i)
+      if (best_sub[i] >= 0) {
+        const EngCfg& a2 = cfgs[(size_t)(i - t0) * kEngMaxConfigs + best_sub[i]];
+        eng_gemm_set(&p.t[i], a2.tm, a2.tn, a2.splits);
+      }
+    eng_gemm_set(&p.t[hi], h.tm, h.tn, h.splits);
   }
 }
 

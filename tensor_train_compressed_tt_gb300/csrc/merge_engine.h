@@ -116,6 +116,8 @@ struct EngBuilder {
   // until its units fit the fewest waves of `budget` CTAs that its
   // narrowest configuration allows (one wave where possible).
   void balance(int budget);
+  // After balance, for a phase of one wave: lowers its costliest unit.
+  void refine(int budget);
 };
 
 // Units for a GEMM task of the engine's tile size and a split-K count.
