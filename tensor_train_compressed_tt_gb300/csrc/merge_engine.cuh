@@ -590,8 +590,7 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
 #endif
   for (int ph = 0; ph < p.nphases; ++ph) {
     const int t0 = p.phase_begin[ph], t1 = p.phase_begin[ph + 1];
-    int total = 0;
-    for (int t = t0; t < t1; ++t) total += p.t[t].units;
+    const int total = p.ptotal[ph];
     // Units are dealt in waves of gridDim.x, costliest tasks first, and every
     // other wave in reverse CTA order, so that the CTAs with the cheapest
     // unit of one wave take the costliest of the next.
@@ -599,8 +598,9 @@ __global__ void __launch_bounds__(kEngThreads) eng_kernel(const __grid_constant_
       const int u = w * (int)gridDim.x +
                     ((w & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
       if (u >= total) continue;
-      int o = t0, uu = u;
-      while (uu >= p.t[p.order[o]].units) uu -= p.t[p.order[o++]].units;
+      int o = t0;
+      while (o + 1 < t1 && u >= p.ustart[o + 1]) ++o;
+      const int uu = u - p.ustart[o];
       const int t = p.order[o];
       const EngTask& k = p.t[t];
 #ifdef TTC_TIMELINE
@@ -1084,6 +1084,12 @@ cudaError_t eng_launch(const EngProgram& prog, cudaStream_t st) {
       for (; j > a && eng_unit_cost(p.t[p.order[j - 1]]) < cv; --j) p.order[j] = p.order[j - 1];
       p.order[j] = v;
     }
+    int acc = 0;
+    for (int i = a; i < b; ++i) {
+      p.ustart[i] = acc;
+      acc += p.t[p.order[i]].units;
+    }
+    p.ptotal[ph] = acc;
   }
   static int dumps = 0;
   if (getenv("TTC_ENG_DUMP") && dumps < 4) {

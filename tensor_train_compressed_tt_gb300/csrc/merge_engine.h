@@ -102,6 +102,12 @@ struct alignas(16) EngProgram {
   // units of a phase are dealt in this task order (set by eng_launch: the
   // tasks with the costliest units first)
   unsigned char order[kEngMaxTasks] = {};
+  // set by eng_launch: the units of a phase dealt before order position i
+  // (ustart), and every phase's units (ptotal), so that a CTA finds its
+  // unit's task in a few reads of adjacent words instead of a walk through
+  // the task records
+  int ustart[kEngMaxTasks] = {};
+  int ptotal[kEngMaxPhases] = {};
   EngTask t[kEngMaxTasks];
 };
 
