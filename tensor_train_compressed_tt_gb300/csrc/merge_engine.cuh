@@ -792,7 +792,7 @@ static double eng_unit_cost(const EngTask& k) {
              (k.gather || k.pack_side ? 500.0 : 0.0);
     case kEChain: return 6000.0;
     case kEGemmFinal: return 400.0 + 50.0 * k.splits;
-    case kEColdot: return 800.0;
+    case kEColdot: return 800.0 + 0.5 * (double)k.n;  // one column over n strided rows
     case kEPack:
     case kEUnpack:
     case kEDd: return 800.0;
