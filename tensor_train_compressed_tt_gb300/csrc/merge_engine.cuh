@@ -788,8 +788,12 @@ void eng_gemm_task(EngTask* t, const GemmArgs& g, float* partial_ws, size_t part
 static double eng_unit_cost(const EngTask& k) {
   switch (k.kind) {
     case kEGemm:
+      // a gathered operand (token sums through the compaction map) stages
+      // element by element from rows 64 floats apart: about twice the cost
+      // a float of a contiguous one
       return 2000.0 + 0.25 * (double)k.kchunk * (k.tm + k.tn) + (k.fold_g ? 500.0 : 0.0) +
-             (k.gather || k.pack_side ? 500.0 : 0.0);
+             (k.gather || k.pack_side ? 500.0 : 0.0) +
+             (k.gather ? 0.5 * (double)k.kchunk * (k.gather_op == 0 ? k.tm : k.tn) : 0.0);
     case kEChain: return 6000.0;
     case kEGemmFinal: return 400.0 + 50.0 * k.splits;
     case kEColdot: return 800.0 + 0.5 * (double)k.n;  // one column over n strided rows
