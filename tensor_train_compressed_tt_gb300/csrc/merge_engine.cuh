@@ -900,6 +900,71 @@ void EngBuilder::balance(int budget) {
     }
   }
   if (one_wave) refine(budget);
+  else refine_waves();
+}
+
+// The phase's length as eng_kernel deals it: tasks costliest unit first,
+// waves of `grid` units, every other wave in reverse CTA order; the largest
+// sum of unit costs a CTA gets.
+static double eng_phase_makespan(const EngProgram& p, int t0, int t1, int grid) {
+  int order[kEngMaxTasks];
+  int n = 0;
+  for (int i = t0; i < t1; ++i) {
+    const double c = eng_unit_cost(p.t[i]);
+    int j = n;
+    for (; j > 0 && eng_unit_cost(p.t[order[j - 1]]) < c; --j) order[j] = order[j - 1];
+    order[j] = i;
+    ++n;
+  }
+  std::vector<double> load((size_t)grid, 0.0);
+  int64_t u = 0;
+  for (int o = 0; o < n; ++o) {
+    const EngTask& k = p.t[order[o]];
+    const double c = eng_unit_cost(k);
+    for (int i = 0; i < k.units; ++i, ++u) {
+      const int64_t w = u / grid, r = u - w * grid;
+      load[(size_t)((w & 1) ? grid - 1 - r : r)] += c;
+    }
+  }
+  double m = 0.0;
+  for (double v : load) m = v > m ? v : m;
+  return m;
+}
+
+// A phase of several waves: GEMM tasks take the configuration (tile and K
+// splits) that shortens the dealt phase the most, one task at a time, while
+// any step shortens it.  Host work only: the candidate configurations of a
+// task are those within a factor four of its units.
+void EngBuilder::refine_waves() {
+  const int t0 = p.phase_begin[p.nphases - 1], t1 = p.ntasks;
+  const int grid = eng_sm_count();
+  EngCfg cfg[kEngMaxConfigs];
+  double best = eng_phase_makespan(p, t0, t1, grid);
+  for (int iter = 0; iter < 8; ++iter) {
+    bool improved = false;
+    for (int i = t0; i < t1; ++i) {
+      if (p.t[i].kind != kEGemm) continue;
+      const EngTask keep = p.t[i];
+      const int nc = eng_gemm_configs(keep, cfg);
+      int pick = -1;
+      for (int c = 0; c < nc; ++c) {
+        if (cfg[c].units == keep.units && cfg[c].tm == keep.tm && cfg[c].tn == keep.tn) continue;
+        if (cfg[c].units > 4 * keep.units || 4 * cfg[c].units < keep.units) continue;
+        eng_gemm_set(&p.t[i], cfg[c].tm, cfg[c].tn, cfg[c].splits);
+        const double m = eng_phase_makespan(p, t0, t1, grid);
+        if (m < best - 1.0) {
+          best = m;
+          pick = c;
+        }
+      }
+      p.t[i] = keep;
+      if (pick >= 0) {
+        eng_gemm_set(&p.t[i], cfg[pick].tm, cfg[pick].tn, cfg[pick].splits);
+        improved = true;
+      }
+    }
+    if (!improved) return;
+  }
 }
 
 // In a phase of one unit a CTA the phase lasts as long as its costliest

@@ -124,6 +124,8 @@ struct EngBuilder {
   void balance(int budget);
   // After balance, for a phase of one wave: lowers its costliest unit.
   void refine(int budget);
+  // After balance, for a phase of several waves: shortens it as dealt.
+  void refine_waves();
 };
 
 // Units for a GEMM task of the engine's tile size and a split-K count.
