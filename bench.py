@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--graph-passes", type=int, default=4,
+                   help="passes over the rotating input sets one CUDA graph holds")
     p.add_argument("--eager", action="store_true",
                    help="launch every step from the host instead of replaying a CUDA graph")
     p.add_argument("--no-reuse", action="store_true",
@@ -554,29 +556,32 @@ def run_ours(args, w):
     # (PDL) edges between their kernels; --eager launches from the host every
     # time instead.
     graph, graph_note, launches_per_step = None, "eager", None
+    # steps one replay runs: passes over the sets, one step per set
+    gsteps = nsets * max(1, args.graph_passes)
     if not args.eager:
         try:
             g = torch.cuda.CUDAGraph()
             c0 = ttc.lib().tt_launch_count()
             with torch.cuda.graph(g):
                 cs = int(torch.cuda.current_stream().cuda_stream)
-                for j in range(nsets):
+                for j in range(gsteps):
                     step(j, cs)
-            launches_per_step = int(ttc.lib().tt_launch_count() - c0) // nsets
+            launches_per_step = int(ttc.lib().tt_launch_count() - c0) // gsteps
             for _ in range(3):
                 g.replay()
             torch.cuda.synchronize(dev)
             ttc.check(ttc.tt_get_device_status(sh), "device status after graph warm-up")
             graph = g
-            graph_note = f"cuda_graph ({nsets} steps per replay, one per rotating input set)"
+            graph_note = (f"cuda_graph ({gsteps} steps per replay: {gsteps // nsets} passes over "
+                          f"the {nsets} rotating input sets)")
         except Exception as e:  # capture unsupported: time the eager loop
             graph, graph_note = None, f"eager (graph capture failed: {type(e).__name__}: {e})"
             torch.cuda.synchronize(dev)
 
     def run(i):
-        """Step i; with the graph, a replay runs steps i .. i + nsets - 1."""
+        """Step i; with the graph, a replay runs steps i .. i + gsteps - 1."""
         if graph is not None:
-            if i % nsets == 0:
+            if i % gsteps == 0:
                 graph.replay()
         else:
             step(i)
@@ -585,7 +590,7 @@ def run_ours(args, w):
     # median repeat gives ms_per_step
     K = args.steps if args.steps is not None else 20
     if graph is not None:
-        K = -(-K // nsets) * nsets   # whole replays
+        K = -(-K // gsteps) * gsteps   # whole replays
     barrier()
 
     # ---- timed region
