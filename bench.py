@@ -1294,27 +1294,29 @@ def run_encoder(args):
     ttc.check(ttc.tt_get_device_status(int(stream.cuda_stream)), "device status after warm-up")
     barrier()
     graph, note, per_step = None, "eager", None
+    gsteps = nsets * max(1, args.graph_passes)  # block steps one replay runs
     if not args.eager:
         g = torch.cuda.CUDAGraph()
         c0 = ttc.lib().tt_launch_count()
         with torch.cuda.graph(g):
-            for j in range(nsets):
+            for j in range(gsteps):
                 step(j)
-        per_step = int(ttc.lib().tt_launch_count() - c0) // nsets
+        per_step = int(ttc.lib().tt_launch_count() - c0) // gsteps
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize(dev)
-        graph, note = g, f"cuda_graph ({nsets} block steps per replay, one per input set)"
+        graph, note = g, (f"cuda_graph ({gsteps} block steps per replay: {gsteps // nsets} "
+                          f"passes over the {nsets} input sets)")
 
     def run(i):
         if graph is not None:
-            if i % nsets == 0:
+            if i % gsteps == 0:
                 graph.replay()
         else:
             step(i)
     K = args.steps if args.steps is not None else 8
     if graph is not None:
-        K = -(-K // nsets) * nsets
+        K = -(-K // gsteps) * gsteps
     barrier()
     uuid = getattr(props, "uuid", None)
     clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
