@@ -1041,31 +1041,35 @@ def run_ttm(args, w):
     ttc.check(ttc.tt_get_device_status(sh), "device status after warm-up")
     barrier()
     uniq, pairs = emb.stats(ws)
-    graphs, graph_note, per_step = None, "eager", None
+    graph, graph_note, per_step = None, "eager", None
+    gsteps = nsets * max(1, args.graph_passes)  # steps one replay runs
     if not args.eager:
         try:
-            graphs = []
-            for j in range(nsets):
-                g = torch.cuda.CUDAGraph()
-                c0 = ttc.lib().tt_launch_count()
-                with torch.cuda.graph(g):
-                    step(j, int(torch.cuda.current_stream().cuda_stream))
-                per_step = int(ttc.lib().tt_launch_count() - c0)
-                graphs.append(g)
-            for j in range(max(3, nsets)):
-                graphs[j % nsets].replay()
+            g = torch.cuda.CUDAGraph()
+            c0 = ttc.lib().tt_launch_count()
+            with torch.cuda.graph(g):
+                cs = int(torch.cuda.current_stream().cuda_stream)
+                for j in range(gsteps):
+                    step(j, cs)
+            per_step = int(ttc.lib().tt_launch_count() - c0) // gsteps
+            for _ in range(3):
+                g.replay()
             torch.cuda.synchronize(dev)
-            graph_note = "cuda_graph"
+            graph, graph_note = g, (f"cuda_graph ({gsteps} steps per replay: {gsteps // nsets} "
+                                    f"passes over the {nsets} input sets)")
         except Exception as e:
-            graphs, graph_note = None, f"eager (graph capture failed: {type(e).__name__}: {e})"
+            graph, graph_note = None, f"eager (graph capture failed: {type(e).__name__}: {e})"
             torch.cuda.synchronize(dev)
 
     def run(i):
-        if graphs is not None:
-            graphs[i % nsets].replay()
+        if graph is not None:
+            if i % gsteps == 0:
+                graph.replay()
         else:
             step(i)
     K = args.steps if args.steps is not None else 20
+    if graph is not None:
+        K = -(-K // gsteps) * gsteps
     barrier()
     uuid = getattr(props, "uuid", None)
     clocks = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
@@ -1074,7 +1078,7 @@ def run_ttm(args, w):
     l0 = ttc.lib().tt_launch_count()
     rep_ms, windows = timed_repeats(run, K, barrier, stream, args.target_seconds)
     launches = int(ttc.lib().tt_launch_count() - l0) // len(rep_ms)
-    if graphs is not None:
+    if graph is not None:
         launches = K * per_step
     clk = clocks.stop()
     if clk is not None:
