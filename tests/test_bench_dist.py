@@ -120,6 +120,21 @@ def test_single_process_is_identity():
     assert bench.whole_job_rate(100, 1, 1.0) == pytest.approx(1e5)
 
 
+def test_graph_steps_are_whole_passes_over_the_sets():
+    """A graph replay runs whole passes over the rotating input sets (every
+    set as often as the others), several passes for a few sets, one pass once
+    the sets alone reach the 64-step limit."""
+    import bench
+    for nsets in (2, 3, 4, 16, 17, 64, 65, 16545):
+        for passes in (1, 2, 4):
+            g = bench.graph_steps(nsets, passes)
+            assert g % nsets == 0 and nsets <= g <= nsets * passes
+            assert g <= max(64, nsets)
+    assert bench.graph_steps(4, 4) == 16
+    assert bench.graph_steps(16545, 4) == 16545
+    assert bench.graph_steps(4, 0) == 4
+
+
 def test_algorithmic_bytes_per_activation_type():
     """The roofline's algorithmic bytes: x read by both passes, dy read, y and
     dx written, at the bytes of an input element (E4M3: 1) and of an output
